@@ -1,0 +1,229 @@
+"""Seeded synthetic decode workloads (inputs only).
+
+This module draws the inputs that both the CUDA path and the CPU oracle
+consume: the physical KV pool, the queries, the block tables (a seeded random
+placement of each sequence's logical blocks in the pool), the context lengths,
+the new token's K/V rows and, for the shared-prefix workload, the
+copy-on-write pairs.  It holds none of the method's arithmetic: no slot
+addressing, no attention.  Each side derives slot mappings itself.
+
+Every tensor is drawn from ``torch.Generator`` seeds, values N(0, 1) in the
+stated 16-bit dtype.  The whole pool is filled (unused blocks included) so
+that a read of a stale or wrong block shows up as a wrong result.
+
+The five named workloads follow the shapes the pages discuss:
+  tiny    -- 4 sequences, context lengths {1, 17, 100, 33}, MHA 4 heads,
+             head_dim 64, block_size 16, 64-block pool; the 100-token
+             sequence uses the block table [7, 2, 9, 1, 5, 8, 3] of the worked
+             example in "KV Cache与PagedAttention深度解析" §4.2.
+  mha7b   -- Llama-2-7B-shaped MHA layer: 32 heads, head_dim 128, bs 16,
+             32 sequences of 4096 tokens, 8192-block pool fully used.
+  gqa7b   -- 7B GQA layer: 32 q / 8 kv heads, 64 sequences, lengths U[128, 8192].
+  prefix  -- shared 2048-token prefix (64 blocks of 32) in every table plus a
+             private suffix U[64, 1024]; bf16; 128 copy-on-write pairs.
+  long70b -- Llama-2-70B-shaped GQA: 64 q / 8 kv heads, 16 sequences of 32768.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import torch
+
+WORKED_EXAMPLE_TABLE = [7, 2, 9, 1, 5, 8, 3]
+
+
+@dataclass
+class DecodeWorkload:
+    name: str
+    dtype: torch.dtype
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    kv: torch.Tensor                 # [num_blocks, 2, Hkv, bs, d] pool
+    q: torch.Tensor                  # [B, Hq, d]
+    block_tables: torch.Tensor       # [B, max_blocks_per_seq] int32 (unused entries = 0)
+    context_lens: torch.Tensor       # [B] int32, counting the new token
+    k_new: torch.Tensor              # [B, Hkv, d] the new token's K row per sequence
+    v_new: torch.Tensor              # [B, Hkv, d]
+    new_positions: torch.Tensor      # [B] int64 logical position of the new token (= len - 1)
+    scale: float
+    cow_pairs: Optional[torch.Tensor] = None          # [n, 2] int64 (src, dst)
+    block_tables_after_cow: Optional[torch.Tensor] = None
+    shared_prefix_blocks: int = 0
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max().item()) if self.num_seqs else 0
+
+    @property
+    def k_cache(self) -> torch.Tensor:
+        return self.kv[:, 0]
+
+    @property
+    def v_cache(self) -> torch.Tensor:
+        return self.kv[:, 1]
+
+    def to(self, device) -> "DecodeWorkload":
+        moved = {}
+        for name in ("kv", "q", "block_tables", "context_lens", "k_new", "v_new",
+                     "new_positions", "cow_pairs", "block_tables_after_cow"):
+            t = getattr(self, name)
+            moved[name] = None if t is None else t.to(device)
+        return DecodeWorkload(
+            name=self.name, dtype=self.dtype, num_seqs=self.num_seqs,
+            num_q_heads=self.num_q_heads, num_kv_heads=self.num_kv_heads,
+            head_dim=self.head_dim, block_size=self.block_size, num_blocks=self.num_blocks,
+            scale=self.scale, shared_prefix_blocks=self.shared_prefix_blocks,
+            meta=dict(self.meta), **moved)
+
+
+def _randn(shape, dtype, gen, device):
+    return torch.randn(shape, generator=gen, device=device, dtype=torch.float32).to(dtype)
+
+
+def make_decode_workload(*, name: str = "custom", num_seqs: int, num_q_heads: int,
+                         num_kv_heads: int, head_dim: int, block_size: int,
+                         context_lens: Sequence[int], num_blocks: Optional[int] = None,
+                         dtype: torch.dtype = torch.float16, seed: int = 0,
+                         device: str = "cpu", shared_prefix_tokens: int = 0,
+                         fixed_tables: Optional[dict] = None, cow_last_prefix_block: bool = False,
+                         max_blocks_per_seq: Optional[int] = None) -> DecodeWorkload:
+    """Build a seeded workload.
+
+    ``context_lens`` are the per-sequence lengths (the new token included).
+    With ``shared_prefix_tokens`` > 0 (a multiple of block_size) every table
+    starts with the same prefix blocks.  ``fixed_tables`` maps a sequence index
+    to an explicit list of physical blocks.  ``cow_last_prefix_block`` adds one
+    copy-on-write pair per sequence: the last shared prefix block to a fresh
+    private block, and the tables that point at the copies.
+    """
+    lens = [int(x) for x in context_lens]
+    assert len(lens) == num_seqs and num_q_heads % num_kv_heads == 0
+    bs = block_size
+    gen_cpu = torch.Generator().manual_seed(seed)
+    if shared_prefix_tokens:
+        assert shared_prefix_tokens % bs == 0
+        assert all(n >= shared_prefix_tokens for n in lens)
+    prefix_blocks = shared_prefix_tokens // bs
+    need = [math.ceil(n / bs) for n in lens]
+    private = [need[i] - prefix_blocks for i in range(num_seqs)]
+    fixed_tables = fixed_tables or {}
+    total = prefix_blocks + sum(private[i] for i in range(num_seqs) if i not in fixed_tables)
+    total_fixed = sum(len(v) for v in fixed_tables.values())
+    n_cow = num_seqs if (cow_last_prefix_block and prefix_blocks) else 0
+    if num_blocks is None:
+        num_blocks = total + total_fixed + n_cow
+    mb = max_blocks_per_seq or max([1] + need)
+    assert mb >= max([0] + need)
+
+    # seeded random placement of logical blocks in the pool
+    reserved = set()
+    for v in fixed_tables.values():
+        reserved.update(int(b) for b in v)
+    perm = [int(b) for b in torch.randperm(num_blocks, generator=gen_cpu).tolist() if b not in reserved]
+    assert len(perm) >= total + n_cow, "pool too small for the requested lengths"
+    cursor = 0
+    prefix = perm[cursor:cursor + prefix_blocks]
+    cursor += prefix_blocks
+    tables = torch.zeros((num_seqs, mb), dtype=torch.int32)
+    for i in range(num_seqs):
+        if i in fixed_tables:
+            row = [int(b) for b in fixed_tables[i]]
+            assert len(row) == need[i]
+        else:
+            row = prefix + perm[cursor:cursor + private[i]]
+            cursor += private[i]
+        if row:
+            tables[i, :len(row)] = torch.tensor(row, dtype=torch.int32)
+
+    cow_pairs = tables_after = None
+    if n_cow:
+        fresh = perm[cursor:cursor + n_cow]
+        cursor += n_cow
+        src = prefix[-1]
+        cow_pairs = torch.tensor([[src, fresh[i]] for i in range(num_seqs)], dtype=torch.int64)
+        tables_after = tables.clone()
+        tables_after[:, prefix_blocks - 1] = torch.tensor(fresh, dtype=torch.int32)
+
+    gen = torch.Generator(device=device).manual_seed(seed + 1)
+    kv = _randn((num_blocks, 2, num_kv_heads, bs, head_dim), dtype, gen, device)
+    q = _randn((num_seqs, num_q_heads, head_dim), dtype, gen, device)
+    k_new = _randn((num_seqs, num_kv_heads, head_dim), dtype, gen, device)
+    v_new = _randn((num_seqs, num_kv_heads, head_dim), dtype, gen, device)
+    ctx = torch.tensor(lens, dtype=torch.int32)
+    pos = (ctx.to(torch.int64) - 1)
+    return DecodeWorkload(
+        name=name, dtype=dtype, num_seqs=num_seqs, num_q_heads=num_q_heads,
+        num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=bs, num_blocks=num_blocks,
+        kv=kv, q=q, block_tables=tables.to(device), context_lens=ctx.to(device),
+        k_new=k_new, v_new=v_new, new_positions=pos.to(device),
+        scale=1.0 / math.sqrt(head_dim),
+        cow_pairs=None if cow_pairs is None else cow_pairs.to(device),
+        block_tables_after_cow=None if tables_after is None else tables_after.to(device),
+        shared_prefix_blocks=prefix_blocks, meta={"seed": seed})
+
+
+def _uniform_lens(n, lo, hi, seed):
+    g = torch.Generator().manual_seed(seed + 1000)
+    return torch.randint(lo, hi + 1, (n,), generator=g).tolist()
+
+
+# Named workloads.  ``scale_seqs`` shrinks the batch (same per-sequence shape)
+# so the parity tests can run a small copy that the oracle finishes quickly.
+def tiny(device="cpu", seed=0):
+    return make_decode_workload(
+        name="tiny", num_seqs=4, num_q_heads=4, num_kv_heads=4, head_dim=64, block_size=16,
+        context_lens=[1, 17, 100, 33], num_blocks=64, dtype=torch.float16, seed=seed,
+        device=device, fixed_tables={2: WORKED_EXAMPLE_TABLE})
+
+
+def mha7b(device="cpu", seed=1, num_seqs=32, context_len=4096, num_blocks=None):
+    nb = num_blocks if num_blocks is not None else num_seqs * math.ceil(context_len / 16)
+    return make_decode_workload(
+        name="mha7b", num_seqs=num_seqs, num_q_heads=32, num_kv_heads=32, head_dim=128,
+        block_size=16, context_lens=[context_len] * num_seqs, num_blocks=nb,
+        dtype=torch.float16, seed=seed, device=device)
+
+
+def gqa7b(device="cpu", seed=2, num_seqs=64, lo=128, hi=8192, num_blocks=32768):
+    lens = _uniform_lens(num_seqs, lo, hi, seed)
+    nb = max(num_blocks, sum(math.ceil(n / 16) for n in lens))
+    return make_decode_workload(
+        name="gqa7b", num_seqs=num_seqs, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        block_size=16, context_lens=lens, num_blocks=nb, dtype=torch.float16, seed=seed,
+        device=device, max_blocks_per_seq=math.ceil(hi / 16))
+
+
+def prefix(device="cpu", seed=3, num_seqs=128, prefix_tokens=2048, lo=64, hi=1024,
+           num_blocks=8192):
+    suffix = _uniform_lens(num_seqs, lo, hi, seed)
+    lens = [prefix_tokens + s for s in suffix]
+    return make_decode_workload(
+        name="prefix", num_seqs=num_seqs, num_q_heads=32, num_kv_heads=8, head_dim=128,
+        block_size=32, context_lens=lens, num_blocks=num_blocks, dtype=torch.bfloat16,
+        seed=seed, device=device, shared_prefix_tokens=prefix_tokens,
+        cow_last_prefix_block=True, max_blocks_per_seq=(prefix_tokens + hi + 31) // 32)
+
+
+def long70b(device="cpu", seed=4, num_seqs=16, context_len=32768, num_blocks=None):
+    nb = num_blocks if num_blocks is not None else num_seqs * math.ceil(context_len / 16)
+    return make_decode_workload(
+        name="long70b", num_seqs=num_seqs, num_q_heads=64, num_kv_heads=8, head_dim=128,
+        block_size=16, context_lens=[context_len] * num_seqs, num_blocks=nb,
+        dtype=torch.bfloat16, seed=seed, device=device)
+
+
+NAMED = {"tiny": tiny, "mha7b": mha7b, "gqa7b": gqa7b, "prefix": prefix, "long70b": long70b}
+
+# The default partition size each named workload is run with (0 = library's choice).
+DEFAULT_PARTITION = {"tiny": 0, "mha7b": 0, "gqa7b": 0, "prefix": 0, "long70b": 512}
