@@ -1,0 +1,427 @@
+"""Benchmark of the paged decode step on GB300.
+
+A step is one pass of the hot path over one batch: the cache write of each
+sequence's new token (reshape_and_cache) followed by paged decode attention
+(plus the split-context merge when the plan splits).  The default workload is
+the Llama-2-7B-shaped MHA decode layer (32 sequences x 4096 tokens, 32 heads of
+128, block 16, fp16, 2 GiB pool -- larger than L2, so no flush is needed).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mha7b|gqa7b|prefix|long70b|tiny] [--partition P]
+
+Prints one JSON line (rank 0).  `value` is decode tokens/s (one token per
+sequence per step) over all ranks, device-timed with inputs resident in HBM;
+`e2e` is the same metric through the Python API with the step's inputs copied
+from pinned host memory and the output copied back inside the timed region.
+`roofline` reports the decode kernel's algorithmic KV+q+out bytes per launch
+over its CUDA-event time against the measured HBM copy bandwidth.
+`--impl reference` times the CPU oracle (the reference arm of this build) on
+bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn tokens/s and KV-read GB/s (% of GB300 HBM peak)"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------- helpers
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("decode_kernel.cuh", "pkv_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_155_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"paged_decode_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    src = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not src or not val or src.group(1) != _kernel_source_hash():
+        return None
+    return float(val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+def _algorithmic_bytes(wl):
+    """K+V of every context token per KV head (once per GQA group) + q + out."""
+    e = 2
+    tokens = sum(int(x) for x in wl.context_lens.cpu().tolist())
+    kv = tokens * 2 * wl.num_kv_heads * wl.head_dim * e
+    qo = 2 * wl.num_seqs * wl.num_q_heads * wl.head_dim * e
+    return kv + qo
+
+
+def _make_workload(name, device, seed):
+    from paged_kv_cache_155_gb300 import workloads
+    return workloads.NAMED[name](device=device, seed=seed) if name != "tiny" else \
+        workloads.tiny(device=device, seed=seed)
+
+
+def _workload_config(wl, name, plan, partition):
+    lens = wl.context_lens.cpu()
+    return {"workload": name, "num_seqs": wl.num_seqs, "num_q_heads": wl.num_q_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+            "block_size": wl.block_size, "num_blocks": wl.num_blocks,
+            "context_len_min": int(lens.min()), "context_len_max": int(lens.max()),
+            "context_tokens": int(lens.sum()), "partition_size": plan["partition_size"],
+            "num_partitions": plan["num_partitions"], "partition_arg": partition,
+            "l2": f"no flush: pool of {wl.kv.numel() * 2 / 2**30:.2f} GiB > 129 MB L2"}
+
+
+# --------------------------------------------------------------------------- oracle legs
+def _oracle_units(wl_host, pool_bits, units, q_bits):
+    """Run the oracle on (sequence, KV head) units; returns seconds.  Units of one
+    KV head go to the oracle in one call so its OpenMP loop over (sequence,
+    query head) pairs can use every core."""
+    import numpy as np
+    import oracle
+    g = wl_host.num_q_heads // wl_host.num_kv_heads
+    flat = pool_bits.reshape(-1)
+    half = wl_host.num_kv_heads * wl_host.block_size * wl_host.head_dim
+    row_off = wl_host.block_size * wl_host.head_dim
+    tables = wl_host.block_tables.numpy()
+    lens = wl_host.context_lens.numpy()
+    code = oracle.BF16 if str(wl_host.dtype).endswith("bfloat16") else oracle.F16
+    by_head = {}
+    for (i, h) in units:
+        by_head.setdefault(h, []).append(i)
+    t0 = time.perf_counter()
+    for h, seqs in by_head.items():
+        sel = np.array(seqs)
+        # KV head h alone: shift the K/V bases to head h's rows of block 0
+        oracle.paged_decode(q_bits[sel, h * g:(h + 1) * g], flat[h * row_off:],
+                            flat[half + h * row_off:], 2 * half, tables[sel], lens[sel],
+                            1, wl_host.block_size, wl_host.scale, code)
+    return time.perf_counter() - t0
+
+
+def _unit_list(wl_host, n, start=0):
+    total = wl_host.num_seqs * wl_host.num_kv_heads
+    out = []
+    for k in range(start, start + n):
+        k %= total
+        out.append((k % wl_host.num_seqs, k // wl_host.num_seqs))
+    return out
+
+
+def _bits(t):
+    import numpy as np
+    import torch
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def cpu_baseline(wl_dev, budget_s=12.0):
+    """The oracle on a bounded sample of the workload, on this host's cores."""
+    import oracle
+    wl_host = wl_dev.to("cpu")
+    pool = _bits(wl_host.kv)
+    qb = _bits(wl_host.q)
+    units = _unit_list(wl_host, 1)
+    t1 = _oracle_units(wl_host, pool, units, qb)
+    n = max(1, min(wl_host.num_seqs * wl_host.num_kv_heads, int(budget_s / max(t1, 1e-6))))
+    units = _unit_list(wl_host, n, start=1)
+    t = _oracle_units(wl_host, pool, units, qb)
+    tokens = n / wl_host.num_kv_heads  # one decode token = all KV heads of one sequence
+    return {"value": tokens / t, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} (sequence, KV head) units of {wl_host.num_seqs}x{wl_host.num_kv_heads}"
+                      f" ({n / (wl_host.num_seqs * wl_host.num_kv_heads):.3f} of one step),"
+                      f" {t:.1f} s, fp64 C oracle, OpenMP over query heads of a unit"}
+
+
+def run_reference(args):
+    world, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    oracle.build()
+    wl = _make_workload(args.workload, "cpu", 1234)
+    pool, qb = _bits(wl.kv), _bits(wl.q)
+    per_step_budget = max(0.002, 150.0 / max(1, args.steps + args.warmup))
+    t1 = _oracle_units(wl, pool, _unit_list(wl, 1), qb)
+    n = max(1, min(wl.num_seqs * wl.num_kv_heads, int(per_step_budget / max(t1, 1e-6))))
+    cursor = 1
+    for _ in range(args.warmup):
+        _oracle_units(wl, pool, _unit_list(wl, n, cursor), qb)
+        cursor += n
+    total = 0.0
+    for _ in range(args.steps):
+        total += _oracle_units(wl, pool, _unit_list(wl, n, cursor), qb)
+        cursor += n
+    tokens = args.steps * n / wl.num_kv_heads
+    value = tokens / total
+    ms_full = 1000.0 * wl.num_seqs / value
+    sample = (f"each step {n} (sequence, KV head) units of {wl.num_seqs}x{wl.num_kv_heads}; "
+              f"fp64 C oracle")
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_full,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, "num_seqs": wl.num_seqs,
+                       "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads,
+                       "head_dim": wl.head_dim, "block_size": wl.block_size},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = _dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    from paged_kv_cache_155_gb300 import _build
+    _build.build()
+    import paged_kv_cache_155_gb300 as pkv
+
+    wl = _make_workload(args.workload, str(dev), 1234 + rank)
+    k_cache, v_cache = pkv.split_pool(wl.kv)
+    maxl = int(wl.context_lens.max())
+    part = args.partition
+    sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    plan = pkv.decode_plan(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                           wl.block_size, maxl, part, sm)
+    slots = pkv.slot_mapping(wl.block_tables.cpu(), wl.new_positions.cpu(), wl.block_size).to(dev)
+    out = torch.empty_like(wl.q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
+        pkv.paged_attention_decode(wl.q, k_cache, v_cache, wl.block_tables, wl.context_lens,
+                                   wl.scale, out, max_context_len=maxl, partition_size=part)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    flags, names = pkv.get_device_error(dev)
+    if flags:
+        raise RuntimeError(f"device flags during warm-up: {names}")
+
+    # ---- device-timed region
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    time.sleep(0.25 if sampler else 0)
+    launches0 = pkv.launch_count()
+    t_start.record(stream)
+    for k in range(args.steps):
+        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
+        dec_ev[k][0].record(stream)
+        pkv.paged_attention_decode(wl.q, k_cache, v_cache, wl.block_tables, wl.context_lens,
+                                   wl.scale, out, max_context_len=maxl, partition_size=part)
+        dec_ev[k][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = pkv.launch_count() - launches0
+    clocks = sampler.stop() if sampler else None
+    if world > 1:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * wl.num_seqs / (ms_step / 1000.0)
+    flags, names = pkv.get_device_error(dev)
+    if flags:
+        raise RuntimeError(f"device flags during the timed region: {names}")
+
+    # ---- end to end through the API with host buffers
+    pin = lambda t: t.detach().cpu().pin_memory()
+    h_q, h_k, h_v = pin(wl.q), pin(wl.k_new), pin(wl.v_new)
+    h_slots, h_bt, h_cl = pin(slots), pin(wl.block_tables), pin(wl.context_lens)
+    h_out = torch.empty(wl.q.shape, dtype=wl.q.dtype, pin_memory=True)
+    d_q, d_k, d_v = torch.empty_like(wl.q), torch.empty_like(wl.k_new), torch.empty_like(wl.v_new)
+    d_slots, d_bt, d_cl = torch.empty_like(slots), torch.empty_like(wl.block_tables), \
+        torch.empty_like(wl.context_lens)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_cl))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_bt, h_bt),
+                     (d_cl, h_cl)):
+            d.copy_(h, non_blocking=True)
+        pkv.reshape_and_cache(d_k, d_v, d_slots, k_cache, v_cache)
+        pkv.paged_attention_decode(d_q, k_cache, v_cache, d_bt, d_cl, wl.scale, out,
+                                   max_context_len=maxl, partition_size=part)
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 2)
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * wl.num_seqs / (e2e_ms / 1000.0)
+
+    # ---- roofline of the decode kernel(s)
+    peak, peak_kind = _peaks()
+    bytes_launch = _algorithmic_bytes(wl)
+    achieved = bytes_launch / (dec_ms / 1000.0) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": _profiled_traffic(args.workload),
+            "peak_source": f"{peak_kind} hbm_gbs",
+            "kernel": "paged_decode_kernel" + ("+merge" if plan["needs_merge"] else ""),
+            "algorithmic_bytes_per_launch": bytes_launch, "launch_ms": dec_ms}
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16" if wl.dtype == torch.float16 else "bf16", "data": "synthetic",
+            "config": _workload_config(wl, args.workload, plan, part),
+            "kv_read_gbps": achieved, "hbm_frac_of_measured": achieved / peak,
+            "hbm_frac_of_nominal_8000": achieved / 8000.0,
+            "clocks": clocks, "gpu_launches": launches,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "roofline": roof}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mha7b",
+                    choices=["tiny", "mha7b", "gqa7b", "prefix", "long70b"])
+    ap.add_argument("--partition", type=int, default=-1,
+                    help="tokens per split-context partition (0 = library's choice; "
+                         "default: the workload's own setting)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.partition < 0:
+        from paged_kv_cache_155_gb300.workloads import DEFAULT_PARTITION
+        args.partition = DEFAULT_PARTITION[args.workload]
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,196 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv, a GB300 (sm_103a) library for the decode
+ * hot path of paged KV-cache attention.
+ *
+ * Pages the operations follow (title and section):
+ *   P1 = "KV Cache与PagedAttention深度解析：vLLM内存管理革命" (iopencloud.com)
+ *   P2 = "KV Cache从原理到实战：大模型推理内存管理演进与优化" (xnwp.cn/news/16711)
+ *   P3 = PagedAttention + prefix caching via nano-vllm (zwxr.cn/news/317362)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Layout.  The KV pool is [num_blocks][2][num_kv_heads][block_size][head_dim]
+ *   (P1 §4.3 and §5.1, with num_kv_heads for grouped-query models, P2 §5.3).
+ *   Calls take the K half and the V half as two base pointers plus the stride,
+ *   in elements, between consecutive physical blocks: for the packed pool
+ *   k_cache = pool, v_cache = pool + num_kv_heads*block_size*head_dim and
+ *   block_stride_elems = 2*num_kv_heads*block_size*head_dim.  Within a block,
+ *   row (h, offset) of K starts at k_cache + blk*block_stride_elems +
+ *   (h*block_size + offset)*head_dim.
+ * Slots.  Slot s names block s / block_size, offset s % block_size (P1 §5.3).
+ * Heads.  Query head hq reads KV head hq / (num_q_heads / num_kv_heads).
+ * Types.  dtype is fp16 or bf16 for q, K, V and out; accumulation is fp32.
+ *   head_dim is 64 or 128; block_size is 8, 16 or 32.  Others: PKV_ERR_UNSUPPORTED.
+ * Memory.  Every pointer argument except the host-side outputs of
+ *   pkv_get_device_error is a DEVICE pointer owned by the caller.  Tensor base
+ *   pointers must be 16-byte aligned and block strides a multiple of 8
+ *   elements.  The library allocates no memory; its only state is one device
+ *   status word per device (see pkv_get_device_error) and cached device
+ *   attributes.
+ * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).  Every
+ *   call only enqueues work on it and returns; results are ready when the
+ *   stream reaches that point.
+ * Errors.  Arguments that can be checked on the host are checked before any
+ *   launch: PKV_ERR_INVALID_ARG (nothing enqueued).  Values that live in device
+ *   memory (slots, block-table entries, context lengths, copy pairs) are
+ *   checked by the kernels: a bad value is skipped, never dereferenced, and
+ *   raises a flag in the device status word.  A failed launch returns
+ *   PKV_ERR_CUDA.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* host-checkable argument out of contract      */
+    PKV_ERR_UNSUPPORTED = 2,   /* valid but not built (dtype, head_dim, bs)    */
+    PKV_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed         */
+    PKV_ERR_DEVICE = 4         /* pkv_get_device_error found flags raised      */
+} pkv_status;
+
+typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Flags of the device status word (bitwise OR of what the kernels saw). */
+#define PKV_DEVERR_SLOT        0x1u  /* slot_mapping entry >= num_blocks*block_size  */
+#define PKV_DEVERR_BLOCK_TABLE 0x2u  /* block_tables entry outside [0, num_blocks)    */
+#define PKV_DEVERR_CONTEXT_LEN 0x4u  /* context_lens entry < 0, > max_context_len or
+                                        > max_blocks_per_seq*block_size (clamped)      */
+#define PKV_DEVERR_COPY_PAIR   0x8u  /* copy pair entry outside [0, num_blocks)       */
+#define PKV_DEVERR_TIMEOUT     0x10u /* a bounded wait on an async copy gave up       */
+
+/*
+ * pkv_reshape_and_cache -- write each new token's K and V rows into its slot.
+ * (P1 §2.2: compute only K_t, V_t and append them; P1 §5.3: the write goes to
+ * offset t % block_size of the sequence's last block.)
+ *
+ *   k_new, v_new   [num_tokens][num_kv_heads][head_dim], contiguous, dtype.
+ *   slot_mapping   [num_tokens] int64; slot < 0 means "skip this token"
+ *                  (padding); slot >= num_blocks*block_size raises
+ *                  PKV_DEVERR_SLOT and the token is skipped.  Two tokens must
+ *                  not share a slot (the result would be either row).
+ *   k_cache/v_cache, num_blocks, block_stride_elems: the pool, as above.
+ * The copy is bit-exact.  num_tokens == 0 is a no-op.
+ */
+PKV_API pkv_status pkv_reshape_and_cache(const void *k_new, const void *v_new,
+                                         const int64_t *slot_mapping, int64_t num_tokens,
+                                         void *k_cache, void *v_cache, int64_t num_blocks,
+                                         int64_t block_stride_elems, int num_kv_heads,
+                                         int head_dim, int block_size, pkv_dtype dtype,
+                                         void *stream);
+
+/*
+ * pkv_decode_workspace_bytes -- device scratch that pkv_paged_attention_decode
+ * needs for a split-context (partitioned) call: fp32 partial outputs plus the
+ * running maximum and sum of every (sequence, query head, partition).
+ * partition_size 0 means "the library's choice" and returns the size for the
+ * partition count that choice gives on the current device.  Returns 0 when
+ * no split is needed and (size_t)-1 for arguments out of contract.
+ */
+PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int block_size, int max_context_len,
+                                          int partition_size);
+
+/*
+ * pkv_paged_attention_decode -- one query token per sequence attends over its
+ * paged KV cache:  out[i, hq] = softmax(scale * q[i, hq] . K_i^T) V_i
+ * (P1 §2.1), where K_i, V_i are the first context_lens[i] tokens of sequence i
+ * reached through block_tables[i] (P1 §4.2-4.3), accumulated with the running
+ * maximum / running sum rescaling of P1 §7.2 in fp32.
+ *
+ *   q             [num_seqs][num_q_heads][head_dim], contiguous, dtype.
+ *   block_tables  [num_seqs][max_blocks_per_seq] int32, physical block ids.
+ *   context_lens  [num_seqs] int32, tokens to attend over (the new token
+ *                 included); 0 gives a zero output row.
+ *   max_context_len  host-side upper bound of context_lens (sizes the grid; a
+ *                 larger device value raises PKV_DEVERR_CONTEXT_LEN and is
+ *                 clamped).
+ *   scale         softmax scale, normally 1/sqrt(head_dim).
+ *   out           [num_seqs][num_q_heads][head_dim], contiguous, dtype; each
+ *                 value rounded once (to nearest even) from fp32.
+ *   workspace     device scratch of workspace_bytes (>= the value of
+ *                 pkv_decode_workspace_bytes for the same arguments); may be
+ *                 NULL when that value is 0.  Contents need no initialisation.
+ *   partition_size  tokens per split-context partition, a multiple of
+ *                 block_size; 0 = library's choice.  Each (sequence, KV head,
+ *                 partition) is processed independently and merged by a second
+ *                 kernel (log-sum-exp merge) when a sequence spans >1 partition.
+ * The reduction order depends only on logical positions, so the result is
+ * bitwise independent of where blocks sit in the pool.
+ */
+PKV_API pkv_status pkv_paged_attention_decode(
+    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+    int64_t block_stride_elems, const int32_t *block_tables, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, float scale, void *out, void *workspace,
+    size_t workspace_bytes, int partition_size, pkv_dtype dtype, void *stream);
+
+/*
+ * pkv_copy_blocks -- copy-on-write block copies (P1 §8.3; P3 §2.3 and §5.5).
+ * For each pair p, the K half and the V half of block src_dst_pairs[2p] are
+ * copied bit-exactly over those of block src_dst_pairs[2p+1].
+ *
+ *   src_dst_pairs  [num_pairs][2] int64, device.  Destinations must be
+ *                  distinct and must not also appear as sources (otherwise the
+ *                  result depends on the order the GPU runs the copies).  An
+ *                  entry outside [0, num_blocks) raises PKV_DEVERR_COPY_PAIR
+ *                  and that pair is skipped.
+ * num_pairs == 0 is a no-op.
+ */
+PKV_API pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blocks,
+                                   int64_t block_stride_elems, int num_kv_heads, int head_dim,
+                                   int block_size, const int64_t *src_dst_pairs,
+                                   int64_t num_pairs, pkv_dtype dtype, void *stream);
+
+/*
+ * pkv_get_device_error -- synchronise `stream`, read the current device's
+ * status word into *flags (PKV_DEVERR_* bits; may be NULL) and clear it.
+ * Returns PKV_OK when no flag was set, PKV_ERR_DEVICE when one was, and
+ * PKV_ERR_CUDA if the read failed.
+ */
+PKV_API pkv_status pkv_get_device_error(void *stream, uint32_t *flags);
+
+/* Static description of a status code. */
+PKV_API const char *pkv_status_string(pkv_status status);
+
+/* Kernel launches this process has made through the library (all calls). */
+PKV_API uint64_t pkv_launch_count(void);
+
+/*
+ * pkv_decode_plan -- the launch decision pkv_paged_attention_decode makes,
+ * as a pure host function (no CUDA call): given the shape and the SM count it
+ * writes the partition size, partitions per sequence, query heads handled per
+ * block and whether the merge kernel runs.  Returns PKV_OK or the status the
+ * decode call would return for these arguments.
+ */
+PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int max_context_len,
+                                   int partition_size, int sm_count, int *out_partition_size,
+                                   int *out_num_partitions, int *out_heads_per_block,
+                                   int *out_needs_merge);
+
+/*
+ * pkv_debug_wait_timeout -- failure-detection self test.  Launches one block
+ * that waits, with the library's bounded wait, on an mbarrier that nothing
+ * completes; after timeout_ns nanoseconds the wait gives up, raises
+ * PKV_DEVERR_TIMEOUT in the status word and the kernel returns normally.
+ * timeout_ns must be in (0, 10^10].
+ */
+PKV_API pkv_status pkv_debug_wait_timeout(uint64_t timeout_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H */

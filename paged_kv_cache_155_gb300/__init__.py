@@ -1,0 +1,19 @@
+"""GB300-native paged KV-cache decode: a C-ABI CUDA library (libpagedkv) and its
+thin PyTorch binding.
+
+  reshape_and_cache       write each new token's K/V rows into its cache slot
+  paged_attention_decode  one query token per sequence attends over its paged cache
+  copy_blocks             copy-on-write copies of shared blocks
+
+The library must be built first (``__graft_entry__.build()``); the calls raise
+if it is missing.  There is no CPU implementation in this package.
+"""
+from .ops import (F16, BF16, copy_blocks, debug_wait_timeout, decode_plan,  # noqa: F401
+                  decode_workspace_bytes, get_device_error, launch_count,
+                  paged_attention_decode, reshape_and_cache, split_pool)
+from .block_table import slot_mapping  # noqa: F401
+from ._lib import PagedKVError  # noqa: F401
+
+__all__ = ["reshape_and_cache", "paged_attention_decode", "copy_blocks", "split_pool",
+           "decode_workspace_bytes", "decode_plan", "get_device_error", "launch_count",
+           "debug_wait_timeout", "slot_mapping", "PagedKVError"]

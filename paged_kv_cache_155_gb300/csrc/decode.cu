@@ -1,0 +1,157 @@
+// decode.cu -- the pkv_paged_attention_decode entry point: argument checks,
+// the split-context plan, workspace layout, and the launch.
+#include <algorithm>
+#include <cmath>
+
+#include "decode_launch.cuh"
+
+namespace {
+
+constexpr int kResidentCtasPerSm = 2;  // decode CTAs resident per SM (shared-memory bound)
+constexpr int kTargetWaves = 8;        // CTA waves the automatic split aims for
+constexpr int kMinAutoPartition = 256; // tokens: below this the per-CTA set-up dominates
+
+int heads_per_block_for(int group) {
+    if (group % 8 == 0) return 8;
+    if (group % 4 == 0) return 4;
+    if (group % 2 == 0) return 2;
+    return 1;
+}
+
+size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, int num_partitions) {
+    if (num_partitions <= 1) return 0;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * num_partitions;
+    return rows * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
+
+PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int max_context_len,
+                                   int partition_size, int sm_count, int *out_partition_size,
+                                   int *out_num_partitions, int *out_heads_per_block,
+                                   int *out_needs_merge) {
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
+        partition_size < 0 || sm_count <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads) return PKV_ERR_INVALID_ARG;
+    if (partition_size % block_size) return PKV_ERR_INVALID_ARG;
+    const int max_partition = pkv::DecodeGeom<128, 16>::kMaxTableEntries * block_size;
+    if (partition_size > max_partition) return PKV_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    const int gh = heads_per_block_for(group);
+    const int64_t grid_y = static_cast<int64_t>(num_kv_heads) * (group / gh);
+    if (grid_y > 65535 || num_seqs > 65535) return PKV_ERR_INVALID_ARG;
+
+    int part = partition_size;
+    if (part == 0) {
+        // Enough CTAs for several waves over every SM, but partitions no
+        // shorter than kMinAutoPartition tokens.
+        const int64_t units = std::max<int64_t>(1, static_cast<int64_t>(num_seqs) * grid_y);
+        const int64_t target = static_cast<int64_t>(sm_count) * kResidentCtasPerSm * kTargetWaves;
+        const int64_t want = std::max<int64_t>(1, (target + units - 1) / units);
+        int64_t p = (static_cast<int64_t>(max_context_len) + want - 1) / want;
+        p = std::max<int64_t>(p, kMinAutoPartition);
+        p = (p + block_size - 1) / block_size * block_size;
+        part = static_cast<int>(std::min<int64_t>(p, max_partition));
+    }
+    const int nparts = max_context_len > 0 ? (max_context_len + part - 1) / part : 1;
+    if (out_partition_size) *out_partition_size = part;
+    if (out_num_partitions) *out_num_partitions = nparts;
+    if (out_heads_per_block) *out_heads_per_block = gh;
+    if (out_needs_merge) *out_needs_merge = nparts > 1 ? 1 : 0;
+    return PKV_OK;
+}
+
+PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int block_size, int max_context_len,
+                                          int partition_size) {
+    const int sm = partition_size > 0 ? 1 : pkv::current_sm_count();
+    if (sm <= 0) return static_cast<size_t>(-1);
+    int part = 0, nparts = 0, gh = 0, merge = 0;
+    if (pkv_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                        max_context_len, partition_size, sm, &part, &nparts, &gh,
+                        &merge) != PKV_OK)
+        return static_cast<size_t>(-1);
+    return workspace_for(num_seqs, num_q_heads, head_dim, nparts);
+}
+
+PKV_API pkv_status pkv_paged_attention_decode(
+    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+    int64_t block_stride_elems, const int32_t *block_tables, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, float scale, void *out, void *workspace,
+    size_t workspace_bytes, int partition_size, pkv_dtype dtype, void *stream) {
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || max_context_len < 0 ||
+        static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size ||
+        !std::isfinite(scale))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t half_elems = static_cast<int64_t>(num_kv_heads) * block_size * head_dim;
+    if (block_stride_elems < half_elems || block_stride_elems % 8) return PKV_ERR_INVALID_ARG;
+    if (!k_cache || !v_cache || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache))
+        return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !out || !block_tables || !context_lens || !pkv::aligned16(q) || !pkv::aligned16(out))
+        return PKV_ERR_INVALID_ARG;
+
+    int part = 0, nparts = 0, gh = 0, merge = 0;
+    // Validate the shape first (no CUDA call), then plan for the real SM count.
+    pkv_status plan = pkv_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                      max_context_len, partition_size, 1, &part, &nparts, &gh,
+                                      &merge);
+    if (plan != PKV_OK) return plan;
+    if (partition_size == 0) {
+        const int sm = pkv::current_sm_count();
+        if (sm <= 0) return PKV_ERR_CUDA;
+        plan = pkv_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                               max_context_len, 0, sm, &part, &nparts, &gh, &merge);
+        if (plan != PKV_OK) return plan;
+    }
+    const size_t need = workspace_for(num_seqs, num_q_heads, head_dim, nparts);
+    if (need > 0 && (!workspace || workspace_bytes < need || !pkv::aligned16(workspace)))
+        return PKV_ERR_INVALID_ARG;
+    unsigned int *status = pkv::status_word_ptr();
+    if (!status) return PKV_ERR_CUDA;
+
+    const int group = num_q_heads / num_kv_heads;
+    pkv::DecodeParams p{};
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.out = out;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * nparts;
+    p.ws_o = need ? static_cast<float *>(workspace) : nullptr;
+    p.ws_m = need ? p.ws_o + rows * head_dim : nullptr;
+    p.ws_l = need ? p.ws_m + rows : nullptr;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.status = status;
+    p.num_blocks = num_blocks;
+    p.block_stride = block_stride_elems;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.len_cap = max_context_len;  // <= max_blocks_per_seq * block_size (checked above)
+    p.num_q_heads = num_q_heads;
+    p.group = group;
+    p.subgroups = group / gh;
+    p.partition_size = part;
+    p.num_partitions = nparts;
+    p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+
+    const dim3 grid(static_cast<unsigned>(nparts), static_cast<unsigned>(num_kv_heads * p.subgroups),
+                    static_cast<unsigned>(num_seqs));
+    const int merge_rows = merge ? num_seqs * num_q_heads : 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return dtype == PKV_F16
+               ? pkv::launch_decode_f16(p, head_dim, block_size, gh, grid, merge_rows, s)
+               : pkv::launch_decode_bf16(p, head_dim, block_size, gh, grid, merge_rows, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,9 @@
+// decode_f16.cu -- fp16 instantiations of the paged decode kernels.
+#include "decode_launch.cuh"
+
+namespace pkv {
+pkv_status launch_decode_f16(const DecodeParams &p, int head_dim, int block_size, int gh,
+                             dim3 grid, int merge_rows, cudaStream_t s) {
+    return launch_decode_typed<__half>(p, head_dim, block_size, gh, grid, merge_rows, s);
+}
+}  // namespace pkv

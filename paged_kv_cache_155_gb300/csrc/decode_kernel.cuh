@@ -1,0 +1,397 @@
+// decode_kernel.cuh -- paged decode attention, one CTA per
+// (partition of the context, KV head [x query-head subgroup], sequence).
+//
+// What it computes ("KV Cache与PagedAttention深度解析" §2.1 definition, §4.2-4.3
+// block-table addressing, §7.2 running-max / running-sum form): for every query
+// head hq of the CTA's group, over the partition's tokens t,
+//     s_t = scale * q[hq] . K[t],   m = max s_t,   l = sum exp(s_t - m),
+//     o = sum exp(s_t - m) V[t]
+// in fp32.  A sequence that fits in one partition gets out = o / l directly;
+// otherwise (o, m, l) go to the workspace and the merge kernel combines the
+// partitions.  Scores are kept in log2 units (q is pre-multiplied by
+// scale * log2(e)) so every exponential is one ex2.
+//
+// GB300 design:
+//  * K/V are read in place from the paged pool ("gather then compute" would
+//    cost an extra pass over HBM): the per-(block, head) K and V tiles are
+//    contiguous, so each warp streams them with 1-D bulk copies on the TMA
+//    engine into its own ring of shared-memory stages, tracked by one
+//    mbarrier per stage.  Each warp is its own producer and consumer: no
+//    CTA-wide barrier in the main loop.  Tiles are marked evict-first in L2.
+//  * Lane layout: a token row of head_dim 16-bit values is LPT = head_dim/8
+//    lanes x one 16-byte vector, so TPG = 32/LPT tokens are in flight per warp
+//    instruction and shared-memory reads are conflict-free.  The QK partial
+//    sums are reduced across the LPT lanes with xor shuffles; the PV update is
+//    lane-local (each lane owns 8 output dims of every head of the group).
+//  * GQA: all GH query heads of the group share each K/V tile, so a tile is
+//    read from HBM once per group, not once per query head.
+//  * The chunk-to-warp assignment and every merge are fixed by logical token
+//    position, so the output does not depend on the physical placement.
+#pragma once
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+struct DecodeParams {
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    void *out;
+    float *ws_o;  // [num_seqs][num_q_heads][num_partitions][head_dim]
+    float *ws_m;  // [num_seqs][num_q_heads][num_partitions] (log2 units)
+    float *ws_l;  // [num_seqs][num_q_heads][num_partitions]
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    unsigned int *status;
+    int64_t num_blocks;
+    int64_t block_stride;  // elements between consecutive physical blocks
+    int max_blocks_per_seq;
+    int len_cap;     // min(max_context_len, max_blocks_per_seq * block_size)
+    int num_q_heads;
+    int group;       // num_q_heads / num_kv_heads
+    int subgroups;   // group / heads_per_block
+    int partition_size;
+    int num_partitions;
+    float scale_log2;  // scale * log2(e)
+};
+
+// Decode-kernel geometry for one (head_dim, block_size) pair.
+template <int D, int BS>
+struct DecodeGeom {
+    static constexpr int kWarps = 4;
+    static constexpr int kTile = BS < 16 ? BS : 16;      // tokens per stage
+    static constexpr int kVec = 8;                       // 16-bit values per 16-byte vector
+    static constexpr int kLanesPerToken = D / kVec;      // LPT
+    static constexpr int kTokenGroups = 32 / kLanesPerToken;  // TPG
+    static constexpr int kIters = kTile / kTokenGroups;  // token rows per lane per stage
+    static constexpr int kTileBytes = kTile * D * 2;     // one K (or V) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kStagesRaw = 24576 / kStageBytes;
+    static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
+    static constexpr int kMaxTableEntries = 1024;        // table slice per partition
+    static constexpr int kSmemBytes = kWarps * kStages * kStageBytes +
+                                      kWarps * kStages * 8 + kMaxTableEntries * 4;
+    static_assert(kIters >= 1, "tile smaller than a warp's token groups");
+};
+
+template <typename T, int D, int BS, int GH>
+__global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams p) {
+    using G = DecodeGeom<D, BS>;
+    constexpr int NW = G::kWarps, S = G::kStages, TILE = G::kTile, LPT = G::kLanesPerToken,
+                  TPG = G::kTokenGroups, ITERS = G::kIters;
+    // token rows processed between two online-softmax updates (bounds registers)
+    constexpr int IT_STEP = (ITERS * GH <= 32) ? ITERS : (32 / GH > 0 ? 32 / GH : 1);
+    static_assert(ITERS % IT_STEP == 0, "step must divide the stage");
+    static_assert(GH * (D + 4) * 4 <= S * G::kStageBytes, "merge scratch must fit a warp's stages");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *stages = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * S * G::kStageBytes);
+    int32_t *tbl = reinterpret_cast<int32_t *>(smem + NW * S * G::kStageBytes + NW * S * 8);
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int part = blockIdx.x;
+    const int seq = blockIdx.z;
+    const int kvh = blockIdx.y / p.subgroups;
+    const int hq0 = kvh * p.group + (blockIdx.y % p.subgroups) * GH;
+
+    // ---- context length (device value, range-checked) and partition bounds
+    int len = p.context_lens[seq];
+    if (len < 0 || len > p.len_cap) {
+        if (threadIdx.x == 0 && part == 0 && blockIdx.y == 0)
+            raise_flag(p.status, PKV_DEVERR_CONTEXT_LEN);
+        len = len < 0 ? 0 : p.len_cap;
+    }
+    const int nparts = len > 0 ? (len + p.partition_size - 1) / p.partition_size : 1;
+    if (part >= nparts) return;  // uniform over the CTA
+    const int tok0 = part * p.partition_size;
+    const int tok1 = min(len, tok0 + p.partition_size);
+    const int ntok = max(0, tok1 - tok0);
+    const int nchunks = (ntok + TILE - 1) / TILE;
+    const int blk0 = tok0 / BS;
+    const int nblk = (ntok + BS - 1) / BS;
+
+    // ---- table slice of this partition -> shared memory (bad entries -> -1)
+    const int32_t *trow = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + blk0;
+    for (int i = threadIdx.x; i < nblk; i += blockDim.x) {
+        int b = trow[i];
+        if (b < 0 || b >= p.num_blocks) {
+            raise_flag(p.status, PKV_DEVERR_BLOCK_TABLE);
+            b = -1;
+        }
+        tbl[i] = b;
+    }
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[warp * S + s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const T *kc = static_cast<const T *>(p.k_cache);
+    const T *vc = static_cast<const T *>(p.v_cache);
+    unsigned char *my_stages = stages + warp * S * G::kStageBytes;
+    uint64_t *my_bars = bars + warp * S;
+    const uint64_t policy = l2_policy_evict_first();
+
+    // chunk c (partition-local, TILE tokens) -> stage s of this warp
+    auto issue = [&](int c, int s) {
+        const int row = c * TILE;                   // partition-local token index
+        const int b = tbl[row / BS];
+        const int r0 = row % BS;
+        if (b < 0) {  // flagged entry: complete the phase without data
+            mbar_arrive(&my_bars[s]);
+            return;
+        }
+        const int64_t off = static_cast<int64_t>(b) * p.block_stride +
+                            (static_cast<int64_t>(kvh) * BS + r0) * D;
+        unsigned char *dst = my_stages + s * G::kStageBytes;
+        mbar_arrive_expect_tx(&my_bars[s], G::kStageBytes);
+        bulk_copy_g2s(dst, kc + off, G::kTileBytes, &my_bars[s], policy);
+        bulk_copy_g2s(dst + G::kTileBytes, vc + off, G::kTileBytes, &my_bars[s], policy);
+    };
+
+    const int my_chunks = nchunks > warp ? (nchunks - warp + NW - 1) / NW : 0;
+    if (lane == 0) {
+        for (int i = 0; i < S && i < my_chunks; ++i) issue(warp + i * NW, i);
+    }
+
+    // ---- per-lane query slice (pre-scaled) and accumulators
+    const int sub = lane % LPT;   // which 8 dims
+    const int grp = lane / LPT;   // which token row of a TPG-row step
+    float qf[GH][8];
+    {
+        const T *qb = static_cast<const T *>(p.q) +
+                      (static_cast<int64_t>(seq) * p.num_q_heads + hq0) * D + sub * 8;
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(qb + g * D);
+            Elem<T>::to_f32x8(u, qf[g]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qf[g][e] *= p.scale_log2;
+        }
+    }
+    float acc[GH][8];
+    float m[GH], l[GH];
+#pragma unroll
+    for (int g = 0; g < GH; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+    }
+
+    bool aborted = false;
+    for (int i = 0; i < my_chunks; ++i) {
+        const int s = i % S;
+        const uint32_t parity = (i / S) & 1;
+        const bool ok = mbar_wait_bounded(&my_bars[s], parity, kWaitTimeoutNs);
+        if (__any_sync(0xffffffffu, !ok)) {
+            // give up: flag it, let this warp's copies still in flight land, stop
+            if (lane == 0) {
+                raise_flag(p.status, PKV_DEVERR_TIMEOUT);
+                for (int k = i; k < my_chunks && k < i + S; ++k)
+                    mbar_wait_bounded(&my_bars[k % S], (k / S) & 1, kDrainTimeoutNs);
+            }
+            __syncwarp();
+            aborted = true;
+            break;
+        }
+        const int c = warp + i * NW;
+        const int valid = min(TILE, ntok - c * TILE);  // >= 1
+        if (tbl[(c * TILE) / BS] >= 0) {
+            const T *ks = reinterpret_cast<const T *>(my_stages + s * G::kStageBytes);
+            const T *vs = ks + TILE * D;
+#pragma unroll
+            for (int it0 = 0; it0 < ITERS; it0 += IT_STEP) {
+                // QK: partial dot products over this lane's 8 dims
+                float sc[IT_STEP][GH];
+#pragma unroll
+                for (int it = 0; it < IT_STEP; ++it) {
+                    const int t = (it0 + it) * TPG + grp;
+                    const uint4 u = *reinterpret_cast<const uint4 *>(ks + t * D + sub * 8);
+                    float kf[8];
+                    Elem<T>::to_f32x8(u, kf);
+#pragma unroll
+                    for (int g = 0; g < GH; ++g) {
+                        float a = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) a = fmaf(qf[g][e], kf[e], a);
+                        sc[it][g] = a;
+                    }
+                }
+                // full dot products: sum over the LPT lanes of each token row
+#pragma unroll
+                for (int it = 0; it < IT_STEP; ++it)
+#pragma unroll
+                    for (int g = 0; g < GH; ++g)
+#pragma unroll
+                        for (int o = LPT / 2; o > 0; o >>= 1)
+                            sc[it][g] += __shfl_xor_sync(0xffffffffu, sc[it][g], o);
+                // mask rows past the end of the context
+#pragma unroll
+                for (int it = 0; it < IT_STEP; ++it) {
+                    const int t = (it0 + it) * TPG + grp;
+                    if (t >= valid) {
+#pragma unroll
+                        for (int g = 0; g < GH; ++g) sc[it][g] = -INFINITY;
+                    }
+                }
+                // online softmax update (P1 §7.2), m warp-uniform
+#pragma unroll
+                for (int g = 0; g < GH; ++g) {
+                    float mx = sc[0][g];
+#pragma unroll
+                    for (int it = 1; it < IT_STEP; ++it) mx = fmaxf(mx, sc[it][g]);
+#pragma unroll
+                    for (int o = LPT; o < 32; o <<= 1)
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    if (mx > m[g]) {  // warp-uniform branch
+                        const float alpha = fast_exp2(m[g] - mx);  // 0 when m was -inf
+                        l[g] *= alpha;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+                        m[g] = mx;
+                    }
+#pragma unroll
+                    for (int it = 0; it < IT_STEP; ++it) {
+                        sc[it][g] = fast_exp2(sc[it][g] - m[g]);  // masked rows -> 0
+                        l[g] += sc[it][g];
+                    }
+                }
+                // PV: lane-local, each lane owns 8 dims of every head
+#pragma unroll
+                for (int it = 0; it < IT_STEP; ++it) {
+                    const int t = (it0 + it) * TPG + grp;
+                    if (t < valid) {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(vs + t * D + sub * 8);
+                        float vf[8];
+                        Elem<T>::to_f32x8(u, vf);
+#pragma unroll
+                        for (int g = 0; g < GH; ++g)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(sc[it][g], vf[e], acc[g][e]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && i + S < my_chunks) {
+            fence_proxy_async_smem();
+            issue(warp + (i + S) * NW, s);
+        }
+    }
+
+    // ---- merge the token groups of this warp (same m across the warp)
+#pragma unroll
+    for (int g = 0; g < GH; ++g) {
+#pragma unroll
+        for (int o = LPT; o < 32; o <<= 1) {
+            l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
+        }
+    }
+    if (aborted) {
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+        }
+    }
+
+    // ---- merge the warps through shared memory (each warp reuses its own
+    //      stage buffers: all of its copies have landed)
+    float *mine = reinterpret_cast<float *>(my_stages);  // [GH][D + 2]
+    if (grp == 0) {
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+            float4 *dst = reinterpret_cast<float4 *>(mine + g * (D + 4) + sub * 8);
+            dst[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+            dst[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+        }
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+            mine[g * (D + 4) + D] = m[g];
+            mine[g * (D + 4) + D + 1] = l[g];
+        }
+    }
+    __syncthreads();
+
+    const bool single = nparts == 1;
+    for (int idx = threadIdx.x; idx < GH * D; idx += blockDim.x) {
+        const int g = idx / D;
+        const int j = idx - g * D;
+        float mw[NW];
+        float mmax = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float *src = reinterpret_cast<const float *>(stages + w * S * G::kStageBytes);
+            mw[w] = src[g * (D + 4) + D];
+            mmax = fmaxf(mmax, mw[w]);
+        }
+        float lsum = 0.f, osum = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float *src = reinterpret_cast<const float *>(stages + w * S * G::kStageBytes);
+            const float wgt = mw[w] == -INFINITY ? 0.f : fast_exp2(mw[w] - mmax);
+            lsum += wgt * src[g * (D + 4) + D + 1];
+            osum += wgt * src[g * (D + 4) + j];
+        }
+        const int hq = hq0 + g;
+        const int64_t row = static_cast<int64_t>(seq) * p.num_q_heads + hq;
+        if (single) {
+            const float r = lsum > 0.f ? osum / lsum : 0.f;
+            static_cast<T *>(p.out)[row * D + j] = Elem<T>::from_f32(r);
+        } else {
+            const int64_t pr = row * p.num_partitions + part;
+            p.ws_o[pr * D + j] = osum;
+            if (j == 0) {
+                p.ws_m[pr] = mmax;
+                p.ws_l[pr] = lsum;
+            }
+        }
+    }
+}
+
+// Log-sum-exp merge of the partitions of each (sequence, query head):
+//   M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L.
+// One warp per (sequence, query head); sequences that fit one partition were
+// written by the main kernel and are skipped.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) paged_decode_merge_kernel(const DecodeParams p,
+                                                                 int num_rows) {
+    constexpr int PER_LANE = D / 32;
+    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= num_rows) return;
+    const int seq = row / p.num_q_heads;
+    int len = p.context_lens[seq];  // clamped exactly as the main kernel does
+    if (len < 0) len = 0;
+    if (len > p.len_cap) len = p.len_cap;
+    const int nparts = len > 0 ? (len + p.partition_size - 1) / p.partition_size : 1;
+    if (nparts <= 1) return;
+    const int64_t base = static_cast<int64_t>(row) * p.num_partitions;
+    float mmax = -INFINITY;
+    for (int q = 0; q < nparts; ++q) mmax = fmaxf(mmax, p.ws_m[base + q]);
+    float lsum = 0.f;
+    float o[PER_LANE];
+#pragma unroll
+    for (int e = 0; e < PER_LANE; ++e) o[e] = 0.f;
+    for (int q = 0; q < nparts; ++q) {
+        const float mq = p.ws_m[base + q];
+        const float w = mq == -INFINITY ? 0.f : fast_exp2(mq - mmax);
+        lsum += w * p.ws_l[base + q];
+        const float *src = p.ws_o + (base + q) * D + lane * PER_LANE;
+#pragma unroll
+        for (int e = 0; e < PER_LANE; ++e) o[e] += w * src[e];
+    }
+    T *dst = static_cast<T *>(p.out) + static_cast<int64_t>(row) * D + lane * PER_LANE;
+#pragma unroll
+    for (int e = 0; e < PER_LANE; ++e) dst[e] = Elem<T>::from_f32(lsum > 0.f ? o[e] / lsum : 0.f);
+}
+
+}  // namespace pkv

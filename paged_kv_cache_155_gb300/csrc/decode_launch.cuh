@@ -1,0 +1,71 @@
+// decode_launch.cuh -- host-side dispatch from runtime (head_dim, block_size,
+// heads per block) to the decode kernel instantiations of one element type.
+// Included by decode_f16.cu and decode_bf16.cu so the two element types
+// compile as separate translation units.
+#pragma once
+
+#include <atomic>
+
+#include "decode_kernel.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+
+template <typename T, int D, int BS, int GH>
+pkv_status launch_decode_one(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
+    using G = DecodeGeom<D, BS>;
+    static std::atomic<uint64_t> configured_devices{0};  // bit per device ordinal
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    if (!bit || !(configured_devices.load(std::memory_order_acquire) & bit)) {
+        if (cudaFuncSetAttribute(paged_decode_kernel<T, D, BS, GH>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 G::kSmemBytes) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured_devices.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    paged_decode_kernel<T, D, BS, GH><<<grid, G::kWarps * 32, G::kSmemBytes, stream>>>(p);
+    count_launch();
+    return launch_status();
+}
+
+template <typename T, int D, int BS>
+pkv_status launch_decode_gh(const DecodeParams &p, int gh, dim3 grid, cudaStream_t s) {
+    switch (gh) {
+        case 1: return launch_decode_one<T, D, BS, 1>(p, grid, s);
+        case 2: return launch_decode_one<T, D, BS, 2>(p, grid, s);
+        case 4: return launch_decode_one<T, D, BS, 4>(p, grid, s);
+        case 8: return launch_decode_one<T, D, BS, 8>(p, grid, s);
+    }
+    return PKV_ERR_UNSUPPORTED;
+}
+
+template <typename T>
+pkv_status launch_decode_typed(const DecodeParams &p, int head_dim, int block_size, int gh,
+                               dim3 grid, int merge_rows, cudaStream_t s) {
+    pkv_status st = PKV_ERR_UNSUPPORTED;
+    if (head_dim == 128) {
+        if (block_size == 8) st = launch_decode_gh<T, 128, 8>(p, gh, grid, s);
+        else if (block_size == 16) st = launch_decode_gh<T, 128, 16>(p, gh, grid, s);
+        else if (block_size == 32) st = launch_decode_gh<T, 128, 32>(p, gh, grid, s);
+    } else if (head_dim == 64) {
+        if (block_size == 8) st = launch_decode_gh<T, 64, 8>(p, gh, grid, s);
+        else if (block_size == 16) st = launch_decode_gh<T, 64, 16>(p, gh, grid, s);
+        else if (block_size == 32) st = launch_decode_gh<T, 64, 32>(p, gh, grid, s);
+    }
+    if (st != PKV_OK || merge_rows == 0) return st;
+    const unsigned blocks = static_cast<unsigned>((merge_rows + 3) / 4);
+    if (head_dim == 128) paged_decode_merge_kernel<T, 128><<<blocks, 128, 0, s>>>(p, merge_rows);
+    else paged_decode_merge_kernel<T, 64><<<blocks, 128, 0, s>>>(p, merge_rows);
+    count_launch();
+    return launch_status();
+}
+
+// Defined in decode_f16.cu / decode_bf16.cu.
+pkv_status launch_decode_f16(const DecodeParams &p, int head_dim, int block_size, int gh,
+                             dim3 grid, int merge_rows, cudaStream_t s);
+pkv_status launch_decode_bf16(const DecodeParams &p, int head_dim, int block_size, int gh,
+                              dim3 grid, int merge_rows, cudaStream_t s);
+
+}  // namespace pkv

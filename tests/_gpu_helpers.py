@@ -1,0 +1,72 @@
+"""Helpers for the GPU parity tests: run the library's step on the device, run
+the oracle on host copies of the same inputs, compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_cache_155_gb300 as pkv
+from paged_kv_cache_155_gb300 import _build
+from tests._paged_helpers import dtype_code, to_bits
+
+# Acceptance for attention outputs: |got - ref| <= ATOL + RTOL * |ref| elementwise,
+# against the fp64 oracle (max abs error 5e-3, relative error 1e-2).
+ATOL = 5e-3
+RTOL = 1e-2
+
+
+def device():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    _build.build()
+    return torch.device("cuda:0")
+
+
+def assert_close(got: torch.Tensor, ref: np.ndarray, what: str = "decode"):
+    g = got.detach().float().cpu().double().numpy()
+    err = np.abs(g - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} values out of tolerance; "
+                             f"max abs err {err.max():.3e}; first at {idx.tolist()}")
+    assert np.isfinite(g).all()
+    return float(err.max())
+
+
+def check_no_device_flags(dev):
+    flags, names = pkv.get_device_error(dev)
+    assert flags == 0, f"device status flags raised: {names}"
+
+
+def host_pool_bits(kv: torch.Tensor) -> np.ndarray:
+    return to_bits(kv.cpu())
+
+
+def oracle_decode(q_bits, pool_bits, tables, lens, num_kv_heads, block_size, scale, dtype):
+    flat = np.ascontiguousarray(pool_bits).reshape(-1)
+    half = pool_bits.shape[2] * pool_bits.shape[3] * pool_bits.shape[4]
+    return oracle.paged_decode(q_bits, flat, flat[half:], 2 * half, np.asarray(tables),
+                               np.asarray(lens), num_kv_heads, block_size, scale, dtype_code(dtype))
+
+
+def run_step(wl, partition_size=0, tables=None):
+    """The library's decode step on device: cache write of the new token at
+    position len-1, then paged decode.  Returns out (device)."""
+    k_cache, v_cache = pkv.split_pool(wl.kv)
+    bt = wl.block_tables if tables is None else tables
+    slots = pkv.slot_mapping(bt.cpu(), wl.new_positions.cpu(), wl.block_size).to(wl.kv.device)
+    pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
+    return pkv.paged_attention_decode(wl.q, k_cache, v_cache, bt, wl.context_lens, wl.scale,
+                                      max_context_len=int(wl.context_lens.max().item()),
+                                      partition_size=partition_size)
+
+
+def oracle_step_pool(wl_host_pool_bits, wl, tables=None):
+    """Oracle cache write of the new tokens into a host pool copy (in place)."""
+    bt = (wl.block_tables if tables is None else tables).cpu().numpy()
+    slots = oracle.slot_mapping(bt, wl.new_positions.cpu().numpy(), wl.block_size)
+    oracle.reshape_and_cache(to_bits(wl.k_new.cpu()), to_bits(wl.v_new.cpu()), slots,
+                             wl_host_pool_bits, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    return slots

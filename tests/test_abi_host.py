@@ -1,0 +1,165 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, rejects out-of-contract arguments on the host before touching CUDA,
+and its launch planner behaves as documented.  Also checks the product's host
+slot helper against the oracle's slot rule."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_155_gb300 import _build, block_table
+from tests.conftest import ROOT
+
+INVALID, UNSUPPORTED = 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    from paged_kv_cache_155_gb300._lib import lib as load
+    return load()
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    return sorted(set(re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = header_symbols()
+    for name in ("pkv_reshape_and_cache", "pkv_paged_attention_decode", "pkv_copy_blocks",
+                 "pkv_decode_workspace_bytes", "pkv_get_device_error", "pkv_status_string"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    syms = header_symbols()
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(\w+)$", out, flags=re.M))
+    missing = [s for s in syms if s not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    for s in syms:
+        assert getattr(lib, s) is not None
+    # nothing else leaks out under the pkv_ prefix that the header does not declare
+    extra = sorted(s for s in exported if s.startswith("pkv_") and s not in syms)
+    assert not extra, f"exported but undeclared: {extra}"
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.pkv_status_string(code)
+    assert b"unknown" in lib.pkv_status_string(99)
+
+
+def _dec(lib, **kw):
+    a = dict(q=16, k=16, v=16, nb=64, stride=2 * 4 * 16 * 64, bt=16, mb=8, cl=16, maxl=100,
+             b=4, hq=4, hkv=4, d=64, bs=16, scale=0.125, out=16, ws=None, wsb=0, part=0, dt=0)
+    a.update(kw)
+    return lib.pkv_paged_attention_decode(a["q"], a["k"], a["v"], a["nb"], a["stride"], a["bt"],
+                                          a["mb"], a["cl"], a["maxl"], a["b"], a["hq"], a["hkv"],
+                                          a["d"], a["bs"], a["scale"], a["out"], a["ws"], a["wsb"],
+                                          a["part"], a["dt"], None)
+
+
+def test_decode_rejects_bad_arguments_on_host(lib):
+    assert _dec(lib, d=96) == UNSUPPORTED
+    assert _dec(lib, bs=64) == UNSUPPORTED
+    assert _dec(lib, dt=7) == UNSUPPORTED
+    assert _dec(lib, hq=6, hkv=4) == INVALID          # not a multiple
+    assert _dec(lib, maxl=8 * 16 + 1) == INVALID      # beyond max_blocks_per_seq * bs
+    assert _dec(lib, stride=100) == INVALID           # smaller than one half block
+    assert _dec(lib, stride=2 * 4 * 16 * 64 + 4) == INVALID  # not 16-byte aligned
+    assert _dec(lib, k=8) == INVALID                  # misaligned cache pointer
+    assert _dec(lib, q=0) == INVALID                  # null q
+    assert _dec(lib, scale=float("nan")) == INVALID
+    assert _dec(lib, part=24) == INVALID              # not a multiple of block_size
+    assert _dec(lib, nb=0) == INVALID
+    assert _dec(lib, b=-1) == INVALID
+
+
+def test_cache_ops_reject_bad_arguments_on_host(lib):
+    r = lib.pkv_reshape_and_cache
+    good = dict(kn=16, vn=16, sm=16, t=4, kc=16, vc=16, nb=8, stride=2 * 2 * 16 * 64, hkv=2, d=64, bs=16, dt=0)
+
+    def call(**kw):
+        a = dict(good)
+        a.update(kw)
+        return r(a["kn"], a["vn"], a["sm"], a["t"], a["kc"], a["vc"], a["nb"], a["stride"],
+                 a["hkv"], a["d"], a["bs"], a["dt"], None)
+
+    assert call(d=80) == UNSUPPORTED
+    assert call(t=-1) == INVALID
+    assert call(kn=0) == INVALID
+    assert call(sm=12) == INVALID          # int64 slots must be 8-byte aligned
+    assert call(stride=10) == INVALID
+    assert call(t=0, kn=0, vn=0, sm=0) == 0  # empty: no-op, nothing dereferenced
+    c = lib.pkv_copy_blocks
+    assert c(16, 16, 8, 2 * 2 * 16 * 64, 2, 64, 16, 0, 3, 0, None) == INVALID   # null pairs
+    assert c(16, 16, 8, 2 * 2 * 16 * 64, 2, 64, 16, 0, 0, 0, None) == 0         # empty
+    assert c(16, 16, 8, 2 * 2 * 16 * 64, 2, 64, 12, 16, 1, 0, None) == UNSUPPORTED
+    assert lib.pkv_debug_wait_timeout(0, None) == INVALID
+
+
+def plan(lib, b, hq, hkv, d, bs, maxl, part, sm=152):
+    outs = [ctypes.c_int() for _ in range(4)]
+    st = lib.pkv_decode_plan(b, hq, hkv, d, bs, maxl, part, sm, *[ctypes.byref(o) for o in outs])
+    return st, [o.value for o in outs]
+
+
+def test_plan_explicit_partition(lib):
+    st, (p, n, gh, merge) = plan(lib, 16, 64, 8, 128, 16, 32768, 512)
+    assert st == 0 and p == 512 and n == 64 and gh == 8 and merge == 1
+
+
+def test_plan_heads_per_block_follows_the_group(lib):
+    for hq, hkv, want in [(32, 32, 1), (32, 16, 2), (32, 8, 4), (64, 8, 8), (24, 8, 1),
+                          (48, 8, 2), (128, 8, 8)]:
+        st, (_, _, gh, _) = plan(lib, 4, hq, hkv, 128, 16, 1000, 0)
+        assert st == 0 and gh == want, (hq, hkv)
+
+
+def test_plan_auto_split_fills_the_gpu_and_respects_limits(lib):
+    # tiny: never split below the minimum partition
+    st, (p, n, _, merge) = plan(lib, 4, 4, 4, 64, 16, 100, 0)
+    assert st == 0 and n == 1 and merge == 0 and p % 16 == 0
+    # few long sequences: split into several partitions, each a multiple of bs
+    st, (p, n, _, merge) = plan(lib, 16, 64, 8, 128, 16, 32768, 0)
+    assert st == 0 and n > 1 and merge == 1 and p % 16 == 0 and (n - 1) * p < 32768 <= n * p
+    # empty batch of contexts
+    st, (p, n, _, merge) = plan(lib, 4, 4, 4, 64, 16, 0, 0)
+    assert st == 0 and n == 1 and merge == 0
+    # partition too long for the table slice
+    st, _ = plan(lib, 1, 8, 8, 128, 16, 1 << 20, 1024 * 16 + 16)
+    assert st == INVALID
+
+
+def test_workspace_bytes_explicit_partition(lib):
+    n = lib.pkv_decode_workspace_bytes(16, 64, 8, 128, 16, 32768, 512)
+    assert n == 16 * 64 * 64 * (128 + 2) * 4
+    assert lib.pkv_decode_workspace_bytes(4, 4, 4, 64, 16, 100, 256) == 0
+    assert lib.pkv_decode_workspace_bytes(4, 4, 4, 64, 16, 100, 24) == ctypes.c_size_t(-1).value
+
+
+def test_host_slot_helper_matches_oracle_slot_rule():
+    g = torch.Generator().manual_seed(0)
+    for bs in (8, 16, 32):
+        tables = torch.randint(0, 1000, (9, 40), generator=g, dtype=torch.int32)
+        pos = torch.randint(0, 40 * bs, (9,), generator=g)
+        pos[3] = -1
+        got = block_table.slot_mapping(tables, pos, bs).numpy()
+        for i in range(9):
+            if pos[i] < 0:
+                assert got[i] == -1
+            else:
+                assert got[i] == oracle.slot_for_position(tables[i].numpy(), int(pos[i]), bs)
+
+
+def test_package_import_does_not_need_a_gpu():
+    import paged_kv_cache_155_gb300 as pkv
+    assert callable(pkv.paged_attention_decode)
