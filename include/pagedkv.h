@@ -24,9 +24,10 @@
  * Memory.  Every pointer argument except the host-side outputs of
  *   pkv_get_device_error is a DEVICE pointer owned by the caller.  Tensor base
  *   pointers must be 16-byte aligned and block strides a multiple of 8
- *   elements.  The library allocates no memory; its only state is one device
- *   status word per device (see pkv_get_device_error) and cached device
- *   attributes.
+ *   elements.  No call allocates memory; the library's only state is one
+ *   device status word per device (see pkv_get_device_error), the fixed
+ *   scratch array of pkv_paged_attention_decode_static_scratch, and cached
+ *   device attributes.
  * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).  Every
  *   call only enqueues work on it and returns; results are ready when the
  *   stream reaches that point.
@@ -58,7 +59,9 @@ typedef enum pkv_status {
     PKV_ERR_INVALID_ARG = 1,   /* host-checkable argument out of contract      */
     PKV_ERR_UNSUPPORTED = 2,   /* valid but not built (dtype, head_dim, bs)    */
     PKV_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed         */
-    PKV_ERR_DEVICE = 4         /* pkv_get_device_error found flags raised      */
+    PKV_ERR_DEVICE = 4,        /* pkv_get_device_error found flags raised      */
+    PKV_ERR_SCRATCH_LIMIT = 5  /* split-context scratch needed exceeds
+                                  PKV_STATIC_SCRATCH_BYTES (static-scratch decode) */
 } pkv_status;
 
 typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
@@ -153,6 +156,44 @@ PKV_API pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blo
                                    int64_t block_stride_elems, int num_kv_heads, int head_dim,
                                    int block_size, const int64_t *src_dst_pairs,
                                    int64_t num_pairs, pkv_dtype dtype, void *stream);
+
+/* Size of the library's built-in decode scratch array (per device). */
+#define PKV_STATIC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+
+/*
+ * pkv_paged_attention_decode_static_scratch -- pkv_paged_attention_decode for
+ * callers that cannot allocate device memory.  The pages have no counterpart:
+ * this is a deployment convenience, not part of the method.
+ *
+ * Who needs it: a caller that has no device memory to give the decode call
+ * its split-context workspace -- e.g. a serving engine that reserved nearly
+ * all free device memory for its KV block pool up front, or a plug-in whose
+ * host framework hands it tensor pointers but no allocator it may call.
+ *
+ * Arguments and results are those of pkv_paged_attention_decode without the
+ * workspace pair; the scratch comes from a PKV_STATIC_SCRATCH_BYTES array
+ * inside the library that every device loading the library keeps until the
+ * process exits.  The call allocates nothing (no cudaMalloc/cudaFree, no
+ * allocating library routine).
+ *   - A plan whose scratch (pkv_decode_workspace_bytes for the same
+ *     arguments) exceeds PKV_STATIC_SCRATCH_BYTES is rejected with
+ *     PKV_ERR_SCRATCH_LIMIT before anything is enqueued; pass a larger
+ *     partition_size (fewer partitions) or use the workspace entry point.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents.  Nothing in it needs clearing (every value is written before
+ *     it is read), but calls that overlap on the GPU -- e.g. on two streams
+ *     with no ordering between them -- race on it and must be serialised by
+ *     the caller.
+ */
+PKV_API pkv_status pkv_paged_attention_decode_static_scratch(
+    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+    int64_t block_stride_elems, const int32_t *block_tables, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, float scale, void *out, int partition_size,
+    pkv_dtype dtype, void *stream);
 
 /*
  * pkv_get_device_error -- synchronise `stream`, read the current device's

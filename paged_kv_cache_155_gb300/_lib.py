@@ -34,10 +34,13 @@ SIGNATURES = {
                               ctypes.POINTER(I32), ctypes.POINTER(I32), ctypes.POINTER(I32),
                               ctypes.POINTER(I32)]),
     "pkv_debug_wait_timeout": (I32, [U64, P]),
+    "pkv_paged_attention_decode_static_scratch": (I32, [P, P, P, I64, I64, P, I32, P, I32, I32,
+                                                        I32, I32, I32, I32, ctypes.c_float, P,
+                                                        I32, I32, P]),
 }
 
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
-          4: "PKV_ERR_DEVICE"}
+          4: "PKV_ERR_DEVICE", 5: "PKV_ERR_SCRATCH_LIMIT"}
 DEVERR = {0x1: "slot", 0x2: "block_table", 0x4: "context_len", 0x8: "copy_pair", 0x10: "timeout"}
 
 

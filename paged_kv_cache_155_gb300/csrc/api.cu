@@ -104,6 +104,8 @@ PKV_API const char *pkv_status_string(pkv_status status) {
         case PKV_ERR_UNSUPPORTED: return "unsupported dtype, head_dim or block_size";
         case PKV_ERR_CUDA: return "CUDA runtime error";
         case PKV_ERR_DEVICE: return "a kernel raised a device status flag";
+        case PKV_ERR_SCRATCH_LIMIT:
+            return "split-context scratch needed exceeds the library's static scratch array";
     }
     return "unknown status";
 }
