@@ -135,10 +135,10 @@ def _algorithmic_bytes(wl):
     return kv + qo
 
 
-def _make_workload(name, device, seed):
+def _make_workload(name, device, seed, num_seqs=None):
     from paged_kv_cache_155_gb300 import workloads
-    return workloads.NAMED[name](device=device, seed=seed) if name != "tiny" else \
-        workloads.tiny(device=device, seed=seed)
+    kw = {"num_seqs": num_seqs} if (num_seqs and name != "tiny") else {}
+    return workloads.NAMED[name](device=device, seed=seed, **kw)
 
 
 def _workload_config(wl, name, plan, partition):
@@ -202,14 +202,15 @@ def cpu_baseline(wl_dev, budget_s=12.0):
     qb = _bits(wl_host.q)
     units = _unit_list(wl_host, 1)
     t1 = _oracle_units(wl_host, pool, units, qb)
-    n = max(1, min(wl_host.num_seqs * wl_host.num_kv_heads, int(budget_s / max(t1, 1e-6))))
+    total = wl_host.num_seqs * wl_host.num_kv_heads
+    n = max(1, min(64 * total, int(budget_s / max(t1, 1e-6))))   # whole steps repeat if cheap
     units = _unit_list(wl_host, n, start=1)
     t = _oracle_units(wl_host, pool, units, qb)
     tokens = n / wl_host.num_kv_heads  # one decode token = all KV heads of one sequence
     return {"value": tokens / t, "unit": "tokens/s", "cores": oracle.num_threads(),
             "kind": "oracle",
             "sample": f"{n} (sequence, KV head) units of {wl_host.num_seqs}x{wl_host.num_kv_heads}"
-                      f" ({n / (wl_host.num_seqs * wl_host.num_kv_heads):.3f} of one step),"
+                      f" ({n / total:.3f} steps' worth),"
                       f" {t:.1f} s, fp64 C oracle, OpenMP over query heads of a unit"}
 
 
@@ -220,7 +221,7 @@ def run_reference(args):
     import torch
     import oracle
     oracle.build()
-    wl = _make_workload(args.workload, "cpu", 1234)
+    wl = _make_workload(args.workload, "cpu", 1234, args.num_seqs)
     pool, qb = _bits(wl.kv), _bits(wl.q)
     per_step_budget = max(0.002, 150.0 / max(1, args.steps + args.warmup))
     t1 = _oracle_units(wl, pool, _unit_list(wl, 1), qb)
@@ -268,7 +269,7 @@ def run_ours(args):
     _build.build()
     import paged_kv_cache_155_gb300 as pkv
 
-    wl = _make_workload(args.workload, str(dev), 1234 + rank)
+    wl = _make_workload(args.workload, str(dev), 1234 + rank, args.num_seqs)
     k_cache, v_cache = pkv.split_pool(wl.kv)
     maxl = int(wl.context_lens.max())
     part = args.partition
@@ -411,6 +412,8 @@ def main(argv=None):
     ap.add_argument("--partition", type=int, default=-1,
                     help="tokens per split-context partition (0 = library's choice; "
                          "default: the workload's own setting)")
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="override the workload's batch (profiling on a smaller case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
