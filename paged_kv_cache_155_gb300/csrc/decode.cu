@@ -10,6 +10,13 @@ namespace {
 constexpr int kResidentCtasPerSm = 2;  // decode CTAs resident per SM (shared-memory bound)
 constexpr int kTargetWaves = 8;        // CTA waves the automatic split aims for
 constexpr int kMinAutoPartition = 256; // tokens: below this the per-CTA set-up dominates
+constexpr int kTcItemsPerSm = 24;      // tensor-core path: work items per persistent CTA
+
+// head_dim 128 with 4, 8 or 16 query heads per KV head: the group turns
+// QK^T and PV into dense tiles and runs on the tensor cores.
+bool use_tensor_cores(int head_dim, int group) {
+    return head_dim == 128 && (group == 4 || group == 8 || group == 16);
+}
 
 int heads_per_block_for(int group) {
     if (group % 8 == 0) return 8;
@@ -22,6 +29,42 @@ size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, int num_partit
     if (num_partitions <= 1) return 0;
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * num_partitions;
     return rows * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// 3-D view of one half (K or V) of the pool: (head_dim, num_kv_heads*block_size
+// rows, num_blocks) with the caller's block stride; boxes are one block's rows
+// of one head, 64 columns wide, 128-byte swizzled.
+bool encode_half_map(CUtensorMap *map, const void *base, int64_t num_blocks,
+                     int64_t block_stride_elems, int num_kv_heads, int block_size, pkv_dtype dt) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(num_kv_heads) * block_size,
+                                static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(block_stride_elems) * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(block_size), 1};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    return fn(map, dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+              3, const_cast<void *>(base), dims, strides, box, elem_strides,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -43,12 +86,24 @@ PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_hea
     const int max_partition = pkv::DecodeGeom<128, 16>::kMaxTableEntries * block_size;
     if (partition_size > max_partition) return PKV_ERR_INVALID_ARG;
     const int group = num_q_heads / num_kv_heads;
-    const int gh = heads_per_block_for(group);
+    const bool tc = use_tensor_cores(head_dim, group);
+    const int gh = tc ? group : heads_per_block_for(group);
     const int64_t grid_y = static_cast<int64_t>(num_kv_heads) * (group / gh);
     if (grid_y > 65535 || num_seqs > 65535) return PKV_ERR_INVALID_ARG;
 
     int part = partition_size;
-    if (part == 0) {
+    if (part == 0 && tc) {
+        // Persistent CTAs take work items round-robin: enough items per SM to
+        // balance uneven lengths, whole 128-token tiles per partition.
+        const int64_t units = std::max<int64_t>(1, static_cast<int64_t>(num_seqs) * grid_y);
+        const int64_t target = static_cast<int64_t>(sm_count) * kTcItemsPerSm;
+        const int64_t want = std::max<int64_t>(1, (target + units - 1) / units);
+        int64_t p = (static_cast<int64_t>(max_context_len) + want - 1) / want;
+        p = std::max<int64_t>(p, kMinAutoPartition);
+        p = (p + 127) / 128 * 128;
+        p = (p + block_size - 1) / block_size * block_size;
+        part = static_cast<int>(std::min<int64_t>(p, max_partition));
+    } else if (part == 0) {
         // Enough CTAs for several waves over every SM, but partitions no
         // shorter than kMinAutoPartition tokens.
         const int64_t units = std::max<int64_t>(1, static_cast<int64_t>(num_seqs) * grid_y);
@@ -122,6 +177,8 @@ PKV_API pkv_status pkv_paged_attention_decode(
     if (!status) return PKV_ERR_CUDA;
 
     const int group = num_q_heads / num_kv_heads;
+    const bool tc = use_tensor_cores(head_dim, group);
+    if (tc && num_blocks > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
     pkv::DecodeParams p{};
     p.q = q;
     p.k_cache = k_cache;
@@ -138,17 +195,34 @@ PKV_API pkv_status pkv_paged_attention_decode(
     p.block_stride = block_stride_elems;
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.len_cap = max_context_len;  // <= max_blocks_per_seq * block_size (checked above)
+    p.num_seqs = num_seqs;
     p.num_q_heads = num_q_heads;
     p.group = group;
     p.subgroups = group / gh;
+    p.items_y = num_kv_heads * p.subgroups;
     p.partition_size = part;
     p.num_partitions = nparts;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
 
-    const dim3 grid(static_cast<unsigned>(nparts), static_cast<unsigned>(num_kv_heads * p.subgroups),
-                    static_cast<unsigned>(num_seqs));
     const int merge_rows = merge ? num_seqs * num_q_heads : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (tc) {
+        CUtensorMap tk, tv;
+        if (!encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads,
+                             block_size, dtype) ||
+            !encode_half_map(&tv, v_cache, num_blocks, block_stride_elems, num_kv_heads,
+                             block_size, dtype))
+            return PKV_ERR_CUDA;
+        const int sm = pkv::current_sm_count();
+        if (sm <= 0) return PKV_ERR_CUDA;
+        const int64_t items = static_cast<int64_t>(num_seqs) * p.items_y * nparts;
+        const int grid = static_cast<int>(std::min<int64_t>(sm, items));
+        return dtype == PKV_F16
+                   ? pkv::launch_decode_tc_f16(p, tk, tv, block_size, gh, grid, merge_rows, s)
+                   : pkv::launch_decode_tc_bf16(p, tk, tv, block_size, gh, grid, merge_rows, s);
+    }
+    const dim3 grid(static_cast<unsigned>(nparts), static_cast<unsigned>(num_kv_heads * p.subgroups),
+                    static_cast<unsigned>(num_seqs));
     return dtype == PKV_F16
                ? pkv::launch_decode_f16(p, head_dim, block_size, gh, grid, merge_rows, s)
                : pkv::launch_decode_bf16(p, head_dim, block_size, gh, grid, merge_rows, s);

@@ -48,7 +48,9 @@ struct DecodeParams {
     int64_t block_stride;  // elements between consecutive physical blocks
     int max_blocks_per_seq;
     int len_cap;     // min(max_context_len, max_blocks_per_seq * block_size)
+    int num_seqs;
     int num_q_heads;
+    int items_y;     // num_kv_heads * subgroups (work items per sequence partition)
     int group;       // num_q_heads / num_kv_heads
     int subgroups;   // group / heads_per_block
     int partition_size;

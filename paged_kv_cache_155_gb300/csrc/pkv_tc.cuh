@@ -1,0 +1,160 @@
+// pkv_tc.cuh -- Blackwell tensor-core building blocks (sm_100-family PTX):
+// tensor-memory allocation, shared-memory matrix descriptors, the 32-bit
+// instruction descriptor of tcgen05.mma kind::f16, the MMA / commit / TMEM
+// load wrappers and tiled TMA (cp.async.bulk.tensor) loads.
+//
+// Shared-memory operand layouts used here are the 128-byte-swizzled canonical
+// layouts of 16-bit data:
+//   K-major  (rows along M or N, 64 K-elements = 128 B per row): 8-row atoms
+//            of 1024 B; `stride` = byte step between 8-row groups; the K step
+//            of one MMA (16 elements = 32 B) advances the start address.
+//   MN-major (rows along K, 64 M/N-elements = 128 B per row): 8-row atoms of
+//            1024 B; `leading` = byte step between 64-element groups along
+//            M/N, `stride` = byte step between 8-row groups along K.
+// A TMA tile load with CU_TENSOR_MAP_SWIZZLE_128B and a 128-byte inner box
+// writes exactly this layout when its destination is 1024-byte aligned.
+#pragma once
+
+#include <stdint.h>
+
+namespace pkv {
+namespace tc {
+
+// ---- tensor memory ---------------------------------------------------------
+// Executed by one whole warp.  Writes the allocation's TMEM address to *slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(slot))),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---- descriptors -------------------------------------------------------------
+// Shared-memory matrix descriptor: start address, leading / stride byte
+// offsets (16-byte units), descriptor version 1 (bit 46), base offset 0,
+// swizzle mode in bits 61-63 (2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_byte_addr, uint32_t leading_bytes,
+                                                    uint32_t stride_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_byte_addr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((leading_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((stride_bytes >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma .kind::f16 with fp32 accumulation:
+// bits 4-5 D type (1 = f32), 7-9 A type and 10-12 B type (0 = f16, 1 = bf16),
+// bit 15 / 16 A / B major (0 = K-major, 1 = MN-major), 17-22 N>>3, 24-28 M>>4.
+__host__ __device__ constexpr uint32_t idesc_f16_f32acc(bool bf16, int m, int n, bool a_mn_major,
+                                                         bool b_mn_major) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+           ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ---- MMA, commit, TMEM loads ---------------------------------------------------
+// D[tmem] (+)= A[smem] * B[smem], issued by one thread.
+__device__ __forceinline__ void mma_f16_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
+        : "memory");
+}
+
+// 32 lanes x N consecutive 32-bit columns: thread i of the warp gets lane
+// (taddr.lane + i), columns taddr.col .. +N-1.
+__device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, float v[4]) {
+    uint32_t r[4];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, float v[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float v[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float *v) {
+    static_assert(N == 4 || N == 8 || N == 16, "TMEM load width");
+    if constexpr (N == 4) tmem_ld_x4(taddr, v);
+    else if constexpr (N == 8) tmem_ld_x8(taddr, v);
+    else tmem_ld_x16(taddr, v);
+}
+
+// ---- tiled TMA ------------------------------------------------------------------
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// 3-D tile load (coordinates innermost first) into this CTA's shared memory,
+// completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0, int c1, int c2,
+                                            uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(
+            static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2),
+        "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "l"(policy)
+        : "memory");
+}
+
+// Byte offset of element (row, col) of a 128-byte-swizzled panel of 16-bit
+// values whose rows are 128 B (64 elements) and whose 8-row atoms are 1024 B.
+__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
+    const uint32_t chunk = (col >> 3) ^ (row & 7u);
+    return row * 128u + chunk * 16u + (col & 7u) * 2u;
+}
+
+}  // namespace tc
+}  // namespace pkv

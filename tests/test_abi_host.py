@@ -118,10 +118,20 @@ def test_plan_explicit_partition(lib):
 
 
 def test_plan_heads_per_block_follows_the_group(lib):
+    # head_dim 128 with 4, 8 or 16 heads per KV head: the tensor-core path serves the whole group
     for hq, hkv, want in [(32, 32, 1), (32, 16, 2), (32, 8, 4), (64, 8, 8), (24, 8, 1),
-                          (48, 8, 2), (128, 8, 8)]:
+                          (48, 8, 2), (128, 8, 16)]:
         st, (_, _, gh, _) = plan(lib, 4, hq, hkv, 128, 16, 1000, 0)
         assert st == 0 and gh == want, (hq, hkv)
+    # head_dim 64 stays on CUDA cores (at most 8 heads per CTA)
+    st, (_, _, gh, _) = plan(lib, 4, 128, 8, 64, 16, 1000, 0)
+    assert st == 0 and gh == 8
+
+
+def test_plan_tensor_core_partitions_are_whole_tiles(lib):
+    for maxl in (300, 4096, 8192, 32768):
+        st, (p, n, gh, _) = plan(lib, 64, 32, 8, 128, 16, maxl, 0)
+        assert st == 0 and gh == 4 and p % 128 == 0 and (n - 1) * p < maxl <= n * p
 
 
 def test_plan_auto_split_fills_the_gpu_and_respects_limits(lib):
