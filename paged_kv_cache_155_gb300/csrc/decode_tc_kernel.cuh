@@ -19,8 +19,8 @@
 // Structure (one persistent CTA per SM, 6 warps):
 //   warp 0      TMA producer: per 128-token tile, one 3-D tiled bulk-tensor copy
 //               per (block, 64-column half) for K and for V, 128-byte swizzled,
-//               into a 3-stage ring of 64 KiB stages; block-table entries are
-//               read one tile ahead.
+//               into separate rings of 32 KiB K slots and 32 KiB V slots (a K
+//               slot is refilled as soon as QK^T has read it).
 //   warp 1      TMEM owner and MMA issuer (one thread): QK^T of tile i+1 is
 //               issued before PV of tile i so the softmax of tile i overlaps it.
 //   warps 2-5   softmax and accumulation, one TMEM lane quarter each: a thread
@@ -45,33 +45,42 @@ struct TcLayout {
     static constexpr int kTile = 128;          // tokens per MMA tile
     static constexpr int kD = 128;             // head_dim
     static constexpr int kN = 16;              // MMA N (query heads, padded)
-    static constexpr int kStages = 3;
+    // K and V tiles have separate rings: a K slot is free again as soon as
+    // QK^T has read it, a V slot only after PV.
+    static constexpr int kKStages = 2;
+    static constexpr int kVStages = 4;
     static constexpr int kHalfBytes = 128 * 128;        // 128 rows x 64 columns x 2 B
     static constexpr int kKVBytes = 2 * kHalfBytes;     // K (or V) tile: 32 KiB
-    static constexpr int kStageBytes = 2 * kKVBytes;    // K + V: 64 KiB
     static constexpr int kPanelBytes = 4096;            // 16 x 128 x 2 B (Q or P)
-    static constexpr int kOffQ = kStages * kStageBytes;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kKStages * kKVBytes;
+    static constexpr int kOffQ = kOffV + kVStages * kKVBytes;
     static constexpr int kOffP = kOffQ + 2 * kPanelBytes;
     static constexpr int kOffRed = kOffP + 2 * kPanelBytes;           // float [2][4][16] + [4][16]
     static constexpr int kOffBar = kOffRed + 3 * 4 * 16 * 4;
-    static constexpr int kNumBars = 3 + 3 + 2 * 5 + 2 + 1 + 1;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 1 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;           // tmem slot, abort flag
-    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kMaxStagedSeqs = 1024;                      // context lengths kept in smem
+    static constexpr int kOffLens = kOffMisc + 16;
+    static constexpr int kBytes = kOffLens + 4 * kMaxStagedSeqs;
     static constexpr int kSmemBytes = kBytes + 1024;                  // + alignment slack
     static constexpr uint32_t kTmemCols = 64;  // S[2] at 0/16, O[2] at 32/48
 };
 
 // Walks the work items of a launch in order: item r -> (sequence, y, partition).
-// Items of sequence s are nparts(s) * Y consecutive indices.
+// Items of sequence s are nparts(s) * Y consecutive indices.  A CTA's items
+// are gridDim.x apart, so a step may cross several sequences; the lengths come
+// from the shared-memory copy `s_len` when the batch fits it, so that walk
+// costs no global-memory round trips.
 struct ItemWalker {
     int seq = 0;
     int64_t first = 0;  // index of the first item of `seq`
     int nparts = -1;
     int len = 0;
-    __device__ bool seek(const DecodeParams &p, int64_t r, int &y, int &part) {
+    __device__ bool seek(const DecodeParams &p, const int *s_len, int64_t r, int &y, int &part) {
         while (seq < p.num_seqs) {
             if (nparts < 0) {
-                int l = p.context_lens[seq];
+                int l = s_len ? s_len[seq] : p.context_lens[seq];
                 l = l < 0 ? 0 : (l > p.len_cap ? p.len_cap : l);
                 len = l;
                 nparts = l > 0 ? (l + p.partition_size - 1) / p.partition_size : 1;
@@ -122,16 +131,19 @@ __global__ void __launch_bounds__(192, 1)
     unsigned char *sm =
         smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
-    uint64_t *full = bars;            // [3] TMA -> MMA
-    uint64_t *empty = bars + 3;       // [3] MMA -> TMA
-    uint64_t *s_full = bars + 6;      // [2] QK done -> softmax
-    uint64_t *s_empty = bars + 8;     // [2] S read -> MMA
-    uint64_t *p_full = bars + 10;     // [2] P written -> MMA
-    uint64_t *o_full = bars + 12;     // [2] PV done -> softmax
-    uint64_t *o_empty = bars + 14;    // [2] O read -> MMA
-    uint64_t *max_bar = bars + 16;    // [2] softmax tile-max exchange
-    uint64_t *lsum_bar = bars + 18;   // softmax l exchange
-    uint64_t *drain_bar = bars + 19;  // MMA drain on exit
+    constexpr int KS = L::kKStages, VS = L::kVStages;
+    uint64_t *k_full = bars;              // [KS] K tile landed -> MMA
+    uint64_t *k_empty = k_full + KS;      // [KS] QK^T done -> TMA
+    uint64_t *v_full = k_empty + KS;      // [VS] V tile landed -> MMA
+    uint64_t *v_empty = v_full + VS;      // [VS] PV done -> TMA
+    uint64_t *s_full = v_empty + VS;      // [2] QK done -> softmax
+    uint64_t *s_empty = s_full + 2;       // [2] S read -> MMA
+    uint64_t *p_full = s_full + 4;        // [2] P written -> MMA
+    uint64_t *o_full = s_full + 6;        // [2] PV done -> softmax
+    uint64_t *o_empty = s_full + 8;       // [2] O read -> MMA
+    uint64_t *max_bar = s_full + 10;      // [2] softmax tile-max exchange
+    uint64_t *lsum_bar = s_full + 12;     // softmax l exchange
+    uint64_t *drain_bar = s_full + 13;    // MMA drain on exit
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
     float *red_max = reinterpret_cast<float *>(sm + L::kOffRed);            // [2][4][16]
@@ -145,9 +157,13 @@ __global__ void __launch_bounds__(192, 1)
     for (int i = threadIdx.x; i < 4 * L::kPanelBytes / 16; i += blockDim.x)
         reinterpret_cast<uint4 *>(sm + L::kOffQ)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 3; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < KS; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < VS; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
@@ -170,6 +186,17 @@ __global__ void __launch_bounds__(192, 1)
         tc::prefetch_tensormap(&tmap_k);
         tc::prefetch_tensormap(&tmap_v);
     }
+    const bool staged = p.num_seqs <= L::kMaxStagedSeqs;
+    int *s_len = staged ? reinterpret_cast<int *>(sm + L::kOffLens) : nullptr;
+    if (staged) {
+        bool bad = false;
+        for (int i = threadIdx.x; i < p.num_seqs; i += blockDim.x) {
+            const int l = p.context_lens[i];
+            bad |= (l < 0 || l > p.len_cap);
+            s_len[i] = l < 0 ? 0 : (l > p.len_cap ? p.len_cap : l);
+        }
+        if (bad && blockIdx.x == 0) raise_flag(p.status, PKV_DEVERR_CONTEXT_LEN);
+    }
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
@@ -181,11 +208,12 @@ __global__ void __launch_bounds__(192, 1)
         const uint64_t policy = l2_policy_evict_first();
         ItemWalker walk;
         uint32_t g = 0;  // global tile counter
-        int last_issue[3] = {-1, -1, -1};
+        int last_issue[2][8];
+        for (int i = 0; i < 16; ++i) last_issue[i / 8][i % 8] = -1;
         bool ok = true;
         for (int64_t r = blockIdx.x; ok; r += gridDim.x) {
             int y, part;
-            if (!walk.seek(p, r, y, part)) break;
+            if (!walk.seek(p, s_len, r, y, part)) break;
             const int tok0 = part * p.partition_size;
             const int ntok = max(0, min(walk.len, tok0 + p.partition_size) - tok0);
             const int kvh = y / p.subgroups;
@@ -203,61 +231,138 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
                 const unsigned valid = __ballot_sync(0xffffffffu, e >= 0);
-                const int s = g % 3;
-                int go = 1;
-                if (lane == 0) {
-                    go = tc_wait(&empty[s], ((g / 3) & 1) ^ 1, abort_flag, p.status);
-                    if (go) {
-                        const uint32_t bytes = __popc(valid) * BS * 512u;
-                        if (bytes) mbar_arrive_expect_tx(&full[s], bytes);
-                        else mbar_arrive(&full[s]);
-                        last_issue[s] = static_cast<int>(g);
+                const uint32_t bytes = __popc(valid) * BS * 256u;  // per K (or V) tile
+                const int row = lane * BS;
+                // K first (QK^T needs it first), then V; each waits for its own ring
+                for (int kv = 0; kv < 2; ++kv) {
+                    const int nst = kv ? VS : KS;
+                    const int s = g % nst;
+                    uint64_t *fb = kv ? &v_full[s] : &k_full[s];
+                    uint64_t *eb = kv ? &v_empty[s] : &k_empty[s];
+                    int go = 1;
+                    if (lane == 0) {
+                        go = tc_wait(eb, ((g / nst) & 1) ^ 1, abort_flag, p.status);
+                        if (go) {
+                            if (bytes) mbar_arrive_expect_tx(fb, bytes);
+                            else mbar_arrive(fb);
+                            last_issue[kv][s] = static_cast<int>(g);
+                        }
                     }
-                }
-                go = __shfl_sync(0xffffffffu, go, 0);
-                if (!go) {
-                    ok = false;
-                    break;
-                }
-                if (e >= 0) {
-                    unsigned char *stage = sm + s * L::kStageBytes;
-                    const int row = lane * BS;
-                    for (int c = 0; c < 2; ++c) {
-                        tc::tma_load_3d(stage + c * L::kHalfBytes + row * 128, &tmap_k, c * 64,
-                                        kvh * BS, e, &full[s], policy);
-                        tc::tma_load_3d(stage + L::kKVBytes + c * L::kHalfBytes + row * 128, &tmap_v,
-                                        c * 64, kvh * BS, e, &full[s], policy);
+                    if (!__shfl_sync(0xffffffffu, go, 0)) {
+                        ok = false;
+                        break;
                     }
+                    if (e >= 0) {
+                        unsigned char *slot = sm + (kv ? L::kOffV : L::kOffK) + s * L::kKVBytes;
+                        const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            tc::tma_load_3d(slot + c * L::kHalfBytes + row * 128, map, c * 64,
+                                            kvh * BS, e, fb, policy);
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
         }
         if (!ok && lane == 0) {
             // let every copy this warp issued land before the CTA exits
-            for (int s = 0; s < 3; ++s)
-                if (last_issue[s] >= 0)
-                    mbar_wait_bounded(&full[s], (last_issue[s] / 3) & 1, kDrainTimeoutNs);
+            for (int s = 0; s < KS; ++s)
+                if (last_issue[0][s] >= 0)
+                    mbar_wait_bounded(&k_full[s], (last_issue[0][s] / KS) & 1, kDrainTimeoutNs);
+            for (int s = 0; s < VS; ++s)
+                if (last_issue[1][s] >= 0)
+                    mbar_wait_bounded(&v_full[s], (last_issue[1][s] / VS) & 1, kDrainTimeoutNs);
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
+        // Event-driven: lane 0 polls the barriers and issues whichever MMA is
+        // ready, PV first (it frees a V slot), else the next tile's QK^T.  A
+        // fixed order would make PV of one tile wait for the next tile's K.
         constexpr uint32_t idesc_qk = tc::idesc_f16_f32acc(kBF16, 128, L::kN, false, false);
         constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, L::kN, true, false);
-        ItemWalker walk;
-        uint32_t g = 0;
-        uint32_t items_with_tiles = 0;
-        bool ok = true;
-        bool have_prev = false;
+        // Queries of the next item that has tiles, loaded into registers one
+        // item ahead so no global load sits in front of an item's first MMA.
+        constexpr int QCHUNKS = (GH * 16 + 31) / 32;  // 16-byte chunks per lane
+        ItemWalker ahead;
+        int64_t r_ahead = blockIdx.x;
+        uint4 qreg[QCHUNKS];
+        auto load_next_q = [&]() {
+            int ya, pa;
+            while (ahead.seek(p, s_len, r_ahead, ya, pa)) {
+                r_ahead += gridDim.x;
+                const int t0a = pa * p.partition_size;
+                if (min(ahead.len, t0a + p.partition_size) - t0a <= 0) continue;
+                const int hqa = (ya / p.subgroups) * p.group + (ya % p.subgroups) * GH;
+                const T *qsrc = static_cast<const T *>(p.q) +
+                                (static_cast<int64_t>(ahead.seq) * p.num_q_heads + hqa) * D;
+#pragma unroll
+                for (int c = 0; c < QCHUNKS; ++c) {
+                    const int i = lane + c * 32;
+                    if (i < GH * 16)
+                        qreg[c] = *reinterpret_cast<const uint4 *>(qsrc + (i >> 4) * D + (i & 15) * 8);
+                }
+                return;
+            }
+        };
+        load_next_q();
 
-        auto issue_pv = [&](uint32_t t) -> bool {
-            const int b = t & 1;
-            int go = 1;
+        // tiles in QK^T order: the current item and the tile offset within it
+        ItemWalker walk;
+        int64_t r = blockIdx.x;
+        int tok0 = 0, ntok = 0, t0 = 0;
+        auto next_item = [&]() -> bool {
+            int y, part;
+            while (walk.seek(p, s_len, r, y, part)) {
+                r += gridDim.x;
+                tok0 = part * p.partition_size;
+                ntok = max(0, min(walk.len, tok0 + p.partition_size) - tok0);
+                if (ntok > 0) {
+                    t0 = 0;
+                    return true;
+                }
+            }
+            return false;
+        };
+        bool have_tile = next_item();
+        uint32_t n_qk = 0, n_pv = 0;  // tiles whose QK^T / PV have been issued
+        uint32_t items = 0;           // items whose queries went to a panel
+        bool ok = true;
+        uint64_t idle_since = 0;
+        while (ok && (have_tile || n_pv < n_qk)) {
+            int act = 0;  // 1 = PV, 2 = QK
             if (lane == 0) {
-                go = tc_wait(&p_full[b], (t >> 1) & 1, abort_flag, p.status) &&
-                     tc_wait(&o_empty[b], ((t >> 1) & 1) ^ 1, abort_flag, p.status);
-                if (go) {
+                if (n_pv < n_qk && mbar_try_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
+                    mbar_try_wait(&o_empty[n_pv & 1], ((n_pv >> 1) & 1) ^ 1) &&
+                    mbar_try_wait(&v_full[n_pv % VS], (n_pv / VS) & 1))
+                    act = 1;
+                else if (have_tile && mbar_try_wait(&k_full[n_qk % KS], (n_qk / KS) & 1) &&
+                         mbar_try_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
+                    act = 2;
+                if (act) {
+                    idle_since = 0;
+                } else {
+                    const uint64_t now = global_timer_ns();
+                    if (!idle_since) idle_since = now;
+                    if (*abort_flag) {
+                        act = -1;
+                    } else if (now - idle_since > kWaitTimeoutNs) {
+                        raise_flag(p.status, PKV_DEVERR_TIMEOUT);
+                        *abort_flag = 1;
+                        act = -1;
+                    }
+                }
+            }
+            act = __shfl_sync(0xffffffffu, act, 0);
+            if (act < 0) {
+                ok = false;
+                break;
+            }
+            if (act == 1) {
+                if (lane == 0) {
+                    const uint32_t t = n_pv;
+                    const int b = t & 1;
                     tc::fence_after_sync();
-                    const unsigned char *stage = sm + (t % 3) * L::kStageBytes;
-                    const uint32_t v_addr = smem_base + static_cast<uint32_t>(stage - sm) + L::kKVBytes;
+                    const uint32_t v_addr = smem_base + L::kOffV + (t % VS) * L::kKVBytes;
                     const uint32_t p_addr = smem_base + L::kOffP + b * L::kPanelBytes;
 #pragma unroll
                     for (int k = 0; k < TILE / 16; ++k) {
@@ -267,51 +372,35 @@ __global__ void __launch_bounds__(192, 1)
                         tc::mma_f16_ss(tmem + 32 + 16 * b, a, bd, idesc_pv, k > 0);
                     }
                     tc::mma_commit(&o_full[b]);
-                    tc::mma_commit(&empty[t % 3]);
+                    tc::mma_commit(&v_empty[t % VS]);
                 }
-            }
-            return __shfl_sync(0xffffffffu, go, 0) != 0;
-        };
-
-        for (int64_t r = blockIdx.x; ok; r += gridDim.x) {
-            int y, part;
-            if (!walk.seek(p, r, y, part)) break;
-            const int tok0 = part * p.partition_size;
-            const int ntok = max(0, min(walk.len, tok0 + p.partition_size) - tok0);
-            if (ntok == 0) continue;
-            const int kvh = y / p.subgroups;
-            const int hq0 = kvh * p.group + (y % p.subgroups) * GH;
-            const int qb = items_with_tiles & 1;
-            ++items_with_tiles;
-            for (int t0 = 0; t0 < ntok; t0 += TILE, ++g) {
-                const int b = g & 1;
-                int go = 1;
-                if (lane == 0) {
-                    go = tc_wait(&full[g % 3], (g / 3) & 1, abort_flag, p.status) &&
-                         tc_wait(&s_empty[b], ((g >> 1) & 1) ^ 1, abort_flag, p.status);
-                }
-                if (!__shfl_sync(0xffffffffu, go, 0)) {
-                    ok = false;
-                    break;
-                }
+                ++n_pv;
+            } else if (act == 2) {
+                const int qb = (items - (t0 == 0 ? 0 : 1)) & 1;  // panel of this tile's item
                 if (t0 == 0) {
-                    // this item's queries -> Q panel qb (K-major, 128-byte swizzle)
-                    const T *qsrc = static_cast<const T *>(p.q) +
-                                    (static_cast<int64_t>(walk.seq) * p.num_q_heads + hq0) * D;
+                    // this item's queries -> Q panel qb (K-major, 128-byte swizzle).  The
+                    // QK^T that last read this panel (two items back) has completed: the
+                    // s_empty wait above showed S of tile n_qk-2 was consumed.
                     unsigned char *panel = sm + L::kOffQ + qb * L::kPanelBytes;
-                    for (int i = lane; i < GH * 16; i += 32) {
-                        const int row = i >> 4, c8 = i & 15;
-                        const uint4 v = *reinterpret_cast<const uint4 *>(qsrc + row * D + c8 * 8);
-                        const uint32_t off = ((c8 >> 3) * 2 + (row >> 3)) * 1024 + (row & 7) * 128 +
-                                             (((c8 & 7) ^ (row & 7)) << 4);
-                        *reinterpret_cast<uint4 *>(panel + off) = v;
+#pragma unroll
+                    for (int c = 0; c < QCHUNKS; ++c) {
+                        const int i = lane + c * 32;
+                        if (i < GH * 16) {
+                            const int row = i >> 4, c8 = i & 15;
+                            const uint32_t off = ((c8 >> 3) * 2 + (row >> 3)) * 1024 + (row & 7) * 128 +
+                                                 (((c8 & 7) ^ (row & 7)) << 4);
+                            *reinterpret_cast<uint4 *>(panel + off) = qreg[c];
+                        }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
+                    ++items;
                 }
                 if (lane == 0) {
+                    const uint32_t g = n_qk;
+                    const int b = g & 1;
                     tc::fence_after_sync();
-                    const uint32_t k_addr = smem_base + (g % 3) * L::kStageBytes;
+                    const uint32_t k_addr = smem_base + L::kOffK + (g % KS) * L::kKVBytes;
                     const uint32_t q_addr = smem_base + L::kOffQ + qb * L::kPanelBytes;
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
@@ -322,16 +411,15 @@ __global__ void __launch_bounds__(192, 1)
                         tc::mma_f16_ss(tmem + 16 * b, a, bd, idesc_qk, k > 0);
                     }
                     tc::mma_commit(&s_full[b]);
+                    tc::mma_commit(&k_empty[g % KS]);
                 }
                 __syncwarp();
-                if (have_prev && !issue_pv(g - 1)) {
-                    ok = false;
-                    break;
-                }
-                have_prev = true;
+                if (t0 == 0) load_next_q();
+                ++n_qk;
+                t0 += TILE;
+                if (t0 >= ntok) have_tile = next_item();
             }
         }
-        if (ok && have_prev) issue_pv(g - 1);
         if (lane == 0) {
             // all MMAs of this CTA complete before TMEM is released
             tc::mma_commit(drain_bar);
@@ -351,8 +439,8 @@ __global__ void __launch_bounds__(192, 1)
 
         for (int64_t r = blockIdx.x; ok; r += gridDim.x) {
             int y, part;
-            if (!walk.seek(p, r, y, part)) break;
-            if (!flagged_len && warp == 2 && lane == 0) {
+            if (!walk.seek(p, s_len, r, y, part)) break;
+            if (!staged && !flagged_len && warp == 2 && lane == 0) {
                 const int raw = p.context_lens[walk.seq];
                 if (raw < 0 || raw > p.len_cap) {
                     raise_flag(p.status, PKV_DEVERR_CONTEXT_LEN);
@@ -441,13 +529,13 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 if (tile_ntok < TILE) {
                     // rows past the context: zero their V so 0 * stale never reaches the MMA
-                    const int s = g % 3;
-                    if (!tc_wait(&full[s], (g / 3) & 1, abort_flag, p.status)) {
+                    const int s = g % VS;
+                    if (!tc_wait(&v_full[s], (g / VS) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     if (!valid) {
-                        unsigned char *vrow = sm + s * L::kStageBytes + L::kKVBytes + row * 128;
+                        unsigned char *vrow = sm + L::kOffV + s * L::kKVBytes + row * 128;
 #pragma unroll
                         for (int c = 0; c < 2; ++c)
 #pragma unroll
