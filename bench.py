@@ -255,6 +255,98 @@ def run_reference(args):
 
 
 # --------------------------------------------------------------------------- our arm
+def measure_workload(pkv, name, dev, steps, peak, partition=None):
+    """Device-timed decode step of one named workload (eager launches), the
+    decode call's share, and the per-step latency when the step is replayed
+    from a CUDA graph (no host launch cost; what a serving loop that captures
+    its decode step sees)."""
+    import torch
+    from paged_kv_cache_155_gb300 import workloads
+    wl = _make_workload(name, str(dev), 1234)
+    k_cache, v_cache = pkv.split_pool(wl.kv)
+    maxl = int(wl.context_lens.max())
+    part = workloads.DEFAULT_PARTITION[name] if partition is None else partition
+    slots = pkv.slot_mapping(wl.block_tables.cpu(), wl.new_positions.cpu(), wl.block_size).to(dev)
+    out = torch.empty_like(wl.q)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
+        pkv.paged_attention_decode(wl.q, k_cache, v_cache, wl.block_tables, wl.context_lens,
+                                   wl.scale, out, max_context_len=maxl, partition_size=part)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(steps):
+        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
+        ev[k][0].record(stream)
+        pkv.paged_attention_decode(wl.q, k_cache, v_cache, wl.block_tables, wl.context_lens,
+                                   wl.scale, out, max_context_len=maxl, partition_size=part)
+        ev[k][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms_step = t0.elapsed_time(t1) / steps
+    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    nbytes = _algorithmic_bytes(wl)
+    # CUDA-graph replay of `reps` steps
+    reps = 50
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            step()
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(reps):
+            step()
+    graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(4):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = g0.elapsed_time(g1) / (4 * reps)
+    flags, names = pkv.get_device_error(dev)
+    if flags:
+        raise RuntimeError(f"device flags on {name}: {names}")
+    result = {"tokens_per_s": wl.num_seqs / (ms_step / 1e3), "ms_per_step": ms_step,
+              "decode_ms": dec_ms, "kv_read_gbps": nbytes / (dec_ms / 1e3) / 1e9,
+              "hbm_frac_of_measured": nbytes / (dec_ms / 1e3) / 1e9 / peak,
+              "graph_us_per_step": graph_ms * 1e3,
+              "graph_tokens_per_s": wl.num_seqs / (graph_ms / 1e3),
+              "algorithmic_bytes": nbytes, "num_seqs": wl.num_seqs,
+              "partition_size": part}
+    if name == "prefix":
+        result["note"] = ("kv_read_gbps counts every sequence's prefix reads (logical bytes); "
+                          "the 64 shared prefix blocks are read from L2 after the first touch")
+        # copy-on-write of the last shared prefix block into one private block per sequence
+        pairs = wl.cow_pairs
+        blk_bytes = 2 * wl.num_kv_heads * wl.block_size * wl.head_dim * 2
+        for _ in range(3):
+            pkv.copy_blocks(k_cache, v_cache, pairs)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(50):
+            pkv.copy_blocks(k_cache, v_cache, pairs)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        cms = c0.elapsed_time(c1) / 50
+        moved = 2 * pairs.shape[0] * blk_bytes  # read + write
+        result["copy_blocks"] = {"pairs": int(pairs.shape[0]), "us": cms * 1e3,
+                                 "gbps_read_plus_write": moved / (cms / 1e3) / 1e9}
+    del wl, k_cache, v_cache, out, graph
+    torch.cuda.empty_cache()
+    return result
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -394,6 +486,13 @@ def run_ours(args):
             "roofline": roof}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
+    if world == 1 and not args.no_other_workloads:
+        others = {}
+        for name in ("tiny", "mha7b", "gqa7b", "prefix", "long70b"):
+            if name == args.workload:
+                continue
+            others[name] = measure_workload(pkv, name, dev, 300, peak)
+        line["other_workloads"] = others
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -415,6 +514,8 @@ def main(argv=None):
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="override the workload's batch (profiling on a smaller case)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the device-timed lines of the other named workloads")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
