@@ -48,6 +48,23 @@ def _dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value, device, world):
+    """The largest of every rank's value (the slowest rank's time), or value at N=1."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(world, num_seqs, ms_per_step):
+    """Decode tokens/s of all ranks: each rank decodes one token for each of its own
+    num_seqs sequences per step (weak scaling), timed by the slowest rank."""
+    return world * num_seqs / (ms_per_step / 1000.0)
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -414,12 +431,9 @@ def run_ours(args):
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
     dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev, world)
     ms_step = ms_total / args.steps
-    value = world * wl.num_seqs / (ms_step / 1000.0)
+    value = whole_job_tokens_per_s(world, wl.num_seqs, ms_step)
     flags, names = pkv.get_device_error(dev)
     if flags:
         raise RuntimeError(f"device flags during the timed region: {names}")
@@ -457,11 +471,8 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * wl.num_seqs / (e2e_ms / 1000.0)
+    e2e_ms = max_over_ranks(e2e_ms, dev, world)
+    e2e_value = whole_job_tokens_per_s(world, wl.num_seqs, e2e_ms)
 
     # ---- roofline of the decode kernel(s)
     peak, peak_kind = _peaks()
