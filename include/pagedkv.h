@@ -60,8 +60,9 @@ typedef enum pkv_status {
     PKV_ERR_UNSUPPORTED = 2,   /* valid but not built (dtype, head_dim, bs)    */
     PKV_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed         */
     PKV_ERR_DEVICE = 4,        /* pkv_get_device_error found flags raised      */
-    PKV_ERR_SCRATCH_LIMIT = 5  /* split-context scratch needed exceeds
+    PKV_ERR_SCRATCH_LIMIT = 5, /* split-context scratch needed exceeds
                                   PKV_STATIC_SCRATCH_BYTES (static-scratch decode) */
+    PKV_ERR_OUT_OF_BLOCKS = 6  /* block manager: the free pool cannot cover the request */
 } pkv_status;
 
 typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
@@ -230,6 +231,67 @@ PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_hea
  * timeout_ns must be in (0, 10^10].
  */
 PKV_API pkv_status pkv_debug_wait_timeout(uint64_t timeout_ns, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Host block manager (no GPU involved): the bookkeeping that produces the
+ * inputs of the calls above -- block tables, context lengths, slot mappings
+ * and copy-on-write pairs.  P1 §5.2-5.3: a free pool of physical blocks; when
+ * token t is appended the sequence needs ceil((t+1)/block_size) blocks, a new
+ * block comes from the pool when its table is short, and the token's slot is
+ * offset t % block_size of the last block.  P1 §6.2 / §8.2-8.3: finished
+ * sequences return their blocks; shared blocks carry a reference count and are
+ * freed at zero.  P3 §2.3 / §5.5: a sequence about to write into a block that
+ * another sequence references first gets a private copy (a copy-on-write pair
+ * for pkv_copy_blocks).  Blocks are handed out 0, 1, 2, ... from a fresh pool
+ * and reused last-freed-first.  One manager per thread (not thread-safe).
+ * ------------------------------------------------------------------------ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* NULL on bad sizes (num_blocks in [1, 2^31), block_size >= 1, max_blocks_per_seq >= 1). */
+PKV_API pkv_block_manager *pkv_bm_create(int64_t num_blocks, int block_size,
+                                         int max_blocks_per_seq);
+PKV_API void pkv_bm_destroy(pkv_block_manager *bm);
+PKV_API int64_t pkv_bm_num_free(const pkv_block_manager *bm);
+/* Reference count of a physical block (0 = free); -1 for a bad block id. */
+PKV_API int32_t pkv_bm_refcount(const pkv_block_manager *bm, int64_t block);
+/* New empty sequence; PKV_ERR_INVALID_ARG if the id exists. */
+PKV_API pkv_status pkv_bm_add_sequence(pkv_block_manager *bm, int64_t seq_id);
+/* New sequence child_id sharing every block of parent_id (reference counts +1),
+ * e.g. a beam-search branch. */
+PKV_API pkv_status pkv_bm_fork(pkv_block_manager *bm, int64_t parent_id, int64_t child_id);
+/* Prefix caching: the empty sequence dst_id starts with src_id's first
+ * num_tokens tokens (a multiple of block_size) by sharing their blocks. */
+PKV_API pkv_status pkv_bm_share_prefix(pkv_block_manager *bm, int64_t src_id, int64_t dst_id,
+                                       int64_t num_tokens);
+/* Append one token: *slot receives its slot.  If the sequence's last block was
+ * shared, it is replaced by a fresh copy and (*cow_src, *cow_dst) name the copy
+ * to perform before the cache write; otherwise both are -1.
+ * PKV_ERR_OUT_OF_BLOCKS when a block is needed and the pool is empty (nothing
+ * changes); PKV_ERR_INVALID_ARG for an unknown id or a full table. */
+PKV_API pkv_status pkv_bm_append_token(pkv_block_manager *bm, int64_t seq_id, int64_t *slot,
+                                       int64_t *cow_src, int64_t *cow_dst);
+/* Drop a sequence; its blocks' reference counts fall and blocks at zero return
+ * to the pool. */
+PKV_API pkv_status pkv_bm_free_sequence(pkv_block_manager *bm, int64_t seq_id);
+/* Tokens held by a sequence (-1 if unknown). */
+PKV_API int64_t pkv_bm_seq_len(const pkv_block_manager *bm, int64_t seq_id);
+/* Copy a sequence's block table (host int32) into out[capacity]; *num_entries
+ * gets its length (also when capacity is too small, which returns
+ * PKV_ERR_INVALID_ARG). */
+PKV_API pkv_status pkv_bm_block_table(const pkv_block_manager *bm, int64_t seq_id, int32_t *out,
+                                      int capacity, int *num_entries);
+/* One decode step for a batch of distinct sequences, all host buffers: appends
+ * one token to each and writes slot_mapping[num_seqs], block_tables
+ * [num_seqs][max_blocks_per_seq] (unused entries 0), context_lens[num_seqs]
+ * (the new token included) and up to num_seqs copy-on-write pairs
+ * cow_pairs[*num_cow_pairs][2] -- exactly the inputs of pkv_copy_blocks,
+ * pkv_reshape_and_cache and pkv_paged_attention_decode for this step, run in
+ * that order.  The pool is checked for the whole step first: on
+ * PKV_ERR_OUT_OF_BLOCKS nothing changes. */
+PKV_API pkv_status pkv_bm_decode_step(pkv_block_manager *bm, const int64_t *seq_ids,
+                                      int num_seqs, int64_t *slot_mapping,
+                                      int32_t *block_tables, int32_t *context_lens,
+                                      int64_t *cow_pairs, int64_t *num_cow_pairs);
 
 #ifdef __cplusplus
 }

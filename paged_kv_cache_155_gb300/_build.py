@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libpagedkv.so")
 
 SOURCES = ["api.cu", "cache_ops.cu", "decode.cu", "decode_f16.cu", "decode_bf16.cu",
-           "decode_noalloc.cu"]
+           "decode_noalloc.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-v"]
@@ -54,8 +54,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        log = os.path.join(BUILD_DIR, src.replace(".cu", ".ptxas.log"))
+        stem = os.path.splitext(src)[0]
+        obj = os.path.join(BUILD_DIR, stem + ".o")
+        log = os.path.join(BUILD_DIR, stem + ".ptxas.log")
         cmd = [nvcc, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         with open(log, "w") as f:

@@ -37,10 +37,22 @@ SIGNATURES = {
     "pkv_paged_attention_decode_static_scratch": (I32, [P, P, P, I64, I64, P, I32, P, I32, I32,
                                                         I32, I32, I32, I32, ctypes.c_float, P,
                                                         I32, I32, P]),
+    "pkv_bm_create": (P, [I64, I32, I32]),
+    "pkv_bm_destroy": (None, [P]),
+    "pkv_bm_num_free": (I64, [P]),
+    "pkv_bm_refcount": (ctypes.c_int32, [P, I64]),
+    "pkv_bm_add_sequence": (I32, [P, I64]),
+    "pkv_bm_fork": (I32, [P, I64, I64]),
+    "pkv_bm_share_prefix": (I32, [P, I64, I64, I64]),
+    "pkv_bm_append_token": (I32, [P, I64, P, P, P]),
+    "pkv_bm_free_sequence": (I32, [P, I64]),
+    "pkv_bm_seq_len": (I64, [P, I64]),
+    "pkv_bm_block_table": (I32, [P, I64, P, I32, ctypes.POINTER(I32)]),
+    "pkv_bm_decode_step": (I32, [P, P, I32, P, P, P, P, P]),
 }
 
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
-          4: "PKV_ERR_DEVICE", 5: "PKV_ERR_SCRATCH_LIMIT"}
+          4: "PKV_ERR_DEVICE", 5: "PKV_ERR_SCRATCH_LIMIT", 6: "PKV_ERR_OUT_OF_BLOCKS"}
 DEVERR = {0x1: "slot", 0x2: "block_table", 0x4: "context_len", 0x8: "copy_pair", 0x10: "timeout"}
 
 

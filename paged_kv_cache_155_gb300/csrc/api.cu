@@ -106,6 +106,7 @@ PKV_API const char *pkv_status_string(pkv_status status) {
         case PKV_ERR_DEVICE: return "a kernel raised a device status flag";
         case PKV_ERR_SCRATCH_LIMIT:
             return "split-context scratch needed exceeds the library's static scratch array";
+        case PKV_ERR_OUT_OF_BLOCKS: return "out of KV cache blocks";
     }
     return "unknown status";
 }
