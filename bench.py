@@ -359,6 +359,47 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
         moved = 2 * pairs.shape[0] * blk_bytes  # read + write
         result["copy_blocks"] = {"pairs": int(pairs.shape[0]), "us": cms * 1e3,
                                  "gbps_read_plus_write": moved / (cms / 1e3) / 1e9}
+        # the same step with the shared-prefix (cascade) decode: the 2048-token prefix is
+        # attended by all query rows together and read once per 128 rows
+        pre_tokens = wl.shared_prefix_blocks * wl.block_size
+        pre_table = wl.block_tables[0, :wl.shared_prefix_blocks].contiguous()
+
+        def cascade_step():
+            pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
+            pkv.paged_attention_decode_shared_prefix(
+                wl.q, k_cache, v_cache, pre_table, pre_tokens, wl.block_tables, wl.context_lens,
+                wl.scale, out, max_context_len=maxl)
+
+        for _ in range(5):
+            cascade_step()
+        torch.cuda.synchronize()
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for k in range(steps):
+            pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
+            ev2[k][0].record(stream)
+            pkv.paged_attention_decode_shared_prefix(
+                wl.q, k_cache, v_cache, pre_table, pre_tokens, wl.block_tables, wl.context_lens,
+                wl.scale, out, max_context_len=maxl)
+            ev2[k][1].record(stream)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        flags, names = pkv.get_device_error(dev)
+        if flags:
+            raise RuntimeError(f"device flags on the shared-prefix decode: {names}")
+        c_step = s0.elapsed_time(s1) / steps
+        c_dec = statistics.mean(a.elapsed_time(b) for a, b in ev2)
+        row_bytes = 2 * wl.num_kv_heads * wl.head_dim * 2          # K+V of one token, all KV heads
+        suffix_tokens = sum(int(x) - pre_tokens for x in wl.context_lens.cpu().tolist())
+        unique = (pre_tokens + suffix_tokens) * row_bytes + 2 * wl.num_seqs * wl.num_q_heads * wl.head_dim * 2
+        result["shared_prefix_decode"] = {
+            "tokens_per_s": wl.num_seqs / (c_step / 1e3), "ms_per_step": c_step,
+            "decode_ms": c_dec, "speedup_vs_plain_decode": dec_ms / c_dec,
+            "unique_bytes": unique, "unique_gbps": unique / (c_dec / 1e3) / 1e9,
+            "unique_frac_of_measured": unique / (c_dec / 1e3) / 1e9 / peak,
+            "logical_gbps": nbytes / (c_dec / 1e3) / 1e9}
     del wl, k_cache, v_cache, out, graph
     torch.cuda.empty_cache()
     return result

@@ -158,6 +158,43 @@ PKV_API pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blo
                                    int block_size, const int64_t *src_dst_pairs,
                                    int64_t num_pairs, pkv_dtype dtype, void *stream);
 
+/*
+ * pkv_shared_prefix_workspace_bytes -- workspace of
+ * pkv_paged_attention_decode_shared_prefix for these arguments on the current
+ * device ((size_t)-1 if they are out of contract).
+ */
+PKV_API size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                                 int head_dim, int block_size, int prefix_len,
+                                                 int max_context_len, int partition_size);
+
+/*
+ * pkv_paged_attention_decode_shared_prefix -- the same result as
+ * pkv_paged_attention_decode for a batch whose sequences all start with the
+ * same prefix_len tokens held in the blocks prefix_block_table[0 ..
+ * prefix_len/block_size) (prefix caching: P1 §8.2, P3 §2.3 / §3), computed as
+ * a cascade: (1) all num_seqs * G query rows of each KV head attend to the
+ * prefix together as dense tensor-core tiles, so each prefix block is read once
+ * per 128 query rows instead of once per sequence; (2) each sequence attends
+ * to its own tokens [prefix_len, context_len); (3) a log-sum-exp merge.
+ *
+ *   prefix_block_table  [prefix_len / block_size] int32, device.
+ *   prefix_len          > 0, a multiple of block_size, <= max_context_len.
+ *                       Every context_lens[i] must be >= prefix_len (a shorter
+ *                       one raises PKV_DEVERR_CONTEXT_LEN), and every
+ *                       block_tables[i] must start with the prefix's blocks
+ *                       (or blocks holding the same data).
+ *   workspace           >= pkv_shared_prefix_workspace_bytes(...); required.
+ * Other arguments as pkv_paged_attention_decode.  head_dim 128 only (else
+ * PKV_ERR_UNSUPPORTED).
+ */
+PKV_API pkv_status pkv_paged_attention_decode_shared_prefix(
+    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+    int64_t block_stride_elems, const int32_t *prefix_block_table, int prefix_len,
+    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+    int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, float scale, void *out, void *workspace, size_t workspace_bytes,
+    int partition_size, pkv_dtype dtype, void *stream);
+
 /* Size of the library's built-in decode scratch array (per device). */
 #define PKV_STATIC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
 

@@ -10,10 +10,12 @@ if it is missing.  There is no CPU implementation in this package.
 """
 from .ops import (F16, BF16, copy_blocks, debug_wait_timeout, decode_plan,  # noqa: F401
                   decode_workspace_bytes, get_device_error, launch_count,
-                  paged_attention_decode, reshape_and_cache, split_pool)
+                  paged_attention_decode, paged_attention_decode_shared_prefix,
+                  reshape_and_cache, shared_prefix_workspace_bytes, split_pool)
 from .block_table import slot_mapping  # noqa: F401
 from ._lib import PagedKVError  # noqa: F401
 
-__all__ = ["reshape_and_cache", "paged_attention_decode", "copy_blocks", "split_pool",
+__all__ = ["reshape_and_cache", "paged_attention_decode", "paged_attention_decode_shared_prefix",
+           "shared_prefix_workspace_bytes", "copy_blocks", "split_pool",
            "decode_workspace_bytes", "decode_plan", "get_device_error", "launch_count",
            "debug_wait_timeout", "slot_mapping", "PagedKVError"]

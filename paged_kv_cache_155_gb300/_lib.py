@@ -37,6 +37,10 @@ SIGNATURES = {
     "pkv_paged_attention_decode_static_scratch": (I32, [P, P, P, I64, I64, P, I32, P, I32, I32,
                                                         I32, I32, I32, I32, ctypes.c_float, P,
                                                         I32, I32, P]),
+    "pkv_shared_prefix_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32, I32]),
+    "pkv_paged_attention_decode_shared_prefix": (I32, [P, P, P, I64, I64, P, I32, P, I32, P, I32,
+                                                       I32, I32, I32, I32, I32, ctypes.c_float,
+                                                       P, P, SZ, I32, I32, P]),
     "pkv_bm_create": (P, [I64, I32, I32]),
     "pkv_bm_destroy": (None, [P]),
     "pkv_bm_num_free": (I64, [P]),

@@ -12,10 +12,17 @@ constexpr int kTargetWaves = 8;        // CTA waves the automatic split aims for
 constexpr int kMinAutoPartition = 256; // tokens: below this the per-CTA set-up dominates
 constexpr int kTcItemsPerSm = 24;      // tensor-core path: work items per persistent CTA
 
-// head_dim 128 with 4, 8 or 16 query heads per KV head: the group turns
-// QK^T and PV into dense tiles and runs on the tensor cores.
-bool use_tensor_cores(int head_dim, int group) {
-    return head_dim == 128 && (group == 4 || group == 8 || group == 16);
+constexpr int kTcMinContext = 2048;    // tensor-core path from this longest context on
+
+// head_dim 128 with 4, 8 or 16 query heads per KV head: the group turns QK^T
+// and PV into dense tiles and runs on the tensor cores -- when contexts are
+// long.  Measured on GB300 (32 q / 8 kv heads, block 16): for contexts of at
+// most ~1K tokens the non-persistent CUDA-core kernel is faster (each short
+// work item exposes the copy latency of the persistent pipeline), around 1-2K
+// the two tie, from 2K on the tensor-core kernel is faster.
+bool use_tensor_cores(int head_dim, int group, int longest_span) {
+    return head_dim == 128 && (group == 4 || group == 8 || group == 16) &&
+           longest_span >= kTcMinContext;
 }
 
 int heads_per_block_for(int group) {
@@ -86,7 +93,7 @@ PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_hea
     const int max_partition = pkv::DecodeGeom<128, 16>::kMaxTableEntries * block_size;
     if (partition_size > max_partition) return PKV_ERR_INVALID_ARG;
     const int group = num_q_heads / num_kv_heads;
-    const bool tc = use_tensor_cores(head_dim, group);
+    const bool tc = use_tensor_cores(head_dim, group, max_context_len);
     const int gh = tc ? group : heads_per_block_for(group);
     const int64_t grid_y = static_cast<int64_t>(num_kv_heads) * (group / gh);
     if (grid_y > 65535 || num_seqs > 65535) return PKV_ERR_INVALID_ARG;
@@ -177,7 +184,7 @@ PKV_API pkv_status pkv_paged_attention_decode(
     if (!status) return PKV_ERR_CUDA;
 
     const int group = num_q_heads / num_kv_heads;
-    const bool tc = use_tensor_cores(head_dim, group);
+    const bool tc = use_tensor_cores(head_dim, group, max_context_len);
     if (tc && num_blocks > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
     pkv::DecodeParams p{};
     p.q = q;
@@ -226,6 +233,190 @@ PKV_API pkv_status pkv_paged_attention_decode(
     return dtype == PKV_F16
                ? pkv::launch_decode_f16(p, head_dim, block_size, gh, grid, merge_rows, s)
                : pkv::launch_decode_bf16(p, head_dim, block_size, gh, grid, merge_rows, s);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Shared-prefix (cascade) decode.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct CascadePlan {
+    int rows = 0;          // num_seqs * group
+    int row_tiles = 0;     // of 128 query rows
+    int splits = 0;        // prefix splits (workspace slots 0 .. splits-1)
+    int split_tokens = 0;  // multiple of 128
+    int suffix_part = 0;   // suffix partition size
+    int suffix_parts = 0;  // suffix partitions of the longest sequence
+    int gh = 0;            // suffix kernel's heads per block
+    bool suffix_tc = false;
+};
+
+pkv_status plan_cascade(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                        int block_size, int prefix_len, int max_context_len, int partition_size,
+                        int sm_count, CascadePlan *cp) {
+    if (head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
+        prefix_len <= 0 || prefix_len % block_size || prefix_len > max_context_len ||
+        sm_count <= 0)
+        return PKV_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    cp->rows = num_seqs * group;
+    cp->row_tiles = (cp->rows + 127) / 128;
+    if (cp->row_tiles > 0x7fffffff / 2 || num_kv_heads > 65535) return PKV_ERR_INVALID_ARG;
+    // enough prefix splits that the prefix kernel covers the SMs, whole 128-token tiles each
+    const int tiles = (prefix_len + 127) / 128;
+    const int64_t units = static_cast<int64_t>(cp->row_tiles) * num_kv_heads;
+    int splits = static_cast<int>(std::min<int64_t>(tiles, std::max<int64_t>(1, (sm_count + units - 1) / units)));
+    const int tiles_per_split = (tiles + splits - 1) / splits;
+    cp->split_tokens = tiles_per_split * 128;
+    cp->splits = (prefix_len + cp->split_tokens - 1) / cp->split_tokens;
+    if (cp->splits > 65535) return PKV_ERR_INVALID_ARG;
+    // the suffix: the decode plan over the longest suffix
+    const int span = max_context_len - prefix_len;
+    int part = 0, nparts = 0, gh = 0, merge = 0;
+    const pkv_status st = pkv_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                          std::max(span, 1), partition_size, sm_count, &part,
+                                          &nparts, &gh, &merge);
+    if (st != PKV_OK) return st;
+    cp->suffix_part = part;
+    cp->suffix_parts = nparts;
+    cp->gh = gh;
+    cp->suffix_tc = use_tensor_cores(head_dim, group, span);
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+PKV_API size_t pkv_shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                                 int head_dim, int block_size, int prefix_len,
+                                                 int max_context_len, int partition_size) {
+    const int sm = pkv::current_sm_count();
+    if (sm <= 0) return static_cast<size_t>(-1);
+    CascadePlan cp;
+    if (plan_cascade(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, prefix_len,
+                     max_context_len, partition_size, sm, &cp) != PKV_OK)
+        return static_cast<size_t>(-1);
+    const size_t slots = static_cast<size_t>(cp.splits + cp.suffix_parts);
+    return static_cast<size_t>(num_seqs) * num_q_heads * slots * (head_dim + 2) * sizeof(float);
+}
+
+PKV_API pkv_status pkv_paged_attention_decode_shared_prefix(
+    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+    int64_t block_stride_elems, const int32_t *prefix_block_table, int prefix_len,
+    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+    int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, float scale, void *out, void *workspace, size_t workspace_bytes,
+    int partition_size, pkv_dtype dtype, void *stream) {
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 128) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs <= 0 || num_blocks <= 0 || num_blocks > 0x7fffffffLL || max_blocks_per_seq <= 0 ||
+        max_context_len < 0 ||
+        static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size ||
+        !std::isfinite(scale) || partition_size < 0 || partition_size % block_size)
+        return PKV_ERR_INVALID_ARG;
+    const int64_t half_elems = static_cast<int64_t>(num_kv_heads) * block_size * head_dim;
+    if (num_kv_heads <= 0 || block_stride_elems < half_elems || block_stride_elems % 8)
+        return PKV_ERR_INVALID_ARG;
+    if (!q || !out || !k_cache || !v_cache || !block_tables || !context_lens || !prefix_block_table ||
+        !workspace || !pkv::aligned16(q) || !pkv::aligned16(out) || !pkv::aligned16(k_cache) ||
+        !pkv::aligned16(v_cache) || !pkv::aligned16(workspace))
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads <= 0 || num_q_heads % num_kv_heads || prefix_len <= 0 ||
+        prefix_len % block_size || prefix_len > max_context_len)
+        return PKV_ERR_INVALID_ARG;
+    const int sm = pkv::current_sm_count();
+    if (sm <= 0) return PKV_ERR_CUDA;
+    CascadePlan cp;
+    pkv_status st = plan_cascade(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                 prefix_len, max_context_len, partition_size, sm, &cp);
+    if (st != PKV_OK) return st;
+    const int slots = cp.splits + cp.suffix_parts;
+    const size_t need = static_cast<size_t>(num_seqs) * num_q_heads * slots * (head_dim + 2) * sizeof(float);
+    if (workspace_bytes < need) return PKV_ERR_INVALID_ARG;
+    unsigned int *status = pkv::status_word_ptr();
+    if (!status) return PKV_ERR_CUDA;
+    CUtensorMap tk, tv;
+    if (!encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads, block_size, dtype) ||
+        !encode_half_map(&tv, v_cache, num_blocks, block_stride_elems, num_kv_heads, block_size, dtype))
+        return PKV_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int group = num_q_heads / num_kv_heads;
+    const size_t rows_ws = static_cast<size_t>(num_seqs) * num_q_heads * slots;
+    float *ws_o = static_cast<float *>(workspace);
+    float *ws_m = ws_o + rows_ws * head_dim;
+    float *ws_l = ws_m + rows_ws;
+
+    // 1. every query row of a KV head over the shared prefix (dense, tensor cores)
+    pkv::PrefixParams pp{};
+    pp.q = q;
+    pp.ws_o = ws_o;
+    pp.ws_m = ws_m;
+    pp.ws_l = ws_l;
+    pp.prefix_table = prefix_block_table;
+    pp.context_lens = context_lens;
+    pp.status = status;
+    pp.num_blocks = num_blocks;
+    pp.num_seqs = num_seqs;
+    pp.num_q_heads = num_q_heads;
+    pp.group = group;
+    pp.rows = cp.rows;
+    pp.prefix_len = prefix_len;
+    pp.split_tokens = cp.split_tokens;
+    pp.num_partitions = slots;
+    pp.scale_log2 = scale * 1.4426950408889634f;
+    const dim3 pgrid(static_cast<unsigned>(cp.row_tiles), static_cast<unsigned>(num_kv_heads),
+                     static_cast<unsigned>(cp.splits));
+    st = dtype == PKV_F16 ? pkv::launch_prefix_tc_f16(pp, tk, tv, block_size, pgrid, s)
+                          : pkv::launch_prefix_tc_bf16(pp, tk, tv, block_size, pgrid, s);
+    if (st != PKV_OK) return st;
+
+    // 2. each sequence's own tokens after the prefix, into the following slots, then
+    // 3. the log-sum-exp merge of all slots
+    pkv::DecodeParams p{};
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.out = out;
+    p.ws_o = ws_o;
+    p.ws_m = ws_m;
+    p.ws_l = ws_l;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.status = status;
+    p.num_blocks = num_blocks;
+    p.block_stride = block_stride_elems;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.len_cap = max_context_len;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.group = group;
+    p.subgroups = group / cp.gh;
+    p.items_y = num_kv_heads * p.subgroups;
+    p.partition_size = cp.suffix_part;
+    p.num_partitions = slots;
+    p.scale_log2 = pp.scale_log2;
+    p.tok_begin = prefix_len;
+    p.slot_base = cp.splits;
+    p.always_partial = 1;
+    const int merge_rows = num_seqs * num_q_heads;
+    if (cp.suffix_tc) {
+        const int64_t items = static_cast<int64_t>(num_seqs) * p.items_y * cp.suffix_parts;
+        const int grid = static_cast<int>(std::min<int64_t>(sm, items));
+        return dtype == PKV_F16
+                   ? pkv::launch_decode_tc_f16(p, tk, tv, block_size, cp.gh, grid, merge_rows, s)
+                   : pkv::launch_decode_tc_bf16(p, tk, tv, block_size, cp.gh, grid, merge_rows, s);
+    }
+    const dim3 grid(static_cast<unsigned>(cp.suffix_parts), static_cast<unsigned>(p.items_y),
+                    static_cast<unsigned>(num_seqs));
+    return dtype == PKV_F16
+               ? pkv::launch_decode_f16(p, head_dim, block_size, cp.gh, grid, merge_rows, s)
+               : pkv::launch_decode_bf16(p, head_dim, block_size, cp.gh, grid, merge_rows, s);
 }
 
 }  // extern "C"

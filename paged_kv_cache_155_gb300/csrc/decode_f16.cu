@@ -10,4 +10,8 @@ pkv_status launch_decode_tc_f16(const DecodeParams &p, const CUtensorMap &tk, co
                                 int block_size, int gh, int grid, int merge_rows, cudaStream_t s) {
     return launch_decode_tc_typed<__half>(p, tk, tv, block_size, gh, grid, merge_rows, s);
 }
+pkv_status launch_prefix_tc_f16(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                                int block_size, dim3 grid, cudaStream_t s) {
+    return launch_prefix_tc_typed<__half>(p, tk, tv, block_size, grid, s);
+}
 }  // namespace pkv

@@ -54,9 +54,24 @@ struct DecodeParams {
     int group;       // num_q_heads / num_kv_heads
     int subgroups;   // group / heads_per_block
     int partition_size;
-    int num_partitions;
-    float scale_log2;  // scale * log2(e)
+    int num_partitions;  // workspace partition slots per (sequence, query head)
+    float scale_log2;    // scale * log2(e)
+    // Token range and workspace slots of this launch: attention runs over tokens
+    // [tok_begin, context_len) split into partitions of partition_size, whose
+    // partials go to slots slot_base + partition.  always_partial keeps even a
+    // single-partition result in the workspace for a later merge.  The plain
+    // decode uses 0 / 0 / 0; the shared-prefix decode runs the suffix with
+    // tok_begin = prefix length and slot_base = number of prefix splits.
+    int tok_begin;
+    int slot_base;
+    int always_partial;
 };
+
+// Partitions of a sequence of `len` tokens in a launch (at least one, possibly empty).
+__device__ __forceinline__ int partitions_of(const DecodeParams &p, int len) {
+    const int span = len - p.tok_begin;
+    return span > 0 ? (span + p.partition_size - 1) / p.partition_size : 1;
+}
 
 // Decode-kernel geometry for one (head_dim, block_size) pair.
 template <int D, int BS>
@@ -106,9 +121,9 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
             raise_flag(p.status, PKV_DEVERR_CONTEXT_LEN);
         len = len < 0 ? 0 : p.len_cap;
     }
-    const int nparts = len > 0 ? (len + p.partition_size - 1) / p.partition_size : 1;
+    const int nparts = partitions_of(p, len);
     if (part >= nparts) return;  // uniform over the CTA
-    const int tok0 = part * p.partition_size;
+    const int tok0 = p.tok_begin + part * p.partition_size;
     const int tok1 = min(len, tok0 + p.partition_size);
     const int ntok = max(0, tok1 - tok0);
     const int nchunks = (ntok + TILE - 1) / TILE;
@@ -323,7 +338,7 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
     }
     __syncthreads();
 
-    const bool single = nparts == 1;
+    const bool single = nparts == 1 && !p.always_partial;
     for (int idx = threadIdx.x; idx < GH * D; idx += blockDim.x) {
         const int g = idx / D;
         const int j = idx - g * D;
@@ -349,7 +364,7 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
             const float r = lsum > 0.f ? osum / lsum : 0.f;
             static_cast<T *>(p.out)[row * D + j] = Elem<T>::from_f32(r);
         } else {
-            const int64_t pr = row * p.num_partitions + part;
+            const int64_t pr = row * p.num_partitions + p.slot_base + part;
             p.ws_o[pr * D + j] = osum;
             if (j == 0) {
                 p.ws_m[pr] = mmax;
@@ -372,10 +387,12 @@ __global__ void __launch_bounds__(128) paged_decode_merge_kernel(const DecodePar
     if (row >= num_rows) return;
     const int seq = row / p.num_q_heads;
     int len = p.context_lens[seq];  // clamped exactly as the main kernel does
+    if (p.tok_begin > 0 && len < p.tok_begin && lane == 0 && (row % p.num_q_heads) == 0)
+        raise_flag(p.status, PKV_DEVERR_CONTEXT_LEN);  // shorter than the shared prefix
     if (len < 0) len = 0;
     if (len > p.len_cap) len = p.len_cap;
-    const int nparts = len > 0 ? (len + p.partition_size - 1) / p.partition_size : 1;
-    if (nparts <= 1) return;
+    const int nparts = p.slot_base + partitions_of(p, len);  // slots holding partials
+    if (nparts <= 1 && !p.always_partial) return;           // written by the decode kernel
     const int64_t base = static_cast<int64_t>(row) * p.num_partitions;
     float mmax = -INFINITY;
     for (int q = 0; q < nparts; ++q) mmax = fmaxf(mmax, p.ws_m[base + q]);

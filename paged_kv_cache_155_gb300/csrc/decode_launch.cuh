@@ -8,6 +8,7 @@
 
 #include "decode_kernel.cuh"
 #include "decode_tc_kernel.cuh"
+#include "prefix_tc_kernel.cuh"
 #include "pkv_host.h"
 
 namespace pkv {
@@ -108,6 +109,34 @@ pkv_status launch_decode_tc_typed(const DecodeParams &p, const CUtensorMap &tk,
     return launch_status();
 }
 
+template <typename T, int BS>
+pkv_status launch_prefix_tc_one(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                                dim3 grid, cudaStream_t stream) {
+    static std::atomic<uint64_t> configured_devices{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    if (!bit || !(configured_devices.load(std::memory_order_acquire) & bit)) {
+        if (cudaFuncSetAttribute(paged_prefix_tc_kernel<T, BS>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PrefixLayout::kSmemBytes) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        configured_devices.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    paged_prefix_tc_kernel<T, BS><<<grid, 192, PrefixLayout::kSmemBytes, stream>>>(tk, tv, p);
+    count_launch();
+    return launch_status();
+}
+
+template <typename T>
+pkv_status launch_prefix_tc_typed(const PrefixParams &p, const CUtensorMap &tk,
+                                  const CUtensorMap &tv, int block_size, dim3 grid, cudaStream_t s) {
+    if (block_size == 8) return launch_prefix_tc_one<T, 8>(p, tk, tv, grid, s);
+    if (block_size == 16) return launch_prefix_tc_one<T, 16>(p, tk, tv, grid, s);
+    if (block_size == 32) return launch_prefix_tc_one<T, 32>(p, tk, tv, grid, s);
+    return PKV_ERR_UNSUPPORTED;
+}
+
 // Defined in decode_f16.cu / decode_bf16.cu.
 pkv_status launch_decode_f16(const DecodeParams &p, int head_dim, int block_size, int gh,
                              dim3 grid, int merge_rows, cudaStream_t s);
@@ -117,5 +146,9 @@ pkv_status launch_decode_tc_f16(const DecodeParams &p, const CUtensorMap &tk, co
                                 int block_size, int gh, int grid, int merge_rows, cudaStream_t s);
 pkv_status launch_decode_tc_bf16(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                                  int block_size, int gh, int grid, int merge_rows, cudaStream_t s);
+pkv_status launch_prefix_tc_f16(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                                int block_size, dim3 grid, cudaStream_t s);
+pkv_status launch_prefix_tc_bf16(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 int block_size, dim3 grid, cudaStream_t s);
 
 }  // namespace pkv

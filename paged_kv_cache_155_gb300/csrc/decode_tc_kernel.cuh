@@ -83,7 +83,7 @@ struct ItemWalker {
                 int l = s_len ? s_len[seq] : p.context_lens[seq];
                 l = l < 0 ? 0 : (l > p.len_cap ? p.len_cap : l);
                 len = l;
-                nparts = l > 0 ? (l + p.partition_size - 1) / p.partition_size : 1;
+                nparts = partitions_of(p, l);
             }
             const int64_t count = static_cast<int64_t>(nparts) * p.items_y;
             if (r < first + count) {
@@ -114,6 +114,15 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile
             return false;
         }
     }
+}
+
+// tc_wait for a whole warp: every lane waits, and the warp continues only if
+// every lane's wait succeeded, so no lane leaves a loop that the others stay in
+// (the warp-wide shuffles and TMEM accesses that follow need all 32 lanes).
+__device__ __forceinline__ bool tc_wait_warp(uint64_t *bar, uint32_t parity,
+                                             volatile int *abort_flag, unsigned int *status) {
+    const bool ok = tc_wait(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
 }
 
 template <typename T, int BS, int GH>
@@ -214,7 +223,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int64_t r = blockIdx.x; ok; r += gridDim.x) {
             int y, part;
             if (!walk.seek(p, s_len, r, y, part)) break;
-            const int tok0 = part * p.partition_size;
+            const int tok0 = p.tok_begin + part * p.partition_size;
             const int ntok = max(0, min(walk.len, tok0 + p.partition_size) - tok0);
             const int kvh = y / p.subgroups;
             const int32_t *trow = p.block_tables + static_cast<int64_t>(walk.seq) * p.max_blocks_per_seq;
@@ -290,7 +299,7 @@ __global__ void __launch_bounds__(192, 1)
             int ya, pa;
             while (ahead.seek(p, s_len, r_ahead, ya, pa)) {
                 r_ahead += gridDim.x;
-                const int t0a = pa * p.partition_size;
+                const int t0a = p.tok_begin + pa * p.partition_size;
                 if (min(ahead.len, t0a + p.partition_size) - t0a <= 0) continue;
                 const int hqa = (ya / p.subgroups) * p.group + (ya % p.subgroups) * GH;
                 const T *qsrc = static_cast<const T *>(p.q) +
@@ -314,7 +323,7 @@ __global__ void __launch_bounds__(192, 1)
             int y, part;
             while (walk.seek(p, s_len, r, y, part)) {
                 r += gridDim.x;
-                tok0 = part * p.partition_size;
+                tok0 = p.tok_begin + part * p.partition_size;
                 ntok = max(0, min(walk.len, tok0 + p.partition_size) - tok0);
                 if (ntok > 0) {
                     t0 = 0;
@@ -428,14 +437,82 @@ __global__ void __launch_bounds__(192, 1)
         __syncwarp();
     } else {
         // ===================== softmax / accumulate (warps 2..5) =====================
+        // The PV of a tile is folded into o after the softmax of the next tile,
+        // also across work items: an item's last tile, its cross-warp l sum and its
+        // write-out happen after the next item's first tile, so the warps never
+        // wait for the tail of an item's MMAs before starting the next one.
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;  // token row of S, head-dim row of O^T
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+
+        struct Item {
+            int64_t qrow0;  // (sequence, first query head) row of the output
+            int part, nparts;
+            float m[GH], lp[GH], o[GH];
+        };
+        Item cur, pend;   // the item being worked on; the finished one awaiting its last PV
+        bool pend_valid = false;
+        float alpha_prev[GH];
+#pragma unroll
+        for (int h = 0; h < GH; ++h) alpha_prev[h] = 0.f;
         ItemWalker walk;
         uint32_t g = 0;
-        uint32_t items_with_tiles = 0;
+        uint32_t epilogues = 0;
         bool ok = true;
         bool flagged_len = false;
+
+        auto accumulate = [&](uint32_t t, Item &it) -> bool {
+            const int b = t & 1;
+            if (!tc_wait_warp(&o_full[b], (t >> 1) & 1, abort_flag, p.status)) return false;
+            tc::fence_after_sync();
+            float pv[GH];
+            tc::tmem_ld<GH>(lane_base + 32 + 16 * b, pv);
+            tc::tmem_ld_wait();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_empty[b]);
+#pragma unroll
+            for (int h = 0; h < GH; ++h) it.o[h] = fmaf(it.o[h], alpha_prev[h], pv[h]);
+            return true;
+        };
+        // l = sum over the 128 token rows; then the item's output (row = head-dim index)
+        auto epilogue = [&](Item &it) -> bool {
+#pragma unroll
+            for (int h = 0; h < GH; ++h) {
+                float v = it.lp[h];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                it.lp[h] = v;
+            }
+            if (lane == 0) {
+#pragma unroll
+                for (int h = 0; h < GH; ++h) red_l[quarter * 16 + h] = it.lp[h];
+                mbar_arrive(lsum_bar);
+            }
+            if (!tc_wait_warp(lsum_bar, epilogues & 1, abort_flag, p.status)) return false;
+            ++epilogues;
+#pragma unroll
+            for (int h = 0; h < GH; ++h)
+                it.lp[h] = red_l[h] + red_l[16 + h] + red_l[32 + h] + red_l[48 + h];
+            if (it.nparts == 1 && !p.always_partial) {
+#pragma unroll
+                for (int h = 0; h < GH; ++h) {
+                    const float res = it.lp[h] > 0.f ? it.o[h] / it.lp[h] : 0.f;
+                    static_cast<T *>(p.out)[(it.qrow0 + h) * D + row] = Elem<T>::from_f32(res);
+                }
+            } else {
+#pragma unroll
+                for (int h = 0; h < GH; ++h) {
+                    const int64_t pr = (it.qrow0 + h) * p.num_partitions + p.slot_base + it.part;
+                    p.ws_o[pr * D + row] = it.o[h];
+                    if (row == 0) {
+                        p.ws_m[pr] = it.m[h];
+                        p.ws_l[pr] = it.lp[h];
+                    }
+                }
+            }
+            return true;
+        };
 
         for (int64_t r = blockIdx.x; ok; r += gridDim.x) {
             int y, part;
@@ -447,41 +524,41 @@ __global__ void __launch_bounds__(192, 1)
                     flagged_len = true;
                 }
             }
-            const int tok0 = part * p.partition_size;
+            const int tok0 = p.tok_begin + part * p.partition_size;
             const int ntok = max(0, min(walk.len, tok0 + p.partition_size) - tok0);
-            const int nparts = walk.nparts;
             const int kvh = y / p.subgroups;
-            const int hq0 = kvh * p.group + (y % p.subgroups) * GH;
-            float m[GH], lp[GH], o[GH], alpha_prev[GH];
+            const int64_t qrow0 = static_cast<int64_t>(walk.seq) * p.num_q_heads + kvh * p.group +
+                                  (y % p.subgroups) * GH;
+            if (ntok == 0) {
+                // no tokens (empty context or empty range): a zero result, nothing to wait for
+#pragma unroll
+                for (int h = 0; h < GH; ++h) {
+                    if (walk.nparts == 1 && !p.always_partial) {
+                        static_cast<T *>(p.out)[(qrow0 + h) * D + row] = Elem<T>::from_f32(0.f);
+                    } else {
+                        const int64_t pr = (qrow0 + h) * p.num_partitions + p.slot_base + part;
+                        p.ws_o[pr * D + row] = 0.f;
+                        if (row == 0) {
+                            p.ws_m[pr] = -INFINITY;
+                            p.ws_l[pr] = 0.f;
+                        }
+                    }
+                }
+                continue;
+            }
+            cur.qrow0 = qrow0;
+            cur.part = part;
+            cur.nparts = walk.nparts;
 #pragma unroll
             for (int h = 0; h < GH; ++h) {
-                m[h] = -INFINITY;
-                lp[h] = 0.f;
-                o[h] = 0.f;
-                alpha_prev[h] = 0.f;
+                cur.m[h] = -INFINITY;
+                cur.lp[h] = 0.f;
+                cur.o[h] = 0.f;
             }
-
-            auto accumulate = [&](uint32_t t) -> bool {
-                const int b = t & 1;
-                if (!tc_wait(&o_full[b], (t >> 1) & 1, abort_flag, p.status)) return false;
-                tc::fence_after_sync();
-                float pv[GH];
-                tc::tmem_ld<GH>(lane_base + 32 + 16 * b, pv);
-                tc::tmem_ld_wait();
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&o_empty[b]);
-#pragma unroll
-                for (int h = 0; h < GH; ++h) o[h] = fmaf(o[h], alpha_prev[h], pv[h]);
-                return true;
-            };
-
-            if (ntok > 0) ++items_with_tiles;
-            bool have_prev = false;
             for (int t0 = 0; t0 < ntok; t0 += TILE, ++g) {
                 const int tile_ntok = min(TILE, ntok - t0);
                 const int b = g & 1;
-                if (!tc_wait(&s_full[b], (g >> 1) & 1, abort_flag, p.status)) {
+                if (!tc_wait_warp(&s_full[b], (g >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
@@ -509,7 +586,7 @@ __global__ void __launch_bounds__(192, 1)
                     for (int h = 0; h < GH; ++h) red[quarter * 16 + h] = mx[h];
                     mbar_arrive(&max_bar[g & 1]);
                 }
-                if (!tc_wait(&max_bar[g & 1], (g >> 1) & 1, abort_flag, p.status)) {
+                if (!tc_wait_warp(&max_bar[g & 1], (g >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
@@ -518,19 +595,19 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int h = 0; h < GH; ++h) {
                     const float tmax = fmaxf(fmaxf(red[h], red[16 + h]), fmaxf(red[32 + h], red[48 + h]));
-                    const float m_new = fmaxf(m[h], tmax);
-                    alpha[h] = fast_exp2(m[h] - m_new);  // 0 on the first tile (m = -inf)
-                    m[h] = m_new;
+                    const float m_new = fmaxf(cur.m[h], tmax);
+                    alpha[h] = fast_exp2(cur.m[h] - m_new);  // 0 on the first tile (m = -inf)
+                    cur.m[h] = m_new;
                     const float pf = valid ? fast_exp2(sv[h] - m_new) : 0.f;
                     const T p16 = Elem<T>::from_f32(pf);
-                    lp[h] = fmaf(lp[h], alpha[h], static_cast<float>(p16));
+                    cur.lp[h] = fmaf(cur.lp[h], alpha[h], static_cast<float>(p16));
                     const uint32_t off = ((row >> 6) * 2 + (h >> 3)) * 1024 + tc::sw128_offset(h & 7, row & 63);
                     *reinterpret_cast<T *>(panel + off) = p16;
                 }
                 if (tile_ntok < TILE) {
                     // rows past the context: zero their V so 0 * stale never reaches the MMA
                     const int s = g % VS;
-                    if (!tc_wait(&v_full[s], (g / VS) & 1, abort_flag, p.status)) {
+                    if (!tc_wait_warp(&v_full[s], (g / VS) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -546,59 +623,26 @@ __global__ void __launch_bounds__(192, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[b]);
-                if (have_prev && !accumulate(g - 1)) {
+                // fold in the previous tile: the last tile of the pending item, or this item's
+                if (t0 == 0 && pend_valid) {
+                    if (!accumulate(g - 1, pend) || !epilogue(pend)) {
+                        ok = false;
+                        break;
+                    }
+                    pend_valid = false;
+                } else if (t0 > 0 && !accumulate(g - 1, cur)) {
                     ok = false;
                     break;
                 }
 #pragma unroll
                 for (int h = 0; h < GH; ++h) alpha_prev[h] = alpha[h];
-                have_prev = true;
             }
             if (!ok) break;
-            if (have_prev && !accumulate(g - 1)) {
-                ok = false;
-                break;
-            }
-            // l = sum over the 128 token rows of the per-row partial sums
-            if (ntok > 0) {
-#pragma unroll
-                for (int h = 0; h < GH; ++h) {
-                    float v = lp[h];
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-                    lp[h] = v;
-                }
-                if (lane == 0) {
-#pragma unroll
-                    for (int h = 0; h < GH; ++h) red_l[quarter * 16 + h] = lp[h];
-                    mbar_arrive(lsum_bar);
-                }
-                if (!tc_wait(lsum_bar, (items_with_tiles - 1) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-#pragma unroll
-                for (int h = 0; h < GH; ++h) lp[h] = red_l[h] + red_l[16 + h] + red_l[32 + h] + red_l[48 + h];
-            }
-            // ---- write this item's result (row = head-dim index)
-            const int64_t qrow0 = static_cast<int64_t>(walk.seq) * p.num_q_heads + hq0;
-            if (nparts == 1) {
-#pragma unroll
-                for (int h = 0; h < GH; ++h) {
-                    const float res = lp[h] > 0.f ? o[h] / lp[h] : 0.f;
-                    static_cast<T *>(p.out)[(qrow0 + h) * D + row] = Elem<T>::from_f32(res);
-                }
-            } else {
-#pragma unroll
-                for (int h = 0; h < GH; ++h) {
-                    const int64_t pr = (qrow0 + h) * p.num_partitions + part;
-                    p.ws_o[pr * D + row] = o[h];
-                    if (row == 0) {
-                        p.ws_m[pr] = m[h];
-                        p.ws_l[pr] = lp[h];
-                    }
-                }
-            }
+            pend = cur;  // its last tile (g - 1) is folded in after the next tile
+            pend_valid = true;
+        }
+        if (ok && pend_valid) {
+            if (accumulate(g - 1, pend)) epilogue(pend);
         }
     }
 

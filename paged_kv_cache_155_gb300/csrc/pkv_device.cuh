@@ -84,6 +84,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return pol;
 }
 
+// L2 policy for data several CTAs read (a shared prefix).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // Bulk (non-tensor) copy global -> this CTA's shared memory on the TMA engine;
 // completion is signalled as `bytes` of transaction count on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.

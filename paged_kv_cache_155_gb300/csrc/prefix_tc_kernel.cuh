@@ -1,0 +1,416 @@
+// prefix_tc_kernel.cuh -- the shared-prefix half of a cascade decode.
+//
+// When every sequence of a batch starts with the same prefix blocks (prefix
+// caching: "KV Cache与PagedAttention深度解析" §8.2, the nano-vllm article
+// (zwxr.cn) §2.3 / §3), the decode of all B*G query rows of a KV head over the
+// prefix is one dense attention: S = Q K_prefix^T for a [B*G x prefix] tile,
+// then P V_prefix.  Reading the prefix once per 128 query rows instead of once
+// per sequence removes the prefix's repeated reads.  This kernel computes, for
+// a tile of 128 query rows of one KV head and one split of the prefix, the
+// partial (o, m, l) of each row (same definition as the decode kernels:
+// P1 §2.1, running max / running sum of §7.2) and writes it to a workspace
+// slot; the suffix of each sequence is decoded by the usual kernels into the
+// following slots and the log-sum-exp merge combines them.
+//
+// tcgen05 MMAs, M = 128 query rows, N = 128 tokens, K = 128 (head_dim):
+//   S  = Q . K^T      A = Q tile (K-major), B = K tile (K-major)
+//   O += P . V        A = P (K-major), B = V tile (MN-major: head_dim contiguous)
+// S is double-buffered in TMEM (2 x 128 columns), O accumulates in TMEM (128
+// columns).  A row's softmax is local to one thread (TMEM lane = query row).
+// The row maximum used for P is raised only when a tile's maximum exceeds it
+// by more than kRescaleLog2 (then O and l are rescaled in place), so P <=
+// 2^kRescaleLog2.  P is rounded to the input type for the MMA and l sums the
+// rounded values.
+//
+// Warps: 0 TMA producer (K ring and V ring, 2 slots each, 3-D tiled copies with
+// 128-byte swizzle), 1 TMEM owner + MMA issuer (event-driven), 2-5 softmax.
+#pragma once
+
+#include "decode_tc_kernel.cuh"
+
+namespace pkv {
+
+struct PrefixParams {
+    const void *q;
+    float *ws_o;
+    float *ws_m;
+    float *ws_l;
+    const int32_t *prefix_table;  // [prefix_len / block_size] physical blocks
+    const int32_t *context_lens;
+    unsigned int *status;
+    int64_t num_blocks;
+    int num_seqs;
+    int num_q_heads;
+    int group;            // query heads per KV head
+    int rows;             // num_seqs * group
+    int prefix_len;       // tokens, a multiple of block_size
+    int split_tokens;     // tokens per prefix split, a multiple of 128
+    int num_partitions;   // workspace slots per (sequence, query head)
+    float scale_log2;
+};
+
+struct PrefixLayout {
+    static constexpr int kTile = 128;
+    static constexpr int kHalf = 128 * 128;            // 128 rows x 128 B
+    static constexpr int kPanel = 2 * kHalf;           // 128 rows x 128 16-bit values
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kPanel;       // 2 slots
+    static constexpr int kOffV = kOffK + 2 * kPanel;   // 2 slots
+    static constexpr int kOffP = kOffV + 2 * kPanel;   // 2 buffers
+    static constexpr int kOffBar = kOffP + 2 * kPanel;
+    static constexpr int kNumBars = 17;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kSmemBytes = kBytes + 1024;
+    static constexpr uint32_t kTmemCols = 512;           // S[2] at 0 / 128, O at 256
+    static constexpr float kRescaleLog2 = 8.f;
+};
+
+template <typename T, int BS>
+__global__ void __launch_bounds__(192, 1)
+    paged_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                           const __grid_constant__ CUtensorMap tmap_v, const PrefixParams p) {
+    using L = PrefixLayout;
+    constexpr int TILE = L::kTile, D = 128;
+    constexpr bool kBF16 = !std::is_same<T, __half>::value;
+    static_assert(TILE / BS <= 32, "one table entry per producer lane");
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm =
+        smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
+    uint64_t *k_full = bars, *k_empty = bars + 2, *v_full = bars + 4, *v_empty = bars + 6;
+    uint64_t *s_full = bars + 8, *s_empty = bars + 10, *p_full = bars + 12, *o_done = bars + 14;
+    uint64_t *drain_bar = bars + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row_tile = blockIdx.x, kvh = blockIdx.y, split = blockIdx.z;
+    const int tok_lo = split * p.split_tokens;
+    const int tok_hi = min(p.prefix_len, tok_lo + p.split_tokens);
+    const int ntiles = tok_hi > tok_lo ? (tok_hi - tok_lo + TILE - 1) / TILE : 0;
+    const uint32_t smem_base = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_done[i], 1);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, L::kTmemCols);
+        tc::tmem_relinquish();
+    }
+    // query rows of this tile -> Q panel (K-major, 128-byte swizzle); rows past the
+    // batch are zero
+    for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
+        const int r = i >> 4, c8 = i & 15;
+        const int grow = row_tile * 128 + r;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (grow < p.rows) {
+            const int seq = grow / p.group, g = grow - seq * p.group;
+            const T *src = static_cast<const T *>(p.q) +
+                           (static_cast<int64_t>(seq) * p.num_q_heads + kvh * p.group + g) * D;
+            v = *reinterpret_cast<const uint4 *>(src + c8 * 8);
+        }
+        *reinterpret_cast<uint4 *>(sm + L::kOffQ + (c8 >> 3) * L::kHalf + r * 128 +
+                                   (((c8 & 7) ^ (r & 7)) << 4)) = v;
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tensormap(&tmap_k);
+        tc::prefetch_tensormap(&tmap_v);
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ===================== TMA producer =====================
+        const uint64_t policy = l2_policy_evict_last();  // the prefix is read by every row tile
+        int last_issue[2][2] = {{-1, -1}, {-1, -1}};
+        bool ok = true;
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int t0 = tok_lo + j * TILE;
+            const int nblk = (min(TILE, tok_hi - t0) + BS - 1) / BS;
+            int e = -1;
+            if (lane < nblk) {
+                e = p.prefix_table[t0 / BS + lane];
+                if (e < 0 || e >= p.num_blocks) {
+                    raise_flag(p.status, PKV_DEVERR_BLOCK_TABLE);
+                    e = -1;
+                }
+            }
+            const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, e >= 0)) * BS * 256u;
+            for (int kv = 0; kv < 2 && ok; ++kv) {
+                const int s = j & 1;
+                uint64_t *fb = kv ? &v_full[s] : &k_full[s];
+                uint64_t *eb = kv ? &v_empty[s] : &k_empty[s];
+                int go = 1;
+                if (lane == 0) {
+                    go = tc_wait(eb, ((j >> 1) & 1) ^ 1, abort_flag, p.status);
+                    if (go) {
+                        if (bytes) mbar_arrive_expect_tx(fb, bytes);
+                        else mbar_arrive(fb);
+                        last_issue[kv][s] = j;
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, go, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (e >= 0) {
+                    unsigned char *slot = sm + (kv ? L::kOffV : L::kOffK) + s * L::kPanel;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        tc::tma_load_3d(slot + c * L::kHalf + lane * BS * 128, kv ? &tmap_v : &tmap_k,
+                                        c * 64, kvh * BS, e, fb, policy);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && lane == 0) {
+            for (int kv = 0; kv < 2; ++kv)
+                for (int s = 0; s < 2; ++s)
+                    if (last_issue[kv][s] >= 0)
+                        mbar_wait_bounded(kv ? &v_full[s] : &k_full[s], (last_issue[kv][s] >> 1) & 1,
+                                          kDrainTimeoutNs);
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer (event-driven, PV first) =====================
+        constexpr uint32_t idesc_qk = tc::idesc_f16_f32acc(kBF16, 128, 128, false, false);
+        constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, 128, false, true);
+        int n_qk = 0, n_pv = 0;
+        bool ok = true;
+        uint64_t idle_since = 0;
+        while (ok && n_pv < ntiles) {
+            int act = 0;
+            if (lane == 0) {
+                if (n_pv < n_qk && mbar_try_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
+                    mbar_try_wait(&v_full[n_pv & 1], (n_pv >> 1) & 1))
+                    act = 1;
+                else if (n_qk < ntiles && mbar_try_wait(&k_full[n_qk & 1], (n_qk >> 1) & 1) &&
+                         mbar_try_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
+                    act = 2;
+                if (act) {
+                    idle_since = 0;
+                } else {
+                    const uint64_t now = global_timer_ns();
+                    if (!idle_since) idle_since = now;
+                    if (*abort_flag) {
+                        act = -1;
+                    } else if (now - idle_since > kWaitTimeoutNs) {
+                        raise_flag(p.status, PKV_DEVERR_TIMEOUT);
+                        *abort_flag = 1;
+                        act = -1;
+                    }
+                }
+                if (act == 1) {
+                    const int j = n_pv, b = j & 1;
+                    tc::fence_after_sync();
+                    const uint32_t pa = smem_base + L::kOffP + b * L::kPanel;
+                    const uint32_t va = smem_base + L::kOffV + b * L::kPanel;
+#pragma unroll
+                    for (int k = 0; k < TILE / 16; ++k) {
+                        const uint64_t a = tc::smem_desc_sw128(pa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(va + k * 2048, L::kHalf, 1024);
+                        tc::mma_f16_ss(tmem + 256, a, bd, idesc_pv, j > 0 || k > 0);
+                    }
+                    tc::mma_commit(&o_done[b]);
+                    tc::mma_commit(&v_empty[b]);
+                } else if (act == 2) {
+                    const int j = n_qk, b = j & 1;
+                    tc::fence_after_sync();
+                    const uint32_t qa = smem_base + L::kOffQ;
+                    const uint32_t ka = smem_base + L::kOffK + b * L::kPanel;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint64_t a = tc::smem_desc_sw128(qa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(ka + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                        tc::mma_f16_ss(tmem + 128 * b, a, bd, idesc_qk, k > 0);
+                    }
+                    tc::mma_commit(&s_full[b]);
+                    tc::mma_commit(&k_empty[b]);
+                }
+            }
+            act = __shfl_sync(0xffffffffu, act, 0);
+            if (act < 0) ok = false;
+            else if (act == 1) ++n_pv;
+            else if (act == 2) ++n_qk;
+        }
+        if (lane == 0) {
+            // every MMA of this CTA completes before TMEM is released
+            tc::mma_commit(drain_bar);
+            mbar_wait_bounded(drain_bar, 0, kDrainTimeoutNs);
+        }
+        __syncwarp();
+    } else {
+        // ===================== softmax (warps 2..5): thread = query row =====================
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
+        const int grow = row_tile * 128 + r;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int b = j & 1;
+            const int t0 = tok_lo + j * TILE;
+            const int valid = min(TILE, tok_hi - t0);
+            if (!tc_wait_warp(&s_full[b], (j >> 1) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            // pass 1: tile maximum of this row
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < TILE; c += 32) {
+                float x[32];
+                tc::tmem_ld_x16(lane_base + 128 * b + c, x);
+                tc::tmem_ld_x16(lane_base + 128 * b + c + 16, x + 16);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (c + i < valid) tmax = fmaxf(tmax, x[i] * p.scale_log2);
+            }
+            // the reference maximum moves only by more than kRescaleLog2; TMEM loads and
+            // stores are warp-wide, so the warp rescales if any of its rows must
+            const float new_ref = tmax > m_ref + L::kRescaleLog2 ? tmax : m_ref;
+            const float alpha = fast_exp2(m_ref - new_ref);  // 1 if unchanged, 0 on the first tile
+            if (__any_sync(0xffffffffu, new_ref != m_ref)) {
+                if (j > 0) {
+                    // O holds tiles < j: wait for PV(j-1), rescale O in TMEM
+                    if (!tc_wait_warp(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int c = 0; c < D; c += 16) {
+                        float o[16];
+                        tc::tmem_ld_x16(lane_base + 256 + c, o);
+                        tc::tmem_ld_wait();
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(o[i] * alpha);
+                        asm volatile(
+                            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, "
+                            "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(lane_base + 256 + c),
+                            "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                            "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]),
+                            "r"(w[13]), "r"(w[14]), "r"(w[15])
+                            : "memory");
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                }
+                l *= alpha;
+                m_ref = new_ref;
+            }
+            // P[b] was last read by PV(j-2)
+            if (j >= 2 && !tc_wait_warp(&o_done[b], ((j - 2) >> 1) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            // pass 2: P = 2^(s - m_ref), rounded to T, into the K-major P panel
+            unsigned char *prow = sm + L::kOffP + b * L::kPanel + r * 128;
+#pragma unroll
+            for (int c = 0; c < TILE; c += 32) {
+                float x[32];
+                tc::tmem_ld_x16(lane_base + 128 * b + c, x);
+                tc::tmem_ld_x16(lane_base + 128 * b + c + 16, x + 16);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t packed[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int t = c + c8 * 8 + 2 * i;
+                        const float p0 = t < valid ? fast_exp2(x[c8 * 8 + 2 * i] * p.scale_log2 - m_ref) : 0.f;
+                        const float p1 = t + 1 < valid ? fast_exp2(x[c8 * 8 + 2 * i + 1] * p.scale_log2 - m_ref) : 0.f;
+                        const T h0 = Elem<T>::from_f32(p0), h1 = Elem<T>::from_f32(p1);
+                        l += static_cast<float>(h0) + static_cast<float>(h1);
+                        packed[i] = static_cast<uint32_t>(reinterpret_cast<const uint16_t &>(h0)) |
+                                    (static_cast<uint32_t>(reinterpret_cast<const uint16_t &>(h1)) << 16);
+                    }
+                    const int chunk = (c + c8 * 8) >> 3;  // 8-token chunk index, 0..15
+                    *reinterpret_cast<uint4 *>(prow + (chunk >> 3) * L::kHalf + (((chunk & 7) ^ (r & 7)) << 4)) =
+                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                }
+            }
+            tc::fence_before_sync();
+            if (valid < TILE) {
+                // rows of V past the prefix end: zero them so 0 * stale never reaches the MMA
+                if (!tc_wait_warp(&v_full[b], (j >> 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                if (r >= valid) {
+                    unsigned char *vrow = sm + L::kOffV + b * L::kPanel + r * 128;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            reinterpret_cast<uint4 *>(vrow + c * L::kHalf)[i] = make_uint4(0, 0, 0, 0);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&s_empty[b]);
+                mbar_arrive(&p_full[b]);
+            }
+        }
+        // final: O row -> workspace slot `split` of every (sequence, query head) row.
+        // TMEM loads are warp-wide: every lane loads, only rows of the batch store.
+        if (ntiles > 0) {
+            if (ok) ok = tc_wait_warp(&o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
+            if (ok) {
+                tc::fence_after_sync();
+                const bool mine = grow < p.rows;
+                int64_t prow_ws = 0;
+                if (mine) {
+                    const int seq = grow / p.group, g = grow - seq * p.group;
+                    prow_ws = (static_cast<int64_t>(seq) * p.num_q_heads + kvh * p.group + g) *
+                                  p.num_partitions + split;
+                }
+#pragma unroll
+                for (int c = 0; c < D; c += 16) {
+                    float o[16];
+                    tc::tmem_ld_x16(lane_base + 256 + c, o);
+                    tc::tmem_ld_wait();
+                    if (mine) {
+                        float *dst = p.ws_o + prow_ws * D + c;
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4 *>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+                    }
+                }
+                if (mine) {
+                    p.ws_m[prow_ws] = m_ref;
+                    p.ws_l[prow_ws] = l;
+                }
+            }
+        }
+    }
+
+    // ---- tear-down: the MMA warp drained its MMAs; TMEM is freed
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+}  // namespace pkv

@@ -141,6 +141,58 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     return out
 
 
+def shared_prefix_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                  prefix_len, max_context_len, partition_size=0) -> int:
+    n = lib().pkv_shared_prefix_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                block_size, prefix_len, max_context_len,
+                                                partition_size)
+    if n == ctypes.c_size_t(-1).value:
+        raise PagedKVError("pkv_shared_prefix_workspace_bytes", 1)
+    return int(n)
+
+
+def paged_attention_decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor,
+                                         v_cache: torch.Tensor, prefix_block_table: torch.Tensor,
+                                         prefix_len: int, block_tables: torch.Tensor,
+                                         context_lens: torch.Tensor, scale: Optional[float] = None,
+                                         out: Optional[torch.Tensor] = None, *,
+                                         max_context_len: Optional[int] = None,
+                                         partition_size: int = 0,
+                                         workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """paged_attention_decode for a batch that shares its first prefix_len tokens
+    (prefix_block_table holds their blocks): the prefix is attended by all query
+    rows together as dense tiles, then each sequence's suffix, then a merge."""
+    nb, hkv, bs, d, stride = _cache_geometry(k_cache, v_cache)
+    if q.dim() != 3 or q.shape[2] != d or not q.is_contiguous() or q.dtype != k_cache.dtype:
+        raise ValueError(f"q must be a contiguous [num_seqs, num_q_heads, {d}] of the cache dtype")
+    b, hq = int(q.shape[0]), int(q.shape[1])
+    if prefix_block_table.dtype != torch.int32 or not prefix_block_table.is_contiguous():
+        raise ValueError("prefix_block_table must be a contiguous int32 tensor")
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be a contiguous int32 [num_seqs, max_blocks_per_seq]")
+    if context_lens.dtype != torch.int32 or context_lens.numel() != b:
+        raise ValueError("context_lens must be int32 [num_seqs]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item())
+    if out is None:
+        out = torch.empty_like(q)
+    need = shared_prefix_workspace_bytes(b, hq, hkv, d, bs, prefix_len, max_context_len,
+                                         partition_size)
+    if workspace is None:
+        workspace = _workspace(q.device, need)
+    st = lib().pkv_paged_attention_decode_shared_prefix(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), nb, stride,
+        prefix_block_table.data_ptr(), int(prefix_len), block_tables.data_ptr(),
+        int(block_tables.shape[1]), context_lens.data_ptr(), int(max_context_len), b, hq, hkv, d,
+        bs, float(scale), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), int(partition_size), _dtype_code(q),
+        _stream(q))
+    _check(st, "pkv_paged_attention_decode_shared_prefix")
+    return out
+
+
 def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: torch.Tensor) -> None:
     """Copy K and V of block src over block dst for each row (src, dst) of an int64 [n, 2]."""
     nb, hkv, bs, d, stride = _cache_geometry(k_cache, v_cache)

@@ -118,18 +118,20 @@ def test_plan_explicit_partition(lib):
 
 
 def test_plan_heads_per_block_follows_the_group(lib):
-    # head_dim 128 with 4, 8 or 16 heads per KV head: the tensor-core path serves the whole group
+    # long contexts, head_dim 128, 4/8/16 heads per KV head: the tensor-core path serves the group
     for hq, hkv, want in [(32, 32, 1), (32, 16, 2), (32, 8, 4), (64, 8, 8), (24, 8, 1),
                           (48, 8, 2), (128, 8, 16)]:
-        st, (_, _, gh, _) = plan(lib, 4, hq, hkv, 128, 16, 1000, 0)
+        st, (_, _, gh, _) = plan(lib, 4, hq, hkv, 128, 16, 4000, 0)
         assert st == 0 and gh == want, (hq, hkv)
-    # head_dim 64 stays on CUDA cores (at most 8 heads per CTA)
-    st, (_, _, gh, _) = plan(lib, 4, 128, 8, 64, 16, 1000, 0)
+    # short contexts stay on CUDA cores (at most 8 heads per CTA), as does head_dim 64
+    st, (_, _, gh, _) = plan(lib, 4, 128, 8, 128, 16, 1000, 0)
+    assert st == 0 and gh == 8
+    st, (_, _, gh, _) = plan(lib, 4, 128, 8, 64, 16, 4000, 0)
     assert st == 0 and gh == 8
 
 
 def test_plan_tensor_core_partitions_are_whole_tiles(lib):
-    for maxl in (300, 4096, 8192, 32768):
+    for maxl in (2048, 4096, 8192, 32768):
         st, (p, n, gh, _) = plan(lib, 64, 32, 8, 128, 16, maxl, 0)
         assert st == 0 and gh == 4 and p % 128 == 0 and (n - 1) * p < maxl <= n * p
 
@@ -173,3 +175,22 @@ def test_host_slot_helper_matches_oracle_slot_rule():
 def test_package_import_does_not_need_a_gpu():
     import paged_kv_cache_155_gb300 as pkv
     assert callable(pkv.paged_attention_decode)
+
+
+def test_shared_prefix_decode_rejects_bad_arguments_on_host(lib):
+    def call(**kw):
+        a = dict(q=16, k=16, v=16, nb=64, stride=2 * 2 * 16 * 128, pt=16, plen=256, bt=16, mb=32,
+                 cl=16, maxl=400, b=4, hq=8, hkv=2, d=128, bs=16, out=16, ws=16, wsb=1 << 20,
+                 part=0, dt=1)
+        a.update(kw)
+        return lib.pkv_paged_attention_decode_shared_prefix(
+            a["q"], a["k"], a["v"], a["nb"], a["stride"], a["pt"], a["plen"], a["bt"], a["mb"],
+            a["cl"], a["maxl"], a["b"], a["hq"], a["hkv"], a["d"], a["bs"], 0.088, a["out"],
+            a["ws"], a["wsb"], a["part"], a["dt"], None)
+    assert call(d=64) == UNSUPPORTED              # the prefix tiles are built for head_dim 128
+    assert call(plen=250) == INVALID              # not a multiple of block_size
+    assert call(plen=0) == INVALID
+    assert call(plen=512) == INVALID              # longer than max_context_len
+    assert call(pt=0) == INVALID                  # no prefix table
+    assert call(ws=0) == INVALID                  # the workspace is required
+    assert call(hq=6, hkv=4) == INVALID

@@ -34,13 +34,17 @@ def _check_step(wl_dev, partition_size=0):
     return assert_close(out, ref)
 
 
+@pytest.mark.parametrize("longest", [300, 2100], ids=["short", "long"])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("bs", [8, 16, 32])
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (16, 4), (32, 4), (12, 4), (24, 4), (64, 4)])
-def test_decode_shapes(dtype, d, bs, hq, hkv):
+def test_decode_shapes(dtype, d, bs, hq, hkv, longest):
+    """A batch whose longest context is >= 2048 runs on the tensor-core kernel when
+    head_dim is 128 and the group has 4, 8 or 16 heads; a short batch on the CUDA-core
+    kernel: both kernels see every shape."""
     dev = device()
-    lens = [1, bs - 1, bs, bs + 1, 5 * bs + 3, 300, 17]
+    lens = [1, bs - 1, bs, bs + 1, 5 * bs + 3, longest, 17]
     wl = make_decode_workload(num_seqs=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
                               block_size=bs, context_lens=lens, dtype=dtype,
                               seed=hq * 7 + d + bs, device=str(dev))
@@ -51,7 +55,7 @@ def test_decode_shapes(dtype, d, bs, hq, hkv):
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 def test_decode_forced_partitions(partition, dtype):
     dev = device()
-    lens = [1, 15, 16, 17, 511, 512, 513, 1500, 2049]
+    lens = [1, 15, 16, 17, 511, 512, 513, 1500, 2049]   # longest >= 2048: tensor cores
     wl = make_decode_workload(num_seqs=len(lens), num_q_heads=16, num_kv_heads=2, head_dim=128,
                               block_size=16, context_lens=lens, dtype=dtype, seed=partition,
                               device=str(dev))
@@ -112,17 +116,18 @@ def test_decode_extreme_scores_stay_finite():
     _check_step(wl, partition_size=64)
 
 
-def test_decode_output_is_independent_of_block_placement():
+@pytest.mark.parametrize("longest", [2047, 2100], ids=["cuda-cores", "tensor-cores"])
+def test_decode_output_is_independent_of_block_placement(longest):
     """Moving every block to another physical slot leaves the output bitwise unchanged."""
     dev = device()
     wl = make_decode_workload(num_seqs=6, num_q_heads=32, num_kv_heads=8, head_dim=128,
-                              block_size=16, context_lens=[1, 100, 1000, 2047, 16, 555],
+                              block_size=16, context_lens=[1, 100, 1000, longest, 16, 555],
                               dtype=torch.float16, seed=9, device=str(dev))
     k_cache, v_cache = pkv.split_pool(wl.kv)
     outs = []
     for part in (0, 128):
         a = pkv.paged_attention_decode(wl.q, k_cache, v_cache, wl.block_tables, wl.context_lens,
-                                       wl.scale, max_context_len=2047, partition_size=part)
+                                       wl.scale, max_context_len=longest, partition_size=part)
         perm = torch.randperm(wl.num_blocks, generator=torch.Generator().manual_seed(part))
         perm = perm.to(dev)
         kv2 = torch.empty_like(wl.kv)
@@ -130,7 +135,7 @@ def test_decode_output_is_independent_of_block_placement():
         bt2 = perm[wl.block_tables.long()].to(torch.int32)
         k2, v2 = pkv.split_pool(kv2)
         b = pkv.paged_attention_decode(wl.q, k2, v2, bt2, wl.context_lens, wl.scale,
-                                       max_context_len=2047, partition_size=part)
+                                       max_context_len=longest, partition_size=part)
         torch.cuda.synchronize()
         assert torch.equal(a, b)
         outs.append(a)
