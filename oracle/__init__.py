@@ -78,6 +78,19 @@ def _load():
         lib.oracle_reshape_and_cache.restype = None
         lib.oracle_copy_blocks.argtypes = [P, P, i64, i64, P, i64]
         lib.oracle_copy_blocks.restype = None
+        f32 = ctypes.c_float
+        lib.oracle_quantize_int8.argtypes = [ctypes.c_uint16, i32, f32]
+        lib.oracle_quantize_int8.restype = i32
+        lib.oracle_quantize_int8_array.argtypes = [P, i64, P, i64, i32, P]
+        lib.oracle_quantize_int8_array.restype = None
+        lib.oracle_reshape_and_cache_int8.argtypes = [P, P, P, i64, P, P, i64, i32, i32, i32,
+                                                      P, P, i32]
+        lib.oracle_reshape_and_cache_int8.restype = None
+        lib.oracle_paged_decode_int8.argtypes = [P, P, P, P, P, i64, P, i32, P, i32, i32, i32,
+                                                 i32, i32, dbl, i32, P]
+        lib.oracle_paged_decode_int8.restype = None
+        lib.oracle_copy_blocks_bytes.argtypes = [P, P, i64, i64, P, i64]
+        lib.oracle_copy_blocks_bytes.restype = None
         _lib = lib
         return lib
 
@@ -190,6 +203,84 @@ def copy_blocks(kv_pool_bits: np.ndarray, src_dst: np.ndarray, num_kv_heads: int
     base = pool.ctypes.data
     _load().oracle_copy_blocks(ctypes.c_void_p(base), ctypes.c_void_p(base + 2 * half),
                                int(2 * half), int(half), _ptr(pairs), int(pairs.shape[0]))
+
+
+# ---------------------------------------------------------------------------
+# INT8 KV cache with per-channel scales (P2 §5.2).
+# ---------------------------------------------------------------------------
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def quantize_int8_scalar(bits: int, dtype: int, scale: float) -> int:
+    """Code of one 16-bit value: round-half-even(clamp(x / s, -127, 127)) in fp32."""
+    return int(_load().oracle_quantize_int8(int(bits) & 0xFFFF, int(dtype), float(scale)))
+
+
+def quantize_int8(x_bits: np.ndarray, scales: np.ndarray, dtype: int) -> np.ndarray:
+    """Codes of an array [..., heads, head_dim] of 16-bit patterns with per-channel
+    scales [heads, head_dim] (broadcast over the leading axes), or one scale for all."""
+    x = _u16(x_bits)
+    sc = _f32(scales)
+    if sc.size != 1 and x.shape[-sc.ndim:] != sc.shape:
+        raise ValueError("scales must be one value or match the trailing axes of x")
+    codes = np.empty(x.shape, dtype=np.int8)
+    _load().oracle_quantize_int8_array(_ptr(x), int(x.size), _ptr(sc), int(sc.size), int(dtype),
+                                       _ptr(codes))
+    return codes
+
+
+def reshape_and_cache_int8(k_new, v_new, slot_mapping_, kv_pool: np.ndarray, k_scale, v_scale,
+                           num_kv_heads: int, block_size: int, head_dim: int, dtype: int) -> None:
+    """Quantising cache write into a packed INT8 pool [NB, 2, Hkv, bs, d] (in place)."""
+    pool = kv_pool
+    assert pool.dtype == np.int8 and pool.flags.c_contiguous
+    kn, vn = _u16(k_new), _u16(v_new)
+    sm = np.ascontiguousarray(slot_mapping_, dtype=np.int64)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    half = num_kv_heads * block_size * head_dim
+    base = pool.ctypes.data
+    _load().oracle_reshape_and_cache_int8(
+        _ptr(kn), _ptr(vn), _ptr(sm), int(sm.shape[0]), ctypes.c_void_p(base),
+        ctypes.c_void_p(base + half), int(2 * half), int(num_kv_heads), int(head_dim),
+        int(block_size), _ptr(ks), _ptr(vs), int(dtype))
+
+
+def paged_decode_int8(q, kv_pool: np.ndarray, k_scale, v_scale, block_tables, context_lens,
+                      num_kv_heads, block_size, scale, dtype):
+    """Two-pass decode attention over a packed INT8 pool [NB, 2, Hkv, bs, d], each
+    code dequantised as code * scale[h][channel] (P2 §5.2; P1 §2.1, §4.2-4.3).
+    Returns fp64 [num_seqs, num_q_heads, head_dim]."""
+    q = _u16(q)
+    pool = np.ascontiguousarray(kv_pool)
+    assert pool.dtype == np.int8
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    num_seqs, num_q_heads, head_dim = q.shape
+    if num_q_heads % num_kv_heads:
+        raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+    half = num_kv_heads * block_size * head_dim
+    base = pool.ctypes.data
+    out = np.zeros((num_seqs, num_q_heads, head_dim), dtype=np.float64)
+    _load().oracle_paged_decode_int8(
+        _ptr(q), ctypes.c_void_p(base), ctypes.c_void_p(base + half), _ptr(ks), _ptr(vs),
+        int(2 * half), _ptr(bt), int(bt.shape[1]), _ptr(cl), int(num_seqs), int(num_q_heads),
+        int(num_kv_heads), int(head_dim), int(block_size), float(scale), int(dtype), _ptr(out))
+    return out
+
+
+def copy_blocks_bytes(kv_pool: np.ndarray, src_dst: np.ndarray) -> None:
+    """Copy-on-write block copies on a packed pool [NB, 2, ...] of any dtype (in place)."""
+    pool = kv_pool
+    assert pool.flags.c_contiguous
+    pairs = np.ascontiguousarray(src_dst, dtype=np.int64).reshape(-1, 2)
+    block_bytes = pool[0].nbytes
+    base = pool.ctypes.data
+    _load().oracle_copy_blocks_bytes(ctypes.c_void_p(base), ctypes.c_void_p(base + block_bytes // 2),
+                                     int(block_bytes), int(block_bytes // 2), _ptr(pairs),
+                                     int(pairs.shape[0]))
 
 
 # ---------------------------------------------------------------------------

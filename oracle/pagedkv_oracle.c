@@ -249,3 +249,126 @@ void oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, int64_t block_stri
         memcpy(v_cache + dst * block_stride, v_cache + src * block_stride, sizeof(uint16_t) * block_elems);
     }
 }
+
+/* ------------------------------------------------------------------------
+ * INT8 KV cache with per-channel scales (P2 §5.2: storing the cache as INT8
+ * halves its bytes; scales computed per channel, separately for K and V, is
+ * the INT8 variant that page recommends over per-tensor scales).  Channel c of
+ * KV head h owns one K scale and one V scale, scale[h * head_dim + c] > 0.
+ *
+ * Quantise (the page does not fix the rounding; the readings used here):
+ * x is the 16-bit input, widened exactly to IEEE single precision;
+ * r = x / s in single precision; r is clamped to [-127, 127] (symmetric
+ * range, -128 unused) and rounded to the nearest integer, ties to even.
+ * The division is done in single precision because the code is an integer
+ * decided by floating point: both implementations must take that decision in
+ * the same precision.  (A NaN input clamps to -127: fmaxf returns the
+ * non-NaN operand.)
+ * Dequantise: x' = code * s (exact in fp64).  Attention then follows the
+ * same definition as oracle_paged_decode on the dequantised K and V.
+ * ------------------------------------------------------------------------ */
+int oracle_quantize_int8(uint16_t bits, int dtype, float scale) {
+    const float x = (float)decode16(bits, dtype); /* exact: 16-bit values fit in binary32 */
+    float r = x / scale;
+    r = fmaxf(r, -127.0f);
+    r = fminf(r, 127.0f);
+    return (int)nearbyintf(r); /* default rounding mode: to nearest, ties to even */
+}
+
+/* Element i of x uses scale[i % scale_period] (x laid out [..][heads][head_dim]
+ * with scale [heads][head_dim] gives scale_period = heads * head_dim). */
+void oracle_quantize_int8_array(const uint16_t *x, int64_t n, const float *scale,
+                                int64_t scale_period, int dtype, int8_t *codes) {
+    for (int64_t i = 0; i < n; ++i)
+        codes[i] = (int8_t)oracle_quantize_int8(x[i], dtype, scale[i % scale_period]);
+}
+
+/* Cache write into an INT8 pool: token n's head h row is quantised channel by
+ * channel with that head's scales and stored at slot s = slot_mapping[n]
+ * (block s / bs, offset s % bs), exactly as oracle_reshape_and_cache places a
+ * 16-bit row.  A negative slot means "no write". */
+void oracle_reshape_and_cache_int8(const uint16_t *k_new, const uint16_t *v_new,
+                                   const int64_t *slot_mapping, int64_t num_tokens,
+                                   int8_t *k_cache, int8_t *v_cache, int64_t block_stride,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   const float *k_scale, const float *v_scale, int dtype) {
+    for (int64_t n = 0; n < num_tokens; ++n) {
+        const int64_t slot = slot_mapping[n];
+        if (slot < 0) continue;
+        const int64_t blk = slot / block_size;
+        const int64_t off = slot % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            const int64_t dst = blk * block_stride + ((int64_t)h * block_size + off) * head_dim;
+            const int64_t src = (n * num_kv_heads + h) * (int64_t)head_dim;
+            for (int j = 0; j < head_dim; ++j) {
+                k_cache[dst + j] = (int8_t)oracle_quantize_int8(k_new[src + j], dtype, k_scale[h * head_dim + j]);
+                v_cache[dst + j] = (int8_t)oracle_quantize_int8(v_new[src + j], dtype, v_scale[h * head_dim + j]);
+            }
+        }
+    }
+}
+
+/* Decode attention over an INT8 pool: the direct two-pass definition of
+ * oracle_paged_decode with k_t[j] = code * k_scale[h][j] and
+ * v_t[j] = code * v_scale[h][j].  q is 16-bit; out is fp64. */
+void oracle_paged_decode_int8(const uint16_t *q, const int8_t *k_cache, const int8_t *v_cache,
+                              const float *k_scale, const float *v_scale, int64_t block_stride,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, int num_seqs, int num_q_heads,
+                              int num_kv_heads, int head_dim, int block_size, double scale,
+                              int dtype, double *out) {
+    const int group = num_q_heads / num_kv_heads;
+    const int64_t pairs = (int64_t)num_seqs * num_q_heads;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t pair = 0; pair < pairs; ++pair) {
+        const int i = (int)(pair / num_q_heads);
+        const int hq = (int)(pair % num_q_heads);
+        const int h = hq / group;
+        const int64_t len = context_lens[i];
+        const uint16_t *qrow = q + ((int64_t)i * num_q_heads + hq) * head_dim;
+        const float *ks = k_scale + (int64_t)h * head_dim;
+        const float *vs = v_scale + (int64_t)h * head_dim;
+        double *orow = out + ((int64_t)i * num_q_heads + hq) * head_dim;
+        for (int j = 0; j < head_dim; ++j) orow[j] = 0.0;
+        if (len <= 0) continue;
+
+        double *qv = (double *)malloc(sizeof(double) * head_dim);
+        double *score = (double *)malloc(sizeof(double) * len);
+        for (int j = 0; j < head_dim; ++j) qv[j] = decode16(qrow[j], dtype);
+
+        double smax = -INFINITY;
+        for (int64_t t = 0; t < len; ++t) {
+            const int64_t phys = block_tables[(int64_t)i * max_blocks_per_seq + t / block_size];
+            const int64_t off = t % block_size;
+            const int8_t *krow = k_cache + phys * block_stride + ((int64_t)h * block_size + off) * head_dim;
+            double dot = 0.0;
+            for (int j = 0; j < head_dim; ++j) dot += qv[j] * ((double)krow[j] * (double)ks[j]);
+            score[t] = scale * dot;
+            if (score[t] > smax) smax = score[t];
+        }
+        double z = 0.0;
+        for (int64_t t = 0; t < len; ++t) {
+            const int64_t phys = block_tables[(int64_t)i * max_blocks_per_seq + t / block_size];
+            const int64_t off = t % block_size;
+            const int8_t *vrow = v_cache + phys * block_stride + ((int64_t)h * block_size + off) * head_dim;
+            const double w = exp(score[t] - smax);
+            z += w;
+            for (int j = 0; j < head_dim; ++j) orow[j] += w * ((double)vrow[j] * (double)vs[j]);
+        }
+        for (int j = 0; j < head_dim; ++j) orow[j] /= z;
+        free(score);
+        free(qv);
+    }
+}
+
+/* copy-on-write block copies on a pool of any element size: the K and V
+ * halves of block src, block_bytes each, copied byte for byte over block dst's. */
+void oracle_copy_blocks_bytes(unsigned char *k_cache, unsigned char *v_cache,
+                              int64_t block_stride_bytes, int64_t block_bytes,
+                              const int64_t *src_dst, int64_t num_pairs) {
+    for (int64_t p = 0; p < num_pairs; ++p) {
+        const int64_t src = src_dst[2 * p], dst = src_dst[2 * p + 1];
+        memcpy(k_cache + dst * block_stride_bytes, k_cache + src * block_stride_bytes, block_bytes);
+        memcpy(v_cache + dst * block_stride_bytes, v_cache + src * block_stride_bytes, block_bytes);
+    }
+}
