@@ -144,12 +144,36 @@ class ClockSampler:
 
 
 def _algorithmic_bytes(wl):
-    """K+V of every context token per KV head (once per GQA group) + q + out."""
-    e = 2
+    """K+V of every context token per KV head (once per GQA group) + q + out
+    (+ the per-channel scales of an INT8 cache)."""
+    e = wl.kv.element_size()
     tokens = sum(int(x) for x in wl.context_lens.cpu().tolist())
     kv = tokens * 2 * wl.num_kv_heads * wl.head_dim * e
-    qo = 2 * wl.num_seqs * wl.num_q_heads * wl.head_dim * e
-    return kv + qo
+    qo = 2 * wl.num_seqs * wl.num_q_heads * wl.head_dim * wl.q.element_size()
+    scales = 2 * wl.num_kv_heads * wl.head_dim * 4 if wl.k_scale is not None else 0
+    return kv + qo + scales
+
+
+def _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part):
+    """(cache write, decode) of one step through the public API, for a 16-bit or
+    an INT8 pool."""
+    if wl.kv.dtype == __import__("torch").int8:
+        def write(k_new, v_new, slots):
+            pkv.reshape_and_cache_int8(k_new, v_new, slots, k_cache, v_cache, wl.k_scale,
+                                       wl.v_scale)
+
+        def decode(q, bt, cl):
+            pkv.paged_attention_decode_int8(q, k_cache, v_cache, wl.k_scale, wl.v_scale, bt, cl,
+                                            wl.scale, out, max_context_len=maxl,
+                                            partition_size=part)
+    else:
+        def write(k_new, v_new, slots):
+            pkv.reshape_and_cache(k_new, v_new, slots, k_cache, v_cache)
+
+        def decode(q, bt, cl):
+            pkv.paged_attention_decode(q, k_cache, v_cache, bt, cl, wl.scale, out,
+                                       max_context_len=maxl, partition_size=part)
+    return write, decode
 
 
 def _make_workload(name, device, seed, num_seqs=None):
@@ -166,7 +190,9 @@ def _workload_config(wl, name, plan, partition):
             "context_len_min": int(lens.min()), "context_len_max": int(lens.max()),
             "context_tokens": int(lens.sum()), "partition_size": plan["partition_size"],
             "num_partitions": plan["num_partitions"], "partition_arg": partition,
-            "l2": f"no flush: pool of {wl.kv.numel() * 2 / 2**30:.2f} GiB > 129 MB L2"}
+            "kv_dtype": str(wl.kv.dtype).replace("torch.", ""),
+            "l2": f"no flush: pool of {wl.kv.numel() * wl.kv.element_size() / 2**30:.2f} GiB "
+                  "> 129 MB L2"}
 
 
 # --------------------------------------------------------------------------- oracle legs
@@ -286,11 +312,11 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
     slots = pkv.slot_mapping(wl.block_tables.cpu(), wl.new_positions.cpu(), wl.block_size).to(dev)
     out = torch.empty_like(wl.q)
     stream = torch.cuda.current_stream(dev)
+    write, decode = _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part)
 
     def step():
-        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
-        pkv.paged_attention_decode(wl.q, k_cache, v_cache, wl.block_tables, wl.context_lens,
-                                   wl.scale, out, max_context_len=maxl, partition_size=part)
+        write(wl.k_new, wl.v_new, slots)
+        decode(wl.q, wl.block_tables, wl.context_lens)
 
     for _ in range(5):
         step()
@@ -300,10 +326,9 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for k in range(steps):
-        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
+        write(wl.k_new, wl.v_new, slots)
         ev[k][0].record(stream)
-        pkv.paged_attention_decode(wl.q, k_cache, v_cache, wl.block_tables, wl.context_lens,
-                                   wl.scale, out, max_context_len=maxl, partition_size=part)
+        decode(wl.q, wl.block_tables, wl.context_lens)
         ev[k][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -340,7 +365,7 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
               "graph_us_per_step": graph_ms * 1e3,
               "graph_tokens_per_s": wl.num_seqs / (graph_ms / 1e3),
               "algorithmic_bytes": nbytes, "num_seqs": wl.num_seqs,
-              "partition_size": part}
+              "partition_size": part, "kv_dtype": str(wl.kv.dtype).replace("torch.", "")}
     if name == "prefix":
         result["note"] = ("kv_read_gbps counts every sequence's prefix reads (logical bytes); "
                           "the 64 shared prefix blocks are read from L2 after the first touch")
@@ -429,11 +454,11 @@ def run_ours(args):
     slots = pkv.slot_mapping(wl.block_tables.cpu(), wl.new_positions.cpu(), wl.block_size).to(dev)
     out = torch.empty_like(wl.q)
     stream = torch.cuda.current_stream(dev)
+    write, decode = _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part)
 
     def step():
-        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
-        pkv.paged_attention_decode(wl.q, k_cache, v_cache, wl.block_tables, wl.context_lens,
-                                   wl.scale, out, max_context_len=maxl, partition_size=part)
+        write(wl.k_new, wl.v_new, slots)
+        decode(wl.q, wl.block_tables, wl.context_lens)
 
     for _ in range(args.warmup):
         step()
@@ -459,10 +484,9 @@ def run_ours(args):
     launches0 = pkv.launch_count()
     t_start.record(stream)
     for k in range(args.steps):
-        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
+        write(wl.k_new, wl.v_new, slots)
         dec_ev[k][0].record(stream)
-        pkv.paged_attention_decode(wl.q, k_cache, v_cache, wl.block_tables, wl.context_lens,
-                                   wl.scale, out, max_context_len=maxl, partition_size=part)
+        decode(wl.q, wl.block_tables, wl.context_lens)
         dec_ev[k][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -494,9 +518,8 @@ def run_ours(args):
         for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_bt, h_bt),
                      (d_cl, h_cl)):
             d.copy_(h, non_blocking=True)
-        pkv.reshape_and_cache(d_k, d_v, d_slots, k_cache, v_cache)
-        pkv.paged_attention_decode(d_q, k_cache, v_cache, d_bt, d_cl, wl.scale, out,
-                                   max_context_len=maxl, partition_size=part)
+        write(d_k, d_v, d_slots)
+        decode(d_q, d_bt, d_cl)
         h_out.copy_(out, non_blocking=True)
 
     e2e_steps = max(3, args.steps // 2)
@@ -540,7 +563,8 @@ def run_ours(args):
         line["cpu_baseline"] = cpu_baseline(wl)
     if world == 1 and not args.no_other_workloads:
         others = {}
-        for name in ("tiny", "mha7b", "gqa7b", "prefix", "long70b"):
+        for name in ("tiny", "mha7b", "gqa7b", "prefix", "long70b", "mha7b_int8", "gqa7b_int8",
+                     "long70b_int8"):
             if name == args.workload:
                 continue
             others[name] = measure_workload(pkv, name, dev, 300, peak)

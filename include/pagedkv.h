@@ -65,7 +65,9 @@ typedef enum pkv_status {
     PKV_ERR_OUT_OF_BLOCKS = 6  /* block manager: the free pool cannot cover the request */
 } pkv_status;
 
-typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+/* PKV_INT8 names an INT8 cache; only pkv_copy_blocks takes it as `dtype` (the
+ * INT8 entry points below take the query / new-row dtype, fp16 or bf16). */
+typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1, PKV_INT8 = 2 } pkv_dtype;
 
 /* Flags of the device status word (bitwise OR of what the kernels saw). */
 #define PKV_DEVERR_SLOT        0x1u  /* slot_mapping entry >= num_blocks*block_size  */
@@ -144,7 +146,8 @@ PKV_API pkv_status pkv_paged_attention_decode(
 /*
  * pkv_copy_blocks -- copy-on-write block copies (P1 §8.3; P3 §2.3 and §5.5).
  * For each pair p, the K half and the V half of block src_dst_pairs[2p] are
- * copied bit-exactly over those of block src_dst_pairs[2p+1].
+ * copied bit-exactly over those of block src_dst_pairs[2p+1].  dtype is the
+ * cache's: PKV_F16, PKV_BF16 or PKV_INT8.
  *
  *   src_dst_pairs  [num_pairs][2] int64, device.  Destinations must be
  *                  distinct and must not also appear as sources (otherwise the
@@ -157,6 +160,58 @@ PKV_API pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blo
                                    int64_t block_stride_elems, int num_kv_heads, int head_dim,
                                    int block_size, const int64_t *src_dst_pairs,
                                    int64_t num_pairs, pkv_dtype dtype, void *stream);
+
+/* ------------------------------------------------------------------------
+ * INT8 KV cache with per-channel scales (P2 §5.2: storing the cache in INT8
+ * halves its bytes, and with it the bytes a decode step reads; per-channel
+ * scales, computed separately for K and V, are the variant that page
+ * recommends).  The pool keeps the layout above with one signed byte per
+ * element: [num_blocks][2][num_kv_heads][block_size][head_dim] int8, block
+ * strides and offsets counted in elements (= bytes) and a multiple of 16.
+ * Scales are caller-owned device arrays k_scale, v_scale of
+ * [num_kv_heads][head_dim] fp32, each > 0 and finite (calibrated offline;
+ * the library never changes them), 16-byte aligned.
+ * A value x (fp16 / bf16) of KV head h, channel c is stored as
+ *     code = round_half_even(clamp(x / s[h][c], -127, 127))
+ * with the division in IEEE single precision (a NaN input stores -127), and
+ * read back as code * s[h][c].
+ * ------------------------------------------------------------------------ */
+
+/*
+ * pkv_reshape_and_cache_int8 -- pkv_reshape_and_cache into an INT8 cache:
+ * each element of the new rows k_new / v_new ([num_tokens][num_kv_heads]
+ * [head_dim], dtype = fp16 or bf16) is quantised with its channel's scale and
+ * stored at its slot.  Slot rules and errors as pkv_reshape_and_cache.
+ */
+PKV_API pkv_status pkv_reshape_and_cache_int8(const void *k_new, const void *v_new,
+                                              const int64_t *slot_mapping, int64_t num_tokens,
+                                              int8_t *k_cache, int8_t *v_cache, int64_t num_blocks,
+                                              int64_t block_stride_elems, int num_kv_heads,
+                                              int head_dim, int block_size, const float *k_scale,
+                                              const float *v_scale, pkv_dtype dtype, void *stream);
+
+/* Workspace of pkv_paged_attention_decode_int8 (same contract as
+ * pkv_decode_workspace_bytes). */
+PKV_API size_t pkv_decode_int8_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                               int head_dim, int block_size, int max_context_len,
+                                               int partition_size);
+
+/*
+ * pkv_paged_attention_decode_int8 -- pkv_paged_attention_decode over an INT8
+ * cache: the same softmax attention with K_i[t][c] = code * k_scale[h][c] and
+ * V_i[t][c] = code * v_scale[h][c].  q and out are `dtype` (fp16 or bf16);
+ * accumulation is fp32.  The K scales are folded into the query and the V
+ * scales applied once per output channel, so the kernel reads only the codes.
+ * Every other argument, the partitioning and the errors are those of
+ * pkv_paged_attention_decode (runs on the CUDA cores for every shape).
+ */
+PKV_API pkv_status pkv_paged_attention_decode_int8(
+    const void *q, const int8_t *k_cache, const int8_t *v_cache, const float *k_scale,
+    const float *v_scale, int64_t num_blocks, int64_t block_stride_elems,
+    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+    int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, float scale, void *out, void *workspace, size_t workspace_bytes,
+    int partition_size, pkv_dtype dtype, void *stream);
 
 /*
  * pkv_shared_prefix_workspace_bytes -- workspace of

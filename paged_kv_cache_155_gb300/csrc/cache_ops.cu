@@ -1,10 +1,14 @@
-// cache_ops.cu -- the two byte-moving ops of the paged KV cache:
+// cache_ops.cu -- the cache-side ops of the paged KV cache:
 //   pkv_reshape_and_cache: scatter each new token's K/V rows into its slot
 //     ("KV Cache与PagedAttention深度解析" §2.2 append step, §5.3 slot rule);
+//   pkv_reshape_and_cache_int8: the same placement into an INT8 cache, each
+//     value quantised with its channel's scale ("KV Cache从原理到实战" §5.2);
 //   pkv_copy_blocks: copy-on-write copies of whole blocks (same page §8.3;
 //     zwxr.cn nano-vllm article §2.3, §5.5).
-// Both move 16-byte vectors and are bit-exact.  Device-resident indices are
-// range-checked before use; a bad one raises a status flag and is skipped.
+// The 16-bit write and the copy move 16-byte vectors and are bit-exact; the
+// INT8 write's codes are those of the quantiser in pkv_device.cuh.
+// Device-resident indices are range-checked before use; a bad one raises a
+// status flag and is skipped.
 #include "pkv_device.cuh"
 #include "pkv_host.h"
 
@@ -36,6 +40,49 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
         const uint4 vv = v_new[n * per_token + i];
         *reinterpret_cast<uint4 *>(k_cache + dst) = kv;
         *reinterpret_cast<uint4 *>(v_cache + dst) = vv;
+    }
+}
+
+// INT8 cache write ("KV Cache从原理到实战" §5.2, per-channel scales): one CTA
+// per new token; a thread quantises 8 channels of one head of K and of V
+// (one 16-byte input vector -> 8 codes) with those channels' scales.
+template <typename T>
+__global__ void __launch_bounds__(256) reshape_and_cache_int8_kernel(
+    const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+    const int64_t *__restrict__ slot_mapping, int8_t *__restrict__ k_cache,
+    int8_t *__restrict__ v_cache, const float *__restrict__ k_scale,
+    const float *__restrict__ v_scale, int64_t num_slots, int64_t block_stride, int num_kv_heads,
+    int head_dim, int block_size, unsigned int *status) {
+    const int64_t n = blockIdx.x;
+    const int64_t slot = slot_mapping[n];
+    if (slot < 0) return;  // padding token
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0) pkv::raise_flag(status, PKV_DEVERR_SLOT);
+        return;
+    }
+    const int64_t blk = slot / block_size;
+    const int off = static_cast<int>(slot % block_size);
+    const int chunks = head_dim / 8;
+    const int per_token = num_kv_heads * chunks;
+    for (int i = threadIdx.x; i < per_token; i += blockDim.x) {
+        const int h = i / chunks;
+        const int c = i - h * chunks;
+        const int64_t dst = blk * block_stride + (static_cast<int64_t>(h) * block_size + off) * head_dim + c * 8;
+        const int sc = h * head_dim + c * 8;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const uint4 x = (half ? v_new : k_new)[n * per_token + i];
+            const float4 *s4 = reinterpret_cast<const float4 *>((half ? v_scale : k_scale) + sc);
+            const float4 sa = s4[0], sb = s4[1];
+            const float s[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+            float f[8];
+            pkv::Elem<T>::to_f32x8(x, f);
+            uint32_t w[2] = {0u, 0u};
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                w[e / 4] |= (static_cast<uint32_t>(pkv::quantize_int8(f[e], s[e])) & 0xffu) << (8 * (e % 4));
+            *reinterpret_cast<uint2 *>((half ? v_cache : k_cache) + dst) = make_uint2(w[0], w[1]);
+        }
     }
 }
 
@@ -113,16 +160,57 @@ PKV_API pkv_status pkv_reshape_and_cache(const void *k_new, const void *v_new,
     return pkv::launch_status();
 }
 
+PKV_API pkv_status pkv_reshape_and_cache_int8(const void *k_new, const void *v_new,
+                                              const int64_t *slot_mapping, int64_t num_tokens,
+                                              int8_t *k_cache, int8_t *v_cache, int64_t num_blocks,
+                                              int64_t block_stride_elems, int num_kv_heads,
+                                              int head_dim, int block_size, const float *k_scale,
+                                              const float *v_scale, pkv_dtype dtype, void *stream) {
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (!supported_shape(head_dim, block_size)) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
+    const int64_t half_elems = static_cast<int64_t>(num_kv_heads) * block_size * head_dim;
+    if (block_stride_elems < half_elems || block_stride_elems % 16) return PKV_ERR_INVALID_ARG;
+    if (!k_cache || !v_cache || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache))
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_scale || !v_scale || !pkv::aligned16(k_new) ||
+        !pkv::aligned16(v_new) || !pkv::aligned16(k_scale) || !pkv::aligned16(v_scale) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PKV_ERR_INVALID_ARG;
+    unsigned int *status = pkv::status_word_ptr();
+    if (!status) return PKV_ERR_CUDA;
+    const int per_token = num_kv_heads * (head_dim / 8);
+    const int threads = per_token < 256 ? ((per_token + 31) / 32) * 32 : 256;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const unsigned grid = static_cast<unsigned>(num_tokens);
+    if (dtype == PKV_F16)
+        reshape_and_cache_int8_kernel<__half><<<grid, threads, 0, s>>>(
+            static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping,
+            k_cache, v_cache, k_scale, v_scale, num_blocks * block_size, block_stride_elems,
+            num_kv_heads, head_dim, block_size, status);
+    else
+        reshape_and_cache_int8_kernel<__nv_bfloat16><<<grid, threads, 0, s>>>(
+            static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping,
+            k_cache, v_cache, k_scale, v_scale, num_blocks * block_size, block_stride_elems,
+            num_kv_heads, head_dim, block_size, status);
+    pkv::count_launch();
+    return pkv::launch_status();
+}
+
 PKV_API pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blocks,
                                    int64_t block_stride_elems, int num_kv_heads, int head_dim,
                                    int block_size, const int64_t *src_dst_pairs,
                                    int64_t num_pairs, pkv_dtype dtype, void *stream) {
-    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+    if (dtype != PKV_F16 && dtype != PKV_BF16 && dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
     if (!supported_shape(head_dim, block_size)) return PKV_ERR_UNSUPPORTED;
     if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
     if (num_pairs > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
+    const int elem_bytes = dtype == PKV_INT8 ? 1 : 2;
     const int64_t half_elems = static_cast<int64_t>(num_kv_heads) * block_size * head_dim;
-    if (block_stride_elems < half_elems || block_stride_elems % 8) return PKV_ERR_INVALID_ARG;
+    if (block_stride_elems < half_elems || (block_stride_elems * elem_bytes) % 16)
+        return PKV_ERR_INVALID_ARG;
     if (!k_cache || !v_cache || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache))
         return PKV_ERR_INVALID_ARG;
     if (num_pairs == 0) return PKV_OK;
@@ -130,13 +218,13 @@ PKV_API pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blo
         return PKV_ERR_INVALID_ARG;
     unsigned int *status = pkv::status_word_ptr();
     if (!status) return PKV_ERR_CUDA;
-    const int64_t slice_vecs = half_elems * 2 / 16;
+    const int64_t slice_vecs = half_elems * elem_bytes / 16;
     const int64_t chunks = (slice_vecs + kCopyThreads * kCopyUnroll - 1) / (kCopyThreads * kCopyUnroll);
     if (chunks > 65535) return PKV_ERR_INVALID_ARG;
     dim3 grid(static_cast<unsigned>(num_pairs), static_cast<unsigned>(chunks), 2);
     copy_blocks_kernel<<<grid, kCopyThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<char *>(k_cache), static_cast<char *>(v_cache), num_blocks,
-        block_stride_elems * 2, slice_vecs, src_dst_pairs, status);
+        block_stride_elems * elem_bytes, slice_vecs, src_dst_pairs, status);
     pkv::count_launch();
     return pkv::launch_status();
 }

@@ -74,15 +74,12 @@ bool encode_half_map(CUtensorMap *map, const void *base, int64_t num_blocks,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-extern "C" {
-
-PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads,
-                                   int head_dim, int block_size, int max_context_len,
-                                   int partition_size, int sm_count, int *out_partition_size,
-                                   int *out_num_partitions, int *out_heads_per_block,
-                                   int *out_needs_merge) {
+// The launch plan of a decode call; allow_tc = false keeps it on the CUDA-core
+// kernel (the INT8 cache has no tensor-core kernel).
+pkv_status plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int max_context_len, int partition_size, int sm_count,
+                       bool allow_tc, int *out_partition_size, int *out_num_partitions,
+                       int *out_heads_per_block, int *out_needs_merge) {
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
@@ -93,7 +90,7 @@ PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_hea
     const int max_partition = pkv::DecodeGeom<128, 16>::kMaxTableEntries * block_size;
     if (partition_size > max_partition) return PKV_ERR_INVALID_ARG;
     const int group = num_q_heads / num_kv_heads;
-    const bool tc = use_tensor_cores(head_dim, group, max_context_len);
+    const bool tc = allow_tc && use_tensor_cores(head_dim, group, max_context_len);
     const int gh = tc ? group : heads_per_block_for(group);
     const int64_t grid_y = static_cast<int64_t>(num_kv_heads) * (group / gh);
     if (grid_y > 65535 || num_seqs > 65535) return PKV_ERR_INVALID_ARG;
@@ -129,25 +126,28 @@ PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_hea
     return PKV_OK;
 }
 
-PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
-                                          int head_dim, int block_size, int max_context_len,
-                                          int partition_size) {
+size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, int max_context_len, int partition_size,
+                              bool allow_tc) {
     const int sm = partition_size > 0 ? 1 : pkv::current_sm_count();
     if (sm <= 0) return static_cast<size_t>(-1);
     int part = 0, nparts = 0, gh = 0, merge = 0;
-    if (pkv_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                        max_context_len, partition_size, sm, &part, &nparts, &gh,
-                        &merge) != PKV_OK)
+    if (plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                    partition_size, sm, allow_tc, &part, &nparts, &gh, &merge) != PKV_OK)
         return static_cast<size_t>(-1);
     return workspace_for(num_seqs, num_q_heads, head_dim, nparts);
 }
 
-PKV_API pkv_status pkv_paged_attention_decode(
-    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
-    int64_t block_stride_elems, const int32_t *block_tables, int max_blocks_per_seq,
-    const int32_t *context_lens, int max_context_len, int num_seqs, int num_q_heads,
-    int num_kv_heads, int head_dim, int block_size, float scale, void *out, void *workspace,
-    size_t workspace_bytes, int partition_size, pkv_dtype dtype, void *stream) {
+// Decode over a 16-bit cache (k_scale == v_scale == nullptr) or an INT8 cache
+// with per-channel scales.  Element strides and offsets count cache elements.
+pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
+                       const float *k_scale, const float *v_scale, bool int8_kv,
+                       int64_t num_blocks, int64_t block_stride_elems,
+                       const int32_t *block_tables, int max_blocks_per_seq,
+                       const int32_t *context_lens, int max_context_len, int num_seqs,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       float scale, void *out, void *workspace, size_t workspace_bytes,
+                       int partition_size, pkv_dtype dtype, void *stream) {
     if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
@@ -157,8 +157,12 @@ PKV_API pkv_status pkv_paged_attention_decode(
         !std::isfinite(scale))
         return PKV_ERR_INVALID_ARG;
     const int64_t half_elems = static_cast<int64_t>(num_kv_heads) * block_size * head_dim;
-    if (block_stride_elems < half_elems || block_stride_elems % 8) return PKV_ERR_INVALID_ARG;
+    // block starts 16-byte aligned: 8 16-bit elements or 16 INT8 codes
+    if (block_stride_elems < half_elems || block_stride_elems % (int8_kv ? 16 : 8))
+        return PKV_ERR_INVALID_ARG;
     if (!k_cache || !v_cache || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache))
+        return PKV_ERR_INVALID_ARG;
+    if (int8_kv && (!k_scale || !v_scale || !pkv::aligned16(k_scale) || !pkv::aligned16(v_scale)))
         return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
     if (!q || !out || !block_tables || !context_lens || !pkv::aligned16(q) || !pkv::aligned16(out))
@@ -166,15 +170,15 @@ PKV_API pkv_status pkv_paged_attention_decode(
 
     int part = 0, nparts = 0, gh = 0, merge = 0;
     // Validate the shape first (no CUDA call), then plan for the real SM count.
-    pkv_status plan = pkv_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                      max_context_len, partition_size, 1, &part, &nparts, &gh,
-                                      &merge);
+    pkv_status plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                  max_context_len, partition_size, 1, !int8_kv, &part, &nparts,
+                                  &gh, &merge);
     if (plan != PKV_OK) return plan;
     if (partition_size == 0) {
         const int sm = pkv::current_sm_count();
         if (sm <= 0) return PKV_ERR_CUDA;
-        plan = pkv_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                               max_context_len, 0, sm, &part, &nparts, &gh, &merge);
+        plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_context_len, 0, sm, !int8_kv, &part, &nparts, &gh, &merge);
         if (plan != PKV_OK) return plan;
     }
     const size_t need = workspace_for(num_seqs, num_q_heads, head_dim, nparts);
@@ -184,12 +188,14 @@ PKV_API pkv_status pkv_paged_attention_decode(
     if (!status) return PKV_ERR_CUDA;
 
     const int group = num_q_heads / num_kv_heads;
-    const bool tc = use_tensor_cores(head_dim, group, max_context_len);
+    const bool tc = !int8_kv && use_tensor_cores(head_dim, group, max_context_len);
     if (tc && num_blocks > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
     pkv::DecodeParams p{};
     p.q = q;
     p.k_cache = k_cache;
     p.v_cache = v_cache;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
     p.out = out;
     const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * nparts;
     p.ws_o = need ? static_cast<float *>(workspace) : nullptr;
@@ -230,9 +236,66 @@ PKV_API pkv_status pkv_paged_attention_decode(
     }
     const dim3 grid(static_cast<unsigned>(nparts), static_cast<unsigned>(num_kv_heads * p.subgroups),
                     static_cast<unsigned>(num_seqs));
+    if (int8_kv)
+        return dtype == PKV_F16
+                   ? pkv::launch_decode_i8_f16(p, head_dim, block_size, gh, grid, merge_rows, s)
+                   : pkv::launch_decode_i8_bf16(p, head_dim, block_size, gh, grid, merge_rows, s);
     return dtype == PKV_F16
                ? pkv::launch_decode_f16(p, head_dim, block_size, gh, grid, merge_rows, s)
                : pkv::launch_decode_bf16(p, head_dim, block_size, gh, grid, merge_rows, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int max_context_len,
+                                   int partition_size, int sm_count, int *out_partition_size,
+                                   int *out_num_partitions, int *out_heads_per_block,
+                                   int *out_needs_merge) {
+    return plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       max_context_len, partition_size, sm_count, true, out_partition_size,
+                       out_num_partitions, out_heads_per_block, out_needs_merge);
+}
+
+PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int block_size, int max_context_len,
+                                          int partition_size) {
+    return decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                  max_context_len, partition_size, true);
+}
+
+PKV_API pkv_status pkv_paged_attention_decode(
+    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+    int64_t block_stride_elems, const int32_t *block_tables, int max_blocks_per_seq,
+    const int32_t *context_lens, int max_context_len, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, float scale, void *out, void *workspace,
+    size_t workspace_bytes, int partition_size, pkv_dtype dtype, void *stream) {
+    return decode_impl(q, k_cache, v_cache, nullptr, nullptr, false, num_blocks,
+                       block_stride_elems, block_tables, max_blocks_per_seq, context_lens,
+                       max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       scale, out, workspace, workspace_bytes, partition_size, dtype, stream);
+}
+
+PKV_API size_t pkv_decode_int8_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                               int head_dim, int block_size, int max_context_len,
+                                               int partition_size) {
+    return decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                  max_context_len, partition_size, false);
+}
+
+PKV_API pkv_status pkv_paged_attention_decode_int8(
+    const void *q, const int8_t *k_cache, const int8_t *v_cache, const float *k_scale,
+    const float *v_scale, int64_t num_blocks, int64_t block_stride_elems,
+    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+    int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, float scale, void *out, void *workspace, size_t workspace_bytes,
+    int partition_size, pkv_dtype dtype, void *stream) {
+    return decode_impl(q, k_cache, v_cache, k_scale, v_scale, true, num_blocks,
+                       block_stride_elems, block_tables, max_blocks_per_seq, context_lens,
+                       max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       scale, out, workspace, workspace_bytes, partition_size, dtype, stream);
 }
 
 }  // extern "C"

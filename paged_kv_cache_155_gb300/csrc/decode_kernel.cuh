@@ -27,6 +27,12 @@
 //    read from HBM once per group, not once per query head.
 //  * The chunk-to-warp assignment and every merge are fixed by logical token
 //    position, so the output does not depend on the physical placement.
+//  * INT8 cache ("KV Cache从原理到实战" §5.2, per-channel scales): the storage
+//    type KT is int8_t and each lane reads 8 codes (8 bytes) per row, keeping
+//    the lane layout and registers of the 16-bit case.  The per-channel K
+//    scale is folded into the fp32 query once (s_t = sum_j (q_j k_scale_j)
+//    code_j) and the V scale multiplies each output channel once at the end,
+//    so the inner loop only widens codes to fp32.
 #pragma once
 
 #include "pkv_device.cuh"
@@ -41,6 +47,8 @@ struct DecodeParams {
     float *ws_o;  // [num_seqs][num_q_heads][num_partitions][head_dim]
     float *ws_m;  // [num_seqs][num_q_heads][num_partitions] (log2 units)
     float *ws_l;  // [num_seqs][num_q_heads][num_partitions]
+    const float *k_scale;  // INT8 cache: [num_kv_heads][head_dim] per-channel scales
+    const float *v_scale;
     const int32_t *block_tables;
     const int32_t *context_lens;
     unsigned int *status;
@@ -73,16 +81,17 @@ __device__ __forceinline__ int partitions_of(const DecodeParams &p, int len) {
     return span > 0 ? (span + p.partition_size - 1) / p.partition_size : 1;
 }
 
-// Decode-kernel geometry for one (head_dim, block_size) pair.
-template <int D, int BS>
+// Decode-kernel geometry for one (head_dim, block_size, cache element bytes).
+template <int D, int BS, int EB = 2>
 struct DecodeGeom {
     static constexpr int kWarps = 4;
-    static constexpr int kTile = BS < 16 ? BS : 16;      // tokens per stage
-    static constexpr int kVec = 8;                       // 16-bit values per 16-byte vector
+    static constexpr int kMaxTile = 32 / EB;             // 4 KiB K tiles at head_dim 128
+    static constexpr int kTile = BS < kMaxTile ? BS : kMaxTile;  // tokens per stage
+    static constexpr int kVec = 8;                       // values per lane vector (8 * EB bytes)
     static constexpr int kLanesPerToken = D / kVec;      // LPT
     static constexpr int kTokenGroups = 32 / kLanesPerToken;  // TPG
     static constexpr int kIters = kTile / kTokenGroups;  // token rows per lane per stage
-    static constexpr int kTileBytes = kTile * D * 2;     // one K (or V) tile
+    static constexpr int kTileBytes = kTile * D * EB;    // one K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kStagesRaw = 24576 / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
@@ -92,9 +101,12 @@ struct DecodeGeom {
     static_assert(kIters >= 1, "tile smaller than a warp's token groups");
 };
 
-template <typename T, int D, int BS, int GH>
+// T: query / output type; KT: cache storage type (T, or int8_t for the INT8 cache).
+template <typename T, typename KT, int D, int BS, int GH>
 __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams p) {
-    using G = DecodeGeom<D, BS>;
+    constexpr bool kQuant = sizeof(KT) == 1;
+    using G = DecodeGeom<D, BS, sizeof(KT)>;
+    using KVec = typename Elem<KT>::Vec;
     constexpr int NW = G::kWarps, S = G::kStages, TILE = G::kTile, LPT = G::kLanesPerToken,
                   TPG = G::kTokenGroups, ITERS = G::kIters;
     // token rows processed between two online-softmax updates (bounds registers)
@@ -146,8 +158,8 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
     }
     __syncthreads();
 
-    const T *kc = static_cast<const T *>(p.k_cache);
-    const T *vc = static_cast<const T *>(p.v_cache);
+    const KT *kc = static_cast<const KT *>(p.k_cache);
+    const KT *vc = static_cast<const KT *>(p.v_cache);
     unsigned char *my_stages = stages + warp * S * G::kStageBytes;
     uint64_t *my_bars = bars + warp * S;
     const uint64_t policy = l2_policy_evict_first();
@@ -188,6 +200,15 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
 #pragma unroll
             for (int e = 0; e < 8; ++e) qf[g][e] *= p.scale_log2;
         }
+        if constexpr (kQuant) {  // K dequantisation folded into the query
+            const float4 *ks = reinterpret_cast<const float4 *>(p.k_scale + kvh * D + sub * 8);
+            const float4 a = ks[0], b = ks[1];
+            const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int g = 0; g < GH; ++g)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) qf[g][e] *= f[e];
+        }
     }
     float acc[GH][8];
     float m[GH], l[GH];
@@ -218,8 +239,8 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
         const int c = warp + i * NW;
         const int valid = min(TILE, ntok - c * TILE);  // >= 1
         if (tbl[(c * TILE) / BS] >= 0) {
-            const T *ks = reinterpret_cast<const T *>(my_stages + s * G::kStageBytes);
-            const T *vs = ks + TILE * D;
+            const KT *ks = reinterpret_cast<const KT *>(my_stages + s * G::kStageBytes);
+            const KT *vs = ks + TILE * D;
 #pragma unroll
             for (int it0 = 0; it0 < ITERS; it0 += IT_STEP) {
                 // QK: partial dot products over this lane's 8 dims
@@ -227,9 +248,9 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
 #pragma unroll
                 for (int it = 0; it < IT_STEP; ++it) {
                     const int t = (it0 + it) * TPG + grp;
-                    const uint4 u = *reinterpret_cast<const uint4 *>(ks + t * D + sub * 8);
+                    const KVec u = *reinterpret_cast<const KVec *>(ks + t * D + sub * 8);
                     float kf[8];
-                    Elem<T>::to_f32x8(u, kf);
+                    Elem<KT>::to_f32x8(u, kf);
 #pragma unroll
                     for (int g = 0; g < GH; ++g) {
                         float a = 0.f;
@@ -282,9 +303,9 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                 for (int it = 0; it < IT_STEP; ++it) {
                     const int t = (it0 + it) * TPG + grp;
                     if (t < valid) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(vs + t * D + sub * 8);
+                        const KVec u = *reinterpret_cast<const KVec *>(vs + t * D + sub * 8);
                         float vf[8];
-                        Elem<T>::to_f32x8(u, vf);
+                        Elem<KT>::to_f32x8(u, vf);
 #pragma unroll
                         for (int g = 0; g < GH; ++g)
 #pragma unroll
@@ -358,6 +379,7 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
             lsum += wgt * src[g * (D + 4) + D + 1];
             osum += wgt * src[g * (D + 4) + j];
         }
+        if constexpr (kQuant) osum *= p.v_scale[kvh * D + j];  // V dequantisation
         const int hq = hq0 + g;
         const int64_t row = static_cast<int64_t>(seq) * p.num_q_heads + hq;
         if (single) {

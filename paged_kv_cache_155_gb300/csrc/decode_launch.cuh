@@ -13,48 +13,49 @@
 
 namespace pkv {
 
-template <typename T, int D, int BS, int GH>
+template <typename T, typename KT, int D, int BS, int GH>
 pkv_status launch_decode_one(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
-    using G = DecodeGeom<D, BS>;
+    using G = DecodeGeom<D, BS, sizeof(KT)>;
     static std::atomic<uint64_t> configured_devices{0};  // bit per device ordinal
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
     if (!bit || !(configured_devices.load(std::memory_order_acquire) & bit)) {
-        if (cudaFuncSetAttribute(paged_decode_kernel<T, D, BS, GH>,
+        if (cudaFuncSetAttribute(paged_decode_kernel<T, KT, D, BS, GH>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  G::kSmemBytes) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured_devices.fetch_or(bit, std::memory_order_acq_rel);
     }
-    paged_decode_kernel<T, D, BS, GH><<<grid, G::kWarps * 32, G::kSmemBytes, stream>>>(p);
+    paged_decode_kernel<T, KT, D, BS, GH><<<grid, G::kWarps * 32, G::kSmemBytes, stream>>>(p);
     count_launch();
     return launch_status();
 }
 
-template <typename T, int D, int BS>
+template <typename T, typename KT, int D, int BS>
 pkv_status launch_decode_gh(const DecodeParams &p, int gh, dim3 grid, cudaStream_t s) {
     switch (gh) {
-        case 1: return launch_decode_one<T, D, BS, 1>(p, grid, s);
-        case 2: return launch_decode_one<T, D, BS, 2>(p, grid, s);
-        case 4: return launch_decode_one<T, D, BS, 4>(p, grid, s);
-        case 8: return launch_decode_one<T, D, BS, 8>(p, grid, s);
+        case 1: return launch_decode_one<T, KT, D, BS, 1>(p, grid, s);
+        case 2: return launch_decode_one<T, KT, D, BS, 2>(p, grid, s);
+        case 4: return launch_decode_one<T, KT, D, BS, 4>(p, grid, s);
+        case 8: return launch_decode_one<T, KT, D, BS, 8>(p, grid, s);
     }
     return PKV_ERR_UNSUPPORTED;
 }
 
-template <typename T>
+// T: query / output type; KT: cache storage type (T, or int8_t).
+template <typename T, typename KT = T>
 pkv_status launch_decode_typed(const DecodeParams &p, int head_dim, int block_size, int gh,
                                dim3 grid, int merge_rows, cudaStream_t s) {
     pkv_status st = PKV_ERR_UNSUPPORTED;
     if (head_dim == 128) {
-        if (block_size == 8) st = launch_decode_gh<T, 128, 8>(p, gh, grid, s);
-        else if (block_size == 16) st = launch_decode_gh<T, 128, 16>(p, gh, grid, s);
-        else if (block_size == 32) st = launch_decode_gh<T, 128, 32>(p, gh, grid, s);
+        if (block_size == 8) st = launch_decode_gh<T, KT, 128, 8>(p, gh, grid, s);
+        else if (block_size == 16) st = launch_decode_gh<T, KT, 128, 16>(p, gh, grid, s);
+        else if (block_size == 32) st = launch_decode_gh<T, KT, 128, 32>(p, gh, grid, s);
     } else if (head_dim == 64) {
-        if (block_size == 8) st = launch_decode_gh<T, 64, 8>(p, gh, grid, s);
-        else if (block_size == 16) st = launch_decode_gh<T, 64, 16>(p, gh, grid, s);
-        else if (block_size == 32) st = launch_decode_gh<T, 64, 32>(p, gh, grid, s);
+        if (block_size == 8) st = launch_decode_gh<T, KT, 64, 8>(p, gh, grid, s);
+        else if (block_size == 16) st = launch_decode_gh<T, KT, 64, 16>(p, gh, grid, s);
+        else if (block_size == 32) st = launch_decode_gh<T, KT, 64, 32>(p, gh, grid, s);
     }
     if (st != PKV_OK || merge_rows == 0) return st;
     const unsigned blocks = static_cast<unsigned>((merge_rows + 3) / 4);
@@ -137,9 +138,14 @@ pkv_status launch_prefix_tc_typed(const PrefixParams &p, const CUtensorMap &tk,
     return PKV_ERR_UNSUPPORTED;
 }
 
-// Defined in decode_f16.cu / decode_bf16.cu.
+// Defined in decode_f16.cu / decode_bf16.cu (16-bit caches) and
+// decode_i8.cu (INT8 cache, fp16 or bf16 queries).
 pkv_status launch_decode_f16(const DecodeParams &p, int head_dim, int block_size, int gh,
                              dim3 grid, int merge_rows, cudaStream_t s);
+pkv_status launch_decode_i8_f16(const DecodeParams &p, int head_dim, int block_size, int gh,
+                                dim3 grid, int merge_rows, cudaStream_t s);
+pkv_status launch_decode_i8_bf16(const DecodeParams &p, int head_dim, int block_size, int gh,
+                                 dim3 grid, int merge_rows, cudaStream_t s);
 pkv_status launch_decode_bf16(const DecodeParams &p, int head_dim, int block_size, int gh,
                               dim3 grid, int merge_rows, cudaStream_t s);
 pkv_status launch_decode_tc_f16(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,

@@ -113,12 +113,13 @@ __device__ __forceinline__ void raise_flag(unsigned int *status, unsigned int fl
     atomicOr(status, flag);
 }
 
-// 16-bit element traits: eight packed values (one 16-byte vector) -> fp32.
+// Element traits: eight packed values (one Vec) -> fp32.
 template <typename T>
 struct Elem;
 
 template <>
 struct Elem<__half> {
+    using Vec = uint4;
     static __device__ __forceinline__ void to_f32x8(const uint4 &u, float f[8]) {
         const __half2 *h = reinterpret_cast<const __half2 *>(&u);
 #pragma unroll
@@ -133,6 +134,7 @@ struct Elem<__half> {
 
 template <>
 struct Elem<__nv_bfloat16> {
+    using Vec = uint4;
     // bf16 is the high half of an fp32 pattern: widening is a shift / mask.
     static __device__ __forceinline__ void to_f32x8(const uint4 &u, float f[8]) {
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -146,5 +148,35 @@ struct Elem<__nv_bfloat16> {
         return __float2bfloat16_rn(x);
     }
 };
+
+// INT8 codes of the quantised cache: eight codes (8 bytes) -> fp32, exactly.
+// Each code, biased by 128 into [1, 255], is placed in the low mantissa bits
+// of 2^23 (a byte permute) and the float 2^23 + 128 subtracted: two ALU ops
+// per value instead of a conversion-unit I2F.
+template <>
+struct Elem<int8_t> {
+    using Vec = uint2;
+    static __device__ __forceinline__ void to_f32x8(const uint2 &u, float f[8]) {
+        const uint32_t w[2] = {u.x ^ 0x80808080u, u.y ^ 0x80808080u};
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            f[4 * i + 0] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7440u)) - 8388736.f;
+            f[4 * i + 1] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7441u)) - 8388736.f;
+            f[4 * i + 2] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7442u)) - 8388736.f;
+            f[4 * i + 3] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7443u)) - 8388736.f;
+        }
+    }
+};
+
+// Per-channel INT8 quantiser ("KV Cache从原理到实战" §5.2): x / s in IEEE single
+// precision (correctly rounded division), clamped to [-127, 127] -- a NaN
+// quotient clamps to -127, since fmaxf returns the non-NaN operand -- then
+// rounded to the nearest integer, ties to even.
+__device__ __forceinline__ int quantize_int8(float x, float s) {
+    float r = __fdiv_rn(x, s);
+    r = fmaxf(r, -127.f);
+    r = fminf(r, 127.f);
+    return __float2int_rn(r);
+}
 
 }  // namespace pkv

@@ -19,7 +19,7 @@ import torch
 
 from ._lib import DEVERR, PagedKVError, lib
 
-F16, BF16 = 0, 1
+F16, BF16, INT8 = 0, 1, 2
 _workspaces = {}
 
 
@@ -38,6 +38,10 @@ def _stream(t: torch.Tensor):
 def _check(status: int, what: str):
     if status != 0:
         raise PagedKVError(what, status)
+
+
+def _cache_dtype_code(t: torch.Tensor) -> int:
+    return INT8 if t.dtype == torch.int8 else _dtype_code(t)
 
 
 def _cache_geometry(k_cache: torch.Tensor, v_cache: torch.Tensor):
@@ -203,8 +207,91 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: tor
         raise ValueError("src_dst_pairs must be on the device")
     st = lib().pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), nb, stride, hkv, d, bs,
                                src_dst_pairs.data_ptr(), int(src_dst_pairs.shape[0]),
-                               _dtype_code(k_cache), _stream(k_cache))
+                               _cache_dtype_code(k_cache), _stream(k_cache))
     _check(st, "pkv_copy_blocks")
+
+
+# ---------------------------------------------------------------------------
+# INT8 cache with per-channel scales ("KV Cache从原理到实战" §5.2)
+# ---------------------------------------------------------------------------
+
+def _check_int8_cache(k_cache, v_cache, k_scale, v_scale):
+    nb, hkv, bs, d, stride = _cache_geometry(k_cache, v_cache)
+    if k_cache.dtype != torch.int8:
+        raise ValueError("k_cache/v_cache must be int8")
+    for name, sc in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if sc.dtype != torch.float32 or sc.shape != (hkv, d) or not sc.is_contiguous() \
+                or sc.device != k_cache.device:
+            raise ValueError(f"{name} must be a contiguous float32 [{hkv}, {d}] on the cache's device")
+    return nb, hkv, bs, d, stride
+
+
+def reshape_and_cache_int8(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                           k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                           v_scale: torch.Tensor) -> None:
+    """Quantise new K/V rows [T, Hkv, d] (fp16/bf16) with per-channel scales [Hkv, d]
+    and write the codes into their slots of an INT8 cache; slot < 0 skips."""
+    nb, hkv, bs, d, stride = _check_int8_cache(k_cache, v_cache, k_scale, v_scale)
+    t = int(k_new.shape[0])
+    if k_new.shape != (t, hkv, d) or v_new.shape != k_new.shape or v_new.dtype != k_new.dtype:
+        raise ValueError(f"k_new/v_new must be [T, {hkv}, {d}] of one dtype")
+    if not (k_new.is_contiguous() and v_new.is_contiguous() and slot_mapping.is_contiguous()):
+        raise ValueError("k_new, v_new and slot_mapping must be contiguous")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != t:
+        raise ValueError("slot_mapping must be int64 [T]")
+    st = lib().pkv_reshape_and_cache_int8(
+        k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), t, k_cache.data_ptr(),
+        v_cache.data_ptr(), nb, stride, hkv, d, bs, k_scale.data_ptr(), v_scale.data_ptr(),
+        _dtype_code(k_new), _stream(k_cache))
+    _check(st, "pkv_reshape_and_cache_int8")
+
+
+def decode_int8_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                max_context_len, partition_size=0) -> int:
+    n = lib().pkv_decode_int8_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                              block_size, max_context_len, partition_size)
+    if n == ctypes.c_size_t(-1).value:
+        raise PagedKVError("pkv_decode_int8_workspace_bytes", 1)
+    return int(n)
+
+
+def paged_attention_decode_int8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                k_scale: torch.Tensor, v_scale: torch.Tensor,
+                                block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                                *, max_context_len: Optional[int] = None, partition_size: int = 0,
+                                workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """paged_attention_decode over an INT8 cache whose values are code * scale[h][channel];
+    q and out fp16 or bf16."""
+    nb, hkv, bs, d, stride = _check_int8_cache(k_cache, v_cache, k_scale, v_scale)
+    if q.dim() != 3 or q.shape[2] != d or not q.is_contiguous():
+        raise ValueError(f"q must be a contiguous [num_seqs, num_q_heads, {d}]")
+    b, hq = int(q.shape[0]), int(q.shape[1])
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != b \
+            or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be a contiguous int32 [num_seqs, max_blocks_per_seq]")
+    if context_lens.dtype != torch.int32 or context_lens.numel() != b or not context_lens.is_contiguous():
+        raise ValueError("context_lens must be a contiguous int32 [num_seqs]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if max_context_len is None:
+        max_context_len = int(context_lens.max().item()) if b else 0
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must match q")
+    need = decode_int8_workspace_bytes(b, hq, hkv, d, bs, max_context_len, partition_size)
+    if workspace is None:
+        workspace = _workspace(q.device, need)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().pkv_paged_attention_decode_int8(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
+        v_scale.data_ptr(), nb, stride, block_tables.data_ptr(), int(block_tables.shape[1]),
+        context_lens.data_ptr(), int(max_context_len), b, hq, hkv, d, bs, float(scale),
+        out.data_ptr(), ws_ptr, ws_bytes, int(partition_size), _dtype_code(q), _stream(q))
+    _check(st, "pkv_paged_attention_decode_int8")
+    return out
 
 
 def get_device_error(device: Optional[torch.device] = None) -> Tuple[int, list]:

@@ -22,6 +22,14 @@ The five named workloads follow the shapes the pages discuss:
   prefix  -- shared 2048-token prefix (64 blocks of 32) in every table plus a
              private suffix U[64, 1024]; bf16; 128 copy-on-write pairs.
   long70b -- Llama-2-70B-shaped GQA: 64 q / 8 kv heads, 16 sequences of 32768.
+
+INT8-cache variants (``kv_dtype=torch.int8``; "KV Cache从原理到实战" §5.2):
+the pool holds codes drawn as round(32 * N(0, 1)) clipped to [-127, 127] (the
+codes a Gaussian channel quantised with its maximum near 4 sigma would have),
+and every (KV head, channel) gets a K and a V scale sigma_c / 32 with
+sigma_c ~ U[0.5, 1.5], so dequantised values are N(0, sigma_c^2).  The new
+token's rows stay 16-bit (the cache write quantises them).  mha7b_int8,
+gqa7b_int8 and long70b_int8 are the named shapes above over such a pool.
 """
 from __future__ import annotations
 
@@ -52,6 +60,8 @@ class DecodeWorkload:
     v_new: torch.Tensor              # [B, Hkv, d]
     new_positions: torch.Tensor      # [B] int64 logical position of the new token (= len - 1)
     scale: float
+    k_scale: Optional[torch.Tensor] = None            # INT8 pool: [Hkv, d] float32
+    v_scale: Optional[torch.Tensor] = None
     cow_pairs: Optional[torch.Tensor] = None          # [n, 2] int64 (src, dst)
     block_tables_after_cow: Optional[torch.Tensor] = None
     shared_prefix_blocks: int = 0
@@ -76,7 +86,7 @@ class DecodeWorkload:
     def to(self, device) -> "DecodeWorkload":
         moved = {}
         for name in ("kv", "q", "block_tables", "context_lens", "k_new", "v_new",
-                     "new_positions", "cow_pairs", "block_tables_after_cow"):
+                     "new_positions", "k_scale", "v_scale", "cow_pairs", "block_tables_after_cow"):
             t = getattr(self, name)
             moved[name] = None if t is None else t.to(device)
         return DecodeWorkload(
@@ -97,7 +107,8 @@ def make_decode_workload(*, name: str = "custom", num_seqs: int, num_q_heads: in
                          dtype: torch.dtype = torch.float16, seed: int = 0,
                          device: str = "cpu", shared_prefix_tokens: int = 0,
                          fixed_tables: Optional[dict] = None, cow_last_prefix_block: bool = False,
-                         max_blocks_per_seq: Optional[int] = None) -> DecodeWorkload:
+                         max_blocks_per_seq: Optional[int] = None,
+                         kv_dtype: Optional[torch.dtype] = None) -> DecodeWorkload:
     """Build a seeded workload.
 
     ``context_lens`` are the per-sequence lengths (the new token included).
@@ -105,7 +116,9 @@ def make_decode_workload(*, name: str = "custom", num_seqs: int, num_q_heads: in
     starts with the same prefix blocks.  ``fixed_tables`` maps a sequence index
     to an explicit list of physical blocks.  ``cow_last_prefix_block`` adds one
     copy-on-write pair per sequence: the last shared prefix block to a fresh
-    private block, and the tables that point at the copies.
+    private block, and the tables that point at the copies.  ``kv_dtype=torch.int8``
+    draws an INT8 pool and per-channel scales (module docstring); ``dtype`` stays
+    the type of the queries and of the new rows.
     """
     lens = [int(x) for x in context_lens]
     assert len(lens) == num_seqs and num_q_heads % num_kv_heads == 0
@@ -156,7 +169,15 @@ def make_decode_workload(*, name: str = "custom", num_seqs: int, num_q_heads: in
         tables_after[:, prefix_blocks - 1] = torch.tensor(fresh, dtype=torch.int32)
 
     gen = torch.Generator(device=device).manual_seed(seed + 1)
-    kv = _randn((num_blocks, 2, num_kv_heads, bs, head_dim), dtype, gen, device)
+    k_scale = v_scale = None
+    if kv_dtype == torch.int8:
+        kv = torch.randn((num_blocks, 2, num_kv_heads, bs, head_dim), generator=gen,
+                         device=device).mul_(32).round_().clamp_(-127, 127).to(torch.int8)
+        sig = torch.rand((2, num_kv_heads, head_dim), generator=gen, device=device) + 0.5
+        k_scale, v_scale = (sig[0] / 32).contiguous(), (sig[1] / 32).contiguous()
+    else:
+        assert kv_dtype in (None, dtype)
+        kv = _randn((num_blocks, 2, num_kv_heads, bs, head_dim), dtype, gen, device)
     q = _randn((num_seqs, num_q_heads, head_dim), dtype, gen, device)
     k_new = _randn((num_seqs, num_kv_heads, head_dim), dtype, gen, device)
     v_new = _randn((num_seqs, num_kv_heads, head_dim), dtype, gen, device)
@@ -167,7 +188,7 @@ def make_decode_workload(*, name: str = "custom", num_seqs: int, num_q_heads: in
         num_kv_heads=num_kv_heads, head_dim=head_dim, block_size=bs, num_blocks=num_blocks,
         kv=kv, q=q, block_tables=tables.to(device), context_lens=ctx.to(device),
         k_new=k_new, v_new=v_new, new_positions=pos.to(device),
-        scale=1.0 / math.sqrt(head_dim),
+        scale=1.0 / math.sqrt(head_dim), k_scale=k_scale, v_scale=v_scale,
         cow_pairs=None if cow_pairs is None else cow_pairs.to(device),
         block_tables_after_cow=None if tables_after is None else tables_after.to(device),
         shared_prefix_blocks=prefix_blocks, meta={"seed": seed})
@@ -187,21 +208,23 @@ def tiny(device="cpu", seed=0):
         device=device, fixed_tables={2: WORKED_EXAMPLE_TABLE})
 
 
-def mha7b(device="cpu", seed=1, num_seqs=32, context_len=4096, num_blocks=None):
+def mha7b(device="cpu", seed=1, num_seqs=32, context_len=4096, num_blocks=None, kv_dtype=None):
     nb = num_blocks if num_blocks is not None else num_seqs * math.ceil(context_len / 16)
     return make_decode_workload(
-        name="mha7b", num_seqs=num_seqs, num_q_heads=32, num_kv_heads=32, head_dim=128,
-        block_size=16, context_lens=[context_len] * num_seqs, num_blocks=nb,
-        dtype=torch.float16, seed=seed, device=device)
+        name="mha7b" + ("_int8" if kv_dtype == torch.int8 else ""), num_seqs=num_seqs,
+        num_q_heads=32, num_kv_heads=32, head_dim=128, block_size=16,
+        context_lens=[context_len] * num_seqs, num_blocks=nb, dtype=torch.float16, seed=seed,
+        device=device, kv_dtype=kv_dtype)
 
 
-def gqa7b(device="cpu", seed=2, num_seqs=64, lo=128, hi=8192, num_blocks=32768):
+def gqa7b(device="cpu", seed=2, num_seqs=64, lo=128, hi=8192, num_blocks=32768, kv_dtype=None):
     lens = _uniform_lens(num_seqs, lo, hi, seed)
     nb = max(num_blocks, sum(math.ceil(n / 16) for n in lens))
     return make_decode_workload(
-        name="gqa7b", num_seqs=num_seqs, num_q_heads=32, num_kv_heads=8, head_dim=128,
-        block_size=16, context_lens=lens, num_blocks=nb, dtype=torch.float16, seed=seed,
-        device=device, max_blocks_per_seq=math.ceil(hi / 16))
+        name="gqa7b" + ("_int8" if kv_dtype == torch.int8 else ""), num_seqs=num_seqs,
+        num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16, context_lens=lens,
+        num_blocks=nb, dtype=torch.float16, seed=seed, device=device,
+        max_blocks_per_seq=math.ceil(hi / 16), kv_dtype=kv_dtype)
 
 
 def prefix(device="cpu", seed=3, num_seqs=128, prefix_tokens=2048, lo=64, hi=1024,
@@ -215,15 +238,31 @@ def prefix(device="cpu", seed=3, num_seqs=128, prefix_tokens=2048, lo=64, hi=102
         cow_last_prefix_block=True, max_blocks_per_seq=(prefix_tokens + hi + 31) // 32)
 
 
-def long70b(device="cpu", seed=4, num_seqs=16, context_len=32768, num_blocks=None):
+def long70b(device="cpu", seed=4, num_seqs=16, context_len=32768, num_blocks=None,
+            kv_dtype=None):
     nb = num_blocks if num_blocks is not None else num_seqs * math.ceil(context_len / 16)
     return make_decode_workload(
-        name="long70b", num_seqs=num_seqs, num_q_heads=64, num_kv_heads=8, head_dim=128,
-        block_size=16, context_lens=[context_len] * num_seqs, num_blocks=nb,
-        dtype=torch.bfloat16, seed=seed, device=device)
+        name="long70b" + ("_int8" if kv_dtype == torch.int8 else ""), num_seqs=num_seqs,
+        num_q_heads=64, num_kv_heads=8, head_dim=128, block_size=16,
+        context_lens=[context_len] * num_seqs, num_blocks=nb, dtype=torch.bfloat16, seed=seed,
+        device=device, kv_dtype=kv_dtype)
 
 
-NAMED = {"tiny": tiny, "mha7b": mha7b, "gqa7b": gqa7b, "prefix": prefix, "long70b": long70b}
+def mha7b_int8(device="cpu", seed=1, **kw):
+    return mha7b(device=device, seed=seed, kv_dtype=torch.int8, **kw)
+
+
+def gqa7b_int8(device="cpu", seed=2, **kw):
+    return gqa7b(device=device, seed=seed, kv_dtype=torch.int8, **kw)
+
+
+def long70b_int8(device="cpu", seed=4, **kw):
+    return long70b(device=device, seed=seed, kv_dtype=torch.int8, **kw)
+
+
+NAMED = {"tiny": tiny, "mha7b": mha7b, "gqa7b": gqa7b, "prefix": prefix, "long70b": long70b,
+         "mha7b_int8": mha7b_int8, "gqa7b_int8": gqa7b_int8, "long70b_int8": long70b_int8}
 
 # The default partition size each named workload is run with (0 = library's choice).
-DEFAULT_PARTITION = {"tiny": 0, "mha7b": 0, "gqa7b": 0, "prefix": 0, "long70b": 512}
+DEFAULT_PARTITION = {"tiny": 0, "mha7b": 0, "gqa7b": 0, "prefix": 0, "long70b": 512,
+                     "mha7b_int8": 0, "gqa7b_int8": 0, "long70b_int8": 0}

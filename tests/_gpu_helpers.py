@@ -70,3 +70,41 @@ def oracle_step_pool(wl_host_pool_bits, wl, tables=None):
     oracle.reshape_and_cache(to_bits(wl.k_new.cpu()), to_bits(wl.v_new.cpu()), slots,
                              wl_host_pool_bits, wl.num_kv_heads, wl.block_size, wl.head_dim)
     return slots
+
+
+# ---------------------------------------------------------------- INT8 cache
+def run_step_int8(wl, partition_size=0, tables=None):
+    """The library's decode step over an INT8 pool: quantising cache write of the
+    new token at position len-1, then paged decode.  Returns out (device)."""
+    k_cache, v_cache = pkv.split_pool(wl.kv)
+    bt = wl.block_tables if tables is None else tables
+    slots = pkv.slot_mapping(bt.cpu(), wl.new_positions.cpu(), wl.block_size).to(wl.kv.device)
+    pkv.reshape_and_cache_int8(wl.k_new, wl.v_new, slots, k_cache, v_cache, wl.k_scale,
+                               wl.v_scale)
+    return pkv.paged_attention_decode_int8(wl.q, k_cache, v_cache, wl.k_scale, wl.v_scale, bt,
+                                           wl.context_lens, wl.scale,
+                                           max_context_len=int(wl.context_lens.max().item()),
+                                           partition_size=partition_size)
+
+
+def oracle_step_pool_int8(pool_i8: np.ndarray, wl, tables=None):
+    """Oracle quantising cache write of the new tokens into a host INT8 pool copy."""
+    bt = (wl.block_tables if tables is None else tables).cpu().numpy()
+    slots = oracle.slot_mapping(bt, wl.new_positions.cpu().numpy(), wl.block_size)
+    oracle.reshape_and_cache_int8(to_bits(wl.k_new.cpu()), to_bits(wl.v_new.cpu()), slots,
+                                  pool_i8, wl.k_scale.cpu().numpy(), wl.v_scale.cpu().numpy(),
+                                  wl.num_kv_heads, wl.block_size, wl.head_dim,
+                                  dtype_code(wl.dtype))
+    return slots
+
+
+def oracle_decode_int8(wl, pool_i8, sel=None, tables=None):
+    """Oracle decode of (a subset of) a workload's sequences over a host INT8 pool."""
+    bt = (wl.block_tables if tables is None else tables).cpu().numpy()
+    q = to_bits(wl.q.cpu())
+    lens = wl.context_lens.cpu().numpy()
+    if sel is not None:
+        q, bt, lens = q[sel], bt[sel], lens[sel]
+    return oracle.paged_decode_int8(q, pool_i8, wl.k_scale.cpu().numpy(), wl.v_scale.cpu().numpy(),
+                                    bt, lens, wl.num_kv_heads, wl.block_size, wl.scale,
+                                    dtype_code(wl.dtype))

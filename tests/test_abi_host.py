@@ -106,6 +106,50 @@ def test_cache_ops_reject_bad_arguments_on_host(lib):
     assert lib.pkv_debug_wait_timeout(0, None) == INVALID
 
 
+def test_int8_entry_points_reject_bad_arguments_on_host(lib):
+    def dec(**kw):
+        a = dict(q=16, k=16, v=16, ks=16, vs=16, nb=64, stride=2 * 4 * 16 * 64, bt=16, mb=8, cl=16,
+                 maxl=100, b=4, hq=4, hkv=4, d=64, bs=16, scale=0.125, out=16, ws=None, wsb=0,
+                 part=0, dt=0)
+        a.update(kw)
+        return lib.pkv_paged_attention_decode_int8(
+            a["q"], a["k"], a["v"], a["ks"], a["vs"], a["nb"], a["stride"], a["bt"], a["mb"],
+            a["cl"], a["maxl"], a["b"], a["hq"], a["hkv"], a["d"], a["bs"], a["scale"], a["out"],
+            a["ws"], a["wsb"], a["part"], a["dt"], None)
+
+    assert dec(dt=2) == UNSUPPORTED                    # q is fp16 or bf16, not INT8
+    assert dec(d=96) == UNSUPPORTED
+    assert dec(ks=0) == INVALID                        # scales required
+    assert dec(vs=8) == INVALID                        # scales 16-byte aligned
+    assert dec(stride=2 * 4 * 16 * 64 + 8) == INVALID  # INT8 block stride: multiple of 16
+    assert dec(hq=6) == INVALID
+    assert dec(part=24) == INVALID
+    assert dec(b=0) == 0                               # empty batch: nothing to do
+
+    def rc(**kw):
+        a = dict(kn=16, vn=16, sm=16, t=4, kc=16, vc=16, nb=8, stride=2 * 2 * 16 * 64, hkv=2, d=64,
+                 bs=16, ks=16, vs=16, dt=0)
+        a.update(kw)
+        return lib.pkv_reshape_and_cache_int8(a["kn"], a["vn"], a["sm"], a["t"], a["kc"], a["vc"],
+                                              a["nb"], a["stride"], a["hkv"], a["d"], a["bs"],
+                                              a["ks"], a["vs"], a["dt"], None)
+
+    assert rc(dt=2) == UNSUPPORTED                     # the new rows are fp16 or bf16
+    assert rc(d=80) == UNSUPPORTED
+    assert rc(ks=0) == INVALID
+    assert rc(vs=4) == INVALID
+    assert rc(stride=2 * 2 * 16 * 64 + 8) == INVALID
+    assert rc(t=0, kn=0, vn=0, sm=0, ks=0, vs=0) == 0  # empty: no-op
+    c = lib.pkv_copy_blocks
+    assert c(16, 16, 8, 2 * 2 * 16 * 64, 2, 64, 16, 0, 0, 2, None) == 0          # INT8, empty
+    assert c(16, 16, 8, 2 * 2 * 16 * 64 + 8, 2, 64, 16, 16, 1, 2, None) == INVALID  # 8-byte stride
+    assert c(16, 16, 8, 2 * 2 * 16 * 64, 2, 64, 16, 16, 1, 3, None) == UNSUPPORTED
+    # explicit partitions: the INT8 workspace is partials of (d + 2) floats per slot
+    ws = lib.pkv_decode_int8_workspace_bytes(4, 32, 8, 128, 16, 4096, 512)
+    assert ws == 4 * 32 * 8 * (128 + 2) * 4
+    assert lib.pkv_decode_int8_workspace_bytes(4, 32, 8, 128, 16, 500, 512) == 0
+
+
 def plan(lib, b, hq, hkv, d, bs, maxl, part, sm=152):
     outs = [ctypes.c_int() for _ in range(4)]
     st = lib.pkv_decode_plan(b, hq, hkv, d, bs, maxl, part, sm, *[ctypes.byref(o) for o in outs])
