@@ -89,6 +89,9 @@ def _load():
         lib.oracle_paged_decode_int8.argtypes = [P, P, P, P, P, i64, P, i32, P, i32, i32, i32,
                                                  i32, i32, dbl, i32, P]
         lib.oracle_paged_decode_int8.restype = None
+        lib.oracle_paged_prefill.argtypes = [P, P, P, i64, P, i32, P, P, i32, i32, i32, i32, i32,
+                                             dbl, i32, P]
+        lib.oracle_paged_prefill.restype = None
         lib.oracle_copy_blocks_bytes.argtypes = [P, P, i64, i64, P, i64]
         lib.oracle_copy_blocks_bytes.restype = None
         _lib = lib
@@ -203,6 +206,35 @@ def copy_blocks(kv_pool_bits: np.ndarray, src_dst: np.ndarray, num_kv_heads: int
     base = pool.ctypes.data
     _load().oracle_copy_blocks(ctypes.c_void_p(base), ctypes.c_void_p(base + 2 * half),
                                int(2 * half), int(half), _ptr(pairs), int(pairs.shape[0]))
+
+
+def paged_prefill(q, k_cache, v_cache, block_stride, block_tables, query_start, context_lens,
+                  num_kv_heads, block_size, scale, dtype):
+    """Chunked prefill attention over the block tables (P4 §2 causal attention with a
+    cache; P2 §2.3, §5.4).  ``q`` is [num_rows, num_q_heads, head_dim] 16-bit patterns,
+    the chunks of all sequences back to back (sequence i owns rows
+    query_start[i] .. query_start[i+1]-1); context_lens[i] counts the cached tokens
+    including the chunk.  Row j of chunk i, at position L_i - C_i + j, attends to
+    tokens 0 .. that position.  Returns fp64 [num_rows, num_q_heads, head_dim]."""
+    q = _u16(q)
+    kc, vc = _u16(k_cache), _u16(v_cache)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    num_rows, num_q_heads, head_dim = q.shape
+    num_seqs = int(cl.shape[0])
+    if qs.shape[0] != num_seqs + 1 or int(qs[-1]) != num_rows:
+        raise ValueError("query_start must hold num_seqs + 1 offsets ending at num_rows")
+    if num_q_heads % num_kv_heads:
+        raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+    if np.any(np.diff(qs) < 0) or np.any(cl < np.diff(qs)):
+        raise ValueError("each chunk must be non-negative and fit in its context")
+    out = np.zeros((num_rows, num_q_heads, head_dim), dtype=np.float64)
+    _load().oracle_paged_prefill(
+        _ptr(q), _ptr(kc), _ptr(vc), int(block_stride), _ptr(bt), int(bt.shape[1]), _ptr(qs),
+        _ptr(cl), num_seqs, int(num_q_heads), int(num_kv_heads), int(head_dim), int(block_size),
+        float(scale), int(dtype), _ptr(out))
+    return out
 
 
 # ---------------------------------------------------------------------------

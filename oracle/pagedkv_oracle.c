@@ -372,3 +372,73 @@ void oracle_copy_blocks_bytes(unsigned char *k_cache, unsigned char *v_cache,
         memcpy(v_cache + dst * block_stride_bytes, v_cache + src * block_stride_bytes, block_bytes);
     }
 }
+
+/* ------------------------------------------------------------------------
+ * Chunked prefill attention over the paged cache.  P4 §2 (causal
+ * self-attention with a cache): the new tokens' K and V are appended to the
+ * cache, then each new token's query attends to the cached tokens and,
+ * causally, to the new tokens up to itself; P2 §2.3 (prefill handles a whole
+ * prompt at once) and §5.4 (chunked prefill splits a long prompt into pieces).
+ * The page's mask is a square lower triangle over the new tokens only; with
+ * cached tokens in front, the reading used here is the same rule on absolute
+ * positions: query at position p sees tokens 0 .. p.
+ *
+ * Sequence i holds context_lens[i] = L_i tokens in the cache, of which its
+ * chunk is the last C_i = query_start[i+1] - query_start[i] (positions
+ * L_i - C_i .. L_i - 1; the chunk's K and V are already in the cache).  Query
+ * row j of the chunk is global row query_start[i] + j of q
+ * ([num_rows][num_q_heads][head_dim]); at position p = L_i - C_i + j it gives
+ *     out = sum_{t <= p} exp(s_t - M) v_t / sum_{t <= p} exp(s_t - M),
+ *     s_t = scale * q . k_t,  M = max_{t <= p} s_t,
+ * the two-pass direct definition of oracle_paged_decode over tokens 0 .. p.
+ * ------------------------------------------------------------------------ */
+void oracle_paged_prefill(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                          int64_t block_stride, const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *query_start, const int32_t *context_lens, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          double scale, int dtype, double *out) {
+    const int group = num_q_heads / num_kv_heads;
+    const int64_t num_rows = query_start[num_seqs];
+    const int64_t pairs = num_rows * num_q_heads;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t pair = 0; pair < pairs; ++pair) {
+        const int64_t row = pair / num_q_heads;
+        const int hq = (int)(pair % num_q_heads);
+        const int h = hq / group;
+        int i = 0;
+        while (query_start[i + 1] <= row) ++i;            /* the row's sequence */
+        const int64_t chunk = query_start[i + 1] - query_start[i];
+        const int64_t pos = context_lens[i] - chunk + (row - query_start[i]);
+        const int64_t len = pos + 1;                      /* tokens this row sees */
+        const uint16_t *qrow = q + (row * num_q_heads + hq) * head_dim;
+        double *orow = out + (row * num_q_heads + hq) * head_dim;
+        for (int j = 0; j < head_dim; ++j) orow[j] = 0.0;
+        if (len <= 0) continue;
+
+        double *qv = (double *)malloc(sizeof(double) * head_dim);
+        double *score = (double *)malloc(sizeof(double) * len);
+        for (int j = 0; j < head_dim; ++j) qv[j] = decode16(qrow[j], dtype);
+        double smax = -INFINITY;
+        for (int64_t t = 0; t < len; ++t) {
+            const int64_t phys = block_tables[(int64_t)i * max_blocks_per_seq + t / block_size];
+            const int64_t off = t % block_size;
+            const uint16_t *krow = k_cache + phys * block_stride + ((int64_t)h * block_size + off) * head_dim;
+            double dot = 0.0;
+            for (int j = 0; j < head_dim; ++j) dot += qv[j] * decode16(krow[j], dtype);
+            score[t] = scale * dot;
+            if (score[t] > smax) smax = score[t];
+        }
+        double z = 0.0;
+        for (int64_t t = 0; t < len; ++t) {
+            const int64_t phys = block_tables[(int64_t)i * max_blocks_per_seq + t / block_size];
+            const int64_t off = t % block_size;
+            const uint16_t *vrow = v_cache + phys * block_stride + ((int64_t)h * block_size + off) * head_dim;
+            const double w = exp(score[t] - smax);
+            z += w;
+            for (int j = 0; j < head_dim; ++j) orow[j] += w * decode16(vrow[j], dtype);
+        }
+        for (int j = 0; j < head_dim; ++j) orow[j] /= z;
+        free(score);
+        free(qv);
+    }
+}
