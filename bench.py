@@ -430,6 +430,68 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
     return result
 
 
+def _tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def measure_prefill(pkv, name, dev, steps):
+    """Device-timed chunked-prefill step of one named prefill workload: the chunk
+    rows' cache write, then the prefill attention.  Causal FLOPs count 2 * 2 * d
+    per (query head, visible token) pair (QK^T and PV)."""
+    import torch
+    from paged_kv_cache_155_gb300 import workloads
+    wl = workloads.PREFILL_NAMED[name](device=str(dev))
+    k_cache, v_cache = pkv.split_pool(wl.kv)
+    rows_tables = wl.block_tables.cpu()[wl.row_seq.cpu()]
+    slots = pkv.slot_mapping(rows_tables, wl.new_positions.cpu(), wl.block_size).to(dev)
+    out = torch.empty_like(wl.q)
+    stream = torch.cuda.current_stream(dev)
+    mq, mc = wl.max_query_len, wl.max_context_len
+
+    def attn():
+        pkv.paged_attention_prefill(wl.q, k_cache, v_cache, wl.block_tables, wl.query_start,
+                                    wl.context_lens, wl.scale, out, max_query_len=mq,
+                                    max_context_len=mc)
+
+    for _ in range(5):
+        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
+        attn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(steps):
+        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
+        ev[k][0].record(stream)
+        attn()
+        ev[k][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    flags, names = pkv.get_device_error(dev)
+    if flags:
+        raise RuntimeError(f"device flags on {name}: {names}")
+    ms_step = t0.elapsed_time(t1) / steps
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    visible = int((wl.new_positions.cpu() + 1).sum())
+    flops = 4 * wl.head_dim * wl.num_q_heads * visible
+    peak, kind = _tensor_peak()
+    tflops = flops / (attn_ms / 1e3) / 1e12
+    result = {"tokens_per_s": wl.num_rows / (ms_step / 1e3), "ms_per_step": ms_step,
+              "attention_ms": attn_ms, "causal_flops": flops, "tflops": tflops,
+              "tensor_frac_of_measured_bf16": tflops / peak, "peak_source": f"{kind} bf16_tflops",
+              "num_seqs": wl.num_seqs, "query_rows": wl.num_rows,
+              "context_len_max": mc, "chunk_len_max": mq}
+    del wl, k_cache, v_cache, out
+    torch.cuda.empty_cache()
+    return result
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -568,6 +630,8 @@ def run_ours(args):
             if name == args.workload:
                 continue
             others[name] = measure_workload(pkv, name, dev, 300, peak)
+        for name in ("prefill7b", "chunked70b"):
+            others[name] = measure_prefill(pkv, name, dev, 50)
         line["other_workloads"] = others
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -6,6 +6,8 @@
  *   P1 = "KV Cache与PagedAttention深度解析：vLLM内存管理革命" (iopencloud.com)
  *   P2 = "KV Cache从原理到实战：大模型推理内存管理演进与优化" (xnwp.cn/news/16711)
  *   P3 = PagedAttention + prefix caching via nano-vllm (zwxr.cn/news/317362)
+ *   P4 = "大模型 (LLM) 推理加速核心技术解析：从 KV Cache 到 PagedAttention 实战"
+ *        (jsqmd.com/news/745991)
  *
  * Conventions shared by every call
  * --------------------------------
@@ -249,6 +251,53 @@ PKV_API pkv_status pkv_paged_attention_decode_shared_prefix(
     int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
     int block_size, float scale, void *out, void *workspace, size_t workspace_bytes,
     int partition_size, pkv_dtype dtype, void *stream);
+
+/*
+ * pkv_prefill_workspace_bytes -- workspace of pkv_paged_attention_prefill for
+ * these arguments on the current device: 0 when the KV range is not split,
+ * (size_t)-1 for arguments out of contract.  kv_splits as in
+ * pkv_paged_attention_prefill.
+ */
+PKV_API size_t pkv_prefill_workspace_bytes(int num_rows, int num_seqs, int num_q_heads,
+                                           int num_kv_heads, int head_dim, int block_size,
+                                           int max_query_len, int max_context_len, int kv_splits);
+
+/*
+ * pkv_paged_attention_prefill -- chunked prefill attention over the paged
+ * cache (P4 §2: with a cache, the new tokens' queries attend to the cached
+ * tokens and causally to each other; P2 §2.3 / §5.4: a whole prompt, or a long
+ * prompt in chunks).  Sequence i has context_lens[i] = L_i tokens in the
+ * cache, the last C_i = query_start[i+1] - query_start[i] of which are its
+ * chunk (already written, e.g. by pkv_reshape_and_cache with the chunk's
+ * slots).  Chunk row j -- global query row query_start[i] + j, at position
+ * p = L_i - C_i + j -- attends to tokens 0 .. p (the causal rule on absolute
+ * positions):
+ *     out[row, hq] = softmax_t<=p(scale * q[row, hq] . k_t) V,
+ * accumulated in fp32 on the tensor cores (tcgen05, 128 query rows x 128
+ * tokens per tile; the group's heads of each token share the K/V tiles).
+ *
+ *   q, out         [num_rows][num_q_heads][head_dim], contiguous, dtype; the
+ *                  chunks of all sequences back to back.
+ *   query_start    [num_seqs + 1] int32, device: non-decreasing chunk offsets,
+ *                  query_start[num_seqs] <= num_rows.
+ *   context_lens   [num_seqs] int32, device: L_i >= C_i.
+ *   max_query_len, max_context_len   host bounds of C_i and L_i (size the grid;
+ *                  a sequence outside them, or with query_start out of order,
+ *                  raises PKV_DEVERR_CONTEXT_LEN and its rows are not written).
+ *   kv_splits      0 = library's choice; n > 0 splits each row tile's KV range
+ *                  into about n pieces of whole 128-token tiles, merged by a
+ *                  log-sum-exp pass (workspace needed when the plan splits).
+ * Other arguments as pkv_paged_attention_decode; head_dim 128 only (else
+ * PKV_ERR_UNSUPPORTED).  A chunk of one token per sequence computes the same
+ * attention as pkv_paged_attention_decode.
+ */
+PKV_API pkv_status pkv_paged_attention_prefill(
+    const void *q, const void *k_cache, const void *v_cache, int64_t num_blocks,
+    int64_t block_stride_elems, const int32_t *block_tables, int max_blocks_per_seq,
+    const int32_t *query_start, const int32_t *context_lens, int num_rows, int max_query_len,
+    int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, float scale, void *out, void *workspace, size_t workspace_bytes,
+    int kv_splits, pkv_dtype dtype, void *stream);
 
 /* Size of the library's built-in decode scratch array (per device). */
 #define PKV_STATIC_SCRATCH_BYTES (32u << 20) /* 32 MiB */

@@ -7,6 +7,8 @@ thin PyTorch binding.
   paged_attention_decode_shared_prefix   the decode for a batch sharing a prefix
   reshape_and_cache_int8 / paged_attention_decode_int8   the same over an INT8
                           cache with per-channel scales
+  paged_attention_prefill chunked prefill: each sequence's new tokens attend causally
+                          over its paged cache
 
 The library must be built first (``__graft_entry__.build()``); the calls raise
 if it is missing.  There is no CPU implementation in this package.
@@ -15,6 +17,7 @@ from .ops import (F16, BF16, INT8, copy_blocks, debug_wait_timeout,  # noqa: F40
                   decode_int8_workspace_bytes, decode_plan, decode_workspace_bytes,
                   get_device_error, launch_count, paged_attention_decode,
                   paged_attention_decode_int8, paged_attention_decode_shared_prefix,
+                  paged_attention_prefill, prefill_workspace_bytes,
                   reshape_and_cache, reshape_and_cache_int8, shared_prefix_workspace_bytes,
                   split_pool)
 from .block_table import slot_mapping  # noqa: F401
@@ -22,6 +25,6 @@ from ._lib import PagedKVError  # noqa: F401
 
 __all__ = ["reshape_and_cache", "paged_attention_decode", "paged_attention_decode_shared_prefix",
            "shared_prefix_workspace_bytes", "copy_blocks", "split_pool",
-           "reshape_and_cache_int8", "paged_attention_decode_int8", "decode_int8_workspace_bytes",
+           "paged_attention_prefill", "prefill_workspace_bytes", "reshape_and_cache_int8", "paged_attention_decode_int8", "decode_int8_workspace_bytes",
            "decode_workspace_bytes", "decode_plan", "get_device_error", "launch_count",
            "debug_wait_timeout", "slot_mapping", "PagedKVError"]

@@ -47,6 +47,10 @@ SIGNATURES = {
     "pkv_paged_attention_decode_int8": (I32, [P, P, P, P, P, I64, I64, P, I32, P, I32, I32, I32,
                                               I32, I32, I32, ctypes.c_float, P, P, SZ, I32, I32,
                                               P]),
+    "pkv_prefill_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32, I32, I32]),
+    "pkv_paged_attention_prefill": (I32, [P, P, P, I64, I64, P, I32, P, P, I32, I32, I32, I32,
+                                          I32, I32, I32, I32, ctypes.c_float, P, P, SZ, I32, I32,
+                                          P]),
     "pkv_bm_create": (P, [I64, I32, I32]),
     "pkv_bm_destroy": (None, [P]),
     "pkv_bm_num_free": (I64, [P]),

@@ -5,38 +5,7 @@
 
 #include "decode_launch.cuh"
 
-namespace {
-
-constexpr int kResidentCtasPerSm = 2;  // decode CTAs resident per SM (shared-memory bound)
-constexpr int kTargetWaves = 8;        // CTA waves the automatic split aims for
-constexpr int kMinAutoPartition = 256; // tokens: below this the per-CTA set-up dominates
-constexpr int kTcItemsPerSm = 24;      // tensor-core path: work items per persistent CTA
-
-constexpr int kTcMinContext = 2048;    // tensor-core path from this longest context on
-
-// head_dim 128 with 4, 8 or 16 query heads per KV head: the group turns QK^T
-// and PV into dense tiles and runs on the tensor cores -- when contexts are
-// long.  Measured on GB300 (32 q / 8 kv heads, block 16): for contexts of at
-// most ~1K tokens the non-persistent CUDA-core kernel is faster (each short
-// work item exposes the copy latency of the persistent pipeline), around 1-2K
-// the two tie, from 2K on the tensor-core kernel is faster.
-bool use_tensor_cores(int head_dim, int group, int longest_span) {
-    return head_dim == 128 && (group == 4 || group == 8 || group == 16) &&
-           longest_span >= kTcMinContext;
-}
-
-int heads_per_block_for(int group) {
-    if (group % 8 == 0) return 8;
-    if (group % 4 == 0) return 4;
-    if (group % 2 == 0) return 2;
-    return 1;
-}
-
-size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, int num_partitions) {
-    if (num_partitions <= 1) return 0;
-    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * num_partitions;
-    return rows * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
-}
+namespace pkv {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -72,6 +41,41 @@ bool encode_half_map(CUtensorMap *map, const void *base, int64_t num_blocks,
               3, const_cast<void *>(base), dims, strides, box, elem_strides,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace pkv
+
+namespace {
+
+constexpr int kResidentCtasPerSm = 2;  // decode CTAs resident per SM (shared-memory bound)
+constexpr int kTargetWaves = 8;        // CTA waves the automatic split aims for
+constexpr int kMinAutoPartition = 256; // tokens: below this the per-CTA set-up dominates
+constexpr int kTcItemsPerSm = 24;      // tensor-core path: work items per persistent CTA
+
+constexpr int kTcMinContext = 2048;    // tensor-core path from this longest context on
+
+// head_dim 128 with 4, 8 or 16 query heads per KV head: the group turns QK^T
+// and PV into dense tiles and runs on the tensor cores -- when contexts are
+// long.  Measured on GB300 (32 q / 8 kv heads, block 16): for contexts of at
+// most ~1K tokens the non-persistent CUDA-core kernel is faster (each short
+// work item exposes the copy latency of the persistent pipeline), around 1-2K
+// the two tie, from 2K on the tensor-core kernel is faster.
+bool use_tensor_cores(int head_dim, int group, int longest_span) {
+    return head_dim == 128 && (group == 4 || group == 8 || group == 16) &&
+           longest_span >= kTcMinContext;
+}
+
+int heads_per_block_for(int group) {
+    if (group % 8 == 0) return 8;
+    if (group % 4 == 0) return 4;
+    if (group % 2 == 0) return 2;
+    return 1;
+}
+
+size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, int num_partitions) {
+    if (num_partitions <= 1) return 0;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads * num_partitions;
+    return rows * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
 }
 
 // The launch plan of a decode call; allow_tc = false keeps it on the CUDA-core
@@ -221,9 +225,9 @@ pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (tc) {
         CUtensorMap tk, tv;
-        if (!encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads,
+        if (!pkv::encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads,
                              block_size, dtype) ||
-            !encode_half_map(&tv, v_cache, num_blocks, block_stride_elems, num_kv_heads,
+            !pkv::encode_half_map(&tv, v_cache, num_blocks, block_stride_elems, num_kv_heads,
                              block_size, dtype))
             return PKV_ERR_CUDA;
         const int sm = pkv::current_sm_count();
@@ -405,8 +409,8 @@ PKV_API pkv_status pkv_paged_attention_decode_shared_prefix(
     unsigned int *status = pkv::status_word_ptr();
     if (!status) return PKV_ERR_CUDA;
     CUtensorMap tk, tv;
-    if (!encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads, block_size, dtype) ||
-        !encode_half_map(&tv, v_cache, num_blocks, block_stride_elems, num_kv_heads, block_size, dtype))
+    if (!pkv::encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads, block_size, dtype) ||
+        !pkv::encode_half_map(&tv, v_cache, num_blocks, block_stride_elems, num_kv_heads, block_size, dtype))
         return PKV_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int group = num_q_heads / num_kv_heads;

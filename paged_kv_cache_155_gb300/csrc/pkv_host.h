@@ -2,6 +2,7 @@
 // (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,6 +18,13 @@ int current_sm_count();
 
 // Count one kernel launch made through the library.
 void count_launch();
+
+// Tiled tensor map of one half (K or V) of a 16-bit pool for 3-D TMA loads:
+// dims (head_dim 128, num_kv_heads * block_size rows, num_blocks), boxes of one
+// block's rows of one head, 64 columns wide, 128-byte swizzled.  False if the
+// driver entry point is missing or the encode fails.
+bool encode_half_map(CUtensorMap *map, const void *base, int64_t num_blocks,
+                     int64_t block_stride_elems, int num_kv_heads, int block_size, pkv_dtype dt);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -1,0 +1,478 @@
+// prefill_tc_kernel.cuh -- chunked prefill attention over the paged cache.
+//
+// "大模型 (LLM) 推理加速核心技术解析" §2 (causal self-attention with a cache):
+// the new tokens' K and V join the cache, then each new token's query attends
+// to the cached tokens and, causally, to the new tokens up to itself; "KV Cache
+// 从原理到实战" §2.3 / §5.4: a whole prompt at once (prefill), or a long prompt
+// in pieces (chunked prefill).  Sequence i holds L_i tokens in the cache, the
+// last C_i of which are its chunk; chunk row j (global query row
+// query_start[i] + j) sits at position L_i - C_i + j and attends to tokens
+// 0 .. that position.
+//
+// One CTA: 128 query rows of one sequence and one KV head -- row r of the
+// sequence's rows is chunk token r / G, query head r % G of the group, so a
+// KV tile is shared by the G heads of every token in the tile -- over one
+// split of the KV range (all of it unless the grid would be too small).  The
+// KV range ends at the causal limit of the tile's last row; inside a tile a
+// row's columns past its own position are masked.  Same machinery as the
+// shared-prefix tile kernel: tcgen05 MMAs with M = 128 rows, N = 128 tokens,
+// K = 128; S double-buffered in TMEM, O accumulated in TMEM; a row's softmax is
+// local to one thread; the row's reference maximum moves only when a tile
+// exceeds it by more than kRescaleLog2.  With one split the kernel writes the
+// normalised output; with several it writes (o, m, l) partials that
+// paged_prefill_merge_kernel combines.
+//
+// Warps: 0 TMA producer (K ring and V ring, 2 slots each), 1 TMEM owner + MMA
+// issuer, 2-5 softmax (thread = query row).
+#pragma once
+
+#include "prefix_tc_kernel.cuh"
+
+namespace pkv {
+
+struct PrefillParams {
+    const void *q;                 // [num_rows][num_q_heads][128]
+    void *out;                     // [num_rows][num_q_heads][128]
+    float *ws_o;                   // [num_rows * num_q_heads][splits][128] (splits > 1)
+    float *ws_m;                   // [num_rows * num_q_heads][splits] (log2 units)
+    float *ws_l;
+    const int32_t *block_tables;   // [num_seqs][max_blocks_per_seq]
+    const int32_t *query_start;    // [num_seqs + 1]
+    const int32_t *context_lens;   // [num_seqs], chunk included
+    unsigned int *status;
+    int64_t num_blocks;
+    int max_blocks_per_seq;
+    int len_cap;       // host bound of context_lens (<= max_blocks_per_seq * block_size)
+    int qlen_cap;      // host bound of the chunk lengths
+    int num_rows;      // query_start[num_seqs] as given by the host
+    int num_seqs;
+    int num_q_heads;
+    int group;
+    int splits;        // KV splits per row tile
+    int split_tokens;  // tokens per split, a multiple of 128
+    float scale_log2;
+};
+
+// Reads and checks one sequence's (chunk start, chunk length, context length);
+// false (and a raised flag) when they are out of contract.
+__device__ __forceinline__ bool prefill_seq(const PrefillParams &p, int seq, int &q0, int &chunk,
+                                            int &len) {
+    q0 = p.query_start[seq];
+    const int q1 = p.query_start[seq + 1];
+    chunk = q1 - q0;
+    len = p.context_lens[seq];
+    return q0 >= 0 && chunk >= 0 && q1 <= p.num_rows && chunk <= p.qlen_cap && len >= chunk &&
+           len <= p.len_cap;
+}
+
+template <typename T, int BS>
+__global__ void __launch_bounds__(192, 1)
+    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                            const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
+    using L = PrefixLayout;
+    constexpr int TILE = L::kTile, D = 128;
+    constexpr bool kBF16 = !std::is_same<T, __half>::value;
+    static_assert(TILE / BS <= 32, "one table entry per producer lane");
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // heavy (late) row tiles first: they have the longest causal range
+    const int row_tile = gridDim.x - 1 - blockIdx.x;
+    const int kvh = blockIdx.y;
+    const int seq = blockIdx.z / p.splits, split = blockIdx.z - seq * p.splits;
+    int q0, chunk, len;
+    if (!prefill_seq(p, seq, q0, chunk, len)) {
+        if (threadIdx.x == 0 && row_tile == 0 && kvh == 0 && split == 0)
+            raise_flag(p.status, PKV_DEVERR_CONTEXT_LEN);
+        return;  // uniform over the CTA
+    }
+    const int rows = chunk * p.group;  // this sequence's query rows of one KV head
+    const int row0 = row_tile * 128;
+    if (row0 >= rows) return;
+    const int last_row = min(rows, row0 + 128) - 1;
+    const int base_pos = len - chunk;  // position of chunk token 0
+    const int pos_max = base_pos + last_row / p.group;
+    const int tok_lo = split * p.split_tokens;
+    const int tok_hi = min(min(len, pos_max + 1), tok_lo + p.split_tokens);
+    if (tok_hi <= tok_lo) return;  // no row of the tile reaches this split
+    const int ntiles = (tok_hi - tok_lo + TILE - 1) / TILE;
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm =
+        smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
+    uint64_t *k_full = bars, *k_empty = bars + 2, *v_full = bars + 4, *v_empty = bars + 6;
+    uint64_t *s_full = bars + 8, *s_empty = bars + 10, *p_full = bars + 12, *o_done = bars + 14;
+    uint64_t *drain_bar = bars + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
+    const uint32_t smem_base = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_done[i], 1);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, L::kTmemCols);
+        tc::tmem_relinquish();
+    }
+    // query rows of this tile -> Q panel (K-major, 128-byte swizzle); rows past the
+    // chunk are zero
+    for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
+        const int r = i >> 4, c8 = i & 15;
+        const int row = row0 + r;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < rows) {
+            const int j = row / p.group, g = row - j * p.group;
+            const T *src = static_cast<const T *>(p.q) +
+                           ((static_cast<int64_t>(q0) + j) * p.num_q_heads + kvh * p.group + g) * D;
+            v = *reinterpret_cast<const uint4 *>(src + c8 * 8);
+        }
+        *reinterpret_cast<uint4 *>(sm + L::kOffQ + (c8 >> 3) * L::kHalf + r * 128 +
+                                   (((c8 & 7) ^ (r & 7)) << 4)) = v;
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tensormap(&tmap_k);
+        tc::prefetch_tensormap(&tmap_v);
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ===================== TMA producer =====================
+        const uint64_t policy = l2_policy_evict_last();  // every row tile of the sequence reads it
+        const int32_t *trow = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
+        int last_issue[2][2] = {{-1, -1}, {-1, -1}};
+        bool ok = true;
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int t0 = tok_lo + j * TILE;
+            const int nblk = (min(TILE, tok_hi - t0) + BS - 1) / BS;
+            int e = -1;
+            if (lane < nblk) {
+                e = trow[t0 / BS + lane];
+                if (e < 0 || e >= p.num_blocks) {
+                    raise_flag(p.status, PKV_DEVERR_BLOCK_TABLE);
+                    e = -1;
+                }
+            }
+            const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, e >= 0)) * BS * 256u;
+            for (int kv = 0; kv < 2 && ok; ++kv) {
+                const int s = j & 1;
+                uint64_t *fb = kv ? &v_full[s] : &k_full[s];
+                uint64_t *eb = kv ? &v_empty[s] : &k_empty[s];
+                int go = 1;
+                if (lane == 0) {
+                    go = tc_wait(eb, ((j >> 1) & 1) ^ 1, abort_flag, p.status);
+                    if (go) {
+                        if (bytes) mbar_arrive_expect_tx(fb, bytes);
+                        else mbar_arrive(fb);
+                        last_issue[kv][s] = j;
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, go, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (e >= 0) {
+                    unsigned char *slot = sm + (kv ? L::kOffV : L::kOffK) + s * L::kPanel;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        tc::tma_load_3d(slot + c * L::kHalf + lane * BS * 128, kv ? &tmap_v : &tmap_k,
+                                        c * 64, kvh * BS, e, fb, policy);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && lane == 0) {
+            for (int kv = 0; kv < 2; ++kv)
+                for (int s = 0; s < 2; ++s)
+                    if (last_issue[kv][s] >= 0)
+                        mbar_wait_bounded(kv ? &v_full[s] : &k_full[s], (last_issue[kv][s] >> 1) & 1,
+                                          kDrainTimeoutNs);
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer (event-driven, PV first) =====================
+        constexpr uint32_t idesc_qk = tc::idesc_f16_f32acc(kBF16, 128, 128, false, false);
+        constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, 128, false, true);
+        int n_qk = 0, n_pv = 0;
+        bool ok = true;
+        uint64_t idle_since = 0;
+        while (ok && n_pv < ntiles) {
+            int act = 0;
+            if (lane == 0) {
+                if (n_pv < n_qk && mbar_try_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
+                    mbar_try_wait(&v_full[n_pv & 1], (n_pv >> 1) & 1))
+                    act = 1;
+                else if (n_qk < ntiles && mbar_try_wait(&k_full[n_qk & 1], (n_qk >> 1) & 1) &&
+                         mbar_try_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
+                    act = 2;
+                if (act) {
+                    idle_since = 0;
+                } else {
+                    const uint64_t now = global_timer_ns();
+                    if (!idle_since) idle_since = now;
+                    if (*abort_flag) {
+                        act = -1;
+                    } else if (now - idle_since > kWaitTimeoutNs) {
+                        raise_flag(p.status, PKV_DEVERR_TIMEOUT);
+                        *abort_flag = 1;
+                        act = -1;
+                    }
+                }
+                if (act == 1) {
+                    const int j = n_pv, b = j & 1;
+                    tc::fence_after_sync();
+                    const uint32_t pa = smem_base + L::kOffP + b * L::kPanel;
+                    const uint32_t va = smem_base + L::kOffV + b * L::kPanel;
+#pragma unroll
+                    for (int k = 0; k < TILE / 16; ++k) {
+                        const uint64_t a = tc::smem_desc_sw128(pa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(va + k * 2048, L::kHalf, 1024);
+                        tc::mma_f16_ss(tmem + 256, a, bd, idesc_pv, j > 0 || k > 0);
+                    }
+                    tc::mma_commit(&o_done[b]);
+                    tc::mma_commit(&v_empty[b]);
+                } else if (act == 2) {
+                    const int j = n_qk, b = j & 1;
+                    tc::fence_after_sync();
+                    const uint32_t qa = smem_base + L::kOffQ;
+                    const uint32_t ka = smem_base + L::kOffK + b * L::kPanel;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint64_t a = tc::smem_desc_sw128(qa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(ka + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                        tc::mma_f16_ss(tmem + 128 * b, a, bd, idesc_qk, k > 0);
+                    }
+                    tc::mma_commit(&s_full[b]);
+                    tc::mma_commit(&k_empty[b]);
+                }
+            }
+            act = __shfl_sync(0xffffffffu, act, 0);
+            if (act < 0) ok = false;
+            else if (act == 1) ++n_pv;
+            else if (act == 2) ++n_qk;
+        }
+        if (lane == 0) {
+            // every MMA of this CTA completes before TMEM is released
+            tc::mma_commit(drain_bar);
+            mbar_wait_bounded(drain_bar, 0, kDrainTimeoutNs);
+        }
+        __syncwarp();
+    } else {
+        // ===================== softmax (warps 2..5): thread = query row =====================
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
+        const int row = row0 + r;
+        const bool live = row < rows;
+        const int jtok = live ? row / p.group : 0;
+        const int pos = base_pos + jtok;    // this row sees tokens 0 .. pos
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int b = j & 1;
+            const int t0 = tok_lo + j * TILE;
+            const int valid = min(TILE, tok_hi - t0);             // columns loaded
+            const int vr = live ? max(0, min(valid, pos + 1 - t0)) : 0;  // columns this row sees
+            if (!tc_wait_warp(&s_full[b], (j >> 1) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            // pass 1: tile maximum of this row over its visible columns
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < TILE; c += 32) {
+                float x[32];
+                tc::tmem_ld_x16(lane_base + 128 * b + c, x);
+                tc::tmem_ld_x16(lane_base + 128 * b + c + 16, x + 16);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (c + i < vr) tmax = fmaxf(tmax, x[i] * p.scale_log2);
+            }
+            // the reference maximum moves only by more than kRescaleLog2 (a row that sees
+            // nothing keeps -inf and alpha 1); TMEM loads and stores are warp-wide, so the
+            // warp rescales if any of its rows must
+            const float new_ref = tmax > m_ref + L::kRescaleLog2 ? tmax : m_ref;
+            const float alpha = new_ref == m_ref ? 1.f : fast_exp2(m_ref - new_ref);
+            if (__any_sync(0xffffffffu, new_ref != m_ref)) {
+                if (j > 0) {
+                    // O holds tiles < j: wait for PV(j-1), rescale O in TMEM
+                    if (!tc_wait_warp(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int c = 0; c < D; c += 16) {
+                        float o[16];
+                        tc::tmem_ld_x16(lane_base + 256 + c, o);
+                        tc::tmem_ld_wait();
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(o[i] * alpha);
+                        asm volatile(
+                            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, "
+                            "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(lane_base + 256 + c),
+                            "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                            "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]),
+                            "r"(w[13]), "r"(w[14]), "r"(w[15])
+                            : "memory");
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                }
+                l *= alpha;
+                m_ref = new_ref;
+            }
+            // P[b] was last read by PV(j-2)
+            if (j >= 2 && !tc_wait_warp(&o_done[b], ((j - 2) >> 1) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            // pass 2: P = 2^(s - m_ref) on visible columns (0 elsewhere), rounded to T,
+            // into the K-major P panel
+            unsigned char *prow = sm + L::kOffP + b * L::kPanel + r * 128;
+#pragma unroll
+            for (int c = 0; c < TILE; c += 32) {
+                float x[32];
+                tc::tmem_ld_x16(lane_base + 128 * b + c, x);
+                tc::tmem_ld_x16(lane_base + 128 * b + c + 16, x + 16);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    uint32_t packed[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int t = c + c8 * 8 + 2 * i;
+                        const float p0 = t < vr ? fast_exp2(x[c8 * 8 + 2 * i] * p.scale_log2 - m_ref) : 0.f;
+                        const float p1 = t + 1 < vr ? fast_exp2(x[c8 * 8 + 2 * i + 1] * p.scale_log2 - m_ref) : 0.f;
+                        const T h0 = Elem<T>::from_f32(p0), h1 = Elem<T>::from_f32(p1);
+                        l += static_cast<float>(h0) + static_cast<float>(h1);
+                        packed[i] = static_cast<uint32_t>(reinterpret_cast<const uint16_t &>(h0)) |
+                                    (static_cast<uint32_t>(reinterpret_cast<const uint16_t &>(h1)) << 16);
+                    }
+                    const int chunk8 = (c + c8 * 8) >> 3;  // 8-token chunk index, 0..15
+                    *reinterpret_cast<uint4 *>(prow + (chunk8 >> 3) * L::kHalf + (((chunk8 & 7) ^ (r & 7)) << 4)) =
+                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                }
+            }
+            tc::fence_before_sync();
+            if (valid < TILE) {
+                // V rows past the loaded range: zero them so 0 * stale never reaches the MMA
+                if (!tc_wait_warp(&v_full[b], (j >> 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                if (r >= valid) {
+                    unsigned char *vrow = sm + L::kOffV + b * L::kPanel + r * 128;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            reinterpret_cast<uint4 *>(vrow + c * L::kHalf)[i] = make_uint4(0, 0, 0, 0);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&s_empty[b]);
+                mbar_arrive(&p_full[b]);
+            }
+        }
+        // final: the O row -> out (one split) or its partial slot.  TMEM loads are
+        // warp-wide: every lane loads, only live rows store.
+        if (ok) ok = tc_wait_warp(&o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
+        if (ok) {
+            tc::fence_after_sync();
+            const int g = live ? row - jtok * p.group : 0;
+            const int64_t orow = (static_cast<int64_t>(q0) + jtok) * p.num_q_heads + kvh * p.group + g;
+            const bool direct = p.splits == 1;
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+            for (int c = 0; c < D; c += 16) {
+                float o[16];
+                tc::tmem_ld_x16(lane_base + 256 + c, o);
+                tc::tmem_ld_wait();
+                if (!live) continue;
+                if (direct) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const T h0 = Elem<T>::from_f32(o[2 * i] * inv_l);
+                        const T h1 = Elem<T>::from_f32(o[2 * i + 1] * inv_l);
+                        w[i] = static_cast<uint32_t>(reinterpret_cast<const uint16_t &>(h0)) |
+                               (static_cast<uint32_t>(reinterpret_cast<const uint16_t &>(h1)) << 16);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + orow * D + c);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                } else {
+                    float *dst = p.ws_o + (orow * p.splits + split) * D + c;
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4)
+                        *reinterpret_cast<float4 *>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+                }
+            }
+            if (live && !direct) {
+                p.ws_m[orow * p.splits + split] = m_ref;
+                p.ws_l[orow * p.splits + split] = l;
+            }
+        }
+    }
+
+    // ---- tear-down: the MMA warp drained its MMAs; TMEM is freed
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+// Log-sum-exp merge of a prefill's KV splits: one warp per (chunk row, query
+// head); the row at position pos has partials in splits 0 .. pos / split_tokens.
+template <typename T>
+__global__ void __launch_bounds__(128) paged_prefill_merge_kernel(const PrefillParams p) {
+    constexpr int D = 128, PER_LANE = D / 32;
+    const int seq = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const int idx = blockIdx.x * 4 + (threadIdx.x >> 5);  // (chunk token, query head)
+    int q0, chunk, len;
+    if (!prefill_seq(p, seq, q0, chunk, len)) return;    // flagged by the main kernel
+    const int jtok = idx / p.num_q_heads, hq = idx - jtok * p.num_q_heads;
+    if (jtok >= chunk) return;
+    const int pos = len - chunk + jtok;
+    const int nsp = min(p.splits, pos / p.split_tokens + 1);
+    const int64_t orow = (static_cast<int64_t>(q0) + jtok) * p.num_q_heads + hq;
+    const int64_t base = orow * p.splits;
+    float mmax = -INFINITY;
+    for (int s = 0; s < nsp; ++s) mmax = fmaxf(mmax, p.ws_m[base + s]);
+    float lsum = 0.f, o[PER_LANE] = {};
+    for (int s = 0; s < nsp; ++s) {
+        const float ms = p.ws_m[base + s];
+        const float w = ms == -INFINITY ? 0.f : fast_exp2(ms - mmax);
+        lsum += w * p.ws_l[base + s];
+        const float *src = p.ws_o + (base + s) * D + lane * PER_LANE;
+#pragma unroll
+        for (int e = 0; e < PER_LANE; ++e) o[e] += w * src[e];
+    }
+    T *dst = static_cast<T *>(p.out) + orow * D + lane * PER_LANE;
+#pragma unroll
+    for (int e = 0; e < PER_LANE; ++e) dst[e] = Elem<T>::from_f32(lsum > 0.f ? o[e] / lsum : 0.f);
+}
+
+}  // namespace pkv

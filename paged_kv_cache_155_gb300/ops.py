@@ -197,6 +197,59 @@ def paged_attention_decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor,
     return out
 
 
+def prefill_workspace_bytes(num_rows, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                            max_query_len, max_context_len, kv_splits=0) -> int:
+    n = lib().pkv_prefill_workspace_bytes(num_rows, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                          block_size, max_query_len, max_context_len, kv_splits)
+    if n == ctypes.c_size_t(-1).value:
+        raise PagedKVError("pkv_prefill_workspace_bytes", 1)
+    return int(n)
+
+
+def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, query_start: torch.Tensor,
+                            context_lens: torch.Tensor, scale: Optional[float] = None,
+                            out: Optional[torch.Tensor] = None, *, max_query_len: int,
+                            max_context_len: int, kv_splits: int = 0,
+                            workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Chunked prefill attention: q [num_rows, Hq, d] holds every sequence's chunk
+    (sequence i owns rows query_start[i]:query_start[i+1], whose K/V are already in
+    the cache as its last tokens); row j of chunk i attends causally to tokens
+    0 .. context_lens[i] - chunk_i + j.  max_query_len / max_context_len are host bounds."""
+    nb, hkv, bs, d, stride = _cache_geometry(k_cache, v_cache)
+    if q.dim() != 3 or q.shape[2] != d or not q.is_contiguous() or q.dtype != k_cache.dtype:
+        raise ValueError(f"q must be a contiguous [num_rows, num_q_heads, {d}] of the cache dtype")
+    rows, hq = int(q.shape[0]), int(q.shape[1])
+    b = int(context_lens.numel())
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or block_tables.shape[0] != b \
+            or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be a contiguous int32 [num_seqs, max_blocks_per_seq]")
+    if query_start.dtype != torch.int32 or query_start.numel() != b + 1 \
+            or not query_start.is_contiguous():
+        raise ValueError("query_start must be a contiguous int32 [num_seqs + 1]")
+    if context_lens.dtype != torch.int32 or not context_lens.is_contiguous():
+        raise ValueError("context_lens must be a contiguous int32 [num_seqs]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must match q")
+    need = prefill_workspace_bytes(rows, b, hq, hkv, d, bs, max_query_len, max_context_len,
+                                   kv_splits)
+    if workspace is None:
+        workspace = _workspace(q.device, need)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().pkv_paged_attention_prefill(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), nb, stride, block_tables.data_ptr(),
+        int(block_tables.shape[1]), query_start.data_ptr(), context_lens.data_ptr(), rows,
+        int(max_query_len), int(max_context_len), b, hq, hkv, d, bs, float(scale), out.data_ptr(),
+        ws_ptr, ws_bytes, int(kv_splits), _dtype_code(q), _stream(q))
+    _check(st, "pkv_paged_attention_prefill")
+    return out
+
+
 def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst_pairs: torch.Tensor) -> None:
     """Copy K and V of block src over block dst for each row (src, dst) of an int64 [n, 2]."""
     nb, hkv, bs, d, stride = _cache_geometry(k_cache, v_cache)

@@ -23,6 +23,9 @@ The five named workloads follow the shapes the pages discuss:
              private suffix U[64, 1024]; bf16; 128 copy-on-write pairs.
   long70b -- Llama-2-70B-shaped GQA: 64 q / 8 kv heads, 16 sequences of 32768.
 
+Chunked-prefill workloads (prefill7b, chunked70b) are described at
+make_prefill_workload below.
+
 INT8-cache variants (``kv_dtype=torch.int8``; "KV Cache从原理到实战" §5.2):
 the pool holds codes drawn as round(32 * N(0, 1)) clipped to [-127, 127] (the
 codes a Gaussian channel quantised with its maximum near 4 sigma would have),
@@ -258,6 +261,118 @@ def gqa7b_int8(device="cpu", seed=2, **kw):
 
 def long70b_int8(device="cpu", seed=4, **kw):
     return long70b(device=device, seed=seed, kv_dtype=torch.int8, **kw)
+
+
+# ---------------------------------------------------------------------------
+# Chunked prefill workloads ("大模型 (LLM) 推理加速核心技术解析" §2; "KV Cache从原理到实战"
+# §2.3 / §5.4): each sequence has ``cached`` tokens already in the cache and a
+# chunk of ``chunk`` new tokens whose K/V rows are written at the positions
+# that follow; every chunk row is a query.
+# ---------------------------------------------------------------------------
+@dataclass
+class PrefillWorkload:
+    name: str
+    dtype: torch.dtype
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    kv: torch.Tensor                 # [num_blocks, 2, Hkv, bs, d]
+    q: torch.Tensor                  # [num_rows, Hq, d], the chunks back to back
+    k_new: torch.Tensor              # [num_rows, Hkv, d]
+    v_new: torch.Tensor
+    new_positions: torch.Tensor      # [num_rows] int64, absolute position of each chunk row
+    row_seq: torch.Tensor            # [num_rows] int64, the sequence of each chunk row
+    block_tables: torch.Tensor       # [B, max_blocks_per_seq] int32
+    query_start: torch.Tensor        # [B + 1] int32
+    context_lens: torch.Tensor       # [B] int32, chunk included
+    chunk_lens: list
+    scale: float
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def num_rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def max_query_len(self) -> int:
+        return max([0] + list(self.chunk_lens))
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max().item()) if self.num_seqs else 0
+
+
+def make_prefill_workload(*, name: str = "prefill", num_q_heads: int, num_kv_heads: int,
+                          head_dim: int, block_size: int, cached_lens: Sequence[int],
+                          chunk_lens: Sequence[int], dtype: torch.dtype = torch.float16,
+                          seed: int = 0, device: str = "cpu", num_blocks: Optional[int] = None,
+                          extra_rows: int = 0) -> PrefillWorkload:
+    """Seeded chunked-prefill inputs.  ``extra_rows`` appends query rows that belong
+    to no sequence (the call must leave their output untouched)."""
+    cached = [int(x) for x in cached_lens]
+    chunks = [int(x) for x in chunk_lens]
+    assert len(cached) == len(chunks)
+    b, bs = len(chunks), block_size
+    lens = [c + n for c, n in zip(cached, chunks)]
+    need = [math.ceil(n / bs) for n in lens]
+    total = sum(need)
+    nb = num_blocks if num_blocks is not None else total + 8
+    assert nb >= total
+    gen_cpu = torch.Generator().manual_seed(seed)
+    perm = torch.randperm(nb, generator=gen_cpu).tolist()
+    mb = max([1] + need)
+    tables = torch.zeros((b, mb), dtype=torch.int32)
+    cur = 0
+    for i, n in enumerate(need):
+        if n:
+            tables[i, :n] = torch.tensor(perm[cur:cur + n], dtype=torch.int32)
+        cur += n
+    qs = [0]
+    for n in chunks:
+        qs.append(qs[-1] + n)
+    rows = qs[-1] + extra_rows
+    pos, seq_of = [], []
+    for i, (c, n) in enumerate(zip(cached, chunks)):
+        pos += list(range(c, c + n))
+        seq_of += [i] * n
+    gen = torch.Generator(device=device).manual_seed(seed + 1)
+    kv = _randn((nb, 2, num_kv_heads, bs, head_dim), dtype, gen, device)
+    q = _randn((rows, num_q_heads, head_dim), dtype, gen, device)
+    k_new = _randn((qs[-1], num_kv_heads, head_dim), dtype, gen, device)
+    v_new = _randn((qs[-1], num_kv_heads, head_dim), dtype, gen, device)
+    return PrefillWorkload(
+        name=name, dtype=dtype, num_seqs=b, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+        head_dim=head_dim, block_size=bs, num_blocks=nb, kv=kv, q=q, k_new=k_new, v_new=v_new,
+        new_positions=torch.tensor(pos, dtype=torch.int64).to(device),
+        row_seq=torch.tensor(seq_of, dtype=torch.int64).to(device),
+        block_tables=tables.to(device), query_start=torch.tensor(qs, dtype=torch.int32).to(device),
+        context_lens=torch.tensor(lens, dtype=torch.int32).to(device), chunk_lens=chunks,
+        scale=1.0 / math.sqrt(head_dim), meta={"seed": seed, "cached": cached})
+
+
+def prefill7b(device="cpu", seed=5, num_seqs=4, prompt=2048):
+    """Whole prompts: 4 sequences of 2048 new tokens on an empty cache, Llama-2-7B MHA
+    layer (32 heads of 128), block 16, fp16."""
+    return make_prefill_workload(
+        name="prefill7b", num_q_heads=32, num_kv_heads=32, head_dim=128, block_size=16,
+        cached_lens=[0] * num_seqs, chunk_lens=[prompt] * num_seqs, dtype=torch.float16,
+        seed=seed, device=device)
+
+
+def chunked70b(device="cpu", seed=6, num_seqs=8, chunk=512, hi=7680):
+    """Chunked prefill behind long contexts: 8 sequences, each a 512-token chunk after
+    U[0, 7680] cached tokens, Llama-2-70B GQA layer (64 q / 8 kv heads), block 16, bf16."""
+    cached = _uniform_lens(num_seqs, 0, hi, seed)
+    return make_prefill_workload(
+        name="chunked70b", num_q_heads=64, num_kv_heads=8, head_dim=128, block_size=16,
+        cached_lens=cached, chunk_lens=[chunk] * num_seqs, dtype=torch.bfloat16, seed=seed,
+        device=device)
+
+
+PREFILL_NAMED = {"prefill7b": prefill7b, "chunked70b": chunked70b}
 
 
 NAMED = {"tiny": tiny, "mha7b": mha7b, "gqa7b": gqa7b, "prefix": prefix, "long70b": long70b,

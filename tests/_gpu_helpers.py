@@ -108,3 +108,47 @@ def oracle_decode_int8(wl, pool_i8, sel=None, tables=None):
     return oracle.paged_decode_int8(q, pool_i8, wl.k_scale.cpu().numpy(), wl.v_scale.cpu().numpy(),
                                     bt, lens, wl.num_kv_heads, wl.block_size, wl.scale,
                                     dtype_code(wl.dtype))
+
+
+# ---------------------------------------------------------------- chunked prefill
+def run_prefill(wl, kv_splits=0):
+    """The library's prefill step on device: the chunk rows' K/V written at their
+    positions, then chunked prefill attention.  Returns out (device)."""
+    k_cache, v_cache = pkv.split_pool(wl.kv)
+    n = int(wl.query_start[-1])
+    if n:
+        rows_tables = wl.block_tables.cpu()[wl.row_seq.cpu()]
+        slots = pkv.slot_mapping(rows_tables, wl.new_positions.cpu(), wl.block_size)
+        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots.to(wl.kv.device), k_cache, v_cache)
+    out = torch.zeros_like(wl.q)
+    return pkv.paged_attention_prefill(wl.q, k_cache, v_cache, wl.block_tables, wl.query_start,
+                                       wl.context_lens, wl.scale, out,
+                                       max_query_len=wl.max_query_len,
+                                       max_context_len=wl.max_context_len, kv_splits=kv_splits)
+
+
+def oracle_prefill_step(pool_bits: np.ndarray, wl, rows=None):
+    """Oracle cache write of the chunk rows into a host pool copy (in place), then the
+    oracle prefill of every chunk row -- or, with rows = [(seq, j), ...], of just those
+    rows (each as a one-row chunk at its own position).  Returns fp64 outputs."""
+    bt = wl.block_tables.cpu().numpy()
+    n = int(wl.query_start[-1])
+    if n:
+        slots = oracle.slot_mapping(bt[wl.row_seq.cpu().numpy()], wl.new_positions.cpu().numpy(),
+                                    wl.block_size)
+        oracle.reshape_and_cache(to_bits(wl.k_new.cpu()), to_bits(wl.v_new.cpu()), slots, pool_bits,
+                                 wl.num_kv_heads, wl.block_size, wl.head_dim)
+    flat = np.ascontiguousarray(pool_bits).reshape(-1)
+    half = pool_bits.shape[2] * pool_bits.shape[3] * pool_bits.shape[4]
+    q = to_bits(wl.q.cpu())
+    qs = wl.query_start.cpu().numpy()
+    lens = wl.context_lens.cpu().numpy()
+    if rows is None:
+        return oracle.paged_prefill(q[:n], flat, flat[half:], 2 * half, bt, qs, lens,
+                                    wl.num_kv_heads, wl.block_size, wl.scale, dtype_code(wl.dtype))
+    sel_q = np.stack([q[qs[i] + j] for i, j in rows])
+    sel_bt = np.stack([bt[i] for i, _ in rows])
+    sel_len = np.array([lens[i] - (qs[i + 1] - qs[i]) + j + 1 for i, j in rows], dtype=np.int32)
+    return oracle.paged_prefill(sel_q, flat, flat[half:], 2 * half, sel_bt,
+                                np.arange(len(rows) + 1), sel_len, wl.num_kv_heads, wl.block_size,
+                                wl.scale, dtype_code(wl.dtype))

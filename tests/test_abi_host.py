@@ -150,6 +150,37 @@ def test_int8_entry_points_reject_bad_arguments_on_host(lib):
     assert lib.pkv_decode_int8_workspace_bytes(4, 32, 8, 128, 16, 500, 512) == 0
 
 
+def test_prefill_rejects_bad_arguments_on_host(lib):
+    def pf(**kw):
+        a = dict(q=16, k=16, v=16, nb=64, stride=2 * 4 * 16 * 128, bt=16, mb=8, qs=16, cl=16,
+                 rows=100, mq=50, mc=100, b=4, hq=8, hkv=4, d=128, bs=16, scale=0.125, out=16,
+                 ws=None, wsb=0, splits=1, dt=0)
+        a.update(kw)
+        return lib.pkv_paged_attention_prefill(
+            a["q"], a["k"], a["v"], a["nb"], a["stride"], a["bt"], a["mb"], a["qs"], a["cl"],
+            a["rows"], a["mq"], a["mc"], a["b"], a["hq"], a["hkv"], a["d"], a["bs"], a["scale"],
+            a["out"], a["ws"], a["wsb"], a["splits"], a["dt"], None)
+
+    assert pf(d=64) == UNSUPPORTED                   # head_dim 128 only
+    assert pf(bs=64) == UNSUPPORTED
+    assert pf(dt=2) == UNSUPPORTED
+    assert pf(hq=6) == INVALID
+    assert pf(mc=40) == INVALID                      # context bound below the chunk bound
+    assert pf(mc=8 * 16 + 1, mq=1) == INVALID        # beyond the tables
+    assert pf(splits=-1) == INVALID
+    assert pf(scale=float("inf")) == INVALID
+    assert pf(qs=0) == INVALID
+    assert pf(stride=2 * 4 * 16 * 128 + 4) == INVALID
+    assert pf(splits=2, mc=1000, mb=100) == INVALID  # a split plan needs a workspace
+    assert pf(b=0) == 0 and pf(rows=0) == 0 and pf(mq=0) == 0   # nothing to do
+    # explicit splits: whole 128-token tiles, partials of (d + 2) floats per row and split
+    ws = lib.pkv_prefill_workspace_bytes(100, 4, 8, 4, 128, 16, 50, 1000, 3)
+    assert ws == 100 * 8 * 3 * (128 + 2) * 4
+    assert lib.pkv_prefill_workspace_bytes(100, 4, 8, 4, 128, 16, 50, 1000, 1) == 0
+    assert lib.pkv_prefill_workspace_bytes(100, 4, 8, 4, 128, 16, 50, 100, 5) == 0  # one tile
+    assert lib.pkv_prefill_workspace_bytes(100, 4, 8, 4, 64, 16, 50, 100, 1) == ctypes.c_size_t(-1).value
+
+
 def plan(lib, b, hq, hkv, d, bs, maxl, part, sm=152):
     outs = [ctypes.c_int() for _ in range(4)]
     st = lib.pkv_decode_plan(b, hq, hkv, d, bs, maxl, part, sm, *[ctypes.byref(o) for o in outs])
