@@ -223,3 +223,17 @@ def test_int8_named_workload_full_size(name):
     assert np.array_equal(wl.kv.cpu().numpy(), pool), "INT8 cache write not bit-exact"
     sel = _sample(wl)
     assert_close(out[sel], oracle_decode_int8(wl, pool, sel=sel), what=name)
+
+
+@pytest.mark.parametrize("qmag", [3e4, 1e-6], ids=["large", "tiny"])
+def test_int8_tensor_core_query_range(qmag):
+    """GQA over an INT8 pool runs on the tensor cores with the query folded into fp16
+    (q * k_scale * 2^-e per head row): queries whose q * k_scale exceeds the fp16 range,
+    or sits in its subnormals, still match the oracle (scale chosen to keep scores O(1))."""
+    dev = device()
+    wl = make_decode_workload(num_seqs=4, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                              block_size=16, context_lens=[2100, 1, 700, 2500],
+                              dtype=torch.bfloat16, seed=21, device=str(dev), kv_dtype=torch.int8)
+    wl.q.mul_(qmag)
+    wl.scale = 1.0 / (qmag * 128 ** 0.5)
+    _check_step(wl)
