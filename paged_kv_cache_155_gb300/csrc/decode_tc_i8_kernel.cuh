@@ -20,13 +20,15 @@
 //   * P is rounded to fp16 for the second MMA (p <= 1), O^T = codes^T . P^T,
 //     and the V scale multiplies each output channel once at the end.
 //
-// Warps (320 threads, one persistent CTA per SM):
-//   0      producer: 1-D bulk copies of each block's code rows (block_size x
-//          128 bytes per head) into INT8 staging rings for K and V;
+// Warps (352 threads, one persistent CTA per SM):
+//   0 / 6  K / V producers: 1-D bulk copies of each block's code rows
+//          (block_size x 128 bytes per head) into INT8 staging rings;
 //   1      TMEM owner and MMA issuer (event-driven, PV first), writes the
 //          scaled fp16 query panels and each item's score scales;
 //   2-5    softmax and accumulation (as paged_decode_tc_kernel);
-//   6-9    converters: staged codes -> fp16 K / V ring slots.
+//   7-8    K converters, 9-10 V converters: staged codes -> fp16 ring slots.
+// K and V move through separate producers, staging rings and converters, so
+// a V slot still waiting for its PV never holds back the next tile's K.
 // Every wait is bounded; a timeout raises PKV_DEVERR_TIMEOUT and all roles stop.
 #pragma once
 
@@ -36,7 +38,7 @@ namespace pkv {
 
 struct TcI8Layout {
     static constexpr int kTile = 128, kD = 128, kN = 16;
-    static constexpr int kStage = 2;                     // INT8 staging slots (K and V each)
+    static constexpr int kStageK = 2, kStageV = 2;       // INT8 staging slots
     static constexpr int kKStages = 2, kVStages = 2;     // fp16 ring slots
     static constexpr int kStageBytes = 128 * 128;        // 128 tokens x 128 codes
     static constexpr int kHalfBytes = 128 * 128;         // 128 rows x 64 fp16
@@ -44,22 +46,24 @@ struct TcI8Layout {
     static constexpr int kPanelBytes = 4096;             // 16 x 128 fp16 (Q or P)
     static constexpr int kQsRing = 4;                    // per-item score scales in flight
     static constexpr int kOffSK = 0;
-    static constexpr int kOffSV = kOffSK + kStage * kStageBytes;
-    static constexpr int kOffK = kOffSV + kStage * kStageBytes;
+    static constexpr int kOffSV = kOffSK + kStageK * kStageBytes;
+    static constexpr int kOffK = kOffSV + kStageV * kStageBytes;
     static constexpr int kOffV = kOffK + kKStages * kKVBytes;
     static constexpr int kOffQ = kOffV + kVStages * kKVBytes;
     static constexpr int kOffP = kOffQ + 2 * kPanelBytes;
     static constexpr int kOffRed = kOffP + 2 * kPanelBytes;          // float [2][4][16] + [4][16]
     static constexpr int kOffQs = kOffRed + 3 * 4 * 16 * 4;          // float [kQsRing][16]
     static constexpr int kOffBar = kOffQs + kQsRing * 16 * 4;
-    static constexpr int kNumBars = 4 * kStage + 2 * kKStages + 2 * kVStages + 13 + kQsRing + 1;
+    static constexpr int kNumBars = 2 * kStageK + 2 * kStageV + 2 * kKStages + 2 * kVStages + 13 +
+                                    kQsRing + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kMaxStagedSeqs = 1024;
     static constexpr int kOffLens = kOffMisc + 16;
     static constexpr int kBytes = kOffLens + 4 * kMaxStagedSeqs;
     static constexpr int kSmemBytes = kBytes + 1024;
     static constexpr uint32_t kTmemCols = 64;  // S[2] at 0/16, O[2] at 32/48
-    static constexpr int kThreads = 320;
+    static constexpr int kThreads = 352;
+    static_assert(kSmemBytes <= 232448, "dynamic shared memory per block");
 };
 
 // Four INT8 codes (one word) -> four exact fp16 values (two words): each code,
@@ -90,11 +94,11 @@ __device__ __forceinline__ float exp2_int(int e) {  // 2^e, e in [-126, 127]
 }
 
 template <typename T, int BS, int GH>
-__global__ void __launch_bounds__(320, 1) paged_decode_tc_i8_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(352, 1) paged_decode_tc_i8_kernel(const DecodeParams p) {
     using L = TcI8Layout;
     constexpr int TILE = L::kTile, D = L::kD;
     constexpr int BLOCKS_PER_TILE = TILE / BS;
-    constexpr int ST = L::kStage, KS = L::kKStages, VS = L::kVStages;
+    constexpr int STK = L::kStageK, STV = L::kStageV, KS = L::kKStages, VS = L::kVStages;
     static_assert(GH == 4 || GH == 8 || GH == 16, "tensor-core path serves 4, 8 or 16 heads");
     static_assert(BLOCKS_PER_TILE <= 32, "one table entry per producer lane");
 
@@ -102,11 +106,11 @@ __global__ void __launch_bounds__(320, 1) paged_decode_tc_i8_kernel(const Decode
     unsigned char *sm =
         smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
-    uint64_t *sk_full = bars;             // [ST] codes of K landed -> converters
-    uint64_t *sk_empty = sk_full + ST;    // [ST] K codes converted -> producer
-    uint64_t *sv_full = sk_empty + ST;    // [ST]
-    uint64_t *sv_empty = sv_full + ST;    // [ST]
-    uint64_t *k_full = sv_empty + ST;     // [KS] fp16 K tile written -> MMA
+    uint64_t *sk_full = bars;             // [STK] codes of K landed -> K converters
+    uint64_t *sk_empty = sk_full + STK;   // [STK] K codes converted -> K producer
+    uint64_t *sv_full = sk_empty + STK;   // [STV]
+    uint64_t *sv_empty = sv_full + STV;   // [STV]
+    uint64_t *k_full = sv_empty + STV;    // [KS] fp16 K tile written -> MMA
     uint64_t *k_empty = k_full + KS;      // [KS] QK^T done -> converters
     uint64_t *v_full = k_empty + KS;      // [VS]
     uint64_t *v_empty = v_full + VS;      // [VS] PV done -> converters
@@ -133,18 +137,20 @@ __global__ void __launch_bounds__(320, 1) paged_decode_tc_i8_kernel(const Decode
     for (int i = threadIdx.x; i < 4 * L::kPanelBytes / 16; i += blockDim.x)
         reinterpret_cast<uint4 *>(sm + L::kOffQ)[i] = make_uint4(0, 0, 0, 0);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < ST; ++s) {
+        for (int s = 0; s < STK; ++s) {
             mbar_init(&sk_full[s], 1);
-            mbar_init(&sk_empty[s], 4);
+            mbar_init(&sk_empty[s], 2);  // the two K converter warps
+        }
+        for (int s = 0; s < STV; ++s) {
             mbar_init(&sv_full[s], 1);
-            mbar_init(&sv_empty[s], 4);
+            mbar_init(&sv_empty[s], 2);
         }
         for (int s = 0; s < KS; ++s) {
-            mbar_init(&k_full[s], 4);
+            mbar_init(&k_full[s], 2);
             mbar_init(&k_empty[s], 1);
         }
         for (int s = 0; s < VS; ++s) {
-            mbar_init(&v_full[s], 4);
+            mbar_init(&v_full[s], 2);
             mbar_init(&v_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -182,15 +188,19 @@ __global__ void __launch_bounds__(320, 1) paged_decode_tc_i8_kernel(const Decode
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ===================== producer: INT8 code rows -> staging =====================
+    if (warp == 0 || warp == 6) {
+        // ===================== producers: INT8 code rows -> staging (K: warp 0, V: warp 6)
+        const int kv = warp == 6;
+        const int nst = kv ? STV : STK;
         const uint64_t policy = l2_policy_evict_first();
-        const int8_t *kc = static_cast<const int8_t *>(p.k_cache);
-        const int8_t *vc = static_cast<const int8_t *>(p.v_cache);
+        const int8_t *base = static_cast<const int8_t *>(kv ? p.v_cache : p.k_cache);
+        uint64_t *full = kv ? sv_full : sk_full;
+        uint64_t *empty = kv ? sv_empty : sk_empty;
+        unsigned char *stage0 = sm + (kv ? L::kOffSV : L::kOffSK);
         ItemWalker walk;
         uint32_t g = 0;  // global tile counter
-        int last_issue[2][ST];
-        for (int i = 0; i < 2 * ST; ++i) last_issue[i / ST][i % ST] = -1;
+        int last_issue[3] = {-1, -1, -1};
+        static_assert(L::kStageK <= 3 && L::kStageV <= 3, "drain bookkeeping");
         bool ok = true;
         for (int64_t r = blockIdx.x; ok; r += gridDim.x) {
             int y, part;
@@ -211,46 +221,48 @@ __global__ void __launch_bounds__(320, 1) paged_decode_tc_i8_kernel(const Decode
                     }
                 }
                 const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, e >= 0)) * BS * 128u;
-                const int s = g % ST;
-                for (int kv = 0; kv < 2; ++kv) {
-                    uint64_t *fb = kv ? &sv_full[s] : &sk_full[s];
-                    uint64_t *eb = kv ? &sv_empty[s] : &sk_empty[s];
-                    int go = 1;
-                    if (lane == 0) {
-                        go = tc_wait(eb, ((g / ST) & 1) ^ 1, abort_flag, p.status);
-                        if (go) {
-                            if (bytes) mbar_arrive_expect_tx(fb, bytes);
-                            else mbar_arrive(fb);
-                            last_issue[kv][s] = static_cast<int>(g);
-                        }
+                const int s = g % nst;
+                int go = 1;
+                if (lane == 0) {
+                    go = tc_wait(&empty[s], ((g / nst) & 1) ^ 1, abort_flag, p.status);
+                    if (go) {
+                        if (bytes) mbar_arrive_expect_tx(&full[s], bytes);
+                        else mbar_arrive(&full[s]);
+                        last_issue[s] = static_cast<int>(g);
                     }
-                    if (!__shfl_sync(0xffffffffu, go, 0)) {
-                        ok = false;
-                        break;
-                    }
-                    if (e >= 0) {
-                        const int8_t *src = (kv ? vc : kc) + static_cast<int64_t>(e) * p.block_stride +
-                                            static_cast<int64_t>(kvh) * BS * D;
-                        unsigned char *dst = sm + (kv ? L::kOffSV : L::kOffSK) + s * L::kStageBytes +
-                                             lane * BS * D;
-                        bulk_copy_g2s(dst, src, BS * D, fb, policy);
-                    }
-                    __syncwarp();
                 }
+                if (!__shfl_sync(0xffffffffu, go, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (e >= 0)
+                    bulk_copy_g2s(stage0 + s * L::kStageBytes + lane * BS * D,
+                                  base + static_cast<int64_t>(e) * p.block_stride +
+                                      static_cast<int64_t>(kvh) * BS * D,
+                                  BS * D, &full[s], policy);
+                __syncwarp();
             }
         }
         if (!ok && lane == 0) {
-            for (int kv = 0; kv < 2; ++kv)
-                for (int s = 0; s < ST; ++s)
-                    if (last_issue[kv][s] >= 0)
-                        mbar_wait_bounded(kv ? &sv_full[s] : &sk_full[s], (last_issue[kv][s] / ST) & 1,
-                                          kDrainTimeoutNs);
+            for (int s = 0; s < nst; ++s)
+                if (last_issue[s] >= 0)
+                    mbar_wait_bounded(&full[s], (last_issue[s] / nst) & 1, kDrainTimeoutNs);
         }
-    } else if (warp >= 6) {
+    } else if (warp >= 7) {
         // ===================== converters: staged codes -> fp16 ring slots =====================
-        // Thread c (0..127) widens 16-code groups c, c + 128, ...: row = idx / 8 (token),
-        // columns 16 * (idx % 8) .. + 15, written as two swizzled 16-byte chunks.
-        const int c = threadIdx.x - 192;
+        // K: warps 7-8, V: warps 9-10.  Thread c (0..63) widens 16-code groups
+        // c, c + 64, ...: row = idx / 8 (token), columns 16 * (idx % 8) .. + 15,
+        // written as two swizzled 16-byte chunks.
+        const int kv = warp >= 9;
+        const int c = threadIdx.x - (kv ? 288 : 224);
+        const int nsg = kv ? STV : STK;   // staging slots
+        const int nst = kv ? VS : KS;     // ring slots
+        uint64_t *sfull0 = kv ? sv_full : sk_full;
+        uint64_t *sempty0 = kv ? sv_empty : sk_empty;
+        uint64_t *rfull0 = kv ? v_full : k_full;
+        uint64_t *rempty0 = kv ? v_empty : k_empty;
+        const unsigned char *src0 = sm + (kv ? L::kOffSV : L::kOffSK);
+        unsigned char *dst0 = sm + (kv ? L::kOffV : L::kOffK);
         ItemWalker walk;
         uint32_t g = 0;
         bool ok = true;
@@ -259,44 +271,36 @@ __global__ void __launch_bounds__(320, 1) paged_decode_tc_i8_kernel(const Decode
             if (!walk.seek(p, s_len, r, y, part)) break;
             const int tok0 = p.tok_begin + part * p.partition_size;
             const int ntok = max(0, min(walk.len, tok0 + p.partition_size) - tok0);
-            for (int t0 = 0; t0 < ntok && ok; t0 += TILE, ++g) {
-                const int s = g % ST;
-                for (int kv = 0; kv < 2 && ok; ++kv) {
-                    const int nst = kv ? VS : KS;
-                    const int slot = g % nst;
-                    uint64_t *sfull = kv ? &sv_full[s] : &sk_full[s];
-                    uint64_t *sempty = kv ? &sv_empty[s] : &sk_empty[s];
-                    uint64_t *rfull = kv ? &v_full[slot] : &k_full[slot];
-                    uint64_t *rempty = kv ? &v_empty[slot] : &k_empty[slot];
-                    if (!tc_wait_warp(sfull, (g / ST) & 1, abort_flag, p.status) ||
-                        !tc_wait_warp(rempty, ((g / nst) & 1) ^ 1, abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    const unsigned char *src = sm + (kv ? L::kOffSV : L::kOffSK) + s * L::kStageBytes;
-                    unsigned char *dst = sm + (kv ? L::kOffV : L::kOffK) + slot * L::kKVBytes;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int idx = c + 128 * i;
-                        const int row = idx >> 3, grp = idx & 7;
-                        const uint4 w = *reinterpret_cast<const uint4 *>(src + row * 128 + grp * 16);
-                        uint4 a, b;
-                        codes_to_f16x4(w.x, a.x, a.y);
-                        codes_to_f16x4(w.y, a.z, a.w);
-                        codes_to_f16x4(w.z, b.x, b.y);
-                        codes_to_f16x4(w.w, b.z, b.w);
-                        // columns 16*grp .. +15 -> half grp / 4, 8-column chunks 2*(grp%4), +1
-                        unsigned char *half = dst + (grp >> 2) * L::kHalfBytes + row * 128;
-                        const int ch = (grp & 3) * 2;
-                        *reinterpret_cast<uint4 *>(half + (((ch) ^ (row & 7)) << 4)) = a;
-                        *reinterpret_cast<uint4 *>(half + (((ch + 1) ^ (row & 7)) << 4)) = b;
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(rfull);
-                        mbar_arrive(sempty);
-                    }
+            for (int t0 = 0; t0 < ntok; t0 += TILE, ++g) {
+                const int s = g % nsg, slot = g % nst;
+                if (!tc_wait_warp(&sfull0[s], (g / nsg) & 1, abort_flag, p.status) ||
+                    !tc_wait_warp(&rempty0[slot], ((g / nst) & 1) ^ 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                const unsigned char *src = src0 + s * L::kStageBytes;
+                unsigned char *dst = dst0 + slot * L::kKVBytes;
+#pragma unroll 4
+                for (int i = 0; i < 16; ++i) {
+                    const int idx = c + 64 * i;
+                    const int row = idx >> 3, grp = idx & 7;
+                    const uint4 w = *reinterpret_cast<const uint4 *>(src + row * 128 + grp * 16);
+                    uint4 a, b;
+                    codes_to_f16x4(w.x, a.x, a.y);
+                    codes_to_f16x4(w.y, a.z, a.w);
+                    codes_to_f16x4(w.z, b.x, b.y);
+                    codes_to_f16x4(w.w, b.z, b.w);
+                    // columns 16*grp .. +15 -> half grp / 4, 8-column chunks 2*(grp%4), +1
+                    unsigned char *half = dst + (grp >> 2) * L::kHalfBytes + row * 128;
+                    const int ch = (grp & 3) * 2;
+                    *reinterpret_cast<uint4 *>(half + ((ch ^ (row & 7)) << 4)) = a;
+                    *reinterpret_cast<uint4 *>(half + (((ch + 1) ^ (row & 7)) << 4)) = b;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&rfull0[slot]);
+                    mbar_arrive(&sempty0[s]);
                 }
             }
         }
@@ -382,12 +386,12 @@ __global__ void __launch_bounds__(320, 1) paged_decode_tc_i8_kernel(const Decode
         while (ok && (have_tile || n_pv < n_qk)) {
             int act = 0;  // 1 = PV, 2 = QK
             if (lane == 0) {
-                if (n_pv < n_qk && mbar_try_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
-                    mbar_try_wait(&o_empty[n_pv & 1], ((n_pv >> 1) & 1) ^ 1) &&
-                    mbar_try_wait(&v_full[n_pv % VS], (n_pv / VS) & 1))
+                if (n_pv < n_qk && mbar_test_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
+                    mbar_test_wait(&o_empty[n_pv & 1], ((n_pv >> 1) & 1) ^ 1) &&
+                    mbar_test_wait(&v_full[n_pv % VS], (n_pv / VS) & 1))
                     act = 1;
-                else if (have_tile && mbar_try_wait(&k_full[n_qk % KS], (n_qk / KS) & 1) &&
-                         mbar_try_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
+                else if (have_tile && mbar_test_wait(&k_full[n_qk % KS], (n_qk / KS) & 1) &&
+                         mbar_test_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
                     act = 2;
                 if (act) {
                     idle_since = 0;

@@ -340,12 +340,12 @@ __global__ void __launch_bounds__(192, 1)
         while (ok && (have_tile || n_pv < n_qk)) {
             int act = 0;  // 1 = PV, 2 = QK
             if (lane == 0) {
-                if (n_pv < n_qk && mbar_try_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
-                    mbar_try_wait(&o_empty[n_pv & 1], ((n_pv >> 1) & 1) ^ 1) &&
-                    mbar_try_wait(&v_full[n_pv % VS], (n_pv / VS) & 1))
+                if (n_pv < n_qk && mbar_test_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
+                    mbar_test_wait(&o_empty[n_pv & 1], ((n_pv >> 1) & 1) ^ 1) &&
+                    mbar_test_wait(&v_full[n_pv % VS], (n_pv / VS) & 1))
                     act = 1;
-                else if (have_tile && mbar_try_wait(&k_full[n_qk % KS], (n_qk / KS) & 1) &&
-                         mbar_try_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
+                else if (have_tile && mbar_test_wait(&k_full[n_qk % KS], (n_qk / KS) & 1) &&
+                         mbar_test_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
                     act = 2;
                 if (act) {
                     idle_since = 0;

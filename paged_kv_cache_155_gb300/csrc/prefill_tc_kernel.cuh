@@ -213,11 +213,11 @@ __global__ void __launch_bounds__(192, 1)
         while (ok && n_pv < ntiles) {
             int act = 0;
             if (lane == 0) {
-                if (n_pv < n_qk && mbar_try_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
-                    mbar_try_wait(&v_full[n_pv & 1], (n_pv >> 1) & 1))
+                if (n_pv < n_qk && mbar_test_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
+                    mbar_test_wait(&v_full[n_pv & 1], (n_pv >> 1) & 1))
                     act = 1;
-                else if (n_qk < ntiles && mbar_try_wait(&k_full[n_qk & 1], (n_qk >> 1) & 1) &&
-                         mbar_try_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
+                else if (n_qk < ntiles && mbar_test_wait(&k_full[n_qk & 1], (n_qk >> 1) & 1) &&
+                         mbar_test_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
                     act = 2;
                 if (act) {
                     idle_since = 0;
