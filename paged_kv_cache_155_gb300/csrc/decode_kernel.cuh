@@ -19,8 +19,10 @@
 //    mbarrier per stage.  Each warp is its own producer and consumer: no
 //    CTA-wide barrier in the main loop.  Tiles are marked evict-first in L2.
 //  * Lane layout: a token row of head_dim 16-bit values is LPT = head_dim/8
-//    lanes x one 16-byte vector, so TPG = 32/LPT tokens are in flight per warp
-//    instruction and shared-memory reads are conflict-free.  The QK partial
+//    lanes x one 16-byte vector (INT8: head_dim/16 lanes x 16 codes for one or
+//    two heads per block, else head_dim/8 lanes x 8 codes), so TPG = 32/LPT
+//    tokens are in flight per warp instruction and shared-memory reads are
+//    conflict-free.  The QK partial
 //    sums are reduced across the LPT lanes with xor shuffles; the PV update is
 //    lane-local (each lane owns 8 output dims of every head of the group).
 //  * GQA: all GH query heads of the group share each K/V tile, so a tile is
@@ -81,19 +83,45 @@ __device__ __forceinline__ int partitions_of(const DecodeParams &p, int len) {
     return span > 0 ? (span + p.partition_size - 1) / p.partition_size : 1;
 }
 
-// Decode-kernel geometry for one (head_dim, block_size, cache element bytes).
-template <int D, int BS, int EB = 2>
+// Values per lane vector of the CUDA-core kernel (see DecodeGeom).
+template <typename KT, int GH>
+__host__ __device__ constexpr int decode_lane_values() {
+    return (sizeof(KT) == 1 && GH <= 2) ? 16 : 8;
+}
+
+// One lane's VL consecutive cache values of a row in shared memory -> fp32.
+template <typename KT, int VL>
+__device__ __forceinline__ void load_lane(const KT *src, float *f) {
+    if constexpr (sizeof(KT) == 2) {
+        static_assert(VL == 8, "16-bit caches use 8 values per lane");
+        Elem<KT>::to_f32x8(*reinterpret_cast<const uint4 *>(src), f);
+    } else if constexpr (VL == 8) {
+        Elem<KT>::to_f32x8(*reinterpret_cast<const uint2 *>(src), f);
+    } else {
+        const uint4 u = *reinterpret_cast<const uint4 *>(src);
+        Elem<KT>::to_f32x8(make_uint2(u.x, u.y), f);
+        Elem<KT>::to_f32x8(make_uint2(u.z, u.w), f + 8);
+    }
+}
+
+// Decode-kernel geometry for one (head_dim, block_size, cache element bytes,
+// values per lane vector).  16-bit caches use 8 values (16 bytes) per lane;
+// the INT8 cache uses 16 codes (16 bytes) per lane when a block serves at most
+// two query heads (fewer lanes per token row: shorter shuffle reductions and
+// fewer per-row steps per byte), else 8 codes (register budget).  INT8 stages
+// get a smaller per-warp budget so three CTAs fit on an SM.
+template <int D, int BS, int EB = 2, int VL = 8>
 struct DecodeGeom {
     static constexpr int kWarps = 4;
     static constexpr int kMaxTile = 32 / EB;             // 4 KiB K tiles at head_dim 128
     static constexpr int kTile = BS < kMaxTile ? BS : kMaxTile;  // tokens per stage
-    static constexpr int kVec = 8;                       // values per lane vector (8 * EB bytes)
+    static constexpr int kVec = VL;                      // values per lane vector
     static constexpr int kLanesPerToken = D / kVec;      // LPT
     static constexpr int kTokenGroups = 32 / kLanesPerToken;  // TPG
     static constexpr int kIters = kTile / kTokenGroups;  // token rows per lane per stage
     static constexpr int kTileBytes = kTile * D * EB;    // one K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStagesRaw = 24576 / kStageBytes;
+    static constexpr int kStagesRaw = (EB == 1 ? 16384 : 24576) / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kMaxTableEntries = 1024;        // table slice per partition
     static constexpr int kSmemBytes = kWarps * kStages * kStageBytes +
@@ -105,8 +133,8 @@ struct DecodeGeom {
 template <typename T, typename KT, int D, int BS, int GH>
 __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams p) {
     constexpr bool kQuant = sizeof(KT) == 1;
-    using G = DecodeGeom<D, BS, sizeof(KT)>;
-    using KVec = typename Elem<KT>::Vec;
+    constexpr int VL = decode_lane_values<KT, GH>();  // values per lane vector
+    using G = DecodeGeom<D, BS, sizeof(KT), VL>;
     constexpr int NW = G::kWarps, S = G::kStages, TILE = G::kTile, LPT = G::kLanesPerToken,
                   TPG = G::kTokenGroups, ITERS = G::kIters;
     // token rows processed between two online-softmax updates (bounds registers)
@@ -187,37 +215,45 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
     }
 
     // ---- per-lane query slice (pre-scaled) and accumulators
-    const int sub = lane % LPT;   // which 8 dims
+    const int sub = lane % LPT;   // which VL dims
     const int grp = lane / LPT;   // which token row of a TPG-row step
-    float qf[GH][8];
+    float qf[GH][VL];
     {
         const T *qb = static_cast<const T *>(p.q) +
-                      (static_cast<int64_t>(seq) * p.num_q_heads + hq0) * D + sub * 8;
+                      (static_cast<int64_t>(seq) * p.num_q_heads + hq0) * D + sub * VL;
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(qb + g * D);
-            Elem<T>::to_f32x8(u, qf[g]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) qf[g][e] *= p.scale_log2;
+            for (int v = 0; v < VL; v += 8) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(qb + g * D + v);
+                Elem<T>::to_f32x8(u, qf[g] + v);
+            }
+#pragma unroll
+            for (int e = 0; e < VL; ++e) qf[g][e] *= p.scale_log2;
         }
         if constexpr (kQuant) {  // K dequantisation folded into the query
-            const float4 *ks = reinterpret_cast<const float4 *>(p.k_scale + kvh * D + sub * 8);
-            const float4 a = ks[0], b = ks[1];
-            const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            const float4 *ks = reinterpret_cast<const float4 *>(p.k_scale + kvh * D + sub * VL);
 #pragma unroll
-            for (int g = 0; g < GH; ++g)
+            for (int v = 0; v < VL / 4; ++v) {
+                const float4 a = ks[v];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) qf[g][e] *= f[e];
+                for (int g = 0; g < GH; ++g) {
+                    qf[g][4 * v] *= a.x;
+                    qf[g][4 * v + 1] *= a.y;
+                    qf[g][4 * v + 2] *= a.z;
+                    qf[g][4 * v + 3] *= a.w;
+                }
+            }
         }
     }
-    float acc[GH][8];
+    float acc[GH][VL];
     float m[GH], l[GH];
 #pragma unroll
     for (int g = 0; g < GH; ++g) {
         m[g] = -INFINITY;
         l[g] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+        for (int e = 0; e < VL; ++e) acc[g][e] = 0.f;
     }
 
     bool aborted = false;
@@ -248,14 +284,13 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
 #pragma unroll
                 for (int it = 0; it < IT_STEP; ++it) {
                     const int t = (it0 + it) * TPG + grp;
-                    const KVec u = *reinterpret_cast<const KVec *>(ks + t * D + sub * 8);
-                    float kf[8];
-                    Elem<KT>::to_f32x8(u, kf);
+                    float kf[VL];
+                    load_lane<KT, VL>(ks + t * D + sub * VL, kf);
 #pragma unroll
                     for (int g = 0; g < GH; ++g) {
                         float a = 0.f;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) a = fmaf(qf[g][e], kf[e], a);
+                        for (int e = 0; e < VL; ++e) a = fmaf(qf[g][e], kf[e], a);
                         sc[it][g] = a;
                     }
                 }
@@ -289,7 +324,7 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                         const float alpha = fast_exp2(m[g] - mx);  // 0 when m was -inf
                         l[g] *= alpha;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+                        for (int e = 0; e < VL; ++e) acc[g][e] *= alpha;
                         m[g] = mx;
                     }
 #pragma unroll
@@ -303,13 +338,12 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                 for (int it = 0; it < IT_STEP; ++it) {
                     const int t = (it0 + it) * TPG + grp;
                     if (t < valid) {
-                        const KVec u = *reinterpret_cast<const KVec *>(vs + t * D + sub * 8);
-                        float vf[8];
-                        Elem<KT>::to_f32x8(u, vf);
+                        float vf[VL];
+                        load_lane<KT, VL>(vs + t * D + sub * VL, vf);
 #pragma unroll
                         for (int g = 0; g < GH; ++g)
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[g][e] = fmaf(sc[it][g], vf[e], acc[g][e]);
+                            for (int e = 0; e < VL; ++e) acc[g][e] = fmaf(sc[it][g], vf[e], acc[g][e]);
                     }
                 }
             }
@@ -328,7 +362,7 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
         for (int o = LPT; o < 32; o <<= 1) {
             l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
+            for (int e = 0; e < VL; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
         }
     }
     if (aborted) {
@@ -345,9 +379,10 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
     if (grp == 0) {
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
-            float4 *dst = reinterpret_cast<float4 *>(mine + g * (D + 4) + sub * 8);
-            dst[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-            dst[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+            float4 *dst = reinterpret_cast<float4 *>(mine + g * (D + 4) + sub * VL);
+#pragma unroll
+            for (int v = 0; v < VL / 4; ++v)
+                dst[v] = make_float4(acc[g][4 * v], acc[g][4 * v + 1], acc[g][4 * v + 2], acc[g][4 * v + 3]);
         }
     }
     if (lane == 0) {
