@@ -124,6 +124,29 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// max(a, b, c) / min(a, b, c) in one instruction (sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (a0, a1) += (b0, b1) as one packed fp32 add (sm_100 and later).
+__device__ __forceinline__ void add_f32x2(float &a0, float &a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rb, {%2, %3};\n\t"
+        "add.rn.f32x2 ra, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ void raise_flag(unsigned int *status, unsigned int flag) {
     atomicOr(status, flag);
 }
@@ -145,6 +168,11 @@ struct Elem<__half> {
         }
     }
     static __device__ __forceinline__ __half from_f32(float x) { return __float2half_rn(x); }
+    // two values rounded to nearest even, packed low / high (one conversion)
+    static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
 };
 
 template <>
@@ -161,6 +189,10 @@ struct Elem<__nv_bfloat16> {
     }
     static __device__ __forceinline__ __nv_bfloat16 from_f32(float x) {
         return __float2bfloat16_rn(x);
+    }
+    static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
     }
 };
 

@@ -17,8 +17,11 @@
 // row's columns past its own position are masked.  Same machinery as the
 // shared-prefix tile kernel: tcgen05 MMAs with M = 128 rows, N = 128 tokens,
 // K = 128; S double-buffered in TMEM, O accumulated in TMEM; a row's softmax is
-// local to one thread; the row's reference maximum moves only when a tile
-// exceeds it by more than kRescaleLog2.  With one split the kernel writes the
+// local to one thread (its 128 scores are read from TMEM once per tile); the
+// row's reference maximum moves only when a tile exceeds it by more than
+// kRescaleLog2.  The row sum l adds the fp32 weights whose bf16/fp16
+// roundings feed the PV MMA (unbiased rounding, relative error 2^-9 per weight
+// at most).  With one split the kernel writes the
 // normalised output; with several it writes (o, m, l) partials that
 // paged_prefill_merge_kernel combines.
 //
@@ -292,17 +295,33 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             tc::fence_after_sync();
-            // pass 1: tile maximum of this row over its visible columns
+            // this row's 128 scores, read from TMEM once
+            float x[TILE];
+#pragma unroll
+            for (int c = 0; c < TILE; c += 16) tc::tmem_ld_x16(lane_base + 128 * b + c, x + c);
+            tc::tmem_ld_wait();
+            // tiles no row of the warp sees only partly (all but the diagonal and the
+            // last) skip the per-column masks
+            const bool full = __all_sync(0xffffffffu, vr == TILE);
+            // tile maximum of the visible scaled scores: the extreme raw score times
+            // the scale (the maximum for a positive scale, the minimum otherwise)
             float tmax = -INFINITY;
+            if (vr > 0) {
+                const bool pos_scale = p.scale_log2 > 0.f;
+                float ext;
+                if (full) {
+                    ext = x[0];
 #pragma unroll
-            for (int c = 0; c < TILE; c += 32) {
-                float x[32];
-                tc::tmem_ld_x16(lane_base + 128 * b + c, x);
-                tc::tmem_ld_x16(lane_base + 128 * b + c + 16, x + 16);
-                tc::tmem_ld_wait();
+                    for (int i = 1; i + 1 < TILE; i += 2)
+                        ext = pos_scale ? fmax3(ext, x[i], x[i + 1]) : fmin3(ext, x[i], x[i + 1]);
+                    ext = pos_scale ? fmaxf(ext, x[TILE - 1]) : fminf(ext, x[TILE - 1]);
+                } else {
+                    ext = x[0];
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (c + i < vr) tmax = fmaxf(tmax, x[i] * p.scale_log2);
+                    for (int i = 1; i < TILE; ++i)
+                        if (i < vr) ext = pos_scale ? fmaxf(ext, x[i]) : fminf(ext, x[i]);
+                }
+                tmax = ext * p.scale_log2;
             }
             // the reference maximum moves only by more than kRescaleLog2 (a row that sees
             // nothing keeps -inf and alpha 1); TMEM loads and stores are warp-wide, so the
@@ -343,33 +362,29 @@ __global__ void __launch_bounds__(192, 1)
                 ok = false;
                 break;
             }
-            // pass 2: P = 2^(s - m_ref) on visible columns (0 elsewhere), rounded to T,
-            // into the K-major P panel
+            // P = 2^(s - m_ref) on visible columns (0 elsewhere), rounded to T into the
+            // K-major P panel; the row sum l adds the fp32 values
             unsigned char *prow = sm + L::kOffP + b * L::kPanel + r * 128;
+            float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-            for (int c = 0; c < TILE; c += 32) {
-                float x[32];
-                tc::tmem_ld_x16(lane_base + 128 * b + c, x);
-                tc::tmem_ld_x16(lane_base + 128 * b + c + 16, x + 16);
-                tc::tmem_ld_wait();
+            for (int c8 = 0; c8 < TILE / 8; ++c8) {
+                uint32_t packed[4];
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    uint32_t packed[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int t = c + c8 * 8 + 2 * i;
-                        const float p0 = t < vr ? fast_exp2(x[c8 * 8 + 2 * i] * p.scale_log2 - m_ref) : 0.f;
-                        const float p1 = t + 1 < vr ? fast_exp2(x[c8 * 8 + 2 * i + 1] * p.scale_log2 - m_ref) : 0.f;
-                        const T h0 = Elem<T>::from_f32(p0), h1 = Elem<T>::from_f32(p1);
-                        l += static_cast<float>(h0) + static_cast<float>(h1);
-                        packed[i] = static_cast<uint32_t>(reinterpret_cast<const uint16_t &>(h0)) |
-                                    (static_cast<uint32_t>(reinterpret_cast<const uint16_t &>(h1)) << 16);
+                for (int i = 0; i < 4; ++i) {
+                    const int t = c8 * 8 + 2 * i;
+                    float p0 = fast_exp2(fmaf(x[t], p.scale_log2, -m_ref));
+                    float p1 = fast_exp2(fmaf(x[t + 1], p.scale_log2, -m_ref));
+                    if (!full) {
+                        p0 = t < vr ? p0 : 0.f;
+                        p1 = t + 1 < vr ? p1 : 0.f;
                     }
-                    const int chunk8 = (c + c8 * 8) >> 3;  // 8-token chunk index, 0..15
-                    *reinterpret_cast<uint4 *>(prow + (chunk8 >> 3) * L::kHalf + (((chunk8 & 7) ^ (r & 7)) << 4)) =
-                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    add_f32x2(l0, l1, p0, p1);
+                    packed[i] = Elem<T>::pack2(p0, p1);
                 }
+                *reinterpret_cast<uint4 *>(prow + (c8 >> 3) * L::kHalf + (((c8 & 7) ^ (r & 7)) << 4)) =
+                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }
+            l += l0 + l1;
             tc::fence_before_sync();
             if (valid < TILE) {
                 // V rows past the loaded range: zero them so 0 * stale never reaches the MMA
