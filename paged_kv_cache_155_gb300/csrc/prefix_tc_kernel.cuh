@@ -19,8 +19,8 @@
 // columns).  A row's softmax is local to one thread (TMEM lane = query row).
 // The row maximum used for P is raised only when a tile's maximum exceeds it
 // by more than kRescaleLog2 (then O and l are rescaled in place), so P <=
-// 2^kRescaleLog2.  P is rounded to the input type for the MMA and l sums the
-// rounded values.
+// 2^kRescaleLog2.  P is rounded to the input type for the MMA; l adds the fp32
+// values (unbiased rounding, relative error 2^-9 per weight at most).
 //
 // Warps: 0 TMA producer (K ring and V ring, 2 slots each, 3-D tiled copies with
 // 128-byte swizzle), 1 TMEM owner + MMA issuer (event-driven), 2-5 softmax.
@@ -272,18 +272,27 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             tc::fence_after_sync();
-            // pass 1: tile maximum of this row
-            float tmax = -INFINITY;
+            // this row's 128 scores, read from TMEM once; tile maximum of the scaled
+            // scores = the extreme raw score times the scale (max for a positive
+            // scale, min otherwise)
+            float x[TILE];
 #pragma unroll
-            for (int c = 0; c < TILE; c += 32) {
-                float x[32];
-                tc::tmem_ld_x16(lane_base + 128 * b + c, x);
-                tc::tmem_ld_x16(lane_base + 128 * b + c + 16, x + 16);
-                tc::tmem_ld_wait();
+            for (int c = 0; c < TILE; c += 16) tc::tmem_ld_x16(lane_base + 128 * b + c, x + c);
+            tc::tmem_ld_wait();
+            const bool full = valid == TILE;  // uniform over the CTA
+            const bool pos_scale = p.scale_log2 > 0.f;
+            float ext = x[0];
+            if (full) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (c + i < valid) tmax = fmaxf(tmax, x[i] * p.scale_log2);
+                for (int i = 1; i + 1 < TILE; i += 2)
+                    ext = pos_scale ? fmax3(ext, x[i], x[i + 1]) : fmin3(ext, x[i], x[i + 1]);
+                ext = pos_scale ? fmaxf(ext, x[TILE - 1]) : fminf(ext, x[TILE - 1]);
+            } else {
+#pragma unroll
+                for (int i = 1; i < TILE; ++i)
+                    if (i < valid) ext = pos_scale ? fmaxf(ext, x[i]) : fminf(ext, x[i]);
             }
+            const float tmax = ext * p.scale_log2;
             // the reference maximum moves only by more than kRescaleLog2; TMEM loads and
             // stores are warp-wide, so the warp rescales if any of its rows must
             const float new_ref = tmax > m_ref + L::kRescaleLog2 ? tmax : m_ref;
@@ -322,32 +331,29 @@ __global__ void __launch_bounds__(192, 1)
                 ok = false;
                 break;
             }
-            // pass 2: P = 2^(s - m_ref), rounded to T, into the K-major P panel
+            // P = 2^(s - m_ref) (0 past the prefix end), rounded to T into the K-major
+            // P panel; the row sum l adds the fp32 values
             unsigned char *prow = sm + L::kOffP + b * L::kPanel + r * 128;
+            float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-            for (int c = 0; c < TILE; c += 32) {
-                float x[32];
-                tc::tmem_ld_x16(lane_base + 128 * b + c, x);
-                tc::tmem_ld_x16(lane_base + 128 * b + c + 16, x + 16);
-                tc::tmem_ld_wait();
+            for (int c8 = 0; c8 < TILE / 8; ++c8) {
+                uint32_t packed[4];
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    uint32_t packed[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int t = c + c8 * 8 + 2 * i;
-                        const float p0 = t < valid ? fast_exp2(x[c8 * 8 + 2 * i] * p.scale_log2 - m_ref) : 0.f;
-                        const float p1 = t + 1 < valid ? fast_exp2(x[c8 * 8 + 2 * i + 1] * p.scale_log2 - m_ref) : 0.f;
-                        const T h0 = Elem<T>::from_f32(p0), h1 = Elem<T>::from_f32(p1);
-                        l += static_cast<float>(h0) + static_cast<float>(h1);
-                        packed[i] = static_cast<uint32_t>(reinterpret_cast<const uint16_t &>(h0)) |
-                                    (static_cast<uint32_t>(reinterpret_cast<const uint16_t &>(h1)) << 16);
+                for (int i = 0; i < 4; ++i) {
+                    const int t = c8 * 8 + 2 * i;
+                    float p0 = fast_exp2(fmaf(x[t], p.scale_log2, -m_ref));
+                    float p1 = fast_exp2(fmaf(x[t + 1], p.scale_log2, -m_ref));
+                    if (!full) {
+                        p0 = t < valid ? p0 : 0.f;
+                        p1 = t + 1 < valid ? p1 : 0.f;
                     }
-                    const int chunk = (c + c8 * 8) >> 3;  // 8-token chunk index, 0..15
-                    *reinterpret_cast<uint4 *>(prow + (chunk >> 3) * L::kHalf + (((chunk & 7) ^ (r & 7)) << 4)) =
-                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    add_f32x2(l0, l1, p0, p1);
+                    packed[i] = Elem<T>::pack2(p0, p1);
                 }
+                *reinterpret_cast<uint4 *>(prow + (c8 >> 3) * L::kHalf + (((c8 & 7) ^ (r & 7)) << 4)) =
+                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }
+            l += l0 + l1;
             tc::fence_before_sync();
             if (valid < TILE) {
                 // rows of V past the prefix end: zero them so 0 * stale never reaches the MMA
