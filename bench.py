@@ -416,6 +416,29 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
             raise RuntimeError(f"device flags on the shared-prefix decode: {names}")
         c_step = s0.elapsed_time(s1) / steps
         c_dec = statistics.mean(a.elapsed_time(b) for a, b in ev2)
+
+        # the same two decodes with L2 flushed before every call (a 256 MiB write,
+        # outside the timed region): the shared prefix is then read from HBM each time
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+        def flushed_ms(call, n=50):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+            for a, b in evs:
+                flush.fill_(1)
+                a.record(stream)
+                call()
+                b.record(stream)
+            torch.cuda.synchronize()
+            return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+        plain_flushed = flushed_ms(lambda: pkv.paged_attention_decode(
+            wl.q, k_cache, v_cache, wl.block_tables, wl.context_lens, wl.scale, out,
+            max_context_len=maxl, partition_size=part))
+        cascade_flushed = flushed_ms(lambda: pkv.paged_attention_decode_shared_prefix(
+            wl.q, k_cache, v_cache, pre_table, pre_tokens, wl.block_tables, wl.context_lens,
+            wl.scale, out, max_context_len=maxl))
+        del flush
         row_bytes = 2 * wl.num_kv_heads * wl.head_dim * 2          # K+V of one token, all KV heads
         suffix_tokens = sum(int(x) - pre_tokens for x in wl.context_lens.cpu().tolist())
         unique = (pre_tokens + suffix_tokens) * row_bytes + 2 * wl.num_seqs * wl.num_q_heads * wl.head_dim * 2
@@ -424,7 +447,11 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
             "decode_ms": c_dec, "speedup_vs_plain_decode": dec_ms / c_dec,
             "unique_bytes": unique, "unique_gbps": unique / (c_dec / 1e3) / 1e9,
             "unique_frac_of_measured": unique / (c_dec / 1e3) / 1e9 / peak,
-            "logical_gbps": nbytes / (c_dec / 1e3) / 1e9}
+            "logical_gbps": nbytes / (c_dec / 1e3) / 1e9,
+            "l2_flushed": {"plain_decode_ms": plain_flushed, "shared_prefix_decode_ms": cascade_flushed,
+                           "plain_unique_gbps": unique / (plain_flushed / 1e3) / 1e9,
+                           "shared_prefix_unique_gbps": unique / (cascade_flushed / 1e3) / 1e9,
+                           "note": "256 MiB written before each call, outside the timed region"}}
     del wl, k_cache, v_cache, out, graph
     torch.cuda.empty_cache()
     return result
