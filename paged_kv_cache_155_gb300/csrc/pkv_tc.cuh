@@ -90,6 +90,20 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 
 // 32 lanes x N consecutive 32-bit columns: thread i of the warp gets lane
 // (taddr.lane + i), columns taddr.col .. +N-1.
+// One 32-bit column: thread i of the warp reads / writes lane (taddr.lane + i).
+__device__ __forceinline__ float tmem_ld_x1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr) : "memory");
+    return __uint_as_float(r);
+}
+__device__ __forceinline__ void tmem_st_x1(uint32_t taddr, float v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(__float_as_uint(v))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, float v[4]) {
     uint32_t r[4];
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"

@@ -62,11 +62,12 @@ pkv_status launch_prefill_one(const pkv::PrefillParams &p, const CUtensorMap &tk
     if (!bit || !(configured_devices.load(std::memory_order_acquire) & bit)) {
         if (cudaFuncSetAttribute(pkv::paged_prefill_tc_kernel<T, BS>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 pkv::PrefixLayout::kSmemBytes) != cudaSuccess)
+                                 pkv::PrefillLayout::kSmemBytes) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured_devices.fetch_or(bit, std::memory_order_acq_rel);
     }
-    pkv::paged_prefill_tc_kernel<T, BS><<<grid, 192, pkv::PrefixLayout::kSmemBytes, stream>>>(tk, tv, p);
+    pkv::paged_prefill_tc_kernel<T, BS>
+        <<<grid, pkv::PrefillLayout::kThreads, pkv::PrefillLayout::kSmemBytes, stream>>>(tk, tv, p);
     pkv::count_launch();
     return pkv::launch_status();
 }

@@ -26,7 +26,11 @@
 // paged_prefill_merge_kernel combines.
 //
 // Warps: 0 TMA producer (K ring and V ring, 2 slots each), 1 TMEM owner + MMA
-// issuer, 2-5 softmax (thread = query row).
+// issuer, 2-9 softmax in pairs: warps w and w + 4 share TMEM lane quarter w & 3
+// (the same 32 query rows) and take tile columns 0-63 and 64-127.  A pair
+// exchanges its partial row maxima each tile through two spare TMEM columns
+// (an mbarrier with a bounded wait orders them), so both warps hold the same
+// reference maximum; each rescales, writes P for and outputs its own half.
 #pragma once
 
 #include "prefix_tc_kernel.cuh"
@@ -68,11 +72,20 @@ __device__ __forceinline__ bool prefill_seq(const PrefillParams &p, int seq, int
            len <= p.len_cap;
 }
 
+// The shared-prefix layout plus the softmax pairs' barriers.
+struct PrefillLayout : PrefixLayout {
+    static constexpr int kOffPair = kOffMisc + 16;      // uint64 [4 quarters][2 parities]
+    static constexpr int kSmemBytes = PrefixLayout::kSmemBytes + 8 * 8;
+    static constexpr int kThreads = 320;
+    static constexpr uint32_t kXchgCol = 384;           // spare TMEM columns for the pairs
+    static_assert(kSmemBytes <= 232448, "dynamic shared memory per block");
+};
+
 template <typename T, int BS>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
-    using L = PrefixLayout;
+    using L = PrefillLayout;
     constexpr int TILE = L::kTile, D = 128;
     constexpr bool kBF16 = !std::is_same<T, __half>::value;
     static_assert(TILE / BS <= 32, "one table entry per producer lane");
@@ -106,6 +119,7 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t *k_full = bars, *k_empty = bars + 2, *v_full = bars + 4, *v_empty = bars + 6;
     uint64_t *s_full = bars + 8, *s_empty = bars + 10, *p_full = bars + 12, *o_done = bars + 14;
     uint64_t *drain_bar = bars + 16;
+    uint64_t *pair_bar = reinterpret_cast<uint64_t *>(sm + L::kOffPair);  // [quarter][parity]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
     const uint32_t smem_base = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
@@ -117,10 +131,11 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 4);
-            mbar_init(&p_full[i], 4);
+            mbar_init(&s_empty[i], 8);
+            mbar_init(&p_full[i], 8);
             mbar_init(&o_done[i], 1);
         }
+        for (int i = 0; i < 8; ++i) mbar_init(&pair_bar[i], 2);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -275,84 +290,112 @@ __global__ void __launch_bounds__(192, 1)
         }
         __syncwarp();
     } else {
-        // ===================== softmax (warps 2..5): thread = query row =====================
+        // ===================== softmax (warps 2..9): thread = query row, 64 columns =====================
         const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
+        const int half = warp >= 6 ? 1 : 0;  // tile columns 64*half .. +63
+        const int c0 = half * 64;
+        const int r = quarter * 32 + lane;   // row within the tile = TMEM lane
         const int row = row0 + r;
         const bool live = row < rows;
         const int jtok = live ? row / p.group : 0;
-        const int pos = base_pos + jtok;    // this row sees tokens 0 .. pos
+        const int pos = base_pos + jtok;     // this row sees tokens 0 .. pos
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t xchg = lane_base + L::kXchgCol;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
+        // One value per row between the two warps of the pair: step s writes column
+        // 2 (s & 1) + half and reads the partner's; a warp reuses a column two steps
+        // later, after the partner has passed the step in between.
+        auto exchange = [&](int step, float mine, float &other) -> bool {
+            const int par = step & 1;
+            tc::tmem_st_x1(xchg + 2 * par + half, mine);
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            __syncwarp();
+            uint64_t *pb = &pair_bar[quarter * 2 + par];
+            if (lane == 0) mbar_arrive(pb);
+            if (!tc_wait_warp(pb, (step >> 1) & 1, abort_flag, p.status)) return false;
+            tc::fence_after_sync();
+            other = tc::tmem_ld_x1(xchg + 2 * par + (1 - half));
+            tc::tmem_ld_wait();
+            return true;
+        };
         for (int j = 0; j < ntiles && ok; ++j) {
             const int b = j & 1;
             const int t0 = tok_lo + j * TILE;
-            const int valid = min(TILE, tok_hi - t0);             // columns loaded
+            const int valid = min(TILE, tok_hi - t0);                    // columns loaded
             const int vr = live ? max(0, min(valid, pos + 1 - t0)) : 0;  // columns this row sees
+            const int vh = max(0, min(64, vr - c0));                     // ... in this half
             if (!tc_wait_warp(&s_full[b], (j >> 1) & 1, abort_flag, p.status)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            // this row's 128 scores, read from TMEM once
-            float x[TILE];
+            // this row's 64 scores of the half, read from TMEM once
+            float x[64];
 #pragma unroll
-            for (int c = 0; c < TILE; c += 16) tc::tmem_ld_x16(lane_base + 128 * b + c, x + c);
+            for (int c = 0; c < 64; c += 16) tc::tmem_ld_x16(lane_base + 128 * b + c0 + c, x + c);
             tc::tmem_ld_wait();
-            // tiles no row of the warp sees only partly (all but the diagonal and the
-            // last) skip the per-column masks
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[b]);  // S[b] is in registers
+            // tiles every row of the warp sees completely skip the per-column masks
             const bool full = __all_sync(0xffffffffu, vr == TILE);
-            // tile maximum of the visible scaled scores: the extreme raw score times
+            // partial maximum of the visible scaled scores: the extreme raw score times
             // the scale (the maximum for a positive scale, the minimum otherwise)
-            float tmax = -INFINITY;
-            if (vr > 0) {
+            float pmax = -INFINITY;
+            if (vh > 0) {
                 const bool pos_scale = p.scale_log2 > 0.f;
-                float ext;
+                float ext = x[0];
                 if (full) {
-                    ext = x[0];
 #pragma unroll
-                    for (int i = 1; i + 1 < TILE; i += 2)
+                    for (int i = 1; i + 1 < 64; i += 2)
                         ext = pos_scale ? fmax3(ext, x[i], x[i + 1]) : fmin3(ext, x[i], x[i + 1]);
-                    ext = pos_scale ? fmaxf(ext, x[TILE - 1]) : fminf(ext, x[TILE - 1]);
+                    ext = pos_scale ? fmaxf(ext, x[63]) : fminf(ext, x[63]);
                 } else {
-                    ext = x[0];
 #pragma unroll
-                    for (int i = 1; i < TILE; ++i)
-                        if (i < vr) ext = pos_scale ? fmaxf(ext, x[i]) : fminf(ext, x[i]);
+                    for (int i = 1; i < 64; ++i)
+                        if (i < vh) ext = pos_scale ? fmaxf(ext, x[i]) : fminf(ext, x[i]);
                 }
-                tmax = ext * p.scale_log2;
+                pmax = ext * p.scale_log2;
             }
+            float pmax_other;
+            if (!exchange(j, pmax, pmax_other)) {
+                ok = false;
+                break;
+            }
+            const float tmax = fmaxf(pmax, pmax_other);
             // the reference maximum moves only by more than kRescaleLog2 (a row that sees
-            // nothing keeps -inf and alpha 1); TMEM loads and stores are warp-wide, so the
-            // warp rescales if any of its rows must
+            // nothing keeps -inf and alpha 1); both warps of the pair take the same
+            // decision for a row; TMEM loads and stores are warp-wide, so the warp
+            // rescales its half of O if any of its rows must
             const float new_ref = tmax > m_ref + L::kRescaleLog2 ? tmax : m_ref;
             const float alpha = new_ref == m_ref ? 1.f : fast_exp2(m_ref - new_ref);
             if (__any_sync(0xffffffffu, new_ref != m_ref)) {
                 if (j > 0) {
-                    // O holds tiles < j: wait for PV(j-1), rescale O in TMEM
+                    // O holds tiles < j: wait for PV(j-1), rescale this half of O in TMEM
                     if (!tc_wait_warp(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
 #pragma unroll
-                    for (int c = 0; c < D; c += 16) {
+                    for (int c = 0; c < 64; c += 16) {
                         float o[16];
-                        tc::tmem_ld_x16(lane_base + 256 + c, o);
+                        tc::tmem_ld_x16(lane_base + 256 + c0 + c, o);
                         tc::tmem_ld_wait();
                         uint32_t w[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(o[i] * alpha);
                         asm volatile(
                             "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, "
-                            "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(lane_base + 256 + c),
+                            "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(lane_base + 256 + c0 + c),
                             "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
                             "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]),
                             "r"(w[13]), "r"(w[14]), "r"(w[15])
                             : "memory");
                     }
-                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    tc::tmem_st_wait();
                 }
                 l *= alpha;
                 m_ref = new_ref;
@@ -362,12 +405,12 @@ __global__ void __launch_bounds__(192, 1)
                 ok = false;
                 break;
             }
-            // P = 2^(s - m_ref) on visible columns (0 elsewhere), rounded to T into the
-            // K-major P panel; the row sum l adds the fp32 values
-            unsigned char *prow = sm + L::kOffP + b * L::kPanel + r * 128;
+            // P = 2^(s - m_ref) on visible columns (0 elsewhere), rounded to T into this
+            // half of the K-major P panel; the row sum l adds the fp32 values
+            unsigned char *prow = sm + L::kOffP + b * L::kPanel + half * L::kHalf + r * 128;
             float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-            for (int c8 = 0; c8 < TILE / 8; ++c8) {
+            for (int c8 = 0; c8 < 8; ++c8) {
                 uint32_t packed[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -375,76 +418,69 @@ __global__ void __launch_bounds__(192, 1)
                     float p0 = fast_exp2(fmaf(x[t], p.scale_log2, -m_ref));
                     float p1 = fast_exp2(fmaf(x[t + 1], p.scale_log2, -m_ref));
                     if (!full) {
-                        p0 = t < vr ? p0 : 0.f;
-                        p1 = t + 1 < vr ? p1 : 0.f;
+                        p0 = t < vh ? p0 : 0.f;
+                        p1 = t + 1 < vh ? p1 : 0.f;
                     }
                     add_f32x2(l0, l1, p0, p1);
                     packed[i] = Elem<T>::pack2(p0, p1);
                 }
-                *reinterpret_cast<uint4 *>(prow + (c8 >> 3) * L::kHalf + (((c8 & 7) ^ (r & 7)) << 4)) =
+                *reinterpret_cast<uint4 *>(prow + ((c8 ^ (r & 7)) << 4)) =
                     make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }
             l += l0 + l1;
-            tc::fence_before_sync();
             if (valid < TILE) {
-                // V rows past the loaded range: zero them so 0 * stale never reaches the MMA
+                // V rows past the loaded range: zero this half so 0 * stale never reaches
+                // the MMA
                 if (!tc_wait_warp(&v_full[b], (j >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 if (r >= valid) {
-                    unsigned char *vrow = sm + L::kOffV + b * L::kPanel + r * 128;
+                    uint4 *vrow = reinterpret_cast<uint4 *>(sm + L::kOffV + b * L::kPanel + half * L::kHalf + r * 128);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            reinterpret_cast<uint4 *>(vrow + c * L::kHalf)[i] = make_uint4(0, 0, 0, 0);
+                    for (int i = 0; i < 8; ++i) vrow[i] = make_uint4(0, 0, 0, 0);
                 }
             }
-            fence_proxy_async_smem();
+            tc::fence_before_sync();   // the O rescale's TMEM stores precede PV(j)
+            fence_proxy_async_smem();  // P / zeroed V rows visible to the MMA
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&s_empty[b]);
-                mbar_arrive(&p_full[b]);
-            }
+            if (lane == 0) mbar_arrive(&p_full[b]);
         }
-        // final: the O row -> out (one split) or its partial slot.  TMEM loads are
-        // warp-wide: every lane loads, only live rows store.
+        // the pair's row sum, then this half of the O row -> out (one split) or its
+        // partial slot.  TMEM loads are warp-wide: every lane loads, only live rows store.
+        float l_other = 0.f;
+        if (ok) ok = exchange(ntiles, l, l_other);
+        const float lt = l + l_other;
         if (ok) ok = tc_wait_warp(&o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
         if (ok) {
             tc::fence_after_sync();
             const int g = live ? row - jtok * p.group : 0;
             const int64_t orow = (static_cast<int64_t>(q0) + jtok) * p.num_q_heads + kvh * p.group + g;
             const bool direct = p.splits == 1;
-            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
 #pragma unroll
-            for (int c = 0; c < D; c += 16) {
+            for (int c = 0; c < 64; c += 16) {
                 float o[16];
-                tc::tmem_ld_x16(lane_base + 256 + c, o);
+                tc::tmem_ld_x16(lane_base + 256 + c0 + c, o);
                 tc::tmem_ld_wait();
                 if (!live) continue;
                 if (direct) {
                     uint32_t w[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const T h0 = Elem<T>::from_f32(o[2 * i] * inv_l);
-                        const T h1 = Elem<T>::from_f32(o[2 * i + 1] * inv_l);
-                        w[i] = static_cast<uint32_t>(reinterpret_cast<const uint16_t &>(h0)) |
-                               (static_cast<uint32_t>(reinterpret_cast<const uint16_t &>(h1)) << 16);
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + orow * D + c);
+                    for (int i = 0; i < 8; ++i) w[i] = Elem<T>::pack2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + orow * D + c0 + c);
                     dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
                     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
                 } else {
-                    float *dst = p.ws_o + (orow * p.splits + split) * D + c;
+                    float *dst = p.ws_o + (orow * p.splits + split) * D + c0 + c;
 #pragma unroll
                     for (int i = 0; i < 16; i += 4)
                         *reinterpret_cast<float4 *>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
                 }
             }
-            if (live && !direct) {
+            if (live && !direct && half == 0) {
                 p.ws_m[orow * p.splits + split] = m_ref;
-                p.ws_l[orow * p.splits + split] = l;
+                p.ws_l[orow * p.splits + split] = lt;
             }
         }
     }
