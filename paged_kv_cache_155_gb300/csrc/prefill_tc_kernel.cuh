@@ -25,7 +25,7 @@
 // normalised output; with several it writes (o, m, l) partials that
 // paged_prefill_merge_kernel combines.
 //
-// Warps: 0 TMA producer (K ring and V ring, 2 slots each), 1 TMEM owner + MMA
+// Warps: 0 TMA producer (K and V rings of PrefillLayout::kKS / kVS slots), 1 TMEM owner + MMA
 // issuer, 2-9 softmax in pairs: warps w and w + 4 share TMEM lane quarter w & 3
 // (the same 32 query rows) and take tile columns 0-63 and 64-127.  A pair
 // exchanges its partial row maxima each tile through two spare TMEM columns
@@ -72,12 +72,26 @@ __device__ __forceinline__ bool prefill_seq(const PrefillParams &p, int seq, int
            len <= p.len_cap;
 }
 
-// The shared-prefix layout plus the softmax pairs' barriers.
-struct PrefillLayout : PrefixLayout {
-    static constexpr int kOffPair = kOffMisc + 16;      // uint64 [4 quarters][2 parities]
-    static constexpr int kSmemBytes = PrefixLayout::kSmemBytes + 8 * 8;
+// Shared memory: the Q tile, K and V rings of 128-token tiles, P buffers, and
+// the barriers (rings, S / P / O double buffers, the softmax pairs).
+struct PrefillLayout {
+    static constexpr int kTile = 128;
+    static constexpr int kHalf = 128 * 128;           // 128 rows x 128 B
+    static constexpr int kPanel = 2 * kHalf;          // 128 rows x 128 16-bit values
+    static constexpr int kKS = 2, kVS = 2, kPB = 1;   // K slots, V slots, P buffers
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kPanel;
+    static constexpr int kOffV = kOffK + kKS * kPanel;
+    static constexpr int kOffP = kOffV + kVS * kPanel;
+    static constexpr int kOffBar = kOffP + kPB * kPanel;
+    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 8 + 1 + 8;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kSmemBytes = kBytes + 1024;  // + alignment slack
+    static constexpr uint32_t kTmemCols = 512;        // S[2] at 0 / 128, O at 256, exchange 384
+    static constexpr uint32_t kXchgCol = 384;         // spare TMEM columns for the pairs
+    static constexpr float kRescaleLog2 = 8.f;
     static constexpr int kThreads = 320;
-    static constexpr uint32_t kXchgCol = 384;           // spare TMEM columns for the pairs
     static_assert(kSmemBytes <= 232448, "dynamic shared memory per block");
 };
 
@@ -115,21 +129,26 @@ __global__ void __launch_bounds__(320, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm =
         smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
+    constexpr int KS = L::kKS, VS = L::kVS, PB = L::kPB;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
-    uint64_t *k_full = bars, *k_empty = bars + 2, *v_full = bars + 4, *v_empty = bars + 6;
-    uint64_t *s_full = bars + 8, *s_empty = bars + 10, *p_full = bars + 12, *o_done = bars + 14;
-    uint64_t *drain_bar = bars + 16;
-    uint64_t *pair_bar = reinterpret_cast<uint64_t *>(sm + L::kOffPair);  // [quarter][parity]
+    uint64_t *k_full = bars, *k_empty = k_full + KS, *v_full = k_empty + KS, *v_empty = v_full + VS;
+    uint64_t *s_full = v_empty + VS, *s_empty = s_full + 2, *p_full = s_full + 4, *o_done = s_full + 6;
+    uint64_t *drain_bar = s_full + 8;
+    uint64_t *pair_bar = drain_bar + 1;  // [quarter][parity]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
     const uint32_t smem_base = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < KS; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < VS; ++i) {
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_empty[i], 8);
             mbar_init(&p_full[i], 8);
@@ -173,7 +192,8 @@ __global__ void __launch_bounds__(320, 1)
         // ===================== TMA producer =====================
         const uint64_t policy = l2_policy_evict_last();  // every row tile of the sequence reads it
         const int32_t *trow = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
-        int last_issue[2][2] = {{-1, -1}, {-1, -1}};
+        int last_issue[2][4] = {{-1, -1, -1, -1}, {-1, -1, -1, -1}};
+        static_assert(L::kKS <= 4 && L::kVS <= 4, "drain bookkeeping");
         bool ok = true;
         for (int j = 0; j < ntiles && ok; ++j) {
             const int t0 = tok_lo + j * TILE;
@@ -188,12 +208,13 @@ __global__ void __launch_bounds__(320, 1)
             }
             const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, e >= 0)) * BS * 256u;
             for (int kv = 0; kv < 2 && ok; ++kv) {
-                const int s = j & 1;
+                const int nst = kv ? VS : KS;
+                const int s = j % nst;
                 uint64_t *fb = kv ? &v_full[s] : &k_full[s];
                 uint64_t *eb = kv ? &v_empty[s] : &k_empty[s];
                 int go = 1;
                 if (lane == 0) {
-                    go = tc_wait(eb, ((j >> 1) & 1) ^ 1, abort_flag, p.status);
+                    go = tc_wait(eb, ((j / nst) & 1) ^ 1, abort_flag, p.status);
                     if (go) {
                         if (bytes) mbar_arrive_expect_tx(fb, bytes);
                         else mbar_arrive(fb);
@@ -215,11 +236,13 @@ __global__ void __launch_bounds__(320, 1)
             }
         }
         if (!ok && lane == 0) {
-            for (int kv = 0; kv < 2; ++kv)
-                for (int s = 0; s < 2; ++s)
+            for (int kv = 0; kv < 2; ++kv) {
+                const int nst = kv ? VS : KS;
+                for (int s = 0; s < nst; ++s)
                     if (last_issue[kv][s] >= 0)
-                        mbar_wait_bounded(kv ? &v_full[s] : &k_full[s], (last_issue[kv][s] >> 1) & 1,
+                        mbar_wait_bounded(kv ? &v_full[s] : &k_full[s], (last_issue[kv][s] / nst) & 1,
                                           kDrainTimeoutNs);
+            }
         }
     } else if (warp == 1) {
         // ===================== MMA issuer (event-driven, PV first) =====================
@@ -232,9 +255,9 @@ __global__ void __launch_bounds__(320, 1)
             int act = 0;
             if (lane == 0) {
                 if (n_pv < n_qk && mbar_test_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
-                    mbar_test_wait(&v_full[n_pv & 1], (n_pv >> 1) & 1))
+                    mbar_test_wait(&v_full[n_pv % VS], (n_pv / VS) & 1))
                     act = 1;
-                else if (n_qk < ntiles && mbar_test_wait(&k_full[n_qk & 1], (n_qk >> 1) & 1) &&
+                else if (n_qk < ntiles && mbar_test_wait(&k_full[n_qk % KS], (n_qk / KS) & 1) &&
                          mbar_test_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
                     act = 2;
                 if (act) {
@@ -253,8 +276,8 @@ __global__ void __launch_bounds__(320, 1)
                 if (act == 1) {
                     const int j = n_pv, b = j & 1;
                     tc::fence_after_sync();
-                    const uint32_t pa = smem_base + L::kOffP + b * L::kPanel;
-                    const uint32_t va = smem_base + L::kOffV + b * L::kPanel;
+                    const uint32_t pa = smem_base + L::kOffP + (j % PB) * L::kPanel;
+                    const uint32_t va = smem_base + L::kOffV + (j % VS) * L::kPanel;
 #pragma unroll
                     for (int k = 0; k < TILE / 16; ++k) {
                         const uint64_t a = tc::smem_desc_sw128(pa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
@@ -262,12 +285,12 @@ __global__ void __launch_bounds__(320, 1)
                         tc::mma_f16_ss(tmem + 256, a, bd, idesc_pv, j > 0 || k > 0);
                     }
                     tc::mma_commit(&o_done[b]);
-                    tc::mma_commit(&v_empty[b]);
+                    tc::mma_commit(&v_empty[j % VS]);
                 } else if (act == 2) {
                     const int j = n_qk, b = j & 1;
                     tc::fence_after_sync();
                     const uint32_t qa = smem_base + L::kOffQ;
-                    const uint32_t ka = smem_base + L::kOffK + b * L::kPanel;
+                    const uint32_t ka = smem_base + L::kOffK + (j % KS) * L::kPanel;
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint64_t a = tc::smem_desc_sw128(qa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
@@ -275,7 +298,7 @@ __global__ void __launch_bounds__(320, 1)
                         tc::mma_f16_ss(tmem + 128 * b, a, bd, idesc_qk, k > 0);
                     }
                     tc::mma_commit(&s_full[b]);
-                    tc::mma_commit(&k_empty[b]);
+                    tc::mma_commit(&k_empty[j % KS]);
                 }
             }
             act = __shfl_sync(0xffffffffu, act, 0);
@@ -400,14 +423,14 @@ __global__ void __launch_bounds__(320, 1)
                 l *= alpha;
                 m_ref = new_ref;
             }
-            // P[b] was last read by PV(j-2)
-            if (j >= 2 && !tc_wait_warp(&o_done[b], ((j - 2) >> 1) & 1, abort_flag, p.status)) {
+            // P buffer j % PB was last read by PV(j - PB)
+            if (j >= PB && !tc_wait_warp(&o_done[(j - PB) & 1], ((j - PB) >> 1) & 1, abort_flag, p.status)) {
                 ok = false;
                 break;
             }
             // P = 2^(s - m_ref) on visible columns (0 elsewhere), rounded to T into this
             // half of the K-major P panel; the row sum l adds the fp32 values
-            unsigned char *prow = sm + L::kOffP + b * L::kPanel + half * L::kHalf + r * 128;
+            unsigned char *prow = sm + L::kOffP + (j % PB) * L::kPanel + half * L::kHalf + r * 128;
             float l0 = 0.f, l1 = 0.f;
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
@@ -431,12 +454,13 @@ __global__ void __launch_bounds__(320, 1)
             if (valid < TILE) {
                 // V rows past the loaded range: zero this half so 0 * stale never reaches
                 // the MMA
-                if (!tc_wait_warp(&v_full[b], (j >> 1) & 1, abort_flag, p.status)) {
+                if (!tc_wait_warp(&v_full[j % VS], (j / VS) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 if (r >= valid) {
-                    uint4 *vrow = reinterpret_cast<uint4 *>(sm + L::kOffV + b * L::kPanel + half * L::kHalf + r * 128);
+                    uint4 *vrow = reinterpret_cast<uint4 *>(sm + L::kOffV + (j % VS) * L::kPanel + half * L::kHalf +
+                                                            r * 128);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) vrow[i] = make_uint4(0, 0, 0, 0);
                 }
