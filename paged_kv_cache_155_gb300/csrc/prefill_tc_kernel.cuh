@@ -25,8 +25,8 @@
 // normalised output; with several it writes (o, m, l) partials that
 // paged_prefill_merge_kernel combines.
 //
-// Warps: 0 TMA producer (K and V rings of PrefillLayout::kKS / kVS slots), 1 TMEM owner + MMA
-// issuer, 2-9 softmax in pairs: warps w and w + 4 share TMEM lane quarter w & 3
+// Warps: 0 / 10 TMA producers of the K / V rings (PrefillLayout::kKS / kVS
+// slots), 1 TMEM owner + MMA issuer, 2-9 softmax in pairs: warps w and w + 4 share TMEM lane quarter w & 3
 // (the same 32 query rows) and take tile columns 0-63 and 64-127.  A pair
 // exchanges its partial row maxima each tile through two spare TMEM columns
 // (an mbarrier with a bounded wait orders them), so both warps hold the same
@@ -91,12 +91,12 @@ struct PrefillLayout {
     static constexpr uint32_t kTmemCols = 512;        // S[2] at 0 / 128, O at 256, exchange 384
     static constexpr uint32_t kXchgCol = 384;         // spare TMEM columns for the pairs
     static constexpr float kRescaleLog2 = 8.f;
-    static constexpr int kThreads = 320;
+    static constexpr int kThreads = 352;
     static_assert(kSmemBytes <= 232448, "dynamic shared memory per block");
 };
 
 template <typename T, int BS>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
     using L = PrefillLayout;
@@ -188,61 +188,66 @@ __global__ void __launch_bounds__(320, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ===================== TMA producer =====================
+    if (warp == 0 || warp == 10) {
+        // ===================== TMA producers: K (warp 0), V (warp 10) =====================
+        // Separate producers so a K tile never waits behind a V slot that its PV still
+        // holds; each reads the next tile's table entries while it waits for a slot.
+        const int kv = warp == 10;
+        const int nst = kv ? VS : KS;
+        uint64_t *full = kv ? v_full : k_full;
+        uint64_t *empty = kv ? v_empty : k_empty;
+        const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
+        unsigned char *ring = sm + (kv ? L::kOffV : L::kOffK);
         const uint64_t policy = l2_policy_evict_last();  // every row tile of the sequence reads it
         const int32_t *trow = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
-        int last_issue[2][4] = {{-1, -1, -1, -1}, {-1, -1, -1, -1}};
-        static_assert(L::kKS <= 4 && L::kVS <= 4, "drain bookkeeping");
-        bool ok = true;
-        for (int j = 0; j < ntiles && ok; ++j) {
+        auto entry = [&](int j) -> int {  // this lane's block of tile j (-1: none or bad)
             const int t0 = tok_lo + j * TILE;
             const int nblk = (min(TILE, tok_hi - t0) + BS - 1) / BS;
             int e = -1;
             if (lane < nblk) {
                 e = trow[t0 / BS + lane];
                 if (e < 0 || e >= p.num_blocks) {
-                    raise_flag(p.status, PKV_DEVERR_BLOCK_TABLE);
+                    if (kv == 0) raise_flag(p.status, PKV_DEVERR_BLOCK_TABLE);
                     e = -1;
                 }
             }
+            return e;
+        };
+        int last_issue[4] = {-1, -1, -1, -1};
+        static_assert(L::kKS <= 4 && L::kVS <= 4, "drain bookkeeping");
+        bool ok = true;
+        int e_next = ntiles > 0 ? entry(0) : -1;
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int e = e_next;
+            if (j + 1 < ntiles) e_next = entry(j + 1);  // in flight while this tile waits
             const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, e >= 0)) * BS * 256u;
-            for (int kv = 0; kv < 2 && ok; ++kv) {
-                const int nst = kv ? VS : KS;
-                const int s = j % nst;
-                uint64_t *fb = kv ? &v_full[s] : &k_full[s];
-                uint64_t *eb = kv ? &v_empty[s] : &k_empty[s];
-                int go = 1;
-                if (lane == 0) {
-                    go = tc_wait(eb, ((j / nst) & 1) ^ 1, abort_flag, p.status);
-                    if (go) {
-                        if (bytes) mbar_arrive_expect_tx(fb, bytes);
-                        else mbar_arrive(fb);
-                        last_issue[kv][s] = j;
-                    }
+            const int s = j % nst;
+            int go = 1;
+            if (lane == 0) {
+                go = tc_wait(&empty[s], ((j / nst) & 1) ^ 1, abort_flag, p.status);
+                if (go) {
+                    if (bytes) mbar_arrive_expect_tx(&full[s], bytes);
+                    else mbar_arrive(&full[s]);
+                    last_issue[s] = j;
                 }
-                if (!__shfl_sync(0xffffffffu, go, 0)) {
-                    ok = false;
-                    break;
-                }
-                if (e >= 0) {
-                    unsigned char *slot = sm + (kv ? L::kOffV : L::kOffK) + s * L::kPanel;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        tc::tma_load_3d(slot + c * L::kHalf + lane * BS * 128, kv ? &tmap_v : &tmap_k,
-                                        c * 64, kvh * BS, e, fb, policy);
-                }
-                __syncwarp();
             }
+            if (!__shfl_sync(0xffffffffu, go, 0)) {
+                ok = false;
+                break;
+            }
+            if (e >= 0) {
+                unsigned char *slot = ring + s * L::kPanel;
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    tc::tma_load_3d(slot + c * L::kHalf + lane * BS * 128, map, c * 64, kvh * BS, e,
+                                    &full[s], policy);
+            }
+            __syncwarp();
         }
         if (!ok && lane == 0) {
-            for (int kv = 0; kv < 2; ++kv) {
-                const int nst = kv ? VS : KS;
-                for (int s = 0; s < nst; ++s)
-                    if (last_issue[kv][s] >= 0)
-                        mbar_wait_bounded(kv ? &v_full[s] : &k_full[s], (last_issue[kv][s] / nst) & 1,
-                                          kDrainTimeoutNs);
-            }
+            for (int s = 0; s < nst; ++s)
+                if (last_issue[s] >= 0)
+                    mbar_wait_bounded(&full[s], (last_issue[s] / nst) & 1, kDrainTimeoutNs);
         }
     } else if (warp == 1) {
         // ===================== MMA issuer (event-driven, PV first) =====================
