@@ -17,10 +17,11 @@
 // numerator and denominator use identical weights.
 //
 // Structure (one persistent CTA per SM, 6 warps):
-//   warp 0      TMA producer: per 128-token tile, one 3-D tiled bulk-tensor copy
-//               per (block, 64-column half) for K and for V, 128-byte swizzled,
+//   warps 0, 6  TMA producers of K and of V: per 128-token tile, one 3-D tiled
+//               bulk-tensor copy per (block, 64-column half), 128-byte swizzled,
 //               into separate rings of 32 KiB K slots and 32 KiB V slots (a K
-//               slot is refilled as soon as QK^T has read it).
+//               slot is refilled as soon as QK^T has read it; K never waits
+//               behind a V slot).
 //   warp 1      TMEM owner and MMA issuer (one thread): QK^T of tile i+1 is
 //               issued before PV of tile i so the softmax of tile i overlaps it.
 //   warps 2-5   softmax and accumulation, one TMEM lane quarter each: a thread
@@ -126,7 +127,7 @@ __device__ __forceinline__ bool tc_wait_warp(uint64_t *bar, uint32_t parity,
 }
 
 template <typename T, int BS, int GH>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
     using L = TcLayout;
@@ -212,75 +213,93 @@ __global__ void __launch_bounds__(192, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ===================== TMA producer =====================
+    if (warp == 0 || warp == 6) {
+        // ===================== TMA producers: K (warp 0), V (warp 6) =====================
+        // Separate producers so a K tile never waits behind a V slot that its PV still
+        // holds; each loads the next tile's table entries while it waits for a slot.
+        const int kv = warp == 6;
+        const int nst = kv ? VS : KS;
+        uint64_t *full = kv ? v_full : k_full;
+        uint64_t *empty = kv ? v_empty : k_empty;
+        const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
+        unsigned char *ring = sm + (kv ? L::kOffV : L::kOffK);
         const uint64_t policy = l2_policy_evict_first();
-        ItemWalker walk;
-        uint32_t g = 0;  // global tile counter
-        int last_issue[2][8];
-        for (int i = 0; i < 16; ++i) last_issue[i / 8][i % 8] = -1;
-        bool ok = true;
-        for (int64_t r = blockIdx.x; ok; r += gridDim.x) {
+        // the CTA's tiles in order: item (sequence, KV head, partition), tile offset
+        struct Cursor {
+            ItemWalker walk;
+            int64_t r;
+            int tok0 = 0, ntok = 0, t0 = 0, kvh = 0;
+            bool valid = false;
+        } cur;
+        cur.r = blockIdx.x;
+        auto next_item = [&](Cursor &c) {
             int y, part;
-            if (!walk.seek(p, s_len, r, y, part)) break;
-            const int tok0 = p.tok_begin + part * p.partition_size;
-            const int ntok = max(0, min(walk.len, tok0 + p.partition_size) - tok0);
-            const int kvh = y / p.subgroups;
-            const int32_t *trow = p.block_tables + static_cast<int64_t>(walk.seq) * p.max_blocks_per_seq;
-            for (int t0 = 0; t0 < ntok && ok; t0 += TILE, ++g) {
-                const int tile_ntok = min(TILE, ntok - t0);
-                const int nblk = (tile_ntok + BS - 1) / BS;
-                const int blk0 = (tok0 + t0) / BS;
-                int e = -1;
-                if (lane < nblk) {
-                    e = trow[blk0 + lane];
-                    if (e < 0 || e >= p.num_blocks) {
-                        raise_flag(p.status, PKV_DEVERR_BLOCK_TABLE);
-                        e = -1;
-                    }
-                }
-                const unsigned valid = __ballot_sync(0xffffffffu, e >= 0);
-                const uint32_t bytes = __popc(valid) * BS * 256u;  // per K (or V) tile
-                const int row = lane * BS;
-                // K first (QK^T needs it first), then V; each waits for its own ring
-                for (int kv = 0; kv < 2; ++kv) {
-                    const int nst = kv ? VS : KS;
-                    const int s = g % nst;
-                    uint64_t *fb = kv ? &v_full[s] : &k_full[s];
-                    uint64_t *eb = kv ? &v_empty[s] : &k_empty[s];
-                    int go = 1;
-                    if (lane == 0) {
-                        go = tc_wait(eb, ((g / nst) & 1) ^ 1, abort_flag, p.status);
-                        if (go) {
-                            if (bytes) mbar_arrive_expect_tx(fb, bytes);
-                            else mbar_arrive(fb);
-                            last_issue[kv][s] = static_cast<int>(g);
-                        }
-                    }
-                    if (!__shfl_sync(0xffffffffu, go, 0)) {
-                        ok = false;
-                        break;
-                    }
-                    if (e >= 0) {
-                        unsigned char *slot = sm + (kv ? L::kOffV : L::kOffK) + s * L::kKVBytes;
-                        const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
-#pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            tc::tma_load_3d(slot + c * L::kHalfBytes + row * 128, map, c * 64,
-                                            kvh * BS, e, fb, policy);
-                    }
-                    __syncwarp();
+            while (c.walk.seek(p, s_len, c.r, y, part)) {
+                c.r += gridDim.x;
+                c.tok0 = p.tok_begin + part * p.partition_size;
+                c.ntok = max(0, min(c.walk.len, c.tok0 + p.partition_size) - c.tok0);
+                if (c.ntok > 0) {
+                    c.t0 = 0;
+                    c.kvh = y / p.subgroups;
+                    c.valid = true;
+                    return;
                 }
             }
+            c.valid = false;
+        };
+        auto entry = [&](const Cursor &c) -> int {  // this lane's block of the tile (-1: none / bad)
+            const int nblk = (min(TILE, c.ntok - c.t0) + BS - 1) / BS;
+            int e = -1;
+            if (lane < nblk) {
+                e = p.block_tables[static_cast<int64_t>(c.walk.seq) * p.max_blocks_per_seq +
+                                   (c.tok0 + c.t0) / BS + lane];
+                if (e < 0 || e >= p.num_blocks) {
+                    if (kv == 0) raise_flag(p.status, PKV_DEVERR_BLOCK_TABLE);
+                    e = -1;
+                }
+            }
+            return e;
+        };
+        next_item(cur);
+        int e_next = cur.valid ? entry(cur) : -1;
+        int last_issue[8];
+        for (int i = 0; i < 8; ++i) last_issue[i] = -1;
+        bool ok = true;
+        for (uint32_t g = 0; cur.valid && ok; ++g) {
+            const int e = e_next;
+            const int kvh = cur.kvh;
+            cur.t0 += TILE;
+            if (cur.t0 >= cur.ntok) next_item(cur);
+            if (cur.valid) e_next = entry(cur);  // in flight while this tile waits
+            const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, e >= 0)) * BS * 256u;
+            const int s = g % nst;
+            int go = 1;
+            if (lane == 0) {
+                go = tc_wait(&empty[s], ((g / nst) & 1) ^ 1, abort_flag, p.status);
+                if (go) {
+                    if (bytes) mbar_arrive_expect_tx(&full[s], bytes);
+                    else mbar_arrive(&full[s]);
+                    last_issue[s] = static_cast<int>(g);
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, go, 0)) {
+                ok = false;
+                break;
+            }
+            if (e >= 0) {
+                unsigned char *slot = ring + s * L::kKVBytes;
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    tc::tma_load_3d(slot + c * L::kHalfBytes + lane * BS * 128, map, c * 64, kvh * BS, e,
+                                    &full[s], policy);
+            }
+            __syncwarp();
         }
         if (!ok && lane == 0) {
             // let every copy this warp issued land before the CTA exits
-            for (int s = 0; s < KS; ++s)
-                if (last_issue[0][s] >= 0)
-                    mbar_wait_bounded(&k_full[s], (last_issue[0][s] / KS) & 1, kDrainTimeoutNs);
-            for (int s = 0; s < VS; ++s)
-                if (last_issue[1][s] >= 0)
-                    mbar_wait_bounded(&v_full[s], (last_issue[1][s] / VS) & 1, kDrainTimeoutNs);
+            for (int s = 0; s < nst; ++s)
+                if (last_issue[s] >= 0)
+                    mbar_wait_bounded(&full[s], (last_issue[s] / nst) & 1, kDrainTimeoutNs);
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
