@@ -124,7 +124,7 @@ pkv_status launch_prefix_tc_one(const PrefixParams &p, const CUtensorMap &tk, co
             return PKV_ERR_CUDA;
         configured_devices.fetch_or(bit, std::memory_order_acq_rel);
     }
-    paged_prefix_tc_kernel<T, BS><<<grid, 192, PrefixLayout::kSmemBytes, stream>>>(tk, tv, p);
+    paged_prefix_tc_kernel<T, BS><<<grid, 224, PrefixLayout::kSmemBytes, stream>>>(tk, tv, p);
     count_launch();
     return launch_status();
 }

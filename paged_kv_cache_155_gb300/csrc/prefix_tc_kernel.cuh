@@ -22,8 +22,9 @@
 // 2^kRescaleLog2.  P is rounded to the input type for the MMA; l adds the fp32
 // values (unbiased rounding, relative error 2^-9 per weight at most).
 //
-// Warps: 0 TMA producer (K ring and V ring, 2 slots each, 3-D tiled copies with
-// 128-byte swizzle), 1 TMEM owner + MMA issuer (event-driven), 2-5 softmax.
+// Warps: 0 / 6 TMA producers of the K ring and the V ring (2 slots each, 3-D
+// tiled copies with 128-byte swizzle), 1 TMEM owner + MMA issuer (event-driven),
+// 2-5 softmax.
 #pragma once
 
 #include "decode_tc_kernel.cuh"
@@ -67,7 +68,7 @@ struct PrefixLayout {
 };
 
 template <typename T, int BS>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     paged_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const PrefixParams p) {
     using L = PrefixLayout;
@@ -136,56 +137,63 @@ __global__ void __launch_bounds__(192, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ===================== TMA producer =====================
+    if (warp == 0 || warp == 6) {
+        // ===================== TMA producers: K (warp 0), V (warp 6) =====================
+        // Separate producers so a K tile never waits behind a V slot that its PV still
+        // holds; each loads the next tile's table entries while it waits for a slot.
+        const int kv = warp == 6;
+        uint64_t *full = kv ? v_full : k_full;
+        uint64_t *empty = kv ? v_empty : k_empty;
+        const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
+        unsigned char *ring = sm + (kv ? L::kOffV : L::kOffK);
         const uint64_t policy = l2_policy_evict_last();  // the prefix is read by every row tile
-        int last_issue[2][2] = {{-1, -1}, {-1, -1}};
-        bool ok = true;
-        for (int j = 0; j < ntiles && ok; ++j) {
+        auto entry = [&](int j) -> int {  // this lane's block of tile j (-1: none or bad)
             const int t0 = tok_lo + j * TILE;
             const int nblk = (min(TILE, tok_hi - t0) + BS - 1) / BS;
             int e = -1;
             if (lane < nblk) {
                 e = p.prefix_table[t0 / BS + lane];
                 if (e < 0 || e >= p.num_blocks) {
-                    raise_flag(p.status, PKV_DEVERR_BLOCK_TABLE);
+                    if (kv == 0) raise_flag(p.status, PKV_DEVERR_BLOCK_TABLE);
                     e = -1;
                 }
             }
+            return e;
+        };
+        int last_issue[2] = {-1, -1};
+        bool ok = true;
+        int e_next = ntiles > 0 ? entry(0) : -1;
+        for (int j = 0; j < ntiles && ok; ++j) {
+            const int e = e_next;
+            if (j + 1 < ntiles) e_next = entry(j + 1);  // in flight while this tile waits
             const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, e >= 0)) * BS * 256u;
-            for (int kv = 0; kv < 2 && ok; ++kv) {
-                const int s = j & 1;
-                uint64_t *fb = kv ? &v_full[s] : &k_full[s];
-                uint64_t *eb = kv ? &v_empty[s] : &k_empty[s];
-                int go = 1;
-                if (lane == 0) {
-                    go = tc_wait(eb, ((j >> 1) & 1) ^ 1, abort_flag, p.status);
-                    if (go) {
-                        if (bytes) mbar_arrive_expect_tx(fb, bytes);
-                        else mbar_arrive(fb);
-                        last_issue[kv][s] = j;
-                    }
+            const int s = j & 1;
+            int go = 1;
+            if (lane == 0) {
+                go = tc_wait(&empty[s], ((j >> 1) & 1) ^ 1, abort_flag, p.status);
+                if (go) {
+                    if (bytes) mbar_arrive_expect_tx(&full[s], bytes);
+                    else mbar_arrive(&full[s]);
+                    last_issue[s] = j;
                 }
-                if (!__shfl_sync(0xffffffffu, go, 0)) {
-                    ok = false;
-                    break;
-                }
-                if (e >= 0) {
-                    unsigned char *slot = sm + (kv ? L::kOffV : L::kOffK) + s * L::kPanel;
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        tc::tma_load_3d(slot + c * L::kHalf + lane * BS * 128, kv ? &tmap_v : &tmap_k,
-                                        c * 64, kvh * BS, e, fb, policy);
-                }
-                __syncwarp();
             }
+            if (!__shfl_sync(0xffffffffu, go, 0)) {
+                ok = false;
+                break;
+            }
+            if (e >= 0) {
+                unsigned char *slot = ring + s * L::kPanel;
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    tc::tma_load_3d(slot + c * L::kHalf + lane * BS * 128, map, c * 64, kvh * BS, e,
+                                    &full[s], policy);
+            }
+            __syncwarp();
         }
         if (!ok && lane == 0) {
-            for (int kv = 0; kv < 2; ++kv)
-                for (int s = 0; s < 2; ++s)
-                    if (last_issue[kv][s] >= 0)
-                        mbar_wait_bounded(kv ? &v_full[s] : &k_full[s], (last_issue[kv][s] >> 1) & 1,
-                                          kDrainTimeoutNs);
+            for (int s = 0; s < 2; ++s)
+                if (last_issue[s] >= 0)
+                    mbar_wait_bounded(&full[s], (last_issue[s] >> 1) & 1, kDrainTimeoutNs);
         }
     } else if (warp == 1) {
         // ===================== MMA issuer (event-driven, PV first) =====================
