@@ -79,7 +79,7 @@ pkv_status launch_decode_tc_one(const DecodeParams &p, const CUtensorMap &tk,
             return PKV_ERR_CUDA;
         configured_devices.fetch_or(bit, std::memory_order_acq_rel);
     }
-    paged_decode_tc_kernel<T, BS, GH><<<grid, 224, TcLayout::kSmemBytes, stream>>>(tk, tv, p);
+    paged_decode_tc_kernel<T, BS, GH><<<grid, 256, TcLayout::kSmemBytes, stream>>>(tk, tv, p);
     count_launch();
     return launch_status();
 }

@@ -22,8 +22,9 @@
 //               into separate rings of 32 KiB K slots and 32 KiB V slots (a K
 //               slot is refilled as soon as QK^T has read it; K never waits
 //               behind a V slot).
-//   warp 1      TMEM owner and MMA issuer (one thread): QK^T of tile i+1 is
-//               issued before PV of tile i so the softmax of tile i overlaps it.
+//   warp 1      TMEM owner and QK^T issuer (one thread); warp 7 issues PV, so a
+//               ready PV never waits behind a QK^T batch (a batch of MMAs holds
+//               its issuing thread for its whole execution).
 //   warps 2-5   softmax and accumulation, one TMEM lane quarter each: a thread
 //               owns a token row of S and a head-dim row of O^T; the tile max is
 //               exchanged through shared memory; o stays in registers.
@@ -59,7 +60,7 @@ struct TcLayout {
     static constexpr int kOffP = kOffQ + 2 * kPanelBytes;
     static constexpr int kOffRed = kOffP + 2 * kPanelBytes;           // float [2][4][16] + [4][16]
     static constexpr int kOffBar = kOffRed + 3 * 4 * 16 * 4;
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 1 + 1;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 2 * 5 + 2 + 1 + 2;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;           // tmem slot, abort flag
     static constexpr int kMaxStagedSeqs = 1024;                      // context lengths kept in smem
     static constexpr int kOffLens = kOffMisc + 16;
@@ -127,7 +128,7 @@ __device__ __forceinline__ bool tc_wait_warp(uint64_t *bar, uint32_t parity,
 }
 
 template <typename T, int BS, int GH>
-__global__ void __launch_bounds__(224, 1)
+__global__ void __launch_bounds__(256, 1)
     paged_decode_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const DecodeParams p) {
     using L = TcLayout;
@@ -154,6 +155,7 @@ __global__ void __launch_bounds__(224, 1)
     uint64_t *max_bar = s_full + 10;      // [2] softmax tile-max exchange
     uint64_t *lsum_bar = s_full + 12;     // softmax l exchange
     uint64_t *drain_bar = s_full + 13;    // MMA drain on exit
+    uint64_t *drain_pv = s_full + 14;     // PV issuer's drain on exit
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
     float *red_max = reinterpret_cast<float *>(sm + L::kOffRed);            // [2][4][16]
@@ -185,6 +187,7 @@ __global__ void __launch_bounds__(224, 1)
         }
         mbar_init(lsum_bar, 4);
         mbar_init(drain_bar, 1);
+        mbar_init(drain_pv, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -303,11 +306,9 @@ __global__ void __launch_bounds__(224, 1)
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
-        // Event-driven: lane 0 polls the barriers and issues whichever MMA is
-        // ready, PV first (it frees a V slot), else the next tile's QK^T.  A
-        // fixed order would make PV of one tile wait for the next tile's K.
+        // QK^T of each tile in order, as soon as its K landed and its S buffer is
+        // free (PV is issued by warp 7).
         constexpr uint32_t idesc_qk = tc::idesc_f16_f32acc(kBF16, 128, L::kN, false, false);
-        constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, L::kN, true, false);
         // Queries of the next item that has tiles, loaded into registers one
         // item ahead so no global load sits in front of an item's first MMA.
         constexpr int QCHUNKS = (GH * 16 + 31) / 32;  // 16-byte chunks per lane
@@ -352,42 +353,93 @@ __global__ void __launch_bounds__(224, 1)
             return false;
         };
         bool have_tile = next_item();
-        uint32_t n_qk = 0, n_pv = 0;  // tiles whose QK^T / PV have been issued
-        uint32_t items = 0;           // items whose queries went to a panel
+        uint32_t n_qk = 0;   // tiles whose QK^T has been issued
+        uint32_t items = 0;  // items whose queries went to a panel
         bool ok = true;
-        uint64_t idle_since = 0;
-        while (ok && (have_tile || n_pv < n_qk)) {
-            int act = 0;  // 1 = PV, 2 = QK
-            if (lane == 0) {
-                if (n_pv < n_qk && mbar_test_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
-                    mbar_test_wait(&o_empty[n_pv & 1], ((n_pv >> 1) & 1) ^ 1) &&
-                    mbar_test_wait(&v_full[n_pv % VS], (n_pv / VS) & 1))
-                    act = 1;
-                else if (have_tile && mbar_test_wait(&k_full[n_qk % KS], (n_qk / KS) & 1) &&
-                         mbar_test_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
-                    act = 2;
-                if (act) {
-                    idle_since = 0;
-                } else {
-                    const uint64_t now = global_timer_ns();
-                    if (!idle_since) idle_since = now;
-                    if (*abort_flag) {
-                        act = -1;
-                    } else if (now - idle_since > kWaitTimeoutNs) {
-                        raise_flag(p.status, PKV_DEVERR_TIMEOUT);
-                        *abort_flag = 1;
-                        act = -1;
-                    }
-                }
-            }
-            act = __shfl_sync(0xffffffffu, act, 0);
-            if (act < 0) {
+        while (ok && have_tile) {
+            int go = 1;
+            if (lane == 0)
+                go = tc_wait(&k_full[n_qk % KS], (n_qk / KS) & 1, abort_flag, p.status) &&
+                     tc_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1, abort_flag, p.status);
+            if (!__shfl_sync(0xffffffffu, go, 0)) {
                 ok = false;
                 break;
             }
-            if (act == 1) {
+            const int qb = (items - (t0 == 0 ? 0 : 1)) & 1;  // panel of this tile's item
+            if (t0 == 0) {
+                // this item's queries -> Q panel qb (K-major, 128-byte swizzle).  The
+                // QK^T that last read this panel (two items back) has completed: the
+                // s_empty wait above showed S of tile n_qk-2 was consumed.
+                unsigned char *panel = sm + L::kOffQ + qb * L::kPanelBytes;
+#pragma unroll
+                for (int c = 0; c < QCHUNKS; ++c) {
+                    const int i = lane + c * 32;
+                    if (i < GH * 16) {
+                        const int row = i >> 4, c8 = i & 15;
+                        const uint32_t off = ((c8 >> 3) * 2 + (row >> 3)) * 1024 + (row & 7) * 128 +
+                                             (((c8 & 7) ^ (row & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(panel + off) = qreg[c];
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                ++items;
+            }
+            if (lane == 0) {
+                const uint32_t g = n_qk;
+                const int b = g & 1;
+                tc::fence_after_sync();
+                const uint32_t k_addr = smem_base + L::kOffK + (g % KS) * L::kKVBytes;
+                const uint32_t q_addr = smem_base + L::kOffQ + qb * L::kPanelBytes;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t a = tc::smem_desc_sw128(
+                        k_addr + (k / 4) * L::kHalfBytes + (k % 4) * 32, 16, 1024);
+                    const uint64_t bd =
+                        tc::smem_desc_sw128(q_addr + (k / 4) * 2048 + (k % 4) * 32, 16, 1024);
+                    tc::mma_f16_ss(tmem + 16 * b, a, bd, idesc_qk, k > 0);
+                }
+                tc::mma_commit(&s_full[b]);
+                tc::mma_commit(&k_empty[g % KS]);
+            }
+            __syncwarp();
+            if (t0 == 0) load_next_q();
+            ++n_qk;
+            t0 += TILE;
+            if (t0 >= ntok) have_tile = next_item();
+        }
+        if (lane == 0) {
+            // all MMAs of this CTA complete before TMEM is released
+            tc::mma_commit(drain_bar);
+            mbar_wait_bounded(drain_bar, 0, kDrainTimeoutNs);
+        }
+        __syncwarp();
+    } else if (warp == 7) {
+        // ===================== PV issuer =====================
+        // PV of tile t as soon as P(t) is written (and V(t) landed, O(t) of two
+        // tiles back read): a second issuing thread, so a PV never waits behind the
+        // QK^T batch of the next tile (an MMA batch holds its issuing thread for
+        // its whole execution).
+        constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, L::kN, true, false);
+        ItemWalker walk;
+        uint32_t t = 0;
+        bool ok = true;
+        for (int64_t r = blockIdx.x; ok; r += gridDim.x) {
+            int y, part;
+            if (!walk.seek(p, s_len, r, y, part)) break;
+            const int tok0 = p.tok_begin + part * p.partition_size;
+            const int ntok = max(0, min(walk.len, tok0 + p.partition_size) - tok0);
+            for (int t0 = 0; t0 < ntok; t0 += TILE, ++t) {
+                int go = 1;
+                if (lane == 0)
+                    go = tc_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag, p.status) &&
+                         tc_wait(&o_empty[t & 1], ((t >> 1) & 1) ^ 1, abort_flag, p.status) &&
+                         tc_wait(&v_full[t % VS], (t / VS) & 1, abort_flag, p.status);
+                if (!__shfl_sync(0xffffffffu, go, 0)) {
+                    ok = false;
+                    break;
+                }
                 if (lane == 0) {
-                    const uint32_t t = n_pv;
                     const int b = t & 1;
                     tc::fence_after_sync();
                     const uint32_t v_addr = smem_base + L::kOffV + (t % VS) * L::kKVBytes;
@@ -402,56 +454,13 @@ __global__ void __launch_bounds__(224, 1)
                     tc::mma_commit(&o_full[b]);
                     tc::mma_commit(&v_empty[t % VS]);
                 }
-                ++n_pv;
-            } else if (act == 2) {
-                const int qb = (items - (t0 == 0 ? 0 : 1)) & 1;  // panel of this tile's item
-                if (t0 == 0) {
-                    // this item's queries -> Q panel qb (K-major, 128-byte swizzle).  The
-                    // QK^T that last read this panel (two items back) has completed: the
-                    // s_empty wait above showed S of tile n_qk-2 was consumed.
-                    unsigned char *panel = sm + L::kOffQ + qb * L::kPanelBytes;
-#pragma unroll
-                    for (int c = 0; c < QCHUNKS; ++c) {
-                        const int i = lane + c * 32;
-                        if (i < GH * 16) {
-                            const int row = i >> 4, c8 = i & 15;
-                            const uint32_t off = ((c8 >> 3) * 2 + (row >> 3)) * 1024 + (row & 7) * 128 +
-                                                 (((c8 & 7) ^ (row & 7)) << 4);
-                            *reinterpret_cast<uint4 *>(panel + off) = qreg[c];
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    ++items;
-                }
-                if (lane == 0) {
-                    const uint32_t g = n_qk;
-                    const int b = g & 1;
-                    tc::fence_after_sync();
-                    const uint32_t k_addr = smem_base + L::kOffK + (g % KS) * L::kKVBytes;
-                    const uint32_t q_addr = smem_base + L::kOffQ + qb * L::kPanelBytes;
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint64_t a = tc::smem_desc_sw128(
-                            k_addr + (k / 4) * L::kHalfBytes + (k % 4) * 32, 16, 1024);
-                        const uint64_t bd =
-                            tc::smem_desc_sw128(q_addr + (k / 4) * 2048 + (k % 4) * 32, 16, 1024);
-                        tc::mma_f16_ss(tmem + 16 * b, a, bd, idesc_qk, k > 0);
-                    }
-                    tc::mma_commit(&s_full[b]);
-                    tc::mma_commit(&k_empty[g % KS]);
-                }
                 __syncwarp();
-                if (t0 == 0) load_next_q();
-                ++n_qk;
-                t0 += TILE;
-                if (t0 >= ntok) have_tile = next_item();
             }
         }
         if (lane == 0) {
-            // all MMAs of this CTA complete before TMEM is released
-            tc::mma_commit(drain_bar);
-            mbar_wait_bounded(drain_bar, 0, kDrainTimeoutNs);
+            // this thread's MMAs complete before TMEM is released
+            tc::mma_commit(drain_pv);
+            mbar_wait_bounded(drain_pv, 0, kDrainTimeoutNs);
         }
         __syncwarp();
     } else {
