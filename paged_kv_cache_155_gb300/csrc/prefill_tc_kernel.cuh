@@ -26,8 +26,9 @@
 // paged_prefill_merge_kernel combines.
 //
 // Warps: 0 / 10 TMA producers of the K / V rings (PrefillLayout::kKS / kVS
-// slots), 1 TMEM owner + MMA issuer, 2-9 softmax in pairs: warps w and w + 4 share TMEM lane quarter w & 3
-// (the same 32 query rows) and take tile columns 0-63 and 64-127.  A pair
+// slots), 1 TMEM owner + QK^T issuer, 11 PV issuer, 2-9 softmax in pairs:
+// warps w and w + 4 share TMEM lane quarter w & 3 (the same 32 query rows)
+// and take tile columns 0-63 and 64-127.  A pair
 // exchanges its partial row maxima each tile through two spare TMEM columns
 // (an mbarrier with a bounded wait orders them), so both warps hold the same
 // reference maximum; each rescales, writes P for and outputs its own half.
@@ -84,19 +85,19 @@ struct PrefillLayout {
     static constexpr int kOffV = kOffK + kKS * kPanel;
     static constexpr int kOffP = kOffV + kVS * kPanel;
     static constexpr int kOffBar = kOffP + kPB * kPanel;
-    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 8 + 1 + 8;
+    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 8 + 2 + 8;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kSmemBytes = kBytes + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;        // S[2] at 0 / 128, O at 256, exchange 384
     static constexpr uint32_t kXchgCol = 384;         // spare TMEM columns for the pairs
     static constexpr float kRescaleLog2 = 8.f;
-    static constexpr int kThreads = 352;
+    static constexpr int kThreads = 384;
     static_assert(kSmemBytes <= 232448, "dynamic shared memory per block");
 };
 
 template <typename T, int BS>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
     using L = PrefillLayout;
@@ -133,8 +134,9 @@ __global__ void __launch_bounds__(352, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
     uint64_t *k_full = bars, *k_empty = k_full + KS, *v_full = k_empty + KS, *v_empty = v_full + VS;
     uint64_t *s_full = v_empty + VS, *s_empty = s_full + 2, *p_full = s_full + 4, *o_done = s_full + 6;
-    uint64_t *drain_bar = s_full + 8;
-    uint64_t *pair_bar = drain_bar + 1;  // [quarter][parity]
+    uint64_t *drain_bar = s_full + 8;      // QK^T issuer's drain on exit
+    uint64_t *drain_pv = s_full + 9;       // PV issuer's drain on exit
+    uint64_t *pair_bar = drain_pv + 1;     // [quarter][parity]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
     const uint32_t smem_base = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
@@ -156,6 +158,7 @@ __global__ void __launch_bounds__(352, 1)
         }
         for (int i = 0; i < 8; ++i) mbar_init(&pair_bar[i], 2);
         mbar_init(drain_bar, 1);
+        mbar_init(drain_pv, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -250,71 +253,67 @@ __global__ void __launch_bounds__(352, 1)
                     mbar_wait_bounded(&full[s], (last_issue[s] / nst) & 1, kDrainTimeoutNs);
         }
     } else if (warp == 1) {
-        // ===================== MMA issuer (event-driven, PV first) =====================
+        // ===================== QK^T issuer =====================
+        // QK^T of each tile as soon as its K landed and its S buffer is free; PV is
+        // issued by warp 11, so a ready PV never waits behind a QK^T batch (a batch
+        // of MMAs holds its issuing thread for its whole execution).
         constexpr uint32_t idesc_qk = tc::idesc_f16_f32acc(kBF16, 128, 128, false, false);
-        constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, 128, false, true);
-        int n_qk = 0, n_pv = 0;
-        bool ok = true;
-        uint64_t idle_since = 0;
-        while (ok && n_pv < ntiles) {
-            int act = 0;
+        for (int j = 0; j < ntiles; ++j) {
+            int go = 1;
+            if (lane == 0)
+                go = tc_wait(&k_full[j % KS], (j / KS) & 1, abort_flag, p.status) &&
+                     tc_wait(&s_empty[j & 1], ((j >> 1) & 1) ^ 1, abort_flag, p.status);
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
             if (lane == 0) {
-                if (n_pv < n_qk && mbar_test_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
-                    mbar_test_wait(&v_full[n_pv % VS], (n_pv / VS) & 1))
-                    act = 1;
-                else if (n_qk < ntiles && mbar_test_wait(&k_full[n_qk % KS], (n_qk / KS) & 1) &&
-                         mbar_test_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
-                    act = 2;
-                if (act) {
-                    idle_since = 0;
-                } else {
-                    const uint64_t now = global_timer_ns();
-                    if (!idle_since) idle_since = now;
-                    if (*abort_flag) {
-                        act = -1;
-                    } else if (now - idle_since > kWaitTimeoutNs) {
-                        raise_flag(p.status, PKV_DEVERR_TIMEOUT);
-                        *abort_flag = 1;
-                        act = -1;
-                    }
-                }
-                if (act == 1) {
-                    const int j = n_pv, b = j & 1;
-                    tc::fence_after_sync();
-                    const uint32_t pa = smem_base + L::kOffP + (j % PB) * L::kPanel;
-                    const uint32_t va = smem_base + L::kOffV + (j % VS) * L::kPanel;
+                const int b = j & 1;
+                tc::fence_after_sync();
+                const uint32_t qa = smem_base + L::kOffQ;
+                const uint32_t ka = smem_base + L::kOffK + (j % KS) * L::kPanel;
 #pragma unroll
-                    for (int k = 0; k < TILE / 16; ++k) {
-                        const uint64_t a = tc::smem_desc_sw128(pa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
-                        const uint64_t bd = tc::smem_desc_sw128(va + k * 2048, L::kHalf, 1024);
-                        tc::mma_f16_ss(tmem + 256, a, bd, idesc_pv, j > 0 || k > 0);
-                    }
-                    tc::mma_commit(&o_done[b]);
-                    tc::mma_commit(&v_empty[j % VS]);
-                } else if (act == 2) {
-                    const int j = n_qk, b = j & 1;
-                    tc::fence_after_sync();
-                    const uint32_t qa = smem_base + L::kOffQ;
-                    const uint32_t ka = smem_base + L::kOffK + (j % KS) * L::kPanel;
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint64_t a = tc::smem_desc_sw128(qa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
-                        const uint64_t bd = tc::smem_desc_sw128(ka + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
-                        tc::mma_f16_ss(tmem + 128 * b, a, bd, idesc_qk, k > 0);
-                    }
-                    tc::mma_commit(&s_full[b]);
-                    tc::mma_commit(&k_empty[j % KS]);
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t a = tc::smem_desc_sw128(qa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc_sw128(ka + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                    tc::mma_f16_ss(tmem + 128 * b, a, bd, idesc_qk, k > 0);
                 }
+                tc::mma_commit(&s_full[b]);
+                tc::mma_commit(&k_empty[j % KS]);
             }
-            act = __shfl_sync(0xffffffffu, act, 0);
-            if (act < 0) ok = false;
-            else if (act == 1) ++n_pv;
-            else if (act == 2) ++n_qk;
+            __syncwarp();
         }
         if (lane == 0) {
-            // every MMA of this CTA completes before TMEM is released
+            // this thread's MMAs complete before TMEM is released
             tc::mma_commit(drain_bar);
             mbar_wait_bounded(drain_bar, 0, kDrainTimeoutNs);
+        }
+        __syncwarp();
+    } else if (warp == 11) {
+        // ===================== PV issuer =====================
+        constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, 128, false, true);
+        for (int j = 0; j < ntiles; ++j) {
+            int go = 1;
+            if (lane == 0)
+                go = tc_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, p.status) &&
+                     tc_wait(&v_full[j % VS], (j / VS) & 1, abort_flag, p.status);
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
+            if (lane == 0) {
+                const int b = j & 1;
+                tc::fence_after_sync();
+                const uint32_t pa = smem_base + L::kOffP + (j % PB) * L::kPanel;
+                const uint32_t va = smem_base + L::kOffV + (j % VS) * L::kPanel;
+#pragma unroll
+                for (int k = 0; k < TILE / 16; ++k) {
+                    const uint64_t a = tc::smem_desc_sw128(pa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc_sw128(va + k * 2048, L::kHalf, 1024);
+                    tc::mma_f16_ss(tmem + 256, a, bd, idesc_pv, j > 0 || k > 0);
+                }
+                tc::mma_commit(&o_done[b]);
+                tc::mma_commit(&v_empty[j % VS]);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) {
+            tc::mma_commit(drain_pv);
+            mbar_wait_bounded(drain_pv, 0, kDrainTimeoutNs);
         }
         __syncwarp();
     } else {
@@ -514,7 +513,7 @@ __global__ void __launch_bounds__(352, 1)
         }
     }
 
-    // ---- tear-down: the MMA warp drained its MMAs; TMEM is freed
+    // ---- tear-down: both issuers drained their MMAs; TMEM is freed
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) {
