@@ -43,6 +43,24 @@ bool encode_half_map(CUtensorMap *map, const void *base, int64_t num_blocks,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view of the prefill queries [num_rows][num_q_heads][128]: boxes of
+// `tokens` tokens x `group` heads x 64 columns, 128-byte swizzled, so a box
+// lands as tokens * group consecutive 128-byte rows (token-major).
+bool encode_query_map(CUtensorMap *map, const void *q, int num_rows, int num_q_heads, int group,
+                      int tokens, pkv_dtype dt) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(num_q_heads),
+                                static_cast<cuuint64_t>(num_rows)};
+    const cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(num_q_heads) * 128 * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(tokens)};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    return fn(map, dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+              3, const_cast<void *>(q), dims, strides, box, elem_strides,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace pkv
 
 namespace {

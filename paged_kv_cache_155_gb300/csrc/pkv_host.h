@@ -26,6 +26,12 @@ void count_launch();
 bool encode_half_map(CUtensorMap *map, const void *base, int64_t num_blocks,
                      int64_t block_stride_elems, int num_kv_heads, int block_size, pkv_dtype dt);
 
+// Tiled tensor map of the prefill queries [num_rows][num_q_heads][128] for
+// 3-D TMA loads: boxes of `tokens` tokens x `group` query heads x 64 columns,
+// 128-byte swizzled (group <= 256, tokens <= 256).
+bool encode_query_map(CUtensorMap *map, const void *q, int num_rows, int num_q_heads, int group,
+                      int tokens, pkv_dtype dt);
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline pkv_status launch_status() {

@@ -1,6 +1,7 @@
 // prefill.cu -- the pkv_paged_attention_prefill entry point (chunked prefill
-// attention over the paged cache): argument checks, the KV-split plan, and
-// the launches of paged_prefill_tc_kernel and its merge.
+// attention over the paged cache): argument checks, the row-tile and KV-split
+// plan, and the launches of the persistent paged_prefill_tc_kernel and its
+// merge.
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -13,9 +14,11 @@ namespace {
 constexpr int kMinSplitTokens = 512;  // a KV split covers at least 4 tiles
 
 struct PrefillPlan {
-    int row_tiles = 0;     // 128-row tiles of the longest chunk
+    int tile_tokens = 0;   // chunk tokens per row tile: 128 / group
+    int row_tiles = 0;     // row tiles of the longest chunk
     int splits = 0;
     int split_tokens = 0;  // multiple of 128
+    int items = 0;         // row_tiles * num_kv_heads * num_seqs * splits
 };
 
 pkv_status plan_prefill(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -28,8 +31,9 @@ pkv_status plan_prefill(int num_seqs, int num_q_heads, int num_kv_heads, int hea
         num_kv_heads > 65535)
         return PKV_ERR_INVALID_ARG;
     const int group = num_q_heads / num_kv_heads;
-    const int64_t row_tiles = (static_cast<int64_t>(max_query_len) * group + 127) / 128;
-    if (row_tiles > 0x7fffffff) return PKV_ERR_INVALID_ARG;
+    if (group > 128) return PKV_ERR_UNSUPPORTED;  // a row tile holds at least one token
+    pp->tile_tokens = 128 / group;
+    const int64_t row_tiles = (static_cast<int64_t>(max_query_len) + pp->tile_tokens - 1) / pp->tile_tokens;
     pp->row_tiles = static_cast<int>(row_tiles);
     const int64_t ctx_tiles = std::max<int64_t>(1, (max_context_len + 127) / 128);
     int64_t want = kv_splits;
@@ -44,6 +48,9 @@ pkv_status plan_prefill(int num_seqs, int num_q_heads, int num_kv_heads, int hea
     pp->split_tokens = static_cast<int>(tiles_per_split * 128);
     pp->splits = static_cast<int>((ctx_tiles + tiles_per_split - 1) / tiles_per_split);
     if (static_cast<int64_t>(num_seqs) * pp->splits > 65535) return PKV_ERR_INVALID_ARG;
+    const int64_t items = row_tiles * num_kv_heads * num_seqs * pp->splits;  // < 2^63
+    if (items > 0x7fffffff) return PKV_ERR_INVALID_ARG;
+    pp->items = static_cast<int>(items);
     return PKV_OK;
 }
 
@@ -53,8 +60,8 @@ size_t prefill_workspace(int num_rows, int num_q_heads, int splits) {
 }
 
 template <typename T, int BS>
-pkv_status launch_prefill_one(const pkv::PrefillParams &p, const CUtensorMap &tk,
-                              const CUtensorMap &tv, dim3 grid, cudaStream_t stream) {
+pkv_status launch_prefill_one(const pkv::PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                              const CUtensorMap &tv, int grid, cudaStream_t stream) {
     static std::atomic<uint64_t> configured_devices{0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -67,18 +74,19 @@ pkv_status launch_prefill_one(const pkv::PrefillParams &p, const CUtensorMap &tk
         configured_devices.fetch_or(bit, std::memory_order_acq_rel);
     }
     pkv::paged_prefill_tc_kernel<T, BS>
-        <<<grid, pkv::PrefillLayout::kThreads, pkv::PrefillLayout::kSmemBytes, stream>>>(tk, tv, p);
+        <<<grid, pkv::PrefillLayout::kThreads, pkv::PrefillLayout::kSmemBytes, stream>>>(tq, tk, tv, p);
     pkv::count_launch();
     return pkv::launch_status();
 }
 
 template <typename T>
-pkv_status launch_prefill(const pkv::PrefillParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                          int block_size, dim3 grid, int max_query_len, cudaStream_t s) {
+pkv_status launch_prefill(const pkv::PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                          const CUtensorMap &tv, int block_size, int grid, int max_query_len,
+                          cudaStream_t s) {
     pkv_status st = PKV_ERR_UNSUPPORTED;
-    if (block_size == 8) st = launch_prefill_one<T, 8>(p, tk, tv, grid, s);
-    else if (block_size == 16) st = launch_prefill_one<T, 16>(p, tk, tv, grid, s);
-    else if (block_size == 32) st = launch_prefill_one<T, 32>(p, tk, tv, grid, s);
+    if (block_size == 8) st = launch_prefill_one<T, 8>(p, tq, tk, tv, grid, s);
+    else if (block_size == 16) st = launch_prefill_one<T, 16>(p, tq, tk, tv, grid, s);
+    else if (block_size == 32) st = launch_prefill_one<T, 32>(p, tq, tk, tv, grid, s);
     if (st != PKV_OK || p.splits == 1) return st;
     const int64_t rows = static_cast<int64_t>(max_query_len) * p.num_q_heads;
     const dim3 mgrid(static_cast<unsigned>((rows + 3) / 4), static_cast<unsigned>(p.num_seqs));
@@ -132,8 +140,9 @@ PKV_API pkv_status pkv_paged_attention_prefill(
     pkv_status st = plan_prefill(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                  max_query_len, max_context_len, kv_splits, 1, &pp);
     if (st != PKV_OK) return st;
+    int sm = 0;
     if (kv_splits == 0) {
-        const int sm = pkv::current_sm_count();
+        sm = pkv::current_sm_count();
         if (sm <= 0) return PKV_ERR_CUDA;
         st = plan_prefill(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_query_len,
                           max_context_len, 0, sm, &pp);
@@ -144,8 +153,12 @@ PKV_API pkv_status pkv_paged_attention_prefill(
         return PKV_ERR_INVALID_ARG;
     unsigned int *status = pkv::status_word_ptr();
     if (!status) return PKV_ERR_CUDA;
-    CUtensorMap tk, tv;
-    if (!pkv::encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads, block_size,
+    if (sm == 0) sm = pkv::current_sm_count();
+    if (sm <= 0) return PKV_ERR_CUDA;
+    const int group = num_q_heads / num_kv_heads;
+    CUtensorMap tq, tk, tv;
+    if (!pkv::encode_query_map(&tq, q, num_rows, num_q_heads, group, pp.tile_tokens, dtype) ||
+        !pkv::encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads, block_size,
                               dtype) ||
         !pkv::encode_half_map(&tv, v_cache, num_blocks, block_stride_elems, num_kv_heads, block_size,
                               dtype))
@@ -169,16 +182,21 @@ PKV_API pkv_status pkv_paged_attention_prefill(
     p.num_rows = num_rows;
     p.num_seqs = num_seqs;
     p.num_q_heads = num_q_heads;
-    p.group = num_q_heads / num_kv_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = group;
+    p.tile_tokens = pp.tile_tokens;
+    p.tile_rows = pp.tile_tokens * group;
+    p.row_tiles = pp.row_tiles;
+    p.num_items = pp.items;
     p.splits = pp.splits;
     p.split_tokens = pp.split_tokens;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
-    const dim3 grid(static_cast<unsigned>(pp.row_tiles), static_cast<unsigned>(num_kv_heads),
-                    static_cast<unsigned>(num_seqs * pp.splits));
+    // persistent: one CTA per SM (or per item when there are fewer)
+    const int grid = std::min(pp.items, sm);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == PKV_F16
-               ? launch_prefill<__half>(p, tk, tv, block_size, grid, max_query_len, s)
-               : launch_prefill<__nv_bfloat16>(p, tk, tv, block_size, grid, max_query_len, s);
+               ? launch_prefill<__half>(p, tq, tk, tv, block_size, grid, max_query_len, s)
+               : launch_prefill<__nv_bfloat16>(p, tq, tk, tv, block_size, grid, max_query_len, s);
 }
 
 }  // extern "C"

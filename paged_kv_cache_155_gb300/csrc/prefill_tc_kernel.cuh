@@ -9,29 +9,39 @@
 // query_start[i] + j) sits at position L_i - C_i + j and attends to tokens
 // 0 .. that position.
 //
-// One CTA: 128 query rows of one sequence and one KV head -- row r of the
-// sequence's rows is chunk token r / G, query head r % G of the group, so a
-// KV tile is shared by the G heads of every token in the tile -- over one
-// split of the KV range (all of it unless the grid would be too small).  The
-// KV range ends at the causal limit of the tile's last row; inside a tile a
-// row's columns past its own position are masked.  Same machinery as the
-// shared-prefix tile kernel: tcgen05 MMAs with M = 128 rows, N = 128 tokens,
-// K = 128; S double-buffered in TMEM, O accumulated in TMEM; a row's softmax is
-// local to one thread (its 128 scores are read from TMEM once per tile); the
-// row's reference maximum moves only when a tile exceeds it by more than
-// kRescaleLog2.  The row sum l adds the fp32 weights whose bf16/fp16
+// Work item: the query rows of one row tile of one sequence and one KV head --
+// row r of the sequence's rows is chunk token r / G, query head r % G of the
+// group, so a KV tile is shared by the G heads of every token in the tile; a
+// row tile holds 128 / G whole tokens (R = G * (128 / G) <= 128 rows) -- over
+// one split of the KV range (all of it unless the row tiles alone would leave
+// SMs idle).  The KV range ends at the causal limit of the tile's last row;
+// inside a tile a row's columns past its own position are masked.  Same
+// machinery as the shared-prefix tile kernel: tcgen05 MMAs with M = 128 rows,
+// N = 128 tokens, K = 128; S double-buffered in TMEM, O accumulated in TMEM; a
+// row's softmax is local to one thread pair (its scores are read from TMEM once
+// per tile); the row's reference maximum moves only when a tile exceeds it by
+// more than kRescaleLog2.  The row sum l adds the fp32 weights whose bf16/fp16
 // roundings feed the PV MMA (unbiased rounding, relative error 2^-9 per weight
-// at most).  With one split the kernel writes the
-// normalised output; with several it writes (o, m, l) partials that
-// paged_prefill_merge_kernel combines.
+// at most).  With one split the kernel writes the normalised output; with
+// several it writes (o, m, l) partials that paged_prefill_merge_kernel
+// combines.
+//
+// Persistent CTAs, one per SM: CTA c takes items c, c + grid, ... of a static
+// order with the heaviest row tiles (longest causal range) first, which
+// balances the SMs without a shared counter.  Every role walks the same item
+// list and counts tiles across items, so the rings and barriers run on from
+// one item to the next: the queries of the next item (a TMA load into the
+// second of two Q buffers) and its first K/V tiles and S = QK^T are in flight
+// while the softmax warps still write out the current item.
 //
 // Warps: 0 / 10 TMA producers of the K / V rings (PrefillLayout::kKS / kVS
-// slots), 1 TMEM owner + QK^T issuer, 11 PV issuer, 2-9 softmax in pairs:
-// warps w and w + 4 share TMEM lane quarter w & 3 (the same 32 query rows)
-// and take tile columns 0-63 and 64-127.  A pair
-// exchanges its partial row maxima each tile through two spare TMEM columns
-// (an mbarrier with a bounded wait orders them), so both warps hold the same
-// reference maximum; each rescales, writes P for and outputs its own half.
+// slots; warp 0 also loads each item's Q tile), 1 TMEM owner + QK^T issuer,
+// 11 PV issuer, 2-9 softmax in pairs: warps w and w + 4 share TMEM lane
+// quarter w & 3 (the same 32 query rows) and take tile columns 0-63 and
+// 64-127.  A pair exchanges its partial row maxima each tile through two spare
+// TMEM columns (an mbarrier with a bounded wait orders them), so both warps
+// hold the same reference maximum; each rescales, writes P for and outputs
+// its own half.
 #pragma once
 
 #include "prefix_tc_kernel.cuh"
@@ -55,7 +65,12 @@ struct PrefillParams {
     int num_rows;      // query_start[num_seqs] as given by the host
     int num_seqs;
     int num_q_heads;
+    int num_kv_heads;
     int group;
+    int tile_tokens;   // chunk tokens per row tile: 128 / group
+    int tile_rows;     // query rows per row tile: tile_tokens * group
+    int row_tiles;     // row tiles of the longest chunk
+    int num_items;     // row_tiles * num_kv_heads * num_seqs * splits
     int splits;        // KV splits per row tile
     int split_tokens;  // tokens per split, a multiple of 128
     float scale_log2;
@@ -73,19 +88,63 @@ __device__ __forceinline__ bool prefill_seq(const PrefillParams &p, int seq, int
            len <= p.len_cap;
 }
 
-// Shared memory: the Q tile, K and V rings of 128-token tiles, P buffers, and
-// the barriers (rings, S / P / O double buffers, the softmax pairs).
+struct PrefillItem {
+    int q0, chunk, len;  // the sequence's chunk start row, chunk length, context length
+    int kvh, split, row_tile;
+    int rows;            // the sequence's query rows of one KV head: chunk * group
+    int row0;            // first of the item's rows: row_tile * tile_rows
+    int base_pos;        // position of chunk token 0
+    int tok_lo, tok_hi;  // the item's KV tokens
+    int ntiles;          // 128-token KV tiles
+    int seq;
+};
+
+// Item i of the static order: row tiles from the last (longest causal range)
+// down, then sequence and split, then KV head.  False when the item holds no
+// work: a row tile past the chunk, a split past the tile's causal limit, or a
+// sequence out of contract (flagged once when `flag`).
+__device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, bool flag,
+                                             PrefillItem &it) {
+    const int per_tile = p.num_kv_heads * p.num_seqs * p.splits;
+    const int rt_rev = i / per_tile;
+    const int rem = i - rt_rev * per_tile;
+    const int ss = rem / p.num_kv_heads;
+    it.kvh = rem - ss * p.num_kv_heads;
+    it.seq = ss / p.splits;
+    it.split = ss - it.seq * p.splits;
+    it.row_tile = p.row_tiles - 1 - rt_rev;
+    if (!prefill_seq(p, it.seq, it.q0, it.chunk, it.len)) {
+        if (flag && it.row_tile == 0 && it.kvh == 0 && it.split == 0)
+            raise_flag(p.status, PKV_DEVERR_CONTEXT_LEN);
+        return false;
+    }
+    it.rows = it.chunk * p.group;
+    it.row0 = it.row_tile * p.tile_rows;
+    if (it.row0 >= it.rows) return false;
+    const int last_row = min(it.rows, it.row0 + p.tile_rows) - 1;
+    it.base_pos = it.len - it.chunk;
+    const int pos_max = it.base_pos + last_row / p.group;
+    it.tok_lo = it.split * p.split_tokens;
+    it.tok_hi = min(min(it.len, pos_max + 1), it.tok_lo + p.split_tokens);
+    it.ntiles = (it.tok_hi - it.tok_lo + 127) / 128;
+    return it.tok_hi > it.tok_lo;
+}
+
+// Shared memory: two Q tiles (consecutive items), K and V rings of 128-token
+// tiles, P buffers, and the barriers (rings, Q / S / P / O double buffers, the
+// softmax pairs).
 struct PrefillLayout {
     static constexpr int kTile = 128;
     static constexpr int kHalf = 128 * 128;           // 128 rows x 128 B
     static constexpr int kPanel = 2 * kHalf;          // 128 rows x 128 16-bit values
+    static constexpr int kQB = 2;                     // Q buffers
     static constexpr int kKS = 2, kVS = 2, kPB = 1;   // K slots, V slots, P buffers
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kPanel;
+    static constexpr int kOffK = kOffQ + kQB * kPanel;
     static constexpr int kOffV = kOffK + kKS * kPanel;
     static constexpr int kOffP = kOffV + kVS * kPanel;
     static constexpr int kOffBar = kOffP + kPB * kPanel;
-    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 8 + 2 + 8;
+    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 2 * kQB + 8 + 2 + 8;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kSmemBytes = kBytes + 1024;  // + alignment slack
@@ -98,7 +157,8 @@ struct PrefillLayout {
 
 template <typename T, int BS>
 __global__ void __launch_bounds__(384, 1)
-    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
+    paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                            const __grid_constant__ CUtensorMap tmap_k,
                             const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
     using L = PrefillLayout;
     constexpr int TILE = L::kTile, D = 128;
@@ -106,34 +166,16 @@ __global__ void __launch_bounds__(384, 1)
     static_assert(TILE / BS <= 32, "one table entry per producer lane");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // heavy (late) row tiles first: they have the longest causal range
-    const int row_tile = gridDim.x - 1 - blockIdx.x;
-    const int kvh = blockIdx.y;
-    const int seq = blockIdx.z / p.splits, split = blockIdx.z - seq * p.splits;
-    int q0, chunk, len;
-    if (!prefill_seq(p, seq, q0, chunk, len)) {
-        if (threadIdx.x == 0 && row_tile == 0 && kvh == 0 && split == 0)
-            raise_flag(p.status, PKV_DEVERR_CONTEXT_LEN);
-        return;  // uniform over the CTA
-    }
-    const int rows = chunk * p.group;  // this sequence's query rows of one KV head
-    const int row0 = row_tile * 128;
-    if (row0 >= rows) return;
-    const int last_row = min(rows, row0 + 128) - 1;
-    const int base_pos = len - chunk;  // position of chunk token 0
-    const int pos_max = base_pos + last_row / p.group;
-    const int tok_lo = split * p.split_tokens;
-    const int tok_hi = min(min(len, pos_max + 1), tok_lo + p.split_tokens);
-    if (tok_hi <= tok_lo) return;  // no row of the tile reaches this split
-    const int ntiles = (tok_hi - tok_lo + TILE - 1) / TILE;
+    const int R = p.tile_rows;
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm =
         smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
-    constexpr int KS = L::kKS, VS = L::kVS, PB = L::kPB;
+    constexpr int KS = L::kKS, VS = L::kVS, PB = L::kPB, QB = L::kQB;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
     uint64_t *k_full = bars, *k_empty = k_full + KS, *v_full = k_empty + KS, *v_empty = v_full + VS;
-    uint64_t *s_full = v_empty + VS, *s_empty = s_full + 2, *p_full = s_full + 4, *o_done = s_full + 6;
+    uint64_t *q_full = v_empty + VS, *q_empty = q_full + QB;
+    uint64_t *s_full = q_empty + QB, *s_empty = s_full + 2, *p_full = s_full + 4, *o_done = s_full + 6;
     uint64_t *drain_bar = s_full + 8;      // QK^T issuer's drain on exit
     uint64_t *drain_pv = s_full + 9;       // PV issuer's drain on exit
     uint64_t *pair_bar = drain_pv + 1;     // [quarter][parity]
@@ -149,6 +191,10 @@ __global__ void __launch_bounds__(384, 1)
         for (int i = 0; i < VS; ++i) {
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < QB; ++i) {
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
@@ -166,22 +212,17 @@ __global__ void __launch_bounds__(384, 1)
         tc::tmem_alloc(tmem_slot, L::kTmemCols);
         tc::tmem_relinquish();
     }
-    // query rows of this tile -> Q panel (K-major, 128-byte swizzle); rows past the
-    // chunk are zero
-    for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
-        const int r = i >> 4, c8 = i & 15;
-        const int row = row0 + r;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < rows) {
-            const int j = row / p.group, g = row - j * p.group;
-            const T *src = static_cast<const T *>(p.q) +
-                           ((static_cast<int64_t>(q0) + j) * p.num_q_heads + kvh * p.group + g) * D;
-            v = *reinterpret_cast<const uint4 *>(src + c8 * 8);
+    // Q rows R .. 127 are never loaded (a row tile holds whole tokens): zero
+    // them once so the MMA reads finite values there
+    if (R < 128) {
+        for (int i = threadIdx.x; i < QB * 2 * (128 - R) * 8; i += blockDim.x) {
+            const int c16 = i & 7, rr = R + (i >> 3) % (128 - R), h = (i >> 3) / (128 - R);
+            *reinterpret_cast<uint4 *>(sm + L::kOffQ + h * L::kHalf + rr * 128 + c16 * 16) =
+                make_uint4(0, 0, 0, 0);
         }
-        *reinterpret_cast<uint4 *>(sm + L::kOffQ + (c8 >> 3) * L::kHalf + r * 128 +
-                                   (((c8 & 7) ^ (r & 7)) << 4)) = v;
     }
     if (warp == 0 && lane == 0) {
+        tc::prefetch_tensormap(&tmap_q);
         tc::prefetch_tensormap(&tmap_k);
         tc::prefetch_tensormap(&tmap_v);
     }
@@ -195,6 +236,8 @@ __global__ void __launch_bounds__(384, 1)
         // ===================== TMA producers: K (warp 0), V (warp 10) =====================
         // Separate producers so a K tile never waits behind a V slot that its PV still
         // holds; each reads the next tile's table entries while it waits for a slot.
+        // The K producer also loads each item's Q tile into Q buffer n % 2 once the
+        // QK^T of item n - 2 is done.
         const int kv = warp == 10;
         const int nst = kv ? VS : KS;
         uint64_t *full = kv ? v_full : k_full;
@@ -202,55 +245,88 @@ __global__ void __launch_bounds__(384, 1)
         const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
         unsigned char *ring = sm + (kv ? L::kOffV : L::kOffK);
         const uint64_t policy = l2_policy_evict_last();  // every row tile of the sequence reads it
-        const int32_t *trow = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq;
-        auto entry = [&](int j) -> int {  // this lane's block of tile j (-1: none or bad)
-            const int t0 = tok_lo + j * TILE;
-            const int nblk = (min(TILE, tok_hi - t0) + BS - 1) / BS;
-            int e = -1;
-            if (lane < nblk) {
-                e = trow[t0 / BS + lane];
-                if (e < 0 || e >= p.num_blocks) {
-                    if (kv == 0) raise_flag(p.status, PKV_DEVERR_BLOCK_TABLE);
-                    e = -1;
-                }
-            }
-            return e;
-        };
+        const uint64_t q_policy = l2_policy_evict_first();
         int last_issue[4] = {-1, -1, -1, -1};
-        static_assert(L::kKS <= 4 && L::kVS <= 4, "drain bookkeeping");
+        static_assert(L::kKS <= 4 && L::kVS <= 4 && L::kQB == 2, "drain bookkeeping");
+        int q_issue[2] = {-1, -1};
         bool ok = true;
-        int e_next = ntiles > 0 ? entry(0) : -1;
-        for (int j = 0; j < ntiles && ok; ++j) {
-            const int e = e_next;
-            if (j + 1 < ntiles) e_next = entry(j + 1);  // in flight while this tile waits
-            const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, e >= 0)) * BS * 256u;
-            const int s = j % nst;
-            int go = 1;
-            if (lane == 0) {
-                go = tc_wait(&empty[s], ((j / nst) & 1) ^ 1, abort_flag, p.status);
-                if (go) {
-                    if (bytes) mbar_arrive_expect_tx(&full[s], bytes);
-                    else mbar_arrive(&full[s]);
-                    last_issue[s] = j;
+        int jt = 0, n = 0;  // tiles and items so far
+        for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+            PrefillItem it;
+            if (!prefill_item(p, item, kv == 0, it)) continue;
+            const int32_t *trow = p.block_tables + static_cast<int64_t>(it.seq) * p.max_blocks_per_seq;
+            auto entry = [&](int j) -> int {  // this lane's block of tile j (-1: none or bad)
+                const int t0 = it.tok_lo + j * TILE;
+                const int nblk = (min(TILE, it.tok_hi - t0) + BS - 1) / BS;
+                int e = -1;
+                if (lane < nblk) {
+                    e = trow[t0 / BS + lane];
+                    if (e < 0 || e >= p.num_blocks) {
+                        if (kv == 0) raise_flag(p.status, PKV_DEVERR_BLOCK_TABLE);
+                        e = -1;
+                    }
+                }
+                return e;
+            };
+            int e_next = entry(0);
+            if (kv == 0) {
+                const int qb = n & 1;
+                int go = 1;
+                if (lane == 0) {
+                    go = tc_wait(&q_empty[qb], ((n >> 1) & 1) ^ 1, abort_flag, p.status);
+                    if (go) {
+                        // boxes of tile_tokens tokens x group heads x 64 columns; rows of
+                        // tokens past the query array arrive as zeros and count as bytes
+                        mbar_arrive_expect_tx(&q_full[qb], 256u * R);
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            tc::tma_load_3d(sm + L::kOffQ + qb * L::kPanel + c * L::kHalf, &tmap_q, c * 64,
+                                            it.kvh * p.group, it.q0 + it.row_tile * p.tile_tokens,
+                                            &q_full[qb], q_policy);
+                        q_issue[qb] = n;
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, go, 0)) {
+                    ok = false;
+                    break;
                 }
             }
-            if (!__shfl_sync(0xffffffffu, go, 0)) {
-                ok = false;
-                break;
-            }
-            if (e >= 0) {
-                unsigned char *slot = ring + s * L::kPanel;
+            for (int j = 0; j < it.ntiles; ++j, ++jt) {
+                const int e = e_next;
+                if (j + 1 < it.ntiles) e_next = entry(j + 1);  // in flight while this tile waits
+                const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, e >= 0)) * BS * 256u;
+                const int s = jt % nst;
+                int go = 1;
+                if (lane == 0) {
+                    go = tc_wait(&empty[s], ((jt / nst) & 1) ^ 1, abort_flag, p.status);
+                    if (go) {
+                        if (bytes) mbar_arrive_expect_tx(&full[s], bytes);
+                        else mbar_arrive(&full[s]);
+                        last_issue[s] = jt;
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, go, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (e >= 0) {
+                    unsigned char *slot = ring + s * L::kPanel;
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    tc::tma_load_3d(slot + c * L::kHalf + lane * BS * 128, map, c * 64, kvh * BS, e,
-                                    &full[s], policy);
+                    for (int c = 0; c < 2; ++c)
+                        tc::tma_load_3d(slot + c * L::kHalf + lane * BS * 128, map, c * 64, it.kvh * BS, e,
+                                        &full[s], policy);
+                }
+                __syncwarp();
             }
-            __syncwarp();
+            ++n;
         }
         if (!ok && lane == 0) {
+            // copies still in flight land before the CTA exits
             for (int s = 0; s < nst; ++s)
                 if (last_issue[s] >= 0)
                     mbar_wait_bounded(&full[s], (last_issue[s] / nst) & 1, kDrainTimeoutNs);
+            for (int b = 0; b < 2; ++b)
+                if (q_issue[b] >= 0) mbar_wait_bounded(&q_full[b], (q_issue[b] >> 1) & 1, kDrainTimeoutNs);
         }
     } else if (warp == 1) {
         // ===================== QK^T issuer =====================
@@ -258,27 +334,41 @@ __global__ void __launch_bounds__(384, 1)
         // issued by warp 11, so a ready PV never waits behind a QK^T batch (a batch
         // of MMAs holds its issuing thread for its whole execution).
         constexpr uint32_t idesc_qk = tc::idesc_f16_f32acc(kBF16, 128, 128, false, false);
-        for (int j = 0; j < ntiles; ++j) {
+        bool ok = true;
+        int jt = 0, n = 0;
+        for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+            PrefillItem it;
+            if (!prefill_item(p, item, false, it)) continue;
+            const int qb = n & 1;
             int go = 1;
-            if (lane == 0)
-                go = tc_wait(&k_full[j % KS], (j / KS) & 1, abort_flag, p.status) &&
-                     tc_wait(&s_empty[j & 1], ((j >> 1) & 1) ^ 1, abort_flag, p.status);
+            if (lane == 0) go = tc_wait(&q_full[qb], (n >> 1) & 1, abort_flag, p.status);
             if (!__shfl_sync(0xffffffffu, go, 0)) break;
-            if (lane == 0) {
-                const int b = j & 1;
-                tc::fence_after_sync();
-                const uint32_t qa = smem_base + L::kOffQ;
-                const uint32_t ka = smem_base + L::kOffK + (j % KS) * L::kPanel;
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint64_t a = tc::smem_desc_sw128(qa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
-                    const uint64_t bd = tc::smem_desc_sw128(ka + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
-                    tc::mma_f16_ss(tmem + 128 * b, a, bd, idesc_qk, k > 0);
+            for (int j = 0; j < it.ntiles; ++j, ++jt) {
+                if (lane == 0)
+                    go = tc_wait(&k_full[jt % KS], (jt / KS) & 1, abort_flag, p.status) &&
+                         tc_wait(&s_empty[jt & 1], ((jt >> 1) & 1) ^ 1, abort_flag, p.status);
+                if (!__shfl_sync(0xffffffffu, go, 0)) {
+                    ok = false;
+                    break;
                 }
-                tc::mma_commit(&s_full[b]);
-                tc::mma_commit(&k_empty[j % KS]);
+                if (lane == 0) {
+                    const int b = jt & 1;
+                    tc::fence_after_sync();
+                    const uint32_t qa = smem_base + L::kOffQ + qb * L::kPanel;
+                    const uint32_t ka = smem_base + L::kOffK + (jt % KS) * L::kPanel;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint64_t a = tc::smem_desc_sw128(qa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(ka + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                        tc::mma_f16_ss(tmem + 128 * b, a, bd, idesc_qk, k > 0);
+                    }
+                    tc::mma_commit(&s_full[b]);
+                    tc::mma_commit(&k_empty[jt % KS]);
+                    if (j + 1 == it.ntiles) tc::mma_commit(&q_empty[qb]);  // Q buffer free
+                }
+                __syncwarp();
             }
-            __syncwarp();
+            ++n;
         }
         if (lane == 0) {
             // this thread's MMAs complete before TMEM is released
@@ -289,27 +379,37 @@ __global__ void __launch_bounds__(384, 1)
     } else if (warp == 11) {
         // ===================== PV issuer =====================
         constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, 128, false, true);
-        for (int j = 0; j < ntiles; ++j) {
-            int go = 1;
-            if (lane == 0)
-                go = tc_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, p.status) &&
-                     tc_wait(&v_full[j % VS], (j / VS) & 1, abort_flag, p.status);
-            if (!__shfl_sync(0xffffffffu, go, 0)) break;
-            if (lane == 0) {
-                const int b = j & 1;
-                tc::fence_after_sync();
-                const uint32_t pa = smem_base + L::kOffP + (j % PB) * L::kPanel;
-                const uint32_t va = smem_base + L::kOffV + (j % VS) * L::kPanel;
-#pragma unroll
-                for (int k = 0; k < TILE / 16; ++k) {
-                    const uint64_t a = tc::smem_desc_sw128(pa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
-                    const uint64_t bd = tc::smem_desc_sw128(va + k * 2048, L::kHalf, 1024);
-                    tc::mma_f16_ss(tmem + 256, a, bd, idesc_pv, j > 0 || k > 0);
+        bool ok = true;
+        int jt = 0;
+        for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+            PrefillItem it;
+            if (!prefill_item(p, item, false, it)) continue;
+            for (int j = 0; j < it.ntiles; ++j, ++jt) {
+                int go = 1;
+                if (lane == 0)
+                    go = tc_wait(&p_full[jt & 1], (jt >> 1) & 1, abort_flag, p.status) &&
+                         tc_wait(&v_full[jt % VS], (jt / VS) & 1, abort_flag, p.status);
+                if (!__shfl_sync(0xffffffffu, go, 0)) {
+                    ok = false;
+                    break;
                 }
-                tc::mma_commit(&o_done[b]);
-                tc::mma_commit(&v_empty[j % VS]);
+                if (lane == 0) {
+                    const int b = jt & 1;
+                    tc::fence_after_sync();
+                    const uint32_t pa = smem_base + L::kOffP + (jt % PB) * L::kPanel;
+                    const uint32_t va = smem_base + L::kOffV + (jt % VS) * L::kPanel;
+#pragma unroll
+                    for (int k = 0; k < TILE / 16; ++k) {
+                        const uint64_t a = tc::smem_desc_sw128(pa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(va + k * 2048, L::kHalf, 1024);
+                        // the item's first tile starts O afresh
+                        tc::mma_f16_ss(tmem + 256, a, bd, idesc_pv, j > 0 || k > 0);
+                    }
+                    tc::mma_commit(&o_done[b]);
+                    tc::mma_commit(&v_empty[jt % VS]);
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
         if (lane == 0) {
             tc::mma_commit(drain_pv);
@@ -322,14 +422,10 @@ __global__ void __launch_bounds__(384, 1)
         const int half = warp >= 6 ? 1 : 0;  // tile columns 64*half .. +63
         const int c0 = half * 64;
         const int r = quarter * 32 + lane;   // row within the tile = TMEM lane
-        const int row = row0 + r;
-        const bool live = row < rows;
-        const int jtok = live ? row / p.group : 0;
-        const int pos = base_pos + jtok;     // this row sees tokens 0 .. pos
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const uint32_t xchg = lane_base + L::kXchgCol;
-        float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
+        int jt = 0, xs = 0;  // tiles and pair exchanges so far
         // One value per row between the two warps of the pair: step s writes column
         // 2 (s & 1) + half and reads the partner's; a warp reuses a column two steps
         // later, after the partner has passed the step in between.
@@ -347,168 +443,177 @@ __global__ void __launch_bounds__(384, 1)
             tc::tmem_ld_wait();
             return true;
         };
-        for (int j = 0; j < ntiles && ok; ++j) {
-            const int b = j & 1;
-            const int t0 = tok_lo + j * TILE;
-            const int valid = min(TILE, tok_hi - t0);                    // columns loaded
-            const int vr = live ? max(0, min(valid, pos + 1 - t0)) : 0;  // columns this row sees
-            const int vh = max(0, min(64, vr - c0));                     // ... in this half
-            if (!tc_wait_warp(&s_full[b], (j >> 1) & 1, abort_flag, p.status)) {
-                ok = false;
-                break;
-            }
-            tc::fence_after_sync();
-            // this row's 64 scores of the half, read from TMEM once
-            float x[64];
-#pragma unroll
-            for (int c = 0; c < 64; c += 16) tc::tmem_ld_x16(lane_base + 128 * b + c0 + c, x + c);
-            tc::tmem_ld_wait();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[b]);  // S[b] is in registers
-            // tiles every row of the warp sees completely skip the per-column masks
-            const bool full = __all_sync(0xffffffffu, vr == TILE);
-            // partial maximum of the visible scaled scores: the extreme raw score times
-            // the scale (the maximum for a positive scale, the minimum otherwise)
-            float pmax = -INFINITY;
-            if (vh > 0) {
-                const bool pos_scale = p.scale_log2 > 0.f;
-                float ext = x[0];
-                if (full) {
-#pragma unroll
-                    for (int i = 1; i + 1 < 64; i += 2)
-                        ext = pos_scale ? fmax3(ext, x[i], x[i + 1]) : fmin3(ext, x[i], x[i + 1]);
-                    ext = pos_scale ? fmaxf(ext, x[63]) : fminf(ext, x[63]);
-                } else {
-#pragma unroll
-                    for (int i = 1; i < 64; ++i)
-                        if (i < vh) ext = pos_scale ? fmaxf(ext, x[i]) : fminf(ext, x[i]);
-                }
-                pmax = ext * p.scale_log2;
-            }
-            float pmax_other;
-            if (!exchange(j, pmax, pmax_other)) {
-                ok = false;
-                break;
-            }
-            const float tmax = fmaxf(pmax, pmax_other);
-            // the reference maximum moves only by more than kRescaleLog2 (a row that sees
-            // nothing keeps -inf and alpha 1); both warps of the pair take the same
-            // decision for a row; TMEM loads and stores are warp-wide, so the warp
-            // rescales its half of O if any of its rows must
-            const float new_ref = tmax > m_ref + L::kRescaleLog2 ? tmax : m_ref;
-            const float alpha = new_ref == m_ref ? 1.f : fast_exp2(m_ref - new_ref);
-            if (__any_sync(0xffffffffu, new_ref != m_ref)) {
-                if (j > 0) {
-                    // O holds tiles < j: wait for PV(j-1), rescale this half of O in TMEM
-                    if (!tc_wait_warp(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after_sync();
-#pragma unroll
-                    for (int c = 0; c < 64; c += 16) {
-                        float o[16];
-                        tc::tmem_ld_x16(lane_base + 256 + c0 + c, o);
-                        tc::tmem_ld_wait();
-                        uint32_t w[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(o[i] * alpha);
-                        asm volatile(
-                            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, "
-                            "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(lane_base + 256 + c0 + c),
-                            "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-                            "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]),
-                            "r"(w[13]), "r"(w[14]), "r"(w[15])
-                            : "memory");
-                    }
-                    tc::tmem_st_wait();
-                }
-                l *= alpha;
-                m_ref = new_ref;
-            }
-            // P buffer j % PB was last read by PV(j - PB)
-            if (j >= PB && !tc_wait_warp(&o_done[(j - PB) & 1], ((j - PB) >> 1) & 1, abort_flag, p.status)) {
-                ok = false;
-                break;
-            }
-            // P = 2^(s - m_ref) on visible columns (0 elsewhere), rounded to T into this
-            // half of the K-major P panel; the row sum l adds the fp32 values
-            unsigned char *prow = sm + L::kOffP + (j % PB) * L::kPanel + half * L::kHalf + r * 128;
-            float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                uint32_t packed[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int t = c8 * 8 + 2 * i;
-                    float p0 = fast_exp2(fmaf(x[t], p.scale_log2, -m_ref));
-                    float p1 = fast_exp2(fmaf(x[t + 1], p.scale_log2, -m_ref));
-                    if (!full) {
-                        p0 = t < vh ? p0 : 0.f;
-                        p1 = t + 1 < vh ? p1 : 0.f;
-                    }
-                    add_f32x2(l0, l1, p0, p1);
-                    packed[i] = Elem<T>::pack2(p0, p1);
-                }
-                *reinterpret_cast<uint4 *>(prow + ((c8 ^ (r & 7)) << 4)) =
-                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            }
-            l += l0 + l1;
-            if (valid < TILE) {
-                // V rows past the loaded range: zero this half so 0 * stale never reaches
-                // the MMA
-                if (!tc_wait_warp(&v_full[j % VS], (j / VS) & 1, abort_flag, p.status)) {
+        for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+            PrefillItem it;
+            if (!prefill_item(p, item, false, it)) continue;
+            const int row = it.row0 + r;
+            const bool live = r < R && row < it.rows;
+            const int jtok = live ? row / p.group : 0;
+            const int pos = it.base_pos + jtok;  // this row sees tokens 0 .. pos
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < it.ntiles && ok; ++j, ++jt) {
+                const int b = jt & 1;
+                const int t0 = it.tok_lo + j * TILE;
+                const int valid = min(TILE, it.tok_hi - t0);                    // columns loaded
+                const int vr = live ? max(0, min(valid, pos + 1 - t0)) : 0;  // columns this row sees
+                const int vh = max(0, min(64, vr - c0));                     // ... in this half
+                if (!tc_wait_warp(&s_full[b], (jt >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
-                if (r >= valid) {
-                    uint4 *vrow = reinterpret_cast<uint4 *>(sm + L::kOffV + (j % VS) * L::kPanel + half * L::kHalf +
-                                                            r * 128);
+                tc::fence_after_sync();
+                // this row's 64 scores of the half, read from TMEM once
+                float x[64];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) vrow[i] = make_uint4(0, 0, 0, 0);
-                }
-            }
-            tc::fence_before_sync();   // the O rescale's TMEM stores precede PV(j)
-            fence_proxy_async_smem();  // P / zeroed V rows visible to the MMA
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[b]);
-        }
-        // the pair's row sum, then this half of the O row -> out (one split) or its
-        // partial slot.  TMEM loads are warp-wide: every lane loads, only live rows store.
-        float l_other = 0.f;
-        if (ok) ok = exchange(ntiles, l, l_other);
-        const float lt = l + l_other;
-        if (ok) ok = tc_wait_warp(&o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
-        if (ok) {
-            tc::fence_after_sync();
-            const int g = live ? row - jtok * p.group : 0;
-            const int64_t orow = (static_cast<int64_t>(q0) + jtok) * p.num_q_heads + kvh * p.group + g;
-            const bool direct = p.splits == 1;
-            const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-#pragma unroll
-            for (int c = 0; c < 64; c += 16) {
-                float o[16];
-                tc::tmem_ld_x16(lane_base + 256 + c0 + c, o);
+                for (int c = 0; c < 64; c += 16) tc::tmem_ld_x16(lane_base + 128 * b + c0 + c, x + c);
                 tc::tmem_ld_wait();
-                if (!live) continue;
-                if (direct) {
-                    uint32_t w[8];
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_empty[b]);  // S[b] is in registers
+                // tiles every row of the warp sees completely skip the per-column masks
+                const bool full = __all_sync(0xffffffffu, vr == TILE);
+                // partial maximum of the visible scaled scores: the extreme raw score times
+                // the scale (the maximum for a positive scale, the minimum otherwise)
+                float pmax = -INFINITY;
+                if (vh > 0) {
+                    const bool pos_scale = p.scale_log2 > 0.f;
+                    float ext = x[0];
+                    if (full) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) w[i] = Elem<T>::pack2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + orow * D + c0 + c);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                } else {
-                    float *dst = p.ws_o + (orow * p.splits + split) * D + c0 + c;
+                        for (int i = 1; i + 1 < 64; i += 2)
+                            ext = pos_scale ? fmax3(ext, x[i], x[i + 1]) : fmin3(ext, x[i], x[i + 1]);
+                        ext = pos_scale ? fmaxf(ext, x[63]) : fminf(ext, x[63]);
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 16; i += 4)
-                        *reinterpret_cast<float4 *>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+                        for (int i = 1; i < 64; ++i)
+                            if (i < vh) ext = pos_scale ? fmaxf(ext, x[i]) : fminf(ext, x[i]);
+                    }
+                    pmax = ext * p.scale_log2;
                 }
+                float pmax_other;
+                if (!exchange(xs++, pmax, pmax_other)) {
+                    ok = false;
+                    break;
+                }
+                const float tmax = fmaxf(pmax, pmax_other);
+                // the reference maximum moves only by more than kRescaleLog2 (a row that sees
+                // nothing keeps -inf and alpha 1); both warps of the pair take the same
+                // decision for a row; TMEM loads and stores are warp-wide, so the warp
+                // rescales its half of O if any of its rows must
+                const float new_ref = tmax > m_ref + L::kRescaleLog2 ? tmax : m_ref;
+                const float alpha = new_ref == m_ref ? 1.f : fast_exp2(m_ref - new_ref);
+                if (__any_sync(0xffffffffu, new_ref != m_ref)) {
+                    if (j > 0) {
+                        // O holds tiles < j: wait for PV(j-1), rescale this half of O in TMEM
+                        if (!tc_wait_warp(&o_done[(jt - 1) & 1], ((jt - 1) >> 1) & 1, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int c = 0; c < 64; c += 16) {
+                            float o[16];
+                            tc::tmem_ld_x16(lane_base + 256 + c0 + c, o);
+                            tc::tmem_ld_wait();
+                            uint32_t w[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(o[i] * alpha);
+                            asm volatile(
+                                "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, "
+                                "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(lane_base + 256 + c0 + c),
+                                "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                                "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]),
+                                "r"(w[13]), "r"(w[14]), "r"(w[15])
+                                : "memory");
+                        }
+                        tc::tmem_st_wait();
+                    }
+                    l *= alpha;
+                    m_ref = new_ref;
+                }
+                // P buffer jt % PB was last read by PV(jt - PB)
+                if (jt >= PB && !tc_wait_warp(&o_done[(jt - PB) & 1], ((jt - PB) >> 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                // P = 2^(s - m_ref) on visible columns (0 elsewhere), rounded to T into this
+                // half of the K-major P panel; the row sum l adds the fp32 values
+                unsigned char *prow = sm + L::kOffP + (jt % PB) * L::kPanel + half * L::kHalf + r * 128;
+                float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    uint32_t packed[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int t = c8 * 8 + 2 * i;
+                        float p0 = fast_exp2(fmaf(x[t], p.scale_log2, -m_ref));
+                        float p1 = fast_exp2(fmaf(x[t + 1], p.scale_log2, -m_ref));
+                        if (!full) {
+                            p0 = t < vh ? p0 : 0.f;
+                            p1 = t + 1 < vh ? p1 : 0.f;
+                        }
+                        add_f32x2(l0, l1, p0, p1);
+                        packed[i] = Elem<T>::pack2(p0, p1);
+                    }
+                    *reinterpret_cast<uint4 *>(prow + ((c8 ^ (r & 7)) << 4)) =
+                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                }
+                l += l0 + l1;
+                if (valid < TILE) {
+                    // V rows past the loaded range: zero this half so 0 * stale never reaches
+                    // the MMA
+                    if (!tc_wait_warp(&v_full[jt % VS], (jt / VS) & 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    if (r >= valid) {
+                        uint4 *vrow = reinterpret_cast<uint4 *>(sm + L::kOffV + (jt % VS) * L::kPanel + half * L::kHalf +
+                                                                r * 128);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) vrow[i] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                tc::fence_before_sync();   // the O rescale's TMEM stores precede PV(j)
+                fence_proxy_async_smem();  // P / zeroed V rows visible to the MMA
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[b]);
             }
-            if (live && !direct && half == 0) {
-                p.ws_m[orow * p.splits + split] = m_ref;
-                p.ws_l[orow * p.splits + split] = lt;
+            // the pair's row sum, then this half of the O row -> out (one split) or its
+            // partial slot.  TMEM loads are warp-wide: every lane loads, only live rows store.
+            float l_other = 0.f;
+            if (ok) ok = exchange(xs++, l, l_other);
+            const float lt = l + l_other;
+            if (ok) ok = tc_wait_warp(&o_done[(jt - 1) & 1], ((jt - 1) >> 1) & 1, abort_flag, p.status);
+            if (ok) {
+                tc::fence_after_sync();
+                const int g = live ? row - jtok * p.group : 0;
+                const int64_t orow = (static_cast<int64_t>(it.q0) + jtok) * p.num_q_heads + it.kvh * p.group + g;
+                const bool direct = p.splits == 1;
+                const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; c += 16) {
+                    float o[16];
+                    tc::tmem_ld_x16(lane_base + 256 + c0 + c, o);
+                    tc::tmem_ld_wait();
+                    if (!live) continue;
+                    if (direct) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) w[i] = Elem<T>::pack2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + orow * D + c0 + c);
+                        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    } else {
+                        float *dst = p.ws_o + (orow * p.splits + it.split) * D + c0 + c;
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4)
+                            *reinterpret_cast<float4 *>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+                    }
+                }
+                if (live && !direct && half == 0) {
+                    p.ws_m[orow * p.splits + it.split] = m_ref;
+                    p.ws_l[orow * p.splits + it.split] = lt;
+                }
             }
         }
     }
