@@ -41,7 +41,9 @@
 // 64-127.  A pair exchanges its partial row maxima each tile through two spare
 // TMEM columns (an mbarrier with a bounded wait orders them), so both warps
 // hold the same reference maximum; each rescales, writes P for and outputs
-// its own half.
+// its own half.  P goes back into TMEM over the scores it came from (16-bit
+// values packed two per column) and the PV MMA takes it from there, so P is
+// double-buffered with S and the softmax of tile j + 1 runs while PV(j) does.
 #pragma once
 
 #include "prefix_tc_kernel.cuh"
@@ -131,24 +133,23 @@ __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, bool
 }
 
 // Shared memory: two Q tiles (consecutive items), K and V rings of 128-token
-// tiles, P buffers, and the barriers (rings, Q / S / P / O double buffers, the
-// softmax pairs).
+// tiles, and the barriers (rings, Q / S / O double buffers, the softmax pairs).
+// P lives in TMEM.
 struct PrefillLayout {
     static constexpr int kTile = 128;
     static constexpr int kHalf = 128 * 128;           // 128 rows x 128 B
     static constexpr int kPanel = 2 * kHalf;          // 128 rows x 128 16-bit values
     static constexpr int kQB = 2;                     // Q buffers
-    static constexpr int kKS = 2, kVS = 2, kPB = 1;   // K slots, V slots, P buffers
+    static constexpr int kKS = 2, kVS = 2;            // K slots, V slots
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQB * kPanel;
     static constexpr int kOffV = kOffK + kKS * kPanel;
-    static constexpr int kOffP = kOffV + kVS * kPanel;
-    static constexpr int kOffBar = kOffP + kPB * kPanel;
+    static constexpr int kOffBar = kOffV + kVS * kPanel;
     static constexpr int kNumBars = 2 * kKS + 2 * kVS + 2 * kQB + 8 + 2 + 8;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kSmemBytes = kBytes + 1024;  // + alignment slack
-    static constexpr uint32_t kTmemCols = 512;        // S[2] at 0 / 128, O at 256, exchange 384
+    static constexpr uint32_t kTmemCols = 512;        // S[2] at 0 / 128 (P[b] over S[b]), O at 256, exchange 384
     static constexpr uint32_t kXchgCol = 384;         // spare TMEM columns for the pairs
     static constexpr float kRescaleLog2 = 8.f;
     static constexpr int kThreads = 384;
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(384, 1)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm =
         smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
-    constexpr int KS = L::kKS, VS = L::kVS, PB = L::kPB, QB = L::kQB;
+    constexpr int KS = L::kKS, VS = L::kVS, QB = L::kQB;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
     uint64_t *k_full = bars, *k_empty = k_full + KS, *v_full = k_empty + KS, *v_empty = v_full + VS;
     uint64_t *q_full = v_empty + VS, *q_empty = q_full + QB;
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 8);
+            mbar_init(&s_empty[i], 1);
             mbar_init(&p_full[i], 8);
             mbar_init(&o_done[i], 1);
         }
@@ -396,16 +397,16 @@ __global__ void __launch_bounds__(384, 1)
                 if (lane == 0) {
                     const int b = jt & 1;
                     tc::fence_after_sync();
-                    const uint32_t pa = smem_base + L::kOffP + (jt % PB) * L::kPanel;
                     const uint32_t va = smem_base + L::kOffV + (jt % VS) * L::kPanel;
 #pragma unroll
                     for (int k = 0; k < TILE / 16; ++k) {
-                        const uint64_t a = tc::smem_desc_sw128(pa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
                         const uint64_t bd = tc::smem_desc_sw128(va + k * 2048, L::kHalf, 1024);
-                        // the item's first tile starts O afresh
-                        tc::mma_f16_ss(tmem + 256, a, bd, idesc_pv, j > 0 || k > 0);
+                        // P from TMEM (16 tokens = 8 columns per step); the item's first
+                        // tile starts O afresh
+                        tc::mma_f16_ts(tmem + 256, tmem + 128 * b + 8 * k, bd, idesc_pv, j > 0 || k > 0);
                     }
                     tc::mma_commit(&o_done[b]);
+                    tc::mma_commit(&s_empty[b]);  // S[b] / P[b] free for QK^T(jt + 2)
                     tc::mma_commit(&v_empty[jt % VS]);
                 }
                 __syncwarp();
@@ -467,9 +468,6 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int c = 0; c < 64; c += 16) tc::tmem_ld_x16(lane_base + 128 * b + c0 + c, x + c);
                 tc::tmem_ld_wait();
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_empty[b]);  // S[b] is in registers
                 // tiles every row of the warp sees completely skip the per-column masks
                 const bool full = __all_sync(0xffffffffu, vr == TILE);
                 // partial maximum of the visible scaled scores: the extreme raw score times
@@ -531,21 +529,19 @@ __global__ void __launch_bounds__(384, 1)
                     l *= alpha;
                     m_ref = new_ref;
                 }
-                // P buffer jt % PB was last read by PV(jt - PB)
-                if (jt >= PB && !tc_wait_warp(&o_done[(jt - PB) & 1], ((jt - PB) >> 1) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                // P = 2^(s - m_ref) on visible columns (0 elsewhere), rounded to T into this
-                // half of the K-major P panel; the row sum l adds the fp32 values
-                unsigned char *prow = sm + L::kOffP + (jt % PB) * L::kPanel + half * L::kHalf + r * 128;
+                // P = 2^(s - m_ref) on visible columns (0 elsewhere), rounded to T and packed
+                // two per 32-bit column over the first 64 columns of S[b] (tokens 64 half ..
+                // +63 -> columns 32 half .. +31; both warps of the pair have read their
+                // scores, the exchange above orders it), where the PV MMA reads it; the row
+                // sum l adds the fp32 values
+                const uint32_t pcol = lane_base + 128 * b + 32 * half;
                 float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    uint32_t packed[4];
+                for (int c16 = 0; c16 < 2; ++c16) {
+                    uint32_t packed[16];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int t = c8 * 8 + 2 * i;
+                    for (int i = 0; i < 16; ++i) {
+                        const int t = c16 * 32 + 2 * i;
                         float p0 = fast_exp2(fmaf(x[t], p.scale_log2, -m_ref));
                         float p1 = fast_exp2(fmaf(x[t + 1], p.scale_log2, -m_ref));
                         if (!full) {
@@ -555,8 +551,7 @@ __global__ void __launch_bounds__(384, 1)
                         add_f32x2(l0, l1, p0, p1);
                         packed[i] = Elem<T>::pack2(p0, p1);
                     }
-                    *reinterpret_cast<uint4 *>(prow + ((c8 ^ (r & 7)) << 4)) =
-                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    tc::tmem_st_x16(pcol + 16 * c16, packed);
                 }
                 l += l0 + l1;
                 if (valid < TILE) {
@@ -573,8 +568,9 @@ __global__ void __launch_bounds__(384, 1)
                         for (int i = 0; i < 8; ++i) vrow[i] = make_uint4(0, 0, 0, 0);
                     }
                 }
-                tc::fence_before_sync();   // the O rescale's TMEM stores precede PV(j)
-                fence_proxy_async_smem();  // P / zeroed V rows visible to the MMA
+                tc::tmem_st_wait();
+                tc::fence_before_sync();   // P and the O rescale's TMEM stores precede PV(j)
+                fence_proxy_async_smem();  // zeroed V rows visible to the MMA
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[b]);
             }
