@@ -30,9 +30,11 @@
 // order with the heaviest row tiles (longest causal range) first, which
 // balances the SMs without a shared counter.  Every role walks the same item
 // list and counts tiles across items, so the rings and barriers run on from
-// one item to the next: the queries of the next item (a TMA load into the
-// second of two Q buffers) and its first K/V tiles and S = QK^T are in flight
-// while the softmax warps still write out the current item.
+// one item to the next: the queries of the next item (a TMA load into the Q
+// buffer as soon as the last QK^T of the current item has read it) and its
+// first K/V tiles and S = QK^T are in flight while the softmax warps still
+// write out the current item.  With one Q buffer the K and V rings hold three
+// tiles each (measured: faster than two Q buffers with two-slot rings).
 //
 // Warps: 0 / 10 TMA producers of the K / V rings (PrefillLayout::kKS / kVS
 // slots; warp 0 also loads each item's Q tile), 1 TMEM owner + QK^T issuer,
@@ -132,15 +134,16 @@ __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, bool
     return it.tok_hi > it.tok_lo;
 }
 
-// Shared memory: two Q tiles (consecutive items), K and V rings of 128-token
-// tiles, and the barriers (rings, Q / S / O double buffers, the softmax pairs).
+// Shared memory: the Q tile(s) of consecutive items, K and V rings of
+// 128-token tiles, and the barriers (rings, Q, S / O double buffers, the
+// softmax pairs).
 // P lives in TMEM.
 struct PrefillLayout {
     static constexpr int kTile = 128;
     static constexpr int kHalf = 128 * 128;           // 128 rows x 128 B
     static constexpr int kPanel = 2 * kHalf;          // 128 rows x 128 16-bit values
-    static constexpr int kQB = 2;                     // Q buffers
-    static constexpr int kKS = 2, kVS = 2;            // K slots, V slots
+    static constexpr int kQB = 1;                     // Q buffers
+    static constexpr int kKS = 3, kVS = 3;            // K slots, V slots
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQB * kPanel;
     static constexpr int kOffV = kOffK + kKS * kPanel;
@@ -237,8 +240,8 @@ __global__ void __launch_bounds__(384, 1)
         // ===================== TMA producers: K (warp 0), V (warp 10) =====================
         // Separate producers so a K tile never waits behind a V slot that its PV still
         // holds; each reads the next tile's table entries while it waits for a slot.
-        // The K producer also loads each item's Q tile into Q buffer n % 2 once the
-        // QK^T of item n - 2 is done.
+        // The K producer also loads each item's Q tile into Q buffer n % kQB once
+        // the QK^T of item n - kQB is done.
         const int kv = warp == 10;
         const int nst = kv ? VS : KS;
         uint64_t *full = kv ? v_full : k_full;
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint64_t policy = l2_policy_evict_last();  // every row tile of the sequence reads it
         const uint64_t q_policy = l2_policy_evict_first();
         int last_issue[4] = {-1, -1, -1, -1};
-        static_assert(L::kKS <= 4 && L::kVS <= 4 && L::kQB == 2, "drain bookkeeping");
+        static_assert(L::kKS <= 4 && L::kVS <= 4 && L::kQB <= 2, "drain bookkeeping");
         int q_issue[2] = {-1, -1};
         bool ok = true;
         int jt = 0, n = 0;  // tiles and items so far
@@ -271,10 +274,10 @@ __global__ void __launch_bounds__(384, 1)
             };
             int e_next = entry(0);
             if (kv == 0) {
-                const int qb = n & 1;
+                const int qb = n % QB;
                 int go = 1;
                 if (lane == 0) {
-                    go = tc_wait(&q_empty[qb], ((n >> 1) & 1) ^ 1, abort_flag, p.status);
+                    go = tc_wait(&q_empty[qb], ((n / QB) & 1) ^ 1, abort_flag, p.status);
                     if (go) {
                         // boxes of tile_tokens tokens x group heads x 64 columns; rows of
                         // tokens past the query array arrive as zeros and count as bytes
@@ -326,8 +329,8 @@ __global__ void __launch_bounds__(384, 1)
             for (int s = 0; s < nst; ++s)
                 if (last_issue[s] >= 0)
                     mbar_wait_bounded(&full[s], (last_issue[s] / nst) & 1, kDrainTimeoutNs);
-            for (int b = 0; b < 2; ++b)
-                if (q_issue[b] >= 0) mbar_wait_bounded(&q_full[b], (q_issue[b] >> 1) & 1, kDrainTimeoutNs);
+            for (int b = 0; b < QB; ++b)
+                if (q_issue[b] >= 0) mbar_wait_bounded(&q_full[b], (q_issue[b] / QB) & 1, kDrainTimeoutNs);
         }
     } else if (warp == 1) {
         // ===================== QK^T issuer =====================
@@ -340,9 +343,9 @@ __global__ void __launch_bounds__(384, 1)
         for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
             PrefillItem it;
             if (!prefill_item(p, item, false, it)) continue;
-            const int qb = n & 1;
+            const int qb = n % QB;
             int go = 1;
-            if (lane == 0) go = tc_wait(&q_full[qb], (n >> 1) & 1, abort_flag, p.status);
+            if (lane == 0) go = tc_wait(&q_full[qb], (n / QB) & 1, abort_flag, p.status);
             if (!__shfl_sync(0xffffffffu, go, 0)) break;
             for (int j = 0; j < it.ntiles; ++j, ++jt) {
                 if (lane == 0)
