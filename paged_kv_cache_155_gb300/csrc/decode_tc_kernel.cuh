@@ -16,7 +16,7 @@
 // type for the second MMA; l is summed from the same rounded values so
 // numerator and denominator use identical weights.
 //
-// Structure (one persistent CTA per SM, 6 warps):
+// Structure (one persistent CTA per SM, 8 warps):
 //   warps 0, 6  TMA producers of K and of V: per 128-token tile, one 3-D tiled
 //               bulk-tensor copy per (block, 64-column half), 128-byte swizzled,
 //               into separate rings of 32 KiB K slots and 32 KiB V slots (a K
