@@ -559,7 +559,12 @@ __global__ void __launch_bounds__(384, 1)
                 l += l0 + l1;
                 if (valid < TILE) {
                     // V rows past the loaded range: zero this half so 0 * stale never reaches
-                    // the MMA
+                    // the MMA.  The parity wait cannot alias an older phase of the slot: S(jt)
+                    // exists only once PV(jt - 2) has completed (two S buffers), so V(jt - 2),
+                    // the slot's previous tile when kVS == 2, has landed.  With more S buffers
+                    // than V slots the wait could pass on V(jt - kVS)'s phase and zero rows
+                    // that a pending PV still reads.
+                    static_assert(L::kVS >= 2, "V slots >= S buffers (2)");
                     if (!tc_wait_warp(&v_full[jt % VS], (jt / VS) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
