@@ -539,23 +539,28 @@ __global__ void __launch_bounds__(384, 1)
                 // sum l adds the fp32 values
                 const uint32_t pcol = lane_base + 128 * b + 32 * half;
                 float l0 = 0.f, l1 = 0.f;
+                // two copies of the loop, so fully visible tiles carry no per-column mask
+                auto weights = [&](auto masked) {
 #pragma unroll
-                for (int c16 = 0; c16 < 2; ++c16) {
-                    uint32_t packed[16];
+                    for (int c16 = 0; c16 < 2; ++c16) {
+                        uint32_t packed[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int t = c16 * 32 + 2 * i;
-                        float p0 = fast_exp2(fmaf(x[t], p.scale_log2, -m_ref));
-                        float p1 = fast_exp2(fmaf(x[t + 1], p.scale_log2, -m_ref));
-                        if (!full) {
-                            p0 = t < vh ? p0 : 0.f;
-                            p1 = t + 1 < vh ? p1 : 0.f;
+                        for (int i = 0; i < 16; ++i) {
+                            const int t = c16 * 32 + 2 * i;
+                            float p0 = fast_exp2(fmaf(x[t], p.scale_log2, -m_ref));
+                            float p1 = fast_exp2(fmaf(x[t + 1], p.scale_log2, -m_ref));
+                            if constexpr (decltype(masked)::value) {
+                                p0 = t < vh ? p0 : 0.f;
+                                p1 = t + 1 < vh ? p1 : 0.f;
+                            }
+                            add_f32x2(l0, l1, p0, p1);
+                            packed[i] = Elem<T>::pack2(p0, p1);
                         }
-                        add_f32x2(l0, l1, p0, p1);
-                        packed[i] = Elem<T>::pack2(p0, p1);
+                        tc::tmem_st_x16(pcol + 16 * c16, packed);
                     }
-                    tc::tmem_st_x16(pcol + 16 * c16, packed);
-                }
+                };
+                if (full) weights(std::false_type{});
+                else weights(std::true_type{});
                 l += l0 + l1;
                 if (valid < TILE) {
                     // V rows past the loaded range: zero this half so 0 * stale never reaches
