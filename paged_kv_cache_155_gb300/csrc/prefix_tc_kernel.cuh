@@ -343,24 +343,29 @@ __global__ void __launch_bounds__(224, 1)
             // P panel; the row sum l adds the fp32 values
             unsigned char *prow = sm + L::kOffP + b * L::kPanel + r * 128;
             float l0 = 0.f, l1 = 0.f;
+            // two copies of the loop, so full tiles carry no per-column mask
+            auto weights = [&](auto masked) {
 #pragma unroll
-            for (int c8 = 0; c8 < TILE / 8; ++c8) {
-                uint32_t packed[4];
+                for (int c8 = 0; c8 < TILE / 8; ++c8) {
+                    uint32_t packed[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int t = c8 * 8 + 2 * i;
-                    float p0 = fast_exp2(fmaf(x[t], p.scale_log2, -m_ref));
-                    float p1 = fast_exp2(fmaf(x[t + 1], p.scale_log2, -m_ref));
-                    if (!full) {
-                        p0 = t < valid ? p0 : 0.f;
-                        p1 = t + 1 < valid ? p1 : 0.f;
+                    for (int i = 0; i < 4; ++i) {
+                        const int t = c8 * 8 + 2 * i;
+                        float p0 = fast_exp2(fmaf(x[t], p.scale_log2, -m_ref));
+                        float p1 = fast_exp2(fmaf(x[t + 1], p.scale_log2, -m_ref));
+                        if constexpr (decltype(masked)::value) {
+                            p0 = t < valid ? p0 : 0.f;
+                            p1 = t + 1 < valid ? p1 : 0.f;
+                        }
+                        add_f32x2(l0, l1, p0, p1);
+                        packed[i] = Elem<T>::pack2(p0, p1);
                     }
-                    add_f32x2(l0, l1, p0, p1);
-                    packed[i] = Elem<T>::pack2(p0, p1);
+                    *reinterpret_cast<uint4 *>(prow + (c8 >> 3) * L::kHalf + (((c8 & 7) ^ (r & 7)) << 4)) =
+                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
                 }
-                *reinterpret_cast<uint4 *>(prow + (c8 >> 3) * L::kHalf + (((c8 & 7) ^ (r & 7)) << 4)) =
-                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            }
+            };
+            if (full) weights(std::false_type{});
+            else weights(std::true_type{});
             l += l0 + l1;
             tc::fence_before_sync();
             if (valid < TILE) {
