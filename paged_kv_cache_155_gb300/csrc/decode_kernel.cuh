@@ -288,10 +288,19 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                     load_lane<KT, VL>(ks + t * D + sub * VL, kf);
 #pragma unroll
                     for (int g = 0; g < GH; ++g) {
-                        float a = 0.f;
+                        if constexpr (kQuant) {
+                            // codes cost a permute and a subtraction each: pack the FMAs
+                            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-                        for (int e = 0; e < VL; ++e) a = fmaf(qf[g][e], kf[e], a);
-                        sc[it][g] = a;
+                            for (int e = 0; e < VL; e += 2)
+                                fma_f32x2(a0, a1, qf[g][e], qf[g][e + 1], kf[e], kf[e + 1]);
+                            sc[it][g] = a0 + a1;
+                        } else {
+                            float a = 0.f;
+#pragma unroll
+                            for (int e = 0; e < VL; ++e) a = fmaf(qf[g][e], kf[e], a);
+                            sc[it][g] = a;
+                        }
                     }
                 }
                 // full dot products: sum over the LPT lanes of each token row
@@ -341,9 +350,16 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                         float vf[VL];
                         load_lane<KT, VL>(vs + t * D + sub * VL, vf);
 #pragma unroll
-                        for (int g = 0; g < GH; ++g)
+                        for (int g = 0; g < GH; ++g) {
+                            if constexpr (kQuant) {
 #pragma unroll
-                            for (int e = 0; e < VL; ++e) acc[g][e] = fmaf(sc[it][g], vf[e], acc[g][e]);
+                                for (int e = 0; e < VL; e += 2)
+                                    fma_f32x2(acc[g][e], acc[g][e + 1], sc[it][g], sc[it][g], vf[e], vf[e + 1]);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < VL; ++e) acc[g][e] = fmaf(sc[it][g], vf[e], acc[g][e]);
+                            }
+                        }
                     }
                 }
             }

@@ -136,6 +136,18 @@ __device__ __forceinline__ float fmin3(float a, float b, float c) {
     return d;
 }
 
+// (d0, d1) = (a0, a1) * (b0, b1) + (d0, d1) as one packed fp32 FMA (sm_100 and later).
+__device__ __forceinline__ void fma_f32x2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rd, {%0, %1};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // (a0, a1) += (b0, b1) as one packed fp32 add (sm_100 and later).
 __device__ __forceinline__ void add_f32x2(float &a0, float &a1, float b0, float b1) {
     asm("{\n\t.reg .b64 ra, rb;\n\t"
@@ -207,10 +219,12 @@ struct Elem<int8_t> {
         const uint32_t w[2] = {u.x ^ 0x80808080u, u.y ^ 0x80808080u};
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            f[4 * i + 0] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7440u)) - 8388736.f;
-            f[4 * i + 1] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7441u)) - 8388736.f;
-            f[4 * i + 2] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7442u)) - 8388736.f;
-            f[4 * i + 3] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7443u)) - 8388736.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                f[4 * i + j] = __uint_as_float(__byte_perm(w[i], 0x4B000000u, 0x7440u + j));
+            // minus 2^23 + 128, two values per packed add (exact: integers below 2^24)
+            add_f32x2(f[4 * i], f[4 * i + 1], -8388736.f, -8388736.f);
+            add_f32x2(f[4 * i + 2], f[4 * i + 3], -8388736.f, -8388736.f);
         }
     }
 };
