@@ -351,8 +351,11 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int t = c8 * 8 + 2 * i;
-                        float p0 = fast_exp2(fmaf(x[t], p.scale_log2, -m_ref));
-                        float p1 = fast_exp2(fmaf(x[t + 1], p.scale_log2, -m_ref));
+                        // s * scale - m for two columns in one packed FMA
+                        float e0 = -m_ref, e1 = -m_ref;
+                        fma_f32x2(e0, e1, x[t], x[t + 1], p.scale_log2, p.scale_log2);
+                        float p0 = fast_exp2(e0);
+                        float p1 = fast_exp2(e1);
                         if constexpr (decltype(masked)::value) {
                             p0 = t < valid ? p0 : 0.f;
                             p1 = t + 1 < valid ? p1 : 0.f;
