@@ -30,11 +30,16 @@
 //  * The chunk-to-warp assignment and every merge are fixed by logical token
 //    position, so the output does not depend on the physical placement.
 //  * INT8 cache ("KV Cache从原理到实战" §5.2, per-channel scales): the storage
-//    type KT is int8_t and each lane reads 8 codes (8 bytes) per row, keeping
-//    the lane layout and registers of the 16-bit case.  The per-channel K
-//    scale is folded into the fp32 query once (s_t = sum_j (q_j k_scale_j)
-//    code_j) and the V scale multiplies each output channel once at the end,
-//    so the inner loop only widens codes to fp32.
+//    type KT is int8_t.  The per-channel K scale is folded into the query once
+//    (s_t = sum_j (q_j k_scale_j) code_j) and the V scale multiplies each output
+//    channel once at the end, so the inner loop reads only codes.  It runs on
+//    fp16 operands with fp32 sums: the folded query is rounded once to fp16
+//    after a per-head power-of-two scaling (its largest magnitude in [1/2, 1)),
+//    a byte permute turns two codes into the exact fp16 values code + 1152,
+//    and mixed-precision FMAs (fp16 x fp16 + fp32) accumulate.  The offset
+//    leaves known sums: a dot product starts from -1152 times the lane's query
+//    sum, and the output removes 1152 times the weight sum, whose terms are the
+//    weights rounded to fp16 exactly as they meet V.
 #pragma once
 
 #include "pkv_device.cuh"
@@ -101,6 +106,25 @@ __device__ __forceinline__ void load_lane(const KT *src, float *f) {
         const uint4 u = *reinterpret_cast<const uint4 *>(src);
         Elem<KT>::to_f32x8(make_uint2(u.x, u.y), f);
         Elem<KT>::to_f32x8(make_uint2(u.z, u.w), f + 8);
+    }
+}
+
+// One lane's VL consecutive INT8 codes of a row in shared memory -> VL / 2
+// words of two exact fp16 values code + kCodeOffset each (codes 2i and 2i + 1
+// in word i).
+template <int VL>
+__device__ __forceinline__ void load_codes_f16(const int8_t *src, uint32_t *h) {
+    if constexpr (VL == 8) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(src);
+        codes_to_f16x4_offset(u.x, h[0], h[1]);
+        codes_to_f16x4_offset(u.y, h[2], h[3]);
+    } else {
+        static_assert(VL == 16, "8 or 16 codes per lane");
+        const uint4 u = *reinterpret_cast<const uint4 *>(src);
+        codes_to_f16x4_offset(u.x, h[0], h[1]);
+        codes_to_f16x4_offset(u.y, h[2], h[3]);
+        codes_to_f16x4_offset(u.z, h[4], h[5]);
+        codes_to_f16x4_offset(u.w, h[6], h[7]);
     }
 }
 
@@ -246,6 +270,36 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
             }
         }
     }
+    // INT8 cache: the query goes to fp16 with one power-of-two exponent per head
+    // (its largest magnitude lands in [0.5, 1)), so each code pair meets it in two
+    // mixed-precision FMAs (fp16 operands, fp32 sums).  The codes enter as the
+    // exact fp16 values code + kCodeOffset; a dot product starts from minus the
+    // offset times this lane's query sum, and the value sums shed the offset
+    // times the weight sum at the end.
+    uint32_t qh[GH][VL / 2];
+    float qs[GH];  // 2^exponent: the scale of the fp16 query's dot products
+    float qo[GH];  // kCodeOffset * (sum of this lane's fp16 query values)
+    if constexpr (kQuant) {
+#pragma unroll
+        for (int g = 0; g < GH; ++g) {
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < VL; ++e) amax = fmaxf(amax, fabsf(qf[g][e]));
+#pragma unroll
+            for (int o = LPT / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const int qe = row_exponent(amax);
+            qs[g] = exp2_int(qe);
+            const float down = exp2_int(-qe);
+            float qsum = 0.f;
+#pragma unroll
+            for (int e = 0; e < VL; e += 2) {
+                const __half2 h = __floats2half2_rn(qf[g][e] * down, qf[g][e + 1] * down);
+                qh[g][e / 2] = *reinterpret_cast<const uint32_t *>(&h);
+                qsum += __low2float(h) + __high2float(h);
+            }
+            qo[g] = kCodeOffset * qsum;
+        }
+    }
     float acc[GH][VL];
     float m[GH], l[GH];
 #pragma unroll
@@ -284,18 +338,21 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
 #pragma unroll
                 for (int it = 0; it < IT_STEP; ++it) {
                     const int t = (it0 + it) * TPG + grp;
-                    float kf[VL];
-                    load_lane<KT, VL>(ks + t * D + sub * VL, kf);
+                    if constexpr (kQuant) {
+                        uint32_t kh[VL / 2];
+                        load_codes_f16<VL>(ks + t * D + sub * VL, kh);
 #pragma unroll
-                    for (int g = 0; g < GH; ++g) {
-                        if constexpr (kQuant) {
-                            // codes cost a permute and a subtraction each: pack the FMAs
-                            float a0 = 0.f, a1 = 0.f;
+                        for (int g = 0; g < GH; ++g) {
+                            float a0 = -qo[g], a1 = 0.f;
 #pragma unroll
-                            for (int e = 0; e < VL; e += 2)
-                                fma_f32x2(a0, a1, qf[g][e], qf[g][e + 1], kf[e], kf[e + 1]);
-                            sc[it][g] = a0 + a1;
-                        } else {
+                            for (int e = 0; e < VL / 2; ++e) fma_f16x2_f32(qh[g][e], kh[e], a0, a1);
+                            sc[it][g] = (a0 + a1) * qs[g];
+                        }
+                    } else {
+                        float kf[VL];
+                        load_lane<KT, VL>(ks + t * D + sub * VL, kf);
+#pragma unroll
+                        for (int g = 0; g < GH; ++g) {
                             float a = 0.f;
 #pragma unroll
                             for (int e = 0; e < VL; ++e) a = fmaf(qf[g][e], kf[e], a);
@@ -339,6 +396,8 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
 #pragma unroll
                     for (int it = 0; it < IT_STEP; ++it) {
                         sc[it][g] = fast_exp2(sc[it][g] - m[g]);  // masked rows -> 0
+                        // INT8: the weight meets V in fp16; the sum adds the rounded value
+                        if constexpr (kQuant) sc[it][g] = __half2float(__float2half_rn(sc[it][g]));
                         l[g] += sc[it][g];
                     }
                 }
@@ -347,15 +406,22 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                 for (int it = 0; it < IT_STEP; ++it) {
                     const int t = (it0 + it) * TPG + grp;
                     if (t < valid) {
-                        float vf[VL];
-                        load_lane<KT, VL>(vs + t * D + sub * VL, vf);
+                        if constexpr (kQuant) {
+                            uint32_t vh[VL / 2];
+                            load_codes_f16<VL>(vs + t * D + sub * VL, vh);
 #pragma unroll
-                        for (int g = 0; g < GH; ++g) {
-                            if constexpr (kQuant) {
+                            for (int g = 0; g < GH; ++g) {
+                                const __half2 w2 = __float2half2_rn(sc[it][g]);  // exact: rounded above
+                                const uint32_t w = *reinterpret_cast<const uint32_t *>(&w2);
 #pragma unroll
-                                for (int e = 0; e < VL; e += 2)
-                                    fma_f32x2(acc[g][e], acc[g][e + 1], sc[it][g], sc[it][g], vf[e], vf[e + 1]);
-                            } else {
+                                for (int e = 0; e < VL / 2; ++e)
+                                    fma_f16x2_f32(w, vh[e], acc[g][2 * e], acc[g][2 * e + 1]);
+                            }
+                        } else {
+                            float vf[VL];
+                            load_lane<KT, VL>(vs + t * D + sub * VL, vf);
+#pragma unroll
+                            for (int g = 0; g < GH; ++g) {
 #pragma unroll
                                 for (int e = 0; e < VL; ++e) acc[g][e] = fmaf(sc[it][g], vf[e], acc[g][e]);
                             }
@@ -430,7 +496,8 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
             lsum += wgt * src[g * (D + 4) + D + 1];
             osum += wgt * src[g * (D + 4) + j];
         }
-        if constexpr (kQuant) osum *= p.v_scale[kvh * D + j];  // V dequantisation
+        // V: the value sums carry kCodeOffset per unit of weight; then dequantise
+        if constexpr (kQuant) osum = (osum - kCodeOffset * lsum) * p.v_scale[kvh * D + j];
         const int hq = hq0 + g;
         const int64_t row = static_cast<int64_t>(seq) * p.num_q_heads + hq;
         if (single) {

@@ -66,33 +66,6 @@ struct TcI8Layout {
     static_assert(kSmemBytes <= 232448, "dynamic shared memory per block");
 };
 
-// Four INT8 codes (one word) -> four exact fp16 values (two words): each code,
-// biased by 128, goes into the low mantissa byte of 1024.0 (0x64xx) and
-// 1152.0 = 1024 + 128 is subtracted.
-__device__ __forceinline__ void codes_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    const uint32_t b = w ^ 0x80808080u;
-    const uint32_t a0 = __byte_perm(b, 0x64646464u, 0x4140u);
-    const uint32_t a1 = __byte_perm(b, 0x64646464u, 0x4342u);
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-    const __half2 r0 = __hsub2(*reinterpret_cast<const __half2 *>(&a0), bias);
-    const __half2 r1 = __hsub2(*reinterpret_cast<const __half2 *>(&a1), bias);
-    lo = *reinterpret_cast<const uint32_t *>(&r0);
-    hi = *reinterpret_cast<const uint32_t *>(&r1);
-}
-
-// Exponent e with |m| * 2^-e in [1/2, 1) for a finite m > 0 (e = 0 otherwise),
-// clamped so that 2^e and 2^-e are normal floats.
-__device__ __forceinline__ int row_exponent(float m) {
-    if (!(m > 0.f) || !(m < INFINITY)) return 0;
-    const int biased = static_cast<int>((__float_as_uint(m) >> 23) & 0xffu);
-    const int e = (biased == 0 ? 1 : biased) - 126;
-    return e < -125 ? -125 : (e > 126 ? 126 : e);
-}
-
-__device__ __forceinline__ float exp2_int(int e) {  // 2^e, e in [-126, 127]
-    return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-}
-
 template <typename T, int BS, int GH>
 __global__ void __launch_bounds__(352, 1) paged_decode_tc_i8_kernel(const DecodeParams p) {
     using L = TcI8Layout;

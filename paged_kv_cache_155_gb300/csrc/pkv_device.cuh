@@ -229,6 +229,57 @@ struct Elem<int8_t> {
     }
 };
 
+// Four INT8 codes (one word) -> four exact fp16 values (two words): each code,
+// biased by 128, goes into the low mantissa byte of 1024.0 (0x64xx) and
+// 1152.0 = 1024 + 128 is subtracted.
+__device__ __forceinline__ void codes_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t b = w ^ 0x80808080u;
+    const uint32_t a0 = __byte_perm(b, 0x64646464u, 0x4140u);
+    const uint32_t a1 = __byte_perm(b, 0x64646464u, 0x4342u);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    const __half2 r0 = __hsub2(*reinterpret_cast<const __half2 *>(&a0), bias);
+    const __half2 r1 = __hsub2(*reinterpret_cast<const __half2 *>(&a1), bias);
+    lo = *reinterpret_cast<const uint32_t *>(&r0);
+    hi = *reinterpret_cast<const uint32_t *>(&r1);
+}
+
+// Four INT8 codes (one word) -> four exact fp16 values code + 1152 (two words):
+// each code, biased by 128, goes into the low mantissa byte of 1024.0 (0x64xx).
+// Sums over these values remove the offset once, as kCodeOffset times the sum
+// of the other operand.
+constexpr float kCodeOffset = 1152.f;
+__device__ __forceinline__ void codes_to_f16x4_offset(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t b = w ^ 0x80808080u;
+    lo = __byte_perm(b, 0x64646464u, 0x4140u);
+    hi = __byte_perm(b, 0x64646464u, 0x4342u);
+}
+
+// Exponent e with |m| * 2^-e in [1/2, 1) for a finite m > 0 (e = 0 otherwise),
+// clamped so that 2^e and 2^-e are normal floats.
+__device__ __forceinline__ int row_exponent(float m) {
+    if (!(m > 0.f) || !(m < INFINITY)) return 0;
+    const int biased = static_cast<int>((__float_as_uint(m) >> 23) & 0xffu);
+    const int e = (biased == 0 ? 1 : biased) - 126;
+    return e < -125 ? -125 : (e > 126 ? 126 : e);
+}
+
+__device__ __forceinline__ float exp2_int(int e) {  // 2^e, e in [-126, 127]
+    return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+}
+
+// (d0, d1) += (a.lo * b.lo, a.hi * b.hi) for two fp16 pairs, fp32 accumulators:
+// mixed-precision FMAs (fp16 operands, fp32 addend and result, one rounding;
+// the product of two fp16 values is exact in fp32).
+__device__ __forceinline__ void fma_f16x2_f32(uint32_t a, uint32_t b, float &d0, float &d1) {
+    asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\t"
+        "mov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.f16 %1, ah, bh, %1;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "r"(a), "r"(b));
+}
+
 // Per-channel INT8 quantiser ("KV Cache从原理到实战" §5.2): x / s in IEEE single
 // precision (correctly rounded division), clamped to [-127, 127] -- a NaN
 // quotient clamps to -127, since fmaxf returns the non-NaN operand -- then
