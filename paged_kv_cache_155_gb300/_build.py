@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libpagedkv.so")
 
-SOURCES = ["api.cu", "cache_ops.cu", "decode.cu", "decode_f16.cu", "decode_bf16.cu", "decode_i8.cu", "decode_tc_i8.cu", "prefill.cu",
+SOURCES = ["api.cu", "cache_ops.cu", "decode.cu", "decode_f16.cu", "decode_bf16.cu", "decode_i8.cu", "prefill.cu",
            "decode_noalloc.cu", "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",

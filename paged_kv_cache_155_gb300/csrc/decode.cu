@@ -97,7 +97,7 @@ size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, int num_partit
 }
 
 // The launch plan of a decode call; allow_tc = false keeps it on the CUDA-core
-// kernel (the INT8 cache has no tensor-core kernel).
+// kernel (the INT8 cache's path: warp-level MMAs there for 4 or 8 heads per block).
 pkv_status plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                        int block_size, int max_context_len, int partition_size, int sm_count,
                        bool allow_tc, int *out_partition_size, int *out_num_partitions,
@@ -193,14 +193,14 @@ pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
     int part = 0, nparts = 0, gh = 0, merge = 0;
     // Validate the shape first (no CUDA call), then plan for the real SM count.
     pkv_status plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                  max_context_len, partition_size, 1, true, &part, &nparts,
+                                  max_context_len, partition_size, 1, !int8_kv, &part, &nparts,
                                   &gh, &merge);
     if (plan != PKV_OK) return plan;
     if (partition_size == 0) {
         const int sm = pkv::current_sm_count();
         if (sm <= 0) return PKV_ERR_CUDA;
         plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                           max_context_len, 0, sm, true, &part, &nparts, &gh, &merge);
+                           max_context_len, 0, sm, !int8_kv, &part, &nparts, &gh, &merge);
         if (plan != PKV_OK) return plan;
     }
     const size_t need = workspace_for(num_seqs, num_q_heads, head_dim, nparts);
@@ -210,7 +210,7 @@ pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
     if (!status) return PKV_ERR_CUDA;
 
     const int group = num_q_heads / num_kv_heads;
-    const bool tc = use_tensor_cores(head_dim, group, max_context_len);
+    const bool tc = !int8_kv && use_tensor_cores(head_dim, group, max_context_len);
     if (tc && num_blocks > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
     pkv::DecodeParams p{};
     p.q = q;
@@ -241,13 +241,6 @@ pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
 
     const int merge_rows = merge ? num_seqs * num_q_heads : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (tc && int8_kv) {
-        const int sm = pkv::current_sm_count();
-        if (sm <= 0) return PKV_ERR_CUDA;
-        const int64_t items = static_cast<int64_t>(num_seqs) * p.items_y * nparts;
-        const int grid = static_cast<int>(std::min<int64_t>(sm, items));
-        return pkv::launch_decode_tc_i8(p, dtype, block_size, gh, grid, merge_rows, s);
-    }
     if (tc) {
         CUtensorMap tk, tv;
         if (!pkv::encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads,
@@ -311,7 +304,7 @@ PKV_API size_t pkv_decode_int8_workspace_bytes(int num_seqs, int num_q_heads, in
                                                int head_dim, int block_size, int max_context_len,
                                                int partition_size) {
     return decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                  max_context_len, partition_size, true);
+                                  max_context_len, partition_size, false);
 }
 
 PKV_API pkv_status pkv_paged_attention_decode_int8(

@@ -40,6 +40,18 @@
 //    leaves known sums: a dot product starts from -1152 times the lane's query
 //    sum, and the output removes 1152 times the weight sum, whose terms are the
 //    weights rounded to fp16 exactly as they meet V.
+//  * INT8 cache with 4 or 8 query heads per block (grouped-query attention):
+//    the lane loops would spend GH FMAs per code, so both products run as
+//    warp-level MMAs (m16n8k16, fp16 operands, fp32 accumulators) on the same
+//    fp16 values.  Per 16-token step a warp computes S = q' (K + 1152)^T with
+//    the heads as rows (rows past GH are zero) and the tokens as columns: each
+//    lane widens its K codes in registers with one byte permute per pair and
+//    feeds them straight in as the B fragment.  The S accumulators of a row
+//    are the A fragment of P (V + 1152) after the softmax, with no exchange
+//    between lanes; V's B fragment pairs two tokens of one channel, built by a
+//    byte permute and one three-input logic op per pair.  Operands come from
+//    registers, so the widened codes never go back to shared memory, and each
+//    warp still streams its own ring with no hand-off to other warps.
 #pragma once
 
 #include "pkv_device.cuh"
@@ -157,6 +169,9 @@ struct DecodeGeom {
 template <typename T, typename KT, int D, int BS, int GH>
 __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams p) {
     constexpr bool kQuant = sizeof(KT) == 1;
+    // INT8 cache with 4 or 8 query heads per block: the products run as warp-level
+    // MMAs on fp16 copies of the codes (the per-lane loops would spend GH FMAs per code)
+    constexpr bool kMma = kQuant && GH >= 4;
     constexpr int VL = decode_lane_values<KT, GH>();  // values per lane vector
     using G = DecodeGeom<D, BS, sizeof(KT), VL>;
     constexpr int NW = G::kWarps, S = G::kStages, TILE = G::kTile, LPT = G::kLanesPerToken,
@@ -242,7 +257,7 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
     const int sub = lane % LPT;   // which VL dims
     const int grp = lane / LPT;   // which token row of a TPG-row step
     float qf[GH][VL];
-    {
+    if constexpr (!kMma) {
         const T *qb = static_cast<const T *>(p.q) +
                       (static_cast<int64_t>(seq) * p.num_q_heads + hq0) * D + sub * VL;
 #pragma unroll
@@ -279,7 +294,7 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
     uint32_t qh[GH][VL / 2];
     float qs[GH];  // 2^exponent: the scale of the fp16 query's dot products
     float qo[GH];  // kCodeOffset * (sum of this lane's fp16 query values)
-    if constexpr (kQuant) {
+    if constexpr (kQuant && !kMma) {
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
             float amax = 0.f;
@@ -299,6 +314,68 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
             }
             qo[g] = kCodeOffset * qsum;
         }
+    }
+    // Warp-MMA form: lane (mg, mt) = (lane / 4, lane % 4) holds row mg of the A
+    // fragments of S = q' (K + 1152)^T, row mg being query head mg of the block
+    // (rows >= GH, and rows 8..15, are zero).  K-chunk kc = 4 j + w pairs the
+    // channels 64 j + 16 t + 4 w + {0, 1} / {2, 3} of lane t with the MMA's k
+    // indices 2t, 2t+1 / 2t+8, 2t+9, so a lane reads its codes of a token row as
+    // whole 16-byte vectors and its query values are exactly those channels.
+    constexpr int KC = D / 16;                   // k-chunks of QK^T
+    constexpr int NT = D / 8;                    // n-tiles of PV (8 channels each)
+    constexpr int STEP = TILE < 16 ? TILE : 16;  // tokens per MMA step
+    const int mg = lane >> 2, mt = lane & 3;
+    uint32_t qa[KC][2];
+    float mqs = 1.f, mqb = 0.f;  // row mg's score scale 2^e and code-offset bias
+    if constexpr (kMma) {
+        float f[D / 4];
+#pragma unroll
+        for (int e = 0; e < D / 4; ++e) f[e] = 0.f;
+        if (mg < GH) {
+            const T *qrow = static_cast<const T *>(p.q) +
+                            (static_cast<int64_t>(seq) * p.num_q_heads + hq0 + mg) * D + 16 * mt;
+            const float *ksr = p.k_scale + kvh * D + 16 * mt;
+#pragma unroll
+            for (int j = 0; j < D / 64; ++j) {
+                Elem<T>::to_f32x8(*reinterpret_cast<const uint4 *>(qrow + 64 * j), f + 16 * j);
+                Elem<T>::to_f32x8(*reinterpret_cast<const uint4 *>(qrow + 64 * j + 8), f + 16 * j + 8);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const float4 a = reinterpret_cast<const float4 *>(ksr + 64 * j)[v];
+                    f[16 * j + 4 * v] *= a.x * p.scale_log2;
+                    f[16 * j + 4 * v + 1] *= a.y * p.scale_log2;
+                    f[16 * j + 4 * v + 2] *= a.z * p.scale_log2;
+                    f[16 * j + 4 * v + 3] *= a.w * p.scale_log2;
+                }
+            }
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < D / 4; ++e) amax = fmaxf(amax, fabsf(f[e]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int qe = row_exponent(amax);
+        const float down = exp2_int(-qe);
+        float qsum = 0.f;
+#pragma unroll
+        for (int kc = 0; kc < KC; ++kc) {
+            const int e = 4 * kc;  // f index of channel 64 (kc / 4) + 16 t + 4 (kc % 4)
+            const __half2 h0 = __floats2half2_rn(f[e] * down, f[e + 1] * down);
+            const __half2 h1 = __floats2half2_rn(f[e + 2] * down, f[e + 3] * down);
+            qa[kc][0] = *reinterpret_cast<const uint32_t *>(&h0);
+            qa[kc][1] = *reinterpret_cast<const uint32_t *>(&h1);
+            qsum += (__low2float(h0) + __high2float(h0)) + (__low2float(h1) + __high2float(h1));
+        }
+        qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+        qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+        mqs = exp2_int(qe);
+        mqb = mqs * (kCodeOffset * qsum);
+    }
+    float oacc[NT][4];  // O = P (V + 1152): row mg, channels of n-tile nt (d2, d3: rows 8..15)
+    float mrow = -INFINITY, lrow = 0.f;
+    if constexpr (kMma) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.f;
     }
     float acc[GH][VL];
     float m[GH], l[GH];
@@ -331,99 +408,202 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
         if (tbl[(c * TILE) / BS] >= 0) {
             const KT *ks = reinterpret_cast<const KT *>(my_stages + s * G::kStageBytes);
             const KT *vs = ks + TILE * D;
+            if constexpr (kMma) {
+                const int8_t *kt = reinterpret_cast<const int8_t *>(ks);
+                const int8_t *vt = reinterpret_cast<const int8_t *>(vs);
 #pragma unroll
-            for (int it0 = 0; it0 < ITERS; it0 += IT_STEP) {
-                // QK: partial dot products over this lane's 8 dims
-                float sc[IT_STEP][GH];
+                for (int tb = 0; tb < TILE; tb += STEP) {
+                    if (tb >= valid) break;  // warp-uniform: the step holds no context token
+                    // S for the step: n-tile h = tokens tb + 8 h + (0..7); B column mg of it
+                    // is token tb + 8 h + mg, read by lanes (mg, .) as 16-byte vectors
+                    float sacc[STEP / 8][4];
 #pragma unroll
-                for (int it = 0; it < IT_STEP; ++it) {
-                    const int t = (it0 + it) * TPG + grp;
-                    if constexpr (kQuant) {
-                        uint32_t kh[VL / 2];
-                        load_codes_f16<VL>(ks + t * D + sub * VL, kh);
+                    for (int h = 0; h < STEP / 8; ++h) {
+                        sacc[h][0] = sacc[h][1] = sacc[h][2] = sacc[h][3] = 0.f;
+                        const int8_t *krow = kt + (tb + 8 * h + mg) * D + 16 * mt;
 #pragma unroll
-                        for (int g = 0; g < GH; ++g) {
-                            float a0 = -qo[g], a1 = 0.f;
+                        for (int j = 0; j < D / 64; ++j) {
+                            const uint4 u = *reinterpret_cast<const uint4 *>(krow + 64 * j);
+                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                            for (int e = 0; e < VL / 2; ++e) fma_f16x2_f32(qh[g][e], kh[e], a0, a1);
-                            sc[it][g] = (a0 + a1) * qs[g];
-                        }
-                    } else {
-                        float kf[VL];
-                        load_lane<KT, VL>(ks + t * D + sub * VL, kf);
-#pragma unroll
-                        for (int g = 0; g < GH; ++g) {
-                            float a = 0.f;
-#pragma unroll
-                            for (int e = 0; e < VL; ++e) a = fmaf(qf[g][e], kf[e], a);
-                            sc[it][g] = a;
+                            for (int w = 0; w < 4; ++w) {
+                                uint32_t lo, hi;
+                                codes_to_f16x4_offset(w4[w], lo, hi);
+                                mma_16816_f16(sacc[h], qa[4 * j + w][0], 0u, qa[4 * j + w][1], 0u, lo, hi);
+                            }
                         }
                     }
-                }
-                // full dot products: sum over the LPT lanes of each token row
+                    // row mg's scores in log2 units (d0, d1: tokens 2 mt, 2 mt + 1 of the
+                    // n-tile); tokens past the context -> -inf
+                    float sc[STEP / 4];
 #pragma unroll
-                for (int it = 0; it < IT_STEP; ++it)
+                    for (int h = 0; h < STEP / 8; ++h)
 #pragma unroll
-                    for (int g = 0; g < GH; ++g)
+                        for (int e = 0; e < 2; ++e)
+                            sc[2 * h + e] = tb + 8 * h + 2 * mt + e < valid ? fmaf(sacc[h][e], mqs, -mqb)
+                                                                             : -INFINITY;
+                    float mx = sc[0];
 #pragma unroll
-                        for (int o = LPT / 2; o > 0; o >>= 1)
-                            sc[it][g] += __shfl_xor_sync(0xffffffffu, sc[it][g], o);
-                // mask rows past the end of the context
+                    for (int e = 1; e < STEP / 4; ++e) mx = fmaxf(mx, sc[e]);
+                    // over the row's four lanes: finite, as token tb is in the context
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const bool grow = mx > mrow;
+                    if (__any_sync(0xffffffffu, grow)) {
+                        const float alpha = grow ? fast_exp2(mrow - mx) : 1.f;  // 0 when mrow = -inf
+                        lrow *= alpha;
 #pragma unroll
-                for (int it = 0; it < IT_STEP; ++it) {
-                    const int t = (it0 + it) * TPG + grp;
-                    if (t >= valid) {
+                        for (int nt = 0; nt < NT; ++nt) {
+                            oacc[nt][0] *= alpha;
+                            oacc[nt][1] *= alpha;
+                        }
+                        if (grow) mrow = mx;
+                    }
+                    // the weights meet V rounded to fp16 (as the A fragment of P V, rows
+                    // and k indices those of S); the row sum adds the rounded values
+                    uint32_t pa[STEP / 8];
 #pragma unroll
-                        for (int g = 0; g < GH; ++g) sc[it][g] = -INFINITY;
+                    for (int h = 0; h < STEP / 8; ++h) {
+                        const __half2 w2 =
+                            __floats2half2_rn(fast_exp2(sc[2 * h] - mrow), fast_exp2(sc[2 * h + 1] - mrow));
+                        lrow += __low2float(w2) + __high2float(w2);
+                        pa[h] = *reinterpret_cast<const uint32_t *>(&w2);
+                    }
+                    // O += P (V + 1152): B column mg of n-tile nt is channel (D / 8) mg + nt;
+                    // lane (mg, mt) reads tokens tb + 2 mt, +1 (b0) and tb + 8 + 2 mt, +1 (b1)
+                    // at its D / 8 channels and pairs them per channel
+                    constexpr int VW = D / 32;  // 32-bit words of a lane's channels in a row
+                    uint32_t x[STEP / 4][VW];
+                    const int8_t *vrow = vt + (tb + 2 * mt) * D + (D / 8) * mg;
+#pragma unroll
+                    for (int r = 0; r < STEP / 4; ++r) {
+                        const int8_t *src = vrow + ((r >> 1) * 8 + (r & 1)) * D;
+                        if constexpr (VW == 4) {
+                            const uint4 u = *reinterpret_cast<const uint4 *>(src);
+                            x[r][0] = u.x;
+                            x[r][1] = u.y;
+                            x[r][2] = u.z;
+                            x[r][3] = u.w;
+                        } else {
+                            const uint2 u = *reinterpret_cast<const uint2 *>(src);
+                            x[r][0] = u.x;
+                            x[r][1] = u.y;
+                        }
+                    }
+#pragma unroll
+                    for (int w = 0; w < VW; ++w) {
+                        uint32_t b0[4], b1[4] = {0u, 0u, 0u, 0u};
+                        b0[0] = token_pair_f16_offset<0>(x[0][w], x[1][w]);
+                        b0[1] = token_pair_f16_offset<1>(x[0][w], x[1][w]);
+                        b0[2] = token_pair_f16_offset<2>(x[0][w], x[1][w]);
+                        b0[3] = token_pair_f16_offset<3>(x[0][w], x[1][w]);
+                        if constexpr (STEP == 16) {
+                            b1[0] = token_pair_f16_offset<0>(x[2][w], x[3][w]);
+                            b1[1] = token_pair_f16_offset<1>(x[2][w], x[3][w]);
+                            b1[2] = token_pair_f16_offset<2>(x[2][w], x[3][w]);
+                            b1[3] = token_pair_f16_offset<3>(x[2][w], x[3][w]);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            mma_16816_f16(oacc[4 * w + e], pa[0], 0u, STEP == 16 ? pa[STEP / 8 - 1] : 0u, 0u,
+                                          b0[e], b1[e]);
                     }
                 }
-                // online softmax update (P1 §7.2), m warp-uniform
-#pragma unroll
-                for (int g = 0; g < GH; ++g) {
-                    float mx = sc[0][g];
-#pragma unroll
-                    for (int it = 1; it < IT_STEP; ++it) mx = fmaxf(mx, sc[it][g]);
-#pragma unroll
-                    for (int o = LPT; o < 32; o <<= 1)
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                    if (mx > m[g]) {  // warp-uniform branch
-                        const float alpha = fast_exp2(m[g] - mx);  // 0 when m was -inf
-                        l[g] *= alpha;
-#pragma unroll
-                        for (int e = 0; e < VL; ++e) acc[g][e] *= alpha;
-                        m[g] = mx;
-                    }
-#pragma unroll
+            } else {
+    #pragma unroll
+                for (int it0 = 0; it0 < ITERS; it0 += IT_STEP) {
+                    // QK: partial dot products over this lane's 8 dims
+                    float sc[IT_STEP][GH];
+    #pragma unroll
                     for (int it = 0; it < IT_STEP; ++it) {
-                        sc[it][g] = fast_exp2(sc[it][g] - m[g]);  // masked rows -> 0
-                        // INT8: the weight meets V in fp16; the sum adds the rounded value
-                        if constexpr (kQuant) sc[it][g] = __half2float(__float2half_rn(sc[it][g]));
-                        l[g] += sc[it][g];
-                    }
-                }
-                // PV: lane-local, each lane owns 8 dims of every head
-#pragma unroll
-                for (int it = 0; it < IT_STEP; ++it) {
-                    const int t = (it0 + it) * TPG + grp;
-                    if (t < valid) {
+                        const int t = (it0 + it) * TPG + grp;
                         if constexpr (kQuant) {
-                            uint32_t vh[VL / 2];
-                            load_codes_f16<VL>(vs + t * D + sub * VL, vh);
-#pragma unroll
+                            uint32_t kh[VL / 2];
+                            load_codes_f16<VL>(ks + t * D + sub * VL, kh);
+    #pragma unroll
                             for (int g = 0; g < GH; ++g) {
-                                const __half2 w2 = __float2half2_rn(sc[it][g]);  // exact: rounded above
-                                const uint32_t w = *reinterpret_cast<const uint32_t *>(&w2);
-#pragma unroll
-                                for (int e = 0; e < VL / 2; ++e)
-                                    fma_f16x2_f32(w, vh[e], acc[g][2 * e], acc[g][2 * e + 1]);
+                                float a0 = -qo[g], a1 = 0.f;
+    #pragma unroll
+                                for (int e = 0; e < VL / 2; ++e) fma_f16x2_f32(qh[g][e], kh[e], a0, a1);
+                                sc[it][g] = (a0 + a1) * qs[g];
                             }
                         } else {
-                            float vf[VL];
-                            load_lane<KT, VL>(vs + t * D + sub * VL, vf);
-#pragma unroll
+                            float kf[VL];
+                            load_lane<KT, VL>(ks + t * D + sub * VL, kf);
+    #pragma unroll
                             for (int g = 0; g < GH; ++g) {
-#pragma unroll
-                                for (int e = 0; e < VL; ++e) acc[g][e] = fmaf(sc[it][g], vf[e], acc[g][e]);
+                                float a = 0.f;
+    #pragma unroll
+                                for (int e = 0; e < VL; ++e) a = fmaf(qf[g][e], kf[e], a);
+                                sc[it][g] = a;
+                            }
+                        }
+                    }
+                    // full dot products: sum over the LPT lanes of each token row
+    #pragma unroll
+                    for (int it = 0; it < IT_STEP; ++it)
+    #pragma unroll
+                        for (int g = 0; g < GH; ++g)
+    #pragma unroll
+                            for (int o = LPT / 2; o > 0; o >>= 1)
+                                sc[it][g] += __shfl_xor_sync(0xffffffffu, sc[it][g], o);
+                    // mask rows past the end of the context
+    #pragma unroll
+                    for (int it = 0; it < IT_STEP; ++it) {
+                        const int t = (it0 + it) * TPG + grp;
+                        if (t >= valid) {
+    #pragma unroll
+                            for (int g = 0; g < GH; ++g) sc[it][g] = -INFINITY;
+                        }
+                    }
+                    // online softmax update (P1 §7.2), m warp-uniform
+    #pragma unroll
+                    for (int g = 0; g < GH; ++g) {
+                        float mx = sc[0][g];
+    #pragma unroll
+                        for (int it = 1; it < IT_STEP; ++it) mx = fmaxf(mx, sc[it][g]);
+    #pragma unroll
+                        for (int o = LPT; o < 32; o <<= 1)
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                        if (mx > m[g]) {  // warp-uniform branch
+                            const float alpha = fast_exp2(m[g] - mx);  // 0 when m was -inf
+                            l[g] *= alpha;
+    #pragma unroll
+                            for (int e = 0; e < VL; ++e) acc[g][e] *= alpha;
+                            m[g] = mx;
+                        }
+    #pragma unroll
+                        for (int it = 0; it < IT_STEP; ++it) {
+                            sc[it][g] = fast_exp2(sc[it][g] - m[g]);  // masked rows -> 0
+                            // INT8: the weight meets V in fp16; the sum adds the rounded value
+                            if constexpr (kQuant) sc[it][g] = __half2float(__float2half_rn(sc[it][g]));
+                            l[g] += sc[it][g];
+                        }
+                    }
+                    // PV: lane-local, each lane owns 8 dims of every head
+    #pragma unroll
+                    for (int it = 0; it < IT_STEP; ++it) {
+                        const int t = (it0 + it) * TPG + grp;
+                        if (t < valid) {
+                            if constexpr (kQuant) {
+                                uint32_t vh[VL / 2];
+                                load_codes_f16<VL>(vs + t * D + sub * VL, vh);
+    #pragma unroll
+                                for (int g = 0; g < GH; ++g) {
+                                    const __half2 w2 = __float2half2_rn(sc[it][g]);  // exact: rounded above
+                                    const uint32_t w = *reinterpret_cast<const uint32_t *>(&w2);
+    #pragma unroll
+                                    for (int e = 0; e < VL / 2; ++e)
+                                        fma_f16x2_f32(w, vh[e], acc[g][2 * e], acc[g][2 * e + 1]);
+                                }
+                            } else {
+                                float vf[VL];
+                                load_lane<KT, VL>(vs + t * D + sub * VL, vf);
+    #pragma unroll
+                                for (int g = 0; g < GH; ++g) {
+    #pragma unroll
+                                    for (int e = 0; e < VL; ++e) acc[g][e] = fmaf(sc[it][g], vf[e], acc[g][e]);
+                                }
                             }
                         }
                     }
@@ -437,41 +617,67 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
         }
     }
 
-    // ---- merge the token groups of this warp (same m across the warp)
-#pragma unroll
-    for (int g = 0; g < GH; ++g) {
-#pragma unroll
-        for (int o = LPT; o < 32; o <<= 1) {
-            l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
-#pragma unroll
-            for (int e = 0; e < VL; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
+    // ---- merge the token groups of this warp (same m across the warp); in the
+    //      MMA form the row sums of a head's four lanes
+    if constexpr (kMma) {
+        lrow += __shfl_xor_sync(0xffffffffu, lrow, 1);
+        lrow += __shfl_xor_sync(0xffffffffu, lrow, 2);
+        if (aborted) {
+            mrow = -INFINITY;
+            lrow = 0.f;
         }
-    }
-    if (aborted) {
+    } else {
 #pragma unroll
         for (int g = 0; g < GH; ++g) {
-            m[g] = -INFINITY;
-            l[g] = 0.f;
+#pragma unroll
+            for (int o = LPT; o < 32; o <<= 1) {
+                l[g] += __shfl_xor_sync(0xffffffffu, l[g], o);
+#pragma unroll
+                for (int e = 0; e < VL; ++e) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
+            }
+        }
+        if (aborted) {
+#pragma unroll
+            for (int g = 0; g < GH; ++g) {
+                m[g] = -INFINITY;
+                l[g] = 0.f;
+            }
         }
     }
 
     // ---- merge the warps through shared memory (each warp reuses its own
     //      stage buffers: all of its copies have landed)
     float *mine = reinterpret_cast<float *>(my_stages);  // [GH][D + 2]
-    if (grp == 0) {
+    if constexpr (kMma) {
+        // d0 / d1 of n-tile nt: head mg, channels (D / 8) (2 mt) + nt / (D / 8) (2 mt + 1) + nt
+        if (mg < GH) {
+            float *row = mine + mg * (D + 4);
 #pragma unroll
-        for (int g = 0; g < GH; ++g) {
-            float4 *dst = reinterpret_cast<float4 *>(mine + g * (D + 4) + sub * VL);
-#pragma unroll
-            for (int v = 0; v < VL / 4; ++v)
-                dst[v] = make_float4(acc[g][4 * v], acc[g][4 * v + 1], acc[g][4 * v + 2], acc[g][4 * v + 3]);
+            for (int nt = 0; nt < NT; ++nt) {
+                row[(D / 8) * (2 * mt) + nt] = oacc[nt][0];
+                row[(D / 8) * (2 * mt + 1) + nt] = oacc[nt][1];
+            }
+            if (mt == 0) {
+                row[D] = mrow;
+                row[D + 1] = lrow;
+            }
         }
-    }
-    if (lane == 0) {
+    } else {
+        if (grp == 0) {
 #pragma unroll
-        for (int g = 0; g < GH; ++g) {
-            mine[g * (D + 4) + D] = m[g];
-            mine[g * (D + 4) + D + 1] = l[g];
+            for (int g = 0; g < GH; ++g) {
+                float4 *dst = reinterpret_cast<float4 *>(mine + g * (D + 4) + sub * VL);
+#pragma unroll
+                for (int v = 0; v < VL / 4; ++v)
+                    dst[v] = make_float4(acc[g][4 * v], acc[g][4 * v + 1], acc[g][4 * v + 2], acc[g][4 * v + 3]);
+            }
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < GH; ++g) {
+                mine[g * (D + 4) + D] = m[g];
+                mine[g * (D + 4) + D + 1] = l[g];
+            }
         }
     }
     __syncthreads();

@@ -146,9 +146,6 @@ pkv_status launch_decode_i8_f16(const DecodeParams &p, int head_dim, int block_s
                                 dim3 grid, int merge_rows, cudaStream_t s);
 pkv_status launch_decode_i8_bf16(const DecodeParams &p, int head_dim, int block_size, int gh,
                                  dim3 grid, int merge_rows, cudaStream_t s);
-// Defined in decode_tc_i8.cu: the INT8-cache tensor-core kernel (+ merge).
-pkv_status launch_decode_tc_i8(const DecodeParams &p, pkv_dtype dtype, int block_size, int gh,
-                               int grid, int merge_rows, cudaStream_t s);
 pkv_status launch_decode_bf16(const DecodeParams &p, int head_dim, int block_size, int gh,
                               dim3 grid, int merge_rows, cudaStream_t s);
 pkv_status launch_decode_tc_f16(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,

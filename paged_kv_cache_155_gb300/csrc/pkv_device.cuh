@@ -229,20 +229,6 @@ struct Elem<int8_t> {
     }
 };
 
-// Four INT8 codes (one word) -> four exact fp16 values (two words): each code,
-// biased by 128, goes into the low mantissa byte of 1024.0 (0x64xx) and
-// 1152.0 = 1024 + 128 is subtracted.
-__device__ __forceinline__ void codes_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    const uint32_t b = w ^ 0x80808080u;
-    const uint32_t a0 = __byte_perm(b, 0x64646464u, 0x4140u);
-    const uint32_t a1 = __byte_perm(b, 0x64646464u, 0x4342u);
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-    const __half2 r0 = __hsub2(*reinterpret_cast<const __half2 *>(&a0), bias);
-    const __half2 r1 = __hsub2(*reinterpret_cast<const __half2 *>(&a1), bias);
-    lo = *reinterpret_cast<const uint32_t *>(&r0);
-    hi = *reinterpret_cast<const uint32_t *>(&r1);
-}
-
 // Four INT8 codes (one word) -> four exact fp16 values code + 1152 (two words):
 // each code, biased by 128, goes into the low mantissa byte of 1024.0 (0x64xx).
 // Sums over these values remove the offset once, as kCodeOffset times the sum
@@ -252,6 +238,32 @@ __device__ __forceinline__ void codes_to_f16x4_offset(uint32_t w, uint32_t &lo, 
     const uint32_t b = w ^ 0x80808080u;
     lo = __byte_perm(b, 0x64646464u, 0x4140u);
     hi = __byte_perm(b, 0x64646464u, 0x4342u);
+}
+
+// Byte E of x and byte E of y (two INT8 codes of one channel in two token rows)
+// -> the exact fp16 pair (x_E + 1152, y_E + 1152): a byte permute puts the two
+// codes in the low bytes of the two halves, and one three-input logic op flips
+// their sign bits (code + 128) and sets both high bytes to 0x64.
+template <int E>
+__device__ __forceinline__ uint32_t token_pair_f16_offset(uint32_t x, uint32_t y) {
+    constexpr uint32_t sel = E | (E << 4) | ((E + 4) << 8) | ((E + 4) << 12);
+    const uint32_t r = __byte_perm(x, y, sel);
+    uint32_t out;
+    // bits of 0x647F647F pass r, bits of 0x64806480 invert it, both set -> 1
+    asm("lop3.b32 %0, %1, %2, %3, 0xCA;" : "=r"(out) : "r"(r), "r"(0x647F647Fu), "r"(0x64806480u));
+    return out;
+}
+
+// Warp-level MMA m16n8k16, fp16 operands, fp32 accumulators (d += a b):
+// a0 / a2 = row g, k 2t..2t+1 / 2t+8..2t+9; a1 / a3 the same for row g + 8;
+// b0 / b1 = k 2t..2t+1 / 2t+8..2t+9 of column g; d0, d1 = row g, columns
+// 2t, 2t+1; d2, d3 = row g + 8 (g = lane / 4, t = lane % 4).
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Exponent e with |m| * 2^-e in [1/2, 1) for a finite m > 0 (e = 0 otherwise),

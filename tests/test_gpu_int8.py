@@ -226,8 +226,8 @@ def test_int8_named_workload_full_size(name):
 
 
 @pytest.mark.parametrize("qmag", [3e4, 1e-6], ids=["large", "tiny"])
-def test_int8_tensor_core_query_range(qmag):
-    """GQA over an INT8 pool runs on the tensor cores with the query folded into fp16
+def test_int8_grouped_query_range(qmag):
+    """GQA over an INT8 pool runs as warp-level fp16 MMAs with the query folded into fp16
     (q * k_scale * 2^-e per head row): queries whose q * k_scale exceeds the fp16 range,
     or sits in its subnormals, still match the oracle (scale chosen to keep scores O(1))."""
     dev = device()
