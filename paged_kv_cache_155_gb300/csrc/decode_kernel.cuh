@@ -416,10 +416,12 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                     if (tb >= valid) break;  // warp-uniform: the step holds no context token
                     // S for the step: n-tile h = tokens tb + 8 h + (0..7); B column mg of it
                     // is token tb + 8 h + mg, read by lanes (mg, .) as 16-byte vectors
-                    float sacc[STEP / 8][4];
+                    // two accumulators per n-tile (even / odd k-chunks) halve the MMA chains
+                    float sacc[STEP / 8][4], sodd[STEP / 8][4];
 #pragma unroll
                     for (int h = 0; h < STEP / 8; ++h) {
                         sacc[h][0] = sacc[h][1] = sacc[h][2] = sacc[h][3] = 0.f;
+                        sodd[h][0] = sodd[h][1] = sodd[h][2] = sodd[h][3] = 0.f;
                         const int8_t *krow = kt + (tb + 8 * h + mg) * D + 16 * mt;
 #pragma unroll
                         for (int j = 0; j < D / 64; ++j) {
@@ -429,9 +431,12 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                             for (int w = 0; w < 4; ++w) {
                                 uint32_t lo, hi;
                                 codes_to_f16x4_offset(w4[w], lo, hi);
-                                mma_16816_f16(sacc[h], qa[4 * j + w][0], 0u, qa[4 * j + w][1], 0u, lo, hi);
+                                mma_16816_f16(w & 1 ? sodd[h] : sacc[h], qa[4 * j + w][0], 0u, qa[4 * j + w][1], 0u,
+                                              lo, hi);
                             }
                         }
+                        sacc[h][0] += sodd[h][0];
+                        sacc[h][1] += sodd[h][1];
                     }
                     // row mg's scores in log2 units (d0, d1: tokens 2 mt, 2 mt + 1 of the
                     // n-tile); tokens past the context -> -inf
@@ -510,69 +515,69 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                     }
                 }
             } else {
-    #pragma unroll
+#pragma unroll
                 for (int it0 = 0; it0 < ITERS; it0 += IT_STEP) {
                     // QK: partial dot products over this lane's 8 dims
                     float sc[IT_STEP][GH];
-    #pragma unroll
+#pragma unroll
                     for (int it = 0; it < IT_STEP; ++it) {
                         const int t = (it0 + it) * TPG + grp;
                         if constexpr (kQuant) {
                             uint32_t kh[VL / 2];
                             load_codes_f16<VL>(ks + t * D + sub * VL, kh);
-    #pragma unroll
+#pragma unroll
                             for (int g = 0; g < GH; ++g) {
                                 float a0 = -qo[g], a1 = 0.f;
-    #pragma unroll
+#pragma unroll
                                 for (int e = 0; e < VL / 2; ++e) fma_f16x2_f32(qh[g][e], kh[e], a0, a1);
                                 sc[it][g] = (a0 + a1) * qs[g];
                             }
                         } else {
                             float kf[VL];
                             load_lane<KT, VL>(ks + t * D + sub * VL, kf);
-    #pragma unroll
+#pragma unroll
                             for (int g = 0; g < GH; ++g) {
                                 float a = 0.f;
-    #pragma unroll
+#pragma unroll
                                 for (int e = 0; e < VL; ++e) a = fmaf(qf[g][e], kf[e], a);
                                 sc[it][g] = a;
                             }
                         }
                     }
                     // full dot products: sum over the LPT lanes of each token row
-    #pragma unroll
+#pragma unroll
                     for (int it = 0; it < IT_STEP; ++it)
-    #pragma unroll
+#pragma unroll
                         for (int g = 0; g < GH; ++g)
-    #pragma unroll
+#pragma unroll
                             for (int o = LPT / 2; o > 0; o >>= 1)
                                 sc[it][g] += __shfl_xor_sync(0xffffffffu, sc[it][g], o);
                     // mask rows past the end of the context
-    #pragma unroll
+#pragma unroll
                     for (int it = 0; it < IT_STEP; ++it) {
                         const int t = (it0 + it) * TPG + grp;
                         if (t >= valid) {
-    #pragma unroll
+#pragma unroll
                             for (int g = 0; g < GH; ++g) sc[it][g] = -INFINITY;
                         }
                     }
                     // online softmax update (P1 §7.2), m warp-uniform
-    #pragma unroll
+#pragma unroll
                     for (int g = 0; g < GH; ++g) {
                         float mx = sc[0][g];
-    #pragma unroll
+#pragma unroll
                         for (int it = 1; it < IT_STEP; ++it) mx = fmaxf(mx, sc[it][g]);
-    #pragma unroll
+#pragma unroll
                         for (int o = LPT; o < 32; o <<= 1)
                             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                         if (mx > m[g]) {  // warp-uniform branch
                             const float alpha = fast_exp2(m[g] - mx);  // 0 when m was -inf
                             l[g] *= alpha;
-    #pragma unroll
+#pragma unroll
                             for (int e = 0; e < VL; ++e) acc[g][e] *= alpha;
                             m[g] = mx;
                         }
-    #pragma unroll
+#pragma unroll
                         for (int it = 0; it < IT_STEP; ++it) {
                             sc[it][g] = fast_exp2(sc[it][g] - m[g]);  // masked rows -> 0
                             // INT8: the weight meets V in fp16; the sum adds the rounded value
@@ -581,27 +586,27 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                         }
                     }
                     // PV: lane-local, each lane owns 8 dims of every head
-    #pragma unroll
+#pragma unroll
                     for (int it = 0; it < IT_STEP; ++it) {
                         const int t = (it0 + it) * TPG + grp;
                         if (t < valid) {
                             if constexpr (kQuant) {
                                 uint32_t vh[VL / 2];
                                 load_codes_f16<VL>(vs + t * D + sub * VL, vh);
-    #pragma unroll
+#pragma unroll
                                 for (int g = 0; g < GH; ++g) {
                                     const __half2 w2 = __float2half2_rn(sc[it][g]);  // exact: rounded above
                                     const uint32_t w = *reinterpret_cast<const uint32_t *>(&w2);
-    #pragma unroll
+#pragma unroll
                                     for (int e = 0; e < VL / 2; ++e)
                                         fma_f16x2_f32(w, vh[e], acc[g][2 * e], acc[g][2 * e + 1]);
                                 }
                             } else {
                                 float vf[VL];
                                 load_lane<KT, VL>(vs + t * D + sub * VL, vf);
-    #pragma unroll
+#pragma unroll
                                 for (int g = 0; g < GH; ++g) {
-    #pragma unroll
+#pragma unroll
                                     for (int e = 0; e < VL; ++e) acc[g][e] = fmaf(sc[it][g], vf[e], acc[g][e]);
                                 }
                             }
