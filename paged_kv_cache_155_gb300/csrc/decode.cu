@@ -68,21 +68,8 @@ namespace {
 constexpr int kResidentCtasPerSm = 2;  // decode CTAs resident per SM (shared-memory bound)
 constexpr int kTargetWaves = 8;        // CTA waves the automatic split aims for
 constexpr int kMinAutoPartition = 256; // tokens: below this the per-CTA set-up dominates
-constexpr int kTcItemsPerSm = 24;      // tensor-core path: work items per persistent CTA
-
-constexpr int kTcMinContext = 2048;    // tensor-core path from this longest context on
-
-// head_dim 128 with 4, 8 or 16 query heads per KV head: the group turns QK^T
-// and PV into dense tiles and runs on the tensor cores -- when contexts are
-// long.  Measured on GB300 (32 q / 8 kv heads, block 16): for contexts of at
-// most ~1K tokens the non-persistent CUDA-core kernel is faster (each short
-// work item exposes the copy latency of the persistent pipeline), around 1-2K
-// the two tie, from 2K on the tensor-core kernel is faster.
-bool use_tensor_cores(int head_dim, int group, int longest_span) {
-    return head_dim == 128 && (group == 4 || group == 8 || group == 16) &&
-           longest_span >= kTcMinContext;
-}
-
+// Query heads per CTA: the largest of 8, 4, 2, 1 dividing the group (4 or 8
+// run the products as warp-level MMAs, 1 or 2 as per-lane loops).
 int heads_per_block_for(int group) {
     if (group % 8 == 0) return 8;
     if (group % 4 == 0) return 4;
@@ -96,11 +83,10 @@ size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, int num_partit
     return rows * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
 }
 
-// The launch plan of a decode call; allow_tc = false keeps it on the CUDA-core
-// kernel (the INT8 cache's path: warp-level MMAs there for 4 or 8 heads per block).
+// The launch plan of a decode call (16-bit and INT8 caches alike).
 pkv_status plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                        int block_size, int max_context_len, int partition_size, int sm_count,
-                       bool allow_tc, int *out_partition_size, int *out_num_partitions,
+                       int *out_partition_size, int *out_num_partitions,
                        int *out_heads_per_block, int *out_needs_merge) {
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
@@ -112,24 +98,12 @@ pkv_status plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
     const int max_partition = pkv::DecodeGeom<128, 16>::kMaxTableEntries * block_size;
     if (partition_size > max_partition) return PKV_ERR_INVALID_ARG;
     const int group = num_q_heads / num_kv_heads;
-    const bool tc = allow_tc && use_tensor_cores(head_dim, group, max_context_len);
-    const int gh = tc ? group : heads_per_block_for(group);
+    const int gh = heads_per_block_for(group);
     const int64_t grid_y = static_cast<int64_t>(num_kv_heads) * (group / gh);
     if (grid_y > 65535 || num_seqs > 65535) return PKV_ERR_INVALID_ARG;
 
     int part = partition_size;
-    if (part == 0 && tc) {
-        // Persistent CTAs take work items round-robin: enough items per SM to
-        // balance uneven lengths, whole 128-token tiles per partition.
-        const int64_t units = std::max<int64_t>(1, static_cast<int64_t>(num_seqs) * grid_y);
-        const int64_t target = static_cast<int64_t>(sm_count) * kTcItemsPerSm;
-        const int64_t want = std::max<int64_t>(1, (target + units - 1) / units);
-        int64_t p = (static_cast<int64_t>(max_context_len) + want - 1) / want;
-        p = std::max<int64_t>(p, kMinAutoPartition);
-        p = (p + 127) / 128 * 128;
-        p = (p + block_size - 1) / block_size * block_size;
-        part = static_cast<int>(std::min<int64_t>(p, max_partition));
-    } else if (part == 0) {
+    if (part == 0) {
         // Enough CTAs for several waves over every SM, but partitions no
         // shorter than kMinAutoPartition tokens.
         const int64_t units = std::max<int64_t>(1, static_cast<int64_t>(num_seqs) * grid_y);
@@ -149,13 +123,12 @@ pkv_status plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
 }
 
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                              int block_size, int max_context_len, int partition_size,
-                              bool allow_tc) {
+                              int block_size, int max_context_len, int partition_size) {
     const int sm = partition_size > 0 ? 1 : pkv::current_sm_count();
     if (sm <= 0) return static_cast<size_t>(-1);
     int part = 0, nparts = 0, gh = 0, merge = 0;
     if (plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
-                    partition_size, sm, allow_tc, &part, &nparts, &gh, &merge) != PKV_OK)
+                    partition_size, sm, &part, &nparts, &gh, &merge) != PKV_OK)
         return static_cast<size_t>(-1);
     return workspace_for(num_seqs, num_q_heads, head_dim, nparts);
 }
@@ -193,14 +166,14 @@ pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
     int part = 0, nparts = 0, gh = 0, merge = 0;
     // Validate the shape first (no CUDA call), then plan for the real SM count.
     pkv_status plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                  max_context_len, partition_size, 1, !int8_kv, &part, &nparts,
-                                  &gh, &merge);
+                                  max_context_len, partition_size, 1, &part, &nparts, &gh,
+                                  &merge);
     if (plan != PKV_OK) return plan;
     if (partition_size == 0) {
         const int sm = pkv::current_sm_count();
         if (sm <= 0) return PKV_ERR_CUDA;
         plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                           max_context_len, 0, sm, !int8_kv, &part, &nparts, &gh, &merge);
+                           max_context_len, 0, sm, &part, &nparts, &gh, &merge);
         if (plan != PKV_OK) return plan;
     }
     const size_t need = workspace_for(num_seqs, num_q_heads, head_dim, nparts);
@@ -210,8 +183,6 @@ pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
     if (!status) return PKV_ERR_CUDA;
 
     const int group = num_q_heads / num_kv_heads;
-    const bool tc = !int8_kv && use_tensor_cores(head_dim, group, max_context_len);
-    if (tc && num_blocks > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
     pkv::DecodeParams p{};
     p.q = q;
     p.k_cache = k_cache;
@@ -241,21 +212,6 @@ pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
 
     const int merge_rows = merge ? num_seqs * num_q_heads : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (tc) {
-        CUtensorMap tk, tv;
-        if (!pkv::encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads,
-                             block_size, dtype) ||
-            !pkv::encode_half_map(&tv, v_cache, num_blocks, block_stride_elems, num_kv_heads,
-                             block_size, dtype))
-            return PKV_ERR_CUDA;
-        const int sm = pkv::current_sm_count();
-        if (sm <= 0) return PKV_ERR_CUDA;
-        const int64_t items = static_cast<int64_t>(num_seqs) * p.items_y * nparts;
-        const int grid = static_cast<int>(std::min<int64_t>(sm, items));
-        return dtype == PKV_F16
-                   ? pkv::launch_decode_tc_f16(p, tk, tv, block_size, gh, grid, merge_rows, s)
-                   : pkv::launch_decode_tc_bf16(p, tk, tv, block_size, gh, grid, merge_rows, s);
-    }
     const dim3 grid(static_cast<unsigned>(nparts), static_cast<unsigned>(num_kv_heads * p.subgroups),
                     static_cast<unsigned>(num_seqs));
     if (int8_kv)
@@ -277,7 +233,7 @@ PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_hea
                                    int *out_num_partitions, int *out_heads_per_block,
                                    int *out_needs_merge) {
     return plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       max_context_len, partition_size, sm_count, true, out_partition_size,
+                       max_context_len, partition_size, sm_count, out_partition_size,
                        out_num_partitions, out_heads_per_block, out_needs_merge);
 }
 
@@ -285,7 +241,7 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num
                                           int head_dim, int block_size, int max_context_len,
                                           int partition_size) {
     return decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                  max_context_len, partition_size, true);
+                                  max_context_len, partition_size);
 }
 
 PKV_API pkv_status pkv_paged_attention_decode(
@@ -304,7 +260,7 @@ PKV_API size_t pkv_decode_int8_workspace_bytes(int num_seqs, int num_q_heads, in
                                                int head_dim, int block_size, int max_context_len,
                                                int partition_size) {
     return decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                  max_context_len, partition_size, false);
+                                  max_context_len, partition_size);
 }
 
 PKV_API pkv_status pkv_paged_attention_decode_int8(
@@ -335,7 +291,6 @@ struct CascadePlan {
     int suffix_part = 0;   // suffix partition size
     int suffix_parts = 0;  // suffix partitions of the longest sequence
     int gh = 0;            // suffix kernel's heads per block
-    bool suffix_tc = false;
 };
 
 pkv_status plan_cascade(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -369,7 +324,6 @@ pkv_status plan_cascade(int num_seqs, int num_q_heads, int num_kv_heads, int hea
     cp->suffix_part = part;
     cp->suffix_parts = nparts;
     cp->gh = gh;
-    cp->suffix_tc = use_tensor_cores(head_dim, group, span);
     return PKV_OK;
 }
 
@@ -490,13 +444,6 @@ PKV_API pkv_status pkv_paged_attention_decode_shared_prefix(
     p.slot_base = cp.splits;
     p.always_partial = 1;
     const int merge_rows = num_seqs * num_q_heads;
-    if (cp.suffix_tc) {
-        const int64_t items = static_cast<int64_t>(num_seqs) * p.items_y * cp.suffix_parts;
-        const int grid = static_cast<int>(std::min<int64_t>(sm, items));
-        return dtype == PKV_F16
-                   ? pkv::launch_decode_tc_f16(p, tk, tv, block_size, cp.gh, grid, merge_rows, s)
-                   : pkv::launch_decode_tc_bf16(p, tk, tv, block_size, cp.gh, grid, merge_rows, s);
-    }
     const dim3 grid(static_cast<unsigned>(cp.suffix_parts), static_cast<unsigned>(p.items_y),
                     static_cast<unsigned>(num_seqs));
     return dtype == PKV_F16

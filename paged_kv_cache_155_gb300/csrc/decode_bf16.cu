@@ -6,10 +6,6 @@ pkv_status launch_decode_bf16(const DecodeParams &p, int head_dim, int block_siz
                               dim3 grid, int merge_rows, cudaStream_t s) {
     return launch_decode_typed<__nv_bfloat16>(p, head_dim, block_size, gh, grid, merge_rows, s);
 }
-pkv_status launch_decode_tc_bf16(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                                 int block_size, int gh, int grid, int merge_rows, cudaStream_t s) {
-    return launch_decode_tc_typed<__nv_bfloat16>(p, tk, tv, block_size, gh, grid, merge_rows, s);
-}
 pkv_status launch_prefix_tc_bf16(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                                  int block_size, dim3 grid, cudaStream_t s) {
     return launch_prefix_tc_typed<__nv_bfloat16>(p, tk, tv, block_size, grid, s);

@@ -169,9 +169,10 @@ struct DecodeGeom {
 template <typename T, typename KT, int D, int BS, int GH>
 __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams p) {
     constexpr bool kQuant = sizeof(KT) == 1;
-    // INT8 cache with 4 or 8 query heads per block: the products run as warp-level
-    // MMAs on fp16 copies of the codes (the per-lane loops would spend GH FMAs per code)
-    constexpr bool kMma = kQuant && GH >= 4;
+    // 4 or 8 query heads per block: the products run as warp-level MMAs (the per-lane
+    // loops would spend GH FMAs per element), INT8 codes on exact fp16 copies
+    constexpr bool kMma = GH >= 4;
+    constexpr bool kMmaBF16 = std::is_same<KT, __nv_bfloat16>::value;  // MMA operand type
     constexpr int VL = decode_lane_values<KT, GH>();  // values per lane vector
     using G = DecodeGeom<D, BS, sizeof(KT), VL>;
     constexpr int NW = G::kWarps, S = G::kStages, TILE = G::kTile, LPT = G::kLanesPerToken,
@@ -320,56 +321,75 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
     // (rows >= GH, and rows 8..15, are zero).  K-chunk kc = 4 j + w pairs the
     // channels 64 j + 16 t + 4 w + {0, 1} / {2, 3} of lane t with the MMA's k
     // indices 2t, 2t+1 / 2t+8, 2t+9, so a lane reads its codes of a token row as
-    // whole 16-byte vectors and its query values are exactly those channels.
+    // whole 16-byte vectors and its query values are exactly those channels.  A
+    // 16-bit cache packs two channels per word: channels 32 j + 8 t + 4 p + {0, 1} /
+    // {2, 3} form k-chunk kc = 2 j + p.  Either way a lane's values run in RUN-channel
+    // groups and k-chunk kc takes its values 4 kc .. 4 kc + 3.
     constexpr int KC = D / 16;                   // k-chunks of QK^T
     constexpr int NT = D / 8;                    // n-tiles of PV (8 channels each)
     constexpr int STEP = TILE < 16 ? TILE : 16;  // tokens per MMA step
     const int mg = lane >> 2, mt = lane & 3;
     uint32_t qa[KC][2];
+    constexpr int RUN = kQuant ? 16 : 8;         // a lane's contiguous channels (16 bytes)
     float mqs = 1.f, mqb = 0.f;  // row mg's score scale 2^e and code-offset bias
     if constexpr (kMma) {
-        float f[D / 4];
+        const T *qrow = static_cast<const T *>(p.q) +
+                        (static_cast<int64_t>(seq) * p.num_q_heads + hq0 + mg) * D + RUN * mt;
+        if constexpr (kQuant) {
+            // the query times scale * log2(e) and the K scale, then one power-of-two
+            // exponent per head (its largest magnitude into [1/2, 1)) before fp16
+            float f[D / 4];
 #pragma unroll
-        for (int e = 0; e < D / 4; ++e) f[e] = 0.f;
-        if (mg < GH) {
-            const T *qrow = static_cast<const T *>(p.q) +
-                            (static_cast<int64_t>(seq) * p.num_q_heads + hq0 + mg) * D + 16 * mt;
-            const float *ksr = p.k_scale + kvh * D + 16 * mt;
+            for (int e = 0; e < D / 4; ++e) f[e] = 0.f;
+            if (mg < GH) {
 #pragma unroll
-            for (int j = 0; j < D / 64; ++j) {
-                Elem<T>::to_f32x8(*reinterpret_cast<const uint4 *>(qrow + 64 * j), f + 16 * j);
-                Elem<T>::to_f32x8(*reinterpret_cast<const uint4 *>(qrow + 64 * j + 8), f + 16 * j + 8);
+                for (int j = 0; j < D / (4 * RUN); ++j) {
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const float4 a = reinterpret_cast<const float4 *>(ksr + 64 * j)[v];
-                    f[16 * j + 4 * v] *= a.x * p.scale_log2;
-                    f[16 * j + 4 * v + 1] *= a.y * p.scale_log2;
-                    f[16 * j + 4 * v + 2] *= a.z * p.scale_log2;
-                    f[16 * j + 4 * v + 3] *= a.w * p.scale_log2;
+                    for (int v = 0; v < RUN; v += 8)
+                        Elem<T>::to_f32x8(*reinterpret_cast<const uint4 *>(qrow + 4 * RUN * j + v), f + RUN * j + v);
+                    const float *ksr = p.k_scale + kvh * D + 4 * RUN * j + RUN * mt;
+#pragma unroll
+                    for (int v = 0; v < RUN / 4; ++v) {
+                        const float4 a = reinterpret_cast<const float4 *>(ksr)[v];
+                        f[RUN * j + 4 * v] *= a.x * p.scale_log2;
+                        f[RUN * j + 4 * v + 1] *= a.y * p.scale_log2;
+                        f[RUN * j + 4 * v + 2] *= a.z * p.scale_log2;
+                        f[RUN * j + 4 * v + 3] *= a.w * p.scale_log2;
+                    }
                 }
             }
-        }
-        float amax = 0.f;
+            float amax = 0.f;
 #pragma unroll
-        for (int e = 0; e < D / 4; ++e) amax = fmaxf(amax, fabsf(f[e]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const int qe = row_exponent(amax);
-        const float down = exp2_int(-qe);
-        float qsum = 0.f;
+            for (int e = 0; e < D / 4; ++e) amax = fmaxf(amax, fabsf(f[e]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            const int qe = row_exponent(amax);
+            const float down = exp2_int(-qe);
+            float qsum = 0.f;
 #pragma unroll
-        for (int kc = 0; kc < KC; ++kc) {
-            const int e = 4 * kc;  // f index of channel 64 (kc / 4) + 16 t + 4 (kc % 4)
-            const __half2 h0 = __floats2half2_rn(f[e] * down, f[e + 1] * down);
-            const __half2 h1 = __floats2half2_rn(f[e + 2] * down, f[e + 3] * down);
-            qa[kc][0] = *reinterpret_cast<const uint32_t *>(&h0);
-            qa[kc][1] = *reinterpret_cast<const uint32_t *>(&h1);
-            qsum += (__low2float(h0) + __high2float(h0)) + (__low2float(h1) + __high2float(h1));
+            for (int kc = 0; kc < KC; ++kc) {
+                float s0, s1;
+                qa[kc][0] = pack_mma2<false>(f[4 * kc] * down, f[4 * kc + 1] * down, s0);
+                qa[kc][1] = pack_mma2<false>(f[4 * kc + 2] * down, f[4 * kc + 3] * down, s1);
+                qsum += s0 + s1;
+            }
+            qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+            qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+            mqs = exp2_int(qe);
+            mqb = mqs * (kCodeOffset * qsum);
+        } else {
+            // 16-bit cache: the query enters unchanged (the cache's type), the
+            // scores take scale * log2(e) in fp32
+#pragma unroll
+            for (int j = 0; j < D / (4 * RUN); ++j) {
+                const uint4 u = mg < GH ? *reinterpret_cast<const uint4 *>(qrow + 4 * RUN * j) : make_uint4(0, 0, 0, 0);
+                qa[2 * j][0] = u.x;
+                qa[2 * j][1] = u.y;
+                qa[2 * j + 1][0] = u.z;
+                qa[2 * j + 1][1] = u.w;
+            }
+            mqs = p.scale_log2;
         }
-        qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
-        qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
-        mqs = exp2_int(qe);
-        mqb = mqs * (kCodeOffset * qsum);
     }
     float oacc[NT][4];  // O = P (V + 1152): row mg, channels of n-tile nt (d2, d3: rows 8..15)
     float mrow = -INFINITY, lrow = 0.f;
@@ -409,8 +429,8 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
             const KT *ks = reinterpret_cast<const KT *>(my_stages + s * G::kStageBytes);
             const KT *vs = ks + TILE * D;
             if constexpr (kMma) {
-                const int8_t *kt = reinterpret_cast<const int8_t *>(ks);
-                const int8_t *vt = reinterpret_cast<const int8_t *>(vs);
+                const unsigned char *kt = reinterpret_cast<const unsigned char *>(ks);
+                const unsigned char *vt = reinterpret_cast<const unsigned char *>(vs);
 #pragma unroll
                 for (int tb = 0; tb < TILE; tb += STEP) {
                     if (tb >= valid) break;  // warp-uniform: the step holds no context token
@@ -422,17 +442,25 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                     for (int h = 0; h < STEP / 8; ++h) {
                         sacc[h][0] = sacc[h][1] = sacc[h][2] = sacc[h][3] = 0.f;
                         sodd[h][0] = sodd[h][1] = sodd[h][2] = sodd[h][3] = 0.f;
-                        const int8_t *krow = kt + (tb + 8 * h + mg) * D + 16 * mt;
+                        const unsigned char *krow =
+                            kt + ((tb + 8 * h + mg) * D + RUN * mt) * static_cast<int>(sizeof(KT));
 #pragma unroll
-                        for (int j = 0; j < D / 64; ++j) {
+                        for (int j = 0; j < D / (4 * RUN); ++j) {
                             const uint4 u = *reinterpret_cast<const uint4 *>(krow + 64 * j);
                             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                            if constexpr (kQuant) {  // four codes -> the two k pairs of one chunk
 #pragma unroll
-                            for (int w = 0; w < 4; ++w) {
-                                uint32_t lo, hi;
-                                codes_to_f16x4_offset(w4[w], lo, hi);
-                                mma_16816_f16(w & 1 ? sodd[h] : sacc[h], qa[4 * j + w][0], 0u, qa[4 * j + w][1], 0u,
-                                              lo, hi);
+                                for (int w = 0; w < 4; ++w) {
+                                    uint32_t lo, hi;
+                                    codes_to_f16x4_offset(w4[w], lo, hi);
+                                    mma_16816<kMmaBF16>(w & 1 ? sodd[h] : sacc[h], qa[4 * j + w][0], 0u,
+                                                        qa[4 * j + w][1], 0u, lo, hi);
+                                }
+                            } else {  // two 16-bit channels per word: two chunks per vector
+#pragma unroll
+                                for (int q = 0; q < 2; ++q)
+                                    mma_16816<kMmaBF16>(q ? sodd[h] : sacc[h], qa[2 * j + q][0], 0u, qa[2 * j + q][1],
+                                                        0u, w4[2 * q], w4[2 * q + 1]);
                             }
                         }
                         sacc[h][0] += sodd[h][0];
@@ -469,26 +497,31 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                     uint32_t pa[STEP / 8];
 #pragma unroll
                     for (int h = 0; h < STEP / 8; ++h) {
-                        const __half2 w2 =
-                            __floats2half2_rn(fast_exp2(sc[2 * h] - mrow), fast_exp2(sc[2 * h + 1] - mrow));
-                        lrow += __low2float(w2) + __high2float(w2);
-                        pa[h] = *reinterpret_cast<const uint32_t *>(&w2);
+                        float rounded;
+                        pa[h] = pack_mma2<kMmaBF16>(fast_exp2(sc[2 * h] - mrow), fast_exp2(sc[2 * h + 1] - mrow),
+                                                    rounded);
+                        lrow += rounded;
                     }
                     // O += P (V + 1152): B column mg of n-tile nt is channel (D / 8) mg + nt;
                     // lane (mg, mt) reads tokens tb + 2 mt, +1 (b0) and tb + 8 + 2 mt, +1 (b1)
-                    // at its D / 8 channels and pairs them per channel
-                    constexpr int VW = D / 32;  // 32-bit words of a lane's channels in a row
+                    // at its D / 8 channels and pairs them per channel (INT8: a byte permute
+                    // and a lop3 per pair, code + 1152; 16-bit: one byte permute per pair)
+                    constexpr int CPW = 4 / static_cast<int>(sizeof(KT));  // channels per word
+                    constexpr int VW = D / 8 / CPW;  // 32-bit words of a lane's channels in a row
                     uint32_t x[STEP / 4][VW];
-                    const int8_t *vrow = vt + (tb + 2 * mt) * D + (D / 8) * mg;
+                    const unsigned char *vrow = vt + ((tb + 2 * mt) * D + (D / 8) * mg) * static_cast<int>(sizeof(KT));
 #pragma unroll
                     for (int r = 0; r < STEP / 4; ++r) {
-                        const int8_t *src = vrow + ((r >> 1) * 8 + (r & 1)) * D;
-                        if constexpr (VW == 4) {
-                            const uint4 u = *reinterpret_cast<const uint4 *>(src);
-                            x[r][0] = u.x;
-                            x[r][1] = u.y;
-                            x[r][2] = u.z;
-                            x[r][3] = u.w;
+                        const unsigned char *src = vrow + ((r >> 1) * 8 + (r & 1)) * D * static_cast<int>(sizeof(KT));
+                        if constexpr (VW >= 4) {
+#pragma unroll
+                            for (int v = 0; v < VW / 4; ++v) {
+                                const uint4 u = reinterpret_cast<const uint4 *>(src)[v];
+                                x[r][4 * v] = u.x;
+                                x[r][4 * v + 1] = u.y;
+                                x[r][4 * v + 2] = u.z;
+                                x[r][4 * v + 3] = u.w;
+                            }
                         } else {
                             const uint2 u = *reinterpret_cast<const uint2 *>(src);
                             x[r][0] = u.x;
@@ -497,21 +530,32 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                     }
 #pragma unroll
                     for (int w = 0; w < VW; ++w) {
-                        uint32_t b0[4], b1[4] = {0u, 0u, 0u, 0u};
-                        b0[0] = token_pair_f16_offset<0>(x[0][w], x[1][w]);
-                        b0[1] = token_pair_f16_offset<1>(x[0][w], x[1][w]);
-                        b0[2] = token_pair_f16_offset<2>(x[0][w], x[1][w]);
-                        b0[3] = token_pair_f16_offset<3>(x[0][w], x[1][w]);
-                        if constexpr (STEP == 16) {
-                            b1[0] = token_pair_f16_offset<0>(x[2][w], x[3][w]);
-                            b1[1] = token_pair_f16_offset<1>(x[2][w], x[3][w]);
-                            b1[2] = token_pair_f16_offset<2>(x[2][w], x[3][w]);
-                            b1[3] = token_pair_f16_offset<3>(x[2][w], x[3][w]);
+                        uint32_t b0[CPW], b1[CPW];
+#pragma unroll
+                        for (int e = 0; e < CPW; ++e) b1[e] = 0u;
+                        if constexpr (kQuant) {
+                            b0[0] = token_pair_f16_offset<0>(x[0][w], x[1][w]);
+                            b0[1] = token_pair_f16_offset<1>(x[0][w], x[1][w]);
+                            b0[2] = token_pair_f16_offset<2>(x[0][w], x[1][w]);
+                            b0[3] = token_pair_f16_offset<3>(x[0][w], x[1][w]);
+                            if constexpr (STEP == 16) {
+                                b1[0] = token_pair_f16_offset<0>(x[2][w], x[3][w]);
+                                b1[1] = token_pair_f16_offset<1>(x[2][w], x[3][w]);
+                                b1[2] = token_pair_f16_offset<2>(x[2][w], x[3][w]);
+                                b1[3] = token_pair_f16_offset<3>(x[2][w], x[3][w]);
+                            }
+                        } else {
+                            b0[0] = __byte_perm(x[0][w], x[1][w], 0x5410);  // low halves: channel 2 w
+                            b0[1] = __byte_perm(x[0][w], x[1][w], 0x7632);  // high halves: 2 w + 1
+                            if constexpr (STEP == 16) {
+                                b1[0] = __byte_perm(x[2][w], x[3][w], 0x5410);
+                                b1[1] = __byte_perm(x[2][w], x[3][w], 0x7632);
+                            }
                         }
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            mma_16816_f16(oacc[4 * w + e], pa[0], 0u, STEP == 16 ? pa[STEP / 8 - 1] : 0u, 0u,
-                                          b0[e], b1[e]);
+                        for (int e = 0; e < CPW; ++e)
+                            mma_16816<kMmaBF16>(oacc[CPW * w + e], pa[0], 0u, STEP == 16 ? pa[STEP / 8 - 1] : 0u, 0u,
+                                                b0[e], b1[e]);
                     }
                 }
             } else {

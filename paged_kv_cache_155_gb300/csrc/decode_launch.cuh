@@ -7,7 +7,6 @@
 #include <atomic>
 
 #include "decode_kernel.cuh"
-#include "decode_tc_kernel.cuh"
 #include "prefix_tc_kernel.cuh"
 #include "pkv_host.h"
 
@@ -65,51 +64,6 @@ pkv_status launch_decode_typed(const DecodeParams &p, int head_dim, int block_si
     return launch_status();
 }
 
-template <typename T, int BS, int GH>
-pkv_status launch_decode_tc_one(const DecodeParams &p, const CUtensorMap &tk,
-                                const CUtensorMap &tv, int grid, cudaStream_t stream) {
-    static std::atomic<uint64_t> configured_devices{0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
-    if (!bit || !(configured_devices.load(std::memory_order_acquire) & bit)) {
-        if (cudaFuncSetAttribute(paged_decode_tc_kernel<T, BS, GH>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TcLayout::kSmemBytes) != cudaSuccess)
-            return PKV_ERR_CUDA;
-        configured_devices.fetch_or(bit, std::memory_order_acq_rel);
-    }
-    paged_decode_tc_kernel<T, BS, GH><<<grid, 256, TcLayout::kSmemBytes, stream>>>(tk, tv, p);
-    count_launch();
-    return launch_status();
-}
-
-template <typename T, int BS>
-pkv_status launch_decode_tc_gh(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                               int gh, int grid, cudaStream_t s) {
-    switch (gh) {
-        case 4: return launch_decode_tc_one<T, BS, 4>(p, tk, tv, grid, s);
-        case 8: return launch_decode_tc_one<T, BS, 8>(p, tk, tv, grid, s);
-        case 16: return launch_decode_tc_one<T, BS, 16>(p, tk, tv, grid, s);
-    }
-    return PKV_ERR_UNSUPPORTED;
-}
-
-template <typename T>
-pkv_status launch_decode_tc_typed(const DecodeParams &p, const CUtensorMap &tk,
-                                  const CUtensorMap &tv, int block_size, int gh, int grid,
-                                  int merge_rows, cudaStream_t s) {
-    pkv_status st = PKV_ERR_UNSUPPORTED;
-    if (block_size == 8) st = launch_decode_tc_gh<T, 8>(p, tk, tv, gh, grid, s);
-    else if (block_size == 16) st = launch_decode_tc_gh<T, 16>(p, tk, tv, gh, grid, s);
-    else if (block_size == 32) st = launch_decode_tc_gh<T, 32>(p, tk, tv, gh, grid, s);
-    if (st != PKV_OK || merge_rows == 0) return st;
-    const unsigned blocks = static_cast<unsigned>((merge_rows + 3) / 4);
-    paged_decode_merge_kernel<T, 128><<<blocks, 128, 0, s>>>(p, merge_rows);
-    count_launch();
-    return launch_status();
-}
-
 template <typename T, int BS>
 pkv_status launch_prefix_tc_one(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                                 dim3 grid, cudaStream_t stream) {
@@ -148,10 +102,6 @@ pkv_status launch_decode_i8_bf16(const DecodeParams &p, int head_dim, int block_
                                  dim3 grid, int merge_rows, cudaStream_t s);
 pkv_status launch_decode_bf16(const DecodeParams &p, int head_dim, int block_size, int gh,
                               dim3 grid, int merge_rows, cudaStream_t s);
-pkv_status launch_decode_tc_f16(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                                int block_size, int gh, int grid, int merge_rows, cudaStream_t s);
-pkv_status launch_decode_tc_bf16(const DecodeParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
-                                 int block_size, int gh, int grid, int merge_rows, cudaStream_t s);
 pkv_status launch_prefix_tc_f16(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                                 int block_size, dim3 grid, cudaStream_t s);
 pkv_status launch_prefix_tc_bf16(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv,

@@ -254,16 +254,38 @@ __device__ __forceinline__ uint32_t token_pair_f16_offset(uint32_t x, uint32_t y
     return out;
 }
 
-// Warp-level MMA m16n8k16, fp16 operands, fp32 accumulators (d += a b):
+// Warp-level MMA m16n8k16, fp16 (or bf16) operands, fp32 accumulators (d += a b):
 // a0 / a2 = row g, k 2t..2t+1 / 2t+8..2t+9; a1 / a3 the same for row g + 8;
 // b0 / b1 = k 2t..2t+1 / 2t+8..2t+9 of column g; d0, d1 = row g, columns
 // 2t, 2t+1; d2, d3 = row g + 8 (g = lane / 4, t = lane % 4).
-__device__ __forceinline__ void mma_16816_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                              uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+template <bool kBF16 = false>
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    if constexpr (kBF16)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+            "{%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+            "{%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two floats -> one word of two fp16 (or bf16) values, the first in the low half;
+// `sum` receives the sum of the two rounded values.
+template <bool kBF16>
+__device__ __forceinline__ uint32_t pack_mma2(float a, float b, float &sum) {
+    if constexpr (kBF16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        sum = __low2float(h) + __high2float(h);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    } else {
+        const __half2 h = __floats2half2_rn(a, b);
+        sum = __low2float(h) + __high2float(h);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
 }
 
 // Exponent e with |m| * 2^-e in [1/2, 1) for a finite m > 0 (e = 0 otherwise),

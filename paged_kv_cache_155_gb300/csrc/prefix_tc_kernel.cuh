@@ -27,9 +27,39 @@
 // 2-5 softmax.
 #pragma once
 
-#include "decode_tc_kernel.cuh"
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "decode_kernel.cuh"
+#include "pkv_tc.cuh"
 
 namespace pkv {
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                        unsigned int *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+            raise_flag(status, PKV_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// tc_wait for a whole warp: every lane waits, and the warp continues only if
+// every lane's wait succeeded, so no lane leaves a loop that the others stay in
+// (the warp-wide shuffles and TMEM accesses that follow need all 32 lanes).
+__device__ __forceinline__ bool tc_wait_warp(uint64_t *bar, uint32_t parity,
+                                             volatile int *abort_flag, unsigned int *status) {
+    const bool ok = tc_wait(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
 
 struct PrefixParams {
     const void *q;

@@ -193,22 +193,19 @@ def test_plan_explicit_partition(lib):
 
 
 def test_plan_heads_per_block_follows_the_group(lib):
-    # long contexts, head_dim 128, 4/8/16 heads per KV head: the tensor-core path serves the group
+    # a block serves the largest of 8, 4, 2, 1 query heads dividing the group, whatever
+    # the context length and head_dim (a group of 16 takes two blocks of 8)
     for hq, hkv, want in [(32, 32, 1), (32, 16, 2), (32, 8, 4), (64, 8, 8), (24, 8, 1),
-                          (48, 8, 2), (128, 8, 16)]:
-        st, (_, _, gh, _) = plan(lib, 4, hq, hkv, 128, 16, 4000, 0)
-        assert st == 0 and gh == want, (hq, hkv)
-    # short contexts stay on CUDA cores (at most 8 heads per CTA), as does head_dim 64
-    st, (_, _, gh, _) = plan(lib, 4, 128, 8, 128, 16, 1000, 0)
-    assert st == 0 and gh == 8
-    st, (_, _, gh, _) = plan(lib, 4, 128, 8, 64, 16, 4000, 0)
-    assert st == 0 and gh == 8
+                          (48, 8, 2), (128, 8, 8)]:
+        for d, maxl in [(128, 4000), (128, 1000), (64, 4000)]:
+            st, (_, _, gh, _) = plan(lib, 4, hq, hkv, d, 16, maxl, 0)
+            assert st == 0 and gh == want, (hq, hkv, d, maxl)
 
 
-def test_plan_tensor_core_partitions_are_whole_tiles(lib):
+def test_plan_gqa_partitions_cover_the_context(lib):
     for maxl in (2048, 4096, 8192, 32768):
         st, (p, n, gh, _) = plan(lib, 64, 32, 8, 128, 16, maxl, 0)
-        assert st == 0 and gh == 4 and p % 128 == 0 and (n - 1) * p < maxl <= n * p
+        assert st == 0 and gh == 4 and p % 16 == 0 and p >= 256 and (n - 1) * p < maxl <= n * p
 
 
 def test_plan_auto_split_fills_the_gpu_and_respects_limits(lib):

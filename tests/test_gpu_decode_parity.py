@@ -40,9 +40,8 @@ def _check_step(wl_dev, partition_size=0):
 @pytest.mark.parametrize("bs", [8, 16, 32])
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (16, 4), (32, 4), (12, 4), (24, 4), (64, 4)])
 def test_decode_shapes(dtype, d, bs, hq, hkv, longest):
-    """A batch whose longest context is >= 2048 runs on the tensor-core kernel when
-    head_dim is 128 and the group has 4, 8 or 16 heads; a short batch on the CUDA-core
-    kernel: both kernels see every shape."""
+    """Every shape, with a short and a long batch: groups of 4, 8 or 16 query heads per KV
+    head run as warp-level MMAs (16 as two blocks of 8), the others as per-lane loops."""
     dev = device()
     lens = [1, bs - 1, bs, bs + 1, 5 * bs + 3, longest, 17]
     wl = make_decode_workload(num_seqs=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
@@ -55,7 +54,7 @@ def test_decode_shapes(dtype, d, bs, hq, hkv, longest):
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 def test_decode_forced_partitions(partition, dtype):
     dev = device()
-    lens = [1, 15, 16, 17, 511, 512, 513, 1500, 2049]   # longest >= 2048: tensor cores
+    lens = [1, 15, 16, 17, 511, 512, 513, 1500, 2049]
     wl = make_decode_workload(num_seqs=len(lens), num_q_heads=16, num_kv_heads=2, head_dim=128,
                               block_size=16, context_lens=lens, dtype=dtype, seed=partition,
                               device=str(dev))
@@ -116,7 +115,7 @@ def test_decode_extreme_scores_stay_finite():
     _check_step(wl, partition_size=64)
 
 
-@pytest.mark.parametrize("longest", [2047, 2100], ids=["cuda-cores", "tensor-cores"])
+@pytest.mark.parametrize("longest", [2047, 2100], ids=["2047", "2100"])
 def test_decode_output_is_independent_of_block_placement(longest):
     """Moving every block to another physical slot leaves the output bitwise unchanged."""
     dev = device()

@@ -2,7 +2,7 @@
 definition: the cascade must give the same attention as decoding each sequence
 over its whole table.  Covers query-row counts that are not a multiple of 128,
 prefixes that end inside a 128-token tile, MHA and GQA groups (the suffix pass
-then runs on CUDA cores or tensor cores), both dtypes, all block sizes, forced
+then runs per-lane loops or warp-level MMAs), both dtypes, all block sizes, forced
 suffix partitions, empty suffixes, and the full shared-prefix workload."""
 import numpy as np
 import pytest
@@ -121,8 +121,8 @@ def test_shared_prefix_flags_a_sequence_shorter_than_the_prefix():
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
-def test_shared_prefix_long_suffixes_use_the_tensor_core_suffix_pass(dtype):
-    """Suffixes up to 2500 tokens: the suffix pass runs on the tensor-core kernel."""
+def test_shared_prefix_long_suffixes(dtype):
+    """Suffixes up to 2500 tokens, several suffix partitions per sequence."""
     dev = device()
     g = torch.Generator().manual_seed(21)
     n, prefix = 12, 512
