@@ -40,18 +40,23 @@
 //    leaves known sums: a dot product starts from -1152 times the lane's query
 //    sum, and the output removes 1152 times the weight sum, whose terms are the
 //    weights rounded to fp16 exactly as they meet V.
-//  * INT8 cache with 4 or 8 query heads per block (grouped-query attention):
-//    the lane loops would spend GH FMAs per code, so both products run as
-//    warp-level MMAs (m16n8k16, fp16 operands, fp32 accumulators) on the same
-//    fp16 values.  Per 16-token step a warp computes S = q' (K + 1152)^T with
-//    the heads as rows (rows past GH are zero) and the tokens as columns: each
-//    lane widens its K codes in registers with one byte permute per pair and
-//    feeds them straight in as the B fragment.  The S accumulators of a row
-//    are the A fragment of P (V + 1152) after the softmax, with no exchange
-//    between lanes; V's B fragment pairs two tokens of one channel, built by a
-//    byte permute and one three-input logic op per pair.  Operands come from
-//    registers, so the widened codes never go back to shared memory, and each
-//    warp still streams its own ring with no hand-off to other warps.
+//  * 4 or 8 query heads per block (grouped-query attention): the lane loops
+//    would spend GH FMAs per cache element, so both products run as warp-level
+//    MMAs (m16n8k16, fp32 accumulators) on register fragments, 16 tokens per
+//    step, and each warp still streams its own ring with no hand-off to other
+//    warps.  The k indices of QK^T are mapped to channels so that a lane's
+//    16-byte vector of a token row holds whole k pairs.
+//    - 16-bit cache: S = Q K^T with the heads as the 16 rows (rows past GH are
+//      zero) and the tokens as columns; the K words go straight in as the B
+//      fragment, and the S accumulators of a row are the A fragment of P V
+//      after the softmax.  V's B fragment pairs two tokens of one channel with
+//      one byte permute.
+//    - INT8 cache: S^T = K Q^T with the tokens as rows and the heads as
+//      columns, on the fp16 values code + 1152 widened in registers (one byte
+//      permute per pair); P moves into the B layout of O^T = (V + 1152)^T P^T
+//      by two 8 x 8 transposes, and V's A fragment pairs two tokens of a
+//      channel with a byte permute and one three-input logic op.  No padded
+//      head rows: half the MMAs and accumulators, so four CTAs fit an SM.
 #pragma once
 
 #include "pkv_device.cuh"
@@ -157,7 +162,7 @@ struct DecodeGeom {
     static constexpr int kIters = kTile / kTokenGroups;  // token rows per lane per stage
     static constexpr int kTileBytes = kTile * D * EB;    // one K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStagesRaw = (EB == 1 ? 16384 : 24576) / kStageBytes;
+    static constexpr int kStagesRaw = (EB == 1 ? (VL == 8 ? 12288 : 16384) : 24576) / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kMaxTableEntries = 1024;        // table slice per partition
     static constexpr int kSmemBytes = kWarps * kStages * kStageBytes +
@@ -316,17 +321,20 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
             qo[g] = kCodeOffset * qsum;
         }
     }
-    // Warp-MMA form: lane (mg, mt) = (lane / 4, lane % 4) holds row mg of the A
-    // fragments of S = q' (K + 1152)^T, row mg being query head mg of the block
-    // (rows >= GH, and rows 8..15, are zero).  K-chunk kc = 4 j + w pairs the
-    // channels 64 j + 16 t + 4 w + {0, 1} / {2, 3} of lane t with the MMA's k
-    // indices 2t, 2t+1 / 2t+8, 2t+9, so a lane reads its codes of a token row as
-    // whole 16-byte vectors and its query values are exactly those channels.  A
-    // 16-bit cache packs two channels per word: channels 32 j + 8 t + 4 p + {0, 1} /
-    // {2, 3} form k-chunk kc = 2 j + p.  Either way a lane's values run in RUN-channel
-    // groups and k-chunk kc takes its values 4 kc .. 4 kc + 3.
+    // Warp-MMA form (m16n8k16, fp32 accumulators), lane (mg, mt) = (lane / 4, lane % 4).
+    // S^T = K Q^T per 16-token step: the 16 rows are tokens, the 8 columns query heads
+    // (columns >= GH are zero), k runs over channels in chunks of 16.  O^T = V^T P^T:
+    // rows are channels, columns heads, k the step's tokens.  The k indices of QK^T are
+    // mapped to channels so that a lane reads its part of a token row as 16-byte
+    // vectors: INT8 k-chunk kc = 4 j + w pairs channels 64 j + 16 t + 4 w + {0, 1} /
+    // {2, 3} of lane t with k 2t, 2t+1 / 2t+8, 2t+9; a 16-bit cache packs two
+    // channels per word, so chunk kc = 2 j + p takes channels 32 j + 8 t + 4 p + {0, 1}
+    // / {2, 3}.  Either way a lane's values run in RUN-channel groups and chunk kc
+    // takes its values 4 kc .. 4 kc + 3.  The query (B operand of QK^T) of head mg sits
+    // in lanes (mg, .) with exactly those channels.
     constexpr int KC = D / 16;                   // k-chunks of QK^T
-    constexpr int NT = D / 8;                    // n-tiles of PV (8 channels each)
+    constexpr int MT = D / 16;                   // INT8: m-tiles of O^T (16 channels each)
+    constexpr int NT = D / 8;                    // 16-bit: n-tiles of O (8 channels each)
     constexpr int STEP = TILE < 16 ? TILE : 16;  // tokens per MMA step
     const int mg = lane >> 2, mt = lane & 3;
     uint32_t qa[KC][2];
@@ -368,10 +376,10 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
             float qsum = 0.f;
 #pragma unroll
             for (int kc = 0; kc < KC; ++kc) {
-                float s0, s1;
-                qa[kc][0] = pack_mma2<false>(f[4 * kc] * down, f[4 * kc + 1] * down, s0);
-                qa[kc][1] = pack_mma2<false>(f[4 * kc + 2] * down, f[4 * kc + 3] * down, s1);
-                qsum += s0 + s1;
+                float r0, r1, r2, r3;
+                qa[kc][0] = pack_mma2<false>(f[4 * kc] * down, f[4 * kc + 1] * down, r0, r1);
+                qa[kc][1] = pack_mma2<false>(f[4 * kc + 2] * down, f[4 * kc + 3] * down, r2, r3);
+                qsum += (r0 + r1) + (r2 + r3);
             }
             qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
             qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
@@ -391,11 +399,22 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
             mqs = p.scale_log2;
         }
     }
-    float oacc[NT][4];  // O = P (V + 1152): row mg, channels of n-tile nt (d2, d3: rows 8..15)
-    float mrow = -INFINITY, lrow = 0.f;
+    // MMA accumulators of O.  INT8 (O^T = (V + 1152)^T P^T, heads as columns): m-tile j
+    // holds channels (D / 8) mg + 2 j (d0, d1) and + 1 (d2, d3) of heads 2 mt (d0, d2)
+    // and 2 mt + 1 (d1, d3).  16-bit (O = P V, heads as rows): n-tile nt holds head mg
+    // (d0, d1; d2, d3 rows 8..15) at channels (D / 8) (2 mt) + nt and (D / 8) (2 mt + 1) + nt.
+    float oacc[NT][4];
+    float mh[2] = {-INFINITY, -INFINITY}, lh[2] = {0.f, 0.f};  // INT8: heads 2 mt, 2 mt + 1
+    float hqs[2] = {1.f, 1.f}, hqb[2] = {0.f, 0.f};            // their score scales / biases
+    float mrow = -INFINITY, lrow = 0.f;                        // 16-bit: head mg
     if constexpr (kMma) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) oacc[nt][0] = oacc[nt][1] = oacc[nt][2] = oacc[nt][3] = 0.f;
+        for (int j = 0; j < NT; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            hqs[e] = __shfl_sync(0xffffffffu, mqs, 4 * (2 * mt + e));
+            hqb[e] = __shfl_sync(0xffffffffu, mqb, 4 * (2 * mt + e));
+        }
     }
     float acc[GH][VL];
     float m[GH], l[GH];
@@ -428,40 +447,145 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
         if (tbl[(c * TILE) / BS] >= 0) {
             const KT *ks = reinterpret_cast<const KT *>(my_stages + s * G::kStageBytes);
             const KT *vs = ks + TILE * D;
-            if constexpr (kMma) {
+            if constexpr (kMma && kQuant) {
+                // INT8 cache: S^T = K Q^T with the tokens as the 16 rows and the heads as
+                // the 8 columns, O^T = (V + 1152)^T P^T with the channels as rows; P moves
+                // from the S^T accumulators into the B layout by 8 x 8 transposes.  No
+                // padded head rows: half the MMAs and accumulators of the heads-as-rows form.
                 const unsigned char *kt = reinterpret_cast<const unsigned char *>(ks);
                 const unsigned char *vt = reinterpret_cast<const unsigned char *>(vs);
 #pragma unroll
                 for (int tb = 0; tb < TILE; tb += STEP) {
                     if (tb >= valid) break;  // warp-uniform: the step holds no context token
-                    // S for the step: n-tile h = tokens tb + 8 h + (0..7); B column mg of it
-                    // is token tb + 8 h + mg, read by lanes (mg, .) as 16-byte vectors
-                    // two accumulators per n-tile (even / odd k-chunks) halve the MMA chains
+                    // S^T for the step: A rows mg and mg + 8 are tokens tb + mg and tb + 8 + mg,
+                    // read by lanes (mg, .) as 16-byte vectors; two accumulators (even / odd
+                    // k-chunks) halve the MMA chains
+                    float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sodd[4] = {0.f, 0.f, 0.f, 0.f};
+                    const unsigned char *krow0 = kt + (tb + mg) * D + RUN * mt;
+                    const unsigned char *krow1 = krow0 + 8 * D;
+#pragma unroll
+                    for (int j = 0; j < D / (4 * RUN); ++j) {
+                        const uint4 u0 = *reinterpret_cast<const uint4 *>(krow0 + 64 * j);
+                        uint4 u1 = make_uint4(0, 0, 0, 0);
+                        if constexpr (STEP == 16) u1 = *reinterpret_cast<const uint4 *>(krow1 + 64 * j);
+                        const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w};
+                        const uint32_t w1[4] = {u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {  // four codes -> the two k pairs of one chunk
+                            uint32_t lo0, hi0, lo1 = 0u, hi1 = 0u;
+                            codes_to_f16x4_offset(w0[w], lo0, hi0);
+                            if constexpr (STEP == 16) codes_to_f16x4_offset(w1[w], lo1, hi1);
+                            mma_16816<false>(w & 1 ? sodd : sacc, lo0, lo1, hi0, hi1, qa[4 * j + w][0],
+                                             qa[4 * j + w][1]);
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[e] += sodd[e];
+                    // scores in log2 units: d0, d1 = token tb + mg, heads 2 mt, 2 mt + 1; d2, d3 =
+                    // token tb + 8 + mg; tokens past the context -> -inf
+                    float sc[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        sc[e] = tb + mg + 8 * (e >> 1) < valid ? fmaf(sacc[e], hqs[e & 1], -hqb[e & 1]) : -INFINITY;
+                    // per head, the maximum over the step's tokens (the eight lanes with this
+                    // mt hold them): finite, as token tb is in the context
+                    float mx[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        float v = fmaxf(sc[e], sc[2 + e]);
+#pragma unroll
+                        for (int o = 4; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+                        mx[e] = v;
+                    }
+                    const bool grow0 = mx[0] > mh[0], grow1 = mx[1] > mh[1];
+                    if (__any_sync(0xffffffffu, grow0 || grow1)) {
+                        const float a0 = grow0 ? fast_exp2(mh[0] - mx[0]) : 1.f;  // 0 when m = -inf
+                        const float a1 = grow1 ? fast_exp2(mh[1] - mx[1]) : 1.f;
+                        lh[0] *= a0;
+                        lh[1] *= a1;
+#pragma unroll
+                        for (int j = 0; j < MT; ++j) {
+                            oacc[j][0] *= a0;
+                            oacc[j][2] *= a0;
+                            oacc[j][1] *= a1;
+                            oacc[j][3] *= a1;
+                        }
+                        if (grow0) mh[0] = mx[0];
+                        if (grow1) mh[1] = mx[1];
+                    }
+                    // P^T rounded to the MMA type (the row sums add the rounded values), moved
+                    // into the B layout of O^T += V^T P^T (k = tokens, columns = heads) by 8 x 8
+                    // transposes
+                    float r[4];
+                    const uint32_t p0 = pack_mma2<false>(fast_exp2(sc[0] - mh[0]), fast_exp2(sc[1] - mh[1]), r[0], r[1]);
+                    const uint32_t p1 = pack_mma2<false>(fast_exp2(sc[2] - mh[0]), fast_exp2(sc[3] - mh[1]), r[2], r[3]);
+                    lh[0] += r[0] + r[2];
+                    lh[1] += r[1] + r[3];
+                    const uint32_t pb0 = movmatrix_trans(p0);
+                    const uint32_t pb1 = STEP == 16 ? movmatrix_trans(p1) : 0u;
+                    // O^T += (V + 1152)^T P^T: A rows mg / mg + 8 of m-tile j are channels
+                    // (D / 8) mg + 2 j / + 1; lane (mg, mt) reads tokens tb + 2 mt, +1 (k 2t, 2t+1)
+                    // and tb + 8 + 2 mt, +1 (k 2t+8, 2t+9) at its D / 8 channels and pairs them per
+                    // channel (byte permute + lop3, code + 1152)
+                    constexpr int VW = D / 32;  // 32-bit words of a lane's channels in a row
+                    uint32_t x[STEP / 4][VW];
+                    const unsigned char *vrow = vt + (tb + 2 * mt) * D + (D / 8) * mg;
+#pragma unroll
+                    for (int rr = 0; rr < STEP / 4; ++rr) {
+                        const unsigned char *src = vrow + ((rr >> 1) * 8 + (rr & 1)) * D;
+                        if constexpr (VW == 4) {
+                            const uint4 u = *reinterpret_cast<const uint4 *>(src);
+                            x[rr][0] = u.x;
+                            x[rr][1] = u.y;
+                            x[rr][2] = u.z;
+                            x[rr][3] = u.w;
+                        } else {
+                            const uint2 u = *reinterpret_cast<const uint2 *>(src);
+                            x[rr][0] = u.x;
+                            x[rr][1] = u.y;
+                        }
+                    }
+#pragma unroll
+                    for (int w = 0; w < VW; ++w) {  // channels 4 w + e: m-tile 2 w + e / 2, row half e % 2
+                        uint32_t a[4], c[4] = {0u, 0u, 0u, 0u};
+                        a[0] = token_pair_f16_offset<0>(x[0][w], x[1][w]);
+                        a[1] = token_pair_f16_offset<1>(x[0][w], x[1][w]);
+                        a[2] = token_pair_f16_offset<2>(x[0][w], x[1][w]);
+                        a[3] = token_pair_f16_offset<3>(x[0][w], x[1][w]);
+                        if constexpr (STEP == 16) {
+                            c[0] = token_pair_f16_offset<0>(x[2][w], x[3][w]);
+                            c[1] = token_pair_f16_offset<1>(x[2][w], x[3][w]);
+                            c[2] = token_pair_f16_offset<2>(x[2][w], x[3][w]);
+                            c[3] = token_pair_f16_offset<3>(x[2][w], x[3][w]);
+                        }
+                        mma_16816<false>(oacc[2 * w], a[0], a[1], c[0], c[1], pb0, pb1);
+                        mma_16816<false>(oacc[2 * w + 1], a[2], a[3], c[2], c[3], pb0, pb1);
+                    }
+                }
+            } else if constexpr (kMma) {
+                // 16-bit cache: S = Q K^T with the heads as the 16 rows (rows >= GH are
+                // zero) and two 8-token column tiles; O = P V with P taken straight from
+                // the S accumulators (the A fragment of a row is its S fragment)
+                const unsigned char *kt = reinterpret_cast<const unsigned char *>(ks);
+                const unsigned char *vt = reinterpret_cast<const unsigned char *>(vs);
+#pragma unroll
+                for (int tb = 0; tb < TILE; tb += STEP) {
+                    if (tb >= valid) break;  // warp-uniform: the step holds no context token
+                    // n-tile h = tokens tb + 8 h + (0..7); B column mg of it is token
+                    // tb + 8 h + mg, read by lanes (mg, .) as 16-byte vectors (two channels
+                    // per word, so one vector holds two k-chunks); two accumulators per
+                    // n-tile (even / odd k-chunks) halve the MMA chains
                     float sacc[STEP / 8][4], sodd[STEP / 8][4];
 #pragma unroll
                     for (int h = 0; h < STEP / 8; ++h) {
                         sacc[h][0] = sacc[h][1] = sacc[h][2] = sacc[h][3] = 0.f;
                         sodd[h][0] = sodd[h][1] = sodd[h][2] = sodd[h][3] = 0.f;
-                        const unsigned char *krow =
-                            kt + ((tb + 8 * h + mg) * D + RUN * mt) * static_cast<int>(sizeof(KT));
+                        const unsigned char *krow = kt + ((tb + 8 * h + mg) * D + RUN * mt) * 2;
 #pragma unroll
                         for (int j = 0; j < D / (4 * RUN); ++j) {
                             const uint4 u = *reinterpret_cast<const uint4 *>(krow + 64 * j);
-                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-                            if constexpr (kQuant) {  // four codes -> the two k pairs of one chunk
-#pragma unroll
-                                for (int w = 0; w < 4; ++w) {
-                                    uint32_t lo, hi;
-                                    codes_to_f16x4_offset(w4[w], lo, hi);
-                                    mma_16816<kMmaBF16>(w & 1 ? sodd[h] : sacc[h], qa[4 * j + w][0], 0u,
-                                                        qa[4 * j + w][1], 0u, lo, hi);
-                                }
-                            } else {  // two 16-bit channels per word: two chunks per vector
-#pragma unroll
-                                for (int q = 0; q < 2; ++q)
-                                    mma_16816<kMmaBF16>(q ? sodd[h] : sacc[h], qa[2 * j + q][0], 0u, qa[2 * j + q][1],
-                                                        0u, w4[2 * q], w4[2 * q + 1]);
-                            }
+                            mma_16816<kMmaBF16>(sacc[h], qa[2 * j][0], 0u, qa[2 * j][1], 0u, u.x, u.y);
+                            mma_16816<kMmaBF16>(sodd[h], qa[2 * j + 1][0], 0u, qa[2 * j + 1][1], 0u, u.z, u.w);
                         }
                         sacc[h][0] += sodd[h][0];
                         sacc[h][1] += sodd[h][1];
@@ -473,8 +597,7 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                     for (int h = 0; h < STEP / 8; ++h)
 #pragma unroll
                         for (int e = 0; e < 2; ++e)
-                            sc[2 * h + e] = tb + 8 * h + 2 * mt + e < valid ? fmaf(sacc[h][e], mqs, -mqb)
-                                                                             : -INFINITY;
+                            sc[2 * h + e] = tb + 8 * h + 2 * mt + e < valid ? sacc[h][e] * mqs : -INFINITY;
                     float mx = sc[0];
 #pragma unroll
                     for (int e = 1; e < STEP / 4; ++e) mx = fmaxf(mx, sc[e]);
@@ -492,69 +615,46 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                         }
                         if (grow) mrow = mx;
                     }
-                    // the weights meet V rounded to fp16 (as the A fragment of P V, rows
-                    // and k indices those of S); the row sum adds the rounded values
+                    // the weights meet V rounded to the cache type (as the A fragment of P V,
+                    // rows and k indices those of S); the row sum adds the rounded values
                     uint32_t pa[STEP / 8];
 #pragma unroll
                     for (int h = 0; h < STEP / 8; ++h) {
-                        float rounded;
+                        float r0, r1;
                         pa[h] = pack_mma2<kMmaBF16>(fast_exp2(sc[2 * h] - mrow), fast_exp2(sc[2 * h + 1] - mrow),
-                                                    rounded);
-                        lrow += rounded;
+                                                    r0, r1);
+                        lrow += r0 + r1;
                     }
-                    // O += P (V + 1152): B column mg of n-tile nt is channel (D / 8) mg + nt;
-                    // lane (mg, mt) reads tokens tb + 2 mt, +1 (b0) and tb + 8 + 2 mt, +1 (b1)
-                    // at its D / 8 channels and pairs them per channel (INT8: a byte permute
-                    // and a lop3 per pair, code + 1152; 16-bit: one byte permute per pair)
-                    constexpr int CPW = 4 / static_cast<int>(sizeof(KT));  // channels per word
-                    constexpr int VW = D / 8 / CPW;  // 32-bit words of a lane's channels in a row
+                    // O += P V: B column mg of n-tile nt is channel (D / 8) mg + nt; lane
+                    // (mg, mt) reads tokens tb + 2 mt, +1 (b0) and tb + 8 + 2 mt, +1 (b1) at its
+                    // D / 8 channels and pairs them per channel with one byte permute
+                    constexpr int VW = D / 16;  // 32-bit words of a lane's channels in a row
                     uint32_t x[STEP / 4][VW];
-                    const unsigned char *vrow = vt + ((tb + 2 * mt) * D + (D / 8) * mg) * static_cast<int>(sizeof(KT));
+                    const unsigned char *vrow = vt + ((tb + 2 * mt) * D + (D / 8) * mg) * 2;
 #pragma unroll
                     for (int r = 0; r < STEP / 4; ++r) {
-                        const unsigned char *src = vrow + ((r >> 1) * 8 + (r & 1)) * D * static_cast<int>(sizeof(KT));
-                        if constexpr (VW >= 4) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(vrow + ((r >> 1) * 8 + (r & 1)) * D * 2);
 #pragma unroll
-                            for (int v = 0; v < VW / 4; ++v) {
-                                const uint4 u = reinterpret_cast<const uint4 *>(src)[v];
-                                x[r][4 * v] = u.x;
-                                x[r][4 * v + 1] = u.y;
-                                x[r][4 * v + 2] = u.z;
-                                x[r][4 * v + 3] = u.w;
-                            }
-                        } else {
-                            const uint2 u = *reinterpret_cast<const uint2 *>(src);
-                            x[r][0] = u.x;
-                            x[r][1] = u.y;
+                        for (int v = 0; v < VW / 4; ++v) {
+                            const uint4 u = src[v];
+                            x[r][4 * v] = u.x;
+                            x[r][4 * v + 1] = u.y;
+                            x[r][4 * v + 2] = u.z;
+                            x[r][4 * v + 3] = u.w;
                         }
                     }
 #pragma unroll
                     for (int w = 0; w < VW; ++w) {
-                        uint32_t b0[CPW], b1[CPW];
-#pragma unroll
-                        for (int e = 0; e < CPW; ++e) b1[e] = 0u;
-                        if constexpr (kQuant) {
-                            b0[0] = token_pair_f16_offset<0>(x[0][w], x[1][w]);
-                            b0[1] = token_pair_f16_offset<1>(x[0][w], x[1][w]);
-                            b0[2] = token_pair_f16_offset<2>(x[0][w], x[1][w]);
-                            b0[3] = token_pair_f16_offset<3>(x[0][w], x[1][w]);
-                            if constexpr (STEP == 16) {
-                                b1[0] = token_pair_f16_offset<0>(x[2][w], x[3][w]);
-                                b1[1] = token_pair_f16_offset<1>(x[2][w], x[3][w]);
-                                b1[2] = token_pair_f16_offset<2>(x[2][w], x[3][w]);
-                                b1[3] = token_pair_f16_offset<3>(x[2][w], x[3][w]);
-                            }
-                        } else {
-                            b0[0] = __byte_perm(x[0][w], x[1][w], 0x5410);  // low halves: channel 2 w
-                            b0[1] = __byte_perm(x[0][w], x[1][w], 0x7632);  // high halves: 2 w + 1
-                            if constexpr (STEP == 16) {
-                                b1[0] = __byte_perm(x[2][w], x[3][w], 0x5410);
-                                b1[1] = __byte_perm(x[2][w], x[3][w], 0x7632);
-                            }
+                        uint32_t b0[2], b1[2] = {0u, 0u};
+                        b0[0] = __byte_perm(x[0][w], x[1][w], 0x5410);  // low halves: channel 2 w
+                        b0[1] = __byte_perm(x[0][w], x[1][w], 0x7632);  // high halves: 2 w + 1
+                        if constexpr (STEP == 16) {
+                            b1[0] = __byte_perm(x[2][w], x[3][w], 0x5410);
+                            b1[1] = __byte_perm(x[2][w], x[3][w], 0x7632);
                         }
 #pragma unroll
-                        for (int e = 0; e < CPW; ++e)
-                            mma_16816<kMmaBF16>(oacc[CPW * w + e], pa[0], 0u, STEP == 16 ? pa[STEP / 8 - 1] : 0u, 0u,
+                        for (int e = 0; e < 2; ++e)
+                            mma_16816<kMmaBF16>(oacc[2 * w + e], pa[0], 0u, STEP == 16 ? pa[STEP / 8 - 1] : 0u, 0u,
                                                 b0[e], b1[e]);
                     }
                 }
@@ -668,7 +768,17 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
 
     // ---- merge the token groups of this warp (same m across the warp); in the
     //      MMA form the row sums of a head's four lanes
-    if constexpr (kMma) {
+    if constexpr (kMma && kQuant) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) lh[e] += __shfl_xor_sync(0xffffffffu, lh[e], o);
+            if (aborted) {
+                mh[e] = -INFINITY;
+                lh[e] = 0.f;
+            }
+        }
+    } else if constexpr (kMma) {
         lrow += __shfl_xor_sync(0xffffffffu, lrow, 1);
         lrow += __shfl_xor_sync(0xffffffffu, lrow, 2);
         if (aborted) {
@@ -697,7 +807,24 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
     // ---- merge the warps through shared memory (each warp reuses its own
     //      stage buffers: all of its copies have landed)
     float *mine = reinterpret_cast<float *>(my_stages);  // [GH][D + 2]
-    if constexpr (kMma) {
+    if constexpr (kMma && kQuant) {
+        // lane (mg, mt): heads 2 mt, 2 mt + 1 at channels (D / 8) mg + 2 j (+ 1)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = 2 * mt + e;
+            if (h >= GH) continue;
+            float *row = mine + h * (D + 4) + (D / 8) * mg;
+#pragma unroll
+            for (int j = 0; j < MT; ++j) {
+                row[2 * j] = oacc[j][e];
+                row[2 * j + 1] = oacc[j][2 + e];
+            }
+            if (mg == 0) {
+                mine[h * (D + 4) + D] = mh[e];
+                mine[h * (D + 4) + D + 1] = lh[e];
+            }
+        }
+    } else if constexpr (kMma) {
         // d0 / d1 of n-tile nt: head mg, channels (D / 8) (2 mt) + nt / (D / 8) (2 mt + 1) + nt
         if (mg < GH) {
             float *row = mine + mg * (D + 4);

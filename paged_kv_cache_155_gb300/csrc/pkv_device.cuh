@@ -273,17 +273,27 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Transpose of an 8 x 8 matrix of 16-bit values held by a warp: lane i holds
+// row i / 4, columns 2 (i % 4) and 2 (i % 4) + 1 (low half first), before and after.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 // Two floats -> one word of two fp16 (or bf16) values, the first in the low half;
-// `sum` receives the sum of the two rounded values.
+// ra / rb receive the two rounded values.
 template <bool kBF16>
-__device__ __forceinline__ uint32_t pack_mma2(float a, float b, float &sum) {
+__device__ __forceinline__ uint32_t pack_mma2(float a, float b, float &ra, float &rb) {
     if constexpr (kBF16) {
         const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        sum = __low2float(h) + __high2float(h);
+        ra = __low2float(h);
+        rb = __high2float(h);
         return *reinterpret_cast<const uint32_t *>(&h);
     } else {
         const __half2 h = __floats2half2_rn(a, b);
-        sum = __low2float(h) + __high2float(h);
+        ra = __low2float(h);
+        rb = __high2float(h);
         return *reinterpret_cast<const uint32_t *>(&h);
     }
 }
