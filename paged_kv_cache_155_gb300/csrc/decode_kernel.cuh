@@ -149,9 +149,11 @@ __device__ __forceinline__ void load_codes_f16(const int8_t *src, uint32_t *h) {
 // values per lane vector).  16-bit caches use 8 values (16 bytes) per lane;
 // the INT8 cache uses 16 codes (16 bytes) per lane when a block serves at most
 // two query heads (fewer lanes per token row: shorter shuffle reductions and
-// fewer per-row steps per byte), else 8 codes (register budget).  INT8 stages
-// get a smaller per-warp budget so three CTAs fit on an SM.
-template <int D, int BS, int EB = 2, int VL = 8>
+// fewer per-row steps per byte), else 8 codes (register budget).  The stage
+// budget per warp sets how many CTAs share an SM: INT8 lane loops 16 KiB (three),
+// INT8 warp MMAs 12 KiB (four), 16-bit lane loops 24 KiB (two), 16-bit warp MMAs
+// 16 KiB (three).
+template <int D, int BS, int EB = 2, int VL = 8, bool kMmaForm = false>
 struct DecodeGeom {
     static constexpr int kWarps = 4;
     static constexpr int kMaxTile = 32 / EB;             // 4 KiB K tiles at head_dim 128
@@ -162,7 +164,8 @@ struct DecodeGeom {
     static constexpr int kIters = kTile / kTokenGroups;  // token rows per lane per stage
     static constexpr int kTileBytes = kTile * D * EB;    // one K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStagesRaw = (EB == 1 ? (VL == 8 ? 12288 : 16384) : 24576) / kStageBytes;
+    static constexpr int kBudget = EB == 1 ? (kMmaForm ? 12288 : 16384) : (kMmaForm ? 16384 : 24576);
+    static constexpr int kStagesRaw = kBudget / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kMaxTableEntries = 1024;        // table slice per partition
     static constexpr int kSmemBytes = kWarps * kStages * kStageBytes +
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
     constexpr bool kMma = GH >= 4;
     constexpr bool kMmaBF16 = std::is_same<KT, __nv_bfloat16>::value;  // MMA operand type
     constexpr int VL = decode_lane_values<KT, GH>();  // values per lane vector
-    using G = DecodeGeom<D, BS, sizeof(KT), VL>;
+    using G = DecodeGeom<D, BS, sizeof(KT), VL, (GH >= 4)>;
     constexpr int NW = G::kWarps, S = G::kStages, TILE = G::kTile, LPT = G::kLanesPerToken,
                   TPG = G::kTokenGroups, ITERS = G::kIters;
     // token rows processed between two online-softmax updates (bounds registers)
@@ -321,17 +324,19 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
             qo[g] = kCodeOffset * qsum;
         }
     }
-    // Warp-MMA form (m16n8k16, fp32 accumulators), lane (mg, mt) = (lane / 4, lane % 4).
-    // S^T = K Q^T per 16-token step: the 16 rows are tokens, the 8 columns query heads
-    // (columns >= GH are zero), k runs over channels in chunks of 16.  O^T = V^T P^T:
-    // rows are channels, columns heads, k the step's tokens.  The k indices of QK^T are
-    // mapped to channels so that a lane reads its part of a token row as 16-byte
-    // vectors: INT8 k-chunk kc = 4 j + w pairs channels 64 j + 16 t + 4 w + {0, 1} /
-    // {2, 3} of lane t with k 2t, 2t+1 / 2t+8, 2t+9; a 16-bit cache packs two
-    // channels per word, so chunk kc = 2 j + p takes channels 32 j + 8 t + 4 p + {0, 1}
-    // / {2, 3}.  Either way a lane's values run in RUN-channel groups and chunk kc
-    // takes its values 4 kc .. 4 kc + 3.  The query (B operand of QK^T) of head mg sits
-    // in lanes (mg, .) with exactly those channels.
+    // Warp-MMA forms (m16n8k16, fp32 accumulators), lane (mg, mt) = (lane / 4, lane % 4),
+    // per step of 16 tokens, k of QK^T running over channels in chunks of 16:
+    //  - INT8: S^T = K Q^T with the tokens as the 16 rows and the query heads as the 8
+    //    columns (columns >= GH zero), then O^T = V^T P^T with channels as rows;
+    //  - 16-bit: S = Q K^T with the heads as the 16 rows (rows >= GH zero) and two
+    //    8-token column tiles, then O = P V.
+    // The k indices of QK^T are mapped to channels so that a lane reads its part of a
+    // token row as 16-byte vectors: INT8 k-chunk kc = 4 j + w pairs channels
+    // 64 j + 16 t + 4 w + {0, 1} / {2, 3} of lane t with k 2t, 2t+1 / 2t+8, 2t+9; a
+    // 16-bit cache packs two channels per word, so chunk kc = 2 j + p takes channels
+    // 32 j + 8 t + 4 p + {0, 1} / {2, 3}.  Either way a lane's values run in
+    // RUN-channel groups and chunk kc takes its values 4 kc .. 4 kc + 3.  The query of head mg (the B operand of S^T,
+    // the A operand of S) sits in lanes (mg, .) with exactly those channels.
     constexpr int KC = D / 16;                   // k-chunks of QK^T
     constexpr int MT = D / 16;                   // INT8: m-tiles of O^T (16 channels each)
     constexpr int NT = D / 8;                    // 16-bit: n-tiles of O (8 channels each)

@@ -14,7 +14,7 @@ namespace pkv {
 
 template <typename T, typename KT, int D, int BS, int GH>
 pkv_status launch_decode_one(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
-    using G = DecodeGeom<D, BS, sizeof(KT), decode_lane_values<KT, GH>()>;
+    using G = DecodeGeom<D, BS, sizeof(KT), decode_lane_values<KT, GH>(), (GH >= 4)>;
     static std::atomic<uint64_t> configured_devices{0};  // bit per device ordinal
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
