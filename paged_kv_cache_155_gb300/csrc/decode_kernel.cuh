@@ -150,9 +150,9 @@ __device__ __forceinline__ void load_codes_f16(const int8_t *src, uint32_t *h) {
 // the INT8 cache uses 16 codes (16 bytes) per lane when a block serves at most
 // two query heads (fewer lanes per token row: shorter shuffle reductions and
 // fewer per-row steps per byte), else 8 codes (register budget).  The stage
-// budget per warp sets how many CTAs share an SM: INT8 lane loops 16 KiB (three),
-// INT8 warp MMAs 12 KiB (four), 16-bit lane loops 24 KiB (two), 16-bit warp MMAs
-// 16 KiB (three).
+// budget per warp sets how many CTAs share an SM: INT8 lane loops 8 KiB (six at
+// 80 registers), INT8 warp MMAs 12 KiB (four), 16-bit lane loops 24 KiB (two),
+// 16-bit warp MMAs 16 KiB (three).
 template <int D, int BS, int EB = 2, int VL = 8, bool kMmaForm = false>
 struct DecodeGeom {
     static constexpr int kWarps = 4;
@@ -164,7 +164,7 @@ struct DecodeGeom {
     static constexpr int kIters = kTile / kTokenGroups;  // token rows per lane per stage
     static constexpr int kTileBytes = kTile * D * EB;    // one K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kBudget = EB == 1 ? (kMmaForm ? 12288 : 16384) : (kMmaForm ? 16384 : 24576);
+    static constexpr int kBudget = EB == 1 ? (kMmaForm ? 12288 : 8192) : (kMmaForm ? 16384 : 24576);
     static constexpr int kStagesRaw = kBudget / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kMaxTableEntries = 1024;        // table slice per partition
