@@ -223,6 +223,16 @@ def test_plan_auto_split_fills_the_gpu_and_respects_limits(lib):
     assert st == INVALID
 
 
+def test_int8_and_16bit_decode_share_one_plan(lib):
+    # the INT8 cache runs the same kernel template and plan as the 16-bit caches, so the
+    # two workspace queries agree for every shape (explicit partitions: no device query)
+    for b, hq, hkv, d, bs, maxl, part in [(4, 32, 8, 128, 16, 4096, 512), (16, 64, 8, 128, 16, 32768, 1024),
+                                          (3, 4, 4, 64, 8, 100, 16), (7, 48, 8, 128, 32, 2000, 256)]:
+        a = lib.pkv_decode_workspace_bytes(b, hq, hkv, d, bs, maxl, part)
+        i8 = lib.pkv_decode_int8_workspace_bytes(b, hq, hkv, d, bs, maxl, part)
+        assert a == i8 and a == (0 if maxl <= part else b * hq * -(-maxl // part) * (d + 2) * 4)
+
+
 def test_workspace_bytes_explicit_partition(lib):
     n = lib.pkv_decode_workspace_bytes(16, 64, 8, 128, 16, 32768, 512)
     assert n == 16 * 64 * 64 * (128 + 2) * 4
