@@ -157,6 +157,67 @@ def _algorithmic_bytes(wl):
     return kv + qo + scales
 
 
+def _unique_bytes(wl):
+    """Bytes a decode must read at least once: K+V of every distinct context token
+    (a prefix shared by every table counted once) + q + out (+ INT8 scales).  Equal
+    to the algorithmic bytes except for the shared-prefix workload."""
+    if not wl.shared_prefix_blocks:
+        return _algorithmic_bytes(wl)
+    e = wl.kv.element_size()
+    pre = wl.shared_prefix_blocks * wl.block_size
+    tokens = pre + sum(int(x) - pre for x in wl.context_lens.cpu().tolist())
+    qo = 2 * wl.num_seqs * wl.num_q_heads * wl.head_dim * wl.q.element_size()
+    return tokens * 2 * wl.num_kv_heads * wl.head_dim * e + qo
+
+
+# The pages' five configurations, by workload name.
+CONFIG_WORKLOADS = {"1": "tiny", "2": "mha7b", "3": "gqa7b", "4": "prefix", "5": "long70b"}
+
+
+def _config_summary(main, line, others):
+    """Compact per-configuration figures (kept short: the last key of the line)."""
+    r3 = lambda x: None if x is None else round(float(x), 3)
+    out = {}
+    for key, name in CONFIG_WORKLOADS.items():
+        if name == main:
+            e = {"workload": name, "tokens_per_s": round(line["value"]),
+                 "kv_read_gbps": round(line["kv_read_gbps"]),
+                 "hbm_frac": r3(line["hbm_frac_of_measured"]),
+                 "decode_us": round(line["roofline"]["launch_ms"] * 1e3, 1)}
+        else:
+            w = others.get(name)
+            if w is None:
+                continue
+            e = {"workload": name, "tokens_per_s": round(w["tokens_per_s"]),
+                 "kv_read_gbps": round(w["kv_read_gbps"]), "hbm_frac": r3(w["hbm_frac_of_measured"]),
+                 "decode_us": round(w["decode_ms"] * 1e3, 1)}
+            if name == "tiny":
+                e.update({"eager_us_per_step": round(w["ms_per_step"] * 1e3, 1),
+                          "graph_us_per_step": round(w["graph_us_per_step"], 1)})
+                e.pop("kv_read_gbps"), e.pop("hbm_frac")
+            if name == "prefix":
+                c = w["shared_prefix_decode"]
+                e = {"workload": "prefix, shared-prefix decode",
+                     "tokens_per_s": round(c["tokens_per_s"]), "unique_gbps": round(c["unique_gbps"]),
+                     "hbm_frac_unique": r3(c["unique_frac_of_measured"]),
+                     "hbm_frac_unique_l2_flushed":
+                         r3(c["l2_flushed"]["shared_prefix_unique_frac_of_measured"]),
+                     "decode_us": round(c["decode_ms"] * 1e3, 1),
+                     "plain_decode_hbm_frac_unique": r3(w["hbm_frac_of_measured"])}
+        out[key] = e
+    for name in ("mha7b_int8", "gqa7b_int8", "long70b_int8"):
+        w = others.get(name)
+        if w is not None:
+            out[name] = {"hbm_frac": r3(w["hbm_frac_of_measured"]),
+                         "decode_us": round(w["decode_ms"] * 1e3, 1)}
+    for name in ("prefill7b", "chunked70b"):
+        w = others.get(name)
+        if w is not None:
+            out[name] = {"tflops": round(w["tflops"]), "frac": r3(w["tensor_frac_of_measured_bf16"]),
+                         "attention_us": round(w["attention_ms"] * 1e3, 1)}
+    return out
+
+
 def _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part):
     """(cache write, decode) of one step through the public API, for a 16-bit or
     an INT8 pool."""
@@ -312,7 +373,8 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
     k_cache, v_cache = pkv.split_pool(wl.kv)
     maxl = int(wl.context_lens.max())
     part = workloads.DEFAULT_PARTITION[name] if partition is None else partition
-    slots = pkv.slot_mapping(wl.block_tables.cpu(), wl.new_positions.cpu(), wl.block_size).to(dev)
+    slots = pkv.slot_mapping(wl.block_tables, wl.new_positions, wl.block_size,
+                             num_blocks=wl.num_blocks)
     out = torch.empty_like(wl.q)
     stream = torch.cuda.current_stream(dev)
     write, decode = _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part)
@@ -336,8 +398,10 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
     t1.record(stream)
     torch.cuda.synchronize()
     ms_step = t0.elapsed_time(t1) / steps
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    dec_times = [a.elapsed_time(b) for a, b in ev]
+    dec_ms = statistics.median(dec_times)
     nbytes = _algorithmic_bytes(wl)
+    unique = _unique_bytes(wl)
     # CUDA-graph replay of `reps` steps
     reps = 50
     side = torch.cuda.Stream(dev)
@@ -363,15 +427,18 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
     if flags:
         raise RuntimeError(f"device flags on {name}: {names}")
     result = {"tokens_per_s": wl.num_seqs / (ms_step / 1e3), "ms_per_step": ms_step,
-              "decode_ms": dec_ms, "kv_read_gbps": nbytes / (dec_ms / 1e3) / 1e9,
-              "hbm_frac_of_measured": nbytes / (dec_ms / 1e3) / 1e9 / peak,
+              "decode_ms": dec_ms, "decode_ms_mean": statistics.mean(dec_times),
+              "kv_read_gbps": unique / (dec_ms / 1e3) / 1e9,
+              "hbm_frac_of_measured": unique / (dec_ms / 1e3) / 1e9 / peak,
               "graph_us_per_step": graph_ms * 1e3,
               "graph_tokens_per_s": wl.num_seqs / (graph_ms / 1e3),
               "algorithmic_bytes": nbytes, "num_seqs": wl.num_seqs,
               "partition_size": part, "kv_dtype": str(wl.kv.dtype).replace("torch.", "")}
     if name == "prefix":
-        result["note"] = ("kv_read_gbps counts every sequence's prefix reads (logical bytes); "
-                          "the 64 shared prefix blocks are read from L2 after the first touch")
+        result["effective_gbps"] = nbytes / (dec_ms / 1e3) / 1e9
+        result["note"] = ("kv_read_gbps and hbm_frac count unique bytes (the shared prefix "
+                          "once); effective_gbps counts every sequence's prefix reads (logical "
+                          "bytes), which after the first touch come from L2")
         # copy-on-write of the last shared prefix block into one private block per sequence
         pairs = wl.cow_pairs
         blk_bytes = 2 * wl.num_kv_heads * wl.block_size * wl.head_dim * 2
@@ -418,7 +485,7 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
         if flags:
             raise RuntimeError(f"device flags on the shared-prefix decode: {names}")
         c_step = s0.elapsed_time(s1) / steps
-        c_dec = statistics.mean(a.elapsed_time(b) for a, b in ev2)
+        c_dec = statistics.median(a.elapsed_time(b) for a, b in ev2)
 
         # the same two decodes with L2 flushed before every call (a 256 MiB write,
         # outside the timed region): the shared prefix is then read from HBM each time
@@ -433,7 +500,7 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
                 call()
                 b.record(stream)
             torch.cuda.synchronize()
-            return statistics.mean(a.elapsed_time(b) for a, b in evs)
+            return statistics.median(a.elapsed_time(b) for a, b in evs)
 
         plain_flushed = flushed_ms(lambda: pkv.paged_attention_decode(
             wl.q, k_cache, v_cache, wl.block_tables, wl.context_lens, wl.scale, out,
@@ -442,9 +509,6 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
             wl.q, k_cache, v_cache, pre_table, pre_tokens, wl.block_tables, wl.context_lens,
             wl.scale, out, max_context_len=maxl))
         del flush
-        row_bytes = 2 * wl.num_kv_heads * wl.head_dim * 2          # K+V of one token, all KV heads
-        suffix_tokens = sum(int(x) - pre_tokens for x in wl.context_lens.cpu().tolist())
-        unique = (pre_tokens + suffix_tokens) * row_bytes + 2 * wl.num_seqs * wl.num_q_heads * wl.head_dim * 2
         result["shared_prefix_decode"] = {
             "tokens_per_s": wl.num_seqs / (c_step / 1e3), "ms_per_step": c_step,
             "decode_ms": c_dec, "speedup_vs_plain_decode": dec_ms / c_dec,
@@ -454,6 +518,8 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
             "l2_flushed": {"plain_decode_ms": plain_flushed, "shared_prefix_decode_ms": cascade_flushed,
                            "plain_unique_gbps": unique / (plain_flushed / 1e3) / 1e9,
                            "shared_prefix_unique_gbps": unique / (cascade_flushed / 1e3) / 1e9,
+                           "shared_prefix_unique_frac_of_measured":
+                               unique / (cascade_flushed / 1e3) / 1e9 / peak,
                            "note": "256 MiB written before each call, outside the timed region"}}
     del wl, k_cache, v_cache, out, graph
     torch.cuda.empty_cache()
@@ -477,8 +543,8 @@ def measure_prefill(pkv, name, dev, steps):
     from paged_kv_cache_155_gb300 import workloads
     wl = workloads.PREFILL_NAMED[name](device=str(dev))
     k_cache, v_cache = pkv.split_pool(wl.kv)
-    rows_tables = wl.block_tables.cpu()[wl.row_seq.cpu()]
-    slots = pkv.slot_mapping(rows_tables, wl.new_positions.cpu(), wl.block_size).to(dev)
+    slots = pkv.slot_mapping(wl.block_tables, wl.new_positions, wl.block_size,
+                             token_rows=wl.row_seq, num_blocks=wl.num_blocks)
     out = torch.empty_like(wl.q)
     stream = torch.cuda.current_stream(dev)
     mq, mc = wl.max_query_len, wl.max_context_len
@@ -507,7 +573,7 @@ def measure_prefill(pkv, name, dev, steps):
     if flags:
         raise RuntimeError(f"device flags on {name}: {names}")
     ms_step = t0.elapsed_time(t1) / steps
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    attn_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
     visible = int((wl.new_positions.cpu() + 1).sum())
     flops = 4 * wl.head_dim * wl.num_q_heads * visible
     peak, kind = _tensor_peak()
@@ -543,7 +609,8 @@ def run_ours(args):
     sm = torch.cuda.get_device_properties(dev).multi_processor_count
     plan = pkv.decode_plan(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
                            wl.block_size, maxl, part, sm)
-    slots = pkv.slot_mapping(wl.block_tables.cpu(), wl.new_positions.cpu(), wl.block_size).to(dev)
+    slots = pkv.slot_mapping(wl.block_tables, wl.new_positions, wl.block_size,
+                             num_blocks=wl.num_blocks)
     out = torch.empty_like(wl.q)
     stream = torch.cuda.current_stream(dev)
     write, decode = _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part)
@@ -587,7 +654,8 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dec_ev)
+    dec_times = [a.elapsed_time(b) for a, b in dec_ev]
+    dec_ms = statistics.median(dec_times)
     ms_total = max_over_ranks(ms_total, dev, world)
     ms_step = ms_total / args.steps
     value = whole_job_tokens_per_s(world, wl.num_seqs, ms_step)
@@ -684,13 +752,15 @@ def run_ours(args):
 
     # ---- roofline of the decode kernel(s)
     peak, peak_kind = _peaks()
-    bytes_launch = _algorithmic_bytes(wl)
+    bytes_launch = _unique_bytes(wl)
     achieved = bytes_launch / (dec_ms / 1000.0) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": achieved / peak, "traffic": _profiled_traffic(args.workload),
             "peak_source": f"{peak_kind} hbm_gbs",
             "kernel": "paged_decode_kernel" + ("+merge" if plan["needs_merge"] else ""),
-            "algorithmic_bytes_per_launch": bytes_launch, "launch_ms": dec_ms}
+            "algorithmic_bytes_per_launch": bytes_launch, "launch_ms": dec_ms,
+            "launch_ms_is": f"median of {len(dec_times)} CUDA-event-timed calls in the timed "
+                            "region", "launch_ms_mean": statistics.mean(dec_times)}
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -718,6 +788,7 @@ def run_ours(args):
         for name in ("prefill7b", "chunked70b"):
             others[name] = measure_prefill(pkv, name, dev, 50)
         line["other_workloads"] = others
+        line["configs"] = _config_summary(args.workload, line, others)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -23,8 +23,9 @@
  * Heads.  Query head hq reads KV head hq / (num_q_heads / num_kv_heads).
  * Types.  dtype is fp16 or bf16 for q, K, V and out; accumulation is fp32.
  *   head_dim is 64 or 128; block_size is 8, 16 or 32.  Others: PKV_ERR_UNSUPPORTED.
- * Memory.  Every pointer argument except the host-side outputs of
- *   pkv_get_device_error is a DEVICE pointer owned by the caller.  Tensor base
+ * Memory.  Every pointer argument is a DEVICE pointer owned by the caller,
+ *   except where a call says HOST (pkv_slot_mapping_host, the outputs of
+ *   pkv_get_device_error and the block manager's arrays).  Tensor base
  *   pointers must be 16-byte aligned and block strides a multiple of 8
  *   elements.  No call allocates memory; the library's only state is one
  *   device status word per device (see pkv_get_device_error), the fixed
@@ -98,6 +99,44 @@ PKV_API pkv_status pkv_reshape_and_cache(const void *k_new, const void *v_new,
                                          int64_t block_stride_elems, int num_kv_heads,
                                          int head_dim, int block_size, pkv_dtype dtype,
                                          void *stream);
+
+/*
+ * pkv_slot_mapping -- the slot each new token's K/V rows are written to, i.e.
+ * the slot_mapping input of pkv_reshape_and_cache (P1 §5.3: logical position t
+ * of a sequence lies in its table entry t / block_size at offset
+ * t % block_size; the flat slot is entry * block_size + offset; P1 §4.2's worked
+ * table [7, 2, 9, 1, 5, 8, 3] puts position 99 in slot 3*16 + 3).
+ *
+ *   block_tables   [num_table_rows][max_blocks_per_seq] int32, device.
+ *   token_rows     [num_tokens] int64, device: the table row of each token's
+ *                  sequence; NULL means token i uses row i (then
+ *                  num_table_rows >= num_tokens).
+ *   positions      [num_tokens] int64, device: each token's logical position;
+ *                  a negative position is padding and gets slot -1.
+ *   num_blocks     pool size, for the range check of table entries.
+ *   slot_mapping   [num_tokens] int64, device output.
+ * A position past the table (>= max_blocks_per_seq * block_size) or a token row
+ * outside the table raises PKV_DEVERR_SLOT, a table entry outside
+ * [0, num_blocks) raises PKV_DEVERR_BLOCK_TABLE; such a token gets slot -1.
+ * Enqueued on `stream`; num_tokens == 0 is a no-op.
+ */
+PKV_API pkv_status pkv_slot_mapping(const int32_t *block_tables, int64_t num_table_rows,
+                                    int max_blocks_per_seq, const int64_t *token_rows,
+                                    const int64_t *positions, int64_t num_tokens, int block_size,
+                                    int64_t num_blocks, int64_t *slot_mapping, void *stream);
+
+/*
+ * pkv_slot_mapping_host -- pkv_slot_mapping on HOST arrays, computed on the
+ * calling thread (no CUDA call), for callers that keep their block tables in
+ * host memory.  Same rule and outputs; instead of device flags it returns
+ * PKV_ERR_INVALID_ARG when any token had a bad position, row or table entry
+ * (every slot is still written, those tokens' as -1).
+ */
+PKV_API pkv_status pkv_slot_mapping_host(const int32_t *block_tables, int64_t num_table_rows,
+                                         int max_blocks_per_seq, const int64_t *token_rows,
+                                         const int64_t *positions, int64_t num_tokens,
+                                         int block_size, int64_t num_blocks,
+                                         int64_t *slot_mapping);
 
 /*
  * pkv_decode_workspace_bytes -- device scratch that pkv_paged_attention_decode

@@ -23,6 +23,8 @@ SZ = ctypes.c_size_t
 # name -> (restype, argtypes); mirrors include/pagedkv.h
 SIGNATURES = {
     "pkv_reshape_and_cache": (I32, [P, P, P, I64, P, P, I64, I64, I32, I32, I32, I32, P]),
+    "pkv_slot_mapping": (I32, [P, I64, I32, P, P, I64, I32, I64, P, P]),
+    "pkv_slot_mapping_host": (I32, [P, I64, I32, P, P, I64, I32, I64, P]),
     "pkv_decode_workspace_bytes": (SZ, [I32, I32, I32, I32, I32, I32, I32]),
     "pkv_paged_attention_decode": (I32, [P, P, P, I64, I64, P, I32, P, I32, I32, I32, I32,
                                          I32, I32, ctypes.c_float, P, P, SZ, I32, I32, P]),

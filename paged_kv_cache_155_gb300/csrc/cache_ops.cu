@@ -4,7 +4,9 @@
 //   pkv_reshape_and_cache_int8: the same placement into an INT8 cache, each
 //     value quantised with its channel's scale ("KV Cache从原理到实战" §5.2);
 //   pkv_copy_blocks: copy-on-write copies of whole blocks (same page §8.3;
-//     zwxr.cn nano-vllm article §2.3, §5.5).
+//     zwxr.cn nano-vllm article §2.3, §5.5);
+//   pkv_slot_mapping / pkv_slot_mapping_host: the slot each new token is
+//     written to (same page §5.3), on the device or on host arrays.
 // The 16-bit write and the copy move 16-byte vectors and are bit-exact; the
 // INT8 write's codes are those of the quantiser in pkv_device.cuh.
 // Device-resident indices are range-checked before use; a bad one raises a
@@ -119,6 +121,42 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(
     }
 }
 
+// Slot rule of "KV Cache与PagedAttention深度解析" §5.3 for one token: position t
+// of a sequence lies in the table entry t / block_size at offset t % block_size,
+// and the flat slot is entry * block_size + offset.  A negative position is
+// padding (slot -1).  Returns the PKV_DEVERR_* flag of a bad input (its slot is
+// -1 too) or 0.  Shared by the device kernel and the host entry point.
+__host__ __device__ inline unsigned int slot_of(const int32_t *table_row, int max_blocks_per_seq,
+                                                int64_t pos, int block_size, int64_t num_blocks,
+                                                int64_t *slot) {
+    *slot = -1;
+    if (pos < 0) return 0;
+    const int64_t entry = pos / block_size;
+    if (entry >= max_blocks_per_seq) return PKV_DEVERR_SLOT;
+    const int64_t blk = table_row[entry];
+    if (blk < 0 || blk >= num_blocks) return PKV_DEVERR_BLOCK_TABLE;
+    *slot = blk * block_size + pos % block_size;
+    return 0;
+}
+
+// One thread per token; token i reads table row token_rows[i] (or row i).
+__global__ void __launch_bounds__(256) slot_mapping_kernel(
+    const int32_t *__restrict__ block_tables, int64_t num_table_rows, int max_blocks_per_seq,
+    const int64_t *__restrict__ token_rows, const int64_t *__restrict__ positions,
+    int64_t num_tokens, int block_size, int64_t num_blocks, int64_t *__restrict__ slot_mapping,
+    unsigned int *status) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= num_tokens) return;
+    const int64_t row = token_rows ? token_rows[i] : i;
+    int64_t slot = -1;
+    unsigned int flag = PKV_DEVERR_SLOT;  // a token row outside the table
+    if (row >= 0 && row < num_table_rows)
+        flag = slot_of(block_tables + row * max_blocks_per_seq, max_blocks_per_seq, positions[i],
+                       block_size, num_blocks, &slot);
+    if (flag) pkv::raise_flag(status, flag);
+    slot_mapping[i] = slot;
+}
+
 bool supported_shape(int head_dim, int block_size) {
     return (head_dim == 64 || head_dim == 128) &&
            (block_size == 8 || block_size == 16 || block_size == 32);
@@ -197,6 +235,54 @@ PKV_API pkv_status pkv_reshape_and_cache_int8(const void *k_new, const void *v_n
             num_kv_heads, head_dim, block_size, status);
     pkv::count_launch();
     return pkv::launch_status();
+}
+
+PKV_API pkv_status pkv_slot_mapping(const int32_t *block_tables, int64_t num_table_rows,
+                                    int max_blocks_per_seq, const int64_t *token_rows,
+                                    const int64_t *positions, int64_t num_tokens, int block_size,
+                                    int64_t num_blocks, int64_t *slot_mapping, void *stream) {
+    if (num_tokens < 0 || num_table_rows < 0 || max_blocks_per_seq <= 0 || block_size <= 0 ||
+        num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (!token_rows && num_table_rows < num_tokens) return PKV_ERR_INVALID_ARG;
+    if ((num_tokens + 255) / 256 > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!block_tables || !positions || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    unsigned int *status = pkv::status_word_ptr();
+    if (!status) return PKV_ERR_CUDA;
+    slot_mapping_kernel<<<static_cast<unsigned>((num_tokens + 255) / 256), 256, 0,
+                          static_cast<cudaStream_t>(stream)>>>(
+        block_tables, num_table_rows, max_blocks_per_seq, token_rows, positions, num_tokens,
+        block_size, num_blocks, slot_mapping, status);
+    pkv::count_launch();
+    return pkv::launch_status();
+}
+
+PKV_API pkv_status pkv_slot_mapping_host(const int32_t *block_tables, int64_t num_table_rows,
+                                         int max_blocks_per_seq, const int64_t *token_rows,
+                                         const int64_t *positions, int64_t num_tokens,
+                                         int block_size, int64_t num_blocks,
+                                         int64_t *slot_mapping) {
+    if (num_tokens < 0 || num_table_rows < 0 || max_blocks_per_seq <= 0 || block_size <= 0 ||
+        num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (!token_rows && num_table_rows < num_tokens) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!block_tables || !positions || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    bool bad = false;
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        const int64_t row = token_rows ? token_rows[i] : i;
+        int64_t slot = -1;
+        if (row >= 0 && row < num_table_rows) {
+            if (slot_of(block_tables + row * max_blocks_per_seq, max_blocks_per_seq, positions[i],
+                        block_size, num_blocks, &slot))
+                bad = true;
+        } else {
+            bad = true;
+        }
+        slot_mapping[i] = slot;
+    }
+    return bad ? PKV_ERR_INVALID_ARG : PKV_OK;
 }
 
 PKV_API pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, int64_t num_blocks,

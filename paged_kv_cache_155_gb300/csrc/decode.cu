@@ -43,6 +43,23 @@ bool encode_half_map(CUtensorMap *map, const void *base, int64_t num_blocks,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view of one half (K or V) of an INT8 pool with head_dim 128: (128 codes,
+// num_kv_heads*block_size rows, num_blocks) with the caller's block stride;
+// boxes are one block's rows of one head (128 bytes each), 128-byte swizzled.
+bool encode_i8_half_map(CUtensorMap *map, const void *base, int64_t num_blocks,
+                        int64_t block_stride_elems, int num_kv_heads, int block_size) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(num_kv_heads) * block_size,
+                                static_cast<cuuint64_t>(num_blocks)};
+    const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(block_stride_elems)};
+    const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(block_size), 1};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
+              elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D view of the prefill queries [num_rows][num_q_heads][128]: boxes of
 // `tokens` tokens x `group` heads x 64 columns, 128-byte swizzled, so a box
 // lands as tokens * group consecutive 128-byte rows (token-major).
@@ -214,13 +231,20 @@ pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(static_cast<unsigned>(nparts), static_cast<unsigned>(num_kv_heads * p.subgroups),
                     static_cast<unsigned>(num_seqs));
+    // The INT8 warp-MMA form at head_dim 128 (4 or 8 heads per block) stages K/V
+    // tiles by tiled TMA copies with a 128-byte swizzle
+    pkv::DecodeMaps maps{};
+    if (int8_kv && head_dim == 128 && gh >= 4 &&
+        (!pkv::encode_i8_half_map(&maps.k, k_cache, num_blocks, block_stride_elems, num_kv_heads, block_size) ||
+         !pkv::encode_i8_half_map(&maps.v, v_cache, num_blocks, block_stride_elems, num_kv_heads, block_size)))
+        return PKV_ERR_CUDA;
     if (int8_kv)
         return dtype == PKV_F16
-                   ? pkv::launch_decode_i8_f16(p, head_dim, block_size, gh, grid, merge_rows, s)
-                   : pkv::launch_decode_i8_bf16(p, head_dim, block_size, gh, grid, merge_rows, s);
+                   ? pkv::launch_decode_i8_f16(p, maps, head_dim, block_size, gh, grid, merge_rows, s)
+                   : pkv::launch_decode_i8_bf16(p, maps, head_dim, block_size, gh, grid, merge_rows, s);
     return dtype == PKV_F16
-               ? pkv::launch_decode_f16(p, head_dim, block_size, gh, grid, merge_rows, s)
-               : pkv::launch_decode_bf16(p, head_dim, block_size, gh, grid, merge_rows, s);
+               ? pkv::launch_decode_f16(p, maps, head_dim, block_size, gh, grid, merge_rows, s)
+               : pkv::launch_decode_bf16(p, maps, head_dim, block_size, gh, grid, merge_rows, s);
 }
 
 }  // namespace
@@ -283,6 +307,11 @@ PKV_API pkv_status pkv_paged_attention_decode_int8(
 // ---------------------------------------------------------------------------
 namespace {
 
+#ifndef PKV_PREFIX_SM_SHARE
+#define PKV_PREFIX_SM_SHARE 5
+#endif
+constexpr int kPrefixSmShare = PKV_PREFIX_SM_SHARE;  // prefix CTAs ~ SMs / this
+
 struct CascadePlan {
     int rows = 0;          // num_seqs * group
     int row_tiles = 0;     // of 128 query rows
@@ -306,10 +335,14 @@ pkv_status plan_cascade(int num_seqs, int num_q_heads, int num_kv_heads, int hea
     cp->rows = num_seqs * group;
     cp->row_tiles = (cp->rows + 127) / 128;
     if (cp->row_tiles > 0x7fffffff / 2 || num_kv_heads > 65535) return PKV_ERR_INVALID_ARG;
-    // enough prefix splits that the prefix kernel covers the SMs, whole 128-token tiles each
+    // The prefix CTAs (one per SM: their shared memory fills it) run beside the
+    // suffix decode, which overlaps them: split the prefix, in whole 128-token
+    // tiles, only as far as about sm_count / kPrefixSmShare CTAs, so the suffix
+    // keeps most SMs and each prefix CTA runs enough tiles to amortise its set-up.
     const int tiles = (prefix_len + 127) / 128;
     const int64_t units = static_cast<int64_t>(cp->row_tiles) * num_kv_heads;
-    int splits = static_cast<int>(std::min<int64_t>(tiles, std::max<int64_t>(1, (sm_count + units - 1) / units)));
+    const int64_t want = std::max(1, sm_count / kPrefixSmShare);
+    int splits = static_cast<int>(std::min<int64_t>(tiles, std::max<int64_t>(1, (want + units - 1) / units)));
     const int tiles_per_split = (tiles + splits - 1) / splits;
     cp->split_tokens = tiles_per_split * 128;
     cp->splits = (prefix_len + cp->split_tokens - 1) / cp->split_tokens;
@@ -415,8 +448,10 @@ PKV_API pkv_status pkv_paged_attention_decode_shared_prefix(
                           : pkv::launch_prefix_tc_bf16(pp, tk, tv, block_size, pgrid, s);
     if (st != PKV_OK) return st;
 
-    // 2. each sequence's own tokens after the prefix, into the following slots, then
-    // 3. the log-sum-exp merge of all slots
+    // 2. each sequence's own tokens after the prefix, into the following slots: a
+    //    programmatic dependent launch that runs beside step 1 on the SMs it leaves
+    //    free (the two write disjoint slots); the grid completes only after step 1
+    // 3. the log-sum-exp merge of all slots, behind step 2
     pkv::DecodeParams p{};
     p.q = q;
     p.k_cache = k_cache;
@@ -443,12 +478,14 @@ PKV_API pkv_status pkv_paged_attention_decode_shared_prefix(
     p.tok_begin = prefix_len;
     p.slot_base = cp.splits;
     p.always_partial = 1;
+    p.wait_prior_grid = 1;  // overlaps the prefix tiles; the merge still follows both
     const int merge_rows = num_seqs * num_q_heads;
     const dim3 grid(static_cast<unsigned>(cp.suffix_parts), static_cast<unsigned>(p.items_y),
                     static_cast<unsigned>(num_seqs));
+    const pkv::DecodeMaps maps{};  // 16-bit forms stage by 1-D bulk copies
     return dtype == PKV_F16
-               ? pkv::launch_decode_f16(p, head_dim, block_size, cp.gh, grid, merge_rows, s)
-               : pkv::launch_decode_bf16(p, head_dim, block_size, cp.gh, grid, merge_rows, s);
+               ? pkv::launch_decode_f16(p, maps, head_dim, block_size, cp.gh, grid, merge_rows, s)
+               : pkv::launch_decode_bf16(p, maps, head_dim, block_size, cp.gh, grid, merge_rows, s);
 }
 
 }  // extern "C"

@@ -2,9 +2,9 @@
 #include "decode_launch.cuh"
 
 namespace pkv {
-pkv_status launch_decode_bf16(const DecodeParams &p, int head_dim, int block_size, int gh,
+pkv_status launch_decode_bf16(const DecodeParams &p, const DecodeMaps &m, int head_dim, int block_size, int gh,
                               dim3 grid, int merge_rows, cudaStream_t s) {
-    return launch_decode_typed<__nv_bfloat16>(p, head_dim, block_size, gh, grid, merge_rows, s);
+    return launch_decode_typed<__nv_bfloat16>(p, m, head_dim, block_size, gh, grid, merge_rows, s);
 }
 pkv_status launch_prefix_tc_bf16(const PrefixParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
                                  int block_size, dim3 grid, cudaStream_t s) {

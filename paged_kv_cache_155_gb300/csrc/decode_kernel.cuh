@@ -59,7 +59,12 @@
 //      head rows: half the MMAs and accumulators, so four CTAs fit an SM.
 #pragma once
 
+#include <cuda.h>
+
+#include <type_traits>
+
 #include "pkv_device.cuh"
+#include "pkv_tc.cuh"
 
 namespace pkv {
 
@@ -97,6 +102,18 @@ struct DecodeParams {
     int tok_begin;
     int slot_base;
     int always_partial;
+    // Set when this launch overlaps the kernel before it in the stream
+    // (programmatic dependent launch, the shared-prefix decode): the CTA with the
+    // last block index waits for that kernel before it exits, so this grid -- and
+    // whatever the stream runs after it -- completes only after that kernel.
+    int wait_prior_grid;
+};
+
+// Tensor maps of the two pool halves for the forms that stage by tiled TMA
+// copies (zero-filled otherwise).
+struct DecodeMaps {
+    CUtensorMap k;
+    CUtensorMap v;
 };
 
 // Partitions of a sequence of `len` tokens in a launch (at least one, possibly empty).
@@ -168,14 +185,23 @@ struct DecodeGeom {
     static constexpr int kStagesRaw = kBudget / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kMaxTableEntries = 1024;        // table slice per partition
+    // INT8 warp-MMA form at head_dim 128: K/V tiles arrive by tiled TMA copies with a
+    // 128-byte swizzle, whose 8-row atoms need 1024-byte-aligned stages
+    static constexpr bool kSwizzled = EB == 1 && kMmaForm && D == 128;
+    static constexpr int kAlignPad = kSwizzled ? 1024 : 0;
     static constexpr int kSmemBytes = kWarps * kStages * kStageBytes +
-                                      kWarps * kStages * 8 + kMaxTableEntries * 4;
+                                      kWarps * kStages * 8 + kMaxTableEntries * 4 + kAlignPad;
     static_assert(kIters >= 1, "tile smaller than a warp's token groups");
 };
 
 // T: query / output type; KT: cache storage type (T, or int8_t for the INT8 cache).
+// tmap_k / tmap_v: tiled tensor maps of the INT8 pool halves (box: one block's
+// TILE token rows of one head, 128 bytes each, 128-byte swizzle), used by the
+// INT8 warp-MMA form at head_dim 128; the other forms ignore them.
 template <typename T, typename KT, int D, int BS, int GH>
-__global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(128, 1) paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                                              const __grid_constant__ CUtensorMap tmap_v,
+                                                              const DecodeParams p) {
     constexpr bool kQuant = sizeof(KT) == 1;
     // 4 or 8 query heads per block: the products run as warp-level MMAs (the per-lane
     // loops would spend GH FMAs per element), INT8 codes on exact fp16 copies
@@ -190,7 +216,18 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
     static_assert(ITERS % IT_STEP == 0, "step must divide the stage");
     static_assert(GH * (D + 4) * 4 <= S * G::kStageBytes, "merge scratch must fit a warp's stages");
 
-    extern __shared__ __align__(128) unsigned char smem[];
+    // the merge kernel, launched behind this one, may start as this grid's CTAs run
+    pdl_trigger();
+    if (p.wait_prior_grid && blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 &&
+        blockIdx.z == gridDim.z - 1)
+        pdl_wait();  // uniform over the CTA; normally dispatched last, when nothing is left to wait for
+
+    // INT8 warp-MMA form at head_dim 128: stages filled by swizzled tiled TMA copies
+    constexpr bool kSwz = G::kSwizzled;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *smem = smem_raw;
+    if constexpr (kSwz)
+        smem += (1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u;
     unsigned char *stages = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + NW * S * G::kStageBytes);
     int32_t *tbl = reinterpret_cast<int32_t *>(smem + NW * S * G::kStageBytes + NW * S * 8);
@@ -253,8 +290,15 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                             (static_cast<int64_t>(kvh) * BS + r0) * D;
         unsigned char *dst = my_stages + s * G::kStageBytes;
         mbar_arrive_expect_tx(&my_bars[s], G::kStageBytes);
-        bulk_copy_g2s(dst, kc + off, G::kTileBytes, &my_bars[s], policy);
-        bulk_copy_g2s(dst + G::kTileBytes, vc + off, G::kTileBytes, &my_bars[s], policy);
+        if constexpr (kSwz) {
+            // token row t of the tile lands as 128 bytes whose 16-byte chunk c sits at
+            // chunk c ^ (t & 7)
+            tc::tma_load_3d(dst, &tmap_k, 0, kvh * BS + r0, b, &my_bars[s], policy);
+            tc::tma_load_3d(dst + G::kTileBytes, &tmap_v, 0, kvh * BS + r0, b, &my_bars[s], policy);
+        } else {
+            bulk_copy_g2s(dst, kc + off, G::kTileBytes, &my_bars[s], policy);
+            bulk_copy_g2s(dst + G::kTileBytes, vc + off, G::kTileBytes, &my_bars[s], policy);
+        }
     };
 
     const int my_chunks = nchunks > warp ? (nchunks - warp + NW - 1) / NW : 0;
@@ -345,9 +389,13 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
     uint32_t qa[KC][2];
     constexpr int RUN = kQuant ? 16 : 8;         // a lane's contiguous channels (16 bytes)
     float mqs = 1.f, mqb = 0.f;  // row mg's score scale 2^e and code-offset bias
+    // swizzled INT8 staging reads lane t's K chunks 2 t and 2 t + 1 (conflict-free
+    // under the swizzle), so its channels are 2 RUN t + RUN j + (0 .. RUN - 1), j = 0, 1
+    constexpr int kLaneStride = kSwz ? 2 * RUN : RUN;  // channel offset of lane t's first vector
+    constexpr int kVecStride = kSwz ? RUN : 4 * RUN;   // ... between its vectors j and j + 1
     if constexpr (kMma) {
         const T *qrow = static_cast<const T *>(p.q) +
-                        (static_cast<int64_t>(seq) * p.num_q_heads + hq0 + mg) * D + RUN * mt;
+                        (static_cast<int64_t>(seq) * p.num_q_heads + hq0 + mg) * D + kLaneStride * mt;
         if constexpr (kQuant) {
             // the query times scale * log2(e) and the K scale, then one power-of-two
             // exponent per head (its largest magnitude into [1/2, 1)) before fp16
@@ -359,8 +407,8 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                 for (int j = 0; j < D / (4 * RUN); ++j) {
 #pragma unroll
                     for (int v = 0; v < RUN; v += 8)
-                        Elem<T>::to_f32x8(*reinterpret_cast<const uint4 *>(qrow + 4 * RUN * j + v), f + RUN * j + v);
-                    const float *ksr = p.k_scale + kvh * D + 4 * RUN * j + RUN * mt;
+                        Elem<T>::to_f32x8(*reinterpret_cast<const uint4 *>(qrow + kVecStride * j + v), f + RUN * j + v);
+                    const float *ksr = p.k_scale + kvh * D + kVecStride * j + kLaneStride * mt;
 #pragma unroll
                     for (int v = 0; v < RUN / 4; ++v) {
                         const float4 a = reinterpret_cast<const float4 *>(ksr)[v];
@@ -466,13 +514,15 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                     // read by lanes (mg, .) as 16-byte vectors; two accumulators (even / odd
                     // k-chunks) halve the MMA chains
                     float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sodd[4] = {0.f, 0.f, 0.f, 0.f};
-                    const unsigned char *krow0 = kt + (tb + mg) * D + RUN * mt;
+                    const unsigned char *krow0 = kt + (tb + mg) * D;
                     const unsigned char *krow1 = krow0 + 8 * D;
 #pragma unroll
                     for (int j = 0; j < D / (4 * RUN); ++j) {
-                        const uint4 u0 = *reinterpret_cast<const uint4 *>(krow0 + 64 * j);
+                        // this lane's vector j of rows tb + mg and tb + 8 + mg (both = mg mod 8)
+                        const int kofs = kSwz ? ((((2 * mt + j) ^ mg) & 7) << 4) : RUN * mt + 64 * j;
+                        const uint4 u0 = *reinterpret_cast<const uint4 *>(krow0 + kofs);
                         uint4 u1 = make_uint4(0, 0, 0, 0);
-                        if constexpr (STEP == 16) u1 = *reinterpret_cast<const uint4 *>(krow1 + 64 * j);
+                        if constexpr (STEP == 16) u1 = *reinterpret_cast<const uint4 *>(krow1 + kofs);
                         const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w};
                         const uint32_t w1[4] = {u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
@@ -534,10 +584,11 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                     // channel (byte permute + lop3, code + 1152)
                     constexpr int VW = D / 32;  // 32-bit words of a lane's channels in a row
                     uint32_t x[STEP / 4][VW];
-                    const unsigned char *vrow = vt + (tb + 2 * mt) * D + (D / 8) * mg;
 #pragma unroll
                     for (int rr = 0; rr < STEP / 4; ++rr) {
-                        const unsigned char *src = vrow + ((rr >> 1) * 8 + (rr & 1)) * D;
+                        const int vr = tb + 2 * mt + (rr >> 1) * 8 + (rr & 1);  // token row
+                        // its D / 8 channels at (D / 8) mg: chunk mg, at chunk mg ^ (row & 7) swizzled
+                        const unsigned char *src = vt + vr * D + (kSwz ? (((mg ^ vr) & 7) << 4) : (D / 8) * mg);
                         if constexpr (VW == 4) {
                             const uint4 u = *reinterpret_cast<const uint4 *>(src);
                             x[rr][0] = u.x;
@@ -646,6 +697,18 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
                             x[r][4 * v + 1] = u.y;
                             x[r][4 * v + 2] = u.z;
                             x[r][4 * v + 3] = u.w;
+                        }
+                    }
+                    if (tb + STEP > valid) {  // warp-uniform: a step that ends past the context
+                        // rows past the context are unwritten slots of the last block; their
+                        // weight is 0, but 0 * NaN or 0 * Inf would still poison O, so the
+                        // rows themselves are zeroed before they reach the MMA
+#pragma unroll
+                        for (int r = 0; r < STEP / 4; ++r) {
+                            if (tb + (r >> 1) * 8 + 2 * mt + (r & 1) >= valid) {
+#pragma unroll
+                                for (int w = 0; w < VW; ++w) x[r][w] = 0u;
+                            }
                         }
                     }
 #pragma unroll
@@ -904,11 +967,21 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const DecodeParams
 // Log-sum-exp merge of the partitions of each (sequence, query head):
 //   M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L.
 // One warp per (sequence, query head); sequences that fit one partition were
-// written by the main kernel and are skipped.
+// written by the main kernel and are skipped.  Lane q reads partition q's m and
+// l, so the maximum and the weights take one round of loads and shuffles; the
+// partial outputs (D / 32 values per lane and partition) are then read
+// kMergeUnroll partitions at a time, all in flight together.  Launched behind
+// the decode kernel (programmatic dependent launch): it waits for that grid's
+// partials before reading any.
+constexpr int kMergeUnroll = 8;
+
 template <typename T, int D>
 __global__ void __launch_bounds__(128) paged_decode_merge_kernel(const DecodeParams p,
                                                                  int num_rows) {
+    pdl_wait();
     constexpr int PER_LANE = D / 32;
+    using Part = typename std::conditional<PER_LANE == 4, float4, float2>::type;
+    static_assert(PER_LANE == 4 || PER_LANE == 2, "head_dim 128 or 64");
     const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= num_rows) return;
@@ -922,19 +995,40 @@ __global__ void __launch_bounds__(128) paged_decode_merge_kernel(const DecodePar
     if (nparts <= 1 && !p.always_partial) return;           // written by the decode kernel
     const int64_t base = static_cast<int64_t>(row) * p.num_partitions;
     float mmax = -INFINITY;
-    for (int q = 0; q < nparts; ++q) mmax = fmaxf(mmax, p.ws_m[base + q]);
+    for (int q = lane; q < nparts; q += 32) mmax = fmaxf(mmax, p.ws_m[base + q]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
     float lsum = 0.f;
     float o[PER_LANE];
 #pragma unroll
     for (int e = 0; e < PER_LANE; ++e) o[e] = 0.f;
-    for (int q = 0; q < nparts; ++q) {
-        const float mq = p.ws_m[base + q];
-        const float w = mq == -INFINITY ? 0.f : fast_exp2(mq - mmax);
-        lsum += w * p.ws_l[base + q];
-        const float *src = p.ws_o + (base + q) * D + lane * PER_LANE;
+    const Part *parts = reinterpret_cast<const Part *>(p.ws_o + base * D) + lane;  // slot q at q * 32
+    for (int q0 = 0; q0 < nparts; q0 += 32) {
+        const int cnt = min(32, nparts - q0);
+        float w = 0.f;  // this lane's partition q0 + lane
+        if (lane < cnt) {
+            const float mq = p.ws_m[base + q0 + lane];
+            w = mq == -INFINITY ? 0.f : fast_exp2(mq - mmax);
+            lsum += w * p.ws_l[base + q0 + lane];
+        }
+        for (int j0 = 0; j0 < cnt; j0 += kMergeUnroll) {
+            Part v[kMergeUnroll];
 #pragma unroll
-        for (int e = 0; e < PER_LANE; ++e) o[e] += w * src[e];
+            for (int u = 0; u < kMergeUnroll; ++u)
+                if (j0 + u < cnt) v[u] = parts[static_cast<int64_t>(q0 + j0 + u) * 32];
+#pragma unroll
+            for (int u = 0; u < kMergeUnroll; ++u) {
+                const float wu = __shfl_sync(0xffffffffu, w, (j0 + u) & 31);
+                if (j0 + u < cnt) {
+                    const float *f = reinterpret_cast<const float *>(&v[u]);
+#pragma unroll
+                    for (int e = 0; e < PER_LANE; ++e) o[e] = fmaf(wu, f[e], o[e]);
+                }
+            }
+        }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
     T *dst = static_cast<T *>(p.out) + static_cast<int64_t>(row) * D + lane * PER_LANE;
 #pragma unroll
     for (int e = 0; e < PER_LANE; ++e) dst[e] = Elem<T>::from_f32(lsum > 0.f ? o[e] / lsum : 0.f);

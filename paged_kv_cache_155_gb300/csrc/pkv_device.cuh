@@ -118,6 +118,16 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
+// Programmatic dependent launch.  pdl_trigger: this CTA no longer holds back
+// the next kernel of the stream if that kernel was launched with programmatic
+// stream serialisation (it may start on free SMs while this grid runs).
+// pdl_wait: block until the grids this one was launched behind have completed
+// and their memory is visible.  Both are no-ops without such a launch.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -26,6 +26,12 @@ void count_launch();
 bool encode_half_map(CUtensorMap *map, const void *base, int64_t num_blocks,
                      int64_t block_stride_elems, int num_kv_heads, int block_size, pkv_dtype dt);
 
+// Tiled tensor map of one half (K or V) of an INT8 pool with head_dim 128 for
+// 3-D TMA loads: dims (128 codes, num_kv_heads * block_size rows, num_blocks),
+// boxes of one block's rows of one head (128 bytes each), 128-byte swizzled.
+bool encode_i8_half_map(CUtensorMap *map, const void *base, int64_t num_blocks,
+                        int64_t block_stride_elems, int num_kv_heads, int block_size);
+
 // Tiled tensor map of the prefill queries [num_rows][num_q_heads][128] for
 // 3-D TMA loads: boxes of `tokens` tokens x `group` query heads x 64 columns,
 // 128-byte swizzled (group <= 256, tokens <= 256).

@@ -16,15 +16,17 @@
 //   S  = Q . K^T      A = Q tile (K-major), B = K tile (K-major)
 //   O += P . V        A = P (K-major), B = V tile (MN-major: head_dim contiguous)
 // S is double-buffered in TMEM (2 x 128 columns), O accumulates in TMEM (128
-// columns).  A row's softmax is local to one thread (TMEM lane = query row).
-// The row maximum used for P is raised only when a tile's maximum exceeds it
-// by more than kRescaleLog2 (then O and l are rescaled in place), so P <=
-// 2^kRescaleLog2.  P is rounded to the input type for the MMA; l adds the fp32
-// values (unbiased rounding, relative error 2^-9 per weight at most).
+// columns).  A row's softmax belongs to one pair of threads (TMEM lane = query
+// row), each taking 64 of the tile's 128 columns; the pair exchanges its
+// partial row maxima through spare TMEM columns, so both halves use one
+// reference maximum.  That maximum is raised only when a tile's maximum
+// exceeds it by more than kRescaleLog2 (then O and l are rescaled in place),
+// so P <= 2^kRescaleLog2.  P is rounded to the input type for the MMA; l adds
+// the fp32 values (unbiased rounding, relative error 2^-9 per weight at most).
 //
-// Warps: 0 / 6 TMA producers of the K ring and the V ring (2 slots each, 3-D
+// Warps: 0 / 10 TMA producers of the K ring and the V ring (2 slots each, 3-D
 // tiled copies with 128-byte swizzle), 1 TMEM owner + MMA issuer (event-driven),
-// 2-5 softmax.
+// 2-9 softmax in pairs (warps w and w + 4 share TMEM lane quarter w & 3).
 #pragma once
 
 #include <cuda.h>
@@ -81,6 +83,7 @@ struct PrefixParams {
 };
 
 struct PrefixLayout {
+    static constexpr int kThreads = 352;               // 11 warps (roles below)
     static constexpr int kTile = 128;
     static constexpr int kHalf = 128 * 128;            // 128 rows x 128 B
     static constexpr int kPanel = 2 * kHalf;           // 128 rows x 128 16-bit values
@@ -89,20 +92,21 @@ struct PrefixLayout {
     static constexpr int kOffV = kOffK + 2 * kPanel;   // 2 slots
     static constexpr int kOffP = kOffV + 2 * kPanel;   // 2 buffers
     static constexpr int kOffBar = kOffP + 2 * kPanel;
-    static constexpr int kNumBars = 17;
+    static constexpr int kNumBars = 25;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kSmemBytes = kBytes + 1024;
-    static constexpr uint32_t kTmemCols = 512;           // S[2] at 0 / 128, O at 256
+    static constexpr uint32_t kTmemCols = 512;           // S[2] at 0 / 128, O at 256, exchange 384
+    static constexpr uint32_t kXchgCol = 384;            // spare TMEM columns for the pairs
     static constexpr float kRescaleLog2 = 8.f;
 };
 
 template <typename T, int BS>
-__global__ void __launch_bounds__(224, 1)
+__global__ void __launch_bounds__(PrefixLayout::kThreads, 1)
     paged_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const PrefixParams p) {
     using L = PrefixLayout;
-    constexpr int TILE = L::kTile, D = 128;
+    constexpr int TILE = L::kTile, D = 128, kThreads = L::kThreads;
     constexpr bool kBF16 = !std::is_same<T, __half>::value;
     static_assert(TILE / BS <= 32, "one table entry per producer lane");
 
@@ -113,9 +117,13 @@ __global__ void __launch_bounds__(224, 1)
     uint64_t *k_full = bars, *k_empty = bars + 2, *v_full = bars + 4, *v_empty = bars + 6;
     uint64_t *s_full = bars + 8, *s_empty = bars + 10, *p_full = bars + 12, *o_done = bars + 14;
     uint64_t *drain_bar = bars + 16;
+    uint64_t *pair_bar = bars + 17;  // [quarter][parity]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
 
+    // the suffix decode, launched behind this kernel, may start on the SMs this grid
+    // leaves free (its last CTA waits for this grid before it exits)
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row_tile = blockIdx.x, kvh = blockIdx.y, split = blockIdx.z;
     const int tok_lo = split * p.split_tokens;
@@ -130,11 +138,12 @@ __global__ void __launch_bounds__(224, 1)
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 4);
-            mbar_init(&p_full[i], 4);
+            mbar_init(&s_empty[i], 8);
+            mbar_init(&p_full[i], 8);
             mbar_init(&o_done[i], 1);
         }
         mbar_init(drain_bar, 1);
+        for (int i = 0; i < 8; ++i) mbar_init(&pair_bar[i], 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -143,19 +152,32 @@ __global__ void __launch_bounds__(224, 1)
         tc::tmem_relinquish();
     }
     // query rows of this tile -> Q panel (K-major, 128-byte swizzle); rows past the
-    // batch are zero
-    for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
-        const int r = i >> 4, c8 = i & 15;
-        const int grow = row_tile * 128 + r;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (grow < p.rows) {
-            const int seq = grow / p.group, g = grow - seq * p.group;
-            const T *src = static_cast<const T *>(p.q) +
-                           (static_cast<int64_t>(seq) * p.num_q_heads + kvh * p.group + g) * D;
-            v = *reinterpret_cast<const uint4 *>(src + c8 * 8);
+    // batch are zero.  Every thread issues all of its loads before its first store,
+    // so the panel costs about one global-memory latency, not one per vector.
+    {
+        constexpr int kItems = 128 * 16, kPer = (kItems + kThreads - 1) / kThreads;
+        uint4 v[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int i = threadIdx.x + u * kThreads;
+            const int r = i >> 4, c8 = i & 15;
+            const int grow = row_tile * 128 + r;
+            v[u] = make_uint4(0, 0, 0, 0);
+            if (i < kItems && grow < p.rows) {
+                const int seq = grow / p.group, g = grow - seq * p.group;
+                const T *src = static_cast<const T *>(p.q) +
+                               (static_cast<int64_t>(seq) * p.num_q_heads + kvh * p.group + g) * D;
+                v[u] = *reinterpret_cast<const uint4 *>(src + c8 * 8);
+            }
         }
-        *reinterpret_cast<uint4 *>(sm + L::kOffQ + (c8 >> 3) * L::kHalf + r * 128 +
-                                   (((c8 & 7) ^ (r & 7)) << 4)) = v;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int i = threadIdx.x + u * kThreads;
+            const int r = i >> 4, c8 = i & 15;
+            if (i < kItems)
+                *reinterpret_cast<uint4 *>(sm + L::kOffQ + (c8 >> 3) * L::kHalf + r * 128 +
+                                           (((c8 & 7) ^ (r & 7)) << 4)) = v[u];
+        }
     }
     if (warp == 0 && lane == 0) {
         tc::prefetch_tensormap(&tmap_k);
@@ -167,11 +189,11 @@ __global__ void __launch_bounds__(224, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 || warp == 6) {
-        // ===================== TMA producers: K (warp 0), V (warp 6) =====================
+    if (warp == 0 || warp == 10) {
+        // ===================== TMA producers: K (warp 0), V (warp 10) =====================
         // Separate producers so a K tile never waits behind a V slot that its PV still
         // holds; each loads the next tile's table entries while it waits for a slot.
-        const int kv = warp == 6;
+        const int kv = warp == 10;
         uint64_t *full = kv ? v_full : k_full;
         uint64_t *empty = kv ? v_empty : k_empty;
         const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
@@ -294,72 +316,97 @@ __global__ void __launch_bounds__(224, 1)
         }
         __syncwarp();
     } else {
-        // ===================== softmax (warps 2..5): thread = query row =====================
+        // ===================== softmax (warps 2..9): thread = query row, 64 columns =====================
         const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
+        const int half = warp >= 6 ? 1 : 0;  // tile columns 64 half .. +63
+        const int c0 = half * 64;
+        const int r = quarter * 32 + lane;   // row within the tile = TMEM lane
         const int grow = row_tile * 128 + r;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t xchg = lane_base + L::kXchgCol;
+        // One value per row between the two warps of the pair: step s writes column
+        // 2 (s & 1) + half and reads the partner's; a warp reuses a column two steps
+        // later, after the partner has passed the step in between.
+        auto exchange = [&](int step, float mine, float &other) -> bool {
+            const int par = step & 1;
+            tc::tmem_st_x1(xchg + 2 * par + half, mine);
+            tc::tmem_st_wait();
+            tc::fence_before_sync();
+            __syncwarp();
+            uint64_t *pb = &pair_bar[quarter * 2 + par];
+            if (lane == 0) mbar_arrive(pb);
+            if (!tc_wait_warp(pb, (step >> 1) & 1, abort_flag, p.status)) return false;
+            tc::fence_after_sync();
+            other = tc::tmem_ld_x1(xchg + 2 * par + (1 - half));
+            tc::tmem_ld_wait();
+            return true;
+        };
+        const bool pos_scale = p.scale_log2 > 0.f;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
+        int xs = 0;  // pair exchanges so far
         for (int j = 0; j < ntiles && ok; ++j) {
             const int b = j & 1;
             const int t0 = tok_lo + j * TILE;
-            const int valid = min(TILE, tok_hi - t0);
+            const int valid = min(TILE, tok_hi - t0);  // >= 1: column 0 is always in the prefix
+            const int vh = max(0, min(64, valid - c0));  // ... of this half
             if (!tc_wait_warp(&s_full[b], (j >> 1) & 1, abort_flag, p.status)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            // this row's 128 scores, read from TMEM once; tile maximum of the scaled
-            // scores = the extreme raw score times the scale (max for a positive
-            // scale, min otherwise)
-            float x[TILE];
+            // this row's 64 scores of the half, read from TMEM once; the half's extreme
+            // raw score (max for a positive scale, min otherwise; a half past the prefix
+            // end contributes the neutral infinity)
+            float x[64];
 #pragma unroll
-            for (int c = 0; c < TILE; c += 16) tc::tmem_ld_x16(lane_base + 128 * b + c, x + c);
+            for (int c = 0; c < 64; c += 16) tc::tmem_ld_x16(lane_base + 128 * b + c0 + c, x + c);
             tc::tmem_ld_wait();
-            const bool full = valid == TILE;  // uniform over the CTA
-            const bool pos_scale = p.scale_log2 > 0.f;
-            float ext = x[0];
+            const bool full = vh == 64;  // uniform over the warp
+            float ext;
             if (full) {
+                ext = x[0];
 #pragma unroll
-                for (int i = 1; i + 1 < TILE; i += 2)
+                for (int i = 1; i + 1 < 64; i += 2)
                     ext = pos_scale ? fmax3(ext, x[i], x[i + 1]) : fmin3(ext, x[i], x[i + 1]);
-                ext = pos_scale ? fmaxf(ext, x[TILE - 1]) : fminf(ext, x[TILE - 1]);
+                ext = pos_scale ? fmaxf(ext, x[63]) : fminf(ext, x[63]);
             } else {
+                ext = pos_scale ? -INFINITY : INFINITY;
 #pragma unroll
-                for (int i = 1; i < TILE; ++i)
-                    if (i < valid) ext = pos_scale ? fmaxf(ext, x[i]) : fminf(ext, x[i]);
+                for (int i = 0; i < 64; ++i)
+                    if (i < vh) ext = pos_scale ? fmaxf(ext, x[i]) : fminf(ext, x[i]);
             }
-            const float tmax = ext * p.scale_log2;
+            float ext_other;
+            if (!exchange(xs++, ext, ext_other)) {
+                ok = false;
+                break;
+            }
+            // both threads of the pair derive the same tile maximum and reference
+            const float tmax = (pos_scale ? fmaxf(ext, ext_other) : fminf(ext, ext_other)) * p.scale_log2;
             // the reference maximum moves only by more than kRescaleLog2; TMEM loads and
-            // stores are warp-wide, so the warp rescales if any of its rows must
+            // stores are warp-wide, so the warp rescales if any of its rows must (the
+            // two warps of a pair see the same rows, so they decide alike)
             const float new_ref = tmax > m_ref + L::kRescaleLog2 ? tmax : m_ref;
             const float alpha = fast_exp2(m_ref - new_ref);  // 1 if unchanged, 0 on the first tile
             if (__any_sync(0xffffffffu, new_ref != m_ref)) {
                 if (j > 0) {
-                    // O holds tiles < j: wait for PV(j-1), rescale O in TMEM
+                    // O holds tiles < j: wait for PV(j-1), rescale this half of O in TMEM
                     if (!tc_wait_warp(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after_sync();
 #pragma unroll
-                    for (int c = 0; c < D; c += 16) {
+                    for (int c = 0; c < 64; c += 16) {
                         float o[16];
-                        tc::tmem_ld_x16(lane_base + 256 + c, o);
+                        tc::tmem_ld_x16(lane_base + 256 + c0 + c, o);
                         tc::tmem_ld_wait();
                         uint32_t w[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(o[i] * alpha);
-                        asm volatile(
-                            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, "
-                            "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(lane_base + 256 + c),
-                            "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-                            "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]),
-                            "r"(w[13]), "r"(w[14]), "r"(w[15])
-                            : "memory");
+                        tc::tmem_st_x16(lane_base + 256 + c0 + c, w);
                     }
-                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    tc::tmem_st_wait();
                 }
                 l *= alpha;
                 m_ref = new_ref;
@@ -369,14 +416,14 @@ __global__ void __launch_bounds__(224, 1)
                 ok = false;
                 break;
             }
-            // P = 2^(s - m_ref) (0 past the prefix end), rounded to T into the K-major
-            // P panel; the row sum l adds the fp32 values
-            unsigned char *prow = sm + L::kOffP + b * L::kPanel + r * 128;
+            // P = 2^(s - m_ref) (0 past the prefix end), rounded to T into this half of
+            // the K-major P panel; the row sum l adds the fp32 values
+            unsigned char *prow = sm + L::kOffP + b * L::kPanel + half * L::kHalf + r * 128;
             float l0 = 0.f, l1 = 0.f;
-            // two copies of the loop, so full tiles carry no per-column mask
+            // two copies of the loop, so full halves carry no per-column mask
             auto weights = [&](auto masked) {
 #pragma unroll
-                for (int c8 = 0; c8 < TILE / 8; ++c8) {
+                for (int c8 = 0; c8 < 8; ++c8) {
                     uint32_t packed[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -387,13 +434,13 @@ __global__ void __launch_bounds__(224, 1)
                         float p0 = fast_exp2(e0);
                         float p1 = fast_exp2(e1);
                         if constexpr (decltype(masked)::value) {
-                            p0 = t < valid ? p0 : 0.f;
-                            p1 = t + 1 < valid ? p1 : 0.f;
+                            p0 = t < vh ? p0 : 0.f;
+                            p1 = t + 1 < vh ? p1 : 0.f;
                         }
                         add_f32x2(l0, l1, p0, p1);
                         packed[i] = Elem<T>::pack2(p0, p1);
                     }
-                    *reinterpret_cast<uint4 *>(prow + (c8 >> 3) * L::kHalf + (((c8 & 7) ^ (r & 7)) << 4)) =
+                    *reinterpret_cast<uint4 *>(prow + ((c8 ^ (r & 7)) << 4)) =
                         make_uint4(packed[0], packed[1], packed[2], packed[3]);
                 }
             };
@@ -402,18 +449,16 @@ __global__ void __launch_bounds__(224, 1)
             l += l0 + l1;
             tc::fence_before_sync();
             if (valid < TILE) {
-                // rows of V past the prefix end: zero them so 0 * stale never reaches the MMA
+                // rows of V past the prefix end: zero them (this thread: row r, this
+                // half's 64 channels) so 0 * stale never reaches the MMA
                 if (!tc_wait_warp(&v_full[b], (j >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 if (r >= valid) {
-                    unsigned char *vrow = sm + L::kOffV + b * L::kPanel + r * 128;
+                    uint4 *vrow = reinterpret_cast<uint4 *>(sm + L::kOffV + b * L::kPanel + half * L::kHalf + r * 128);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            reinterpret_cast<uint4 *>(vrow + c * L::kHalf)[i] = make_uint4(0, 0, 0, 0);
+                    for (int i = 0; i < 8; ++i) vrow[i] = make_uint4(0, 0, 0, 0);
                 }
             }
             fence_proxy_async_smem();
@@ -423,9 +468,12 @@ __global__ void __launch_bounds__(224, 1)
                 mbar_arrive(&p_full[b]);
             }
         }
-        // final: O row -> workspace slot `split` of every (sequence, query head) row.
-        // TMEM loads are warp-wide: every lane loads, only rows of the batch store.
+        // final: the pair's row sum, then this half of the O row -> workspace slot
+        // `split` of the row's (sequence, query head).  TMEM loads are warp-wide:
+        // every lane loads, only rows of the batch store.
         if (ntiles > 0) {
+            float l_other = 0.f;
+            if (ok) ok = exchange(xs++, l, l_other);
             if (ok) ok = tc_wait_warp(&o_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag, p.status);
             if (ok) {
                 tc::fence_after_sync();
@@ -437,20 +485,20 @@ __global__ void __launch_bounds__(224, 1)
                                   p.num_partitions + split;
                 }
 #pragma unroll
-                for (int c = 0; c < D; c += 16) {
+                for (int c = 0; c < 64; c += 16) {
                     float o[16];
-                    tc::tmem_ld_x16(lane_base + 256 + c, o);
+                    tc::tmem_ld_x16(lane_base + 256 + c0 + c, o);
                     tc::tmem_ld_wait();
                     if (mine) {
-                        float *dst = p.ws_o + prow_ws * D + c;
+                        float *dst = p.ws_o + prow_ws * D + c0 + c;
 #pragma unroll
                         for (int i = 0; i < 16; i += 4)
                             *reinterpret_cast<float4 *>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
                     }
                 }
-                if (mine) {
+                if (mine && half == 0) {
                     p.ws_m[prow_ws] = m_ref;
-                    p.ws_l[prow_ws] = l;
+                    p.ws_l[prow_ws] = l + l_other;
                 }
             }
         }

@@ -56,7 +56,7 @@ def run_step(wl, partition_size=0, tables=None):
     position len-1, then paged decode.  Returns out (device)."""
     k_cache, v_cache = pkv.split_pool(wl.kv)
     bt = wl.block_tables if tables is None else tables
-    slots = pkv.slot_mapping(bt.cpu(), wl.new_positions.cpu(), wl.block_size).to(wl.kv.device)
+    slots = pkv.slot_mapping(bt, wl.new_positions, wl.block_size, num_blocks=wl.num_blocks)
     pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
     return pkv.paged_attention_decode(wl.q, k_cache, v_cache, bt, wl.context_lens, wl.scale,
                                       max_context_len=int(wl.context_lens.max().item()),
@@ -78,7 +78,7 @@ def run_step_int8(wl, partition_size=0, tables=None):
     new token at position len-1, then paged decode.  Returns out (device)."""
     k_cache, v_cache = pkv.split_pool(wl.kv)
     bt = wl.block_tables if tables is None else tables
-    slots = pkv.slot_mapping(bt.cpu(), wl.new_positions.cpu(), wl.block_size).to(wl.kv.device)
+    slots = pkv.slot_mapping(bt, wl.new_positions, wl.block_size, num_blocks=wl.num_blocks)
     pkv.reshape_and_cache_int8(wl.k_new, wl.v_new, slots, k_cache, v_cache, wl.k_scale,
                                wl.v_scale)
     return pkv.paged_attention_decode_int8(wl.q, k_cache, v_cache, wl.k_scale, wl.v_scale, bt,
@@ -117,9 +117,9 @@ def run_prefill(wl, kv_splits=0):
     k_cache, v_cache = pkv.split_pool(wl.kv)
     n = int(wl.query_start[-1])
     if n:
-        rows_tables = wl.block_tables.cpu()[wl.row_seq.cpu()]
-        slots = pkv.slot_mapping(rows_tables, wl.new_positions.cpu(), wl.block_size)
-        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots.to(wl.kv.device), k_cache, v_cache)
+        slots = pkv.slot_mapping(wl.block_tables, wl.new_positions, wl.block_size,
+                                 token_rows=wl.row_seq, num_blocks=wl.num_blocks)
+        pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
     out = torch.zeros_like(wl.q)
     return pkv.paged_attention_prefill(wl.q, k_cache, v_cache, wl.block_tables, wl.query_start,
                                        wl.context_lens, wl.scale, out,
@@ -152,3 +152,35 @@ def oracle_prefill_step(pool_bits: np.ndarray, wl, rows=None):
     return oracle.paged_prefill(sel_q, flat, flat[half:], 2 * half, sel_bt,
                                 np.arange(len(rows) + 1), sel_len, wl.num_kv_heads, wl.block_size,
                                 wl.scale, dtype_code(wl.dtype))
+
+
+# ---------------------------------------------------------------- stale slots
+# NaN, +Inf and -Inf bit patterns of each 16-bit type
+_NONFINITE = {torch.float16: (0x7E00, 0x7C00, 0xFC00),
+              torch.bfloat16: (0x7FC0, 0x7F80, 0xFF80)}
+
+
+def poison_unused_slots(kv: torch.Tensor, tables, lens, block_size: int) -> int:
+    """Overwrite every pool slot that no sequence's context covers -- the tail rows
+    of each last block and every block no table reaches -- with NaN, +Inf and -Inf
+    in turn, in K and V and for every KV head (a pool from torch.empty may hold
+    anything there).  Attention must not read them: the result stays that of the
+    covered tokens.  Returns the number of poisoned slots."""
+    nb = kv.shape[0]
+    covered = np.zeros((nb, block_size), dtype=bool)
+    tables = np.asarray(tables.cpu() if torch.is_tensor(tables) else tables)
+    lens = np.asarray(lens.cpu() if torch.is_tensor(lens) else lens)
+    for i, n in enumerate(lens.tolist()):
+        nblk = -(-int(n) // block_size)
+        if nblk == 0:
+            continue
+        blocks = tables[i, :nblk]
+        covered[blocks[:-1], :] = True
+        covered[blocks[-1], :int(n) - (nblk - 1) * block_size] = True
+    bits = to_bits(kv.cpu())
+    pats = _NONFINITE[kv.dtype]
+    bad = np.argwhere(~covered)
+    for k, (b, o) in enumerate(bad):
+        bits[b, :, :, o, :] = pats[k % 3]
+    kv.copy_(torch.from_numpy(bits.view(np.int16)).view(kv.dtype).to(kv.device))
+    return len(bad)

@@ -254,6 +254,61 @@ def test_host_slot_helper_matches_oracle_slot_rule():
                 assert got[i] == oracle.slot_for_position(tables[i].numpy(), int(pos[i]), bs)
 
 
+def _host_slots(lib, tables, pos, bs, rows=None, num_blocks=1 << 40):
+    bt = np.ascontiguousarray(tables, dtype=np.int32)
+    p = np.ascontiguousarray(pos, dtype=np.int64)
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.full(p.shape[0], 12345, dtype=np.int64)
+    st = lib.pkv_slot_mapping_host(bt.ctypes.data, bt.shape[0], bt.shape[1],
+                                   None if r is None else r.ctypes.data, p.ctypes.data,
+                                   p.shape[0], bs, num_blocks, out.ctypes.data)
+    return st, out
+
+
+def test_slot_mapping_host_worked_example(lib):
+    """The worked table of "KV Cache与PagedAttention深度解析" §4.2 through the C ABI:
+    positions 0 / 15 / 16 / 47 / 95 / 96 / 99 land where the page's table puts them,
+    and a negative position is padding."""
+    from tests.conftest import read_golden
+    gold = read_golden("worked_example_block_table.txt")
+    table = [int(x) for x in gold["block_table"].split()]
+    bs = int(gold["block_size"])
+    pos = [0, 15, 16, 47, 95, 96, 99, -1]
+    st, out = _host_slots(lib, [table] * len(pos), pos, bs)
+    assert st == 0
+    for t, slot in zip(pos, out):
+        if t < 0:
+            assert slot == -1
+            continue
+        blk, off = (int(x) for x in gold[f"token_{t}"].split())
+        assert (slot // bs, slot % bs) == (blk, off)
+    # one table row shared by every token through token_rows
+    st, out2 = _host_slots(lib, [table], pos, bs, rows=[0] * len(pos))
+    assert st == 0 and np.array_equal(out, out2)
+
+
+def test_slot_mapping_host_matches_oracle_and_flags_bad_inputs(lib):
+    g = np.random.default_rng(3)
+    for bs in (8, 16, 32):
+        tables = g.integers(0, 1000, (9, 40)).astype(np.int32)
+        pos = g.integers(0, 40 * bs, 9)
+        pos[4] = -3
+        rows = g.integers(0, 9, 9)
+        st, out = _host_slots(lib, tables, pos, bs, rows=rows, num_blocks=1000)
+        assert st == 0
+        ref = [-1 if p < 0 else oracle.slot_for_position(tables[r], int(p), bs)
+               for r, p in zip(rows, pos)]
+        assert out.tolist() == ref
+    tables = np.array([[3, 1], [0, 2]], dtype=np.int32)
+    # a position past the table, a table entry past the pool, a token row past the table
+    for pos, rows, nb in (([32, 1], None, 4), ([1, 17], None, 2), ([1, 1], [0, 2], 4)):
+        st, out = _host_slots(lib, tables, pos, 16, rows=rows, num_blocks=nb)
+        assert st == INVALID
+        assert -1 in out.tolist() and 12345 not in out.tolist()
+    st, _ = _host_slots(lib, tables[:1], [0, 1], 16)   # fewer rows than tokens, no token_rows
+    assert st == INVALID
+
+
 def test_package_import_does_not_need_a_gpu():
     import paged_kv_cache_155_gb300 as pkv
     assert callable(pkv.paged_attention_decode)

@@ -59,6 +59,46 @@ def test_reshape_and_cache_worked_example_positions():
         assert torch.equal(kv[blk, 1, :, off], v_new[n])
 
 
+def test_slot_mapping_kernel_worked_example_and_oracle():
+    """pkv_slot_mapping on the device: the worked table [7,2,9,1,5,8,3] puts positions
+    0 / 15 / 16 / 99 at slots of (7,0), (7,15), (2,0), (3,3); random tables and token
+    rows match the oracle's slot rule exactly; negative positions give -1."""
+    dev = device()
+    table = torch.tensor([[7, 2, 9, 1, 5, 8, 3]], dtype=torch.int32, device=dev)
+    pos = torch.tensor([0, 15, 16, 99, -1], device=dev)
+    rows = torch.zeros(5, dtype=torch.int64, device=dev)
+    got = pkv.slot_mapping(table, pos, 16, token_rows=rows, num_blocks=10).cpu().tolist()
+    assert got == [7 * 16, 7 * 16 + 15, 2 * 16, 3 * 16 + 3, -1]
+    g = torch.Generator().manual_seed(9)
+    for bs in (8, 16, 32):
+        tables = torch.randint(0, 5000, (37, 64), generator=g, dtype=torch.int32)
+        pos = torch.randint(-2, 64 * bs, (1000,), generator=g)
+        rows = torch.randint(0, 37, (1000,), generator=g)
+        got = pkv.slot_mapping(tables.to(dev), pos.to(dev), bs, token_rows=rows.to(dev),
+                               num_blocks=5000)
+        torch.cuda.synchronize()
+        check_no_device_flags(dev)
+        ref = [-1 if p < 0 else oracle.slot_for_position(tables[r].numpy(), int(p), bs)
+               for r, p in zip(rows.tolist(), pos.tolist())]
+        assert got.cpu().tolist() == ref
+        host = pkv.slot_mapping(tables, pos, bs, token_rows=rows, num_blocks=5000)
+        assert host.tolist() == ref
+
+
+def test_slot_mapping_kernel_flags_bad_inputs():
+    dev = device()
+    tables = torch.tensor([[3, 1], [0, 2]], dtype=torch.int32, device=dev)
+    for pos, rows, nb, flag in (([32, 1], None, 4, "slot"), ([1, 17], None, 2, "block_table"),
+                                ([1, 1], [0, 2], 4, "slot")):
+        r = None if rows is None else torch.tensor(rows, device=dev)
+        got = pkv.slot_mapping(tables, torch.tensor(pos, device=dev), 16, token_rows=r,
+                               num_blocks=nb)
+        flags, names = pkv.get_device_error(dev)
+        assert flag in names
+        assert -1 in got.cpu().tolist()
+    check_no_device_flags(dev)
+
+
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 @pytest.mark.parametrize("hkv,bs,d", [(8, 32, 128), (4, 16, 64), (32, 16, 128), (1, 8, 64)])
 def test_copy_blocks_bit_exact(dtype, hkv, bs, d):

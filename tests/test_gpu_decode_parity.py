@@ -14,7 +14,7 @@ import torch
 import paged_kv_cache_155_gb300 as pkv
 from paged_kv_cache_155_gb300.workloads import make_decode_workload
 from tests._gpu_helpers import (assert_close, check_no_device_flags, device, host_pool_bits,
-                                oracle_decode, oracle_step_pool, run_step)
+                                oracle_decode, oracle_step_pool, poison_unused_slots, run_step)
 from tests._paged_helpers import to_bits
 
 pytestmark = pytest.mark.gpu
@@ -50,6 +50,26 @@ def test_decode_shapes(dtype, d, bs, hq, hkv, longest):
     _check_step(wl)
 
 
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 128), (8, 4, 128), (16, 4, 128), (32, 4, 128),
+                                      (64, 4, 128), (32, 4, 64)])
+def test_decode_ignores_nonfinite_unused_slots(dtype, bs, hq, hkv, d):
+    """Slots past each context (the unwritten tail of a last block) and blocks no table
+    reaches hold NaN / +Inf / -Inf: the output is still the oracle's, finite, for the
+    per-lane loops (groups 1, 2) and the warp-MMA forms (groups 4, 8, 16), one
+    partition and several."""
+    dev = device()
+    lens = [1, bs - 1, bs + 1, 5 * bs + 3, 300, 17, 2 * bs]
+    need = sum(-(-n // bs) for n in lens)
+    wl = make_decode_workload(num_seqs=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                              block_size=bs, context_lens=lens, dtype=dtype, seed=hq + bs + d,
+                              device=str(dev), num_blocks=need + 6)
+    assert poison_unused_slots(wl.kv, wl.block_tables, wl.context_lens, bs) > 6 * bs
+    _check_step(wl)
+    _check_step(wl, partition_size=4 * bs)
+
+
 @pytest.mark.parametrize("partition", [16, 32, 48, 256, 1024])
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 def test_decode_forced_partitions(partition, dtype):
@@ -59,6 +79,35 @@ def test_decode_forced_partitions(partition, dtype):
                               block_size=16, context_lens=lens, dtype=dtype, seed=partition,
                               device=str(dev))
     _check_step(wl, partition_size=partition)
+
+
+@pytest.mark.parametrize("hq,hkv,dtype", [(32, 32, torch.float16), (32, 8, torch.bfloat16),
+                                          (64, 8, torch.bfloat16)])
+def test_decode_merge_never_reads_stale_partials(hq, hkv, dtype):
+    """The merge starts behind the decode kernel and must wait for its partials: with
+    the workspace filled with NaN before each call and new queries each time, every
+    split-context call gives the oracle's result."""
+    dev = device()
+    lens = [4096, 1, 2049, 3000, 512, 4000]
+    wl = make_decode_workload(num_seqs=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                              block_size=16, context_lens=lens, dtype=dtype, seed=hq + hkv,
+                              device=str(dev))
+    k_cache, v_cache = pkv.split_pool(wl.kv)
+    need = pkv.decode_workspace_bytes(len(lens), hq, hkv, 128, 16, 4096, 256)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    pool = host_pool_bits(wl.kv)
+    qg = torch.Generator(device=dev).manual_seed(7)
+    for call in range(4):
+        q = torch.randn(wl.q.shape, generator=qg, device=dev).to(dtype)
+        ws.view(torch.float32).fill_(float("nan"))
+        out = pkv.paged_attention_decode(q, k_cache, v_cache, wl.block_tables, wl.context_lens,
+                                         wl.scale, max_context_len=4096, partition_size=256,
+                                         workspace=ws)
+        torch.cuda.synchronize()
+        check_no_device_flags(dev)
+        ref = oracle_decode(to_bits(q.cpu()), pool, wl.block_tables.cpu(), wl.context_lens.cpu(),
+                            hkv, 16, wl.scale, dtype)
+        assert_close(out, ref, what=f"split decode, call {call}")
 
 
 @pytest.mark.parametrize("bs", [8, 32])

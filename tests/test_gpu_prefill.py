@@ -13,7 +13,7 @@ import paged_kv_cache_155_gb300 as pkv
 from paged_kv_cache_155_gb300 import workloads
 from paged_kv_cache_155_gb300.workloads import make_prefill_workload
 from tests._gpu_helpers import (assert_close, check_no_device_flags, device, host_pool_bits,
-                                oracle_prefill_step, run_prefill)
+                                oracle_prefill_step, poison_unused_slots, run_prefill)
 
 pytestmark = pytest.mark.gpu
 
@@ -44,6 +44,20 @@ def test_prefill_shapes(dtype, bs, hq, hkv):
                                cached_lens=cached, chunk_lens=chunks, dtype=dtype,
                                seed=hq + bs, device=str(dev))
     _check(wl)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_prefill_ignores_nonfinite_unused_slots(dtype, bs):
+    """NaN / Inf in every slot past each context (the chunk's K/V rows are written over
+    theirs first) and in unused blocks: the output is the oracle's."""
+    dev = device()
+    wl = make_prefill_workload(num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=bs,
+                               cached_lens=[0, 5, 130, 37], chunk_lens=[1, 127, 129, 64],
+                               dtype=dtype, seed=bs + 70, device=str(dev))
+    poison_unused_slots(wl.kv, wl.block_tables, wl.context_lens, bs)
+    _check(wl)
+    _check(wl, kv_splits=2)
 
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 7])

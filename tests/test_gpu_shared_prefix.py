@@ -12,7 +12,7 @@ import paged_kv_cache_155_gb300 as pkv
 from paged_kv_cache_155_gb300 import workloads
 from paged_kv_cache_155_gb300.workloads import make_decode_workload
 from tests._gpu_helpers import (assert_close, check_no_device_flags, device, host_pool_bits,
-                                oracle_decode)
+                                oracle_decode, poison_unused_slots)
 from tests._paged_helpers import to_bits
 
 pytestmark = pytest.mark.gpu
@@ -54,6 +54,54 @@ def test_shared_prefix_shapes(dtype, hq, hkv, bs, prefix_blocks):
                               block_size=bs, context_lens=lens, dtype=dtype, seed=prefix + hq,
                               device=str(dev), shared_prefix_tokens=prefix)
     _cascade_vs_oracle(wl, prefix)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_shared_prefix_ignores_nonfinite_unused_slots(dtype, bs):
+    """NaN / Inf in every slot past each context and in unused blocks: the prefix tiles
+    (which load whole 128-token tiles) and the suffix pass still give the oracle's result."""
+    dev = device()
+    prefix = 9 * bs
+    lens = [prefix + 1, prefix, prefix + bs + 3, prefix + 200, prefix + 5 * bs - 1]
+    need = sum(-(-n // bs) for n in lens) - 4 * (prefix // bs)
+    wl = make_decode_workload(num_seqs=5, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                              block_size=bs, context_lens=lens, dtype=dtype, seed=bs + 40,
+                              device=str(dev), shared_prefix_tokens=prefix, num_blocks=need + 5)
+    poison_unused_slots(wl.kv, wl.block_tables, wl.context_lens, bs)
+    _cascade_vs_oracle(wl, prefix)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+def test_shared_prefix_merge_never_reads_stale_partials(dtype):
+    """The prefix tiles and the suffix pass overlap on the GPU and the merge follows
+    both: with the workspace filled with NaN before each call and new queries each
+    time, every call must still give the oracle's result (a merge that ran ahead of
+    either producer would read NaN or the previous call's partials)."""
+    dev = device()
+    g = torch.Generator().manual_seed(31)
+    n, prefix = 64, 1024
+    lens = (prefix + torch.randint(1, 1200, (n,), generator=g)).tolist()
+    wl = make_decode_workload(num_seqs=n, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                              block_size=16, context_lens=lens, dtype=dtype, seed=32,
+                              device=str(dev), shared_prefix_tokens=prefix)
+    k_cache, v_cache = pkv.split_pool(wl.kv)
+    maxl = int(wl.context_lens.max())
+    need = pkv.shared_prefix_workspace_bytes(n, 32, 8, 128, 16, prefix, maxl)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    pool = host_pool_bits(wl.kv)
+    qg = torch.Generator(device=dev).manual_seed(33)
+    for call in range(4):
+        q = torch.randn(wl.q.shape, generator=qg, device=dev).to(dtype)
+        ws.view(torch.float32).fill_(float("nan"))
+        out = pkv.paged_attention_decode_shared_prefix(
+            q, k_cache, v_cache, wl.block_tables[0, :prefix // 16].contiguous(), prefix,
+            wl.block_tables, wl.context_lens, wl.scale, max_context_len=maxl, workspace=ws)
+        torch.cuda.synchronize()
+        check_no_device_flags(dev)
+        ref = oracle_decode(to_bits(q.cpu()), pool, wl.block_tables.cpu(), wl.context_lens.cpu(),
+                            8, 16, wl.scale, dtype)
+        assert_close(out, ref, what=f"shared-prefix decode, call {call}")
 
 
 @pytest.mark.parametrize("partition", [0, 64, 256])

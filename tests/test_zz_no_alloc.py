@@ -4,9 +4,10 @@
 It exists for callers that cannot allocate device memory for the decode
 workspace: a serving engine that reserved nearly all free device memory for
 its KV block pool, or a plug-in that gets tensor pointers but no allocator.
-It must give the same results as the workspace-taking entry point, on two
-calls in a row (the shared scratch array keeps the previous call's contents),
-and must reject plans whose scratch would not fit its fixed array.
+It must give the oracle's results, and the same results as the
+workspace-taking entry point, on two calls in a row (the shared scratch array
+keeps the previous call's contents), and must reject plans whose scratch would
+not fit its fixed array.
 
 This file is collected last on purpose; it builds its own inputs so that it
 passes alone in a fresh process as well as after the other tests.
@@ -20,7 +21,9 @@ import torch
 import paged_kv_cache_155_gb300 as pkv
 from paged_kv_cache_155_gb300._lib import lib
 from paged_kv_cache_155_gb300.workloads import make_decode_workload
-from tests._gpu_helpers import ATOL, RTOL, check_no_device_flags, device
+from tests._gpu_helpers import (ATOL, RTOL, assert_close, check_no_device_flags, device,
+                                host_pool_bits, oracle_decode)
+from tests._paged_helpers import to_bits
 
 SCRATCH_LIMIT = 5          # PKV_ERR_SCRATCH_LIMIT
 SCRATCH_BYTES = 32 << 20   # PKV_STATIC_SCRATCH_BYTES
@@ -44,7 +47,7 @@ def _close(got, ref):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
-def test_static_scratch_decode_matches_workspace_decode(dtype):
+def test_static_scratch_decode_matches_oracle_and_workspace_decode(dtype):
     dev = device()
     lens = [1, 700, 4096, 33, 2500, 1024, 17, 3000]
     wl = make_decode_workload(num_seqs=len(lens), num_q_heads=32, num_kv_heads=8, head_dim=128,
@@ -55,6 +58,7 @@ def test_static_scratch_decode_matches_workspace_decode(dtype):
     need = pkv.decode_workspace_bytes(wl.num_seqs, 32, 8, 128, 16, maxl, part)
     assert 0 < need <= SCRATCH_BYTES
     k_cache, v_cache = pkv.split_pool(wl.kv)
+    pool = host_pool_bits(wl.kv)
     g = torch.Generator(device=dev).manual_seed(5)
     for call in range(2):                       # two calls in a row, different queries
         q = torch.randn(wl.q.shape, generator=g, device=dev).to(dtype)
@@ -65,6 +69,10 @@ def test_static_scratch_decode_matches_workspace_decode(dtype):
         assert st == 0, f"call {call}: status {st}"
         torch.cuda.synchronize()
         check_no_device_flags(dev)
+        oracle_ref = oracle_decode(to_bits(q.cpu()), pool, wl.block_tables.cpu(),
+                                   wl.context_lens.cpu(), wl.num_kv_heads, wl.block_size,
+                                   wl.scale, dtype)
+        assert_close(out, oracle_ref, what=f"static-scratch decode, call {call}")
         _close(out, ref)
     # a plan whose scratch would exceed the fixed array is refused before any launch
     big = make_decode_workload(num_seqs=64, num_q_heads=64, num_kv_heads=8, head_dim=128,
