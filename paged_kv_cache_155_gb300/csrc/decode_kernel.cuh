@@ -239,6 +239,16 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const __grid_const
     const int kvh = blockIdx.y / p.subgroups;
     const int hq0 = kvh * p.group + (blockIdx.y % p.subgroups) * GH;
 
+    // ---- the partition's first table entries are fetched together with the context
+    //      length (where the partition starts does not depend on it), so the first
+    //      tile copies wait for one global-memory round trip, not two
+    const int tok0 = p.tok_begin + part * p.partition_size;
+    const int blk0 = tok0 / BS;
+    const int32_t *trow = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + blk0;
+    int first_entry = 0;  // entry threadIdx.x of the slice, if the table has it
+    if (static_cast<int>(threadIdx.x) < min(p.max_blocks_per_seq - blk0, p.partition_size / BS))
+        first_entry = trow[threadIdx.x];
+
     // ---- context length (device value, range-checked) and partition bounds
     int len = p.context_lens[seq];
     if (len < 0 || len > p.len_cap) {
@@ -248,17 +258,14 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const __grid_const
     }
     const int nparts = partitions_of(p, len);
     if (part >= nparts) return;  // uniform over the CTA
-    const int tok0 = p.tok_begin + part * p.partition_size;
     const int tok1 = min(len, tok0 + p.partition_size);
     const int ntok = max(0, tok1 - tok0);
     const int nchunks = (ntok + TILE - 1) / TILE;
-    const int blk0 = tok0 / BS;
-    const int nblk = (ntok + BS - 1) / BS;
+    const int nblk = (ntok + BS - 1) / BS;  // <= partition_size / BS, within the table
 
     // ---- table slice of this partition -> shared memory (bad entries -> -1)
-    const int32_t *trow = p.block_tables + static_cast<int64_t>(seq) * p.max_blocks_per_seq + blk0;
     for (int i = threadIdx.x; i < nblk; i += blockDim.x) {
-        int b = trow[i];
+        int b = i < static_cast<int>(blockDim.x) ? first_entry : trow[i];
         if (b < 0 || b >= p.num_blocks) {
             raise_flag(p.status, PKV_DEVERR_BLOCK_TABLE);
             b = -1;

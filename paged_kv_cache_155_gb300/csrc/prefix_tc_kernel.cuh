@@ -14,9 +14,11 @@
 //
 // tcgen05 MMAs, M = 128 query rows, N = 128 tokens, K = 128 (head_dim):
 //   S  = Q . K^T      A = Q tile (K-major), B = K tile (K-major)
-//   O += P . V        A = P (K-major), B = V tile (MN-major: head_dim contiguous)
+//   O += P . V        A = P from TMEM, B = V tile (MN-major: head_dim contiguous)
 // S is double-buffered in TMEM (2 x 128 columns), O accumulates in TMEM (128
-// columns).  A row's softmax belongs to one pair of threads (TMEM lane = query
+// columns); P is written back over its scores (two 16-bit values per column),
+// so shared memory holds only Q and three-slot K and V rings, whose depth
+// covers the load latency while the suffix decode keeps HBM busy.  A row's softmax belongs to one pair of threads (TMEM lane = query
 // row), each taking 64 of the tile's 128 columns; the pair exchanges its
 // partial row maxima through spare TMEM columns, so both halves use one
 // reference maximum.  That maximum is raised only when a tile's maximum
@@ -24,8 +26,8 @@
 // so P <= 2^kRescaleLog2.  P is rounded to the input type for the MMA; l adds
 // the fp32 values (unbiased rounding, relative error 2^-9 per weight at most).
 //
-// Warps: 0 / 10 TMA producers of the K ring and the V ring (2 slots each, 3-D
-// tiled copies with 128-byte swizzle), 1 TMEM owner + MMA issuer (event-driven),
+// Warps: 0 / 10 TMA producers of the K ring and the V ring (3 slots each, 3-D
+// tiled copies with 128-byte swizzle), 1 TMEM owner + QK^T issuer, 11 PV issuer,
 // 2-9 softmax in pairs (warps w and w + 4 share TMEM lane quarter w & 3).
 #pragma once
 
@@ -83,20 +85,20 @@ struct PrefixParams {
 };
 
 struct PrefixLayout {
-    static constexpr int kThreads = 352;               // 11 warps (roles below)
+    static constexpr int kThreads = 384;               // 12 warps (roles below)
     static constexpr int kTile = 128;
     static constexpr int kHalf = 128 * 128;            // 128 rows x 128 B
     static constexpr int kPanel = 2 * kHalf;           // 128 rows x 128 16-bit values
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kPanel;       // 2 slots
-    static constexpr int kOffV = kOffK + 2 * kPanel;   // 2 slots
-    static constexpr int kOffP = kOffV + 2 * kPanel;   // 2 buffers
-    static constexpr int kOffBar = kOffP + 2 * kPanel;
-    static constexpr int kNumBars = 25;
+    static constexpr int kKS = 3, kVS = 3;             // K / V ring slots
+    static constexpr int kOffK = kOffQ + kPanel;
+    static constexpr int kOffV = kOffK + kKS * kPanel;
+    static constexpr int kOffBar = kOffV + kVS * kPanel;
+    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 8 + 2 + 8;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kSmemBytes = kBytes + 1024;
-    static constexpr uint32_t kTmemCols = 512;           // S[2] at 0 / 128, O at 256, exchange 384
+    static constexpr uint32_t kTmemCols = 512;           // S[2] (P[b] over S[b]) at 0 / 128, O at 256, exchange 384
     static constexpr uint32_t kXchgCol = 384;            // spare TMEM columns for the pairs
     static constexpr float kRescaleLog2 = 8.f;
 };
@@ -106,7 +108,8 @@ __global__ void __launch_bounds__(PrefixLayout::kThreads, 1)
     paged_prefix_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v, const PrefixParams p) {
     using L = PrefixLayout;
-    constexpr int TILE = L::kTile, D = 128, kThreads = L::kThreads;
+    constexpr int TILE = L::kTile, D = 128, kThreads = L::kThreads, KS = L::kKS, VS = L::kVS;
+    static_assert(VS >= 2, "V slots >= S buffers (2): see the V-row zeroing wait");
     constexpr bool kBF16 = !std::is_same<T, __half>::value;
     static_assert(TILE / BS <= 32, "one table entry per producer lane");
 
@@ -114,10 +117,10 @@ __global__ void __launch_bounds__(PrefixLayout::kThreads, 1)
     unsigned char *sm =
         smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
-    uint64_t *k_full = bars, *k_empty = bars + 2, *v_full = bars + 4, *v_empty = bars + 6;
-    uint64_t *s_full = bars + 8, *s_empty = bars + 10, *p_full = bars + 12, *o_done = bars + 14;
-    uint64_t *drain_bar = bars + 16;
-    uint64_t *pair_bar = bars + 17;  // [quarter][parity]
+    uint64_t *k_full = bars, *k_empty = k_full + KS, *v_full = k_empty + KS, *v_empty = v_full + VS;
+    uint64_t *s_full = v_empty + VS, *s_empty = s_full + 2, *p_full = s_empty + 2, *o_done = p_full + 2;
+    uint64_t *drain_bar = o_done + 2;    // [QK issuer, PV issuer]
+    uint64_t *pair_bar = drain_bar + 2;  // [quarter][parity]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
 
@@ -132,17 +135,22 @@ __global__ void __launch_bounds__(PrefixLayout::kThreads, 1)
     const uint32_t smem_base = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < KS; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < VS; ++i) {
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 8);
+            mbar_init(&s_empty[i], 1);  // committed by PV(j): P[b] lives over S[b]
             mbar_init(&p_full[i], 8);
             mbar_init(&o_done[i], 1);
         }
-        mbar_init(drain_bar, 1);
+        mbar_init(&drain_bar[0], 1);
+        mbar_init(&drain_bar[1], 1);
         for (int i = 0; i < 8; ++i) mbar_init(&pair_bar[i], 2);
         *abort_flag = 0;
         fence_mbar_init();
@@ -196,6 +204,7 @@ __global__ void __launch_bounds__(PrefixLayout::kThreads, 1)
         const int kv = warp == 10;
         uint64_t *full = kv ? v_full : k_full;
         uint64_t *empty = kv ? v_empty : k_empty;
+        const int nst = kv ? VS : KS;
         const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
         unsigned char *ring = sm + (kv ? L::kOffV : L::kOffK);
         const uint64_t policy = l2_policy_evict_last();  // the prefix is read by every row tile
@@ -212,17 +221,17 @@ __global__ void __launch_bounds__(PrefixLayout::kThreads, 1)
             }
             return e;
         };
-        int last_issue[2] = {-1, -1};
+        int last_issue[3] = {-1, -1, -1};
         bool ok = true;
         int e_next = ntiles > 0 ? entry(0) : -1;
         for (int j = 0; j < ntiles && ok; ++j) {
             const int e = e_next;
             if (j + 1 < ntiles) e_next = entry(j + 1);  // in flight while this tile waits
             const uint32_t bytes = __popc(__ballot_sync(0xffffffffu, e >= 0)) * BS * 256u;
-            const int s = j & 1;
+            const int s = j % nst;
             int go = 1;
             if (lane == 0) {
-                go = tc_wait(&empty[s], ((j >> 1) & 1) ^ 1, abort_flag, p.status);
+                go = tc_wait(&empty[s], ((j / nst) & 1) ^ 1, abort_flag, p.status);
                 if (go) {
                     if (bytes) mbar_arrive_expect_tx(&full[s], bytes);
                     else mbar_arrive(&full[s]);
@@ -243,76 +252,72 @@ __global__ void __launch_bounds__(PrefixLayout::kThreads, 1)
             __syncwarp();
         }
         if (!ok && lane == 0) {
-            for (int s = 0; s < 2; ++s)
+            for (int s = 0; s < nst; ++s)
                 if (last_issue[s] >= 0)
-                    mbar_wait_bounded(&full[s], (last_issue[s] >> 1) & 1, kDrainTimeoutNs);
+                    mbar_wait_bounded(&full[s], (last_issue[s] / nst) & 1, kDrainTimeoutNs);
         }
     } else if (warp == 1) {
-        // ===================== MMA issuer (event-driven, PV first) =====================
+        // ===================== QK^T issuer =====================
+        // QK^T of each tile as soon as its K landed and its S buffer is free; PV is
+        // issued by warp 11, so a ready PV never waits behind a QK^T batch (a batch of
+        // MMAs holds its issuing thread for its whole execution).
         constexpr uint32_t idesc_qk = tc::idesc_f16_f32acc(kBF16, 128, 128, false, false);
-        constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, 128, false, true);
-        int n_qk = 0, n_pv = 0;
-        bool ok = true;
-        uint64_t idle_since = 0;
-        while (ok && n_pv < ntiles) {
-            int act = 0;
+        for (int j = 0; j < ntiles; ++j) {
+            int go = 1;
+            if (lane == 0)
+                go = tc_wait(&k_full[j % KS], (j / KS) & 1, abort_flag, p.status) &&
+                     tc_wait(&s_empty[j & 1], ((j >> 1) & 1) ^ 1, abort_flag, p.status);
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
             if (lane == 0) {
-                if (n_pv < n_qk && mbar_test_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1) &&
-                    mbar_test_wait(&v_full[n_pv & 1], (n_pv >> 1) & 1))
-                    act = 1;
-                else if (n_qk < ntiles && mbar_test_wait(&k_full[n_qk & 1], (n_qk >> 1) & 1) &&
-                         mbar_test_wait(&s_empty[n_qk & 1], ((n_qk >> 1) & 1) ^ 1))
-                    act = 2;
-                if (act) {
-                    idle_since = 0;
-                } else {
-                    const uint64_t now = global_timer_ns();
-                    if (!idle_since) idle_since = now;
-                    if (*abort_flag) {
-                        act = -1;
-                    } else if (now - idle_since > kWaitTimeoutNs) {
-                        raise_flag(p.status, PKV_DEVERR_TIMEOUT);
-                        *abort_flag = 1;
-                        act = -1;
-                    }
-                }
-                if (act == 1) {
-                    const int j = n_pv, b = j & 1;
-                    tc::fence_after_sync();
-                    const uint32_t pa = smem_base + L::kOffP + b * L::kPanel;
-                    const uint32_t va = smem_base + L::kOffV + b * L::kPanel;
+                const int b = j & 1;
+                tc::fence_after_sync();
+                const uint32_t qa = smem_base + L::kOffQ;
+                const uint32_t ka = smem_base + L::kOffK + (j % KS) * L::kPanel;
 #pragma unroll
-                    for (int k = 0; k < TILE / 16; ++k) {
-                        const uint64_t a = tc::smem_desc_sw128(pa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
-                        const uint64_t bd = tc::smem_desc_sw128(va + k * 2048, L::kHalf, 1024);
-                        tc::mma_f16_ss(tmem + 256, a, bd, idesc_pv, j > 0 || k > 0);
-                    }
-                    tc::mma_commit(&o_done[b]);
-                    tc::mma_commit(&v_empty[b]);
-                } else if (act == 2) {
-                    const int j = n_qk, b = j & 1;
-                    tc::fence_after_sync();
-                    const uint32_t qa = smem_base + L::kOffQ;
-                    const uint32_t ka = smem_base + L::kOffK + b * L::kPanel;
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint64_t a = tc::smem_desc_sw128(qa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
-                        const uint64_t bd = tc::smem_desc_sw128(ka + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
-                        tc::mma_f16_ss(tmem + 128 * b, a, bd, idesc_qk, k > 0);
-                    }
-                    tc::mma_commit(&s_full[b]);
-                    tc::mma_commit(&k_empty[b]);
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint64_t a = tc::smem_desc_sw128(qa + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc_sw128(ka + (k / 4) * L::kHalf + (k % 4) * 32, 16, 1024);
+                    tc::mma_f16_ss(tmem + 128 * b, a, bd, idesc_qk, k > 0);
                 }
+                tc::mma_commit(&s_full[b]);
+                tc::mma_commit(&k_empty[j % KS]);
             }
-            act = __shfl_sync(0xffffffffu, act, 0);
-            if (act < 0) ok = false;
-            else if (act == 1) ++n_pv;
-            else if (act == 2) ++n_qk;
+            __syncwarp();
         }
         if (lane == 0) {
-            // every MMA of this CTA completes before TMEM is released
-            tc::mma_commit(drain_bar);
-            mbar_wait_bounded(drain_bar, 0, kDrainTimeoutNs);
+            // this thread's MMAs complete before TMEM is released
+            tc::mma_commit(&drain_bar[0]);
+            mbar_wait_bounded(&drain_bar[0], 0, kDrainTimeoutNs);
+        }
+        __syncwarp();
+    } else if (warp == 11) {
+        // ===================== PV issuer =====================
+        constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, 128, false, true);
+        for (int j = 0; j < ntiles; ++j) {
+            int go = 1;
+            if (lane == 0)
+                go = tc_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag, p.status) &&
+                     tc_wait(&v_full[j % VS], (j / VS) & 1, abort_flag, p.status);
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
+            if (lane == 0) {
+                const int b = j & 1;
+                tc::fence_after_sync();
+                const uint32_t va = smem_base + L::kOffV + (j % VS) * L::kPanel;
+#pragma unroll
+                for (int k = 0; k < TILE / 16; ++k) {
+                    const uint64_t bd = tc::smem_desc_sw128(va + k * 2048, L::kHalf, 1024);
+                    // P from TMEM: 16 tokens = 8 packed columns per step
+                    tc::mma_f16_ts(tmem + 256, tmem + 128 * b + 8 * k, bd, idesc_pv, j > 0 || k > 0);
+                }
+                tc::mma_commit(&o_done[b]);
+                tc::mma_commit(&s_empty[b]);  // S[b] / P[b] free for QK^T(j + 2)
+                tc::mma_commit(&v_empty[j % VS]);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) {
+            tc::mma_commit(&drain_bar[1]);
+            mbar_wait_bounded(&drain_bar[1], 0, kDrainTimeoutNs);
         }
         __syncwarp();
     } else {
@@ -411,23 +416,21 @@ __global__ void __launch_bounds__(PrefixLayout::kThreads, 1)
                 l *= alpha;
                 m_ref = new_ref;
             }
-            // P[b] was last read by PV(j-2)
-            if (j >= 2 && !tc_wait_warp(&o_done[b], ((j - 2) >> 1) & 1, abort_flag, p.status)) {
-                ok = false;
-                break;
-            }
-            // P = 2^(s - m_ref) (0 past the prefix end), rounded to T into this half of
-            // the K-major P panel; the row sum l adds the fp32 values
-            unsigned char *prow = sm + L::kOffP + b * L::kPanel + half * L::kHalf + r * 128;
+            // P = 2^(s - m_ref) (0 past the prefix end), rounded to T and packed two per
+            // 32-bit column over the first 64 columns of S[b] (tokens 64 half .. +63 ->
+            // columns 32 half .. +31; both threads of the pair have read their scores,
+            // the exchange above orders it), where the PV MMA reads it; the row sum l
+            // adds the fp32 values.  S[b] was free for QK^T(j) only after PV(j-2).
+            const uint32_t pcol = lane_base + 128 * b + 32 * half;
             float l0 = 0.f, l1 = 0.f;
             // two copies of the loop, so full halves carry no per-column mask
             auto weights = [&](auto masked) {
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    uint32_t packed[4];
+                for (int c16 = 0; c16 < 2; ++c16) {
+                    uint32_t packed[16];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int t = c8 * 8 + 2 * i;
+                    for (int i = 0; i < 16; ++i) {
+                        const int t = c16 * 32 + 2 * i;
                         // s * scale - m for two columns in one packed FMA
                         float e0 = -m_ref, e1 = -m_ref;
                         fma_f32x2(e0, e1, x[t], x[t + 1], p.scale_log2, p.scale_log2);
@@ -440,33 +443,34 @@ __global__ void __launch_bounds__(PrefixLayout::kThreads, 1)
                         add_f32x2(l0, l1, p0, p1);
                         packed[i] = Elem<T>::pack2(p0, p1);
                     }
-                    *reinterpret_cast<uint4 *>(prow + ((c8 ^ (r & 7)) << 4)) =
-                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    tc::tmem_st_x16(pcol + 16 * c16, packed);
                 }
             };
             if (full) weights(std::false_type{});
             else weights(std::true_type{});
             l += l0 + l1;
-            tc::fence_before_sync();
             if (valid < TILE) {
                 // rows of V past the prefix end: zero them (this thread: row r, this
-                // half's 64 channels) so 0 * stale never reaches the MMA
-                if (!tc_wait_warp(&v_full[b], (j >> 1) & 1, abort_flag, p.status)) {
+                // half's 64 channels) so 0 * stale never reaches the MMA.  The parity
+                // wait cannot pass on an older phase of the slot: S(j) exists only once
+                // PV(j-2) has completed (two S buffers), and with VS >= 2 the slot's
+                // previous tile, V(j - VS), was consumed by then.
+                if (!tc_wait_warp(&v_full[j % VS], (j / VS) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 if (r >= valid) {
-                    uint4 *vrow = reinterpret_cast<uint4 *>(sm + L::kOffV + b * L::kPanel + half * L::kHalf + r * 128);
+                    uint4 *vrow = reinterpret_cast<uint4 *>(sm + L::kOffV + (j % VS) * L::kPanel + half * L::kHalf +
+                                                            r * 128);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) vrow[i] = make_uint4(0, 0, 0, 0);
                 }
             }
-            fence_proxy_async_smem();
+            tc::tmem_st_wait();
+            tc::fence_before_sync();   // P and the O rescale's TMEM stores precede PV(j)
+            fence_proxy_async_smem();  // zeroed V rows visible to the MMA
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&s_empty[b]);
-                mbar_arrive(&p_full[b]);
-            }
+            if (lane == 0) mbar_arrive(&p_full[b]);
         }
         // final: the pair's row sum, then this half of the O row -> workspace slot
         // `split` of the row's (sequence, query head).  TMEM loads are warp-wide:
@@ -504,7 +508,7 @@ __global__ void __launch_bounds__(PrefixLayout::kThreads, 1)
         }
     }
 
-    // ---- tear-down: the MMA warp drained its MMAs; TMEM is freed
+    // ---- tear-down: both issuers drained their MMAs; TMEM is freed
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 1) {
