@@ -11,7 +11,8 @@ the Llama-2-7B-shaped MHA decode layer (32 sequences x 4096 tokens, 32 heads of
 
 Prints one JSON line (rank 0).  `value` is decode tokens/s (one token per
 sequence per step) over all ranks, device-timed with inputs resident in HBM;
-`e2e` is the same metric through the Python API with each step's inputs copied
+`e2e` is the same metric through the Python API (calls prepared once on their
+buffers, re-issued each step) with each step's inputs copied
 from pinned host memory and its output copied back inside the timed region, as a
 serving loop runs it: two sets of device buffers, the copies on their own
 streams, so step i's copies overlap step i-1's kernels (`e2e.serial_value` is
@@ -218,25 +219,20 @@ def _config_summary(main, line, others):
     return out
 
 
-def _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part):
-    """(cache write, decode) of one step through the public API, for a 16-bit or
-    an INT8 pool."""
+def _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part, k_new, v_new, slots, q, bt, cl):
+    """(cache write, decode) of one step through the public API, for a 16-bit or an
+    INT8 pool, each prepared once on the given buffers (a serving loop reuses its
+    buffers; only the library calls are re-issued per step)."""
     if wl.kv.dtype == __import__("torch").int8:
-        def write(k_new, v_new, slots):
-            pkv.reshape_and_cache_int8(k_new, v_new, slots, k_cache, v_cache, wl.k_scale,
-                                       wl.v_scale)
-
-        def decode(q, bt, cl):
-            pkv.paged_attention_decode_int8(q, k_cache, v_cache, wl.k_scale, wl.v_scale, bt, cl,
-                                            wl.scale, out, max_context_len=maxl,
-                                            partition_size=part)
+        write = pkv.prepare_reshape_and_cache_int8(k_new, v_new, slots, k_cache, v_cache, wl.k_scale,
+                                                   wl.v_scale)
+        decode = pkv.prepare_paged_attention_decode_int8(q, k_cache, v_cache, wl.k_scale, wl.v_scale,
+                                                         bt, cl, wl.scale, out, max_context_len=maxl,
+                                                         partition_size=part)
     else:
-        def write(k_new, v_new, slots):
-            pkv.reshape_and_cache(k_new, v_new, slots, k_cache, v_cache)
-
-        def decode(q, bt, cl):
-            pkv.paged_attention_decode(q, k_cache, v_cache, bt, cl, wl.scale, out,
-                                       max_context_len=maxl, partition_size=part)
+        write = pkv.prepare_reshape_and_cache(k_new, v_new, slots, k_cache, v_cache)
+        decode = pkv.prepare_paged_attention_decode(q, k_cache, v_cache, bt, cl, wl.scale, out,
+                                                    max_context_len=maxl, partition_size=part)
     return write, decode
 
 
@@ -377,11 +373,12 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
                              num_blocks=wl.num_blocks)
     out = torch.empty_like(wl.q)
     stream = torch.cuda.current_stream(dev)
-    write, decode = _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part)
+    write, decode = _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part, wl.k_new, wl.v_new,
+                                slots, wl.q, wl.block_tables, wl.context_lens)
 
     def step():
-        write(wl.k_new, wl.v_new, slots)
-        decode(wl.q, wl.block_tables, wl.context_lens)
+        write()
+        decode()
 
     for _ in range(5):
         step()
@@ -391,9 +388,9 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for k in range(steps):
-        write(wl.k_new, wl.v_new, slots)
+        write()
         ev[k][0].record(stream)
-        decode(wl.q, wl.block_tables, wl.context_lens)
+        decode()
         ev[k][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -459,25 +456,21 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
         pre_tokens = wl.shared_prefix_blocks * wl.block_size
         pre_table = wl.block_tables[0, :wl.shared_prefix_blocks].contiguous()
 
-        def cascade_step():
-            pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
-            pkv.paged_attention_decode_shared_prefix(
-                wl.q, k_cache, v_cache, pre_table, pre_tokens, wl.block_tables, wl.context_lens,
-                wl.scale, out, max_context_len=maxl)
-
+        cascade = pkv.prepare_paged_attention_decode_shared_prefix(
+            wl.q, k_cache, v_cache, pre_table, pre_tokens, wl.block_tables, wl.context_lens,
+            wl.scale, out, max_context_len=maxl)
         for _ in range(5):
-            cascade_step()
+            write()
+            cascade()
         torch.cuda.synchronize()
         ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(steps)]
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record(stream)
         for k in range(steps):
-            pkv.reshape_and_cache(wl.k_new, wl.v_new, slots, k_cache, v_cache)
+            write()
             ev2[k][0].record(stream)
-            pkv.paged_attention_decode_shared_prefix(
-                wl.q, k_cache, v_cache, pre_table, pre_tokens, wl.block_tables, wl.context_lens,
-                wl.scale, out, max_context_len=maxl)
+            cascade()
             ev2[k][1].record(stream)
         s1.record(stream)
         torch.cuda.synchronize()
@@ -502,12 +495,8 @@ def measure_workload(pkv, name, dev, steps, peak, partition=None):
             torch.cuda.synchronize()
             return statistics.median(a.elapsed_time(b) for a, b in evs)
 
-        plain_flushed = flushed_ms(lambda: pkv.paged_attention_decode(
-            wl.q, k_cache, v_cache, wl.block_tables, wl.context_lens, wl.scale, out,
-            max_context_len=maxl, partition_size=part))
-        cascade_flushed = flushed_ms(lambda: pkv.paged_attention_decode_shared_prefix(
-            wl.q, k_cache, v_cache, pre_table, pre_tokens, wl.block_tables, wl.context_lens,
-            wl.scale, out, max_context_len=maxl))
+        plain_flushed = flushed_ms(decode)
+        cascade_flushed = flushed_ms(cascade)
         del flush
         result["shared_prefix_decode"] = {
             "tokens_per_s": wl.num_seqs / (c_step / 1e3), "ms_per_step": c_step,
@@ -613,11 +602,12 @@ def run_ours(args):
                              num_blocks=wl.num_blocks)
     out = torch.empty_like(wl.q)
     stream = torch.cuda.current_stream(dev)
-    write, decode = _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part)
+    write, decode = _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part, wl.k_new, wl.v_new,
+                                slots, wl.q, wl.block_tables, wl.context_lens)
 
     def step():
-        write(wl.k_new, wl.v_new, slots)
-        decode(wl.q, wl.block_tables, wl.context_lens)
+        write()
+        decode()
 
     for _ in range(args.warmup):
         step()
@@ -643,9 +633,9 @@ def run_ours(args):
     launches0 = pkv.launch_count()
     t_start.record(stream)
     for k in range(args.steps):
-        write(wl.k_new, wl.v_new, slots)
+        write()
         dec_ev[k][0].record(stream)
-        decode(wl.q, wl.block_tables, wl.context_lens)
+        decode()
         dec_ev[k][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -673,13 +663,15 @@ def run_ours(args):
         torch.empty_like(wl.context_lens)
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots, h_bt, h_cl))
     d2h = h_out.numel() * h_out.element_size()
+    write_e, decode_e = _step_calls(pkv, wl, k_cache, v_cache, out, maxl, part, d_k, d_v, d_slots,
+                                    d_q, d_bt, d_cl)
 
     def e2e_step():
         for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_slots, h_slots), (d_bt, h_bt),
                      (d_cl, h_cl)):
             d.copy_(h, non_blocking=True)
-        write(d_k, d_v, d_slots)
-        decode(d_q, d_bt, d_cl)
+        write_e()
+        decode_e()
         h_out.copy_(out, non_blocking=True)
 
     def time_loop(one_step, n, tail=None):
@@ -711,7 +703,9 @@ def run_ours(args):
                                                    wl.block_tables, wl.context_lens))
         d_res = torch.empty_like(wl.q)
         h_res = torch.empty(wl.q.shape, dtype=wl.q.dtype, pin_memory=True)
-        w_b, dec_b = _step_calls(pkv, wl, k_cache, v_cache, d_res, maxl, part)
+        q_, k_, v_, sl_, bt_, cl_ = d_in
+        w_b, dec_b = _step_calls(pkv, wl, k_cache, v_cache, d_res, maxl, part, k_, v_, sl_, q_, bt_,
+                                 cl_)
         sets.append({"in": d_in, "res": d_res, "h_res": h_res, "write": w_b, "decode": dec_b,
                      "copied_in": torch.cuda.Event(), "computed": torch.cuda.Event(),
                      "copied_out": torch.cuda.Event()})
@@ -726,9 +720,8 @@ def run_ours(args):
             b["copied_in"].record(cs_in)
         stream.wait_event(b["copied_in"])
         stream.wait_event(b["copied_out"])      # step i-2's result has left this buffer
-        q_, k_, v_, sl_, bt_, cl_ = b["in"]
-        b["write"](k_, v_, sl_)
-        b["decode"](q_, bt_, cl_)
+        b["write"]()
+        b["decode"]()
         b["computed"].record(stream)
         with torch.cuda.stream(cs_out):
             cs_out.wait_event(b["computed"])

@@ -3,6 +3,11 @@ marshalling only.  Tensors supply device pointers and shapes; the current
 CUDA stream of the tensors' device is passed as the stream.  Every step runs
 in the library's kernels; if the library is missing the calls raise.
 
+``prepare_*`` variants check and marshal a call's arguments once and return a
+``PreparedCall``; calling it enqueues the same library call again on the
+current stream (a serving loop that reuses its buffers pays the argument
+checks once, not per step).
+
 Cache tensors: ``k_cache`` / ``v_cache`` are [num_blocks, num_kv_heads,
 block_size, head_dim] views sharing one block stride, normally the two
 halves ``kv[:, 0]`` / ``kv[:, 1]`` of a pool ``kv`` of shape
@@ -31,8 +36,44 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}: fp16 or bf16 expected")
 
 
+_raw_stream_getter = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _raw_stream(device_index: int) -> int:
+    """cudaStream_t of the device's current stream, as an integer."""
+    if _raw_stream_getter is not None:
+        return _raw_stream_getter(device_index)
+    return torch.cuda.current_stream(device_index).cuda_stream
+
+
 def _stream(t: torch.Tensor):
-    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+    return ctypes.c_void_p(_raw_stream(t.device.index if t.device.index is not None
+                                       else torch.cuda.current_device()))
+
+
+class PreparedCall:
+    """One library call whose arguments were checked and marshalled once.
+
+    Calling it enqueues the same call on the current stream of its device and
+    returns the call's output tensor (or None).  It holds the tensors it was
+    prepared with; they must keep their storage, while their contents may change
+    between calls (new queries and rows, new context lengths within the bound
+    given at preparation)."""
+    __slots__ = ("_fn", "_args", "_dev", "_what", "_tensors", "_result")
+
+    def __init__(self, what: str, args: tuple, device: torch.device, tensors: tuple, result=None):
+        self._fn = getattr(lib(), what)
+        self._args = args
+        self._dev = device.index if device.index is not None else torch.cuda.current_device()
+        self._what = what
+        self._tensors = tensors
+        self._result = result
+
+    def __call__(self):
+        st = self._fn(*self._args, _raw_stream(self._dev))
+        if st != 0:
+            raise PagedKVError(self._what, st)
+        return self._result
 
 
 def _check(status: int, what: str):
@@ -65,6 +106,12 @@ def split_pool(kv: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
 def reshape_and_cache(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
                       k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
     """Write new K/V rows [T, Hkv, d] into their slots (bit-exact); slot < 0 skips."""
+    prepare_reshape_and_cache(k_new, v_new, slot_mapping, k_cache, v_cache)()
+
+
+def prepare_reshape_and_cache(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                              k_cache: torch.Tensor, v_cache: torch.Tensor) -> PreparedCall:
+    """reshape_and_cache, checked and marshalled once (see PreparedCall)."""
     nb, hkv, bs, d, stride = _cache_geometry(k_cache, v_cache)
     t = int(k_new.shape[0])
     if k_new.shape != (t, hkv, d) or v_new.shape != k_new.shape:
@@ -75,10 +122,10 @@ def reshape_and_cache(k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: to
         raise ValueError("slot_mapping must be int64 [T]")
     if k_new.dtype != k_cache.dtype or v_new.dtype != k_cache.dtype:
         raise ValueError("k_new/v_new dtype must match the cache")
-    st = lib().pkv_reshape_and_cache(
-        k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), t, k_cache.data_ptr(),
-        v_cache.data_ptr(), nb, stride, hkv, d, bs, _dtype_code(k_cache), _stream(k_cache))
-    _check(st, "pkv_reshape_and_cache")
+    args = (k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), t, k_cache.data_ptr(),
+            v_cache.data_ptr(), nb, stride, hkv, d, bs, _dtype_code(k_cache))
+    return PreparedCall("pkv_reshape_and_cache", args, k_cache.device,
+                        (k_new, v_new, slot_mapping, k_cache, v_cache))
 
 
 def decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
@@ -112,6 +159,18 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     context_lens int32 [num_seqs].  ``max_context_len`` (a host int) bounds
     context_lens; if omitted it is read back from the device (a synchronisation).
     """
+    return prepare_paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                          out, max_context_len=max_context_len,
+                                          partition_size=partition_size, workspace=workspace)()
+
+
+def prepare_paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                   block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                   scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                                   *, max_context_len: Optional[int] = None, partition_size: int = 0,
+                                   workspace: Optional[torch.Tensor] = None) -> PreparedCall:
+    """paged_attention_decode, checked and marshalled once (see PreparedCall); the
+    call returns ``out``.  Later context lengths must stay within max_context_len."""
     nb, hkv, bs, d, stride = _cache_geometry(k_cache, v_cache)
     if q.dim() != 3 or q.shape[2] != d or not q.is_contiguous():
         raise ValueError(f"q must be a contiguous [num_seqs, num_q_heads, {d}]")
@@ -136,13 +195,11 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         workspace = _workspace(q.device, need)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = lib().pkv_paged_attention_decode(
-        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), nb, stride, block_tables.data_ptr(),
-        int(block_tables.shape[1]), context_lens.data_ptr(), int(max_context_len), b, hq, hkv, d, bs,
-        float(scale), out.data_ptr(), ws_ptr, ws_bytes, int(partition_size), _dtype_code(q),
-        _stream(q))
-    _check(st, "pkv_paged_attention_decode")
-    return out
+    args = (q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), nb, stride, block_tables.data_ptr(),
+            int(block_tables.shape[1]), context_lens.data_ptr(), int(max_context_len), b, hq, hkv, d,
+            bs, float(scale), out.data_ptr(), ws_ptr, ws_bytes, int(partition_size), _dtype_code(q))
+    return PreparedCall("pkv_paged_attention_decode", args, q.device,
+                        (q, k_cache, v_cache, block_tables, context_lens, out, workspace), out)
 
 
 def shared_prefix_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
@@ -165,7 +222,20 @@ def paged_attention_decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor,
                                          workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """paged_attention_decode for a batch that shares its first prefix_len tokens
     (prefix_block_table holds their blocks): the prefix is attended by all query
-    rows together as dense tiles, then each sequence's suffix, then a merge."""
+    rows together as dense tiles, beside each sequence's suffix, then a merge."""
+    return prepare_paged_attention_decode_shared_prefix(
+        q, k_cache, v_cache, prefix_block_table, prefix_len, block_tables, context_lens, scale, out,
+        max_context_len=max_context_len, partition_size=partition_size, workspace=workspace)()
+
+
+def prepare_paged_attention_decode_shared_prefix(
+        q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+        prefix_block_table: torch.Tensor, prefix_len: int, block_tables: torch.Tensor,
+        context_lens: torch.Tensor, scale: Optional[float] = None,
+        out: Optional[torch.Tensor] = None, *, max_context_len: Optional[int] = None,
+        partition_size: int = 0, workspace: Optional[torch.Tensor] = None) -> PreparedCall:
+    """paged_attention_decode_shared_prefix, checked and marshalled once (see
+    PreparedCall); the call returns ``out``."""
     nb, hkv, bs, d, stride = _cache_geometry(k_cache, v_cache)
     if q.dim() != 3 or q.shape[2] != d or not q.is_contiguous() or q.dtype != k_cache.dtype:
         raise ValueError(f"q must be a contiguous [num_seqs, num_q_heads, {d}] of the cache dtype")
@@ -186,15 +256,14 @@ def paged_attention_decode_shared_prefix(q: torch.Tensor, k_cache: torch.Tensor,
                                          partition_size)
     if workspace is None:
         workspace = _workspace(q.device, need)
-    st = lib().pkv_paged_attention_decode_shared_prefix(
-        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), nb, stride,
-        prefix_block_table.data_ptr(), int(prefix_len), block_tables.data_ptr(),
-        int(block_tables.shape[1]), context_lens.data_ptr(), int(max_context_len), b, hq, hkv, d,
-        bs, float(scale), out.data_ptr(), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), int(partition_size), _dtype_code(q),
-        _stream(q))
-    _check(st, "pkv_paged_attention_decode_shared_prefix")
-    return out
+    args = (q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), nb, stride,
+            prefix_block_table.data_ptr(), int(prefix_len), block_tables.data_ptr(),
+            int(block_tables.shape[1]), context_lens.data_ptr(), int(max_context_len), b, hq, hkv, d,
+            bs, float(scale), out.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), int(partition_size), _dtype_code(q))
+    return PreparedCall("pkv_paged_attention_decode_shared_prefix", args, q.device,
+                        (q, k_cache, v_cache, prefix_block_table, block_tables, context_lens, out,
+                         workspace), out)
 
 
 def prefill_workspace_bytes(num_rows, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
@@ -284,6 +353,14 @@ def reshape_and_cache_int8(k_new: torch.Tensor, v_new: torch.Tensor, slot_mappin
                            v_scale: torch.Tensor) -> None:
     """Quantise new K/V rows [T, Hkv, d] (fp16/bf16) with per-channel scales [Hkv, d]
     and write the codes into their slots of an INT8 cache; slot < 0 skips."""
+    prepare_reshape_and_cache_int8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale)()
+
+
+def prepare_reshape_and_cache_int8(k_new: torch.Tensor, v_new: torch.Tensor,
+                                   slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+                                   v_cache: torch.Tensor, k_scale: torch.Tensor,
+                                   v_scale: torch.Tensor) -> PreparedCall:
+    """reshape_and_cache_int8, checked and marshalled once (see PreparedCall)."""
     nb, hkv, bs, d, stride = _check_int8_cache(k_cache, v_cache, k_scale, v_scale)
     t = int(k_new.shape[0])
     if k_new.shape != (t, hkv, d) or v_new.shape != k_new.shape or v_new.dtype != k_new.dtype:
@@ -292,11 +369,11 @@ def reshape_and_cache_int8(k_new: torch.Tensor, v_new: torch.Tensor, slot_mappin
         raise ValueError("k_new, v_new and slot_mapping must be contiguous")
     if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != t:
         raise ValueError("slot_mapping must be int64 [T]")
-    st = lib().pkv_reshape_and_cache_int8(
-        k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), t, k_cache.data_ptr(),
-        v_cache.data_ptr(), nb, stride, hkv, d, bs, k_scale.data_ptr(), v_scale.data_ptr(),
-        _dtype_code(k_new), _stream(k_cache))
-    _check(st, "pkv_reshape_and_cache_int8")
+    args = (k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), t, k_cache.data_ptr(),
+            v_cache.data_ptr(), nb, stride, hkv, d, bs, k_scale.data_ptr(), v_scale.data_ptr(),
+            _dtype_code(k_new))
+    return PreparedCall("pkv_reshape_and_cache_int8", args, k_cache.device,
+                        (k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale))
 
 
 def decode_int8_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
@@ -316,6 +393,21 @@ def paged_attention_decode_int8(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
                                 workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """paged_attention_decode over an INT8 cache whose values are code * scale[h][channel];
     q and out fp16 or bf16."""
+    return prepare_paged_attention_decode_int8(
+        q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, scale, out,
+        max_context_len=max_context_len, partition_size=partition_size, workspace=workspace)()
+
+
+def prepare_paged_attention_decode_int8(q: torch.Tensor, k_cache: torch.Tensor,
+                                        v_cache: torch.Tensor, k_scale: torch.Tensor,
+                                        v_scale: torch.Tensor, block_tables: torch.Tensor,
+                                        context_lens: torch.Tensor, scale: Optional[float] = None,
+                                        out: Optional[torch.Tensor] = None, *,
+                                        max_context_len: Optional[int] = None,
+                                        partition_size: int = 0,
+                                        workspace: Optional[torch.Tensor] = None) -> PreparedCall:
+    """paged_attention_decode_int8, checked and marshalled once (see PreparedCall); the
+    call returns ``out``."""
     nb, hkv, bs, d, stride = _check_int8_cache(k_cache, v_cache, k_scale, v_scale)
     if q.dim() != 3 or q.shape[2] != d or not q.is_contiguous():
         raise ValueError(f"q must be a contiguous [num_seqs, num_q_heads, {d}]")
@@ -338,13 +430,13 @@ def paged_attention_decode_int8(q: torch.Tensor, k_cache: torch.Tensor, v_cache:
         workspace = _workspace(q.device, need)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = lib().pkv_paged_attention_decode_int8(
-        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
-        v_scale.data_ptr(), nb, stride, block_tables.data_ptr(), int(block_tables.shape[1]),
-        context_lens.data_ptr(), int(max_context_len), b, hq, hkv, d, bs, float(scale),
-        out.data_ptr(), ws_ptr, ws_bytes, int(partition_size), _dtype_code(q), _stream(q))
-    _check(st, "pkv_paged_attention_decode_int8")
-    return out
+    args = (q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), k_scale.data_ptr(),
+            v_scale.data_ptr(), nb, stride, block_tables.data_ptr(), int(block_tables.shape[1]),
+            context_lens.data_ptr(), int(max_context_len), b, hq, hkv, d, bs, float(scale),
+            out.data_ptr(), ws_ptr, ws_bytes, int(partition_size), _dtype_code(q))
+    return PreparedCall("pkv_paged_attention_decode_int8", args, q.device,
+                        (q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens, out,
+                         workspace), out)
 
 
 def get_device_error(device: Optional[torch.device] = None) -> Tuple[int, list]:
