@@ -26,16 +26,17 @@ EncodeTiledFn encode_tiled_fn() {
 }
 
 // 3-D view of one half (K or V) of the pool: (head_dim, num_kv_heads*block_size
-// rows, num_blocks) with the caller's block stride; boxes are one block's rows
-// of one head, 64 columns wide, 128-byte swizzled.
+// rows, num_blocks) with the caller's block stride; boxes are box_rows rows of one
+// head (0: a whole block's), 64 columns wide, 128-byte swizzled.
 bool encode_half_map(CUtensorMap *map, const void *base, int64_t num_blocks,
-                     int64_t block_stride_elems, int num_kv_heads, int block_size, pkv_dtype dt) {
+                     int64_t block_stride_elems, int num_kv_heads, int block_size, pkv_dtype dt,
+                     int box_rows) {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(num_kv_heads) * block_size,
                                 static_cast<cuuint64_t>(num_blocks)};
     const cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(block_stride_elems) * 2};
-    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(block_size), 1};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows > 0 ? box_rows : block_size), 1};
     const cuuint32_t elem_strides[3] = {1, 1, 1};
     return fn(map, dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
               3, const_cast<void *>(base), dims, strides, box, elem_strides,
@@ -150,6 +151,24 @@ size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, i
     return workspace_for(num_seqs, num_q_heads, head_dim, nparts);
 }
 
+// Tensor maps of the swizzled warp-MMA staging: INT8 boxes of one block's token
+// rows (128 codes each); 16-bit boxes of one stage's token rows (min(block_size,
+// 16)) by 64 channels.
+bool encode_decode_maps(pkv::DecodeMaps *maps, const void *k_cache, const void *v_cache,
+                        bool int8_kv, int64_t num_blocks, int64_t block_stride_elems,
+                        int num_kv_heads, int block_size, pkv_dtype dtype) {
+    if (int8_kv)
+        return pkv::encode_i8_half_map(&maps->k, k_cache, num_blocks, block_stride_elems, num_kv_heads,
+                                       block_size) &&
+               pkv::encode_i8_half_map(&maps->v, v_cache, num_blocks, block_stride_elems, num_kv_heads,
+                                       block_size);
+    const int rows = std::min(block_size, 16);
+    return pkv::encode_half_map(&maps->k, k_cache, num_blocks, block_stride_elems, num_kv_heads,
+                                block_size, dtype, rows) &&
+           pkv::encode_half_map(&maps->v, v_cache, num_blocks, block_stride_elems, num_kv_heads,
+                                block_size, dtype, rows);
+}
+
 // Decode over a 16-bit cache (k_scale == v_scale == nullptr) or an INT8 cache
 // with per-channel scales.  Element strides and offsets count cache elements.
 pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
@@ -231,12 +250,12 @@ pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(static_cast<unsigned>(nparts), static_cast<unsigned>(num_kv_heads * p.subgroups),
                     static_cast<unsigned>(num_seqs));
-    // The INT8 warp-MMA form at head_dim 128 (4 or 8 heads per block) stages K/V
-    // tiles by tiled TMA copies with a 128-byte swizzle
+    // The warp-MMA forms at head_dim 128 (4 or 8 heads per block) stage K/V tiles by
+    // tiled TMA copies with a 128-byte swizzle
     pkv::DecodeMaps maps{};
-    if (int8_kv && head_dim == 128 && gh >= 4 &&
-        (!pkv::encode_i8_half_map(&maps.k, k_cache, num_blocks, block_stride_elems, num_kv_heads, block_size) ||
-         !pkv::encode_i8_half_map(&maps.v, v_cache, num_blocks, block_stride_elems, num_kv_heads, block_size)))
+    if (head_dim == 128 && gh >= 4 &&
+        !encode_decode_maps(&maps, k_cache, v_cache, int8_kv, num_blocks, block_stride_elems,
+                            num_kv_heads, block_size, dtype))
         return PKV_ERR_CUDA;
     if (int8_kv)
         return dtype == PKV_F16
@@ -414,8 +433,8 @@ PKV_API pkv_status pkv_paged_attention_decode_shared_prefix(
     unsigned int *status = pkv::status_word_ptr();
     if (!status) return PKV_ERR_CUDA;
     CUtensorMap tk, tv;
-    if (!pkv::encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads, block_size, dtype) ||
-        !pkv::encode_half_map(&tv, v_cache, num_blocks, block_stride_elems, num_kv_heads, block_size, dtype))
+    if (!pkv::encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads, block_size, dtype, 0) ||
+        !pkv::encode_half_map(&tv, v_cache, num_blocks, block_stride_elems, num_kv_heads, block_size, dtype, 0))
         return PKV_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int group = num_q_heads / num_kv_heads;
@@ -482,7 +501,10 @@ PKV_API pkv_status pkv_paged_attention_decode_shared_prefix(
     const int merge_rows = num_seqs * num_q_heads;
     const dim3 grid(static_cast<unsigned>(cp.suffix_parts), static_cast<unsigned>(p.items_y),
                     static_cast<unsigned>(num_seqs));
-    const pkv::DecodeMaps maps{};  // 16-bit forms stage by 1-D bulk copies
+    pkv::DecodeMaps maps{};
+    if (cp.gh >= 4 && !encode_decode_maps(&maps, k_cache, v_cache, false, num_blocks, block_stride_elems,
+                                          num_kv_heads, block_size, dtype))
+        return PKV_ERR_CUDA;
     return dtype == PKV_F16
                ? pkv::launch_decode_f16(p, maps, head_dim, block_size, cp.gh, grid, merge_rows, s)
                : pkv::launch_decode_bf16(p, maps, head_dim, block_size, cp.gh, grid, merge_rows, s);

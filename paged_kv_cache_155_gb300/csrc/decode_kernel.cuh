@@ -185,9 +185,10 @@ struct DecodeGeom {
     static constexpr int kStagesRaw = kBudget / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kMaxTableEntries = 1024;        // table slice per partition
-    // INT8 warp-MMA form at head_dim 128: K/V tiles arrive by tiled TMA copies with a
-    // 128-byte swizzle, whose 8-row atoms need 1024-byte-aligned stages
-    static constexpr bool kSwizzled = EB == 1 && kMmaForm && D == 128;
+    // Warp-MMA forms at head_dim 128: K/V tiles arrive by tiled TMA copies with a
+    // 128-byte swizzle (16-bit tiles as two 64-channel half panels), whose 8-row
+    // atoms need 1024-byte-aligned stages
+    static constexpr bool kSwizzled = kMmaForm && D == 128;
     static constexpr int kAlignPad = kSwizzled ? 1024 : 0;
     static constexpr int kSmemBytes = kWarps * kStages * kStageBytes +
                                       kWarps * kStages * 8 + kMaxTableEntries * 4 + kAlignPad;
@@ -195,9 +196,10 @@ struct DecodeGeom {
 };
 
 // T: query / output type; KT: cache storage type (T, or int8_t for the INT8 cache).
-// tmap_k / tmap_v: tiled tensor maps of the INT8 pool halves (box: one block's
-// TILE token rows of one head, 128 bytes each, 128-byte swizzle), used by the
-// INT8 warp-MMA form at head_dim 128; the other forms ignore them.
+// tmap_k / tmap_v: tiled tensor maps of the pool halves (box: TILE token rows of
+// one head, 128 bytes each -- all 128 INT8 codes, or 64 16-bit values -- with a
+// 128-byte swizzle), used by the warp-MMA forms at head_dim 128; the other forms
+// ignore them.
 template <typename T, typename KT, int D, int BS, int GH>
 __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                               const __grid_constant__ CUtensorMap tmap_v,
@@ -222,8 +224,9 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const __grid_const
         blockIdx.z == gridDim.z - 1)
         pdl_wait();  // uniform over the CTA; normally dispatched last, when nothing is left to wait for
 
-    // INT8 warp-MMA form at head_dim 128: stages filled by swizzled tiled TMA copies
+    // warp-MMA forms at head_dim 128: stages filled by swizzled tiled TMA copies
     constexpr bool kSwz = G::kSwizzled;
+    constexpr int kHalfBytes = TILE * 128;  // 16-bit swizzled tiles: one 64-channel half panel
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *smem = smem_raw;
     if constexpr (kSwz)
@@ -297,11 +300,20 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const __grid_const
                             (static_cast<int64_t>(kvh) * BS + r0) * D;
         unsigned char *dst = my_stages + s * G::kStageBytes;
         mbar_arrive_expect_tx(&my_bars[s], G::kStageBytes);
-        if constexpr (kSwz) {
+        if constexpr (kSwz && kQuant) {
             // token row t of the tile lands as 128 bytes whose 16-byte chunk c sits at
             // chunk c ^ (t & 7)
             tc::tma_load_3d(dst, &tmap_k, 0, kvh * BS + r0, b, &my_bars[s], policy);
             tc::tma_load_3d(dst + G::kTileBytes, &tmap_v, 0, kvh * BS + r0, b, &my_bars[s], policy);
+        } else if constexpr (kSwz) {
+            // 16-bit: channels 64 c .. 64 c + 63 of token row t land in half panel c
+            // as 128 bytes whose 16-byte chunk j sits at chunk j ^ (t & 7)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                tc::tma_load_3d(dst + c * kHalfBytes, &tmap_k, 64 * c, kvh * BS + r0, b, &my_bars[s], policy);
+                tc::tma_load_3d(dst + G::kTileBytes + c * kHalfBytes, &tmap_v, 64 * c, kvh * BS + r0, b,
+                                &my_bars[s], policy);
+            }
         } else {
             bulk_copy_g2s(dst, kc + off, G::kTileBytes, &my_bars[s], policy);
             bulk_copy_g2s(dst + G::kTileBytes, vc + off, G::kTileBytes, &my_bars[s], policy);
@@ -447,10 +459,13 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const __grid_const
             mqb = mqs * (kCodeOffset * qsum);
         } else {
             // 16-bit cache: the query enters unchanged (the cache's type), the
-            // scores take scale * log2(e) in fp32
+            // scores take scale * log2(e) in fp32.  Swizzled staging: lane t's vector
+            // j holds channels 64 (j / 2) + 16 t + 8 (j % 2) .. + 7, chunk 2 t + j % 2
+            // of half panel j / 2, like its K vectors
 #pragma unroll
             for (int j = 0; j < D / (4 * RUN); ++j) {
-                const uint4 u = mg < GH ? *reinterpret_cast<const uint4 *>(qrow + 4 * RUN * j) : make_uint4(0, 0, 0, 0);
+                const int qofs = kSwz ? 64 * (j >> 1) + 8 * (j & 1) : 4 * RUN * j;
+                const uint4 u = mg < GH ? *reinterpret_cast<const uint4 *>(qrow + qofs) : make_uint4(0, 0, 0, 0);
                 qa[2 * j][0] = u.x;
                 qa[2 * j][1] = u.y;
                 qa[2 * j + 1][0] = u.z;
@@ -643,10 +658,15 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const __grid_const
                     for (int h = 0; h < STEP / 8; ++h) {
                         sacc[h][0] = sacc[h][1] = sacc[h][2] = sacc[h][3] = 0.f;
                         sodd[h][0] = sodd[h][1] = sodd[h][2] = sodd[h][3] = 0.f;
-                        const unsigned char *krow = kt + ((tb + 8 * h + mg) * D + RUN * mt) * 2;
+                        const int kr = tb + 8 * h + mg;  // token row (= mg mod 8)
+                        const unsigned char *krow = kt + (kr * D + RUN * mt) * 2;
 #pragma unroll
                         for (int j = 0; j < D / (4 * RUN); ++j) {
-                            const uint4 u = *reinterpret_cast<const uint4 *>(krow + 64 * j);
+                            // swizzled: chunk 2 mt + j % 2 of half panel j / 2, at chunk ^ mg
+                            const unsigned char *kp =
+                                kSwz ? kt + (j >> 1) * kHalfBytes + kr * 128 + ((((2 * mt + (j & 1)) ^ mg) & 7) << 4)
+                                     : krow + 64 * j;
+                            const uint4 u = *reinterpret_cast<const uint4 *>(kp);
                             mma_16816<kMmaBF16>(sacc[h], qa[2 * j][0], 0u, qa[2 * j][1], 0u, u.x, u.y);
                             mma_16816<kMmaBF16>(sodd[h], qa[2 * j + 1][0], 0u, qa[2 * j + 1][1], 0u, u.z, u.w);
                         }
@@ -696,14 +716,35 @@ __global__ void __launch_bounds__(128, 1) paged_decode_kernel(const __grid_const
                     const unsigned char *vrow = vt + ((tb + 2 * mt) * D + (D / 8) * mg) * 2;
 #pragma unroll
                     for (int r = 0; r < STEP / 4; ++r) {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(vrow + ((r >> 1) * 8 + (r & 1)) * D * 2);
+                        if constexpr (kSwz) {
+                            // this lane's channels 16 mg .. + 15 are chunks 2 mg, 2 mg + 1 (mod 8) of
+                            // half panel mg / 4, at chunk ^ (row & 7); odd mg read the second
+                            // chunk first, which keeps the eight lanes of a quarter-warp on
+                            // eight different chunks
+                            const int vr = tb + 2 * mt + (r >> 1) * 8 + (r & 1);
+                            const unsigned char *vp = vt + (mg >> 2) * kHalfBytes + vr * 128;
+                            const int odd = mg & 1;
+                            const uint4 a = *reinterpret_cast<const uint4 *>(vp + ((((2 * mg + odd) ^ vr) & 7) << 4));
+                            const uint4 c = *reinterpret_cast<const uint4 *>(vp + ((((2 * mg + 1 - odd) ^ vr) & 7) << 4));
+                            const uint4 lo = odd ? c : a, hi = odd ? a : c;
+                            x[r][0] = lo.x;
+                            x[r][1] = lo.y;
+                            x[r][2] = lo.z;
+                            x[r][3] = lo.w;
+                            x[r][4] = hi.x;
+                            x[r][5] = hi.y;
+                            x[r][6] = hi.z;
+                            x[r][7] = hi.w;
+                        } else {
+                            const uint4 *src = reinterpret_cast<const uint4 *>(vrow + ((r >> 1) * 8 + (r & 1)) * D * 2);
 #pragma unroll
-                        for (int v = 0; v < VW / 4; ++v) {
-                            const uint4 u = src[v];
-                            x[r][4 * v] = u.x;
-                            x[r][4 * v + 1] = u.y;
-                            x[r][4 * v + 2] = u.z;
-                            x[r][4 * v + 3] = u.w;
+                            for (int v = 0; v < VW / 4; ++v) {
+                                const uint4 u = src[v];
+                                x[r][4 * v] = u.x;
+                                x[r][4 * v + 1] = u.y;
+                                x[r][4 * v + 2] = u.z;
+                                x[r][4 * v + 3] = u.w;
+                            }
                         }
                     }
                     if (tb + STEP > valid) {  // warp-uniform: a step that ends past the context

@@ -20,11 +20,12 @@ int current_sm_count();
 void count_launch();
 
 // Tiled tensor map of one half (K or V) of a 16-bit pool for 3-D TMA loads:
-// dims (head_dim 128, num_kv_heads * block_size rows, num_blocks), boxes of one
-// block's rows of one head, 64 columns wide, 128-byte swizzled.  False if the
-// driver entry point is missing or the encode fails.
+// dims (head_dim 128, num_kv_heads * block_size rows, num_blocks), boxes of
+// box_rows rows of one head (0: a whole block's), 64 columns wide, 128-byte
+// swizzled.  False if the driver entry point is missing or the encode fails.
 bool encode_half_map(CUtensorMap *map, const void *base, int64_t num_blocks,
-                     int64_t block_stride_elems, int num_kv_heads, int block_size, pkv_dtype dt);
+                     int64_t block_stride_elems, int num_kv_heads, int block_size, pkv_dtype dt,
+                     int box_rows);
 
 // Tiled tensor map of one half (K or V) of an INT8 pool with head_dim 128 for
 // 3-D TMA loads: dims (128 codes, num_kv_heads * block_size rows, num_blocks),

@@ -159,9 +159,9 @@ PKV_API pkv_status pkv_paged_attention_prefill(
     CUtensorMap tq, tk, tv;
     if (!pkv::encode_query_map(&tq, q, num_rows, num_q_heads, group, pp.tile_tokens, dtype) ||
         !pkv::encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads, block_size,
-                              dtype) ||
+                              dtype, 0) ||
         !pkv::encode_half_map(&tv, v_cache, num_blocks, block_stride_elems, num_kv_heads, block_size,
-                              dtype))
+                              dtype, 0))
         return PKV_ERR_CUDA;
 
     pkv::PrefillParams p{};
