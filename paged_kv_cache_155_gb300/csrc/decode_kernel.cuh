@@ -201,7 +201,8 @@ struct DecodeGeom {
 // 128-byte swizzle), used by the warp-MMA forms at head_dim 128; the other forms
 // ignore them.
 template <typename T, typename KT, int D, int BS, int GH>
-__global__ void __launch_bounds__(128, 1) paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+__global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                               const __grid_constant__ CUtensorMap tmap_v,
                                                               const DecodeParams p) {
     constexpr bool kQuant = sizeof(KT) == 1;
