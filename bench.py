@@ -7,7 +7,8 @@ the Llama-2-7B-shaped MHA decode layer (32 sequences x 4096 tokens, 32 heads of
 128, block 16, fp16, 2 GiB pool -- larger than L2, so no flush is needed).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload mha7b|gqa7b|prefix|long70b|tiny] [--partition P]
+                    [--workload mha7b|gqa7b|prefix|long70b|tiny|mha7b_int8|gqa7b_int8|long70b_int8]
+                    [--partition P]
 
 Prints one JSON line (rank 0).  `value` is decode tokens/s (one token per
 sequence per step) over all ranks, device-timed with inputs resident in HBM;
@@ -282,6 +283,36 @@ def _oracle_units(wl_host, pool_bits, units, q_bits):
     return time.perf_counter() - t0
 
 
+def _oracle_int8_seqs(wl_host, pool_i8, seqs, q_bits):
+    """The INT8 oracle on whole sequences (every KV head); returns seconds."""
+    import numpy as np
+    import oracle
+    code = oracle.BF16 if str(wl_host.dtype).endswith("bfloat16") else oracle.F16
+    sel = np.array(seqs)
+    t0 = time.perf_counter()
+    oracle.paged_decode_int8(q_bits[sel], pool_i8, wl_host.k_scale.numpy(), wl_host.v_scale.numpy(),
+                             wl_host.block_tables.numpy()[sel], wl_host.context_lens.numpy()[sel],
+                             wl_host.num_kv_heads, wl_host.block_size, wl_host.scale, code)
+    return time.perf_counter() - t0
+
+
+def _oracle_sample(wl_host, pool, qb, n, start):
+    """The oracle on n work units from `start` on: (sequence, KV head) units of a 16-bit
+    pool, whole sequences of an INT8 one.  Returns (seconds, decode tokens done)."""
+    if wl_host.k_scale is not None:
+        seqs = [(start + k) % wl_host.num_seqs for k in range(n)]
+        return _oracle_int8_seqs(wl_host, pool, seqs, qb), float(n)
+    return _oracle_units(wl_host, pool, _unit_list(wl_host, n, start), qb), n / wl_host.num_kv_heads
+
+
+def _pool_host(wl_host):
+    """Host pool in the oracle's form: 16-bit patterns, or the INT8 codes."""
+    import torch
+    if wl_host.kv.dtype == torch.int8:
+        return wl_host.kv.contiguous().numpy()
+    return _bits(wl_host.kv)
+
+
 def _unit_list(wl_host, n, start=0):
     total = wl_host.num_seqs * wl_host.num_kv_heads
     out = []
@@ -301,20 +332,19 @@ def cpu_baseline(wl_dev, budget_s=12.0):
     """The oracle on a bounded sample of the workload, on this host's cores."""
     import oracle
     wl_host = wl_dev.to("cpu")
-    pool = _bits(wl_host.kv)
+    pool = _pool_host(wl_host)
     qb = _bits(wl_host.q)
-    units = _unit_list(wl_host, 1)
-    t1 = _oracle_units(wl_host, pool, units, qb)
-    total = wl_host.num_seqs * wl_host.num_kv_heads
+    i8 = wl_host.k_scale is not None
+    t1, _ = _oracle_sample(wl_host, pool, qb, 1, 0)
+    total = wl_host.num_seqs * (1 if i8 else wl_host.num_kv_heads)
     n = max(1, min(64 * total, int(budget_s / max(t1, 1e-6))))   # whole steps repeat if cheap
-    units = _unit_list(wl_host, n, start=1)
-    t = _oracle_units(wl_host, pool, units, qb)
-    tokens = n / wl_host.num_kv_heads  # one decode token = all KV heads of one sequence
+    t, tokens = _oracle_sample(wl_host, pool, qb, n, 1)
+    unit = "whole sequences" if i8 else "(sequence, KV head) units"
     return {"value": tokens / t, "unit": "tokens/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{n} (sequence, KV head) units of {wl_host.num_seqs}x{wl_host.num_kv_heads}"
+            "sample": f"{n} {unit} of {wl_host.num_seqs}x{wl_host.num_kv_heads}"
                       f" ({n / total:.3f} steps' worth),"
-                      f" {t:.1f} s, fp64 C oracle, OpenMP over query heads of a unit"}
+                      f" {t:.1f} s, fp64 C oracle, OpenMP over query heads"}
 
 
 def run_reference(args):
@@ -325,23 +355,25 @@ def run_reference(args):
     import oracle
     oracle.build()
     wl = _make_workload(args.workload, "cpu", 1234, args.num_seqs)
-    pool, qb = _bits(wl.kv), _bits(wl.q)
+    pool, qb = _pool_host(wl), _bits(wl.q)
+    i8 = wl.k_scale is not None
     per_step_budget = max(0.002, 150.0 / max(1, args.steps + args.warmup))
-    t1 = _oracle_units(wl, pool, _unit_list(wl, 1), qb)
-    n = max(1, min(wl.num_seqs * wl.num_kv_heads, int(per_step_budget / max(t1, 1e-6))))
+    t1, _ = _oracle_sample(wl, pool, qb, 1, 0)
+    n = max(1, min(wl.num_seqs * (1 if i8 else wl.num_kv_heads), int(per_step_budget / max(t1, 1e-6))))
     cursor = 1
     for _ in range(args.warmup):
-        _oracle_units(wl, pool, _unit_list(wl, n, cursor), qb)
+        _oracle_sample(wl, pool, qb, n, cursor)
         cursor += n
-    total = 0.0
+    total, tokens = 0.0, 0.0
     for _ in range(args.steps):
-        total += _oracle_units(wl, pool, _unit_list(wl, n, cursor), qb)
+        dt, tk = _oracle_sample(wl, pool, qb, n, cursor)
+        total += dt
+        tokens += tk
         cursor += n
-    tokens = args.steps * n / wl.num_kv_heads
     value = tokens / total
     ms_full = 1000.0 * wl.num_seqs / value
-    sample = (f"each step {n} (sequence, KV head) units of {wl.num_seqs}x{wl.num_kv_heads}; "
-              f"fp64 C oracle")
+    unit = "whole sequences" if i8 else "(sequence, KV head) units"
+    sample = f"each step {n} {unit} of {wl.num_seqs}x{wl.num_kv_heads}; fp64 C oracle"
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_full,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -796,7 +828,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mha7b",
-                    choices=["tiny", "mha7b", "gqa7b", "prefix", "long70b"])
+                    choices=["tiny", "mha7b", "gqa7b", "prefix", "long70b", "mha7b_int8",
+                             "gqa7b_int8", "long70b_int8"])
     ap.add_argument("--partition", type=int, default=-1,
                     help="tokens per split-context partition (0 = library's choice; "
                          "default: the workload's own setting)")
