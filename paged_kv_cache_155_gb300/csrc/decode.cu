@@ -247,6 +247,7 @@ pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
 
     const int merge_rows = merge ? num_seqs * num_q_heads : 0;
+    p.trigger_dependents = merge_rows > 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(static_cast<unsigned>(nparts), static_cast<unsigned>(num_kv_heads * p.subgroups),
                     static_cast<unsigned>(num_seqs));
@@ -498,6 +499,7 @@ PKV_API pkv_status pkv_paged_attention_decode_shared_prefix(
     p.slot_base = cp.splits;
     p.always_partial = 1;
     p.wait_prior_grid = 1;  // overlaps the prefix tiles; the merge still follows both
+    p.trigger_dependents = 1;
     const int merge_rows = num_seqs * num_q_heads;
     const dim3 grid(static_cast<unsigned>(cp.suffix_parts), static_cast<unsigned>(p.items_y),
                     static_cast<unsigned>(num_seqs));

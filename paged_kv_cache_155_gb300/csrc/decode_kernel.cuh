@@ -107,6 +107,10 @@ struct DecodeParams {
     // last block index waits for that kernel before it exits, so this grid -- and
     // whatever the stream runs after it -- completes only after that kernel.
     int wait_prior_grid;
+    // Set when the library's merge kernel follows as a programmatic dependent: the
+    // CTAs signal at their start that it may be placed.  Without it the next kernel
+    // of the stream starts only when this grid has completed.
+    int trigger_dependents;
 };
 
 // Tensor maps of the two pool halves for the forms that stage by tiled TMA
@@ -219,8 +223,8 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
     static_assert(ITERS % IT_STEP == 0, "step must divide the stage");
     static_assert(GH * (D + 4) * 4 <= S * G::kStageBytes, "merge scratch must fit a warp's stages");
 
-    // the merge kernel, launched behind this one, may start as this grid's CTAs run
-    pdl_trigger();
+    // the merge kernel, launched behind this one, may be placed as this grid's CTAs run
+    if (p.trigger_dependents) pdl_trigger();
     if (p.wait_prior_grid && blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 &&
         blockIdx.z == gridDim.z - 1)
         pdl_wait();  // uniform over the CTA; normally dispatched last, when nothing is left to wait for
