@@ -184,6 +184,30 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0,
         : "memory");
 }
 
+// Shared memory -> global memory: the box at (c0, c1, c2) of `tmap` from `src`
+// (laid out as the matching tma_load_3d would have written it), in this
+// thread's current bulk group.
+__device__ __forceinline__ void tma_store_3d(const void *tmap, int c0, int c1, int c2, const void *src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(static_cast<uint32_t>(__cvta_generic_to_shared(src)))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The shared-memory sources of this thread's bulk groups have been read.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// This thread's bulk groups have completed (their global writes are done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Warm L2 with the box a later tma_load_3d of the same coordinates will read (no
+// shared-memory destination, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0),
+                 "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // Byte offset of element (row, col) of a 128-byte-swizzled panel of 16-bit
 // values whose rows are 128 B (64 elements) and whose 8-row atoms are 1024 B.
 __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {

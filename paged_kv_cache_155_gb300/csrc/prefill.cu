@@ -61,7 +61,7 @@ size_t prefill_workspace(int num_rows, int num_q_heads, int splits) {
 
 template <typename T, int BS>
 pkv_status launch_prefill_one(const pkv::PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                              const CUtensorMap &tv, int grid, cudaStream_t stream) {
+                              const CUtensorMap &tv, const CUtensorMap &to, int grid, cudaStream_t stream) {
     static std::atomic<uint64_t> configured_devices{0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -74,19 +74,19 @@ pkv_status launch_prefill_one(const pkv::PrefillParams &p, const CUtensorMap &tq
         configured_devices.fetch_or(bit, std::memory_order_acq_rel);
     }
     pkv::paged_prefill_tc_kernel<T, BS>
-        <<<grid, pkv::PrefillLayout::kThreads, pkv::PrefillLayout::kSmemBytes, stream>>>(tq, tk, tv, p);
+        <<<grid, pkv::PrefillLayout::kThreads, pkv::PrefillLayout::kSmemBytes, stream>>>(tq, tk, tv, to, p);
     pkv::count_launch();
     return pkv::launch_status();
 }
 
 template <typename T>
 pkv_status launch_prefill(const pkv::PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                          const CUtensorMap &tv, int block_size, int grid, int max_query_len,
-                          cudaStream_t s) {
+                          const CUtensorMap &tv, const CUtensorMap &to, int block_size, int grid,
+                          int max_query_len, cudaStream_t s) {
     pkv_status st = PKV_ERR_UNSUPPORTED;
-    if (block_size == 8) st = launch_prefill_one<T, 8>(p, tq, tk, tv, grid, s);
-    else if (block_size == 16) st = launch_prefill_one<T, 16>(p, tq, tk, tv, grid, s);
-    else if (block_size == 32) st = launch_prefill_one<T, 32>(p, tq, tk, tv, grid, s);
+    if (block_size == 8) st = launch_prefill_one<T, 8>(p, tq, tk, tv, to, grid, s);
+    else if (block_size == 16) st = launch_prefill_one<T, 16>(p, tq, tk, tv, to, grid, s);
+    else if (block_size == 32) st = launch_prefill_one<T, 32>(p, tq, tk, tv, to, grid, s);
     if (st != PKV_OK || p.splits == 1) return st;
     const int64_t rows = static_cast<int64_t>(max_query_len) * p.num_q_heads;
     const dim3 mgrid(static_cast<unsigned>((rows + 3) / 4), static_cast<unsigned>(p.num_seqs));
@@ -156,8 +156,10 @@ PKV_API pkv_status pkv_paged_attention_prefill(
     if (sm == 0) sm = pkv::current_sm_count();
     if (sm <= 0) return PKV_ERR_CUDA;
     const int group = num_q_heads / num_kv_heads;
-    CUtensorMap tq, tk, tv;
+    // the output has the queries' shape: full row tiles leave through the same boxes
+    CUtensorMap tq, tk, tv, to;
     if (!pkv::encode_query_map(&tq, q, num_rows, num_q_heads, group, pp.tile_tokens, dtype) ||
+        !pkv::encode_query_map(&to, out, num_rows, num_q_heads, group, pp.tile_tokens, dtype) ||
         !pkv::encode_half_map(&tk, k_cache, num_blocks, block_stride_elems, num_kv_heads, block_size,
                               dtype, 0) ||
         !pkv::encode_half_map(&tv, v_cache, num_blocks, block_stride_elems, num_kv_heads, block_size,
@@ -190,13 +192,17 @@ PKV_API pkv_status pkv_paged_attention_prefill(
     p.num_items = pp.items;
     p.splits = pp.splits;
     p.split_tokens = pp.split_tokens;
+    // whole prompts of one length (every chunk max_query_len tokens on an empty
+    // cache): pair order, for L2 reuse of each (sequence, KV head)'s K/V tiles
+    p.pair_order = pp.splits == 1 && num_rows == static_cast<int64_t>(num_seqs) * max_query_len &&
+                   max_context_len == max_query_len;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     // persistent: one CTA per SM (or per item when there are fewer)
     const int grid = std::min(pp.items, sm);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return dtype == PKV_F16
-               ? launch_prefill<__half>(p, tq, tk, tv, block_size, grid, max_query_len, s)
-               : launch_prefill<__nv_bfloat16>(p, tq, tk, tv, block_size, grid, max_query_len, s);
+               ? launch_prefill<__half>(p, tq, tk, tv, to, block_size, grid, max_query_len, s)
+               : launch_prefill<__nv_bfloat16>(p, tq, tk, tv, to, block_size, grid, max_query_len, s);
 }
 
 }  // extern "C"

@@ -17,7 +17,7 @@
 // SMs idle).  The KV range ends at the causal limit of the tile's last row;
 // inside a tile a row's columns past its own position are masked.  Same
 // machinery as the shared-prefix tile kernel: tcgen05 MMAs with M = 128 rows,
-// N = 128 tokens, K = 128; S double-buffered in TMEM, O accumulated in TMEM; a
+// N = 128 tokens, K = 128; S triple-buffered in TMEM, O accumulated in TMEM; a
 // row's softmax is local to one thread pair (its scores are read from TMEM once
 // per tile); the row's reference maximum moves only when a tile exceeds it by
 // more than kRescaleLog2.  The row sum l adds the fp32 weights whose bf16/fp16
@@ -40,12 +40,14 @@
 // slots; warp 0 also loads each item's Q tile), 1 TMEM owner + QK^T issuer,
 // 11 PV issuer, 2-9 softmax in pairs: warps w and w + 4 share TMEM lane
 // quarter w & 3 (the same 32 query rows) and take tile columns 0-63 and
-// 64-127.  A pair exchanges its partial row maxima each tile through two spare
-// TMEM columns (an mbarrier with a bounded wait orders them), so both warps
-// hold the same reference maximum; each rescales, writes P for and outputs
-// its own half.  P goes back into TMEM over the scores it came from (16-bit
-// values packed two per column) and the PV MMA takes it from there, so P is
-// double-buffered with S and the softmax of tile j + 1 runs while PV(j) does.
+// 64-127.  A pair exchanges its partial row maxima each tile through two
+// columns of the tile's own S buffer whose scores are already read (an
+// mbarrier with a bounded wait orders them), so both warps hold the same
+// reference maximum; each rescales, writes P for and outputs its own half.
+// P goes back into TMEM over the scores it came from (16-bit values packed two
+// per column) and the PV MMA takes it from there, so P is triple-buffered with
+// S: QK^T(j + 3) waits only for PV(j), and the softmax of tile j + 1 runs
+// while PV(j) does.
 #pragma once
 
 #include "prefix_tc_kernel.cuh"
@@ -77,18 +79,43 @@ struct PrefillParams {
     int num_items;     // row_tiles * num_kv_heads * num_seqs * splits
     int splits;        // KV splits per row tile
     int split_tokens;  // tokens per split, a multiple of 128
+    int pair_order;    // 1: (sequence, KV head)-major order, heavy and light row tiles paired
     float scale_log2;
 };
 
-// Reads and checks one sequence's (chunk start, chunk length, context length);
-// false (and a raised flag) when they are out of contract.
-__device__ __forceinline__ bool prefill_seq(const PrefillParams &p, int seq, int &q0, int &chunk,
-                                            int &len) {
-    q0 = p.query_start[seq];
-    const int q1 = p.query_start[seq + 1];
-    chunk = q1 - q0;
-    len = p.context_lens[seq];
-    return q0 >= 0 && chunk >= 0 && q1 <= p.num_rows && chunk <= p.qlen_cap && len >= chunk &&
+// One sequence's chunk start, chunk end and context length, as read from the
+// device arrays.
+struct PrefillSeqVals {
+    int q0, q1, len;
+};
+
+// The sequence of item i (no memory access).
+__device__ __forceinline__ int prefill_item_seq(const PrefillParams &p, int i) {
+    if (p.pair_order) return i / p.row_tiles / p.num_kv_heads;
+    const int per_tile = p.num_kv_heads * p.num_seqs * p.splits;
+    return (i % per_tile) / p.num_kv_heads / p.splits;
+}
+
+// Loads item i's sequence values (zeros past the item count).
+__device__ __forceinline__ PrefillSeqVals prefill_seq_vals(const PrefillParams &p, int i) {
+    PrefillSeqVals v{0, 0, 0};
+    if (i < p.num_items) {
+        const int seq = prefill_item_seq(p, i);
+        v.q0 = p.query_start[seq];
+        v.q1 = p.query_start[seq + 1];
+        v.len = p.context_lens[seq];
+    }
+    return v;
+}
+
+// Checks one sequence's (chunk start, chunk length, context length); false when
+// they are out of contract.
+__device__ __forceinline__ bool prefill_seq(const PrefillParams &p, const PrefillSeqVals &v, int &q0,
+                                            int &chunk, int &len) {
+    q0 = v.q0;
+    chunk = v.q1 - v.q0;
+    len = v.len;
+    return q0 >= 0 && chunk >= 0 && v.q1 <= p.num_rows && chunk <= p.qlen_cap && len >= chunk &&
            len <= p.len_cap;
 }
 
@@ -103,21 +130,36 @@ struct PrefillItem {
     int seq;
 };
 
-// Item i of the static order: row tiles from the last (longest causal range)
-// down, then sequence and split, then KV head.  False when the item holds no
-// work: a row tile past the chunk, a split past the tile's causal limit, or a
-// sequence out of contract (flagged once when `flag`).
-__device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, bool flag,
-                                             PrefillItem &it) {
-    const int per_tile = p.num_kv_heads * p.num_seqs * p.splits;
-    const int rt_rev = i / per_tile;
-    const int rem = i - rt_rev * per_tile;
-    const int ss = rem / p.num_kv_heads;
-    it.kvh = rem - ss * p.num_kv_heads;
-    it.seq = ss / p.splits;
-    it.split = ss - it.seq * p.splits;
-    it.row_tile = p.row_tiles - 1 - rt_rev;
-    if (!prefill_seq(p, it.seq, it.q0, it.chunk, it.len)) {
+// Item i of the static order.  Default: row tiles from the last (longest causal
+// range) down, then sequence and split, then KV head, so that CTA c's items c,
+// c + grid, ... are heaviest first.  Pair order (whole prompts of one length, one
+// split): (sequence, KV head) major, and within it the row tiles as last, first,
+// second to last, second, ..., taken two at a time by a CTA (prefill_slot_item),
+// so that every CTA's pair of row tiles carries the same causal work and the
+// CTAs that run together share the K/V tiles of a few (sequence, KV head)
+// pairs in L2.  False when the item holds no work: a row tile past the chunk, a
+// split past the tile's causal limit, or a sequence out of contract (flagged
+// once when `flag`).
+__device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, const PrefillSeqVals &sv,
+                                             bool flag, PrefillItem &it) {
+    if (p.pair_order) {
+        const int g = i / p.row_tiles;
+        const int pos = i - g * p.row_tiles;
+        it.seq = g / p.num_kv_heads;
+        it.kvh = g - it.seq * p.num_kv_heads;
+        it.split = 0;
+        it.row_tile = (pos & 1) ? pos >> 1 : p.row_tiles - 1 - (pos >> 1);
+    } else {
+        const int per_tile = p.num_kv_heads * p.num_seqs * p.splits;
+        const int rt_rev = i / per_tile;
+        const int rem = i - rt_rev * per_tile;
+        const int ss = rem / p.num_kv_heads;
+        it.kvh = rem - ss * p.num_kv_heads;
+        it.seq = ss / p.splits;
+        it.split = ss - it.seq * p.splits;
+        it.row_tile = p.row_tiles - 1 - rt_rev;
+    }
+    if (!prefill_seq(p, sv, it.q0, it.chunk, it.len)) {
         if (flag && it.row_tile == 0 && it.kvh == 0 && it.split == 0)
             raise_flag(p.status, PKV_DEVERR_CONTEXT_LEN);
         return false;
@@ -134,6 +176,20 @@ __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, bool
     return it.tok_hi > it.tok_lo;
 }
 
+// The k-th item of this CTA: items blockIdx.x + k * grid in the default order,
+// the pairs (2 q, 2 q + 1) for q = blockIdx.x + (k / 2) * grid in pair order.
+__device__ __forceinline__ int prefill_slot_item(const PrefillParams &p, int k) {
+    if (p.pair_order) return 2 * (blockIdx.x + (k >> 1) * gridDim.x) + (k & 1);
+    return blockIdx.x + k * gridDim.x;
+}
+
+// Items whose O tile leaves through the output tensor map, staged in the item's
+// last V slot (one split, and every row of the row tile inside the chunk, so the
+// box holds no other sequence's rows); the others store row by row.
+__device__ __forceinline__ bool prefill_staged(const PrefillParams &p, const PrefillItem &it) {
+    return p.splits == 1 && it.row0 + p.tile_rows <= it.rows;
+}
+
 // Shared memory: the Q tile(s) of consecutive items, K and V rings of
 // 128-token tiles, and the barriers (rings, Q, S / O double buffers, the
 // softmax pairs).
@@ -148,12 +204,14 @@ struct PrefillLayout {
     static constexpr int kOffK = kOffQ + kQB * kPanel;
     static constexpr int kOffV = kOffK + kKS * kPanel;
     static constexpr int kOffBar = kOffV + kVS * kPanel;
-    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 2 * kQB + 8 + 2 + 8;
+    static constexpr int kSB = 3;                     // S buffers (P over S) in TMEM
+    static constexpr int kNumBars = 2 * kKS + 2 * kVS + 2 * kQB + 4 * kSB + 2 + 8 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kOffSum = kOffMisc + 16;     // row-sum exchange: [2 halves][128 rows] fp32
+    static constexpr int kBytes = kOffSum + 2 * 128 * 4;
     static constexpr int kSmemBytes = kBytes + 1024;  // + alignment slack
-    static constexpr uint32_t kTmemCols = 512;        // S[2] at 0 / 128 (P[b] over S[b]), O at 256, exchange 384
-    static constexpr uint32_t kXchgCol = 384;         // spare TMEM columns for the pairs
+    static constexpr uint32_t kTmemCols = 512;        // S[3] at 0 / 128 / 256 (P[b] over S[b]), O at 384
+    static constexpr uint32_t kOCol = 384;
     static constexpr float kRescaleLog2 = 8.f;
     static constexpr int kThreads = 384;
     static_assert(kSmemBytes <= 232448, "dynamic shared memory per block");
@@ -163,7 +221,8 @@ template <typename T, int BS>
 __global__ void __launch_bounds__(384, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                             const __grid_constant__ CUtensorMap tmap_k,
-                            const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p) {
+                            const __grid_constant__ CUtensorMap tmap_v,
+                            const __grid_constant__ CUtensorMap tmap_o, const PrefillParams p) {
     using L = PrefillLayout;
     constexpr int TILE = L::kTile, D = 128;
     constexpr bool kBF16 = !std::is_same<T, __half>::value;
@@ -179,10 +238,12 @@ __global__ void __launch_bounds__(384, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
     uint64_t *k_full = bars, *k_empty = k_full + KS, *v_full = k_empty + KS, *v_empty = v_full + VS;
     uint64_t *q_full = v_empty + VS, *q_empty = q_full + QB;
-    uint64_t *s_full = q_empty + QB, *s_empty = s_full + 2, *p_full = s_full + 4, *o_done = s_full + 6;
-    uint64_t *drain_bar = s_full + 8;      // QK^T issuer's drain on exit
-    uint64_t *drain_pv = s_full + 9;       // PV issuer's drain on exit
+    constexpr int SB = L::kSB;
+    uint64_t *s_full = q_empty + QB, *s_empty = s_full + SB, *p_full = s_full + 2 * SB, *o_done = s_full + 3 * SB;
+    uint64_t *drain_bar = s_full + 4 * SB;  // QK^T issuer's drain on exit
+    uint64_t *drain_pv = drain_bar + 1;     // PV issuer's drain on exit
     uint64_t *pair_bar = drain_pv + 1;     // [quarter][parity]
+    uint64_t *o_staged = pair_bar + 8;     // an item's O tile is in its last V slot
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
     const uint32_t smem_base = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
@@ -200,13 +261,14 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < SB; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_empty[i], 1);
             mbar_init(&p_full[i], 8);
             mbar_init(&o_done[i], 1);
         }
         for (int i = 0; i < 8; ++i) mbar_init(&pair_bar[i], 2);
+        mbar_init(o_staged, 8);
         mbar_init(drain_bar, 1);
         mbar_init(drain_pv, 1);
         *abort_flag = 0;
@@ -229,6 +291,7 @@ __global__ void __launch_bounds__(384, 1)
         tc::prefetch_tensormap(&tmap_q);
         tc::prefetch_tensormap(&tmap_k);
         tc::prefetch_tensormap(&tmap_v);
+        tc::prefetch_tensormap(&tmap_o);
     }
     fence_proxy_async_smem();
     tc::fence_before_sync();
@@ -241,7 +304,7 @@ __global__ void __launch_bounds__(384, 1)
         // Separate producers so a K tile never waits behind a V slot that its PV still
         // holds; each reads the next tile's table entries while it waits for a slot.
         // The K producer also loads each item's Q tile into Q buffer n % kQB once
-        // the QK^T of item n - kQB is done.
+        // the QK^T of item n - kQB is done, without holding back the item's K tiles.
         const int kv = warp == 10;
         const int nst = kv ? VS : KS;
         uint64_t *full = kv ? v_full : k_full;
@@ -255,9 +318,9 @@ __global__ void __launch_bounds__(384, 1)
         int q_issue[2] = {-1, -1};
         bool ok = true;
         int jt = 0, n = 0;  // tiles and items so far
-        for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+        for (int ki = 0, item = prefill_slot_item(p, 0); item < p.num_items && ok; item = prefill_slot_item(p, ++ki)) {
             PrefillItem it;
-            if (!prefill_item(p, item, kv == 0, it)) continue;
+            if (!prefill_item(p, item, prefill_seq_vals(p, item), kv == 0, it)) continue;
             const int32_t *trow = p.block_tables + static_cast<int64_t>(it.seq) * p.max_blocks_per_seq;
             auto entry = [&](int j) -> int {  // this lane's block of tile j (-1: none or bad)
                 const int t0 = it.tok_lo + j * TILE;
@@ -273,28 +336,50 @@ __global__ void __launch_bounds__(384, 1)
                 return e;
             };
             int e_next = entry(0);
-            if (kv == 0) {
-                const int qb = n % QB;
-                int go = 1;
-                if (lane == 0) {
-                    go = tc_wait(&q_empty[qb], ((n / QB) & 1) ^ 1, abort_flag, p.status);
-                    if (go) {
-                        // boxes of tile_tokens tokens x group heads x 64 columns; rows of
-                        // tokens past the query array arrive as zeros and count as bytes
-                        mbar_arrive_expect_tx(&q_full[qb], 256u * R);
+            // The K producer loads the item's Q tile as soon as Q buffer n % kQB is free
+            // (the QK^T of item n - kQB done), while it already streams the item's K
+            // tiles: lane 0 polls that buffer whenever it waits for a K slot, and waits
+            // for it at the latest after the item's last K tile.
+            const int qb = n % QB;
+            const uint32_t q_par = ((n / QB) & 1) ^ 1;
+            bool q_pending = kv == 0;  // lane 0's state
+            auto issue_q = [&]() {
+                // boxes of tile_tokens tokens x group heads x 64 columns; rows of tokens
+                // past the query array arrive as zeros and count as bytes
+                mbar_arrive_expect_tx(&q_full[qb], 256u * R);
 #pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            tc::tma_load_3d(sm + L::kOffQ + qb * L::kPanel + c * L::kHalf, &tmap_q, c * 64,
-                                            it.kvh * p.group, it.q0 + it.row_tile * p.tile_tokens,
-                                            &q_full[qb], q_policy);
-                        q_issue[qb] = n;
-                    }
-                }
-                if (!__shfl_sync(0xffffffffu, go, 0)) {
-                    ok = false;
+                for (int c = 0; c < 2; ++c)
+                    tc::tma_load_3d(sm + L::kOffQ + qb * L::kPanel + c * L::kHalf, &tmap_q, c * 64,
+                                    it.kvh * p.group, it.q0 + it.row_tile * p.tile_tokens, &q_full[qb], q_policy);
+                q_issue[qb] = n;
+                q_pending = false;
+                // the next item's Q box into L2 now, so its load does not wait for HBM
+                PrefillItem nx;
+                for (int k2 = ki + 1, i2 = prefill_slot_item(p, k2); i2 < p.num_items; i2 = prefill_slot_item(p, ++k2)) {
+                    if (!prefill_item(p, i2, prefill_seq_vals(p, i2), false, nx)) continue;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        tc::tma_prefetch_3d(&tmap_q, c * 64, nx.kvh * p.group, nx.q0 + nx.row_tile * p.tile_tokens);
                     break;
                 }
-            }
+            };
+            // lane 0: bounded wait for `bar`, issuing the pending Q load when its buffer
+            // frees up meanwhile
+            auto wait_slot = [&](uint64_t *bar, uint32_t par) -> bool {
+                if (!q_pending) return tc_wait(bar, par, abort_flag, p.status);
+                const uint64_t t0 = global_timer_ns();
+                while (true) {
+                    if (q_pending && mbar_test_wait(&q_empty[qb], q_par)) issue_q();
+                    if (mbar_test_wait(bar, par)) return true;
+                    if (!q_pending) return tc_wait(bar, par, abort_flag, p.status);
+                    if (*abort_flag) return false;
+                    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+                        raise_flag(p.status, PKV_DEVERR_TIMEOUT);
+                        *abort_flag = 1;
+                        return false;
+                    }
+                }
+            };
             for (int j = 0; j < it.ntiles; ++j, ++jt) {
                 const int e = e_next;
                 if (j + 1 < it.ntiles) e_next = entry(j + 1);  // in flight while this tile waits
@@ -302,7 +387,7 @@ __global__ void __launch_bounds__(384, 1)
                 const int s = jt % nst;
                 int go = 1;
                 if (lane == 0) {
-                    go = tc_wait(&empty[s], ((jt / nst) & 1) ^ 1, abort_flag, p.status);
+                    go = wait_slot(&empty[s], ((jt / nst) & 1) ^ 1);
                     if (go) {
                         if (bytes) mbar_arrive_expect_tx(&full[s], bytes);
                         else mbar_arrive(&full[s]);
@@ -322,6 +407,14 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 __syncwarp();
             }
+            if (ok && kv == 0) {
+                int go = 1;
+                if (lane == 0 && q_pending) {
+                    go = tc_wait(&q_empty[qb], q_par, abort_flag, p.status);
+                    if (go) issue_q();
+                }
+                if (!__shfl_sync(0xffffffffu, go, 0)) ok = false;
+            }
             ++n;
         }
         if (!ok && lane == 0) {
@@ -340,9 +433,9 @@ __global__ void __launch_bounds__(384, 1)
         constexpr uint32_t idesc_qk = tc::idesc_f16_f32acc(kBF16, 128, 128, false, false);
         bool ok = true;
         int jt = 0, n = 0;
-        for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+        for (int ki = 0, item = prefill_slot_item(p, 0); item < p.num_items && ok; item = prefill_slot_item(p, ++ki)) {
             PrefillItem it;
-            if (!prefill_item(p, item, false, it)) continue;
+            if (!prefill_item(p, item, prefill_seq_vals(p, item), false, it)) continue;
             const int qb = n % QB;
             int go = 1;
             if (lane == 0) go = tc_wait(&q_full[qb], (n / QB) & 1, abort_flag, p.status);
@@ -350,13 +443,13 @@ __global__ void __launch_bounds__(384, 1)
             for (int j = 0; j < it.ntiles; ++j, ++jt) {
                 if (lane == 0)
                     go = tc_wait(&k_full[jt % KS], (jt / KS) & 1, abort_flag, p.status) &&
-                         tc_wait(&s_empty[jt & 1], ((jt >> 1) & 1) ^ 1, abort_flag, p.status);
+                         tc_wait(&s_empty[jt % SB], ((jt / SB) & 1) ^ 1, abort_flag, p.status);
                 if (!__shfl_sync(0xffffffffu, go, 0)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
-                    const int b = jt & 1;
+                    const int b = jt % SB;
                     tc::fence_after_sync();
                     const uint32_t qa = smem_base + L::kOffQ + qb * L::kPanel;
                     const uint32_t ka = smem_base + L::kOffK + (jt % KS) * L::kPanel;
@@ -384,21 +477,22 @@ __global__ void __launch_bounds__(384, 1)
         // ===================== PV issuer =====================
         constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, 128, false, true);
         bool ok = true;
-        int jt = 0;
-        for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+        int jt = 0, n_staged = 0;
+        for (int ki = 0, item = prefill_slot_item(p, 0); item < p.num_items && ok; item = prefill_slot_item(p, ++ki)) {
             PrefillItem it;
-            if (!prefill_item(p, item, false, it)) continue;
+            if (!prefill_item(p, item, prefill_seq_vals(p, item), false, it)) continue;
+            const bool staged = prefill_staged(p, it);
             for (int j = 0; j < it.ntiles; ++j, ++jt) {
                 int go = 1;
                 if (lane == 0)
-                    go = tc_wait(&p_full[jt & 1], (jt >> 1) & 1, abort_flag, p.status) &&
+                    go = tc_wait(&p_full[jt % SB], (jt / SB) & 1, abort_flag, p.status) &&
                          tc_wait(&v_full[jt % VS], (jt / VS) & 1, abort_flag, p.status);
                 if (!__shfl_sync(0xffffffffu, go, 0)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
-                    const int b = jt & 1;
+                    const int b = jt % SB;
                     tc::fence_after_sync();
                     const uint32_t va = smem_base + L::kOffV + (jt % VS) * L::kPanel;
 #pragma unroll
@@ -406,16 +500,41 @@ __global__ void __launch_bounds__(384, 1)
                         const uint64_t bd = tc::smem_desc_sw128(va + k * 2048, L::kHalf, 1024);
                         // P from TMEM (16 tokens = 8 columns per step); the item's first
                         // tile starts O afresh
-                        tc::mma_f16_ts(tmem + 256, tmem + 128 * b + 8 * k, bd, idesc_pv, j > 0 || k > 0);
+                        tc::mma_f16_ts(tmem + L::kOCol, tmem + 128 * b + 8 * k, bd, idesc_pv, j > 0 || k > 0);
                     }
                     tc::mma_commit(&o_done[b]);
-                    tc::mma_commit(&s_empty[b]);  // S[b] / P[b] free for QK^T(jt + 2)
-                    tc::mma_commit(&v_empty[jt % VS]);
+                    tc::mma_commit(&s_empty[b]);  // S[b] / P[b] free for QK^T(jt + SB)
+                    // a staged item's last V slot receives its O tile: freed below
+                    if (!(staged && j + 1 == it.ntiles)) tc::mma_commit(&v_empty[jt % VS]);
                 }
                 __syncwarp();
+                if (staged && j + 1 == it.ntiles) {
+                    // the softmax warps have written the normalised O tile into this V
+                    // slot (after PV(jt) completed): store it with the queries' boxes,
+                    // then free the slot once the copies have read it
+                    if (lane == 0) {
+                        go = tc_wait(o_staged, n_staged & 1, abort_flag, p.status);
+                        if (go) {
+                            unsigned char *slot = sm + L::kOffV + (jt % VS) * L::kPanel;
+#pragma unroll
+                            for (int c = 0; c < 2; ++c)
+                                tc::tma_store_3d(&tmap_o, c * 64, it.kvh * p.group,
+                                                 it.q0 + it.row_tile * p.tile_tokens, slot + c * L::kHalf);
+                            tc::bulk_commit_group();
+                            tc::bulk_wait_read_all();
+                            mbar_arrive(&v_empty[jt % VS]);
+                        }
+                    }
+                    ++n_staged;
+                    if (!__shfl_sync(0xffffffffu, go, 0)) {
+                        ok = false;
+                        break;
+                    }
+                }
             }
         }
         if (lane == 0) {
+            tc::bulk_wait_all();  // output tiles written before the CTA exits
             tc::mma_commit(drain_pv);
             mbar_wait_bounded(drain_pv, 0, kDrainTimeoutNs);
         }
@@ -427,41 +546,56 @@ __global__ void __launch_bounds__(384, 1)
         const int c0 = half * 64;
         const int r = quarter * 32 + lane;   // row within the tile = TMEM lane
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const uint32_t xchg = lane_base + L::kXchgCol;
+        float *sum_x = reinterpret_cast<float *>(sm + L::kOffSum);  // [half][row]
         bool ok = true;
         int jt = 0, xs = 0;  // tiles and pair exchanges so far
-        // One value per row between the two warps of the pair: step s writes column
-        // 2 (s & 1) + half and reads the partner's; a warp reuses a column two steps
-        // later, after the partner has passed the step in between.
-        auto exchange = [&](int step, float mine, float &other) -> bool {
-            const int par = step & 1;
-            tc::tmem_st_x1(xchg + 2 * par + half, mine);
+        // One value per row between the two warps of the pair, ordered by the pair's
+        // mbarrier (phase s & 1 of barrier [quarter][s & 1] for exchange step s).
+        // A tile's partial maxima travel in S[b] itself, in columns whose scores their
+        // writer has already read and that nothing overwrites before the partner has
+        // read them: half 0 writes column 32 (half 1's P lands there only after half 1
+        // has read it), half 1 column 64 (no P store reaches it; QK^T(jt + SB) rewrites
+        // S[b] only after PV(jt), which waits for both warps).  An item's row sums go
+        // through shared memory; a slot is rewritten only after the next tile's
+        // exchange, which the partner reaches after reading it.
+        auto pair_sync = [&](int step) -> bool {
+            __syncwarp();
+            uint64_t *pb = &pair_bar[quarter * 2 + (step & 1)];
+            if (lane == 0) mbar_arrive(pb);
+            return tc_wait_warp(pb, (step >> 1) & 1, abort_flag, p.status);
+        };
+        auto exchange_max = [&](int step, int b, float mine, float &other) -> bool {
+            const uint32_t sb = lane_base + 128 * b;
+            tc::tmem_st_x1(sb + (half ? 64 : 32), mine);
             tc::tmem_st_wait();
             tc::fence_before_sync();
-            __syncwarp();
-            uint64_t *pb = &pair_bar[quarter * 2 + par];
-            if (lane == 0) mbar_arrive(pb);
-            if (!tc_wait_warp(pb, (step >> 1) & 1, abort_flag, p.status)) return false;
+            if (!pair_sync(step)) return false;
             tc::fence_after_sync();
-            other = tc::tmem_ld_x1(xchg + 2 * par + (1 - half));
+            other = tc::tmem_ld_x1(sb + (half ? 32 : 64));
             tc::tmem_ld_wait();
             return true;
         };
-        for (int item = blockIdx.x; item < p.num_items && ok; item += gridDim.x) {
+        auto exchange_sum = [&](int step, float mine, float &other) -> bool {
+            sum_x[half * 128 + r] = mine;
+            if (!pair_sync(step)) return false;
+            other = sum_x[(1 - half) * 128 + r];
+            return true;
+        };
+        for (int ki = 0, item = prefill_slot_item(p, 0); item < p.num_items && ok; item = prefill_slot_item(p, ++ki)) {
             PrefillItem it;
-            if (!prefill_item(p, item, false, it)) continue;
+            if (!prefill_item(p, item, prefill_seq_vals(p, item), false, it)) continue;
             const int row = it.row0 + r;
             const bool live = r < R && row < it.rows;
             const int jtok = live ? row / p.group : 0;
             const int pos = it.base_pos + jtok;  // this row sees tokens 0 .. pos
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < it.ntiles && ok; ++j, ++jt) {
-                const int b = jt & 1;
+                const int b = jt % SB;
                 const int t0 = it.tok_lo + j * TILE;
                 const int valid = min(TILE, it.tok_hi - t0);                    // columns loaded
                 const int vr = live ? max(0, min(valid, pos + 1 - t0)) : 0;  // columns this row sees
                 const int vh = max(0, min(64, vr - c0));                     // ... in this half
-                if (!tc_wait_warp(&s_full[b], (jt >> 1) & 1, abort_flag, p.status)) {
+                if (!tc_wait_warp(&s_full[b], (jt / SB) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
@@ -492,7 +626,7 @@ __global__ void __launch_bounds__(384, 1)
                     pmax = ext * p.scale_log2;
                 }
                 float pmax_other;
-                if (!exchange(xs++, pmax, pmax_other)) {
+                if (!exchange_max(xs++, b, pmax, pmax_other)) {
                     ok = false;
                     break;
                 }
@@ -506,7 +640,7 @@ __global__ void __launch_bounds__(384, 1)
                 if (__any_sync(0xffffffffu, new_ref != m_ref)) {
                     if (j > 0) {
                         // O holds tiles < j: wait for PV(j-1), rescale this half of O in TMEM
-                        if (!tc_wait_warp(&o_done[(jt - 1) & 1], ((jt - 1) >> 1) & 1, abort_flag, p.status)) {
+                        if (!tc_wait_warp(&o_done[(jt - 1) % SB], ((jt - 1) / SB) & 1, abort_flag, p.status)) {
                             ok = false;
                             break;
                         }
@@ -514,14 +648,14 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                         for (int c = 0; c < 64; c += 16) {
                             float o[16];
-                            tc::tmem_ld_x16(lane_base + 256 + c0 + c, o);
+                            tc::tmem_ld_x16(lane_base + L::kOCol + c0 + c, o);
                             tc::tmem_ld_wait();
                             uint32_t w[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(o[i] * alpha);
                             asm volatile(
                                 "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, "
-                                "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(lane_base + 256 + c0 + c),
+                                "%8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(lane_base + L::kOCol + c0 + c),
                                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
                                 "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]),
                                 "r"(w[13]), "r"(w[14]), "r"(w[15])
@@ -568,11 +702,11 @@ __global__ void __launch_bounds__(384, 1)
                 if (valid < TILE) {
                     // V rows past the loaded range: zero this half so 0 * stale never reaches
                     // the MMA.  The parity wait cannot alias an older phase of the slot: S(jt)
-                    // exists only once PV(jt - 2) has completed (two S buffers), so V(jt - 2),
-                    // the slot's previous tile when kVS == 2, has landed.  With more S buffers
-                    // than V slots the wait could pass on V(jt - kVS)'s phase and zero rows
-                    // that a pending PV still reads.
-                    static_assert(L::kVS >= 2, "V slots >= S buffers (2)");
+                    // exists only once PV(jt - kSB) has completed, so V(jt - kVS), the slot's
+                    // previous tile, has landed when kVS >= kSB.  With more S buffers than V
+                    // slots the wait could pass on V(jt - kVS)'s phase and zero rows that a
+                    // pending PV still reads.
+                    static_assert(L::kVS >= L::kSB, "V slots >= S buffers");
                     if (!tc_wait_warp(&v_full[jt % VS], (jt / VS) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
@@ -593,10 +727,34 @@ __global__ void __launch_bounds__(384, 1)
             // the pair's row sum, then this half of the O row -> out (one split) or its
             // partial slot.  TMEM loads are warp-wide: every lane loads, only live rows store.
             float l_other = 0.f;
-            if (ok) ok = exchange(xs++, l, l_other);
+            if (ok) ok = exchange_sum(xs++, l, l_other);
             const float lt = l + l_other;
-            if (ok) ok = tc_wait_warp(&o_done[(jt - 1) & 1], ((jt - 1) >> 1) & 1, abort_flag, p.status);
-            if (ok) {
+            if (ok) ok = tc_wait_warp(&o_done[(jt - 1) % SB], ((jt - 1) / SB) & 1, abort_flag, p.status);
+            if (ok && prefill_staged(p, it)) {
+                // normalised O rows into the item's last V slot (free since PV(jt - 1)
+                // completed), laid out as the queries' boxes land: two half panels of
+                // 128-byte rows, 16-byte chunk c of row r at chunk c ^ (r & 7); the PV
+                // issuer stores them with the output tensor map
+                tc::fence_after_sync();
+                unsigned char *orow_s = sm + L::kOffV + ((jt - 1) % VS) * L::kPanel + half * L::kHalf + r * 128;
+                const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; c += 16) {
+                    float o[16];
+                    tc::tmem_ld_x16(lane_base + L::kOCol + c0 + c, o);
+                    tc::tmem_ld_wait();
+                    if (!live) continue;
+                    uint32_t w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) w[i] = Elem<T>::pack2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+                    const int k0 = c / 8;  // chunks k0, k0 + 1 of the row
+                    *reinterpret_cast<uint4 *>(orow_s + (((k0) ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(orow_s + (((k0 + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+                fence_proxy_async_smem();  // visible to the tensor store
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_staged);
+            } else if (ok) {
                 tc::fence_after_sync();
                 const int g = live ? row - jtok * p.group : 0;
                 const int64_t orow = (static_cast<int64_t>(it.q0) + jtok) * p.num_q_heads + it.kvh * p.group + g;
@@ -605,7 +763,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int c = 0; c < 64; c += 16) {
                     float o[16];
-                    tc::tmem_ld_x16(lane_base + 256 + c0 + c, o);
+                    tc::tmem_ld_x16(lane_base + L::kOCol + c0 + c, o);
                     tc::tmem_ld_wait();
                     if (!live) continue;
                     if (direct) {
@@ -648,7 +806,8 @@ __global__ void __launch_bounds__(128) paged_prefill_merge_kernel(const PrefillP
     const int lane = threadIdx.x & 31;
     const int idx = blockIdx.x * 4 + (threadIdx.x >> 5);  // (chunk token, query head)
     int q0, chunk, len;
-    if (!prefill_seq(p, seq, q0, chunk, len)) return;    // flagged by the main kernel
+    const PrefillSeqVals sv{p.query_start[seq], p.query_start[seq + 1], p.context_lens[seq]};
+    if (!prefill_seq(p, sv, q0, chunk, len)) return;     // flagged by the main kernel
     const int jtok = idx / p.num_q_heads, hq = idx - jtok * p.num_q_heads;
     if (jtok >= chunk) return;
     const int pos = len - chunk + jtok;
