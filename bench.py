@@ -629,7 +629,7 @@ def run_ours(args):
     part = args.partition
     sm = torch.cuda.get_device_properties(dev).multi_processor_count
     plan = pkv.decode_plan(wl.num_seqs, wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
-                           wl.block_size, maxl, part, sm)
+                           wl.block_size, maxl, part, sm, int8=wl.kv.dtype == torch.int8)
     slots = pkv.slot_mapping(wl.block_tables, wl.new_positions, wl.block_size,
                              num_blocks=wl.num_blocks)
     out = torch.empty_like(wl.q)

@@ -243,8 +243,8 @@ PKV_API size_t pkv_decode_int8_workspace_bytes(int num_seqs, int num_q_heads, in
  * V_i[t][c] = code * v_scale[h][c].  q and out are `dtype` (fp16 or bf16);
  * accumulation is fp32.  The K scales are folded into the query and the V
  * scales applied once per output channel, so the kernel reads only the codes.
- * Every other argument, the partitioning and the errors are those of
- * pkv_paged_attention_decode (runs on the CUDA cores for every shape).
+ * Every other argument and the errors are those of pkv_paged_attention_decode;
+ * the automatic split is pkv_decode_int8_plan's.
  */
 PKV_API pkv_status pkv_paged_attention_decode_int8(
     const void *q, const int8_t *k_cache, const int8_t *v_cache, const float *k_scale,
@@ -395,13 +395,28 @@ PKV_API uint64_t pkv_launch_count(void);
  * as a pure host function (no CUDA call): given the shape and the SM count it
  * writes the partition size, partitions per sequence, query heads handled per
  * block and whether the merge kernel runs.  Returns PKV_OK or the status the
- * decode call would return for these arguments.
+ * decode call would return for these arguments.  With partition_size 0 the
+ * split aims at eight waves of the kernel form's resident blocks per SM (two
+ * for the per-lane form, three for the warp-MMA form of 4 or 8 heads per
+ * block), with partitions of at least 256 tokens whose K/V bytes are at least
+ * 32 times their partial outputs.
  */
 PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads,
                                    int head_dim, int block_size, int max_context_len,
                                    int partition_size, int sm_count, int *out_partition_size,
                                    int *out_num_partitions, int *out_heads_per_block,
                                    int *out_needs_merge);
+
+/*
+ * pkv_decode_int8_plan -- pkv_decode_plan for pkv_paged_attention_decode_int8
+ * (the same rules; the INT8 forms keep six (per-lane) or four (warp MMAs)
+ * blocks resident per SM, and a token's K/V is half the bytes).
+ */
+PKV_API pkv_status pkv_decode_int8_plan(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int max_context_len,
+                                        int partition_size, int sm_count, int *out_partition_size,
+                                        int *out_num_partitions, int *out_heads_per_block,
+                                        int *out_needs_merge);
 
 /*
  * pkv_debug_wait_timeout -- failure-detection self test.  Launches one block

@@ -35,6 +35,9 @@ SIGNATURES = {
     "pkv_decode_plan": (I32, [I32, I32, I32, I32, I32, I32, I32, I32,
                               ctypes.POINTER(I32), ctypes.POINTER(I32), ctypes.POINTER(I32),
                               ctypes.POINTER(I32)]),
+    "pkv_decode_int8_plan": (I32, [I32, I32, I32, I32, I32, I32, I32, I32,
+                                   ctypes.POINTER(I32), ctypes.POINTER(I32), ctypes.POINTER(I32),
+                                   ctypes.POINTER(I32)]),
     "pkv_debug_wait_timeout": (I32, [U64, P]),
     "pkv_paged_attention_decode_static_scratch": (I32, [P, P, P, I64, I64, P, I32, P, I32, I32,
                                                         I32, I32, I32, I32, ctypes.c_float, P,

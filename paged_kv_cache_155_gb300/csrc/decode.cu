@@ -83,9 +83,17 @@ bool encode_query_map(CUtensorMap *map, const void *q, int num_rows, int num_q_h
 
 namespace {
 
-constexpr int kResidentCtasPerSm = 2;  // decode CTAs resident per SM (shared-memory bound)
 constexpr int kTargetWaves = 8;        // CTA waves the automatic split aims for
 constexpr int kMinAutoPartition = 256; // tokens: below this the per-CTA set-up dominates
+constexpr int kMergeShare = 32;        // a partition's K/V bytes >= this x its partial bytes
+
+// Decode CTAs resident per SM for each kernel form (their stage budgets and
+// register counts): 16-bit per-lane loops two, 16-bit warp MMAs three, INT8
+// per-lane loops six, INT8 warp MMAs four.
+int resident_ctas_per_sm(bool int8_kv, int heads_per_block) {
+    if (int8_kv) return heads_per_block >= 4 ? 4 : 6;
+    return heads_per_block >= 4 ? 3 : 2;
+}
 // Query heads per CTA: the largest of 8, 4, 2, 1 dividing the group (4 or 8
 // run the products as warp-level MMAs, 1 or 2 as per-lane loops).
 int heads_per_block_for(int group) {
@@ -101,11 +109,13 @@ size_t workspace_for(int num_seqs, int num_q_heads, int head_dim, int num_partit
     return rows * (static_cast<size_t>(head_dim) + 2) * sizeof(float);
 }
 
-// The launch plan of a decode call (16-bit and INT8 caches alike).
+// The launch plan of a decode call over a 16-bit or an INT8 cache.
+// `resident` overrides the form's resident CTAs per SM in the automatic split
+// (0: the form's own count).
 pkv_status plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                        int block_size, int max_context_len, int partition_size, int sm_count,
-                       int *out_partition_size, int *out_num_partitions,
-                       int *out_heads_per_block, int *out_needs_merge) {
+                       bool int8_kv, int *out_partition_size, int *out_num_partitions,
+                       int *out_heads_per_block, int *out_needs_merge, int resident = 0) {
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (block_size != 8 && block_size != 16 && block_size != 32) return PKV_ERR_UNSUPPORTED;
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len < 0 ||
@@ -122,13 +132,19 @@ pkv_status plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
 
     int part = partition_size;
     if (part == 0) {
-        // Enough CTAs for several waves over every SM, but partitions no
-        // shorter than kMinAutoPartition tokens.
+        // Enough CTAs for kTargetWaves waves of the form's resident CTAs over every
+        // SM, but partitions no shorter than kMinAutoPartition tokens, nor so short
+        // that the partial outputs (GH rows of head_dim + 2 floats, written and read
+        // back by the merge) pass 1 / kMergeShare of the partition's K/V bytes.
         const int64_t units = std::max<int64_t>(1, static_cast<int64_t>(num_seqs) * grid_y);
-        const int64_t target = static_cast<int64_t>(sm_count) * kResidentCtasPerSm * kTargetWaves;
+        const int64_t target = static_cast<int64_t>(sm_count) *
+                               (resident > 0 ? resident : resident_ctas_per_sm(int8_kv, gh)) * kTargetWaves;
         const int64_t want = std::max<int64_t>(1, (target + units - 1) / units);
         int64_t p = (static_cast<int64_t>(max_context_len) + want - 1) / want;
+        const int64_t kv_per_token = 2LL * head_dim * (int8_kv ? 1 : 2);
+        const int64_t partial = 2LL * gh * (head_dim + 2) * 4;
         p = std::max<int64_t>(p, kMinAutoPartition);
+        p = std::max<int64_t>(p, (kMergeShare * partial + kv_per_token - 1) / kv_per_token);
         p = (p + block_size - 1) / block_size * block_size;
         part = static_cast<int>(std::min<int64_t>(p, max_partition));
     }
@@ -141,12 +157,12 @@ pkv_status plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
 }
 
 size_t decode_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                              int block_size, int max_context_len, int partition_size) {
+                              int block_size, int max_context_len, int partition_size, bool int8_kv) {
     const int sm = partition_size > 0 ? 1 : pkv::current_sm_count();
     if (sm <= 0) return static_cast<size_t>(-1);
     int part = 0, nparts = 0, gh = 0, merge = 0;
     if (plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
-                    partition_size, sm, &part, &nparts, &gh, &merge) != PKV_OK)
+                    partition_size, sm, int8_kv, &part, &nparts, &gh, &merge) != PKV_OK)
         return static_cast<size_t>(-1);
     return workspace_for(num_seqs, num_q_heads, head_dim, nparts);
 }
@@ -202,14 +218,14 @@ pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
     int part = 0, nparts = 0, gh = 0, merge = 0;
     // Validate the shape first (no CUDA call), then plan for the real SM count.
     pkv_status plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                  max_context_len, partition_size, 1, &part, &nparts, &gh,
+                                  max_context_len, partition_size, 1, int8_kv, &part, &nparts, &gh,
                                   &merge);
     if (plan != PKV_OK) return plan;
     if (partition_size == 0) {
         const int sm = pkv::current_sm_count();
         if (sm <= 0) return PKV_ERR_CUDA;
         plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                           max_context_len, 0, sm, &part, &nparts, &gh, &merge);
+                           max_context_len, 0, sm, int8_kv, &part, &nparts, &gh, &merge);
         if (plan != PKV_OK) return plan;
     }
     const size_t need = workspace_for(num_seqs, num_q_heads, head_dim, nparts);
@@ -277,7 +293,17 @@ PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_hea
                                    int *out_num_partitions, int *out_heads_per_block,
                                    int *out_needs_merge) {
     return plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       max_context_len, partition_size, sm_count, out_partition_size,
+                       max_context_len, partition_size, sm_count, false, out_partition_size,
+                       out_num_partitions, out_heads_per_block, out_needs_merge);
+}
+
+PKV_API pkv_status pkv_decode_int8_plan(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int max_context_len,
+                                        int partition_size, int sm_count, int *out_partition_size,
+                                        int *out_num_partitions, int *out_heads_per_block,
+                                        int *out_needs_merge) {
+    return plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       max_context_len, partition_size, sm_count, true, out_partition_size,
                        out_num_partitions, out_heads_per_block, out_needs_merge);
 }
 
@@ -285,7 +311,7 @@ PKV_API size_t pkv_decode_workspace_bytes(int num_seqs, int num_q_heads, int num
                                           int head_dim, int block_size, int max_context_len,
                                           int partition_size) {
     return decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                  max_context_len, partition_size);
+                                  max_context_len, partition_size, false);
 }
 
 PKV_API pkv_status pkv_paged_attention_decode(
@@ -304,7 +330,7 @@ PKV_API size_t pkv_decode_int8_workspace_bytes(int num_seqs, int num_q_heads, in
                                                int head_dim, int block_size, int max_context_len,
                                                int partition_size) {
     return decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                  max_context_len, partition_size);
+                                  max_context_len, partition_size, true);
 }
 
 PKV_API pkv_status pkv_paged_attention_decode_int8(
@@ -331,6 +357,7 @@ namespace {
 #define PKV_PREFIX_SM_SHARE 5
 #endif
 constexpr int kPrefixSmShare = PKV_PREFIX_SM_SHARE;  // prefix CTAs ~ SMs / this
+constexpr int kCascadeSuffixResident = 2;            // suffix split: see plan_cascade
 
 struct CascadePlan {
     int rows = 0;          // num_seqs * group
@@ -367,12 +394,14 @@ pkv_status plan_cascade(int num_seqs, int num_q_heads, int num_kv_heads, int hea
     cp->split_tokens = tiles_per_split * 128;
     cp->splits = (prefix_len + cp->split_tokens - 1) / cp->split_tokens;
     if (cp->splits > 65535) return PKV_ERR_INVALID_ARG;
-    // the suffix: the decode plan over the longest suffix
+    // the suffix: the decode plan over the longest suffix, its split sized as for
+    // two resident CTAs per SM (the prefix tiles hold some SMs meanwhile; measured
+    // faster than the form's own three)
     const int span = max_context_len - prefix_len;
     int part = 0, nparts = 0, gh = 0, merge = 0;
-    const pkv_status st = pkv_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                          std::max(span, 1), partition_size, sm_count, &part,
-                                          &nparts, &gh, &merge);
+    const pkv_status st = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                      std::max(span, 1), partition_size, sm_count, false, &part,
+                                      &nparts, &gh, &merge, kCascadeSuffixResident);
     if (st != PKV_OK) return st;
     cp->suffix_part = part;
     cp->suffix_parts = nparts;

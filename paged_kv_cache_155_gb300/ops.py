@@ -457,13 +457,15 @@ def launch_count() -> int:
 
 
 def decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
-                partition_size, sm_count) -> dict:
-    """The library's launch decision for these arguments (pure host function)."""
+                partition_size, sm_count, int8=False) -> dict:
+    """The library's launch decision for these arguments (pure host function): that of
+    pkv_paged_attention_decode, or of the INT8-cache decode when ``int8``."""
     outs = [ctypes.c_int(0) for _ in range(4)]
-    st = lib().pkv_decode_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                               max_context_len, partition_size, sm_count,
-                               *[ctypes.byref(o) for o in outs])
-    _check(st, "pkv_decode_plan")
+    name = "pkv_decode_int8_plan" if int8 else "pkv_decode_plan"
+    st = getattr(lib(), name)(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                              max_context_len, partition_size, sm_count,
+                              *[ctypes.byref(o) for o in outs])
+    _check(st, name)
     return {"partition_size": outs[0].value, "num_partitions": outs[1].value,
             "heads_per_block": outs[2].value, "needs_merge": bool(outs[3].value)}
 

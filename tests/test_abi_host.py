@@ -223,9 +223,47 @@ def test_plan_auto_split_fills_the_gpu_and_respects_limits(lib):
     assert st == INVALID
 
 
-def test_int8_and_16bit_decode_share_one_plan(lib):
-    # the INT8 cache runs the same kernel template and plan as the 16-bit caches, so the
-    # two workspace queries agree for every shape (explicit partitions: no device query)
+def plan_int8(lib, b, hq, hkv, d, bs, maxl, part, sm=152):
+    outs = [ctypes.c_int() for _ in range(4)]
+    st = lib.pkv_decode_int8_plan(b, hq, hkv, d, bs, maxl, part, sm, *[ctypes.byref(o) for o in outs])
+    return st, [o.value for o in outs]
+
+
+def test_plan_auto_split_per_kernel_form(lib):
+    # partition_size 0: eight waves of the form's resident blocks per SM (16-bit per-lane
+    # 2, 16-bit warp MMAs 3, INT8 per-lane 6, INT8 warp MMAs 4), partitions of at least
+    # 256 tokens, a multiple of the block size, whose K/V bytes are at least 32x their
+    # partial outputs (GH rows of head_dim + 2 floats, written and read back)
+    def expect(b, hq, hkv, d, bs, maxl, resident, kv_bytes, sm=152):
+        gh = next(x for x in (8, 4, 2, 1) if (hq // hkv) % x == 0)
+        units = b * hkv * (hq // hkv // gh)
+        want = max(1, -(-(sm * resident * 8) // units))
+        p = max(-(-maxl // want), 256, -(-(32 * 2 * gh * (d + 2) * 4) // (2 * d * kv_bytes)))
+        return -(-p // bs) * bs
+    cases = [  # (plan, b, hq, hkv, d, bs, maxl, resident, kv bytes per value)
+        (plan, 32, 32, 32, 128, 16, 4096, 2, 2),        # MHA 7B: 1376-token partitions
+        (plan, 64, 32, 8, 128, 16, 8192, 3, 2),         # GQA 7B, warp MMAs
+        (plan, 16, 64, 8, 128, 16, 32768, 3, 2),        # 70B long context
+        (plan_int8, 64, 32, 8, 128, 16, 8192, 4, 1),    # INT8 GQA 7B
+        (plan_int8, 16, 64, 8, 128, 16, 32768, 4, 1),   # INT8 70B: the partial-bytes floor
+        (plan_int8, 32, 32, 32, 128, 16, 4096, 6, 1),   # INT8 MHA 7B, per-lane loops
+        (plan_int8, 4, 4, 4, 64, 16, 100, 6, 1),        # tiny: one partition
+    ]
+    got = {}
+    for fn, b, hq, hkv, d, bs, maxl, resident, eb in cases:
+        st, (p, n, _, merge) = fn(lib, b, hq, hkv, d, bs, maxl, 0)
+        assert st == 0 and p == expect(b, hq, hkv, d, bs, maxl, resident, eb), (fn.__name__, b, hq, hkv, maxl, p)
+        assert (n - 1) * p < max(maxl, 1) <= n * p and merge == (n > 1)
+        got[(fn.__name__, b, hq, hkv, maxl)] = p
+    assert got[("plan", 32, 32, 32, 4096)] == 1376
+    assert got[("plan_int8", 64, 32, 8, 8192)] == 832
+    assert got[("plan_int8", 16, 64, 8, 32768)] == 1040
+    assert got[("plan_int8", 32, 32, 32, 4096)] == 512
+
+
+def test_int8_and_16bit_decode_share_explicit_partitions(lib):
+    # with an explicit partition the INT8 and 16-bit calls split alike, so the two
+    # workspace queries agree for every shape (explicit partitions: no device query)
     for b, hq, hkv, d, bs, maxl, part in [(4, 32, 8, 128, 16, 4096, 512), (16, 64, 8, 128, 16, 32768, 1024),
                                           (3, 4, 4, 64, 8, 100, 16), (7, 48, 8, 128, 32, 2000, 256)]:
         a = lib.pkv_decode_workspace_bytes(b, hq, hkv, d, bs, maxl, part)
