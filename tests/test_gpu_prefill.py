@@ -2,9 +2,9 @@
 ("大模型 (LLM) 推理加速核心技术解析" §2 causal attention with a cache; "KV Cache从原理到实战"
 §2.3 / §5.4): within |got-ref| <= 5e-3 + 1e-2|ref| over GQA groups 1..16, every
 block size, both 16-bit types, ragged chunks (1 token, tile edges, several row
-tiles), empty caches and long cached prefixes, forced KV splits, empty chunks,
-rows outside any chunk, out-of-contract lengths (flagged, not written), and the
-full-size prefill workloads on sampled rows."""
+tiles), whole prompts of one length, empty caches and long cached prefixes, forced
+KV splits, empty chunks, rows outside any chunk, out-of-contract lengths (flagged,
+not written), and the full-size prefill workloads on sampled rows."""
 import numpy as np
 import pytest
 import torch
@@ -43,6 +43,21 @@ def test_prefill_shapes(dtype, bs, hq, hkv):
     wl = make_prefill_workload(num_q_heads=hq, num_kv_heads=hkv, head_dim=128, block_size=bs,
                                cached_lens=cached, chunk_lens=chunks, dtype=dtype,
                                seed=hq + bs, device=str(dev))
+    _check(wl)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("hq,hkv,prompt", [(8, 8, 256), (8, 8, 300), (32, 8, 512), (32, 8, 333),
+                                           (48, 8, 200), (64, 8, 129)])
+def test_prefill_whole_prompts_of_one_length(dtype, hq, hkv, prompt):
+    """Whole prompts of one length on an empty cache (the (sequence, KV head)-major order of
+    row-tile pairs): full row tiles leave through the output tensor map, a last row tile that
+    reaches past its chunk row by row (prompt not a multiple of 128 / G tokens; G = 6 leaves
+    rows R..127 of every tile unused)."""
+    dev = device()
+    wl = make_prefill_workload(num_q_heads=hq, num_kv_heads=hkv, head_dim=128, block_size=16,
+                               cached_lens=[0] * 5, chunk_lens=[prompt] * 5, dtype=dtype,
+                               seed=hq + prompt, device=str(dev))
     _check(wl)
 
 
