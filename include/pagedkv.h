@@ -395,11 +395,13 @@ PKV_API uint64_t pkv_launch_count(void);
  * as a pure host function (no CUDA call): given the shape and the SM count it
  * writes the partition size, partitions per sequence, query heads handled per
  * block and whether the merge kernel runs.  Returns PKV_OK or the status the
- * decode call would return for these arguments.  With partition_size 0 the
- * split aims at eight waves of the kernel form's resident blocks per SM (two
- * for the per-lane form, three for the warp-MMA form of 4 or 8 heads per
- * block), with partitions of at least 256 tokens whose K/V bytes are at least
- * 32 times their partial outputs.
+ * decode call would return for these arguments.  A block serves the largest
+ * of 16 (head_dim 128), 8, 4, 2, 1 query heads dividing the group.  With
+ * partition_size 0 the split aims at eight waves of the kernel form's resident
+ * blocks per SM (two for the per-lane form and for 16 heads per block, three
+ * for the warp-MMA form of 4 or 8 heads per block), with partitions of at
+ * least 256 tokens whose K/V bytes are at least 32 times their partial
+ * outputs.
  */
 PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads,
                                    int head_dim, int block_size, int max_context_len,
@@ -409,8 +411,9 @@ PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_hea
 
 /*
  * pkv_decode_int8_plan -- pkv_decode_plan for pkv_paged_attention_decode_int8
- * (the same rules; the INT8 forms keep six (per-lane) or four (warp MMAs)
- * blocks resident per SM, and a token's K/V is half the bytes).
+ * (the same rules, with at most 8 heads per block; the INT8 forms keep six
+ * (per-lane) or four (warp MMAs) blocks resident per SM, and a token's K/V is
+ * half the bytes).
  */
 PKV_API pkv_status pkv_decode_int8_plan(int num_seqs, int num_q_heads, int num_kv_heads,
                                         int head_dim, int block_size, int max_context_len,

@@ -88,15 +88,18 @@ constexpr int kMinAutoPartition = 256; // tokens: below this the per-CTA set-up 
 constexpr int kMergeShare = 32;        // a partition's K/V bytes >= this x its partial bytes
 
 // Decode CTAs resident per SM for each kernel form (their stage budgets and
-// register counts): 16-bit per-lane loops two, 16-bit warp MMAs three, INT8
-// per-lane loops six, INT8 warp MMAs four.
+// register counts): 16-bit per-lane loops two, 16-bit warp MMAs three (two with
+// 16 heads per block), INT8 per-lane loops six, INT8 warp MMAs four.
 int resident_ctas_per_sm(bool int8_kv, int heads_per_block) {
     if (int8_kv) return heads_per_block >= 4 ? 4 : 6;
+    if (heads_per_block == 16) return 2;
     return heads_per_block >= 4 ? 3 : 2;
 }
-// Query heads per CTA: the largest of 8, 4, 2, 1 dividing the group (4 or 8
-// run the products as warp-level MMAs, 1 or 2 as per-lane loops).
-int heads_per_block_for(int group) {
+// Query heads per CTA: the largest of 16 (16-bit caches at head_dim 128), 8, 4, 2, 1
+// dividing the group (4 to 16 run the products as warp-level MMAs, 1 or 2 as
+// per-lane loops).
+int heads_per_block_for(int group, bool int8_kv, int head_dim) {
+    if (!int8_kv && head_dim == 128 && group % 16 == 0) return 16;
     if (group % 8 == 0) return 8;
     if (group % 4 == 0) return 4;
     if (group % 2 == 0) return 2;
@@ -126,7 +129,7 @@ pkv_status plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
     const int max_partition = pkv::DecodeGeom<128, 16>::kMaxTableEntries * block_size;
     if (partition_size > max_partition) return PKV_ERR_INVALID_ARG;
     const int group = num_q_heads / num_kv_heads;
-    const int gh = heads_per_block_for(group);
+    const int gh = heads_per_block_for(group, int8_kv, head_dim);
     const int64_t grid_y = static_cast<int64_t>(num_kv_heads) * (group / gh);
     if (grid_y > 65535 || num_seqs > 65535) return PKV_ERR_INVALID_ARG;
 

@@ -205,7 +205,7 @@ struct DecodeGeom {
 // 128-byte swizzle), used by the warp-MMA forms at head_dim 128; the other forms
 // ignore them.
 template <typename T, typename KT, int D, int BS, int GH>
-__global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
+__global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? (GH == 16 ? 2 : 3) : 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                                               const __grid_constant__ CUtensorMap tmap_v,
                                                               const DecodeParams p) {
@@ -411,6 +411,10 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
     constexpr int STEP = TILE < 16 ? TILE : 16;  // tokens per MMA step
     const int mg = lane >> 2, mt = lane & 3;
     uint32_t qa[KC][2];
+    // 16-bit warp MMAs with 16 heads per block: a lane also holds head mg + 8, the
+    // MMA rows 8..15 that fewer heads leave zero
+    constexpr bool kRows16 = kMma && !kQuant && GH == 16;
+    uint32_t qb[kRows16 ? KC : 1][2];
     constexpr int RUN = kQuant ? 16 : 8;         // a lane's contiguous channels (16 bytes)
     float mqs = 1.f, mqb = 0.f;  // row mg's score scale 2^e and code-offset bias
     // swizzled INT8 staging reads lane t's K chunks 2 t and 2 t + 1 (conflict-free
@@ -475,6 +479,13 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
                 qa[2 * j][1] = u.y;
                 qa[2 * j + 1][0] = u.z;
                 qa[2 * j + 1][1] = u.w;
+                if constexpr (kRows16) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 8 * D + qofs);  // head mg + 8
+                    qb[2 * j][0] = w.x;
+                    qb[2 * j][1] = w.y;
+                    qb[2 * j + 1][0] = w.z;
+                    qb[2 * j + 1][1] = w.w;
+                }
             }
             mqs = p.scale_log2;
         }
@@ -487,6 +498,7 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
     float mh[2] = {-INFINITY, -INFINITY}, lh[2] = {0.f, 0.f};  // INT8: heads 2 mt, 2 mt + 1
     float hqs[2] = {1.f, 1.f}, hqb[2] = {0.f, 0.f};            // their score scales / biases
     float mrow = -INFINITY, lrow = 0.f;                        // 16-bit: head mg
+    float mrow2 = -INFINITY, lrow2 = 0.f;                      // ... and head mg + 8 (16 heads)
     if constexpr (kMma) {
 #pragma unroll
         for (int j = 0; j < NT; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
@@ -672,11 +684,22 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
                                 kSwz ? kt + (j >> 1) * kHalfBytes + kr * 128 + ((((2 * mt + (j & 1)) ^ mg) & 7) << 4)
                                      : krow + 64 * j;
                             const uint4 u = *reinterpret_cast<const uint4 *>(kp);
-                            mma_16816<kMmaBF16>(sacc[h], qa[2 * j][0], 0u, qa[2 * j][1], 0u, u.x, u.y);
-                            mma_16816<kMmaBF16>(sodd[h], qa[2 * j + 1][0], 0u, qa[2 * j + 1][1], 0u, u.z, u.w);
+                            if constexpr (kRows16) {
+                                mma_16816<kMmaBF16>(sacc[h], qa[2 * j][0], qb[2 * j][0], qa[2 * j][1], qb[2 * j][1],
+                                                    u.x, u.y);
+                                mma_16816<kMmaBF16>(sodd[h], qa[2 * j + 1][0], qb[2 * j + 1][0], qa[2 * j + 1][1],
+                                                    qb[2 * j + 1][1], u.z, u.w);
+                            } else {
+                                mma_16816<kMmaBF16>(sacc[h], qa[2 * j][0], 0u, qa[2 * j][1], 0u, u.x, u.y);
+                                mma_16816<kMmaBF16>(sodd[h], qa[2 * j + 1][0], 0u, qa[2 * j + 1][1], 0u, u.z, u.w);
+                            }
                         }
                         sacc[h][0] += sodd[h][0];
                         sacc[h][1] += sodd[h][1];
+                        if constexpr (kRows16) {
+                            sacc[h][2] += sodd[h][2];
+                            sacc[h][3] += sodd[h][3];
+                        }
                     }
                     // row mg's scores in log2 units (d0, d1: tokens 2 mt, 2 mt + 1 of the
                     // n-tile); tokens past the context -> -inf
@@ -686,14 +709,30 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
 #pragma unroll
                         for (int e = 0; e < 2; ++e)
                             sc[2 * h + e] = tb + 8 * h + 2 * mt + e < valid ? sacc[h][e] * mqs : -INFINITY;
-                    float mx = sc[0];
+                    // ... and row mg + 8's (d2, d3) with 16 heads per block
+                    float sc2[kRows16 ? STEP / 4 : 1];
+                    if constexpr (kRows16) {
 #pragma unroll
-                    for (int e = 1; e < STEP / 4; ++e) mx = fmaxf(mx, sc[e]);
+                        for (int h = 0; h < STEP / 8; ++h)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e)
+                                sc2[2 * h + e] = tb + 8 * h + 2 * mt + e < valid ? sacc[h][2 + e] * mqs : -INFINITY;
+                    }
+                    float mx = sc[0], mx2 = kRows16 ? sc2[0] : -INFINITY;
+#pragma unroll
+                    for (int e = 1; e < STEP / 4; ++e) {
+                        mx = fmaxf(mx, sc[e]);
+                        if constexpr (kRows16) mx2 = fmaxf(mx2, sc2[e]);
+                    }
                     // over the row's four lanes: finite, as token tb is in the context
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                    const bool grow = mx > mrow;
-                    if (__any_sync(0xffffffffu, grow)) {
+                    if constexpr (kRows16) {
+                        mx2 = fmaxf(mx2, __shfl_xor_sync(0xffffffffu, mx2, 1));
+                        mx2 = fmaxf(mx2, __shfl_xor_sync(0xffffffffu, mx2, 2));
+                    }
+                    const bool grow = mx > mrow, grow2 = kRows16 && mx2 > mrow2;
+                    if (__any_sync(0xffffffffu, grow || grow2)) {
                         const float alpha = grow ? fast_exp2(mrow - mx) : 1.f;  // 0 when mrow = -inf
                         lrow *= alpha;
 #pragma unroll
@@ -702,16 +741,32 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
                             oacc[nt][1] *= alpha;
                         }
                         if (grow) mrow = mx;
+                        if constexpr (kRows16) {
+                            const float alpha2 = grow2 ? fast_exp2(mrow2 - mx2) : 1.f;
+                            lrow2 *= alpha2;
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                oacc[nt][2] *= alpha2;
+                                oacc[nt][3] *= alpha2;
+                            }
+                            if (grow2) mrow2 = mx2;
+                        }
                     }
                     // the weights meet V rounded to the cache type (as the A fragment of P V,
                     // rows and k indices those of S); the row sum adds the rounded values
-                    uint32_t pa[STEP / 8];
+                    uint32_t pa[STEP / 8], pb[STEP / 8];
 #pragma unroll
                     for (int h = 0; h < STEP / 8; ++h) {
                         float r0, r1;
                         pa[h] = pack_mma2<kMmaBF16>(fast_exp2(sc[2 * h] - mrow), fast_exp2(sc[2 * h + 1] - mrow),
                                                     r0, r1);
                         lrow += r0 + r1;
+                        pb[h] = 0u;
+                        if constexpr (kRows16) {
+                            pb[h] = pack_mma2<kMmaBF16>(fast_exp2(sc2[2 * h] - mrow2),
+                                                        fast_exp2(sc2[2 * h + 1] - mrow2), r0, r1);
+                            lrow2 += r0 + r1;
+                        }
                     }
                     // O += P V: B column mg of n-tile nt is channel (D / 8) mg + nt; lane
                     // (mg, mt) reads tokens tb + 2 mt, +1 (b0) and tb + 8 + 2 mt, +1 (b1) at its
@@ -775,8 +830,8 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
                         }
 #pragma unroll
                         for (int e = 0; e < 2; ++e)
-                            mma_16816<kMmaBF16>(oacc[2 * w + e], pa[0], 0u, STEP == 16 ? pa[STEP / 8 - 1] : 0u, 0u,
-                                                b0[e], b1[e]);
+                            mma_16816<kMmaBF16>(oacc[2 * w + e], pa[0], pb[0], STEP == 16 ? pa[STEP / 8 - 1] : 0u,
+                                                STEP == 16 ? pb[STEP / 8 - 1] : 0u, b0[e], b1[e]);
                     }
                 }
             } else {
@@ -902,9 +957,11 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
     } else if constexpr (kMma) {
         lrow += __shfl_xor_sync(0xffffffffu, lrow, 1);
         lrow += __shfl_xor_sync(0xffffffffu, lrow, 2);
+        lrow2 += __shfl_xor_sync(0xffffffffu, lrow2, 1);
+        lrow2 += __shfl_xor_sync(0xffffffffu, lrow2, 2);
         if (aborted) {
-            mrow = -INFINITY;
-            lrow = 0.f;
+            mrow = mrow2 = -INFINITY;
+            lrow = lrow2 = 0.f;
         }
     } else {
 #pragma unroll
@@ -946,7 +1003,8 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
             }
         }
     } else if constexpr (kMma) {
-        // d0 / d1 of n-tile nt: head mg, channels (D / 8) (2 mt) + nt / (D / 8) (2 mt + 1) + nt
+        // d0 / d1 of n-tile nt: head mg, channels (D / 8) (2 mt) + nt / (D / 8) (2 mt + 1) + nt;
+        // d2 / d3: head mg + 8 (16 heads per block)
         if (mg < GH) {
             float *row = mine + mg * (D + 4);
 #pragma unroll
@@ -957,6 +1015,18 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? 3 : 1)
             if (mt == 0) {
                 row[D] = mrow;
                 row[D + 1] = lrow;
+            }
+        }
+        if constexpr (kRows16) {
+            float *row = mine + (mg + 8) * (D + 4);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                row[(D / 8) * (2 * mt) + nt] = oacc[nt][2];
+                row[(D / 8) * (2 * mt + 1) + nt] = oacc[nt][3];
+            }
+            if (mt == 0) {
+                row[D] = mrow2;
+                row[D + 1] = lrow2;
             }
         }
     } else {

@@ -65,6 +65,10 @@ pkv_status launch_decode_gh(const DecodeParams &p, const DecodeMaps &m, int gh, 
         case 2: return launch_decode_one<T, KT, D, BS, 2>(p, m, grid, s, overlap);
         case 4: return launch_decode_one<T, KT, D, BS, 4>(p, m, grid, s, overlap);
         case 8: return launch_decode_one<T, KT, D, BS, 8>(p, m, grid, s, overlap);
+        case 16:
+            // 16 heads per block: the 16-bit warp-MMA form at head_dim 128
+            if constexpr (sizeof(KT) == 2 && D == 128) return launch_decode_one<T, KT, D, BS, 16>(p, m, grid, s, overlap);
+            break;
     }
     return PKV_ERR_UNSUPPORTED;
 }

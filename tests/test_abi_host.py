@@ -193,13 +193,16 @@ def test_plan_explicit_partition(lib):
 
 
 def test_plan_heads_per_block_follows_the_group(lib):
-    # a block serves the largest of 8, 4, 2, 1 query heads dividing the group, whatever
-    # the context length and head_dim (a group of 16 takes two blocks of 8)
+    # a block serves the largest of 16 (16-bit caches at head_dim 128), 8, 4, 2, 1 query
+    # heads dividing the group, whatever the context length; a group of 16 takes one block
+    # of 16 at head_dim 128 and two blocks of 8 at head_dim 64 or over an INT8 cache
     for hq, hkv, want in [(32, 32, 1), (32, 16, 2), (32, 8, 4), (64, 8, 8), (24, 8, 1),
-                          (48, 8, 2), (128, 8, 8)]:
+                          (48, 8, 2), (128, 8, 16), (256, 8, 16)]:
         for d, maxl in [(128, 4000), (128, 1000), (64, 4000)]:
             st, (_, _, gh, _) = plan(lib, 4, hq, hkv, d, 16, maxl, 0)
-            assert st == 0 and gh == want, (hq, hkv, d, maxl)
+            assert st == 0 and gh == (8 if want == 16 and d == 64 else want), (hq, hkv, d, maxl)
+            st, (_, _, gh8, _) = plan_int8(lib, 4, hq, hkv, d, 16, maxl, 0)
+            assert st == 0 and gh8 == min(want, 8), (hq, hkv, d, maxl)
 
 
 def test_plan_gqa_partitions_cover_the_context(lib):

@@ -41,7 +41,8 @@ def _check_step(wl_dev, partition_size=0):
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (8, 4), (16, 4), (32, 4), (12, 4), (24, 4), (64, 4)])
 def test_decode_shapes(dtype, d, bs, hq, hkv, longest):
     """Every shape, with a short and a long batch: groups of 4, 8 or 16 query heads per KV
-    head run as warp-level MMAs (16 as two blocks of 8), the others as per-lane loops."""
+    head run as warp-level MMAs (16 in one block at head_dim 128, as two blocks of 8 at
+    head_dim 64), the others as per-lane loops."""
     dev = device()
     lens = [1, bs - 1, bs, bs + 1, 5 * bs + 3, longest, 17]
     wl = make_decode_workload(num_seqs=len(lens), num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
