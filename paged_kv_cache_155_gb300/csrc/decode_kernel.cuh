@@ -1089,36 +1089,45 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? (GH == 16 
 
 // Log-sum-exp merge of the partitions of each (sequence, query head):
 //   M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L.
-// One warp per (sequence, query head); sequences that fit one partition were
-// written by the main kernel and are skipped.  Lane q reads partition q's m and
-// l, so the maximum and the weights take one round of loads and shuffles; the
-// partial outputs (D / 32 values per lane and partition) are then read
-// kMergeUnroll partitions at a time, all in flight together.  Launched behind
-// the decode kernel (programmatic dependent launch): it waits for that grid's
-// partials before reading any.
+// WPR warps per (sequence, query head): one (four rows per block) for a few
+// partitions, four (one row per block) for many, warp w taking partitions w,
+// w + 4, ... and the four results combined through shared memory as they would
+// be partitions (the same formula over M_w, L_w, O_w).  Sequences that fit one
+// partition were written by the main kernel and are skipped.  In a warp, lane q
+// reads its q-th partition's m and l, so the maximum and the weights take one
+// round of loads and shuffles; the partial outputs (D / 32 values per lane and
+// partition) are then read kMergeUnroll partitions at a time, all in flight
+// together.  Launched behind the decode kernel (programmatic dependent launch):
+// it waits for that grid's partials before reading any.
 constexpr int kMergeUnroll = 8;
+constexpr int kMergeWideFrom = 32;  // partitions per row from which four warps share a row
 
-template <typename T, int D>
+template <typename T, int D, int WPR>
 __global__ void __launch_bounds__(128) paged_decode_merge_kernel(const DecodeParams p,
                                                                  int num_rows) {
+    static_assert(WPR == 1 || WPR == 4, "one or four warps per row");
     pdl_wait();
     constexpr int PER_LANE = D / 32;
     using Part = typename std::conditional<PER_LANE == 4, float4, float2>::type;
     static_assert(PER_LANE == 4 || PER_LANE == 2, "head_dim 128 or 64");
-    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    __shared__ float comb[WPR == 4 ? 4 : 1][D + 2];  // four warps' (o, m, l) of one row
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (4 / WPR) + warp / WPR;  // uniform over a block when WPR == 4
+    const int share = warp % WPR;                          // this warp takes partitions share + WPR i
     if (row >= num_rows) return;
     const int seq = row / p.num_q_heads;
     int len = p.context_lens[seq];  // clamped exactly as the main kernel does
-    if (p.tok_begin > 0 && len < p.tok_begin && lane == 0 && (row % p.num_q_heads) == 0)
+    if (p.tok_begin > 0 && len < p.tok_begin && lane == 0 && share == 0 && (row % p.num_q_heads) == 0)
         raise_flag(p.status, PKV_DEVERR_CONTEXT_LEN);  // shorter than the shared prefix
     if (len < 0) len = 0;
     if (len > p.len_cap) len = p.len_cap;
     const int nparts = p.slot_base + partitions_of(p, len);  // slots holding partials
     if (nparts <= 1 && !p.always_partial) return;           // written by the decode kernel
+    const int mine = nparts > share ? (nparts - share + WPR - 1) / WPR : 0;  // this warp's partitions
     const int64_t base = static_cast<int64_t>(row) * p.num_partitions;
+    auto slot = [&](int i) { return share + WPR * i; };  // the slot of this warp's i-th partition
     float mmax = -INFINITY;
-    for (int q = lane; q < nparts; q += 32) mmax = fmaxf(mmax, p.ws_m[base + q]);
+    for (int q = lane; q < mine; q += 32) mmax = fmaxf(mmax, p.ws_m[base + slot(q)]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mmax = fmaxf(mmax, __shfl_xor_sync(0xffffffffu, mmax, o));
     float lsum = 0.f;
@@ -1126,19 +1135,19 @@ __global__ void __launch_bounds__(128) paged_decode_merge_kernel(const DecodePar
 #pragma unroll
     for (int e = 0; e < PER_LANE; ++e) o[e] = 0.f;
     const Part *parts = reinterpret_cast<const Part *>(p.ws_o + base * D) + lane;  // slot q at q * 32
-    for (int q0 = 0; q0 < nparts; q0 += 32) {
-        const int cnt = min(32, nparts - q0);
+    for (int q0 = 0; q0 < mine; q0 += 32) {
+        const int cnt = min(32, mine - q0);
         float w = 0.f;  // this lane's partition q0 + lane
         if (lane < cnt) {
-            const float mq = p.ws_m[base + q0 + lane];
+            const float mq = p.ws_m[base + slot(q0 + lane)];
             w = mq == -INFINITY ? 0.f : fast_exp2(mq - mmax);
-            lsum += w * p.ws_l[base + q0 + lane];
+            lsum += w * p.ws_l[base + slot(q0 + lane)];
         }
         for (int j0 = 0; j0 < cnt; j0 += kMergeUnroll) {
             Part v[kMergeUnroll];
 #pragma unroll
             for (int u = 0; u < kMergeUnroll; ++u)
-                if (j0 + u < cnt) v[u] = parts[static_cast<int64_t>(q0 + j0 + u) * 32];
+                if (j0 + u < cnt) v[u] = parts[static_cast<int64_t>(slot(q0 + j0 + u)) * 32];
 #pragma unroll
             for (int u = 0; u < kMergeUnroll; ++u) {
                 const float wu = __shfl_sync(0xffffffffu, w, (j0 + u) & 31);
@@ -1152,6 +1161,33 @@ __global__ void __launch_bounds__(128) paged_decode_merge_kernel(const DecodePar
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    if constexpr (WPR == 4) {
+        // the four warps' results, relative to their own maxima, combined in warp 0
+#pragma unroll
+        for (int e = 0; e < PER_LANE; ++e) comb[share][lane * PER_LANE + e] = o[e];
+        if (lane == 0) {
+            comb[share][D] = mmax;
+            comb[share][D + 1] = lsum;
+        }
+        __syncthreads();
+        if (share != 0) return;
+        float mw[4], mall = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            mw[w] = comb[w][D];
+            mall = fmaxf(mall, mw[w]);
+        }
+        lsum = 0.f;
+#pragma unroll
+        for (int e = 0; e < PER_LANE; ++e) o[e] = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float sw = mw[w] == -INFINITY ? 0.f : fast_exp2(mw[w] - mall);
+            lsum += sw * comb[w][D + 1];
+#pragma unroll
+            for (int e = 0; e < PER_LANE; ++e) o[e] = fmaf(sw, comb[w][lane * PER_LANE + e], o[e]);
+        }
+    }
     T *dst = static_cast<T *>(p.out) + static_cast<int64_t>(row) * D + lane * PER_LANE;
 #pragma unroll
     for (int e = 0; e < PER_LANE; ++e) dst[e] = Elem<T>::from_f32(lsum > 0.f ? o[e] / lsum : 0.f);

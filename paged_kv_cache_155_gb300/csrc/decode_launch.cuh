@@ -92,11 +92,17 @@ pkv_status launch_decode_typed(const DecodeParams &p, const DecodeMaps &m, int h
         else if (block_size == 32) st = launch_decode_gh<T, KT, 64, 32>(p, m, gh, grid, s, overlap);
     }
     if (st != PKV_OK || merge_rows == 0) return st;
-    const unsigned blocks = static_cast<unsigned>((merge_rows + 3) / 4);
-    const cudaError_t err =
-        head_dim == 128
-            ? launch_kernel(paged_decode_merge_kernel<T, 128>, dim3(blocks), dim3(128), 0, s, true, p, merge_rows)
-            : launch_kernel(paged_decode_merge_kernel<T, 64>, dim3(blocks), dim3(128), 0, s, true, p, merge_rows);
+    // four warps share a row once a row has many partitions (their loads in flight
+    // together instead of one warp's rounds of them)
+    const bool wide = p.num_partitions >= kMergeWideFrom;
+    const unsigned blocks = static_cast<unsigned>(wide ? merge_rows : (merge_rows + 3) / 4);
+    cudaError_t err;
+    if (head_dim == 128)
+        err = wide ? launch_kernel(paged_decode_merge_kernel<T, 128, 4>, dim3(blocks), dim3(128), 0, s, true, p, merge_rows)
+                   : launch_kernel(paged_decode_merge_kernel<T, 128, 1>, dim3(blocks), dim3(128), 0, s, true, p, merge_rows);
+    else
+        err = wide ? launch_kernel(paged_decode_merge_kernel<T, 64, 4>, dim3(blocks), dim3(128), 0, s, true, p, merge_rows)
+                   : launch_kernel(paged_decode_merge_kernel<T, 64, 1>, dim3(blocks), dim3(128), 0, s, true, p, merge_rows);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
