@@ -7,7 +7,7 @@ the Llama-2-7B-shaped MHA decode layer (32 sequences x 4096 tokens, 32 heads of
 128, block 16, fp16, 2 GiB pool -- larger than L2, so no flush is needed).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload mha7b|gqa7b|prefix|long70b|tiny|mha7b_int8|gqa7b_int8|long70b_int8]
+                    [--workload mha7b|gqa7b|prefix|long70b|tiny|mha7b_int8|gqa7b_int8|long70b_int8|gqa16]
                     [--partition P]
 
 Prints one JSON line (rank 0).  `value` is decode tokens/s (one token per
@@ -207,7 +207,7 @@ def _config_summary(main, line, others):
                      "decode_us": round(c["decode_ms"] * 1e3, 1),
                      "plain_decode_hbm_frac_unique": r3(w["hbm_frac_of_measured"])}
         out[key] = e
-    for name in ("mha7b_int8", "gqa7b_int8", "long70b_int8"):
+    for name in ("mha7b_int8", "gqa7b_int8", "long70b_int8", "gqa16"):
         w = others.get(name)
         if w is not None:
             out[name] = {"hbm_frac": r3(w["hbm_frac_of_measured"]),
@@ -806,7 +806,7 @@ def run_ours(args):
     if world == 1 and not args.no_other_workloads:
         others = {}
         for name in ("tiny", "mha7b", "gqa7b", "prefix", "long70b", "mha7b_int8", "gqa7b_int8",
-                     "long70b_int8"):
+                     "long70b_int8", "gqa16"):
             if name == args.workload:
                 continue
             others[name] = measure_workload(pkv, name, dev, 300, peak)
@@ -829,7 +829,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mha7b",
                     choices=["tiny", "mha7b", "gqa7b", "prefix", "long70b", "mha7b_int8",
-                             "gqa7b_int8", "long70b_int8"])
+                             "gqa7b_int8", "long70b_int8", "gqa16"])
     ap.add_argument("--partition", type=int, default=-1,
                     help="tokens per split-context partition (0 = library's choice; "
                          "default: the workload's own setting)")

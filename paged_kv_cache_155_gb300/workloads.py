@@ -23,6 +23,10 @@ The five named workloads follow the shapes the pages discuss:
              private suffix U[64, 1024]; bf16; 128 copy-on-write pairs.
   long70b -- Llama-2-70B-shaped GQA: 64 q / 8 kv heads, 16 sequences of 32768.
 
+An extra decode shape, outside the pages' configurations, exercises groups of 16
+query heads per KV head (one 16-head block per KV head):
+  gqa16   -- 128 q / 8 kv heads, head_dim 128, bs 16, 16 sequences of 8192, bf16.
+
 Chunked-prefill workloads (prefill7b, chunked70b) are described at
 make_prefill_workload below.
 
@@ -251,6 +255,14 @@ def long70b(device="cpu", seed=4, num_seqs=16, context_len=32768, num_blocks=Non
         device=device, kv_dtype=kv_dtype)
 
 
+def gqa16(device="cpu", seed=8, num_seqs=16, context_len=8192, num_blocks=None):
+    nb = num_blocks if num_blocks is not None else num_seqs * math.ceil(context_len / 16)
+    return make_decode_workload(
+        name="gqa16", num_seqs=num_seqs, num_q_heads=128, num_kv_heads=8, head_dim=128,
+        block_size=16, context_lens=[context_len] * num_seqs, num_blocks=nb,
+        dtype=torch.bfloat16, seed=seed, device=device)
+
+
 def mha7b_int8(device="cpu", seed=1, **kw):
     return mha7b(device=device, seed=seed, kv_dtype=torch.int8, **kw)
 
@@ -376,8 +388,9 @@ PREFILL_NAMED = {"prefill7b": prefill7b, "chunked70b": chunked70b}
 
 
 NAMED = {"tiny": tiny, "mha7b": mha7b, "gqa7b": gqa7b, "prefix": prefix, "long70b": long70b,
-         "mha7b_int8": mha7b_int8, "gqa7b_int8": gqa7b_int8, "long70b_int8": long70b_int8}
+         "mha7b_int8": mha7b_int8, "gqa7b_int8": gqa7b_int8, "long70b_int8": long70b_int8,
+         "gqa16": gqa16}
 
 # The default partition size each named workload is run with (0 = library's choice).
 DEFAULT_PARTITION = {"tiny": 0, "mha7b": 0, "gqa7b": 0, "prefix": 0, "long70b": 512,
-                     "mha7b_int8": 0, "gqa7b_int8": 0, "long70b_int8": 0}
+                     "mha7b_int8": 0, "gqa7b_int8": 0, "long70b_int8": 0, "gqa16": 0}

@@ -1,8 +1,9 @@
-"""The five named workloads at full size, in the launch configuration the
-benchmark times: the cache write is compared bit-exactly over the whole pool,
-attention on sampled sequences against the oracle (which computes them one by
-one), and the shared-prefix workload's copy-on-write step is checked both
-bit-exactly and as an attention invariant (before vs after the copies)."""
+"""The five named workloads (and the 16-head GQA shape) at full size, in the
+launch configuration the benchmark times: the cache write is compared
+bit-exactly over the whole pool, attention on sampled sequences against the
+oracle (which computes them one by one), and the shared-prefix workload's
+copy-on-write step is checked both bit-exactly and as an attention invariant
+(before vs after the copies)."""
 import numpy as np
 import pytest
 import torch
@@ -23,7 +24,7 @@ def _sample(wl):
     return sorted(sel)
 
 
-@pytest.mark.parametrize("name", ["tiny", "mha7b", "gqa7b", "long70b"])
+@pytest.mark.parametrize("name", ["tiny", "mha7b", "gqa7b", "long70b", "gqa16"])
 def test_named_workload_full_size(name):
     dev = device()
     wl = workloads.NAMED[name](device=str(dev))
