@@ -270,7 +270,7 @@ pkv_status decode_impl(const void *q, const void *k_cache, const void *v_cache,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 grid(static_cast<unsigned>(nparts), static_cast<unsigned>(num_kv_heads * p.subgroups),
                     static_cast<unsigned>(num_seqs));
-    // The warp-MMA forms at head_dim 128 (4 or 8 heads per block) stage K/V tiles by
+    // The warp-MMA forms at head_dim 128 (4, 8 or 16 heads per block) stage K/V tiles by
     // tiled TMA copies with a 128-byte swizzle
     pkv::DecodeMaps maps{};
     if (head_dim == 128 && gh >= 4 &&

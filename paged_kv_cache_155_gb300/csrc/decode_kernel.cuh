@@ -40,17 +40,17 @@
 //    leaves known sums: a dot product starts from -1152 times the lane's query
 //    sum, and the output removes 1152 times the weight sum, whose terms are the
 //    weights rounded to fp16 exactly as they meet V.
-//  * 4 or 8 query heads per block (grouped-query attention): the lane loops
+//  * 4, 8 or 16 query heads per block (grouped-query attention): the lane loops
 //    would spend GH FMAs per cache element, so both products run as warp-level
 //    MMAs (m16n8k16, fp32 accumulators) on register fragments, 16 tokens per
 //    step, and each warp still streams its own ring with no hand-off to other
 //    warps.  The k indices of QK^T are mapped to channels so that a lane's
 //    16-byte vector of a token row holds whole k pairs.
 //    - 16-bit cache: S = Q K^T with the heads as the 16 rows (rows past GH are
-//      zero) and the tokens as columns; the K words go straight in as the B
-//      fragment, and the S accumulators of a row are the A fragment of P V
-//      after the softmax.  V's B fragment pairs two tokens of one channel with
-//      one byte permute.
+//      zero; with 16 heads a lane holds heads g and g + 8) and the tokens as
+//      columns; the K words go straight in as the B fragment, and the S
+//      accumulators of a row are the A fragment of P V after the softmax.  V's
+//      B fragment pairs two tokens of one channel with one byte permute.
 //    - INT8 cache: S^T = K Q^T with the tokens as rows and the heads as
 //      columns, on the fp16 values code + 1152 widened in registers (one byte
 //      permute per pair); P moves into the B layout of O^T = (V + 1152)^T P^T
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? (GH == 16 
                                                               const __grid_constant__ CUtensorMap tmap_v,
                                                               const DecodeParams p) {
     constexpr bool kQuant = sizeof(KT) == 1;
-    // 4 or 8 query heads per block: the products run as warp-level MMAs (the per-lane
+    // 4, 8 or 16 query heads per block: the products run as warp-level MMAs (the per-lane
     // loops would spend GH FMAs per element), INT8 codes on exact fp16 copies
     constexpr bool kMma = GH >= 4;
     constexpr bool kMmaBF16 = std::is_same<KT, __nv_bfloat16>::value;  // MMA operand type
