@@ -59,7 +59,7 @@ size_t prefill_workspace(int num_rows, int num_q_heads, int splits) {
     return static_cast<size_t>(num_rows) * num_q_heads * splits * (128 + 2) * sizeof(float);
 }
 
-template <typename T, int BS>
+template <typename T, int BS, bool kSorted>
 pkv_status launch_prefill_one(const pkv::PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                               const CUtensorMap &tv, const CUtensorMap &to, int grid, cudaStream_t stream) {
     static std::atomic<uint64_t> configured_devices{0};
@@ -67,13 +67,13 @@ pkv_status launch_prefill_one(const pkv::PrefillParams &p, const CUtensorMap &tq
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
     if (!bit || !(configured_devices.load(std::memory_order_acquire) & bit)) {
-        if (cudaFuncSetAttribute(pkv::paged_prefill_tc_kernel<T, BS>,
+        if (cudaFuncSetAttribute(pkv::paged_prefill_tc_kernel<T, BS, kSorted>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  pkv::PrefillLayout::kSmemBytes) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured_devices.fetch_or(bit, std::memory_order_acq_rel);
     }
-    pkv::paged_prefill_tc_kernel<T, BS>
+    pkv::paged_prefill_tc_kernel<T, BS, kSorted>
         <<<grid, pkv::PrefillLayout::kThreads, pkv::PrefillLayout::kSmemBytes, stream>>>(tq, tk, tv, to, p);
     pkv::count_launch();
     return pkv::launch_status();
@@ -84,9 +84,16 @@ pkv_status launch_prefill(const pkv::PrefillParams &p, const CUtensorMap &tq, co
                           const CUtensorMap &tv, const CUtensorMap &to, int block_size, int grid,
                           int max_query_len, cudaStream_t s) {
     pkv_status st = PKV_ERR_UNSUPPORTED;
-    if (block_size == 8) st = launch_prefill_one<T, 8>(p, tq, tk, tv, to, grid, s);
-    else if (block_size == 16) st = launch_prefill_one<T, 16>(p, tq, tk, tv, to, grid, s);
-    else if (block_size == 32) st = launch_prefill_one<T, 32>(p, tq, tk, tv, to, grid, s);
+    const bool sorted = p.order == pkv::kOrderSortedGroups;
+    if (block_size == 8)
+        st = sorted ? launch_prefill_one<T, 8, true>(p, tq, tk, tv, to, grid, s)
+                    : launch_prefill_one<T, 8, false>(p, tq, tk, tv, to, grid, s);
+    else if (block_size == 16)
+        st = sorted ? launch_prefill_one<T, 16, true>(p, tq, tk, tv, to, grid, s)
+                    : launch_prefill_one<T, 16, false>(p, tq, tk, tv, to, grid, s);
+    else if (block_size == 32)
+        st = sorted ? launch_prefill_one<T, 32, true>(p, tq, tk, tv, to, grid, s)
+                    : launch_prefill_one<T, 32, false>(p, tq, tk, tv, to, grid, s);
     if (st != PKV_OK || p.splits == 1) return st;
     const int64_t rows = static_cast<int64_t>(max_query_len) * p.num_q_heads;
     const dim3 mgrid(static_cast<unsigned>((rows + 3) / 4), static_cast<unsigned>(p.num_seqs));
@@ -192,10 +199,16 @@ PKV_API pkv_status pkv_paged_attention_prefill(
     p.num_items = pp.items;
     p.splits = pp.splits;
     p.split_tokens = pp.split_tokens;
-    // whole prompts of one length (every chunk max_query_len tokens on an empty
-    // cache): pair order, for L2 reuse of each (sequence, KV head)'s K/V tiles
-    p.pair_order = pp.splits == 1 && num_rows == static_cast<int64_t>(num_seqs) * max_query_len &&
-                   max_context_len == max_query_len;
+    // item order (prefill_item): whole prompts of one length (every chunk
+    // max_query_len tokens on an empty cache) in row-tile pairs, a few sequences of
+    // different lengths by (sequence, KV head) sorted by length, both for L2 reuse
+    // of each (sequence, KV head)'s K/V tiles; otherwise row tiles, heaviest first
+    const bool whole_prompts = num_rows == static_cast<int64_t>(num_seqs) * max_query_len &&
+                               max_context_len == max_query_len;
+    p.order = pp.splits != 1 ? pkv::kOrderRowTiles
+              : whole_prompts ? pkv::kOrderPairs
+              : num_seqs <= pkv::kSortedGroupsMaxSeqs ? pkv::kOrderSortedGroups
+                                                      : pkv::kOrderRowTiles;
     p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
     // persistent: one CTA per SM (or per item when there are fewer)
     const int grid = std::min(pp.items, sm);

@@ -79,9 +79,13 @@ struct PrefillParams {
     int num_items;     // row_tiles * num_kv_heads * num_seqs * splits
     int splits;        // KV splits per row tile
     int split_tokens;  // tokens per split, a multiple of 128
-    int pair_order;    // 1: (sequence, KV head)-major order, heavy and light row tiles paired
+    int order;         // item order: kOrderRowTiles, kOrderPairs or kOrderSortedGroups
     float scale_log2;
 };
+
+// Item orders (PrefillParams::order), see prefill_item.
+constexpr int kOrderRowTiles = 0, kOrderPairs = 1, kOrderSortedGroups = 2;
+constexpr int kSortedGroupsMaxSeqs = 32;  // sequences a block ranks by length itself
 
 // One sequence's chunk start, chunk end and context length, as read from the
 // device arrays.
@@ -89,18 +93,25 @@ struct PrefillSeqVals {
     int q0, q1, len;
 };
 
-// The sequence of item i (no memory access).
-__device__ __forceinline__ int prefill_item_seq(const PrefillParams &p, int i) {
-    if (p.pair_order) return i / p.row_tiles / p.num_kv_heads;
+// The sequence of item i (no global-memory access).  by_len: the sequences by
+// context length, longest first (sorted-groups order only).
+// kSorted: the sorted-groups order (compiled apart, so the other orders' code is
+// not shaped by it).
+template <bool kSorted>
+__device__ __forceinline__ int prefill_item_seq(const PrefillParams &p, int i, const unsigned char *by_len) {
+    if constexpr (kSorted) return by_len[i / p.row_tiles / p.num_kv_heads];
+    if (p.order == kOrderPairs) return i / p.row_tiles / p.num_kv_heads;
     const int per_tile = p.num_kv_heads * p.num_seqs * p.splits;
     return (i % per_tile) / p.num_kv_heads / p.splits;
 }
 
 // Loads item i's sequence values (zeros past the item count).
-__device__ __forceinline__ PrefillSeqVals prefill_seq_vals(const PrefillParams &p, int i) {
+template <bool kSorted>
+__device__ __forceinline__ PrefillSeqVals prefill_seq_vals(const PrefillParams &p, int i,
+                                                          const unsigned char *by_len) {
     PrefillSeqVals v{0, 0, 0};
     if (i < p.num_items) {
-        const int seq = prefill_item_seq(p, i);
+        const int seq = prefill_item_seq<kSorted>(p, i, by_len);
         v.q0 = p.query_start[seq];
         v.q1 = p.query_start[seq + 1];
         v.len = p.context_lens[seq];
@@ -130,19 +141,35 @@ struct PrefillItem {
     int seq;
 };
 
-// Item i of the static order.  Default: row tiles from the last (longest causal
-// range) down, then sequence and split, then KV head, so that CTA c's items c,
-// c + grid, ... are heaviest first.  Pair order (whole prompts of one length, one
-// split): (sequence, KV head) major, and within it the row tiles as last, first,
-// second to last, second, ..., taken two at a time by a CTA (prefill_slot_item),
-// so that every CTA's pair of row tiles carries the same causal work and the
-// CTAs that run together share the K/V tiles of a few (sequence, KV head)
-// pairs in L2.  False when the item holds no work: a row tile past the chunk, a
-// split past the tile's causal limit, or a sequence out of contract (flagged
-// once when `flag`).
+// Item i of the static order.
+// - Row tiles (default): row tiles from the last (longest causal range) down, then
+//   sequence and split, then KV head, so that CTA c's items c, c + grid, ... are
+//   heaviest first.
+// - Pairs (whole prompts of one length, one split): (sequence, KV head) major, and
+//   within it the row tiles as last, first, second to last, second, ..., taken two
+//   at a time by a CTA (prefill_slot_item), so that every CTA's pair of row tiles
+//   carries the same causal work.
+// - Sorted groups (one split, at most kSortedGroupsMaxSeqs sequences of different
+//   lengths): (sequence, KV head) major with the sequences by context length,
+//   longest first (by_len), and within a group the row tiles from the last down;
+//   the CTAs take the items in rounds of one each, every other round in reverse
+//   (prefill_slot_item), which spreads the long and short items evenly.
+// In the last two the CTAs that run together share the K/V tiles of a few
+// (sequence, KV head) pairs in L2.  False when the item holds no work: a row tile
+// past the chunk, a split past the tile's causal limit, or a sequence out of
+// contract (flagged once when `flag`).
+template <bool kSorted>
 __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, const PrefillSeqVals &sv,
-                                             bool flag, PrefillItem &it) {
-    if (p.pair_order) {
+                                             bool flag, PrefillItem &it, const unsigned char *by_len) {
+    if constexpr (kSorted) {
+        const int g = i / p.row_tiles;
+        const int pos = i - g * p.row_tiles;
+        const int rank = g / p.num_kv_heads;
+        it.seq = by_len[rank];
+        it.kvh = g - rank * p.num_kv_heads;
+        it.split = 0;
+        it.row_tile = p.row_tiles - 1 - pos;
+    } else if (p.order == kOrderPairs) {
         const int g = i / p.row_tiles;
         const int pos = i - g * p.row_tiles;
         it.seq = g / p.num_kv_heads;
@@ -176,10 +203,14 @@ __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, cons
     return it.tok_hi > it.tok_lo;
 }
 
-// The k-th item of this CTA: items blockIdx.x + k * grid in the default order,
-// the pairs (2 q, 2 q + 1) for q = blockIdx.x + (k / 2) * grid in pair order.
+// The k-th item of this CTA: items blockIdx.x + k * grid in the row-tile order,
+// the pairs (2 q, 2 q + 1) for q = blockIdx.x + (k / 2) * grid in pair order, and
+// item blockIdx.x of round k (counted from the end in odd rounds) in sorted-groups
+// order.
+template <bool kSorted>
 __device__ __forceinline__ int prefill_slot_item(const PrefillParams &p, int k) {
-    if (p.pair_order) return 2 * (blockIdx.x + (k >> 1) * gridDim.x) + (k & 1);
+    if constexpr (kSorted) return k * gridDim.x + ((k & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
+    if (p.order == kOrderPairs) return 2 * (blockIdx.x + (k >> 1) * gridDim.x) + (k & 1);
     return blockIdx.x + k * gridDim.x;
 }
 
@@ -208,7 +239,8 @@ struct PrefillLayout {
     static constexpr int kNumBars = 2 * kKS + 2 * kVS + 2 * kQB + 4 * kSB + 2 + 8 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kOffSum = kOffMisc + 16;     // row-sum exchange: [2 halves][128 rows] fp32
-    static constexpr int kBytes = kOffSum + 2 * 128 * 4;
+    static constexpr int kOffByLen = kOffSum + 2 * 128 * 4;  // sequences by length (sorted-groups order)
+    static constexpr int kBytes = kOffByLen + kSortedGroupsMaxSeqs;
     static constexpr int kSmemBytes = kBytes + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;        // S[3] at 0 / 128 / 256 (P[b] over S[b]), O at 384
     static constexpr uint32_t kOCol = 384;
@@ -217,7 +249,7 @@ struct PrefillLayout {
     static_assert(kSmemBytes <= 232448, "dynamic shared memory per block");
 };
 
-template <typename T, int BS>
+template <typename T, int BS, bool kSorted>
 __global__ void __launch_bounds__(384, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                             const __grid_constant__ CUtensorMap tmap_k,
@@ -246,6 +278,7 @@ __global__ void __launch_bounds__(384, 1)
     uint64_t *o_staged = pair_bar + 8;     // an item's O tile is in its last V slot
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kOffMisc + 4);
+    unsigned char *by_len = sm + L::kOffByLen;  // sorted-groups order: sequences by length
     const uint32_t smem_base = static_cast<uint32_t>(__cvta_generic_to_shared(sm));
 
     if (threadIdx.x == 0) {
@@ -287,6 +320,16 @@ __global__ void __launch_bounds__(384, 1)
                 make_uint4(0, 0, 0, 0);
         }
     }
+    if (kSorted && warp == 2) {
+        // rank the (at most 32) sequences by context length, longest first, ties by index
+        const int len = lane < p.num_seqs ? p.context_lens[lane] : 0;
+        int rank = 0;
+        for (int j = 0; j < p.num_seqs; ++j) {
+            const int lj = __shfl_sync(0xffffffffu, len, j);
+            rank += (lj > len || (lj == len && j < lane)) ? 1 : 0;
+        }
+        if (lane < p.num_seqs) by_len[rank] = static_cast<unsigned char>(lane);
+    }
     if (warp == 0 && lane == 0) {
         tc::prefetch_tensormap(&tmap_q);
         tc::prefetch_tensormap(&tmap_k);
@@ -318,9 +361,9 @@ __global__ void __launch_bounds__(384, 1)
         int q_issue[2] = {-1, -1};
         bool ok = true;
         int jt = 0, n = 0;  // tiles and items so far
-        for (int ki = 0, item = prefill_slot_item(p, 0); item < p.num_items && ok; item = prefill_slot_item(p, ++ki)) {
+        for (int ki = 0, item = prefill_slot_item<kSorted>(p, 0); item < p.num_items && ok; item = prefill_slot_item<kSorted>(p, ++ki)) {
             PrefillItem it;
-            if (!prefill_item(p, item, prefill_seq_vals(p, item), kv == 0, it)) continue;
+            if (!prefill_item<kSorted>(p, item, prefill_seq_vals<kSorted>(p, item, by_len), kv == 0, it, by_len)) continue;
             const int32_t *trow = p.block_tables + static_cast<int64_t>(it.seq) * p.max_blocks_per_seq;
             auto entry = [&](int j) -> int {  // this lane's block of tile j (-1: none or bad)
                 const int t0 = it.tok_lo + j * TILE;
@@ -355,8 +398,8 @@ __global__ void __launch_bounds__(384, 1)
                 q_pending = false;
                 // the next item's Q box into L2 now, so its load does not wait for HBM
                 PrefillItem nx;
-                for (int k2 = ki + 1, i2 = prefill_slot_item(p, k2); i2 < p.num_items; i2 = prefill_slot_item(p, ++k2)) {
-                    if (!prefill_item(p, i2, prefill_seq_vals(p, i2), false, nx)) continue;
+                for (int k2 = ki + 1, i2 = prefill_slot_item<kSorted>(p, k2); i2 < p.num_items; i2 = prefill_slot_item<kSorted>(p, ++k2)) {
+                    if (!prefill_item<kSorted>(p, i2, prefill_seq_vals<kSorted>(p, i2, by_len), false, nx, by_len)) continue;
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
                         tc::tma_prefetch_3d(&tmap_q, c * 64, nx.kvh * p.group, nx.q0 + nx.row_tile * p.tile_tokens);
@@ -433,9 +476,9 @@ __global__ void __launch_bounds__(384, 1)
         constexpr uint32_t idesc_qk = tc::idesc_f16_f32acc(kBF16, 128, 128, false, false);
         bool ok = true;
         int jt = 0, n = 0;
-        for (int ki = 0, item = prefill_slot_item(p, 0); item < p.num_items && ok; item = prefill_slot_item(p, ++ki)) {
+        for (int ki = 0, item = prefill_slot_item<kSorted>(p, 0); item < p.num_items && ok; item = prefill_slot_item<kSorted>(p, ++ki)) {
             PrefillItem it;
-            if (!prefill_item(p, item, prefill_seq_vals(p, item), false, it)) continue;
+            if (!prefill_item<kSorted>(p, item, prefill_seq_vals<kSorted>(p, item, by_len), false, it, by_len)) continue;
             const int qb = n % QB;
             int go = 1;
             if (lane == 0) go = tc_wait(&q_full[qb], (n / QB) & 1, abort_flag, p.status);
@@ -478,9 +521,9 @@ __global__ void __launch_bounds__(384, 1)
         constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, 128, false, true);
         bool ok = true;
         int jt = 0, n_staged = 0;
-        for (int ki = 0, item = prefill_slot_item(p, 0); item < p.num_items && ok; item = prefill_slot_item(p, ++ki)) {
+        for (int ki = 0, item = prefill_slot_item<kSorted>(p, 0); item < p.num_items && ok; item = prefill_slot_item<kSorted>(p, ++ki)) {
             PrefillItem it;
-            if (!prefill_item(p, item, prefill_seq_vals(p, item), false, it)) continue;
+            if (!prefill_item<kSorted>(p, item, prefill_seq_vals<kSorted>(p, item, by_len), false, it, by_len)) continue;
             const bool staged = prefill_staged(p, it);
             for (int j = 0; j < it.ntiles; ++j, ++jt) {
                 int go = 1;
@@ -581,9 +624,9 @@ __global__ void __launch_bounds__(384, 1)
             other = sum_x[(1 - half) * 128 + r];
             return true;
         };
-        for (int ki = 0, item = prefill_slot_item(p, 0); item < p.num_items && ok; item = prefill_slot_item(p, ++ki)) {
+        for (int ki = 0, item = prefill_slot_item<kSorted>(p, 0); item < p.num_items && ok; item = prefill_slot_item<kSorted>(p, ++ki)) {
             PrefillItem it;
-            if (!prefill_item(p, item, prefill_seq_vals(p, item), false, it)) continue;
+            if (!prefill_item<kSorted>(p, item, prefill_seq_vals<kSorted>(p, item, by_len), false, it, by_len)) continue;
             const int row = it.row0 + r;
             const bool live = r < R && row < it.rows;
             const int jtok = live ? row / p.group : 0;
