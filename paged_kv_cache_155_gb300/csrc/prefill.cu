@@ -59,7 +59,7 @@ size_t prefill_workspace(int num_rows, int num_q_heads, int splits) {
     return static_cast<size_t>(num_rows) * num_q_heads * splits * (128 + 2) * sizeof(float);
 }
 
-template <typename T, int BS, bool kSorted>
+template <typename T, int BS, int ORDER>
 pkv_status launch_prefill_one(const pkv::PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                               const CUtensorMap &tv, const CUtensorMap &to, int grid, cudaStream_t stream) {
     static std::atomic<uint64_t> configured_devices{0};
@@ -67,16 +67,25 @@ pkv_status launch_prefill_one(const pkv::PrefillParams &p, const CUtensorMap &tq
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
     if (!bit || !(configured_devices.load(std::memory_order_acquire) & bit)) {
-        if (cudaFuncSetAttribute(pkv::paged_prefill_tc_kernel<T, BS, kSorted>,
+        if (cudaFuncSetAttribute(pkv::paged_prefill_tc_kernel<T, BS, ORDER>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  pkv::PrefillLayout::kSmemBytes) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured_devices.fetch_or(bit, std::memory_order_acq_rel);
     }
-    pkv::paged_prefill_tc_kernel<T, BS, kSorted>
+    pkv::paged_prefill_tc_kernel<T, BS, ORDER>
         <<<grid, pkv::PrefillLayout::kThreads, pkv::PrefillLayout::kSmemBytes, stream>>>(tq, tk, tv, to, p);
     pkv::count_launch();
     return pkv::launch_status();
+}
+
+template <typename T, int BS>
+pkv_status launch_prefill_bs(const pkv::PrefillParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                             const CUtensorMap &tv, const CUtensorMap &to, int grid, cudaStream_t s) {
+    if (p.order == pkv::kOrderSortedGroups)
+        return launch_prefill_one<T, BS, pkv::kOrderSortedGroups>(p, tq, tk, tv, to, grid, s);
+    if (p.order == pkv::kOrderPairs) return launch_prefill_one<T, BS, pkv::kOrderPairs>(p, tq, tk, tv, to, grid, s);
+    return launch_prefill_one<T, BS, pkv::kOrderRowTiles>(p, tq, tk, tv, to, grid, s);
 }
 
 template <typename T>
@@ -84,16 +93,9 @@ pkv_status launch_prefill(const pkv::PrefillParams &p, const CUtensorMap &tq, co
                           const CUtensorMap &tv, const CUtensorMap &to, int block_size, int grid,
                           int max_query_len, cudaStream_t s) {
     pkv_status st = PKV_ERR_UNSUPPORTED;
-    const bool sorted = p.order == pkv::kOrderSortedGroups;
-    if (block_size == 8)
-        st = sorted ? launch_prefill_one<T, 8, true>(p, tq, tk, tv, to, grid, s)
-                    : launch_prefill_one<T, 8, false>(p, tq, tk, tv, to, grid, s);
-    else if (block_size == 16)
-        st = sorted ? launch_prefill_one<T, 16, true>(p, tq, tk, tv, to, grid, s)
-                    : launch_prefill_one<T, 16, false>(p, tq, tk, tv, to, grid, s);
-    else if (block_size == 32)
-        st = sorted ? launch_prefill_one<T, 32, true>(p, tq, tk, tv, to, grid, s)
-                    : launch_prefill_one<T, 32, false>(p, tq, tk, tv, to, grid, s);
+    if (block_size == 8) st = launch_prefill_bs<T, 8>(p, tq, tk, tv, to, grid, s);
+    else if (block_size == 16) st = launch_prefill_bs<T, 16>(p, tq, tk, tv, to, grid, s);
+    else if (block_size == 32) st = launch_prefill_bs<T, 32>(p, tq, tk, tv, to, grid, s);
     if (st != PKV_OK || p.splits == 1) return st;
     const int64_t rows = static_cast<int64_t>(max_query_len) * p.num_q_heads;
     const dim3 mgrid(static_cast<unsigned>((rows + 3) / 4), static_cast<unsigned>(p.num_seqs));

@@ -95,23 +95,23 @@ struct PrefillSeqVals {
 
 // The sequence of item i (no global-memory access).  by_len: the sequences by
 // context length, longest first (sorted-groups order only).
-// kSorted: the sorted-groups order (compiled apart, so the other orders' code is
-// not shaped by it).
-template <bool kSorted>
+// ORDER: the item order (each compiled apart, so no order's code is shaped by the
+// others').
+template <int ORDER>
 __device__ __forceinline__ int prefill_item_seq(const PrefillParams &p, int i, const unsigned char *by_len) {
-    if constexpr (kSorted) return by_len[i / p.row_tiles / p.num_kv_heads];
-    if (p.order == kOrderPairs) return i / p.row_tiles / p.num_kv_heads;
+    if constexpr (ORDER == kOrderSortedGroups) return by_len[i / p.row_tiles / p.num_kv_heads];
+    if constexpr (ORDER == kOrderPairs) return i / p.row_tiles / p.num_kv_heads;
     const int per_tile = p.num_kv_heads * p.num_seqs * p.splits;
     return (i % per_tile) / p.num_kv_heads / p.splits;
 }
 
 // Loads item i's sequence values (zeros past the item count).
-template <bool kSorted>
+template <int ORDER>
 __device__ __forceinline__ PrefillSeqVals prefill_seq_vals(const PrefillParams &p, int i,
                                                           const unsigned char *by_len) {
     PrefillSeqVals v{0, 0, 0};
     if (i < p.num_items) {
-        const int seq = prefill_item_seq<kSorted>(p, i, by_len);
+        const int seq = prefill_item_seq<ORDER>(p, i, by_len);
         v.q0 = p.query_start[seq];
         v.q1 = p.query_start[seq + 1];
         v.len = p.context_lens[seq];
@@ -158,10 +158,10 @@ struct PrefillItem {
 // (sequence, KV head) pairs in L2.  False when the item holds no work: a row tile
 // past the chunk, a split past the tile's causal limit, or a sequence out of
 // contract (flagged once when `flag`).
-template <bool kSorted>
+template <int ORDER>
 __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, const PrefillSeqVals &sv,
                                              bool flag, PrefillItem &it, const unsigned char *by_len) {
-    if constexpr (kSorted) {
+    if constexpr (ORDER == kOrderSortedGroups) {
         const int g = i / p.row_tiles;
         const int pos = i - g * p.row_tiles;
         const int rank = g / p.num_kv_heads;
@@ -169,7 +169,7 @@ __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, cons
         it.kvh = g - rank * p.num_kv_heads;
         it.split = 0;
         it.row_tile = p.row_tiles - 1 - pos;
-    } else if (p.order == kOrderPairs) {
+    } else if constexpr (ORDER == kOrderPairs) {
         const int g = i / p.row_tiles;
         const int pos = i - g * p.row_tiles;
         it.seq = g / p.num_kv_heads;
@@ -207,10 +207,11 @@ __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, cons
 // the pairs (2 q, 2 q + 1) for q = blockIdx.x + (k / 2) * grid in pair order, and
 // item blockIdx.x of round k (counted from the end in odd rounds) in sorted-groups
 // order.
-template <bool kSorted>
+template <int ORDER>
 __device__ __forceinline__ int prefill_slot_item(const PrefillParams &p, int k) {
-    if constexpr (kSorted) return k * gridDim.x + ((k & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
-    if (p.order == kOrderPairs) return 2 * (blockIdx.x + (k >> 1) * gridDim.x) + (k & 1);
+    if constexpr (ORDER == kOrderSortedGroups)
+        return k * gridDim.x + ((k & 1) ? gridDim.x - 1 - blockIdx.x : blockIdx.x);
+    if constexpr (ORDER == kOrderPairs) return 2 * (blockIdx.x + (k >> 1) * gridDim.x) + (k & 1);
     return blockIdx.x + k * gridDim.x;
 }
 
@@ -249,7 +250,7 @@ struct PrefillLayout {
     static_assert(kSmemBytes <= 232448, "dynamic shared memory per block");
 };
 
-template <typename T, int BS, bool kSorted>
+template <typename T, int BS, int ORDER>
 __global__ void __launch_bounds__(384, 1)
     paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                             const __grid_constant__ CUtensorMap tmap_k,
@@ -320,7 +321,7 @@ __global__ void __launch_bounds__(384, 1)
                 make_uint4(0, 0, 0, 0);
         }
     }
-    if (kSorted && warp == 2) {
+    if (ORDER == kOrderSortedGroups && warp == 2) {
         // rank the (at most 32) sequences by context length, longest first, ties by index
         const int len = lane < p.num_seqs ? p.context_lens[lane] : 0;
         int rank = 0;
@@ -361,9 +362,9 @@ __global__ void __launch_bounds__(384, 1)
         int q_issue[2] = {-1, -1};
         bool ok = true;
         int jt = 0, n = 0;  // tiles and items so far
-        for (int ki = 0, item = prefill_slot_item<kSorted>(p, 0); item < p.num_items && ok; item = prefill_slot_item<kSorted>(p, ++ki)) {
+        for (int ki = 0, item = prefill_slot_item<ORDER>(p, 0); item < p.num_items && ok; item = prefill_slot_item<ORDER>(p, ++ki)) {
             PrefillItem it;
-            if (!prefill_item<kSorted>(p, item, prefill_seq_vals<kSorted>(p, item, by_len), kv == 0, it, by_len)) continue;
+            if (!prefill_item<ORDER>(p, item, prefill_seq_vals<ORDER>(p, item, by_len), kv == 0, it, by_len)) continue;
             const int32_t *trow = p.block_tables + static_cast<int64_t>(it.seq) * p.max_blocks_per_seq;
             auto entry = [&](int j) -> int {  // this lane's block of tile j (-1: none or bad)
                 const int t0 = it.tok_lo + j * TILE;
@@ -398,8 +399,8 @@ __global__ void __launch_bounds__(384, 1)
                 q_pending = false;
                 // the next item's Q box into L2 now, so its load does not wait for HBM
                 PrefillItem nx;
-                for (int k2 = ki + 1, i2 = prefill_slot_item<kSorted>(p, k2); i2 < p.num_items; i2 = prefill_slot_item<kSorted>(p, ++k2)) {
-                    if (!prefill_item<kSorted>(p, i2, prefill_seq_vals<kSorted>(p, i2, by_len), false, nx, by_len)) continue;
+                for (int k2 = ki + 1, i2 = prefill_slot_item<ORDER>(p, k2); i2 < p.num_items; i2 = prefill_slot_item<ORDER>(p, ++k2)) {
+                    if (!prefill_item<ORDER>(p, i2, prefill_seq_vals<ORDER>(p, i2, by_len), false, nx, by_len)) continue;
 #pragma unroll
                     for (int c = 0; c < 2; ++c)
                         tc::tma_prefetch_3d(&tmap_q, c * 64, nx.kvh * p.group, nx.q0 + nx.row_tile * p.tile_tokens);
@@ -476,9 +477,9 @@ __global__ void __launch_bounds__(384, 1)
         constexpr uint32_t idesc_qk = tc::idesc_f16_f32acc(kBF16, 128, 128, false, false);
         bool ok = true;
         int jt = 0, n = 0;
-        for (int ki = 0, item = prefill_slot_item<kSorted>(p, 0); item < p.num_items && ok; item = prefill_slot_item<kSorted>(p, ++ki)) {
+        for (int ki = 0, item = prefill_slot_item<ORDER>(p, 0); item < p.num_items && ok; item = prefill_slot_item<ORDER>(p, ++ki)) {
             PrefillItem it;
-            if (!prefill_item<kSorted>(p, item, prefill_seq_vals<kSorted>(p, item, by_len), false, it, by_len)) continue;
+            if (!prefill_item<ORDER>(p, item, prefill_seq_vals<ORDER>(p, item, by_len), false, it, by_len)) continue;
             const int qb = n % QB;
             int go = 1;
             if (lane == 0) go = tc_wait(&q_full[qb], (n / QB) & 1, abort_flag, p.status);
@@ -521,9 +522,9 @@ __global__ void __launch_bounds__(384, 1)
         constexpr uint32_t idesc_pv = tc::idesc_f16_f32acc(kBF16, 128, 128, false, true);
         bool ok = true;
         int jt = 0, n_staged = 0;
-        for (int ki = 0, item = prefill_slot_item<kSorted>(p, 0); item < p.num_items && ok; item = prefill_slot_item<kSorted>(p, ++ki)) {
+        for (int ki = 0, item = prefill_slot_item<ORDER>(p, 0); item < p.num_items && ok; item = prefill_slot_item<ORDER>(p, ++ki)) {
             PrefillItem it;
-            if (!prefill_item<kSorted>(p, item, prefill_seq_vals<kSorted>(p, item, by_len), false, it, by_len)) continue;
+            if (!prefill_item<ORDER>(p, item, prefill_seq_vals<ORDER>(p, item, by_len), false, it, by_len)) continue;
             const bool staged = prefill_staged(p, it);
             for (int j = 0; j < it.ntiles; ++j, ++jt) {
                 int go = 1;
@@ -624,9 +625,9 @@ __global__ void __launch_bounds__(384, 1)
             other = sum_x[(1 - half) * 128 + r];
             return true;
         };
-        for (int ki = 0, item = prefill_slot_item<kSorted>(p, 0); item < p.num_items && ok; item = prefill_slot_item<kSorted>(p, ++ki)) {
+        for (int ki = 0, item = prefill_slot_item<ORDER>(p, 0); item < p.num_items && ok; item = prefill_slot_item<ORDER>(p, ++ki)) {
             PrefillItem it;
-            if (!prefill_item<kSorted>(p, item, prefill_seq_vals<kSorted>(p, item, by_len), false, it, by_len)) continue;
+            if (!prefill_item<ORDER>(p, item, prefill_seq_vals<ORDER>(p, item, by_len), false, it, by_len)) continue;
             const int row = it.row0 + r;
             const bool live = r < R && row < it.rows;
             const int jtok = live ? row / p.group : 0;
