@@ -140,16 +140,41 @@ pkv_status plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
         // that the partial outputs (GH rows of head_dim + 2 floats, written and read
         // back by the merge) pass 1 / kMergeShare of the partition's K/V bytes.
         const int64_t units = std::max<int64_t>(1, static_cast<int64_t>(num_seqs) * grid_y);
-        const int64_t target = static_cast<int64_t>(sm_count) *
-                               (resident > 0 ? resident : resident_ctas_per_sm(int8_kv, gh)) * kTargetWaves;
+        const int64_t slots = static_cast<int64_t>(sm_count) *
+                              (resident > 0 ? resident : resident_ctas_per_sm(int8_kv, gh));
+        const int64_t target = slots * kTargetWaves;
         const int64_t want = std::max<int64_t>(1, (target + units - 1) / units);
-        int64_t p = (static_cast<int64_t>(max_context_len) + want - 1) / want;
+        const int64_t len = max_context_len;
+        int64_t p = (len + want - 1) / want;
         const int64_t kv_per_token = 2LL * head_dim * (int8_kv ? 1 : 2);
         const int64_t partial = 2LL * gh * (head_dim + 2) * 4;
         p = std::max<int64_t>(p, kMinAutoPartition);
         p = std::max<int64_t>(p, (kMergeShare * partial + kv_per_token - 1) / kv_per_token);
         p = (p + block_size - 1) / block_size * block_size;
-        part = static_cast<int>(std::min<int64_t>(p, max_partition));
+        p = std::min<int64_t>(p, max_partition);
+        // When the floors leave fewer than kTargetWaves waves of a form with two
+        // resident CTAs per SM, the CTAs of sequences at max_context_len run in a few
+        // rounds, and a last round that fills few slots idles most SMs: take the
+        // partition count in [n / 2, n] whose CTAs fill whole waves best (the largest
+        // count among equals).
+        const int64_t n = len > 0 ? (len + p - 1) / p : 1;
+        if (n > 1 && units * n < target && slots <= 2LL * sm_count) {
+            auto fill = [&](int64_t parts) {  // CTAs / (rounds x slots)
+                const int64_t ctas = units * parts;
+                return static_cast<double>(ctas) / static_cast<double>((ctas + slots - 1) / slots * slots);
+            };
+            double best = fill(n);
+            for (int64_t k = n - 1; k >= (n + 1) / 2; --k) {
+                const int64_t pk = ((len + k - 1) / k + block_size - 1) / block_size * block_size;
+                if (pk > max_partition) break;
+                const double f = fill((len + pk - 1) / pk);
+                if (f > best + 1e-9) {
+                    best = f;
+                    p = pk;
+                }
+            }
+        }
+        part = static_cast<int>(p);
     }
     const int nparts = max_context_len > 0 ? (max_context_len + part - 1) / part : 1;
     if (out_partition_size) *out_partition_size = part;

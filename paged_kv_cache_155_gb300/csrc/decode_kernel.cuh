@@ -173,8 +173,9 @@ __device__ __forceinline__ void load_codes_f16(const int8_t *src, uint32_t *h) {
 // fewer per-row steps per byte), else 8 codes (register budget).  The stage
 // budget per warp sets how many CTAs share an SM: INT8 lane loops 8 KiB (six at
 // 80 registers), INT8 warp MMAs 12 KiB (four), 16-bit lane loops 24 KiB (two),
-// 16-bit warp MMAs 16 KiB (three).
-template <int D, int BS, int EB = 2, int VL = 8, bool kMmaForm = false>
+// 16-bit warp MMAs 16 KiB (three), and 24 KiB for sixteen heads per block, whose
+// registers allow two CTAs per SM (a CTA's bytes in flight bound its rate).
+template <int D, int BS, int EB = 2, int VL = 8, bool kMmaForm = false, bool kWide = false>
 struct DecodeGeom {
     static constexpr int kWarps = 4;
     static constexpr int kMaxTile = 32 / EB;             // 4 KiB K tiles at head_dim 128
@@ -185,7 +186,7 @@ struct DecodeGeom {
     static constexpr int kIters = kTile / kTokenGroups;  // token rows per lane per stage
     static constexpr int kTileBytes = kTile * D * EB;    // one K (or V) tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kBudget = EB == 1 ? (kMmaForm ? 12288 : 8192) : (kMmaForm ? 16384 : 24576);
+    static constexpr int kBudget = EB == 1 ? (kMmaForm ? 12288 : 8192) : (kMmaForm && !kWide ? 16384 : 24576);
     static constexpr int kStagesRaw = kBudget / kStageBytes;
     static constexpr int kStages = kStagesRaw < 2 ? 2 : (kStagesRaw > 8 ? 8 : kStagesRaw);
     static constexpr int kMaxTableEntries = 1024;        // table slice per partition
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(128, (GH >= 4 && sizeof(KT) == 2) ? (GH == 16 
     constexpr bool kMma = GH >= 4;
     constexpr bool kMmaBF16 = std::is_same<KT, __nv_bfloat16>::value;  // MMA operand type
     constexpr int VL = decode_lane_values<KT, GH>();  // values per lane vector
-    using G = DecodeGeom<D, BS, sizeof(KT), VL, (GH >= 4)>;
+    using G = DecodeGeom<D, BS, sizeof(KT), VL, (GH >= 4), (GH == 16)>;
     constexpr int NW = G::kWarps, S = G::kStages, TILE = G::kTile, LPT = G::kLanesPerToken,
                   TPG = G::kTokenGroups, ITERS = G::kIters;
     // token rows processed between two online-softmax updates (bounds registers)

@@ -36,7 +36,7 @@ cudaError_t launch_kernel(void (*kernel)(Params...), dim3 grid, dim3 block, size
 template <typename T, typename KT, int D, int BS, int GH>
 pkv_status launch_decode_one(const DecodeParams &p, const DecodeMaps &maps, dim3 grid, cudaStream_t stream,
                              bool overlap) {
-    using G = DecodeGeom<D, BS, sizeof(KT), decode_lane_values<KT, GH>(), (GH >= 4)>;
+    using G = DecodeGeom<D, BS, sizeof(KT), decode_lane_values<KT, GH>(), (GH >= 4), (GH == 16)>;
     static std::atomic<uint64_t> configured_devices{0};  // bit per device ordinal
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
