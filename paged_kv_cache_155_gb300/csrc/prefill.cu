@@ -201,6 +201,11 @@ PKV_API pkv_status pkv_paged_attention_prefill(
     p.num_items = pp.items;
     p.splits = pp.splits;
     p.split_tokens = pp.split_tokens;
+    p.div_row_tiles = pkv::make_fast_div(p.row_tiles);
+    p.div_kv_heads = pkv::make_fast_div(num_kv_heads);
+    p.div_group = pkv::make_fast_div(group);
+    p.div_splits = pkv::make_fast_div(p.splits);
+    p.div_per_tile = pkv::make_fast_div(num_kv_heads * num_seqs * p.splits);
     // item order (prefill_item): whole prompts of one length (every chunk
     // max_query_len tokens on an empty cache) in row-tile pairs, a few sequences of
     // different lengths by (sequence, KV head) sorted by length, both for L2 reuse

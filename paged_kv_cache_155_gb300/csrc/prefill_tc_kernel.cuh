@@ -54,6 +54,25 @@
 
 namespace pkv {
 
+// Division of a non-negative int by a fixed positive divisor through one multiplication
+// (Granlund and Montgomery, "Division by Invariant Integers using Multiplication", 1994,
+// the form with a 33-bit add): l = ceil(log2 d), m = floor(2^32 (2^l - d) / d) + 1, and
+// n / d = (umulhi(m, n) + n) >> l for 0 <= n < 2^31 (umulhi(m, n) < n, so the add does
+// not wrap).  The item arithmetic divides by the same few launch constants in every role.
+struct FastDiv {
+    uint32_t m, l;
+};
+inline FastDiv make_fast_div(int d) {
+    if (d < 1) d = 1;  // no launch divides by less (empty launches return before)
+    uint32_t l = 0;
+    while ((1ull << l) < static_cast<uint64_t>(d)) ++l;
+    const uint64_t m = (1ull << 32) * ((1ull << l) - static_cast<uint64_t>(d)) / static_cast<uint64_t>(d) + 1;
+    return FastDiv{static_cast<uint32_t>(m), l};
+}
+__device__ __forceinline__ int fast_div(int n, FastDiv f) {
+    return static_cast<int>((__umulhi(static_cast<uint32_t>(n), f.m) + static_cast<uint32_t>(n)) >> f.l);
+}
+
 struct PrefillParams {
     const void *q;                 // [num_rows][num_q_heads][128]
     void *out;                     // [num_rows][num_q_heads][128]
@@ -80,6 +99,8 @@ struct PrefillParams {
     int splits;        // KV splits per row tile
     int split_tokens;  // tokens per split, a multiple of 128
     int order;         // item order: kOrderRowTiles, kOrderPairs or kOrderSortedGroups
+    FastDiv div_row_tiles, div_kv_heads, div_group, div_splits, div_per_tile;  // make_fast_div of
+                       // row_tiles, num_kv_heads, group, splits, num_kv_heads * num_seqs * splits
     float scale_log2;
 };
 
@@ -99,10 +120,12 @@ struct PrefillSeqVals {
 // others').
 template <int ORDER>
 __device__ __forceinline__ int prefill_item_seq(const PrefillParams &p, int i, const unsigned char *by_len) {
-    if constexpr (ORDER == kOrderSortedGroups) return by_len[i / p.row_tiles / p.num_kv_heads];
-    if constexpr (ORDER == kOrderPairs) return i / p.row_tiles / p.num_kv_heads;
+    if constexpr (ORDER == kOrderSortedGroups)
+        return by_len[fast_div(fast_div(i, p.div_row_tiles), p.div_kv_heads)];
+    if constexpr (ORDER == kOrderPairs) return fast_div(fast_div(i, p.div_row_tiles), p.div_kv_heads);
     const int per_tile = p.num_kv_heads * p.num_seqs * p.splits;
-    return (i % per_tile) / p.num_kv_heads / p.splits;
+    const int rem = i - fast_div(i, p.div_per_tile) * per_tile;
+    return fast_div(fast_div(rem, p.div_kv_heads), p.div_splits);
 }
 
 // Loads item i's sequence values (zeros past the item count).
@@ -162,27 +185,27 @@ template <int ORDER>
 __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, const PrefillSeqVals &sv,
                                              bool flag, PrefillItem &it, const unsigned char *by_len) {
     if constexpr (ORDER == kOrderSortedGroups) {
-        const int g = i / p.row_tiles;
+        const int g = fast_div(i, p.div_row_tiles);
         const int pos = i - g * p.row_tiles;
-        const int rank = g / p.num_kv_heads;
+        const int rank = fast_div(g, p.div_kv_heads);
         it.seq = by_len[rank];
         it.kvh = g - rank * p.num_kv_heads;
         it.split = 0;
         it.row_tile = p.row_tiles - 1 - pos;
     } else if constexpr (ORDER == kOrderPairs) {
-        const int g = i / p.row_tiles;
+        const int g = fast_div(i, p.div_row_tiles);
         const int pos = i - g * p.row_tiles;
-        it.seq = g / p.num_kv_heads;
+        it.seq = fast_div(g, p.div_kv_heads);
         it.kvh = g - it.seq * p.num_kv_heads;
         it.split = 0;
         it.row_tile = (pos & 1) ? pos >> 1 : p.row_tiles - 1 - (pos >> 1);
     } else {
         const int per_tile = p.num_kv_heads * p.num_seqs * p.splits;
-        const int rt_rev = i / per_tile;
+        const int rt_rev = fast_div(i, p.div_per_tile);
         const int rem = i - rt_rev * per_tile;
-        const int ss = rem / p.num_kv_heads;
+        const int ss = fast_div(rem, p.div_kv_heads);
         it.kvh = rem - ss * p.num_kv_heads;
-        it.seq = ss / p.splits;
+        it.seq = fast_div(ss, p.div_splits);
         it.split = ss - it.seq * p.splits;
         it.row_tile = p.row_tiles - 1 - rt_rev;
     }
@@ -196,7 +219,7 @@ __device__ __forceinline__ bool prefill_item(const PrefillParams &p, int i, cons
     if (it.row0 >= it.rows) return false;
     const int last_row = min(it.rows, it.row0 + p.tile_rows) - 1;
     it.base_pos = it.len - it.chunk;
-    const int pos_max = it.base_pos + last_row / p.group;
+    const int pos_max = it.base_pos + fast_div(last_row, p.div_group);
     it.tok_lo = it.split * p.split_tokens;
     it.tok_hi = min(min(it.len, pos_max + 1), it.tok_lo + p.split_tokens);
     it.ntiles = (it.tok_hi - it.tok_lo + 127) / 128;
@@ -630,7 +653,7 @@ __global__ void __launch_bounds__(384, 1)
             if (!prefill_item<ORDER>(p, item, prefill_seq_vals<ORDER>(p, item, by_len), false, it, by_len)) continue;
             const int row = it.row0 + r;
             const bool live = r < R && row < it.rows;
-            const int jtok = live ? row / p.group : 0;
+            const int jtok = live ? fast_div(row, p.div_group) : 0;
             const int pos = it.base_pos + jtok;  // this row sees tokens 0 .. pos
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < it.ntiles && ok; ++j, ++jt) {
