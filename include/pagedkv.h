@@ -403,8 +403,8 @@ PKV_API uint64_t pkv_launch_count(void);
  * least 256 tokens whose K/V bytes are at least 32 times their partial
  * outputs.  For the forms with two resident blocks per SM, when those floors
  * leave fewer than eight waves, the partition count per max_context_len
- * sequence is the one in [n/2, n] (n: the floors' count) whose blocks fill
- * whole waves best, the largest among equals.
+ * sequence is the smallest in [n/2, n] (n: the floors' count) whose blocks
+ * fill whole waves within 0.15 of the best count in that range.
  */
 PKV_API pkv_status pkv_decode_plan(int num_seqs, int num_q_heads, int num_kv_heads,
                                    int head_dim, int block_size, int max_context_len,

@@ -86,6 +86,7 @@ namespace {
 constexpr int kTargetWaves = 8;        // CTA waves the automatic split aims for
 constexpr int kMinAutoPartition = 256; // tokens: below this the per-CTA set-up dominates
 constexpr int kMergeShare = 32;        // a partition's K/V bytes >= this x its partial bytes
+constexpr double kFillSlack = 0.15;    // wave fill given up for fewer, longer partitions (two-per-SM forms)
 
 // Decode CTAs resident per SM for each kernel form (their stage budgets and
 // register counts): 16-bit per-lane loops two, 16-bit warp MMAs three (two with
@@ -154,23 +155,26 @@ pkv_status plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
         p = std::min<int64_t>(p, max_partition);
         // When the floors leave fewer than kTargetWaves waves of a form with two
         // resident CTAs per SM, the CTAs of sequences at max_context_len run in a few
-        // rounds, and a last round that fills few slots idles most SMs: take the
-        // partition count in [n / 2, n] whose CTAs fill whole waves best (the largest
-        // count among equals).
+        // rounds: a last round that fills few slots idles most SMs, and each CTA's
+        // start-up costs its SM half its streams.  Take the fewest partitions in
+        // [n / 2, n] whose CTAs fill whole waves within kFillSlack of the best count.
         const int64_t n = len > 0 ? (len + p - 1) / p : 1;
         if (n > 1 && units * n < target && slots <= 2LL * sm_count) {
             auto fill = [&](int64_t parts) {  // CTAs / (rounds x slots)
                 const int64_t ctas = units * parts;
                 return static_cast<double>(ctas) / static_cast<double>((ctas + slots - 1) / slots * slots);
             };
+            auto part_for = [&](int64_t k) {  // tokens per partition for k partitions
+                return ((len + k - 1) / k + block_size - 1) / block_size * block_size;
+            };
             double best = fill(n);
-            for (int64_t k = n - 1; k >= (n + 1) / 2; --k) {
-                const int64_t pk = ((len + k - 1) / k + block_size - 1) / block_size * block_size;
-                if (pk > max_partition) break;
-                const double f = fill((len + pk - 1) / pk);
-                if (f > best + 1e-9) {
-                    best = f;
+            for (int64_t k = (n + 1) / 2; k < n; ++k)
+                if (part_for(k) <= max_partition) best = std::max(best, fill((len + part_for(k) - 1) / part_for(k)));
+            for (int64_t k = (n + 1) / 2; k < n; ++k) {
+                const int64_t pk = part_for(k);
+                if (pk <= max_partition && fill((len + pk - 1) / pk) >= best - kFillSlack) {
                     p = pk;
+                    break;
                 }
             }
         }
